@@ -1,0 +1,173 @@
+/*
+ * pcsum.h - C ABI of the GB300 log-space sum-layer library (libpcsum.so).
+ *
+ * What it computes
+ * ----------------
+ * The dense sum layer of a probabilistic circuit, in log space, and the circuits
+ * built from it (pyjuice pull request #62, "precision option / dense sum layers
+ * through cuBLAS / fp32 backward on tensor cores", Summary 2 and 3):
+ *
+ *   forward    out[i,b] = m_b + log sum_j theta[i,j] * exp(x[j,b] - m_b)
+ *              m_b = max_j x[j,b], the per-sample maximum over the group's children
+ *   element    e[j,b]   = sum_i theta[i,j] * f[i,b] * exp(x[j,b] - out[i,b])
+ *   parameter  F[i,j]   = theta[i,j] * sum_b f[i,b] * exp(x[j,b] - out[i,b])
+ *
+ * and the LowRank "exp_sum" per-sample scale (pyjuice.parameterizations.LowRank
+ * API doc, intro formulas and Training):
+ *   theta_b[i,j] = theta[i,j] * exp((A_b B_b)[i,j]) / Z_b[i].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every array argument is DEVICE memory owned by the caller, unless its comment
+ *   says HOST. The library never allocates device memory: scratch comes from the
+ *   caller's workspace `ws` of at least the size the matching *_workspace query
+ *   reports (16-byte aligned). float arrays are float32, row-major (C order).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream), perform no host synchronisation and allocate nothing.
+ * - Arguments are validated before anything is launched. On failure the call
+ *   returns a status other than PC_OK, launches nothing and leaves a one-line
+ *   reason in pc_last_error() (thread-local). PC_ERR_CUDA reports a CUDA launch
+ *   error; device-side waits are bounded and a timed-out kernel records
+ *   PC_ERR_TIMEOUT in a device status word read by pc_device_status().
+ * - Precision (pyjuice PR #62, Summary 1 table) selects how the products of the
+ *   contractions are formed; accumulation is always float32 in tensor memory:
+ *     PC_PREC_AUTO  bfloat16 operands (round to nearest even)
+ *     PC_PREC_TF32  TF32 operands (round to nearest, ties away from zero)
+ *     PC_PREC_FP32  three TF32 products hi*hi + hi*lo + lo*hi (fp32-level)
+ *   Any other value returns PC_ERR_UNKNOWN_PRECISION, naming the valid modes.
+ * - Flow outputs are overwritten, or added to when `accumulate` != 0.
+ */
+#ifndef PCSUM_H_
+#define PCSUM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PCSUM_API __attribute__((visibility("default")))
+#else
+#define PCSUM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pc_stream_t;
+
+typedef enum {
+  PC_PREC_AUTO = 0, /* bf16 products */
+  PC_PREC_TF32 = 1, /* TF32 products */
+  PC_PREC_FP32 = 2  /* 3xTF32 products */
+} pc_precision_t;
+
+typedef enum {
+  PC_OK = 0,
+  PC_ERR_NULL = 1,              /* a required pointer is NULL */
+  PC_ERR_SHAPE = 2,             /* a size is out of range or inconsistent */
+  PC_ERR_ALIGNMENT = 3,         /* a pointer is not 16-byte aligned */
+  PC_ERR_UNKNOWN_PRECISION = 4, /* precision is not one of pc_precision_t */
+  PC_ERR_WORKSPACE = 5,         /* workspace NULL or smaller than the query's size */
+  PC_ERR_UNSUPPORTED = 6,       /* a valid request outside this build's limits */
+  PC_ERR_CUDA = 7,              /* a CUDA call failed (launch or device query) */
+  PC_ERR_TIMEOUT = 8            /* a device-side wait ran out (see pc_device_status) */
+} pc_status_t;
+
+/* Library version string, e.g. "pcsum 0.1 sm_103a". Static storage. */
+PCSUM_API const char* pc_version(void);
+
+/* Static English name of a status code. */
+PCSUM_API const char* pc_status_string(pc_status_t status);
+
+/* Detail of the last failing call on this host thread ("" if none). Valid until the
+ * next call into the library from the same thread. */
+PCSUM_API const char* pc_last_error(void);
+
+/* Number of kernels this library has launched in the process so far (all entry
+ * points, all devices). */
+PCSUM_API unsigned long long pc_launch_count(void);
+
+/* Synchronises `stream`, then reads and clears the device status word of the current
+ * device. Returns PC_OK, or PC_ERR_TIMEOUT if a kernel gave up a bounded wait since
+ * the last read, or PC_ERR_CUDA. Diagnostic; not for the hot path. */
+PCSUM_API pc_status_t pc_device_status(pc_stream_t stream);
+
+/* Per-launch timing of the tensor-core contractions, for measurement. Between
+ * pc_profile_start(capacity) and pc_profile_stop, every contraction the library
+ * launches records a CUDA event pair on its stream (at most `capacity` launches).
+ * pc_profile_stop synchronises the device, then writes for each recorded launch i
+ * (i < *count <= capacity): ms[i] = elapsed device time, kind[i] = which contraction
+ * (PC_KIND_*), flops[i] = its algorithmic flops 2*M*N*K (each product counted once).
+ * Not thread-safe; host-side event objects only, no device memory. */
+typedef enum {
+  PC_KIND_LAYER_FWD = 0, PC_KIND_LAYER_ELEM = 1, PC_KIND_LAYER_PARAM = 2,
+  PC_KIND_HMM_FWD = 3, PC_KIND_HMM_ELEM = 4, PC_KIND_HMM_PARAM = 5,
+  PC_KIND_HCLT_FWD = 6, PC_KIND_HCLT_ELEM = 7, PC_KIND_HCLT_PARAM = 8,
+  PC_KIND_LOWRANK_FWD = 9, PC_KIND_LOWRANK_BWD = 10
+} pc_kind_t;
+PCSUM_API pc_status_t pc_profile_start(int capacity);
+PCSUM_API pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long long* flops,
+                                      int capacity);
+
+/* ------------------------------------------------------------------------------
+ * Dense sum layer, G groups (pyjuice PR #62, Summary 2: shared-children layers
+ * and evenly strided child groups run as batched GEMMs; Summary 3: the element-
+ * and parameter-flow contractions).
+ *
+ *   theta [G][M][N]   parameters of group g (row i = node, column j = child).
+ *   x     [R][B]      child log-values, one row of B samples per child; group g's
+ *                     children are rows g*child_stride .. g*child_stride+N-1.
+ *                     G == 1: any child_stride (0 is the shared-children layout).
+ *                     G > 1: child_stride >= N (non-overlapping groups).
+ *   out   [G][M][B]   node log-values. -inf where the sum is 0 or every child is -inf.
+ *   f     [G][M][B]   node flows (backward input).
+ *   e     like x      element flows; rows outside every group are not touched.
+ *                     NULL = not computed.
+ *   F     [G][M][N]   parameter flows. NULL = not computed.
+ * Limits: 1 <= G, M, N, B; M, N < 2^24; B < 2^24; x and the arrays above hold at
+ * most 2^31 rows. Scratch: pc_sum_layer_workspace (covers both directions).
+ * ---------------------------------------------------------------------------- */
+PCSUM_API pc_status_t pc_sum_layer_workspace(int G, int M, int N, int B, pc_precision_t prec,
+                                   size_t* bytes);
+
+PCSUM_API pc_status_t pc_sum_layer_fwd(int G, int M, int N, int B, const float* theta, const float* x,
+                             long long child_stride, float* out, pc_precision_t prec,
+                             void* ws, size_t ws_bytes, pc_stream_t stream);
+
+PCSUM_API pc_status_t pc_sum_layer_bwd(int G, int M, int N, int B, const float* theta, const float* x,
+                             long long child_stride, const float* out, const float* f,
+                             float* e, float* F, int accumulate, pc_precision_t prec,
+                             void* ws, size_t ws_bytes, pc_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * Whole HMM circuit, forward + backward (pyjuice PR #62, Results table "HMM, 4096
+ * latents, 32 positions"; Summary 2, first bullet: its layers share their children).
+ * The circuit is P(x) = sum_z pi(z_1) prod_t E(z_t, x_t) prod_t A(z_t, z_{t+1}),
+ * built from the last position back as T-1 tied H x H sum layers with product
+ * (emission) layers between them and a root sum layer over pi.
+ *
+ *   tokens [B][T] int32 in [0, V)           observed sequence of each sample
+ *   pi [H], A [H][H] (A[k][l] = P(z_{t+1}=l | z_t=k)), E [H][V]  (non-negative)
+ *   ll [B] double                           log P(x) per sample (written)
+ *   dpi [H], dA [H][H], dE [H][V]           EM flows summed over the batch (posterior
+ *                                           expected counts); each may be NULL. When
+ *                                           all three are NULL only ll is computed.
+ * Limits: 1 <= H <= 16384, 1 <= T <= 4096, 1 <= V <= 65536, 1 <= B <= 65536.
+ * Tokens outside [0, V) are undefined behaviour. Numerical range: the per-layer
+ * rescaling keeps node values in float32 range when, at every position, the most
+ * likely state's value is within e^-80 of max_k E[k,x_t] * sum_l A[k,l] times the
+ * previous position's maximum; the per-sample log-offsets are accumulated in double.
+ * ---------------------------------------------------------------------------- */
+PCSUM_API pc_status_t pc_hmm_workspace(int H, int T, int V, int B, pc_precision_t prec, size_t* bytes);
+
+PCSUM_API pc_status_t pc_hmm_fwd_bwd(int H, int T, int V, int B, const int32_t* tokens, const float* pi,
+                           const float* A, const float* E, double* ll, float* dpi, float* dA,
+                           float* dE, int accumulate, pc_precision_t prec, void* ws,
+                           size_t ws_bytes, pc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCSUM_H_ */

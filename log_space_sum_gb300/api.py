@@ -1,0 +1,186 @@
+"""PyTorch-facing wrappers of the C ABI: argument checks and marshalling only.
+
+Every computation runs in libpcsum.so's CUDA kernels. PyTorch supplies device
+memory (outputs and the scratch workspace) and the current CUDA stream.
+
+Precision modes (pyjuice PR #62, Summary 1 table): "auto" (bf16 products),
+"tf32" (TF32 products), "fp32" (3xTF32 products). The removed flags
+``force_use_bf16`` / ``force_use_fp32`` raise a TypeError naming ``precision=``
+when set to True and are accepted and ignored when False (same page, Breaking
+change).
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _native as N
+
+PRECISIONS = {"auto": 0, "tf32": 1, "fp32": 2}
+
+_ws_cache: dict = {}
+
+
+def precision_code(precision) -> int:
+    if isinstance(precision, str):
+        if precision not in PRECISIONS:
+            raise ValueError(f"unknown precision {precision!r}; valid modes are 'auto' (bf16 "
+                             "products), 'tf32' and 'fp32' (3xTF32)")
+        return PRECISIONS[precision]
+    if isinstance(precision, int) and not isinstance(precision, bool):
+        return precision            # the library rejects unknown codes with PC_ERR_UNKNOWN_PRECISION
+    raise TypeError(f"precision must be 'auto', 'tf32' or 'fp32', not {type(precision).__name__}")
+
+
+def _removed_flags(kwargs: dict, where: str) -> None:
+    for flag in ("force_use_bf16", "force_use_fp32"):
+        if flag in kwargs:
+            if kwargs.pop(flag):
+                raise TypeError(f"{where}: {flag} was removed; pass precision='auto', 'tf32' or "
+                                "'fp32' instead")
+    if kwargs:
+        raise TypeError(f"{where}: unexpected keyword arguments {sorted(kwargs)}")
+
+
+def _check(t: torch.Tensor, name: str, dtype=torch.float32, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> C.c_void_p:
+    return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """Scratch buffer of at least nbytes, cached per (device, stream)."""
+    key = (device, torch.cuda.current_stream(device).cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def _query(name: str, *args) -> int:
+    out = C.c_size_t(0)
+    N.call(name, *args, C.byref(out))
+    return out.value
+
+
+# --------------------------------------------------------------------- sum layer
+def sum_layer_fwd(theta, x, child_stride=None, precision="auto", out=None, **removed):
+    """out[g,i,b] = m_b + log sum_j theta[g,i,j] exp(x[g*cs+j, b] - m_b) (pc_sum_layer_fwd)."""
+    _removed_flags(removed, "sum_layer_fwd")
+    prec = precision_code(precision)
+    _check(theta, "theta")
+    dev = theta.device
+    _check(x, "x", device=dev)
+    G, M, Nn = theta.shape
+    B = x.shape[1]
+    cs = (Nn if G > 1 else 0) if child_stride is None else int(child_stride)
+    if out is None:
+        out = torch.empty(G, M, B, dtype=torch.float32, device=dev)
+    _check(out, "out", device=dev)
+    nb = _query("pc_sum_layer_workspace", G, M, Nn, B, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_sum_layer_fwd", G, M, Nn, B, _ptr(theta), _ptr(x), cs, _ptr(out), prec,
+           _ptr(ws), ws.numel(), _stream(dev))
+    return out
+
+
+def sum_layer_bwd(theta, x, out, f, child_stride=None, precision="auto", element_flows=True,
+                  param_flows=True, e=None, F=None, accumulate=False, **removed):
+    """Element flows e (shaped like x) and parameter flows F (shaped like theta)
+    (pc_sum_layer_bwd). Without ``accumulate`` the flows are overwritten; rows of x
+    outside every group keep e's previous values (zeros for a fresh e)."""
+    _removed_flags(removed, "sum_layer_bwd")
+    prec = precision_code(precision)
+    _check(theta, "theta")
+    dev = theta.device
+    for t, n in ((x, "x"), (out, "out"), (f, "f")):
+        _check(t, n, device=dev)
+    G, M, Nn = theta.shape
+    B = x.shape[1]
+    cs = (Nn if G > 1 else 0) if child_stride is None else int(child_stride)
+    if element_flows and e is None:
+        e = torch.zeros_like(x)
+    if param_flows and F is None:
+        F = torch.empty_like(theta)
+    if e is not None:
+        _check(e, "e", device=dev)
+    if F is not None:
+        _check(F, "F", device=dev)
+    nb = _query("pc_sum_layer_workspace", G, M, Nn, B, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_sum_layer_bwd", G, M, Nn, B, _ptr(theta), _ptr(x), cs, _ptr(out), _ptr(f),
+           _ptr(e if element_flows else None), _ptr(F if param_flows else None), int(bool(accumulate)),
+           prec, _ptr(ws), ws.numel(), _stream(dev))
+    return (e if element_flows else None), (F if param_flows else None)
+
+
+# --------------------------------------------------------------------------- HMM
+def hmm_fwd_bwd(tokens, pi, A, E, precision="auto", flows=True, ll=None, dpi=None, dA=None, dE=None,
+                accumulate=False, **removed):
+    """Whole HMM circuit (pc_hmm_fwd_bwd): returns (ll [B] float64, dpi [H], dA [H,H],
+    dE [H,V]); the flows are None when ``flows`` is False."""
+    _removed_flags(removed, "hmm_fwd_bwd")
+    prec = precision_code(precision)
+    _check(A, "A")
+    dev = A.device
+    _check(tokens, "tokens", dtype=torch.int32, device=dev)
+    _check(pi, "pi", device=dev)
+    _check(E, "E", device=dev)
+    B, T = tokens.shape
+    H, V = E.shape
+    if ll is None:
+        ll = torch.empty(B, dtype=torch.float64, device=dev)
+    _check(ll, "ll", dtype=torch.float64, device=dev)
+    if flows:
+        dpi = torch.empty(H, dtype=torch.float32, device=dev) if dpi is None else dpi
+        dA = torch.empty(H, H, dtype=torch.float32, device=dev) if dA is None else dA
+        dE = torch.empty(H, V, dtype=torch.float32, device=dev) if dE is None else dE
+        for t, n in ((dpi, "dpi"), (dA, "dA"), (dE, "dE")):
+            _check(t, n, device=dev)
+    else:
+        dpi = dA = dE = None
+    nb = _query("pc_hmm_workspace", H, T, V, B, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_hmm_fwd_bwd", H, T, V, B, _ptr(tokens), _ptr(pi), _ptr(A), _ptr(E), _ptr(ll),
+           _ptr(dpi), _ptr(dA), _ptr(dE), int(bool(accumulate)), prec, _ptr(ws), ws.numel(),
+           _stream(dev))
+    return ll, dpi, dA, dE
+
+
+# -------------------------------------------------------------------- diagnostics
+def device_status(device=None) -> None:
+    """Synchronises the current stream and raises PCError if a kernel gave up a bounded wait."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    N.call("pc_device_status", _stream(dev))
+
+
+def profile_start(capacity: int = 4096) -> None:
+    N.call("pc_profile_start", int(capacity))
+
+
+def profile_stop(capacity: int = 4096):
+    """Returns [(kind, ms, flops)] for every contraction launched since profile_start."""
+    cnt = C.c_int(0)
+    ms = (C.c_float * capacity)()
+    kind = (C.c_int * capacity)()
+    flops = (C.c_longlong * capacity)()
+    N.call("pc_profile_stop", C.byref(cnt), ms, kind, flops, int(capacity))
+    return [(N.KINDS.get(kind[i], str(kind[i])), float(ms[i]), int(flops[i])) for i in range(cnt.value)]

@@ -1,0 +1,575 @@
+// Whole HMM circuit, forward + backward, on the tensor-core contraction.
+//
+// The circuit (pyjuice PR #62, Results table: "HMM, 4096 latents, 32 positions";
+// Summary 2, first bullet: the HMM's sum layers share their children) is built from
+// the last position back, with positions t = 0..T-1:
+//   P_{T-1}(k) = E[k, x_{T-1}]
+//   S_t(k)     = sum_l A[k,l] P_{t+1}(l)            tied H x H sum layer, shared children
+//   P_t(k)     = E[k, x_t] S_t(k)                    product (emission) layer
+//   LL         = log sum_k pi[k] P_0(k)              root sum layer
+//
+// Each sum layer's log-space form out = m + log sum_l A exp(x - m) is evaluated with
+// the exponentials of its children kept from the layer below: the epilogue of S_t
+// writes the next layer's shifted children u_t = exp(x_t - shift_t) directly as
+//   u_t[k,b] = E[k, x_{t,b}] * D_t[k,b] * c_{t,b},   D_t = sum_l A[k,l] u_{t+1}[l,b]
+// (the log of the epilogue and the exp of the next prologue cancel), where
+//   c_{t,b} = 1 / (max_l u_{t+1}[l,b] * max_k E[k, x_{t,b}] sum_l A[k,l])
+// bounds every u_t by 1. max_l u_{t+1} is the exact column maximum of the layer
+// below (reduced by that layer's epilogue), so the bound's slack never accumulates
+// over positions. The per-sample log-scales accumulate in double:
+//   LL_b = log sum_k pi[k] u_0[k,b] - sum_t log c_{t,b}.
+//
+// Backward (root flow 1 per sample; product nodes pass flows to their children):
+//   r_b        = 1 / sum_k pi[k] u_0[k,b]
+//   f_0[k,b]   = pi[k] u_0[k,b] r_b                   flows of P_0 (posteriors)
+//   w_t[k,b]   = f_t / D_t = E[k,x_t] c_t s_t          sum-layer flow / its value,
+//                (w_0 = pi[k] r_b E[k,x_0] c_0)        the contraction's right factor
+//   s_{t+1}[j,b] = sum_i A[i,j] w_t[i,b]               element-flow contraction
+//   f_{t+1}    = u_{t+1} s_{t+1}                       element flows = posteriors
+//   dA[i,j]    = A[i,j] sum_{t,b} w_t[i,b] u_{t+1}[j,b] parameter flows, all T-1 tied
+//                                                       layers in one contraction of
+//                                                       depth (T-1) B
+//   dE[k,v]    = sum_{t,b: x_{t,b}=v} f_t[k,b],  dpi[k] = sum_b f_0[k,b]
+#include <cmath>
+
+#include "pc_launch.cuh"
+
+namespace pc {
+namespace {
+
+constexpr int kChainBN = 128;
+
+// ------------------------------------------------------------------ set-up
+__global__ void k_transpose_f32(const float* __restrict__ src, int R, int C, float* __restrict__ dst) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int r = r0 + k, c = c0 + threadIdx.x;
+    tile[k][threadIdx.x] = (r < R && c < C) ? src[static_cast<long long>(r) * C + c] : 0.f;
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int c = c0 + k, r = r0 + threadIdx.x;
+    if (r < R && c < C) dst[static_cast<long long>(c) * R + r] = tile[threadIdx.x][k];
+  }
+}
+
+// dst[c][r] (+)= src[r][c]
+__global__ void k_transpose_add_f32(const float* __restrict__ src, int R, int C, float* __restrict__ dst,
+                                    int accumulate) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int r = r0 + k, c = c0 + threadIdx.x;
+    tile[k][threadIdx.x] = (r < R && c < C) ? src[static_cast<long long>(r) * C + c] : 0.f;
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int c = c0 + k, r = r0 + threadIdx.x;
+    if (r < R && c < C) {
+      float* d = dst + static_cast<long long>(c) * R + r;
+      *d = accumulate ? *d + tile[threadIdx.x][k] : tile[threadIdx.x][k];
+    }
+  }
+}
+
+// rs[k] = sum_l A[k,l], one warp per row.
+__global__ void k_rowsum(const float* __restrict__ A, int H, float* __restrict__ rs) {
+  const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (row >= H) return;
+  const float* a = A + static_cast<long long>(row) * H;
+  double s = 0.0;
+  for (int l = threadIdx.x & 31; l < H; l += 32) s += a[l];
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) rs[row] = static_cast<float>(s);
+}
+
+// emax[v] = max_k E[k,v];  emax_rs[v] = max_k E[k,v] * rs[k]   (Et = E transposed)
+__global__ void k_emission_bounds(const float* __restrict__ Et, const float* __restrict__ rs, int H,
+                                  float* __restrict__ emax, float* __restrict__ emax_rs) {
+  __shared__ float r0[32], r1[32];
+  const int v = blockIdx.x;
+  const float* e = Et + static_cast<long long>(v) * H;
+  float m0 = 0.f, m1 = 0.f;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    const float ev = e[k];
+    m0 = fmaxf(m0, ev);
+    m1 = fmaxf(m1, ev * rs[k]);
+  }
+  for (int o = 16; o; o >>= 1) {
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    r0[threadIdx.x / 32] = m0;
+    r1[threadIdx.x / 32] = m1;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) {
+      m0 = fmaxf(m0, r0[w]);
+      m1 = fmaxf(m1, r1[w]);
+    }
+    emax[v] = m0;
+    emax_rs[v] = m1;
+  }
+}
+
+__device__ __forceinline__ void write_scale(float c, float* cf, double* logc, long long idx) {
+  cf[idx] = c;
+  logc[idx] = c > 0.f ? log(static_cast<double>(c)) : static_cast<double>(INFINITY);
+}
+
+// The last position: u_{T-1}[k,b] = E[k, x_{T-1,b}] / max_k E[k, x_{T-1,b}].
+// Tile of 32 states (lanes) x 32 samples; writes the next forward operand
+// (batch-major), the parameter-flow operand (node-major, column block T-2), or
+// u_0 in float32 when T = 1; and the column maximum.
+template <int P>
+__global__ void k_hmm_leaf(int H, int B, int T, const int* __restrict__ tokens,
+                           const float* __restrict__ Et, const float* __restrict__ emax,
+                           void* ubm, long long ubm_ld, size_t ubm_lo, void* un, long long un_ld,
+                           size_t un_lo, long long un_col, float* U0, float* umax, float* cf,
+                           double* logc) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
+  const int k = k0 + threadIdx.x;
+  const int t = T - 1;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int b = b0 + i;
+    float u = 0.f;
+    if (b < B) {
+      const int tok = tokens[static_cast<long long>(b) * T + t];
+      const float em = emax[tok];
+      const float c = em > 0.f ? 1.f / em : 0.f;
+      if (k < H) {
+        u = Et[static_cast<long long>(tok) * H + k] * c;
+        if (ubm) store_operand<P>(ubm, static_cast<size_t>(b * ubm_ld + k), ubm_lo, u);
+        if (U0) U0[static_cast<long long>(b) * H + k] = u;
+      }
+      if (blockIdx.x == 0 && threadIdx.x == 0) write_scale(c, cf, logc, static_cast<long long>(t) * B + b);
+      float m = u;
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (threadIdx.x == 0) atomic_max_nonneg(&umax[static_cast<long long>(t) * B + b], m);
+    }
+    tile[i][threadIdx.x] = u;
+  }
+  if (!un) return;
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int kk = k0 + i, b = b0 + threadIdx.x;
+    if (kk < H && b < B)
+      store_operand<P>(un, static_cast<size_t>(kk * un_ld + un_col + b), un_lo, tile[threadIdx.x][i]);
+  }
+}
+
+// ----------------------------------------------------------- forward epilogue
+template <int P>
+struct EpiHmmFwd {
+  struct Params {
+    int H, B, T, t;
+    const int* tokens;
+    const float* Et;
+    const float* emax_rs;
+    const float* umax_prev;  // column maxima of u_{t+1}
+    float* umax_cur;         // column maxima of u_t (atomic max, zeroed beforehand)
+    float* cf;
+    double* logc;
+    void* ubm;               // u_t batch-major for S_{t-1} (NULL at t = 0)
+    long long ubm_ld;
+    size_t ubm_lo;
+    void* un;                // u_t node-major, column (t-1) B, for dA (NULL if not needed)
+    long long un_ld;
+    size_t un_lo;
+    float* U0;               // u_0 float32 [B][H] (t = 0 only)
+  };
+  static constexpr int kSmemBytes = kChainBN * 4 * 2 + 4 * kChainBN * 4;
+
+  __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
+    int* tok_s = reinterpret_cast<int*>(smem);
+    float* c_s = reinterpret_cast<float*>(smem) + kChainBN;
+    for (int c = et; c < kChainBN; c += 128) {
+      const int b = n0 + c;
+      int tok = 0;
+      float cv = 0.f;
+      if (b < p.B) {
+        tok = p.tokens[static_cast<long long>(b) * p.T + p.t];
+        const float d = p.umax_prev[b] * p.emax_rs[tok];
+        cv = d > 0.f ? 1.f / d : 0.f;
+        if (m0 == 0) write_scale(cv, p.cf, p.logc, static_cast<long long>(p.t) * p.B + b);
+      }
+      tok_s[c] = tok;
+      c_s[c] = cv;
+    }
+  }
+
+  __device__ static void apply(const Params& p, int, int m0, int n0, int row, int col0,
+                               float (&v)[32], uint8_t* smem) {
+    const int* tok_s = reinterpret_cast<const int*>(smem);
+    const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
+    float* red = reinterpret_cast<float*>(smem) + 2 * kChainBN;
+    const int k = m0 + row;
+    const bool kin = k < p.H;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int lc = col0 + c;
+      const int b = n0 + lc;
+      float u = 0.f;
+      if (kin && b < p.B) {
+        u = p.Et[static_cast<long long>(tok_s[lc]) * p.H + k] * v[c] * c_s[lc];
+        if (p.ubm) store_operand<P>(p.ubm, static_cast<size_t>(b * p.ubm_ld + k), p.ubm_lo, u);
+        if (p.un)
+          store_operand<P>(p.un, static_cast<size_t>(k * p.un_ld + static_cast<long long>(p.t - 1) * p.B + b),
+                           p.un_lo, u);
+        if (p.U0) p.U0[static_cast<long long>(b) * p.H + k] = u;
+      }
+      v[c] = u;
+    }
+    const float mx = warp_transpose_max(v);
+    const int q = (threadIdx.x >> 5) & 3;
+    red[q * kChainBN + col0 + (threadIdx.x & 31)] = mx;
+  }
+
+  __device__ static void finish(const Params& p, int, int, int n0, int et, uint8_t* smem) {
+    const float* red = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
+    for (int c = et; c < kChainBN; c += 128) {
+      const int b = n0 + c;
+      if (b < p.B) {
+        const float m = fmaxf(fmaxf(red[c], red[kChainBN + c]), fmaxf(red[2 * kChainBN + c], red[3 * kChainBN + c]));
+        atomic_max_nonneg(&p.umax_cur[b], m);
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------- root
+// ll[b] = log sum_k pi[k] u_0[k,b] - sum_t log c_{t,b};  r[b] = 1 / sum_k pi u_0.
+__global__ void k_hmm_root(int H, int B, int T, const float* __restrict__ pi, const float* __restrict__ U0,
+                           const double* __restrict__ logc, double* __restrict__ ll, float* __restrict__ rroot) {
+  __shared__ double red[32];
+  const int b = blockIdx.x;
+  const float* u = U0 + static_cast<long long>(b) * H;
+  double s = 0.0;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) s += static_cast<double>(pi[k]) * u[k];
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) s += red[w];
+    double off = 0.0;
+    for (int t = 0; t < T; ++t) off += logc[static_cast<long long>(t) * B + b];
+    const bool zero = !(s > 0.0) || !(off < INFINITY);
+    ll[b] = zero ? -INFINITY : log(s) - off;
+    rroot[b] = zero ? 0.f : static_cast<float>(1.0 / s);
+  }
+}
+
+// Root flows: f_0 = pi u_0 r, w_0 = pi r E[., x_0] c_0; dE and dpi contributions.
+template <int P>
+__global__ void k_hmm_root_flows(int H, int B, int T, const int* __restrict__ tokens,
+                                 const float* __restrict__ pi, const float* __restrict__ U0,
+                                 const float* __restrict__ Et, const float* __restrict__ cf,
+                                 const float* __restrict__ rroot, void* wbm, long long wbm_ld,
+                                 size_t wbm_lo, void* wn, long long wn_ld, size_t wn_lo,
+                                 float* dEt, float* dpi) {
+  __shared__ float tile[32][33];
+  __shared__ float fsum[8][32];
+  const int k0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
+  const int k = k0 + threadIdx.x;
+  const float pk = k < H ? pi[k] : 0.f;
+  float facc = 0.f;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int b = b0 + i;
+    float w = 0.f;
+    if (b < B && k < H) {
+      const int tok = tokens[static_cast<long long>(b) * T];
+      const float r = rroot[b];
+      const float f = pk * U0[static_cast<long long>(b) * H + k] * r;
+      w = pk * r * Et[static_cast<long long>(tok) * H + k] * cf[b];
+      facc += f;
+      if (dEt) atomicAdd(&dEt[static_cast<long long>(tok) * H + k], f);
+      if (wbm) store_operand<P>(wbm, static_cast<size_t>(b * wbm_ld + k), wbm_lo, w);
+    }
+    tile[i][threadIdx.x] = w;
+  }
+  fsum[threadIdx.y][threadIdx.x] = facc;
+  __syncthreads();
+  if (dpi && threadIdx.y == 0 && k < H) {
+    float s = 0.f;
+    for (int y = 0; y < 8; ++y) s += fsum[y][threadIdx.x];
+    atomicAdd(&dpi[k], s);
+  }
+  if (!wn) return;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int kk = k0 + i, b = b0 + threadIdx.x;
+    if (kk < H && b < B) store_operand<P>(wn, static_cast<size_t>(kk * wn_ld + b), wn_lo, tile[threadIdx.x][i]);
+  }
+}
+
+// ---------------------------------------------------------- backward epilogue
+template <int P>
+struct EpiHmmBwd : EpiNoHooks {
+  struct Params {
+    int H, B, T, t;
+    const int* tokens;
+    const float* Et;
+    const float* cf;
+    const void* un;          // u_{t+1} node-major at column t B
+    long long un_ld;
+    size_t un_lo;
+    float* dEt;              // [V][H] or NULL
+    void* wbm;               // w_{t+1} batch-major for the next step (NULL at the end)
+    long long wbm_ld;
+    size_t wbm_lo;
+    void* wn;                // w_{t+1} node-major at column (t+1) B for dA (NULL if unused)
+    long long wn_ld;
+    size_t wn_lo;
+  };
+  static constexpr int kSmemBytes = kChainBN * 8;
+
+  __device__ static void prepare(const Params& p, int, int, int n0, int et, uint8_t* smem) {
+    int* tok_s = reinterpret_cast<int*>(smem);
+    float* c_s = reinterpret_cast<float*>(smem) + kChainBN;
+    for (int c = et; c < kChainBN; c += 128) {
+      const int b = n0 + c;
+      tok_s[c] = b < p.B ? p.tokens[static_cast<long long>(b) * p.T + p.t + 1] : 0;
+      c_s[c] = b < p.B ? p.cf[static_cast<long long>(p.t + 1) * p.B + b] : 0.f;
+    }
+  }
+
+  __device__ static void apply(const Params& p, int, int m0, int n0, int row, int col0,
+                               float (&v)[32], uint8_t* smem) {
+    const int* tok_s = reinterpret_cast<const int*>(smem);
+    const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
+    const int j = m0 + row;
+    if (j >= p.H) return;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int lc = col0 + c;
+      const int b = n0 + lc;
+      if (b < p.B) {
+        const float s = v[c];
+        const long long tokH = static_cast<long long>(tok_s[lc]) * p.H;
+        if (p.dEt) {
+          const float u = load_operand<P>(p.un, static_cast<size_t>(j * p.un_ld + static_cast<long long>(p.t) * p.B + b),
+                                          p.un_lo);
+          atomicAdd(&p.dEt[tokH + j], u * s);
+        }
+        if (p.wbm) {
+          const float w = p.Et[tokH + j] * c_s[lc] * s;
+          store_operand<P>(p.wbm, static_cast<size_t>(b * p.wbm_ld + j), p.wbm_lo, w);
+          if (p.wn)
+            store_operand<P>(p.wn, static_cast<size_t>(j * p.wn_ld + static_cast<long long>(p.t + 1) * p.B + b),
+                             p.wn_lo, w);
+        }
+      }
+    }
+  }
+};
+
+// -------------------------------------------------------------- workspace
+struct HmmWs {
+  Operand Aop, Atop, ubm[2], wbm[2], un, wn;
+  float *Et, *rs, *emax, *emax_rs, *U0, *umax, *cf, *rroot, *dEt;
+  double* logc;
+};
+
+size_t carve_hmm(void* base, pc_precision_t p, int H, int T, int V, int B, bool flows, bool chain,
+                 bool want_dE, HmmWs* w) {
+  Carver c(base);
+  *w = HmmWs{};
+  w->Aop = c.operand(p, 1, H, H);
+  w->ubm[0] = c.operand(p, 1, B, H);
+  w->ubm[1] = c.operand(p, 1, B, H);
+  w->Et = static_cast<float*>(c.take(size_t(V) * H * 4));
+  w->rs = static_cast<float*>(c.take(size_t(H) * 4));
+  w->emax = static_cast<float*>(c.take(size_t(V) * 4));
+  w->emax_rs = static_cast<float*>(c.take(size_t(V) * 4));
+  w->U0 = static_cast<float*>(c.take(size_t(B) * H * 4));
+  w->umax = static_cast<float*>(c.take(size_t(T) * B * 4));
+  w->cf = static_cast<float*>(c.take(size_t(T) * B * 4));
+  w->logc = static_cast<double*>(c.take(size_t(T) * B * 8));
+  w->rroot = static_cast<float*>(c.take(size_t(B) * 4));
+  if (flows && chain) {
+    w->Atop = c.operand(p, 1, H, H);
+    w->wbm[0] = c.operand(p, 1, B, H);
+    w->wbm[1] = c.operand(p, 1, B, H);
+    w->un = c.operand(p, 1, H, static_cast<long long>(T - 1) * B);
+    w->wn = c.operand(p, 1, H, static_cast<long long>(T - 1) * B);
+  }
+  if (flows && want_dE) w->dEt = static_cast<float*>(c.take(size_t(V) * H * 4));
+  return c.used;
+}
+
+size_t hmm_ws_bytes(pc_precision_t p, int H, int T, int V, int B) {
+  HmmWs w;
+  return carve_hmm(nullptr, p, H, T, V, B, true, T >= 2, true, &w) + 256;
+}
+
+pc_status_t check_hmm_shape(int H, int T, int V, int B) {
+  PC_CHECK(H >= 1 && T >= 1 && V >= 1 && B >= 1, PC_ERR_SHAPE,
+           "H, T, V, B must be >= 1 (got %d, %d, %d, %d)", H, T, V, B);
+  PC_CHECK(H <= 16384 && T <= 4096 && V <= 65536 && B <= 65536, PC_ERR_SHAPE,
+           "sizes out of range (H <= 16384, T <= 4096, V <= 65536, B <= 65536)");
+  PC_CHECK(static_cast<long long>(T) * B < (1ll << 31), PC_ERR_SHAPE, "T * B must be < 2^31");
+  return PC_OK;
+}
+
+template <int P>
+pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const float* pi, const float* A,
+                    const float* E, double* ll, float* dpi, float* dA, float* dE, int accumulate,
+                    pc_precision_t prec, void* ws, cudaStream_t s) {
+  constexpr int kParamBN = (P == kTF32x3) ? 128 : 256;
+  const bool flows = dpi || dA || dE;
+  const bool chain = flows && (dA || dE) && T >= 2;
+  HmmWs w;
+  void* base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+  carve_hmm(base, prec, H, T, V, B, flows, T >= 2, dE != nullptr, &w);
+  pc_status_t st;
+
+  PC_CUDA(cudaMemsetAsync(w.umax, 0, size_t(T) * B * 4, s));
+  if (w.dEt) PC_CUDA(cudaMemsetAsync(w.dEt, 0, size_t(V) * H * 4, s));
+  if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
+  if (dA && !accumulate && T < 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
+
+  // set-up: E transposed, row sums of A, emission bounds, operand copies of A
+  k_transpose_f32<<<dim3(cdiv(V, 32), cdiv(H, 32)), dim3(32, 8), 0, s>>>(E, H, V, w.Et);
+  PC_LAUNCH_CHECK();
+  k_rowsum<<<cdiv(H, 8), 256, 0, s>>>(A, H, w.rs);
+  PC_LAUNCH_CHECK();
+  k_emission_bounds<<<V, 256, 0, s>>>(w.Et, w.rs, H, w.emax, w.emax_rs);
+  PC_LAUNCH_CHECK();
+  if (T >= 2 && (st = rows_to_operand<P>(A, H, 0, 1, H, H, w.Aop, s)) != PC_OK) return st;
+  if (chain && (st = transpose_to_operand<P>(A, H, 0, 1, H, H, w.Atop, s)) != PC_OK) return st;
+
+  // leaf (position T-1)
+  {
+    const int t = T - 1;
+    const bool has_next = T >= 2;
+    const Operand& ub = w.ubm[t & 1];
+    k_hmm_leaf<P><<<dim3(cdiv(H, 32), cdiv(B, 32)), dim3(32, 8), 0, s>>>(
+        H, B, T, tokens, w.Et, w.emax, has_next ? ub.ptr : nullptr, ub.ld, ub.lo_elems,
+        chain ? w.un.ptr : nullptr, w.un.ld, w.un.lo_elems, static_cast<long long>(T - 2) * B,
+        T == 1 ? w.U0 : nullptr, w.umax, w.cf, w.logc);
+    PC_LAUNCH_CHECK();
+  }
+
+  // forward chain: S_t for t = T-2 .. 0
+  if (T >= 2) {
+    OperandMaps ma, mb[2];
+    if ((st = encode_maps(&ma, w.Aop, prec, kBM)) != PC_OK) return st;
+    for (int i = 0; i < 2; ++i)
+      if ((st = encode_maps(&mb[i], w.ubm[i], prec, kChainBN)) != PC_OK) return st;
+    const dim3 grid(cdiv(H, kBM), cdiv(B, kChainBN), 1);
+    const int nkb = num_k_blocks(H, prec);
+    for (int t = T - 2; t >= 0; --t) {
+      typename EpiHmmFwd<P>::Params ep{};
+      ep.H = H; ep.B = B; ep.T = T; ep.t = t;
+      ep.tokens = tokens; ep.Et = w.Et; ep.emax_rs = w.emax_rs;
+      ep.umax_prev = w.umax + static_cast<long long>(t + 1) * B;
+      ep.umax_cur = w.umax + static_cast<long long>(t) * B;
+      ep.cf = w.cf; ep.logc = w.logc;
+      if (t >= 1) {
+        ep.ubm = w.ubm[t & 1].ptr; ep.ubm_ld = w.ubm[t & 1].ld; ep.ubm_lo = w.ubm[t & 1].lo_elems;
+        if (chain) { ep.un = w.un.ptr; ep.un_ld = w.un.ld; ep.un_lo = w.un.lo_elems; }
+      } else {
+        ep.U0 = w.U0;
+      }
+      const OperandMaps& b = mb[(t + 1) & 1];
+      if ((st = launch_gemm<P, kChainBN, EpiHmmFwd<P>>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                        PC_KIND_HMM_FWD, 2ll * H * H * B)) != PC_OK)
+        return st;
+    }
+  }
+
+  k_hmm_root<<<B, 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, ll, w.rroot);
+  PC_LAUNCH_CHECK();
+  if (!flows) return PC_OK;
+
+  k_hmm_root_flows<P><<<dim3(cdiv(H, 32), cdiv(B, 32)), dim3(32, 8), 0, s>>>(
+      H, B, T, tokens, pi, w.U0, w.Et, w.cf, w.rroot, chain ? w.wbm[0].ptr : nullptr, w.wbm[0].ld,
+      w.wbm[0].lo_elems, (chain && dA) ? w.wn.ptr : nullptr, w.wn.ld, w.wn.lo_elems, w.dEt, dpi);
+  PC_LAUNCH_CHECK();
+
+  if (chain) {
+    OperandMaps ma, mb[2];
+    if ((st = encode_maps(&ma, w.Atop, prec, kBM)) != PC_OK) return st;
+    for (int i = 0; i < 2; ++i)
+      if ((st = encode_maps(&mb[i], w.wbm[i], prec, kChainBN)) != PC_OK) return st;
+    const dim3 grid(cdiv(H, kBM), cdiv(B, kChainBN), 1);
+    const int nkb = num_k_blocks(H, prec);
+    for (int t = 0; t <= T - 2; ++t) {
+      typename EpiHmmBwd<P>::Params ep{};
+      ep.H = H; ep.B = B; ep.T = T; ep.t = t;
+      ep.tokens = tokens; ep.Et = w.Et; ep.cf = w.cf;
+      ep.un = w.un.ptr; ep.un_ld = w.un.ld; ep.un_lo = w.un.lo_elems;
+      ep.dEt = w.dEt;
+      if (t + 1 <= T - 2) {
+        const Operand& nb = w.wbm[(t + 1) & 1];
+        ep.wbm = nb.ptr; ep.wbm_ld = nb.ld; ep.wbm_lo = nb.lo_elems;
+        if (dA) { ep.wn = w.wn.ptr; ep.wn_ld = w.wn.ld; ep.wn_lo = w.wn.lo_elems; }
+      }
+      const OperandMaps& b = mb[t & 1];
+      if ((st = launch_gemm<P, kChainBN, EpiHmmBwd<P>>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                        PC_KIND_HMM_ELEM, 2ll * H * H * B)) != PC_OK)
+        return st;
+    }
+    if (dA) {
+      OperandMaps pa, pb;
+      if ((st = encode_maps(&pa, w.wn, prec, kBM)) != PC_OK) return st;
+      if ((st = encode_maps(&pb, w.un, prec, kParamBN)) != PC_OK) return st;
+      EpiThetaScale::Params ep{dA, A, H, H, accumulate};
+      if ((st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), 1), pa.hi, pa.lo,
+                                                        pb.hi, pb.lo, num_k_blocks(static_cast<long long>(T - 1) * B, prec),
+                                                        ep, s, PC_KIND_HMM_PARAM,
+                                                        2ll * H * H * (T - 1) * B)) != PC_OK)
+        return st;
+    }
+  } else if (dA && !accumulate && T >= 2) {
+    PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
+  }
+  if (dE) {
+    k_transpose_add_f32<<<dim3(cdiv(H, 32), cdiv(V, 32)), dim3(32, 8), 0, s>>>(w.dEt, V, H, dE, accumulate);
+    PC_LAUNCH_CHECK();
+  }
+  return PC_OK;
+}
+
+}  // namespace
+}  // namespace pc
+
+extern "C" {
+
+pc_status_t pc_hmm_workspace(int H, int T, int V, int B, pc_precision_t prec, size_t* bytes) {
+  pc::clear_error();
+  PC_CHECK(bytes != nullptr, PC_ERR_NULL, "bytes is NULL");
+  pc_status_t st;
+  if ((st = pc::check_precision(prec)) != PC_OK) return st;
+  if ((st = pc::check_hmm_shape(H, T, V, B)) != PC_OK) return st;
+  *bytes = pc::hmm_ws_bytes(prec, H, T, V, B);
+  return PC_OK;
+}
+
+pc_status_t pc_hmm_fwd_bwd(int H, int T, int V, int B, const int32_t* tokens, const float* pi,
+                           const float* A, const float* E, double* ll, float* dpi, float* dA,
+                           float* dE, int accumulate, pc_precision_t prec, void* ws,
+                           size_t ws_bytes, pc_stream_t stream) {
+  pc::clear_error();
+  pc_status_t st;
+  if ((st = pc::check_precision(prec)) != PC_OK) return st;
+  if ((st = pc::check_hmm_shape(H, T, V, B)) != PC_OK) return st;
+  PC_CHECK(tokens && pi && A && E && ll, PC_ERR_NULL, "tokens, pi, A, E and ll must not be NULL");
+  PC_CHECK(ws, PC_ERR_WORKSPACE, "workspace is NULL");
+  const size_t need = pc::hmm_ws_bytes(prec, H, T, V, B);
+  PC_CHECK(ws_bytes >= need, PC_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, need);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (prec) {
+    case PC_PREC_AUTO:
+      return pc::hmm_run<pc::kBF16>(H, T, V, B, tokens, pi, A, E, ll, dpi, dA, dE, accumulate, prec, ws, s);
+    case PC_PREC_TF32:
+      return pc::hmm_run<pc::kTF32>(H, T, V, B, tokens, pi, A, E, ll, dpi, dA, dE, accumulate, prec, ws, s);
+    default:
+      return pc::hmm_run<pc::kTF32x3>(H, T, V, B, tokens, pi, A, E, ll, dpi, dA, dE, accumulate, prec, ws, s);
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,214 @@
+// One warp-specialised tensor-core contraction, used by every sum-layer pass:
+//
+//   D[m, n] = sum_k Aop[g][m][k] * Bop[g][n][k]        (both operands K-major)
+//
+// followed by a pass-specific epilogue on the float32 accumulator. A CTA owns one
+// 128 x BN tile of D for group g = blockIdx.z:
+//   warp 0     TMA producer (one thread): 128-byte-swizzled K-slices of A and B into a
+//              STAGES-deep shared-memory ring, completion counted in transaction bytes
+//   warp 1     MMA issuer (one thread): tcgen05.mma (kind::f16 or kind::tf32, M = 128,
+//              N = BN) into a TMEM accumulator; tcgen05.commit frees each ring slot
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (row of D) per
+//              thread, 32 columns at a time, into the pass's epilogue functor
+// Precision kTF32x3 forms each product from three TF32 MMAs (lo*hi + hi*lo + hi*hi)
+// into the same accumulator (pyjuice PR #62, Summary 3, "tf32x3").
+//
+// Every wait is bounded (pc::mbar_wait); on a timeout the kernel records the reason
+// in the device status word, lets the producer drain its in-flight copies, frees its
+// TMEM and returns.
+#pragma once
+
+#include "pc_device.cuh"
+
+namespace pc {
+
+constexpr int kGemmThreads = 192;
+constexpr int kBM = 128;
+
+template <int P, int BN>
+struct GemmShape {
+  static constexpr int kElem = operand_bytes<P>();
+  static constexpr int kBK = 128 / kElem;                // K elements per 128-byte row
+  static constexpr int kParts = (P == kTF32x3) ? 2 : 1;  // hi (+ lo)
+  static constexpr uint32_t kABytes = kBM * 128;
+  static constexpr uint32_t kBBytes = BN * 128;
+  static constexpr uint32_t kStageBytes = kParts * (kABytes + kBBytes);
+  static constexpr int kMaxStages = 8;
+  static constexpr int kStages =
+      (200 * 1024 / kStageBytes) < kMaxStages ? (200 * 1024 / kStageBytes) : kMaxStages;
+  static constexpr uint32_t kUmmaK = (P == kBF16) ? 16 : 8;  // K per MMA instruction
+  static constexpr uint32_t kKSteps = kBK / kUmmaK;          // MMAs per ring slot (4)
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(kStages >= 2, "stages");
+};
+
+template <int P, int BN, class Epi>
+constexpr size_t gemm_smem_bytes() {
+  using S = GemmShape<P, BN>;
+  return 1024 /* alignment slack */ + size_t(S::kStages) * S::kStageBytes + 256 /* barriers */ +
+         Epi::kSmemBytes;
+}
+
+__device__ __forceinline__ void epilogue_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int P, int BN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
+                int num_kb, unsigned* status, const typename Epi::Params ep) {
+  using S = GemmShape<P, BN>;
+  constexpr int kStages = S::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * S::kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint8_t* epi_smem = smem + kStages * S::kStageBytes + 256;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kBM;
+  const int n0 = blockIdx.y * BN;
+  const int g = blockIdx.z;
+
+  auto a_tile = [&](int s, int part) { return smem + s * S::kStageBytes + part * S::kABytes; };
+  auto b_tile = [&](int s, int part) {
+    return smem + s * S::kStageBytes + S::kParts * S::kABytes + part * S::kBBytes;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      mbar_init(acc_full, 1);
+      fence_barrier_init();
+      tma_prefetch_map(&tmA);
+      tma_prefetch_map(&tmB);
+      if constexpr (P == kTF32x3) {
+        tma_prefetch_map(&tmA_lo);
+        tma_prefetch_map(&tmB_lo);
+      }
+    }
+    __syncwarp();
+    tmem_alloc(tmem_slot, BN);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int issued = 0;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, status, kErrTimeoutProducer)) break;
+        mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+        const int kx = kb * S::kBK;
+        tma_load_3d(a_tile(s, 0), &tmA, &full[s], kx, m0, g);
+        tma_load_3d(b_tile(s, 0), &tmB, &full[s], kx, n0, g);
+        if constexpr (P == kTF32x3) {
+          tma_load_3d(a_tile(s, 1), &tmA_lo, &full[s], kx, m0, g);
+          tma_load_3d(b_tile(s, 1), &tmB_lo, &full[s], kx, n0, g);
+        }
+        issued = kb + 1;
+      }
+      // Drain: every slot's most recent fill must have landed before the CTA exits.
+      for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb) {
+        mbar_wait(&full[kb % kStages], (kb / kStages) & 1, status, kErrTimeoutDrain);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = umma_idesc(P == kBF16 ? 1u : 2u, kBM, BN);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1;
+        if (!mbar_wait(&full[s], ph, status, kErrTimeoutMma)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_addr(a_tile(s, 0));
+        const uint32_t b0 = smem_addr(b_tile(s, 0));
+#pragma unroll
+        for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
+          const uint32_t off = kk * 32;  // 32 bytes of K per MMA
+          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+          if constexpr (P == kBF16) {
+            umma_bf16(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+          } else if constexpr (P == kTF32) {
+            umma_tf32(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+          } else {
+            const uint32_t a1 = smem_addr(a_tile(s, 1));
+            const uint32_t b1 = smem_addr(b_tile(s, 1));
+            umma_tf32(tmem, umma_desc_sw128(a1 + off), umma_desc_sw128(b0 + off), idesc, acc);
+            umma_tf32(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, 1u);
+            umma_tf32(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, 1u);
+          }
+        }
+        umma_commit(&empty[s]);
+      }
+      umma_commit(acc_full);  // also on a timeout: the epilogue must not wait forever
+    }
+  } else {
+    // ------------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;  // 0..127
+    Epi::prepare(ep, g, m0, n0, et, epi_smem);
+    epilogue_bar_sync();
+    const bool ok = mbar_wait(acc_full, 0, status, kErrTimeoutEpilogue);
+    tc_fence_after();
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld_32x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
+        Epi::apply(ep, g, m0, n0, row, c, v, epi_smem);
+      }
+    }
+    tc_fence_before();
+    epilogue_bar_sync();
+    if (ok) Epi::finish(ep, g, m0, n0, et, epi_smem);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+// Default hooks for epilogues that need no per-CTA set-up or reduction.
+struct EpiNoHooks {
+  static constexpr int kSmemBytes = 0;
+  template <class Params>
+  __device__ static void prepare(const Params&, int, int, int, int, uint8_t*) {}
+  template <class Params>
+  __device__ static void finish(const Params&, int, int, int, int, uint8_t*) {}
+};
+
+// Lane l of the warp ends with the maximum over the 32 lanes of v[l] (v is clobbered).
+__device__ __forceinline__ float warp_transpose_max(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      v[i] = fmaxf(keep, recv);
+    }
+  }
+  return v[0];
+}
+
+}  // namespace pc

@@ -1,0 +1,107 @@
+// Host-side helpers shared by the entry points: error reporting, argument checks,
+// workspace carving, TMA tensor-map encoding and GEMM launches.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstddef>
+#include <cstdint>
+#include <cstdio>
+
+#include "../../include/pcsum.h"
+
+namespace pc {
+
+// ------------------------------------------------------------------ errors
+pc_status_t set_error(pc_status_t st, const char* fmt, ...);
+void clear_error();
+
+// Device status word of the current device (a __device__ variable; its address is
+// looked up once per device).
+unsigned* device_status_word();
+
+// Contraction profiler hooks (no-ops unless pc_profile_start is active).
+int profile_begin(cudaStream_t s);
+void profile_end(int slot, cudaStream_t s, int kind, long long flops);
+
+#define PC_CHECK(cond, st, ...)                 \
+  do {                                          \
+    if (!(cond)) return ::pc::set_error(st, __VA_ARGS__); \
+  } while (0)
+
+#define PC_CUDA(call)                                                                     \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess)                                                                \
+      return ::pc::set_error(PC_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+// Counts every kernel the library launches (pc_launch_count) after checking the launch.
+void count_launch();
+#define PC_LAUNCH_CHECK()         \
+  do {                            \
+    PC_CUDA(cudaGetLastError());  \
+    ::pc::count_launch();         \
+  } while (0)
+
+inline pc_status_t check_precision(pc_precision_t p) {
+  if (p != PC_PREC_AUTO && p != PC_PREC_TF32 && p != PC_PREC_FP32)
+    return set_error(PC_ERR_UNKNOWN_PRECISION,
+                     "unknown precision %d; valid modes are PC_PREC_AUTO (0, bf16 products), "
+                     "PC_PREC_TF32 (1) and PC_PREC_FP32 (2, 3xTF32)",
+                     static_cast<int>(p));
+  return PC_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
+
+// Bytes of one stored operand element, and the number of stored parts (hi, lo).
+inline int operand_elem_bytes(pc_precision_t p) { return p == PC_PREC_AUTO ? 2 : 4; }
+inline int operand_parts(pc_precision_t p) { return p == PC_PREC_FP32 ? 2 : 1; }
+
+// An operand matrix [groups][rows][ld] in a precision's storage format. For 3xTF32
+// the lo part follows the hi part at +lo_elems elements.
+struct Operand {
+  void* ptr = nullptr;
+  long long rows = 0, cols = 0, ld = 0, groups = 1;
+  size_t lo_elems = 0;
+  static size_t bytes(pc_precision_t p, long long groups, long long rows, long long cols) {
+    const long long ld = round_up(cols > 0 ? cols : 1, 64);
+    return size_t(groups) * rows * ld * operand_elem_bytes(p) * operand_parts(p);
+  }
+};
+
+// Bump allocator over the caller's workspace (256-byte granules).
+struct Carver {
+  uint8_t* base;
+  size_t used = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t n) {
+    used = static_cast<size_t>(round_up(static_cast<long long>(used), 256));
+    void* p = base ? base + used : nullptr;
+    used += n;
+    return p;
+  }
+  Operand operand(pc_precision_t p, long long groups, long long rows, long long cols) {
+    Operand o;
+    o.groups = groups;
+    o.rows = rows;
+    o.cols = cols;
+    o.ld = round_up(cols > 0 ? cols : 1, 64);
+    const size_t part = size_t(groups) * rows * o.ld;
+    o.lo_elems = operand_parts(p) == 2 ? part : 0;
+    o.ptr = take(Operand::bytes(p, groups, rows, cols));
+    return o;
+  }
+};
+
+// 3-D tensor map over an Operand: dims {cols (K), rows, groups}, box {128 bytes of K,
+// box_rows, 1}, 128-byte swizzle, zero fill outside the tensor. part 1 = the lo half.
+pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision_t p,
+                               int box_rows, int part);
+
+}  // namespace pc

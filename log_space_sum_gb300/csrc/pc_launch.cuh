@@ -1,0 +1,145 @@
+// Launch helpers: the tensor-core contraction and the small elementwise kernels that
+// build its operands.
+#pragma once
+
+#include "pc_gemm.cuh"
+#include "pc_host.h"
+
+namespace pc {
+
+template <int P, int BN, class Epi>
+pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo,
+                        const CUtensorMap& b, const CUtensorMap& b_lo, int num_kb,
+                        const typename Epi::Params& ep, cudaStream_t stream, int kind,
+                        long long flops) {
+  constexpr size_t smem = gemm_smem_bytes<P, BN, Epi>();
+  static_assert(smem <= 232448, "shared memory per CTA");
+  static bool attr_set[64] = {};
+  int dev = 0;
+  PC_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return set_error(PC_ERR_CUDA, "device index %d out of range", dev);
+  if (!attr_set[dev]) {
+    PC_CUDA(cudaFuncSetAttribute(k_umma_gemm<P, BN, Epi>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+    attr_set[dev] = true;
+  }
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return PC_OK;
+  const int slot = profile_begin(stream);
+  k_umma_gemm<P, BN, Epi><<<grid, kGemmThreads, smem, stream>>>(a, a_lo, b, b_lo, num_kb,
+                                                                device_status_word(), ep);
+  PC_LAUNCH_CHECK();
+  profile_end(slot, stream, kind, flops);
+  return PC_OK;
+}
+
+// Tensor maps of an operand's hi and (3xTF32) lo parts.
+struct OperandMaps {
+  CUtensorMap hi, lo;
+};
+
+inline pc_status_t encode_maps(OperandMaps* m, const Operand& op, pc_precision_t p, int box_rows) {
+  pc_status_t st = encode_operand_map(&m->hi, op, p, box_rows, 0);
+  if (st != PC_OK) return st;
+  if (p == PC_PREC_FP32) return encode_operand_map(&m->lo, op, p, box_rows, 1);
+  m->lo = m->hi;
+  return PC_OK;
+}
+
+inline int num_k_blocks(long long K, pc_precision_t p) {
+  const int bk = 128 / operand_elem_bytes(p);
+  return static_cast<int>((K + bk - 1) / bk);
+}
+
+inline unsigned cdiv(long long a, long long b) { return static_cast<unsigned>((a + b - 1) / b); }
+
+// ---------------------------------------------------------------------------------
+// Operand builders.
+
+// dst[g][r][c] = op(src[g][r][c]); src row stride src_ld, group stride src_gs.
+template <int P>
+__global__ void k_rows_to_operand(const float* __restrict__ src, long long src_ld,
+                                  long long src_gs, int G, int R, int C, void* dst,
+                                  long long dst_ld, size_t lo) {
+  const long long total = static_cast<long long>(G) * R * C;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long c = idx % C;
+    const long long gr = idx / C;
+    const long long r = gr % R;
+    const long long g = gr / R;
+    const float v = src[g * src_gs + r * src_ld + c];
+    store_operand<P>(dst, static_cast<size_t>((g * R + r) * dst_ld + c), lo, v);
+  }
+}
+
+// dst[g][c][r] = op(src[g][r][c]) through 32x32 shared-memory tiles.
+template <int P>
+__global__ void k_transpose_to_operand(const float* __restrict__ src, long long src_ld,
+                                       long long src_gs, int R, int C, void* dst,
+                                       long long dst_ld, size_t lo) {
+  __shared__ float tile[32][33];
+  const int g = blockIdx.z;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int k = ty; k < 32; k += 8) {
+    const int r = r0 + k, c = c0 + tx;
+    tile[k][tx] = (r < R && c < C) ? src[g * src_gs + static_cast<long long>(r) * src_ld + c] : 0.f;
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int c = c0 + k, r = r0 + tx;
+    if (r < R && c < C)
+      store_operand<P>(dst, static_cast<size_t>((static_cast<long long>(g) * C + c) * dst_ld + r),
+                       lo, tile[tx][k]);
+  }
+}
+
+template <int P>
+pc_status_t rows_to_operand(const float* src, long long src_ld, long long src_gs, int G, int R,
+                            int C, const Operand& dst, cudaStream_t s) {
+  const long long total = static_cast<long long>(G) * R * C;
+  if (total == 0) return PC_OK;
+  const unsigned blocks = static_cast<unsigned>((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
+  k_rows_to_operand<P><<<blocks, 256, 0, s>>>(src, src_ld, src_gs, G, R, C, dst.ptr, dst.ld, dst.lo_elems);
+  PC_LAUNCH_CHECK();
+  return PC_OK;
+}
+
+template <int P>
+pc_status_t transpose_to_operand(const float* src, long long src_ld, long long src_gs, int G,
+                                 int R, int C, const Operand& dst, cudaStream_t s) {
+  if (G == 0 || R == 0 || C == 0) return PC_OK;
+  dim3 grid(cdiv(C, 32), cdiv(R, 32), G);
+  k_transpose_to_operand<P><<<grid, dim3(32, 8), 0, s>>>(src, src_ld, src_gs, R, C, dst.ptr, dst.ld,
+                                                         dst.lo_elems);
+  PC_LAUNCH_CHECK();
+  return PC_OK;
+}
+
+// Shared with the circuits: F[g][i][j] (+)= theta[g][i][j] * D[i,j].
+struct EpiThetaScale : EpiNoHooks {
+  struct Params {
+    float* F;
+    const float* theta;
+    int M, N, accumulate;
+  };
+  __device__ static void apply(const Params& p, int g, int m0, int n0, int row, int col0,
+                               float (&v)[32], uint8_t*) {
+    const int i = m0 + row;
+    if (i >= p.M) return;
+    const long long base = (static_cast<long long>(g) * p.M + i) * p.N;
+    const int jj = n0 + col0;
+    const float* t = p.theta + base;
+    float* F = p.F + base;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int j = jj + c;
+      if (j < p.N) {
+        const float val = t[j] * v[c];
+        F[j] = p.accumulate ? F[j] + val : val;
+      }
+    }
+  }
+};
+
+}  // namespace pc
