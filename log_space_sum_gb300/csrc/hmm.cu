@@ -209,21 +209,22 @@ struct EpiHmmFwd {
     float* red = reinterpret_cast<float*>(smem) + 2 * kChainBN;
     const int k = m0 + row;
     const bool kin = k < p.H;
+    const int nvalid = kin ? min(32, p.B - (n0 + col0)) : 0;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const int lc = col0 + c;
       const int b = n0 + lc;
       float u = 0.f;
-      if (kin && b < p.B) {
+      if (c < nvalid) {
         u = p.Et[static_cast<long long>(tok_s[lc]) * p.H + k] * v[c] * c_s[lc];
         if (p.ubm) store_operand<P>(p.ubm, static_cast<size_t>(b * p.ubm_ld + k), p.ubm_lo, u);
-        if (p.un)
-          store_operand<P>(p.un, static_cast<size_t>(k * p.un_ld + static_cast<long long>(p.t - 1) * p.B + b),
-                           p.un_lo, u);
         if (p.U0) p.U0[static_cast<long long>(b) * p.H + k] = u;
       }
       v[c] = u;
     }
+    if (p.un && nvalid > 0)
+      store_operand_run<P>(p.un, static_cast<size_t>(k * p.un_ld + static_cast<long long>(p.t - 1) * p.B + n0 + col0),
+                           p.un_lo, v, nvalid);
     const float mx = warp_transpose_max(v);
     const int q = (threadIdx.x >> 5) & 3;
     red[q * kChainBN + col0 + (threadIdx.x & 31)] = mx;
@@ -342,27 +343,30 @@ struct EpiHmmBwd : EpiNoHooks {
     const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
     const int j = m0 + row;
     if (j >= p.H) return;
+    const int nvalid = min(32, p.B - (n0 + col0));
+    if (nvalid <= 0) return;
+    if (p.dEt) {
+      float u[32];
+      load_operand_run<P>(p.un, static_cast<size_t>(j * p.un_ld + static_cast<long long>(p.t) * p.B + n0 + col0),
+                          p.un_lo, u, nvalid);
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) atomicAdd(&p.dEt[static_cast<long long>(tok_s[col0 + c]) * p.H + j], u[c] * v[c]);
+    }
+    if (!p.wbm) return;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const int lc = col0 + c;
-      const int b = n0 + lc;
-      if (b < p.B) {
-        const float s = v[c];
-        const long long tokH = static_cast<long long>(tok_s[lc]) * p.H;
-        if (p.dEt) {
-          const float u = load_operand<P>(p.un, static_cast<size_t>(j * p.un_ld + static_cast<long long>(p.t) * p.B + b),
-                                          p.un_lo);
-          atomicAdd(&p.dEt[tokH + j], u * s);
-        }
-        if (p.wbm) {
-          const float w = p.Et[tokH + j] * c_s[lc] * s;
-          store_operand<P>(p.wbm, static_cast<size_t>(b * p.wbm_ld + j), p.wbm_lo, w);
-          if (p.wn)
-            store_operand<P>(p.wn, static_cast<size_t>(j * p.wn_ld + static_cast<long long>(p.t + 1) * p.B + b),
-                             p.wn_lo, w);
-        }
+      float w = 0.f;
+      if (c < nvalid) {
+        w = p.Et[static_cast<long long>(tok_s[lc]) * p.H + j] * c_s[lc] * v[c];
+        store_operand<P>(p.wbm, static_cast<size_t>((n0 + lc) * p.wbm_ld + j), p.wbm_lo, w);
       }
+      v[c] = w;
     }
+    if (p.wn)
+      store_operand_run<P>(p.wn, static_cast<size_t>(j * p.wn_ld + static_cast<long long>(p.t + 1) * p.B + n0 + col0),
+                           p.wn_lo, v, nvalid);
   }
 };
 
@@ -418,7 +422,7 @@ template <int P>
 pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const float* pi, const float* A,
                     const float* E, double* ll, float* dpi, float* dA, float* dE, int accumulate,
                     pc_precision_t prec, void* ws, cudaStream_t s) {
-  constexpr int kParamBN = (P == kTF32x3) ? 128 : 256;
+  constexpr int kParamBN = (P == kBF16) ? 256 : 128;  // sliced modes hold BN sums per thread
   const bool flows = dpi || dA || dE;
   const bool chain = flows && (dA || dE) && T >= 2;
   HmmWs w;

@@ -46,6 +46,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -227,6 +231,83 @@ __device__ __forceinline__ float load_operand(const void* base, size_t idx, size
 
 template <int P>
 constexpr int operand_bytes() { return P == kBF16 ? 2 : 4; }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// A thread's run of n <= 32 consecutive operand values starting at element idx:
+// 16-byte vector accesses when the run is full and aligned, scalar ones otherwise.
+template <int P>
+__device__ __forceinline__ void store_operand_run(void* base, size_t idx, size_t lo,
+                                                  const float (&v)[32], int n) {
+  constexpr int kVec = P == kBF16 ? 8 : 4;
+  if (n == 32 && (idx % kVec) == 0) {
+    if constexpr (P == kBF16) {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + idx);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    } else {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx);
+      float4* dlo = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx + lo);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 h = make_float4(tf32_rna(v[4 * q]), tf32_rna(v[4 * q + 1]), tf32_rna(v[4 * q + 2]),
+                                     tf32_rna(v[4 * q + 3]));
+        dst[q] = h;
+        if constexpr (P == kTF32x3)
+          dlo[q] = make_float4(tf32_rna(v[4 * q] - h.x), tf32_rna(v[4 * q + 1] - h.y),
+                               tf32_rna(v[4 * q + 2] - h.z), tf32_rna(v[4 * q + 3] - h.w));
+      }
+    }
+  } else {
+    for (int i = 0; i < n; ++i) store_operand<P>(base, idx + i, lo, v[i]);
+  }
+}
+
+template <int P>
+__device__ __forceinline__ void load_operand_run(const void* base, size_t idx, size_t lo,
+                                                 float (&v)[32], int n) {
+  constexpr int kVec = P == kBF16 ? 8 : 4;
+  if (n == 32 && (idx % kVec) == 0) {
+    if constexpr (P == kBF16) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = src[q];
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          v[8 * q + 2 * r] = __uint_as_float(ww[r] << 16);
+          v[8 * q + 2 * r + 1] = __uint_as_float(ww[r] & 0xFFFF0000u);
+        }
+      }
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
+      const float4* slo = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx + lo);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 h = src[q];
+        if constexpr (P == kTF32x3) {
+          const float4 l = slo[q];
+          h.x += l.x;
+          h.y += l.y;
+          h.z += l.z;
+          h.w += l.w;
+        }
+        v[4 * q] = h.x;
+        v[4 * q + 1] = h.y;
+        v[4 * q + 2] = h.z;
+        v[4 * q + 3] = h.w;
+      }
+    }
+  } else {
+    for (int i = 0; i < 32; ++i) v[i] = i < n ? load_operand<P>(base, idx + i, lo) : 0.f;
+  }
+}
 
 // Non-negative floats order like their bit patterns: atomicMax on the bits.
 __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {

@@ -53,6 +53,20 @@ __device__ __forceinline__ void epilogue_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Named barrier of the 128 epilogue threads that also ANDs a predicate over them.
+__device__ __forceinline__ bool epilogue_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
 template <int P, int BN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
@@ -60,13 +74,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 int num_kb, unsigned* status, const typename Epi::Params ep) {
   using S = GemmShape<P, BN>;
   constexpr int kStages = S::kStages;
+  // TF32 modes: every K slice (kSliceKB ring slots) is accumulated from zero in one
+  // of two TMEM buffers and added into registers by the epilogue with round-to-
+  // nearest adds. The tensor-core accumulator truncates on every accumulation, so
+  // its bias grows with the number of MMAs summed into one value; slicing bounds
+  // that number whatever K is (3xTF32: one slot = 4 k-steps x 3 products, issued
+  // small cross terms first; TF32: four slots = 16 MMAs).
+  constexpr int kSliceKB = (P == kTF32x3) ? 1 : (P == kTF32 ? 4 : 0);
+  constexpr bool kSliced = kSliceKB > 0;
+  constexpr uint32_t kTmemCols = kSliced ? 2 * BN : BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * S::kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = empty + kStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;    // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   uint8_t* epi_smem = smem + kStages * S::kStageBytes + 256;
 
   const int warp = threadIdx.x >> 5;
@@ -86,7 +110,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);
       }
-      mbar_init(acc_full, 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&acc_full[b], 1);
+        mbar_init(&acc_empty[b], 1);
+      }
       fence_barrier_init();
       tma_prefetch_map(&tmA);
       tma_prefetch_map(&tmB);
@@ -96,7 +123,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     __syncwarp();
-    tmem_alloc(tmem_slot, BN);
+    tmem_alloc(tmem_slot, kTmemCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -133,55 +160,110 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = (kb / kStages) & 1;
+        const int slice = kSliced ? kb / (kSliceKB > 0 ? kSliceKB : 1) : 0;
+        const bool first = kSliced ? (kb % (kSliceKB > 0 ? kSliceKB : 1)) == 0 : kb == 0;
+        const bool last = kSliced && ((kb % (kSliceKB > 0 ? kSliceKB : 1)) == kSliceKB - 1 || kb == num_kb - 1);
+        uint32_t d = tmem;
+        if constexpr (kSliced) {
+          const int buf = slice & 1;
+          if (first && !mbar_wait(&acc_empty[buf], ((slice >> 1) & 1) ^ 1, status, kErrTimeoutMma)) break;
+          d = tmem + static_cast<uint32_t>(buf * BN);
+        }
         if (!mbar_wait(&full[s], ph, status, kErrTimeoutMma)) break;
         tc_fence_after();
         const uint32_t a0 = smem_addr(a_tile(s, 0));
         const uint32_t b0 = smem_addr(b_tile(s, 0));
+        if constexpr (P == kTF32x3) {
+          const uint32_t a1 = smem_addr(a_tile(s, 1));
+          const uint32_t b1 = smem_addr(b_tile(s, 1));
+          // the small cross terms first, then hi*hi, into the zeroed buffer
 #pragma unroll
-        for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
-          const uint32_t off = kk * 32;  // 32 bytes of K per MMA
-          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-          if constexpr (P == kBF16) {
-            umma_bf16(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
-          } else if constexpr (P == kTF32) {
-            umma_tf32(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
-          } else {
-            const uint32_t a1 = smem_addr(a_tile(s, 1));
-            const uint32_t b1 = smem_addr(b_tile(s, 1));
-            umma_tf32(tmem, umma_desc_sw128(a1 + off), umma_desc_sw128(b0 + off), idesc, acc);
-            umma_tf32(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, 1u);
-            umma_tf32(tmem, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, 1u);
+          for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
+            const uint32_t off = kk * 32;
+            umma_tf32(d, umma_desc_sw128(a1 + off), umma_desc_sw128(b0 + off), idesc,
+                      (first && kk == 0) ? 0u : 1u);
+            umma_tf32(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, 1u);
+          }
+#pragma unroll
+          for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
+            const uint32_t off = kk * 32;
+            umma_tf32(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, 1u);
+          }
+        } else {
+#pragma unroll
+          for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
+            const uint32_t off = kk * 32;  // 32 bytes of K per MMA
+            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+            if constexpr (P == kBF16) {
+              umma_bf16(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+            } else {
+              umma_tf32(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+            }
           }
         }
         umma_commit(&empty[s]);
+        if (last) umma_commit(&acc_full[slice & 1]);
       }
-      umma_commit(acc_full);  // also on a timeout: the epilogue must not wait forever
+      // also on a timeout: the epilogue must not wait forever
+      if constexpr (!kSliced) umma_commit(&acc_full[0]);
     }
   } else {
     // ------------------------------------------------------------------- epilogue
     const int et = threadIdx.x - 64;  // 0..127
     Epi::prepare(ep, g, m0, n0, et, epi_smem);
     epilogue_bar_sync();
-    const bool ok = mbar_wait(acc_full, 0, status, kErrTimeoutEpilogue);
-    tc_fence_after();
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    if (ok) {
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    bool ok = true;
+    if constexpr (kSliced) {
+      float acc[BN / 32][32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[c][i] = 0.f;
+      const int num_slices = (num_kb + kSliceKB - 1) / kSliceKB;
+      for (int sl = 0; sl < num_slices; ++sl) {
+        const int buf = sl & 1;
+        // all 128 epilogue threads agree on whether the slice arrived
+        ok = epilogue_bar_and(mbar_wait(&acc_full[buf], (sl >> 1) & 1, status, kErrTimeoutEpilogue));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld_32x32(lane_base + static_cast<uint32_t>(buf * BN + c * 32), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c][i] += v[i];
+        }
+        tc_fence_before();
+        epilogue_bar_sync();
+        if (et == 0) mbar_arrive(&acc_empty[buf]);
+      }
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) Epi::apply(ep, g, m0, n0, row, c * 32, acc[c], epi_smem);
+      }
+    } else {
+      ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue));
+      tc_fence_after();
+      if (ok) {
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        tmem_ld_32x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c), v);
-        Epi::apply(ep, g, m0, n0, row, c, v, epi_smem);
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld_32x32(lane_base + static_cast<uint32_t>(c), v);
+          Epi::apply(ep, g, m0, n0, row, c, v, epi_smem);
+        }
       }
     }
     tc_fence_before();
-    epilogue_bar_sync();
+    ok = epilogue_bar_and(ok);
     if (ok) Epi::finish(ep, g, m0, n0, et, epi_smem);
   }
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 

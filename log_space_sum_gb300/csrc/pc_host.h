@@ -10,7 +10,7 @@
 #include <cstdint>
 #include <cstdio>
 
-#include "../../include/pcsum.h"
+#include "pcsum.h"
 
 namespace pc {
 

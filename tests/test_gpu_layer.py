@@ -6,7 +6,7 @@ import torch
 
 import log_space_sum_gb300 as pc
 from oracle.sum_layer import sum_layer_fwd, sum_layer_bwd
-from tolerances import FLOW_TOL, LL_TOL, MODES, flow_err, ll_err
+from tolerances import FLOW_TOL, LL_TOL, MODES, flow_err, out_err
 from workloads import layer, layer_inputs
 
 pytestmark = pytest.mark.gpu
@@ -22,21 +22,28 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def _run(d, mode, f=None):
+def _run(d, mode):
+    """GPU forward, and GPU backward on the oracle's node values rounded to float32:
+    both sides of the backward comparison then get the same inputs (theta, x, out, f)."""
     th, x = _dev(d["theta"]), _dev(d["x"])
     cs = d["child_stride"]
     out = pc.sum_layer_fwd(th, x, child_stride=cs, precision=mode)
-    ff = _dev(d["f"] if f is None else f)
-    e, F = pc.sum_layer_bwd(th, x, out, ff, child_stride=cs, precision=mode)
+    out_in = _dev(_oracle_out(d).astype(np.float32))
+    e, F = pc.sum_layer_bwd(th, x, out_in, _dev(d["f"]), child_stride=cs, precision=mode)
     torch.cuda.synchronize()
     pc.device_status()
     return out.cpu().numpy(), e.cpu().numpy(), F.cpu().numpy()
 
 
+def _oracle_out(d):
+    return sum_layer_fwd(d["theta"].astype(np.float64), d["x"].astype(np.float64), d["child_stride"])
+
+
 def _ref(d):
     th, x = d["theta"].astype(np.float64), d["x"].astype(np.float64)
-    out = sum_layer_fwd(th, x, d["child_stride"])
-    e, F = sum_layer_bwd(th, x, d["child_stride"], out, d["f"].astype(np.float64))
+    out = _oracle_out(d)
+    out32 = out.astype(np.float32).astype(np.float64)        # what the GPU backward receives
+    e, F = sum_layer_bwd(th, x, d["child_stride"], out32, d["f"].astype(np.float64))
     return out, e, F
 
 
@@ -50,7 +57,7 @@ def layer_case():
 def test_single_layer_workload(layer_case, mode):
     d, (ro, re, rF) = layer_case
     out, e, F = _run(d, mode)
-    eo, ee, eF = ll_err(out, ro), flow_err(e, re), flow_err(F, rF)
+    eo, ee, eF = out_err(out, ro), flow_err(e, re), flow_err(F, rF)
     print(f"layer {mode}: out {eo:.3e}  e {ee:.3e}  F {eF:.3e}")
     assert eo <= LL_TOL[mode]
     assert ee <= FLOW_TOL[mode]
@@ -63,7 +70,7 @@ def test_grouped_ragged(mode):
     d = layer_inputs(3, 200, 150, 77, seed=60, child_stride=160, x_scale=5.0, f_kind="uniform")
     ro, re, rF = _ref(d)
     out, e, F = _run(d, mode)
-    assert ll_err(out, ro) <= LL_TOL[mode]
+    assert out_err(out, ro) <= LL_TOL[mode]
     assert flow_err(e, re) <= FLOW_TOL[mode]
     assert flow_err(F, rF) <= FLOW_TOL[mode]
     # rows between the groups are nobody's children: untouched (zero)
@@ -75,7 +82,7 @@ def test_tiny_and_single_sample():
         d = layer_inputs(G, M, N, B, seed=61, f_kind="uniform")
         ro, re, rF = _ref(d)
         out, e, F = _run(d, "fp32")
-        assert ll_err(out, ro) <= 1e-5
+        assert out_err(out, ro) <= 1e-5
         assert flow_err(e, re) <= 1e-5 and flow_err(F, rF) <= 1e-5
 
 
@@ -92,7 +99,7 @@ def test_edge_cases_fp32():
     ro, re, rF = _ref(d)
     out, e, F = _run(d, "fp32")
     assert np.all(np.isneginf(out[0, :, 5])) and np.all(np.isneginf(out[0, 11]))
-    assert ll_err(out, ro) <= 1e-5
+    assert out_err(out, ro) <= 1e-5
     assert np.all(np.isfinite(e)) and np.all(np.isfinite(F))
     assert flow_err(e, re) <= 1e-5 and flow_err(F, rF) <= 1e-5
     assert np.all(e[:70, 5] == 0) and e[3, 7] == 0 and np.all(F[0, 11] == 0)
@@ -119,7 +126,7 @@ def test_tf32_downgrade_fails_the_fp32_bar(layer_case):
     # Tests: downgrading either flow kernel's dots to TF32 fails the fp32 test)
     d, (ro, re, rF) = layer_case
     out, e, F = _run(d, "tf32")
-    assert ll_err(out, ro) > LL_TOL["fp32"]
+    assert out_err(out, ro) > LL_TOL["fp32"]
     assert flow_err(e, re) > FLOW_TOL["fp32"]
     assert flow_err(F, rF) > FLOW_TOL["fp32"]
 

@@ -24,6 +24,20 @@ def ll_err(gpu, ref):
     return float(d.max()) if d.size else 0.0
 
 
+def out_err(gpu, ref):
+    """ll_err for a float32 output array: the error beyond the float32 representation
+    of the exact value (|fl32(ref) - ref|, up to half an ulp), which no float32
+    result can avoid (at |out| = 1000 that alone is 3e-5)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if np.any(np.isneginf(gpu) != np.isneginf(ref)):
+        return np.inf
+    fin = np.isfinite(ref)
+    rep = np.abs(ref[fin].astype(np.float32).astype(np.float64) - ref[fin])
+    d = np.maximum(np.abs(gpu[fin] - ref[fin]) - rep, 0.0)
+    return float(d.max()) if d.size else 0.0
+
+
 def flow_err(gpu, ref):
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
