@@ -162,6 +162,111 @@ __global__ void k_hmm_leaf(int H, int B, int T, const int* __restrict__ tokens,
   }
 }
 
+// ---------------------------------------------------------- token buckets
+// count[v] = number of (position, sample) pairs with token v (tokens outside [0, V)
+// are ignored).
+__global__ void k_token_hist(const int* __restrict__ tokens, int n, int V, int* __restrict__ count) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const int v = tokens[i];
+    if (v >= 0 && v < V) atomicAdd(&count[v], 1);
+  }
+}
+
+// offset[v] = sum_{u < v} count[u] for v = 0..V, one block of 1024 threads.
+__global__ void k_exclusive_scan(const int* __restrict__ count, int V, int* __restrict__ offset) {
+  __shared__ int part[1024];
+  const int per = (V + 1023) / 1024;
+  const int lo = threadIdx.x * per;
+  int local = 0;
+  for (int i = lo; i < lo + per && i < V; ++i) local += count[i];
+  part[threadIdx.x] = local;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {
+    const int add = threadIdx.x >= d ? part[threadIdx.x - d] : 0;
+    __syncthreads();
+    part[threadIdx.x] += add;
+    __syncthreads();
+  }
+  int run = part[threadIdx.x] - local;  // exclusive prefix of this thread's range
+  for (int i = lo; i < lo + per && i < V; ++i) {
+    offset[i] = run;
+    run += count[i];
+  }
+  if (threadIdx.x == 1023) offset[V] = part[1023];
+}
+
+// order[offset[v] ..] = the batch-major flow rows t*B + b of every pair with token v,
+// in increasing token-array index b*T + t: a stable, deterministic bucketing (one
+// block per token value scans the whole token array).
+__global__ void k_token_bucket(const int* __restrict__ tokens, int T, int B, const int* __restrict__ offset,
+                               int* __restrict__ order) {
+  __shared__ int warp_n[8];
+  const int v = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = T * B;
+  int base = offset[v];
+  for (int i0 = 0; i0 < n; i0 += 256) {
+    const int i = i0 + threadIdx.x;
+    const bool match = i < n && tokens[i] == v;
+    const unsigned bal = __ballot_sync(0xffffffffu, match);
+    if (lane == 0) warp_n[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      before += w < warp ? warp_n[w] : 0;
+      total += warp_n[w];
+    }
+    if (match) {
+      const int b = i / T, t = i - b * T;
+      order[base + before + __popc(bal & ((1u << lane) - 1u))] = t * B + b;
+    }
+    base += total;
+    __syncthreads();
+  }
+}
+
+// dEt[v][k] = sum over the pairs of bucket v (in bucket order) of the flows f[row][k].
+__global__ void k_dE_gather(const float* __restrict__ fbm, int H, const int* __restrict__ offset,
+                            const int* __restrict__ order, float* __restrict__ dEt) {
+  const int v = blockIdx.x;
+  const int k = blockIdx.y * blockDim.x + threadIdx.x;
+  if (k >= H) return;
+  float acc = 0.f;
+  const int e1 = offset[v + 1];
+  for (int e = offset[v]; e < e1; ++e) acc += fbm[static_cast<long long>(order[e]) * H + k];
+  dEt[static_cast<long long>(v) * H + k] = acc;
+}
+
+// Stages the CTA's emission block Es[c][r] = E[m0 + r, x_{t,b}] (b = n0 + c) into shared
+// memory: rows and columns outside the problem read 0. The epilogue warps do this
+// while the contraction's K loop runs, so the gathers are off the critical path.
+// Each warp owns 32 columns and issues 8 columns x 4 rows of loads per batch.
+__device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, int H, int B, int m0, int n0,
+                                                const int* tok_s, float* Es, int et) {
+  const int lane = et & 31;
+  const int c_begin = (et >> 5) * 32;
+#pragma unroll 1
+  for (int cb = c_begin; cb < c_begin + 32; cb += 8) {
+    float vals[8][4];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const bool bin = n0 + cb + c < B;
+      const float* src = Et + static_cast<long long>(tok_s[cb + c]) * H + m0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        vals[c][i] = (bin && m0 + r < H) ? src[r] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) Es[(cb + c) * kBM + lane + 32 * i] = vals[c][i];
+  }
+}
+
 // ----------------------------------------------------------- forward epilogue
 template <int P>
 struct EpiHmmFwd {
@@ -182,7 +287,10 @@ struct EpiHmmFwd {
     size_t un_lo;
     float* U0;               // u_0 float32 [B][H] (t = 0 only)
   };
-  static constexpr int kSmemBytes = kChainBN * 4 * 2 + 4 * kChainBN * 4;
+  static constexpr bool kTranspose = false;
+  // the 3xTF32 ring needs the room: it gathers emissions directly instead
+  static constexpr bool kStageE = P != kTF32x3;
+  static constexpr int kSmemBytes = kChainBN * 4 * 2 + (kStageE ? kChainBN * kBM * 4 : 0);
 
   __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
@@ -200,46 +308,52 @@ struct EpiHmmFwd {
       tok_s[c] = tok;
       c_s[c] = cv;
     }
+    if constexpr (kStageE) {
+      epilogue_bar_sync();
+      stage_emissions(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
+    }
   }
 
+  // Thread = state k (TMEM lane), registers = 32 consecutive samples.
   __device__ static void apply(const Params& p, int, int m0, int n0, int row, int col0,
-                               float (&v)[32], uint8_t* smem) {
+                               float (&v)[32], uint8_t* smem, float*) {
     const int* tok_s = reinterpret_cast<const int*>(smem);
     const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
-    float* red = reinterpret_cast<float*>(smem) + 2 * kChainBN;
+    const float* Es = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
     const int k = m0 + row;
     const bool kin = k < p.H;
     const int nvalid = kin ? min(32, p.B - (n0 + col0)) : 0;
+    float e[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const int lc = col0 + c;
-      const int b = n0 + lc;
-      float u = 0.f;
-      if (c < nvalid) {
-        u = p.Et[static_cast<long long>(tok_s[lc]) * p.H + k] * v[c] * c_s[lc];
-        if (p.ubm) store_operand<P>(p.ubm, static_cast<size_t>(b * p.ubm_ld + k), p.ubm_lo, u);
-        if (p.U0) p.U0[static_cast<long long>(b) * p.H + k] = u;
-      }
-      v[c] = u;
+      if constexpr (kStageE)
+        e[c] = Es[(col0 + c) * kBM + row];
+      else
+        e[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + k] : 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * v[c] * c_s[col0 + c] : 0.f;
+    if (p.ubm) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid)
+          store_operand<P>(p.ubm, static_cast<size_t>((n0 + col0 + c) * p.ubm_ld + k), p.ubm_lo, v[c]);
+    }
+    if (p.U0) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) p.U0[static_cast<long long>(n0 + col0 + c) * p.H + k] = v[c];
     }
     if (p.un && nvalid > 0)
       store_operand_run<P>(p.un, static_cast<size_t>(k * p.un_ld + static_cast<long long>(p.t - 1) * p.B + n0 + col0),
                            p.un_lo, v, nvalid);
+    // column maxima: lane l ends with the warp's maximum of column col0 + l
     const float mx = warp_transpose_max(v);
-    const int q = (threadIdx.x >> 5) & 3;
-    red[q * kChainBN + col0 + (threadIdx.x & 31)] = mx;
+    const int b = n0 + col0 + (threadIdx.x & 31);
+    if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
   }
 
-  __device__ static void finish(const Params& p, int, int, int n0, int et, uint8_t* smem) {
-    const float* red = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
-    for (int c = et; c < kChainBN; c += 128) {
-      const int b = n0 + c;
-      if (b < p.B) {
-        const float m = fmaxf(fmaxf(red[c], red[kChainBN + c]), fmaxf(red[2 * kChainBN + c], red[3 * kChainBN + c]));
-        atomic_max_nonneg(&p.umax_cur[b], m);
-      }
-    }
-  }
+  __device__ static void finish(const Params&, int, int, int, int, uint8_t*) {}
 };
 
 // ------------------------------------------------------------------- root
@@ -264,14 +378,14 @@ __global__ void k_hmm_root(int H, int B, int T, const float* __restrict__ pi, co
   }
 }
 
-// Root flows: f_0 = pi u_0 r, w_0 = pi r E[., x_0] c_0; dE and dpi contributions.
+// Root flows: f_0 = pi u_0 r (stored batch-major for dE), w_0 = pi r E[., x_0] c_0; dpi.
 template <int P>
 __global__ void k_hmm_root_flows(int H, int B, int T, const int* __restrict__ tokens,
                                  const float* __restrict__ pi, const float* __restrict__ U0,
                                  const float* __restrict__ Et, const float* __restrict__ cf,
                                  const float* __restrict__ rroot, void* wbm, long long wbm_ld,
                                  size_t wbm_lo, void* wn, long long wn_ld, size_t wn_lo,
-                                 float* dEt, float* dpi) {
+                                 float* fbm, float* dpi) {
   __shared__ float tile[32][33];
   __shared__ float fsum[8][32];
   const int k0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
@@ -287,7 +401,7 @@ __global__ void k_hmm_root_flows(int H, int B, int T, const int* __restrict__ to
       const float f = pk * U0[static_cast<long long>(b) * H + k] * r;
       w = pk * r * Et[static_cast<long long>(tok) * H + k] * cf[b];
       facc += f;
-      if (dEt) atomicAdd(&dEt[static_cast<long long>(tok) * H + k], f);
+      if (fbm) fbm[static_cast<long long>(b) * H + k] = f;
       if (wbm) store_operand<P>(wbm, static_cast<size_t>(b * wbm_ld + k), wbm_lo, w);
     }
     tile[i][threadIdx.x] = w;
@@ -317,7 +431,7 @@ struct EpiHmmBwd : EpiNoHooks {
     const void* un;          // u_{t+1} node-major at column t B
     long long un_ld;
     size_t un_lo;
-    float* dEt;              // [V][H] or NULL
+    float* fbm;              // flows f_{t+1} batch-major [B][H] for dE, or NULL
     void* wbm;               // w_{t+1} batch-major for the next step (NULL at the end)
     long long wbm_ld;
     size_t wbm_lo;
@@ -325,9 +439,10 @@ struct EpiHmmBwd : EpiNoHooks {
     long long wn_ld;
     size_t wn_lo;
   };
-  static constexpr int kSmemBytes = kChainBN * 8;
+  static constexpr bool kStageE = P != kTF32x3;
+  static constexpr int kSmemBytes = kChainBN * 8 + (kStageE ? kChainBN * kBM * 4 : 0);
 
-  __device__ static void prepare(const Params& p, int, int, int n0, int et, uint8_t* smem) {
+  __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
     float* c_s = reinterpret_cast<float*>(smem) + kChainBN;
     for (int c = et; c < kChainBN; c += 128) {
@@ -335,33 +450,48 @@ struct EpiHmmBwd : EpiNoHooks {
       tok_s[c] = b < p.B ? p.tokens[static_cast<long long>(b) * p.T + p.t + 1] : 0;
       c_s[c] = b < p.B ? p.cf[static_cast<long long>(p.t + 1) * p.B + b] : 0.f;
     }
+    if constexpr (kStageE) {
+      if (p.wbm) {
+        epilogue_bar_sync();
+        stage_emissions(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
+      }
+    }
   }
 
+  // Thread = state j, registers = 32 consecutive samples; the u_{t+1} run is loaded
+  // before the first atomic or store.
   __device__ static void apply(const Params& p, int, int m0, int n0, int row, int col0,
-                               float (&v)[32], uint8_t* smem) {
+                               float (&v)[32], uint8_t* smem, float*) {
     const int* tok_s = reinterpret_cast<const int*>(smem);
     const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
+    const float* Es = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
     const int j = m0 + row;
     if (j >= p.H) return;
     const int nvalid = min(32, p.B - (n0 + col0));
     if (nvalid <= 0) return;
-    if (p.dEt) {
-      float u[32];
+    float u[32], e[32];
+    if (p.fbm)
       load_operand_run<P>(p.un, static_cast<size_t>(j * p.un_ld + static_cast<long long>(p.t) * p.B + n0 + col0),
                           p.un_lo, u, nvalid);
+    if (p.wbm) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        if constexpr (kStageE)
+          e[c] = Es[(col0 + c) * kBM + row];
+        else
+          e[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + j] : 0.f;
+      }
+    }
+    if (p.fbm) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
-        if (c < nvalid) atomicAdd(&p.dEt[static_cast<long long>(tok_s[col0 + c]) * p.H + j], u[c] * v[c]);
+        if (c < nvalid) p.fbm[static_cast<long long>(n0 + col0 + c) * p.H + j] = u[c] * v[c];
     }
     if (!p.wbm) return;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const int lc = col0 + c;
-      float w = 0.f;
-      if (c < nvalid) {
-        w = p.Et[static_cast<long long>(tok_s[lc]) * p.H + j] * c_s[lc] * v[c];
-        store_operand<P>(p.wbm, static_cast<size_t>((n0 + lc) * p.wbm_ld + j), p.wbm_lo, w);
-      }
+      const float w = c < nvalid ? e[c] * c_s[col0 + c] * v[c] : 0.f;
+      if (c < nvalid) store_operand<P>(p.wbm, static_cast<size_t>((n0 + col0 + c) * p.wbm_ld + j), p.wbm_lo, w);
       v[c] = w;
     }
     if (p.wn)
@@ -373,7 +503,8 @@ struct EpiHmmBwd : EpiNoHooks {
 // -------------------------------------------------------------- workspace
 struct HmmWs {
   Operand Aop, Atop, ubm[2], wbm[2], un, wn;
-  float *Et, *rs, *emax, *emax_rs, *U0, *umax, *cf, *rroot, *dEt;
+  float *Et, *rs, *emax, *emax_rs, *U0, *umax, *cf, *rroot, *dEt, *fbm;
+  int *tok_count, *tok_offset, *tok_order;
   double* logc;
 };
 
@@ -400,7 +531,13 @@ size_t carve_hmm(void* base, pc_precision_t p, int H, int T, int V, int B, bool 
     w->un = c.operand(p, 1, H, static_cast<long long>(T - 1) * B);
     w->wn = c.operand(p, 1, H, static_cast<long long>(T - 1) * B);
   }
-  if (flows && want_dE) w->dEt = static_cast<float*>(c.take(size_t(V) * H * 4));
+  if (flows && want_dE) {
+    w->dEt = static_cast<float*>(c.take(size_t(V) * H * 4));
+    w->fbm = static_cast<float*>(c.take(size_t(T) * B * H * 4));
+    w->tok_count = static_cast<int*>(c.take(size_t(V + 1) * 4));
+    w->tok_offset = static_cast<int*>(c.take(size_t(V + 1) * 4));
+    w->tok_order = static_cast<int*>(c.take(size_t(T) * B * 4));
+  }
   return c.used;
 }
 
@@ -431,7 +568,16 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   pc_status_t st;
 
   PC_CUDA(cudaMemsetAsync(w.umax, 0, size_t(T) * B * 4, s));
-  if (w.dEt) PC_CUDA(cudaMemsetAsync(w.dEt, 0, size_t(V) * H * 4, s));
+  if (w.dEt) {
+    // token buckets of every (position, sample): dE is then a per-token gather-sum
+    PC_CUDA(cudaMemsetAsync(w.tok_count, 0, size_t(V + 1) * 4, s));
+    k_token_hist<<<cdiv(static_cast<long long>(T) * B, 256), 256, 0, s>>>(tokens, T * B, V, w.tok_count);
+    PC_LAUNCH_CHECK();
+    k_exclusive_scan<<<1, 1024, 0, s>>>(w.tok_count, V, w.tok_offset);
+    PC_LAUNCH_CHECK();
+    k_token_bucket<<<V, 256, 0, s>>>(tokens, T, B, w.tok_offset, w.tok_order);
+    PC_LAUNCH_CHECK();
+  }
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dA && !accumulate && T < 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
 
@@ -491,7 +637,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
 
   k_hmm_root_flows<P><<<dim3(cdiv(H, 32), cdiv(B, 32)), dim3(32, 8), 0, s>>>(
       H, B, T, tokens, pi, w.U0, w.Et, w.cf, w.rroot, chain ? w.wbm[0].ptr : nullptr, w.wbm[0].ld,
-      w.wbm[0].lo_elems, (chain && dA) ? w.wn.ptr : nullptr, w.wn.ld, w.wn.lo_elems, w.dEt, dpi);
+      w.wbm[0].lo_elems, (chain && dA) ? w.wn.ptr : nullptr, w.wn.ld, w.wn.lo_elems, w.fbm, dpi);
   PC_LAUNCH_CHECK();
 
   if (chain) {
@@ -506,7 +652,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       ep.H = H; ep.B = B; ep.T = T; ep.t = t;
       ep.tokens = tokens; ep.Et = w.Et; ep.cf = w.cf;
       ep.un = w.un.ptr; ep.un_ld = w.un.ld; ep.un_lo = w.un.lo_elems;
-      ep.dEt = w.dEt;
+      ep.fbm = w.fbm ? w.fbm + static_cast<long long>(t + 1) * B * H : nullptr;
       if (t + 1 <= T - 2) {
         const Operand& nb = w.wbm[(t + 1) & 1];
         ep.wbm = nb.ptr; ep.wbm_ld = nb.ld; ep.wbm_lo = nb.lo_elems;
@@ -532,6 +678,8 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
     PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
   }
   if (dE) {
+    k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
+    PC_LAUNCH_CHECK();
     k_transpose_add_f32<<<dim3(cdiv(H, 32), cdiv(V, 32)), dim3(32, 8), 0, s>>>(w.dEt, V, H, dE, accumulate);
     PC_LAUNCH_CHECK();
   }

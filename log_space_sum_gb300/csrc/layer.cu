@@ -104,30 +104,33 @@ pc_status_t make_operands(const Src& src, int G, int R, int B, const Operand* nm
 
 // ----------------------------------------------------------------- epilogues
 struct EpiLayerFwd : EpiNoHooks {
+  static constexpr bool kTranspose = true;
   struct Params {
     float* out;
     const float* colmax;
     int M, B;
   };
+  // Transposed: lane l owns sample column b = n0 + col0 + l of the warp's 32 node rows,
+  // so each store instruction writes one contiguous row segment of out.
   __device__ static void apply(const Params& p, int g, int m0, int n0, int row, int col0,
-                               float (&v)[32], uint8_t*) {
-    const int i = m0 + row;
-    if (i >= p.M) return;
-    float* o = p.out + (static_cast<long long>(g) * p.M + i) * p.B;
-    const float* cm = p.colmax + static_cast<long long>(g) * p.B;
-    const int bb = n0 + col0;
+                               float (&v)[32], uint8_t*, float* tbuf) {
+    float w[32];
+    warp_transpose32(v, w, tbuf);
+    const int lane = threadIdx.x & 31;
+    const int i0 = m0 + row - lane;
+    const int b = n0 + col0 + lane;
+    if (b >= p.B) return;
+    const float m = p.colmax[static_cast<long long>(g) * p.B + b];
+    float* o = p.out + (static_cast<long long>(g) * p.M + i0) * p.B + b;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int b = bb + c;
-      if (b < p.B) {
-        const float m = cm[b];
-        o[b] = (m > -INFINITY && v[c] > 0.f) ? m + logf(v[c]) : -INFINITY;
-      }
-    }
+    for (int r = 0; r < 32; ++r)
+      if (i0 + r < p.M)
+        o[static_cast<long long>(r) * p.B] = (m > -INFINITY && w[r] > 0.f) ? m + logf(w[r]) : -INFINITY;
   }
 };
 
 struct EpiLayerElem : EpiNoHooks {
+  static constexpr bool kTranspose = true;
   struct Params {
     float* e;
     const float* x;
@@ -135,23 +138,36 @@ struct EpiLayerElem : EpiNoHooks {
     long long cs;
     int N, B, accumulate;
   };
+  // Transposed like EpiLayerFwd; x (and e when accumulating) are loaded for the whole
+  // chunk before the first store.
   __device__ static void apply(const Params& p, int g, int m0, int n0, int row, int col0,
-                               float (&v)[32], uint8_t*) {
-    const int j = m0 + row;
-    if (j >= p.N) return;
-    const long long r = static_cast<long long>(g) * p.cs + j;
-    const float* xr = p.x + r * p.B;
-    float* er = p.e + r * p.B;
-    const float* cm = p.colmax + static_cast<long long>(g) * p.B;
-    const int bb = n0 + col0;
+                               float (&v)[32], uint8_t*, float* tbuf) {
+    float w[32];
+    warp_transpose32(v, w, tbuf);
+    const int lane = threadIdx.x & 31;
+    const int j0 = m0 + row - lane;
+    const int b = n0 + col0 + lane;
+    if (b >= p.B) return;
+    const float m = p.colmax[static_cast<long long>(g) * p.B + b];
+    const long long ld = p.B;
+    const long long base = (static_cast<long long>(g) * p.cs + j0) * ld + b;
+    const float* xp = p.x + base;
+    float* ep = p.e + base;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int b = bb + c;
-      if (b < p.B) {
-        const float m = cm[b];
-        const float u = (m > -INFINITY) ? expf(xr[b] - m) : 0.f;
-        const float val = u * v[c];
-        er[b] = p.accumulate ? er[b] + val : val;
+    for (int h = 0; h < 32; h += 16) {
+      float xv[16], ev[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const bool in = j0 + h + r < p.N;
+        xv[r] = in ? xp[(h + r) * ld] : -INFINITY;
+        ev[r] = (in && p.accumulate) ? ep[(h + r) * ld] : 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        if (j0 + h + r < p.N) {
+          const float u = (m > -INFINITY) ? expf(xv[r] - m) : 0.f;
+          ep[(h + r) * ld] = ev[r] + u * w[h + r];
+        }
       }
     }
   }

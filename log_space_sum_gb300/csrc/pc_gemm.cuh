@@ -33,20 +33,45 @@ struct GemmShape {
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
   static constexpr uint32_t kStageBytes = kParts * (kABytes + kBBytes);
-  static constexpr int kMaxStages = 8;
-  static constexpr int kStages =
-      (200 * 1024 / kStageBytes) < kMaxStages ? (200 * 1024 / kStageBytes) : kMaxStages;
   static constexpr uint32_t kUmmaK = (P == kBF16) ? 16 : 8;  // K per MMA instruction
   static constexpr uint32_t kKSteps = kBK / kUmmaK;          // MMAs per ring slot (4)
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-  static_assert(kStages >= 2, "stages");
+};
+
+// Per epilogue warp: a padded 32 x 33 float tile for warp_transpose32.
+constexpr int kTBufFloats = 32 * 33;
+
+constexpr size_t kSmemPerCta = 232448;  // opt-in maximum dynamic shared memory per CTA
+
+// Shared-memory plan of one instantiation: the ring gets what the epilogue leaves.
+template <int P, int BN, class Epi>
+struct GemmPlan {
+  using S = GemmShape<P, BN>;
+  static constexpr size_t kTBufBytes = Epi::kTranspose ? 4 * kTBufFloats * sizeof(float) : 0;
+  static constexpr size_t kEpiBytes = ((Epi::kSmemBytes + 15) / 16) * 16;
+  static constexpr size_t kFixed = 1024 /* alignment slack */ + 256 /* barriers */ + kTBufBytes + kEpiBytes;
+  static constexpr int kFit = static_cast<int>((kSmemPerCta - kFixed) / S::kStageBytes);
+  static constexpr int kStages = kFit < 8 ? kFit : 8;
+  static constexpr size_t kBytes = kFixed + size_t(kStages) * S::kStageBytes;
+  static_assert(kStages >= 2, "the epilogue leaves room for fewer than two ring slots");
 };
 
 template <int P, int BN, class Epi>
 constexpr size_t gemm_smem_bytes() {
-  using S = GemmShape<P, BN>;
-  return 1024 /* alignment slack */ + size_t(S::kStages) * S::kStageBytes + 256 /* barriers */ +
-         Epi::kSmemBytes;
+  return GemmPlan<P, BN, Epi>::kBytes;
+}
+
+// The warp holds a 32 x 32 tile one row per lane (v[c] = tile[lane][c]); returns it one
+// column per lane (w[r] = tile[r][lane]) through the warp's padded shared buffer, so
+// that row-major global data can then be read and written a whole row per instruction.
+__device__ __forceinline__ void warp_transpose32(const float (&v)[32], float (&w)[32], float* buf) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) buf[lane * 33 + c] = v[c];
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 32; ++r) w[r] = buf[r * 33 + lane];
+  __syncwarp();
 }
 
 __device__ __forceinline__ void epilogue_bar_sync() {
@@ -73,7 +98,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
                 int num_kb, unsigned* status, const typename Epi::Params ep) {
   using S = GemmShape<P, BN>;
-  constexpr int kStages = S::kStages;
+  constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
   // TF32 modes: every K slice (kSliceKB ring slots) is accumulated from zero in one
   // of two TMEM buffers and added into registers by the epilogue with round-to-
   // nearest adds. The tensor-core accumulator truncates on every accumulation, so
@@ -91,7 +116,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* acc_full = empty + kStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;    // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  uint8_t* epi_smem = smem + kStages * S::kStageBytes + 256;
+  float* tbuf_base = reinterpret_cast<float*>(smem + kStages * S::kStageBytes + 256);
+  uint8_t* epi_smem = reinterpret_cast<uint8_t*>(tbuf_base) + GemmPlan<P, BN, Epi>::kTBufBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -214,6 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     epilogue_bar_sync();
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    float* tbuf = Epi::kTranspose ? tbuf_base + q * kTBufFloats : nullptr;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     bool ok = true;
     if constexpr (kSliced) {
@@ -242,7 +269,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) Epi::apply(ep, g, m0, n0, row, c * 32, acc[c], epi_smem);
+        for (int c = 0; c < BN / 32; ++c) Epi::apply(ep, g, m0, n0, row, c * 32, acc[c], epi_smem, tbuf);
       }
     } else {
       ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue));
@@ -252,7 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld_32x32(lane_base + static_cast<uint32_t>(c), v);
-          Epi::apply(ep, g, m0, n0, row, c, v, epi_smem);
+          Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
         }
       }
     }
@@ -270,6 +297,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Default hooks for epilogues that need no per-CTA set-up or reduction.
 struct EpiNoHooks {
   static constexpr int kSmemBytes = 0;
+  static constexpr bool kTranspose = false;  // true: apply() uses warp_transpose32
   template <class Params>
   __device__ static void prepare(const Params&, int, int, int, int, uint8_t*) {}
   template <class Params>

@@ -118,26 +118,39 @@ pc_status_t transpose_to_operand(const float* src, long long src_ld, long long s
 
 // Shared with the circuits: F[g][i][j] (+)= theta[g][i][j] * D[i,j].
 struct EpiThetaScale : EpiNoHooks {
+  static constexpr bool kTranspose = true;
   struct Params {
     float* F;
     const float* theta;
     int M, N, accumulate;
   };
+  // Transposed so that lane l owns column col0 + l of the warp's 32 rows: every theta
+  // load and F store of the warp covers one contiguous row segment. All loads of the
+  // chunk are issued before the first store.
   __device__ static void apply(const Params& p, int g, int m0, int n0, int row, int col0,
-                               float (&v)[32], uint8_t*) {
-    const int i = m0 + row;
-    if (i >= p.M) return;
-    const long long base = (static_cast<long long>(g) * p.M + i) * p.N;
-    const int jj = n0 + col0;
-    const float* t = p.theta + base;
-    float* F = p.F + base;
+                               float (&v)[32], uint8_t*, float* tbuf) {
+    float w[32];
+    warp_transpose32(v, w, tbuf);
+    const int lane = threadIdx.x & 31;
+    const int i0 = m0 + row - lane;
+    const int j = n0 + col0 + lane;
+    if (j >= p.N) return;
+    const long long ld = p.N;
+    const float* tp = p.theta + (static_cast<long long>(g) * p.M + i0) * ld + j;
+    float* Fp = p.F + (static_cast<long long>(g) * p.M + i0) * ld + j;
+    // two halves of 16 rows keep the loads-before-stores batch within the register budget
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int j = jj + c;
-      if (j < p.N) {
-        const float val = t[j] * v[c];
-        F[j] = p.accumulate ? F[j] + val : val;
+    for (int h = 0; h < 32; h += 16) {
+      float t[16], f[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const bool in = i0 + h + r < p.M;
+        t[r] = in ? tp[(h + r) * ld] : 0.f;
+        f[r] = (in && p.accumulate) ? Fp[(h + r) * ld] : 0.f;
       }
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (i0 + h + r < p.M) Fp[(h + r) * ld] = f[r] + t[r] * w[h + r];
     }
   }
 };
