@@ -140,6 +140,25 @@ PCSUM_API pc_status_t pc_sum_layer_bwd(int G, int M, int N, int B, const float* 
                              float* e, float* F, int accumulate, pc_precision_t prec,
                              void* ws, size_t ws_bytes, pc_stream_t stream);
 
+/* pc_sum_layer_fwd for callers that cannot allocate device memory. The pages have no
+ * counterpart to this entry point; it exists because some callers can neither call
+ * cudaMalloc nor hand over a workspace: a plugin whose host framework owns all device
+ * memory and exposes no allocator, or a hot path where an allocation (and the
+ * synchronisation it brings) is not allowed. Same arguments and results as
+ * pc_sum_layer_fwd, without ws / ws_bytes: the scratch is a 16 MiB array built into
+ * the library, held on every GPU that loads it until the process exits.
+ *   - Requests whose scratch (pc_sum_layer_workspace) exceeds 16 MiB return
+ *     PC_ERR_UNSUPPORTED with the sizes in pc_last_error(); nothing is launched.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call uses the same array: calls that may overlap on the GPU (different
+ *     streams, concurrent graph launches) race and must be serialised by the caller.
+ *     Nothing in the array needs to start at zero; each call writes what it reads. */
+PCSUM_API pc_status_t pc_sum_layer_fwd_noalloc(int G, int M, int N, int B, const float* theta,
+                                               const float* x, long long child_stride, float* out,
+                                               pc_precision_t prec, pc_stream_t stream);
+
 /* ------------------------------------------------------------------------------
  * Whole HMM circuit, forward + backward (pyjuice PR #62, Results table "HMM, 4096
  * latents, 32 positions"; Summary 2, first bullet: its layers share their children).

@@ -39,6 +39,7 @@ SIGNATURES = {
     "pc_sum_layer_workspace": [_i, _i, _i, _i, _i, _p],
     "pc_sum_layer_fwd": [_i, _i, _i, _i, _p, _p, _ll, _p, _i, _p, _sz, _p],
     "pc_sum_layer_bwd": [_i, _i, _i, _i, _p, _p, _ll, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
+    "pc_sum_layer_fwd_noalloc": [_i, _i, _i, _i, _p, _p, _ll, _p, _i, _p],
     "pc_hmm_workspace": [_i, _i, _i, _i, _i, _p],
     "pc_hmm_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
 }

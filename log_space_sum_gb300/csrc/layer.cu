@@ -11,6 +11,7 @@
 //        parameter  D[i,j] = sum_b w[i,b] u[j,b]
 //                   F      = theta * D
 #include <cmath>
+#include <mutex>
 
 #include "pc_launch.cuh"
 
@@ -338,6 +339,70 @@ pc_status_t pc_sum_layer_bwd(int G, int M, int N, int B, const float* theta, con
       return pc::layer_bwd<pc::kTF32>(G, M, N, B, theta, x, child_stride, out, f, e, F, accumulate, prec, ws, s);
     default:
       return pc::layer_bwd<pc::kTF32x3>(G, M, N, B, theta, x, child_stride, out, f, e, F, accumulate, prec, ws, s);
+  }
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// Forward without a caller workspace. Some callers cannot allocate device memory at
+// all: a plugin whose host framework owns every device allocation and hands it no
+// allocator, or a hot path where cudaMalloc (and the synchronisation it implies) is
+// not allowed. For them the scratch lives in this file-scope device array, which every
+// GPU that loads the library holds until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device
+// (host code may not use the symbol itself: it is only a host-side stand-in).
+pc_status_t noalloc_scratch(void** ptr) {
+  int dev = 0;
+  PC_CUDA(cudaGetDevice(&dev));
+  PC_CHECK(dev >= 0 && dev < 64, PC_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return pc::set_error(PC_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed: %s",
+                           cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return PC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pc_status_t pc_sum_layer_fwd_noalloc(int G, int M, int N, int B, const float* theta, const float* x,
+                                     long long child_stride, float* out, pc_precision_t prec,
+                                     pc_stream_t stream) {
+  pc::clear_error();
+  pc_status_t st;
+  if ((st = pc::check_precision(prec)) != PC_OK) return st;
+  if ((st = pc::check_layer_shape(G, M, N, B, child_stride)) != PC_OK) return st;
+  PC_CHECK(theta && x && out, PC_ERR_NULL, "theta, x and out must not be NULL");
+  const size_t need = pc::layer_ws_bytes(prec, G, M, N, B);
+  PC_CHECK(need <= kNoAllocScratchBytes, PC_ERR_UNSUPPORTED,
+           "this layer needs %zu bytes of scratch but the built-in scratch holds %zu; call "
+           "pc_sum_layer_fwd with a workspace instead",
+           need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws)) != PC_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Every value the forward reads from the scratch is written earlier in the same call,
+  // so nothing has to be cleared between calls.
+  switch (prec) {
+    case PC_PREC_AUTO: return pc::layer_fwd<pc::kBF16>(G, M, N, B, theta, x, child_stride, out, prec, ws, s);
+    case PC_PREC_TF32: return pc::layer_fwd<pc::kTF32>(G, M, N, B, theta, x, child_stride, out, prec, ws, s);
+    default: return pc::layer_fwd<pc::kTF32x3>(G, M, N, B, theta, x, child_stride, out, prec, ws, s);
   }
 }
 
