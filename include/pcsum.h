@@ -125,7 +125,7 @@ PCSUM_API pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long lon
  *   e     like x      element flows; rows outside every group are not touched.
  *                     NULL = not computed.
  *   F     [G][M][N]   parameter flows. NULL = not computed.
- * Limits: 1 <= G, M, N, B; M, N < 2^24; B < 2^24; x and the arrays above hold at
+ * Limits: 1 <= G <= 65535; 1 <= M, N, B < 2^24; x and the arrays above hold at
  * most 2^31 rows. Scratch: pc_sum_layer_workspace (covers both directions).
  * ---------------------------------------------------------------------------- */
 PCSUM_API pc_status_t pc_sum_layer_workspace(int G, int M, int N, int B, pc_precision_t prec,

@@ -73,15 +73,24 @@ __global__ void k_transpose_add_f32(const float* __restrict__ src, int R, int C,
   }
 }
 
-// rs[k] = sum_l A[k,l], one warp per row.
+// rs[k] = sum_l A[k,l], one warp per row (float: it only feeds an upper bound).
 __global__ void k_rowsum(const float* __restrict__ A, int H, float* __restrict__ rs) {
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (row >= H) return;
   const float* a = A + static_cast<long long>(row) * H;
-  double s = 0.0;
-  for (int l = threadIdx.x & 31; l < H; l += 32) s += a[l];
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  if ((H & 3) == 0 && (reinterpret_cast<uintptr_t>(a) & 15) == 0) {
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    for (int l = lane; l < H / 4; l += 32) {
+      const float4 v = a4[l];
+      s += (v.x + v.y) + (v.z + v.w);
+    }
+  } else {
+    for (int l = lane; l < H; l += 32) s += a[l];
+  }
   for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) rs[row] = static_cast<float>(s);
+  if (lane == 0) rs[row] = s;
 }
 
 // emax[v] = max_k E[k,v];  emax_rs[v] = max_k E[k,v] * rs[k]   (Et = E transposed)
@@ -197,32 +206,43 @@ __global__ void k_exclusive_scan(const int* __restrict__ count, int V, int* __re
 }
 
 // order[offset[v] ..] = the batch-major flow rows t*B + b of every pair with token v,
-// in increasing token-array index b*T + t: a stable, deterministic bucketing (one
-// block per token value scans the whole token array).
-__global__ void k_token_bucket(const int* __restrict__ tokens, int T, int B, const int* __restrict__ offset,
-                               int* __restrict__ order) {
-  __shared__ int warp_n[8];
-  const int v = blockIdx.x;
+// in increasing token-array index b*T + t: a stable, deterministic bucketing. Each
+// block owns kBucketSpan consecutive token values and scans the whole token array once.
+constexpr int kBucketSpan = 16;
+__global__ void k_token_bucket(const int* __restrict__ tokens, int T, int B, int V,
+                               const int* __restrict__ offset, int* __restrict__ order) {
+  __shared__ int warp_n[kBucketSpan][8];
+  __shared__ int base[kBucketSpan];
+  const int v0 = blockIdx.x * kBucketSpan;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < kBucketSpan) base[threadIdx.x] = v0 + threadIdx.x < V ? offset[v0 + threadIdx.x] : 0;
+  __syncthreads();
   const int n = T * B;
-  int base = offset[v];
   for (int i0 = 0; i0 < n; i0 += 256) {
     const int i = i0 + threadIdx.x;
-    const bool match = i < n && tokens[i] == v;
-    const unsigned bal = __ballot_sync(0xffffffffu, match);
-    if (lane == 0) warp_n[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0, total = 0;
+    const int tok = i < n ? tokens[i] : -1;
+    const int slot = tok - v0;                       // in [0, kBucketSpan) when this block owns it
+    const bool mine = slot >= 0 && slot < kBucketSpan;
+    unsigned my_bal = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      before += w < warp ? warp_n[w] : 0;
-      total += warp_n[w];
+    for (int j = 0; j < kBucketSpan; ++j) {
+      const unsigned bal = __ballot_sync(0xffffffffu, mine && slot == j);
+      if (lane == 0) warp_n[j][warp] = __popc(bal);
+      if (mine && slot == j) my_bal = bal;
     }
-    if (match) {
+    __syncthreads();
+    if (mine) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += warp_n[slot][w];
       const int b = i / T, t = i - b * T;
-      order[base + before + __popc(bal & ((1u << lane) - 1u))] = t * B + b;
+      order[base[slot] + before + __popc(my_bal & ((1u << lane) - 1u))] = t * B + b;
     }
-    base += total;
+    __syncthreads();
+    if (threadIdx.x < kBucketSpan) {
+      int total = 0;
+      for (int w = 0; w < 8; ++w) total += warp_n[threadIdx.x][w];
+      base[threadIdx.x] += total;
+    }
     __syncthreads();
   }
 }
@@ -575,7 +595,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
     PC_LAUNCH_CHECK();
     k_exclusive_scan<<<1, 1024, 0, s>>>(w.tok_count, V, w.tok_offset);
     PC_LAUNCH_CHECK();
-    k_token_bucket<<<V, 256, 0, s>>>(tokens, T, B, w.tok_offset, w.tok_order);
+    k_token_bucket<<<cdiv(V, kBucketSpan), 256, 0, s>>>(tokens, T, B, V, w.tok_offset, w.tok_order);
     PC_LAUNCH_CHECK();
   }
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));

@@ -218,8 +218,8 @@ void* align256(void* p) {
 pc_status_t check_layer_shape(int G, int M, int N, int B, long long cs) {
   PC_CHECK(G >= 1 && M >= 1 && N >= 1 && B >= 1, PC_ERR_SHAPE,
            "G, M, N, B must be >= 1 (got %d, %d, %d, %d)", G, M, N, B);
-  PC_CHECK(M < (1 << 24) && N < (1 << 24) && B < (1 << 24) && G < (1 << 20), PC_ERR_SHAPE,
-           "sizes out of range (M, N, B < 2^24, G < 2^20)");
+  PC_CHECK(M < (1 << 24) && N < (1 << 24) && B < (1 << 24) && G <= 65535, PC_ERR_SHAPE,
+           "sizes out of range (M, N, B < 2^24, G <= 65535)");
   PC_CHECK(cs >= 0, PC_ERR_SHAPE, "child_stride must be >= 0 (got %lld)", cs);
   PC_CHECK(G == 1 || cs >= N, PC_ERR_SHAPE,
            "with G > 1 groups the child groups must not overlap: child_stride %lld < N %d", cs, N);

@@ -94,13 +94,43 @@ __global__ void k_transpose_to_operand(const float* __restrict__ src, long long 
   }
 }
 
+// Four consecutive columns per thread, blockIdx.x = matrix row (16-byte loads).
+template <int P>
+__global__ void k_rows_to_operand4(const float* __restrict__ src, long long src_ld, long long src_gs, int R,
+                                   int C, void* dst, long long dst_ld, size_t lo) {
+  const long long gr = blockIdx.x;
+  const long long g = gr / R, r = gr % R;
+  const int c = 4 * (blockIdx.y * blockDim.x + threadIdx.x);
+  if (c >= C) return;
+  const float4 v = *reinterpret_cast<const float4*>(src + g * src_gs + r * src_ld + c);
+  const size_t idx = static_cast<size_t>(gr * dst_ld + c);
+  if constexpr (P == kBF16) {
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(dst) + idx) =
+        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  } else {
+    const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(dst) + idx) = h;
+    if constexpr (P == kTF32x3)
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(dst) + idx + lo) =
+          make_float4(tf32_rna(v.x - h.x), tf32_rna(v.y - h.y), tf32_rna(v.z - h.z), tf32_rna(v.w - h.w));
+  }
+}
+
 template <int P>
 pc_status_t rows_to_operand(const float* src, long long src_ld, long long src_gs, int G, int R,
                             int C, const Operand& dst, cudaStream_t s) {
   const long long total = static_cast<long long>(G) * R * C;
   if (total == 0) return PC_OK;
-  const unsigned blocks = static_cast<unsigned>((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
-  k_rows_to_operand<P><<<blocks, 256, 0, s>>>(src, src_ld, src_gs, G, R, C, dst.ptr, dst.ld, dst.lo_elems);
+  const bool vec = (C % 4 == 0) && (src_ld % 4 == 0) && (src_gs % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(src) & 15) == 0 && static_cast<long long>(G) * R < (1ll << 31) &&
+                   (C / 4 + 255) / 256 < 65536;
+  if (vec) {
+    const dim3 grid(static_cast<unsigned>(static_cast<long long>(G) * R), cdiv(C / 4, 256));
+    k_rows_to_operand4<P><<<grid, 256, 0, s>>>(src, src_ld, src_gs, R, C, dst.ptr, dst.ld, dst.lo_elems);
+  } else {
+    const unsigned blocks = static_cast<unsigned>((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
+    k_rows_to_operand<P><<<blocks, 256, 0, s>>>(src, src_ld, src_gs, G, R, C, dst.ptr, dst.ld, dst.lo_elems);
+  }
   PC_LAUNCH_CHECK();
   return PC_OK;
 }
