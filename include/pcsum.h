@@ -185,6 +185,34 @@ PCSUM_API pc_status_t pc_hmm_fwd_bwd(int H, int T, int V, int B, const int32_t* 
                            float* dE, int accumulate, pc_precision_t prec, void* ws,
                            size_t ws_bytes, pc_stream_t stream);
 
+/* ------------------------------------------------------------------------------
+ * Whole HCLT circuit, forward + backward (pyjuice PR #62, Results table "HCLT, 1024
+ * latents, 768 variables, 512 categories"; Summary 2, second bullet: its layers run
+ * as batched GEMMs over evenly strided child groups). A latent tree over the
+ * variables:  n_v(z) = E_v[z, x_v] prod_{c: parent[c]=v} sum_{z'} W_c[z,z'] n_c(z'),
+ * LL = log sum_z pi[z] n_0(z). Edges are processed level by level (one grouped
+ * contraction per level of equal child height).
+ *
+ *   parent [nvars] int32 HOST     parent[0] = -1, parent[i] in [0, i)
+ *   data   [B][nvars] int32       category of each variable per sample, in [0, C)
+ *                                 (a category outside [0, C) has emission 0)
+ *   pi [H], W [nvars][H][H] (W[c][z_parent][z_c]; W[0] unused), E [nvars][H][C]
+ *   ll [B] double                 log P(x) per sample (written)
+ *   dpi [H], dW [nvars][H][H] (dW[0] = 0), dE [nvars][H][C]   EM flows summed over
+ *                                 the batch; each may be NULL; all NULL = ll only.
+ * Limits: 1 <= nvars <= 65535, 1 <= H <= 8192, 1 <= C <= 8192, 1 <= B <= 65535.
+ * The call copies a few KB of tree plan host->device with cudaMemcpyAsync from
+ * pageable memory, so unlike the other entry points it is not stream-capturable.
+ * ---------------------------------------------------------------------------- */
+PCSUM_API pc_status_t pc_hclt_workspace(int nvars, int H, int C, int B, pc_precision_t prec,
+                                        size_t* bytes);
+
+PCSUM_API pc_status_t pc_hclt_fwd_bwd(int nvars, int H, int C, int B, const int32_t* parent,
+                                      const int32_t* data, const float* pi, const float* W,
+                                      const float* E, double* ll, float* dpi, float* dW, float* dE,
+                                      int accumulate, pc_precision_t prec, void* ws,
+                                      size_t ws_bytes, pc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

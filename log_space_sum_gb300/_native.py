@@ -42,6 +42,8 @@ SIGNATURES = {
     "pc_sum_layer_fwd_noalloc": [_i, _i, _i, _i, _p, _p, _ll, _p, _i, _p],
     "pc_hmm_workspace": [_i, _i, _i, _i, _i, _p],
     "pc_hmm_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
+    "pc_hclt_workspace": [_i, _i, _i, _i, _i, _p],
+    "pc_hclt_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
 }
 _STR = {"pc_version", "pc_status_string", "pc_last_error"}
 

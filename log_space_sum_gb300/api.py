@@ -165,6 +165,46 @@ def hmm_fwd_bwd(tokens, pi, A, E, precision="auto", flows=True, ll=None, dpi=Non
     return ll, dpi, dA, dE
 
 
+# -------------------------------------------------------------------------- HCLT
+def hclt_fwd_bwd(parent, data, pi, W, E, precision="auto", flows=True, ll=None, dpi=None, dW=None, dE=None,
+                 accumulate=False, **removed):
+    """Whole HCLT circuit (pc_hclt_fwd_bwd). ``parent`` is a host int sequence
+    (parent[0] = -1, parent[i] in [0, i)); data [B, nvars] int32 on the GPU; W
+    [nvars, H, H]; E [nvars, H, C]. Returns (ll [B] float64, dpi, dW, dE)."""
+    import numpy as np
+
+    _removed_flags(removed, "hclt_fwd_bwd")
+    prec = precision_code(precision)
+    _check(W, "W")
+    dev = W.device
+    _check(data, "data", dtype=torch.int32, device=dev)
+    _check(pi, "pi", device=dev)
+    _check(E, "E", device=dev)
+    par = np.ascontiguousarray(np.asarray(parent.cpu() if isinstance(parent, torch.Tensor) else parent,
+                                          dtype=np.int32))
+    B, n = data.shape
+    _, H, Ccat = E.shape
+    if par.shape != (n,):
+        raise ValueError(f"parent has shape {par.shape}, expected ({n},)")
+    if ll is None:
+        ll = torch.empty(B, dtype=torch.float64, device=dev)
+    _check(ll, "ll", dtype=torch.float64, device=dev)
+    if flows:
+        dpi = torch.empty(H, dtype=torch.float32, device=dev) if dpi is None else dpi
+        dW = torch.empty(n, H, H, dtype=torch.float32, device=dev) if dW is None else dW
+        dE = torch.empty(n, H, Ccat, dtype=torch.float32, device=dev) if dE is None else dE
+        for t, nm in ((dpi, "dpi"), (dW, "dW"), (dE, "dE")):
+            _check(t, nm, device=dev)
+    else:
+        dpi = dW = dE = None
+    nb = _query("pc_hclt_workspace", n, H, Ccat, B, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_hclt_fwd_bwd", n, H, Ccat, B, par.ctypes.data_as(C.c_void_p), _ptr(data), _ptr(pi), _ptr(W), _ptr(E),
+           _ptr(ll), _ptr(dpi), _ptr(dW), _ptr(dE), int(bool(accumulate)), prec, _ptr(ws), ws.numel(),
+           _stream(dev))
+    return ll, dpi, dW, dE
+
+
 # -------------------------------------------------------------------- diagnostics
 def device_status(device=None) -> None:
     """Synchronises the current stream and raises PCError if a kernel gave up a bounded wait."""

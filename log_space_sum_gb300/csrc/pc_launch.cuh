@@ -59,7 +59,7 @@ inline unsigned cdiv(long long a, long long b) { return static_cast<unsigned>((a
 template <int P>
 __global__ void k_rows_to_operand(const float* __restrict__ src, long long src_ld,
                                   long long src_gs, int G, int R, int C, void* dst,
-                                  long long dst_ld, size_t lo) {
+                                  long long dst_ld, size_t lo, const int* gmap) {
   const long long total = static_cast<long long>(G) * R * C;
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -67,7 +67,7 @@ __global__ void k_rows_to_operand(const float* __restrict__ src, long long src_l
     const long long gr = idx / C;
     const long long r = gr % R;
     const long long g = gr / R;
-    const float v = src[g * src_gs + r * src_ld + c];
+    const float v = src[(gmap ? gmap[g] : g) * src_gs + r * src_ld + c];
     store_operand<P>(dst, static_cast<size_t>((g * R + r) * dst_ld + c), lo, v);
   }
 }
@@ -76,14 +76,15 @@ __global__ void k_rows_to_operand(const float* __restrict__ src, long long src_l
 template <int P>
 __global__ void k_transpose_to_operand(const float* __restrict__ src, long long src_ld,
                                        long long src_gs, int R, int C, void* dst,
-                                       long long dst_ld, size_t lo) {
+                                       long long dst_ld, size_t lo, const int* gmap) {
   __shared__ float tile[32][33];
   const int g = blockIdx.z;
+  const long long gs = gmap ? gmap[g] : g;
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   const int tx = threadIdx.x, ty = threadIdx.y;
   for (int k = ty; k < 32; k += 8) {
     const int r = r0 + k, c = c0 + tx;
-    tile[k][tx] = (r < R && c < C) ? src[g * src_gs + static_cast<long long>(r) * src_ld + c] : 0.f;
+    tile[k][tx] = (r < R && c < C) ? src[gs * src_gs + static_cast<long long>(r) * src_ld + c] : 0.f;
   }
   __syncthreads();
   for (int k = ty; k < 32; k += 8) {
@@ -97,12 +98,12 @@ __global__ void k_transpose_to_operand(const float* __restrict__ src, long long 
 // Four consecutive columns per thread, blockIdx.x = matrix row (16-byte loads).
 template <int P>
 __global__ void k_rows_to_operand4(const float* __restrict__ src, long long src_ld, long long src_gs, int R,
-                                   int C, void* dst, long long dst_ld, size_t lo) {
+                                   int C, void* dst, long long dst_ld, size_t lo, const int* gmap) {
   const long long gr = blockIdx.x;
   const long long g = gr / R, r = gr % R;
   const int c = 4 * (blockIdx.y * blockDim.x + threadIdx.x);
   if (c >= C) return;
-  const float4 v = *reinterpret_cast<const float4*>(src + g * src_gs + r * src_ld + c);
+  const float4 v = *reinterpret_cast<const float4*>(src + (gmap ? gmap[g] : g) * src_gs + r * src_ld + c);
   const size_t idx = static_cast<size_t>(gr * dst_ld + c);
   if constexpr (P == kBF16) {
     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(dst) + idx) =
@@ -118,7 +119,7 @@ __global__ void k_rows_to_operand4(const float* __restrict__ src, long long src_
 
 template <int P>
 pc_status_t rows_to_operand(const float* src, long long src_ld, long long src_gs, int G, int R,
-                            int C, const Operand& dst, cudaStream_t s) {
+                            int C, const Operand& dst, cudaStream_t s, const int* gmap = nullptr) {
   const long long total = static_cast<long long>(G) * R * C;
   if (total == 0) return PC_OK;
   const bool vec = (C % 4 == 0) && (src_ld % 4 == 0) && (src_gs % 4 == 0) &&
@@ -126,10 +127,10 @@ pc_status_t rows_to_operand(const float* src, long long src_ld, long long src_gs
                    (C / 4 + 255) / 256 < 65536;
   if (vec) {
     const dim3 grid(static_cast<unsigned>(static_cast<long long>(G) * R), cdiv(C / 4, 256));
-    k_rows_to_operand4<P><<<grid, 256, 0, s>>>(src, src_ld, src_gs, R, C, dst.ptr, dst.ld, dst.lo_elems);
+    k_rows_to_operand4<P><<<grid, 256, 0, s>>>(src, src_ld, src_gs, R, C, dst.ptr, dst.ld, dst.lo_elems, gmap);
   } else {
     const unsigned blocks = static_cast<unsigned>((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
-    k_rows_to_operand<P><<<blocks, 256, 0, s>>>(src, src_ld, src_gs, G, R, C, dst.ptr, dst.ld, dst.lo_elems);
+    k_rows_to_operand<P><<<blocks, 256, 0, s>>>(src, src_ld, src_gs, G, R, C, dst.ptr, dst.ld, dst.lo_elems, gmap);
   }
   PC_LAUNCH_CHECK();
   return PC_OK;
@@ -137,11 +138,11 @@ pc_status_t rows_to_operand(const float* src, long long src_ld, long long src_gs
 
 template <int P>
 pc_status_t transpose_to_operand(const float* src, long long src_ld, long long src_gs, int G,
-                                 int R, int C, const Operand& dst, cudaStream_t s) {
+                                 int R, int C, const Operand& dst, cudaStream_t s, const int* gmap = nullptr) {
   if (G == 0 || R == 0 || C == 0) return PC_OK;
   dim3 grid(cdiv(C, 32), cdiv(R, 32), G);
   k_transpose_to_operand<P><<<grid, dim3(32, 8), 0, s>>>(src, src_ld, src_gs, R, C, dst.ptr, dst.ld,
-                                                         dst.lo_elems);
+                                                         dst.lo_elems, gmap);
   PC_LAUNCH_CHECK();
   return PC_OK;
 }
@@ -153,6 +154,7 @@ struct EpiThetaScale : EpiNoHooks {
     float* F;
     const float* theta;
     int M, N, accumulate;
+    const int* gmap;  // group g reads theta / writes F at matrix gmap[g] (NULL: g)
   };
   // Transposed so that lane l owns column col0 + l of the warp's 32 rows: every theta
   // load and F store of the warp covers one contiguous row segment. All loads of the
@@ -166,8 +168,9 @@ struct EpiThetaScale : EpiNoHooks {
     const int j = n0 + col0 + lane;
     if (j >= p.N) return;
     const long long ld = p.N;
-    const float* tp = p.theta + (static_cast<long long>(g) * p.M + i0) * ld + j;
-    float* Fp = p.F + (static_cast<long long>(g) * p.M + i0) * ld + j;
+    const long long gm = p.gmap ? p.gmap[g] : g;
+    const float* tp = p.theta + (gm * p.M + i0) * ld + j;
+    float* Fp = p.F + (gm * p.M + i0) * ld + j;
     // two halves of 16 rows keep the loads-before-stores batch within the register budget
 #pragma unroll
     for (int h = 0; h < 32; h += 16) {

@@ -1,0 +1,109 @@
+"""GPU parity of the whole HCLT circuit (pc_hclt_fwd_bwd through the C ABI) against the
+float64 oracle: random, star, chain and single-variable trees with every size off the
+tile sizes, in every mode; the 768-variable workload on sampled log-likelihoods, flow
+invariants and the uniform-emission closed form."""
+import numpy as np
+import pytest
+import torch
+
+import log_space_sum_gb300 as pc
+from oracle.hclt import hclt_fwd_bwd, hclt_ll
+from tolerances import FLOW_TOL, LL_TOL, MODES, flow_err, ll_err
+from workloads import hclt, hclt_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pc.load()
+
+
+def _gpu_run(d, mode, flows=True):
+    t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda() for k in ("data", "pi", "W", "E")}
+    ll, dpi, dW, dE = pc.hclt_fwd_bwd(d["parent"], t["data"], t["pi"], t["W"], t["E"], precision=mode, flows=flows)
+    torch.cuda.synchronize()
+    pc.device_status()
+    cpu = lambda v: None if v is None else v.cpu().numpy()
+    return cpu(ll), cpu(dpi), cpu(dW), cpu(dE)
+
+
+def _oracle(d):
+    return hclt_fwd_bwd(d["parent"], d["data"], d["pi"], d["W"], d["E"])
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_random_tree_ragged(mode):
+    d = hclt_inputs(40, 130, 17, 45, seed=200)
+    rl, rpi, rW, rE = _oracle(d)
+    ll, dpi, dW, dE = _gpu_run(d, mode)
+    errs = ll_err(ll, rl), flow_err(dpi, rpi), flow_err(dW[1:], rW[1:]), flow_err(dE, rE)
+    print(f"hclt 40x130 {mode}: ll {errs[0]:.3e} dpi {errs[1]:.3e} dW {errs[2]:.3e} dE {errs[3]:.3e}")
+    assert errs[0] <= LL_TOL[mode]
+    assert max(errs[1:]) <= FLOW_TOL[mode]
+    assert np.all(dW[0] == 0)
+
+
+@pytest.mark.parametrize("parent", [
+    [-1],                                   # one variable: no edge
+    [-1, 0],                                # one edge
+    [-1, 0, 0, 0, 0, 0, 0],                 # star: six children in one level
+    [-1, 0, 1, 2, 3, 4, 5, 6],              # chain: eight levels of one edge
+])
+def test_tree_shapes(parent):
+    p = np.array(parent, dtype=np.int32)
+    d = hclt_inputs(len(p), 70, 9, 33, seed=201, parent=p)
+    rl, rpi, rW, rE = _oracle(d)
+    ll, dpi, dW, dE = _gpu_run(d, "fp32")
+    assert ll_err(ll, rl) <= LL_TOL["fp32"]
+    assert flow_err(dpi, rpi) <= FLOW_TOL["fp32"]
+    assert flow_err(dE, rE) <= FLOW_TOL["fp32"]
+    if len(p) > 1:
+        assert flow_err(dW[1:], rW[1:]) <= FLOW_TOL["fp32"]
+
+
+def test_forward_only_and_accumulate():
+    d = hclt_inputs(20, 96, 6, 40, seed=202)
+    a = _gpu_run(d, "fp32", flows=False)
+    assert a[1] is None
+    t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda() for k in ("data", "pi", "W", "E")}
+    ll, dpi, dW, dE = pc.hclt_fwd_bwd(d["parent"], t["data"], t["pi"], t["W"], t["E"], precision="fp32")
+    assert np.array_equal(ll.cpu().numpy(), a[0])
+    ll2, dpi2, dW2, dE2 = pc.hclt_fwd_bwd(d["parent"], t["data"], t["pi"], t["W"], t["E"], precision="fp32",
+                                          dpi=dpi.clone(), dW=dW.clone(), dE=dE.clone(), accumulate=True)
+    for x, y in ((dpi, dpi2), (dW, dW2), (dE, dE2)):
+        torch.testing.assert_close(y, 2 * x, rtol=1e-6, atol=0)
+
+
+@pytest.fixture(scope="module")
+def hclt_full():
+    return hclt()
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_hclt_768_sampled_and_invariants(hclt_full, mode):
+    d = hclt_full
+    ll, dpi, dW, dE = _gpu_run(d, mode)
+    B, n = d["data"].shape
+    pick = np.random.default_rng(210).choice(B, size=4, replace=False)
+    ref = hclt_ll(d["parent"], d["data"][pick], d["pi"], d["W"], d["E"])
+    err = ll_err(ll[pick], ref)
+    print(f"hclt 768 {mode}: sampled ll err {err:.3e}")
+    assert err <= LL_TOL[mode]
+    tol = {"auto": 1e-2, "tf32": 1e-3, "fp32": 1e-5}[mode]
+    assert abs(dpi.astype(np.float64).sum() - B) <= tol * B
+    np.testing.assert_allclose(dW[1:].astype(np.float64).sum(axis=(1, 2)), B, rtol=tol)
+    np.testing.assert_allclose(dE.astype(np.float64).sum(axis=(1, 2)), B, rtol=tol)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_hclt_768_uniform_emissions(hclt_full, mode):
+    d = dict(hclt_full)
+    d["E"] = np.full_like(d["E"], 1.0 / 512)
+    ll, *_ = _gpu_run(d, mode, flows=False)
+    W = d["W"].astype(np.float64)
+    pi = d["pi"].astype(np.float64)
+    # the float32 rows of W and pi sum to 1 only to ~1e-7; bound their effect on LL
+    slack = np.abs(np.log(W[1:].sum(-1))).max(axis=1).sum() + abs(np.log(pi.sum()))
+    assert np.abs(ll + 768 * np.log(512)).max() <= LL_TOL[mode] + slack
