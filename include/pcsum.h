@@ -213,6 +213,45 @@ PCSUM_API pc_status_t pc_hclt_fwd_bwd(int nvars, int H, int C, int B, const int3
                                       int accumulate, pc_precision_t prec, void* ws,
                                       size_t ws_bytes, pc_stream_t stream);
 
+/* ------------------------------------------------------------------------------
+ * LowRank "exp_sum" per-sample scale on a dense sum layer with shared children
+ * (pyjuice LowRank API doc: intro formulas, Tensor layout, Training, Note). Per sample b
+ *   S_b = A_b B_b,  g_b = exp(S_b),  Z_b[i] = sum_j theta[i,j] g_b[i,j],
+ *   theta_b = theta g_b / Z_b,       out[i,b] = log sum_j theta_b[i,j] exp(x[j,b]).
+ * The per-sample scale is made on the tensor cores tile by tile and never stored.
+ *
+ *   theta [M][N]                shared parameters (rows need not sum to 1)
+ *   A [B][M][K], Bm [B][K][N]   the factors, K = rank, 1 <= K <= 64
+ *   x [N][B]                    child log-values
+ *   out [M][B]                  node log-values (written)
+ *   logZ [B][M]                 log Z_b[i] (written by the forward, read by the backward)
+ * Backward for node flows f [M][B], with p = theta_b exp(x_j - out_i), q = theta_b:
+ *   dA [B][M][K] = D B_b^T and dB [B][K][N] = A_b^T D with D = f (p - q), the gradient
+ *   of sum f out; e [N][B] = sum_i f p (element flows); Fplus [M][N] = sum_b f p
+ *   (parameter flows F+); Wstat [M][N] = sum_b f g_b / Z_b (the Z-correction statistic,
+ *   F- = theta Wstat). Each output may be NULL (Wstat NULL = no Z correction); with
+ *   accumulate != 0 the results are added to the outputs. Every output element is
+ *   written by one thread: the results are deterministic.
+ * Precision: S from bf16 hi + lo products (auto), one TF32 pass (tf32) or 3xTF32 (fp32);
+ * the gradient contractions one bf16 term (auto), TF32, or 3xTF32.
+ * Limits: K <= 64 (PC_ERR_UNSUPPORTED above), B <= 65535. M, N or B may be 0.
+ * Workspace: pc_lowrank_exp_sum_workspace(..., with_backward, ...) bytes, 16-byte aligned.
+ * ---------------------------------------------------------------------------- */
+PCSUM_API pc_status_t pc_lowrank_exp_sum_workspace(int M, int N, int K, int B, int with_backward,
+                                                   pc_precision_t prec, size_t* bytes);
+
+PCSUM_API pc_status_t pc_lowrank_exp_sum_fwd(int M, int N, int K, int B, const float* theta,
+                                             const float* A, const float* Bm, const float* x,
+                                             float* out, float* logZ, pc_precision_t prec,
+                                             void* ws, size_t ws_bytes, pc_stream_t stream);
+
+PCSUM_API pc_status_t pc_lowrank_exp_sum_bwd(int M, int N, int K, int B, const float* theta,
+                                             const float* A, const float* Bm, const float* x,
+                                             const float* out, const float* logZ, const float* f,
+                                             float* dA, float* dB, float* e, float* Fplus,
+                                             float* Wstat, int accumulate, pc_precision_t prec,
+                                             void* ws, size_t ws_bytes, pc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -11,6 +11,8 @@ from .api import (  # noqa: F401
     device_status,
     hclt_fwd_bwd,
     hmm_fwd_bwd,
+    lowrank_exp_sum_bwd,
+    lowrank_exp_sum_fwd,
     precision_code,
     profile_start,
     profile_stop,

@@ -44,6 +44,10 @@ SIGNATURES = {
     "pc_hmm_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
     "pc_hclt_workspace": [_i, _i, _i, _i, _i, _p],
     "pc_hclt_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
+    "pc_lowrank_exp_sum_workspace": [_i, _i, _i, _i, _i, _i, _p],
+    "pc_lowrank_exp_sum_fwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p],
+    "pc_lowrank_exp_sum_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz,
+                               _p],
 }
 _STR = {"pc_version", "pc_status_string", "pc_last_error"}
 

@@ -205,6 +205,65 @@ def hclt_fwd_bwd(parent, data, pi, W, E, precision="auto", flows=True, ll=None, 
     return ll, dpi, dW, dE
 
 
+# ----------------------------------------------------------------------- LowRank
+def _lowrank_shapes(theta, A, Bm, x):
+    _check(theta, "theta")
+    dev = theta.device
+    for t, n in ((A, "A"), (Bm, "B"), (x, "x")):
+        _check(t, n, device=dev)
+    M, Nn = theta.shape
+    Bs, Ma, K = A.shape
+    if Ma != M or tuple(Bm.shape) != (Bs, K, Nn) or tuple(x.shape) != (Nn, Bs):
+        raise ValueError(f"LowRank shapes: theta {tuple(theta.shape)}, A {tuple(A.shape)}, B {tuple(Bm.shape)}, "
+                         f"x {tuple(x.shape)}; expected A [B,M,K], B [B,K,N], x [N,B]")
+    return dev, M, Nn, K, Bs
+
+
+def lowrank_exp_sum_fwd(theta, A, Bm, x, precision="auto", out=None, logZ=None, **removed):
+    """LowRank exp_sum layer forward (pc_lowrank_exp_sum_fwd): returns out [M,B] and
+    logZ [B,M] = log Z_b[i], which the backward reads."""
+    _removed_flags(removed, "lowrank_exp_sum_fwd")
+    prec = precision_code(precision)
+    dev, M, Nn, K, Bs = _lowrank_shapes(theta, A, Bm, x)
+    out = torch.empty(M, Bs, dtype=torch.float32, device=dev) if out is None else out
+    logZ = torch.empty(Bs, M, dtype=torch.float32, device=dev) if logZ is None else logZ
+    _check(out, "out", device=dev)
+    _check(logZ, "logZ", device=dev)
+    nb = _query("pc_lowrank_exp_sum_workspace", M, Nn, K, Bs, 0, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_lowrank_exp_sum_fwd", M, Nn, K, Bs, _ptr(theta), _ptr(A), _ptr(Bm), _ptr(x), _ptr(out), _ptr(logZ),
+           prec, _ptr(ws), ws.numel(), _stream(dev))
+    return out, logZ
+
+
+def lowrank_exp_sum_bwd(theta, A, Bm, x, out, logZ, f, precision="auto", grads=True, element_flows=True,
+                        param_flows=True, z_correction=True, dA=None, dB=None, e=None, Fplus=None, W=None,
+                        accumulate=False, **removed):
+    """LowRank exp_sum layer backward (pc_lowrank_exp_sum_bwd): returns a dict with dA
+    [B,M,K], dB [B,K,N] (``grads``), e [N,B] (``element_flows``), Fplus [M,N]
+    (``param_flows``) and W [M,N] (``z_correction``); what is switched off is None."""
+    _removed_flags(removed, "lowrank_exp_sum_bwd")
+    prec = precision_code(precision)
+    dev, M, Nn, K, Bs = _lowrank_shapes(theta, A, Bm, x)
+    for t, n in ((out, "out"), (logZ, "logZ"), (f, "f")):
+        _check(t, n, device=dev)
+    new = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)  # noqa: E731
+    dA = (new(Bs, M, K) if dA is None else dA) if grads else None
+    dB = (new(Bs, K, Nn) if dB is None else dB) if grads else None
+    e = (new(Nn, Bs) if e is None else e) if element_flows else None
+    Fplus = (new(M, Nn) if Fplus is None else Fplus) if param_flows else None
+    W = (new(M, Nn) if W is None else W) if z_correction else None
+    for t, n in ((dA, "dA"), (dB, "dB"), (e, "e"), (Fplus, "Fplus"), (W, "W")):
+        if t is not None:
+            _check(t, n, device=dev)
+    nb = _query("pc_lowrank_exp_sum_workspace", M, Nn, K, Bs, 1, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_lowrank_exp_sum_bwd", M, Nn, K, Bs, _ptr(theta), _ptr(A), _ptr(Bm), _ptr(x), _ptr(out), _ptr(logZ),
+           _ptr(f), _ptr(dA), _ptr(dB), _ptr(e), _ptr(Fplus), _ptr(W), int(bool(accumulate)), prec, _ptr(ws),
+           ws.numel(), _stream(dev))
+    return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=W)
+
+
 # -------------------------------------------------------------------- diagnostics
 def device_status(device=None) -> None:
     """Synchronises the current stream and raises PCError if a kernel gave up a bounded wait."""

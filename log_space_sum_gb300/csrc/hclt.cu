@@ -12,14 +12,17 @@
 // last), so the edges whose child has height L form one contiguous run of slots: one
 // grouped contraction per level, the groups evenly strided in every operand.
 //
-// Values. Every node keeps u_v[b][z] = exp(log n_v(z) - O_v[b]) with max_z u_v = 1 and
-// a per-sample log-offset O_v[b] in double. The product layer is evaluated in log space
-// (a sum of logs, then one exp), so a node with many children cannot underflow:
-//   y_v[b][z] = log E_v[z, x_v] + sum_c logD_c[b][z],   O_v = max_z y_v + sum_c O_c,
-//   u_v = exp(y_v - max_z y_v);
-// each edge's sum layer D_c[b][z] = sum_{z'} W_c[z,z'] u_c[b][z'] keeps logD_c = log D_c
-// (its children are already shifted by their maximum, so the layer's column maximum is 0).
+// Values. Every node keeps u_v[b][z] = n_v(z) / max_z n_v(z) (so max_z u_v = 1) and a
+// per-sample log-offset O_v[b] = log max_z n_v in double. Each edge's sum layer
+//   D_c[b][z] = sum_{z'} W_c[z,z'] u_c[b][z']
+// is kept linear, and the product layer multiplies in float32 with an exact power-of-two
+// exponent carried beside every running product, so a node with many children cannot
+// underflow and no rounding but the multiplies' own round-to-nearest enters:
+//   n'_v[b][z] = E_v[z, x_v] * prod_c D_c[b][z] = m_z 2^{e_z}   (m_z in [1/2, 1)),
+//   u_v = n'_v / max_z n'_v,   O_v = log max_z n'_v + sum_c O_c,
 //   LL_b = O_0[b] + log sum_z pi[z] u_0[b][z].
+// (Taking logs instead would round every y = log E + sum log D to float32 at |y| of
+// several nats, an error of ~1e-7 per node that a 768-node tree accumulates.)
 // Backward (root flow 1; product nodes pass their flow to every child):
 //   f_0 = pi u_0 / sum_z pi u_0,     g_c = f_parent(c) / D_c      (the layer's scaled flow)
 //   f_c[b][z'] = u_c[b][z'] sum_z W_c[z,z'] g_c[b][z]             element flows
@@ -39,13 +42,14 @@ namespace {
 constexpr int kHcltBN = 128;
 
 // ------------------------------------------------------------------ set-up
-// LEt[v][k][z] = log E[v][z][k] (-inf for 0): per-variable transpose with the log taken.
-__global__ void k_hclt_log_et(const float* __restrict__ E, int H, int C, float* __restrict__ LEt) {
+// Et[v][k][z] = E[v][z][k]: per-variable transpose, so that the emissions of one category
+// are a contiguous row over the latents.
+__global__ void k_hclt_et(const float* __restrict__ E, int H, int C, float* __restrict__ Et) {
   __shared__ float tile[32][33];
   const long long v = blockIdx.z;
   const int k0 = blockIdx.x * 32, z0 = blockIdx.y * 32;
   const float* src = E + v * H * C;
-  float* dst = LEt + v * H * C;
+  float* dst = Et + v * H * C;
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int z = z0 + i, k = k0 + threadIdx.x;
     tile[i][threadIdx.x] = (z < H && k < C) ? src[static_cast<long long>(z) * C + k] : 0.f;
@@ -53,61 +57,72 @@ __global__ void k_hclt_log_et(const float* __restrict__ E, int H, int C, float* 
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int k = k0 + i, z = z0 + threadIdx.x;
-    if (z < H && k < C) {
-      const float e = tile[threadIdx.x][i];
-      dst[static_cast<long long>(k) * H + z] = e > 0.f ? logf(e) : -INFINITY;
-    }
+    if (z < H && k < C) dst[static_cast<long long>(k) * H + z] = tile[threadIdx.x][i];
   }
 }
 
 // Product layer of the nodes in slots [s0, s0 + gridDim.x), one block per (node, sample):
-// y = log E_v[., x_v] + sum_children logD, then u = exp(y - max y) (float32 and operand
-// copies), O = max y + sum_children O. For the root it also forms LL and 1 / sum pi u.
+// n' = E_v[., x_v] * prod_children D as float32 mantissas in [1/2, 1) with int exponents,
+// u = n' / max n' (float32 and operand copies), O = log max n' + sum_children O. For the
+// root it also forms LL and 1 / sum pi u.
 template <int P>
 __global__ void k_hclt_product(int s0, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
                                const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr,
-                               const int* __restrict__ child_slots, const float* __restrict__ LEt,
-                               const float* __restrict__ logD, int C, float* __restrict__ U32, void* uop,
+                               const int* __restrict__ child_slots, const float* __restrict__ Et,
+                               const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
                                long long uop_ld, size_t uop_lo, double* __restrict__ O, const float* __restrict__ pi,
                                double* __restrict__ ll, float* __restrict__ rroot) {
-  extern __shared__ float y[];  // H floats
-  __shared__ float red[32];
+  extern __shared__ float mant[];  // H mantissas, then H exponents
+  int* expo = reinterpret_cast<int*>(mant + H);
+  __shared__ long long red[32];
   __shared__ double redd[32];
+  constexpr long long kNone = -0x7fffffffffffffffLL - 1;  // key of a zero product
   const int s = s0 + blockIdx.x;
   const int b = blockIdx.y;
   const int v = var_of_slot[s];
   const int x = data[static_cast<long long>(b) * nvars + v];
   const bool xin = x >= 0 && x < C;  // a category outside [0, C) has emission 0
   const int c0 = child_ptr[s], c1 = child_ptr[s + 1];
-  const float* le = LEt + (static_cast<long long>(v) * C + (xin ? x : 0)) * H;
-  float mx = -INFINITY;
+  const float* er = Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H;
+  // key = e * 2^32 + bits(m) orders the nonzero products m 2^e (m in [1/2, 1)) by value
+  long long best = kNone;
   for (int z = threadIdx.x; z < H; z += blockDim.x) {
-    float acc = xin ? le[z] : -INFINITY;
-    for (int c = c0; c < c1; ++c) acc += logD[(static_cast<long long>(child_slots[c]) * B + b) * H + z];
-    y[z] = acc;
-    mx = fmaxf(mx, acc);
+    int e, k;
+    float m = frexpf(xin ? er[z] : 0.f, &e);
+    for (int c = c0; c < c1; ++c) {
+      m = frexpf(m * D[(static_cast<long long>(child_slots[c]) * B + b) * H + z], &k);
+      e += k;
+    }
+    mant[z] = m;
+    expo[z] = e;
+    if (m > 0.f) best = max(best, static_cast<long long>(e) * 4294967296LL + __float_as_uint(m));
   }
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  for (int o = 16; o; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
   __syncthreads();
   if (threadIdx.x < 32) {
-    float m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : -INFINITY;
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    long long m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : kNone;
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (threadIdx.x == 0) red[0] = m;
   }
   __syncthreads();
-  mx = red[0];
-  const bool live = mx > -INFINITY;
+  best = red[0];
+  const bool live = best != kNone;
+  const unsigned mbits = static_cast<unsigned>(best & 0xffffffffLL);
+  const int emax = live ? static_cast<int>((best - static_cast<long long>(mbits)) / 4294967296LL) : 0;
+  const float mmax = live ? __uint_as_float(mbits) : 1.f;
   const long long row = static_cast<long long>(s) * B + b;
   double dot = 0.0;
   for (int z = threadIdx.x; z < H; z += blockDim.x) {
-    const float u = live ? expf(y[z] - mx) : 0.f;
+    const float m = mant[z];
+    const float u = (live && m > 0.f) ? ldexpf(m / mmax, expo[z] - emax) : 0.f;
     U32[row * H + z] = u;
     if (uop) store_operand<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
     if (s == root_slot) dot += static_cast<double>(pi[z]) * u;
   }
   if (threadIdx.x == 0) {
-    double off = live ? static_cast<double>(mx) : -static_cast<double>(INFINITY);
+    double off = live ? static_cast<double>(emax) * 0.69314718055994530942 + log(static_cast<double>(mmax))
+                      : -static_cast<double>(INFINITY);
     for (int c = c0; c < c1; ++c) off += O[static_cast<long long>(child_slots[c]) * B + b];
     O[row] = off;
   }
@@ -148,7 +163,7 @@ __global__ void k_hclt_root_flows(int root_slot, int H, int B, const float* __re
 // node-major (parameter contraction operand) through a 32 x 32 shared-memory tile.
 template <int P>
 __global__ void k_hclt_scaled_flows(int s0, int H, int B, const int* __restrict__ parent_slot,
-                                    const float* __restrict__ F32, const float* __restrict__ logD, void* gbm,
+                                    const float* __restrict__ F32, const float* __restrict__ D, void* gbm,
                                     long long gbm_ld, size_t gbm_lo, void* gnm, long long gnm_ld, size_t gnm_lo) {
   __shared__ float tile[32][33];
   const int g = blockIdx.z;
@@ -159,8 +174,8 @@ __global__ void k_hclt_scaled_flows(int s0, int H, int B, const int* __restrict_
     const int b = b0 + i, z = z0 + threadIdx.x;
     float w = 0.f;
     if (b < B && z < H) {
-      const float ld = logD[(static_cast<long long>(s) * B + b) * H + z];
-      w = ld > -INFINITY ? F32[(static_cast<long long>(ps) * B + b) * H + z] * expf(-ld) : 0.f;
+      const float d = D[(static_cast<long long>(s) * B + b) * H + z];
+      w = d > 0.f ? F32[(static_cast<long long>(ps) * B + b) * H + z] / d : 0.f;
       store_operand<P>(gbm, static_cast<size_t>((static_cast<long long>(g) * B + b) * gbm_ld + z), gbm_lo, w);
     }
     tile[i][threadIdx.x] = w;
@@ -282,20 +297,24 @@ __device__ __forceinline__ void stage_block(const float* __restrict__ src, int H
   }
 }
 
-// Forward epilogue: logD[g][b][z] = log D (-inf for 0); thread = parent latent z.
+// Forward epilogue: D[g][b][z], the edge's sum layer kept linear; thread = parent latent z.
 struct EpiHcltFwd : EpiNoHooks {
+  // Every edge's D feeds the log-likelihood, and a tree chains hundreds of them: the bf16
+  // mode accumulates K in slices of 16 k-steps so that the accumulator's truncation acts
+  // on partial sums a fraction of D's size.
+  static constexpr int kSliceBF16 = 16;
   struct Params {
-    float* logD;  // at the level's first slot, [G][B][H]
+    float* D;  // at the level's first slot, [G][B][H]
     int H, B;
   };
   __device__ static void apply(const Params& p, int g, int m0, int n0, int row, int col0,
                                float (&v)[32], uint8_t*, float*) {
     const int z = m0 + row;
     if (z >= p.H) return;
-    float* dst = p.logD + (static_cast<long long>(g) * p.B + n0 + col0) * p.H + z;
+    float* dst = p.D + (static_cast<long long>(g) * p.B + n0 + col0) * p.H + z;
 #pragma unroll
     for (int c = 0; c < 32; ++c)
-      if (n0 + col0 + c < p.B) dst[static_cast<long long>(c) * p.H] = v[c] > 0.f ? logf(v[c]) : -INFINITY;
+      if (n0 + col0 + c < p.B) dst[static_cast<long long>(c) * p.H] = v[c];
   }
 };
 
@@ -407,7 +426,7 @@ Operand operand_view(const Operand& op, pc_precision_t p, long long first, long 
 struct HcltWs {
   int* plan;
   Operand Wop, WopT, Uop, Gbm, Gnm, Unm;
-  float *LEt, *U32, *logD, *rroot, *F32, *dEt;
+  float *Et, *U32, *D, *rroot, *F32, *dEt;
   double* O;
   int *cat_order, *cat_off;
 };
@@ -418,10 +437,10 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
   const long long E1 = n > 1 ? n - 1 : 1;
   w->plan = static_cast<int*>(c.take(size_t(4 * n + 2) * 4));
   w->Wop = c.operand(p, E1, H, H);
-  w->LEt = static_cast<float*>(c.take(size_t(n) * C * H * 4));
+  w->Et = static_cast<float*>(c.take(size_t(n) * C * H * 4));
   w->U32 = static_cast<float*>(c.take(size_t(n) * B * H * 4));
   w->Uop = c.operand(p, E1, B, H);
-  w->logD = static_cast<float*>(c.take(size_t(E1) * B * H * 4));
+  w->D = static_cast<float*>(c.take(size_t(E1) * B * H * 4));
   w->O = static_cast<double*>(c.take(size_t(n) * B * 8));
   w->rroot = static_cast<float*>(c.take(size_t(B) * 4));
   if (flows) {
@@ -479,26 +498,30 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dW && !accumulate) PC_CUDA(cudaMemsetAsync(dW, 0, size_t(H) * H * 4, s));  // W[0] has no edge
 
-  k_hclt_log_et<<<dim3(cdiv(C, 32), cdiv(H, 32), n), dim3(32, 8), 0, s>>>(Em, H, C, w.LEt);
+  k_hclt_et<<<dim3(cdiv(C, 32), cdiv(H, 32), n), dim3(32, 8), 0, s>>>(Em, H, C, w.Et);
   PC_LAUNCH_CHECK();
   if (E > 0 && (st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, d_var)) != PC_OK)
     return st;
 
   // -------------------------------------------------------------- forward
+  const size_t prod_smem = size_t(H) * 8;  // mantissas and exponents, up to 64 KB
+  if (prod_smem > 48 * 1024)
+    PC_CUDA(cudaFuncSetAttribute(k_hclt_product<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prod_smem)));
   OperandMaps ma, mb;
   for (int L = 0; L <= pl.maxh; ++L) {
     const int sA = pl.level_start[L], sB = pl.level_start[L + 1];
     const int G = sB - sA;
     if (G <= 0) continue;
     const bool edges = L < pl.maxh;
-    k_hclt_product<P><<<dim3(G, B), 256, size_t(H) * 4, s>>>(
-        sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.LEt, w.logD, C, w.U32, edges ? w.Uop.ptr : nullptr,
+    k_hclt_product<P><<<dim3(G, B), 256, prod_smem, s>>>(
+        sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, w.U32, edges ? w.Uop.ptr : nullptr,
         w.Uop.ld, w.Uop.lo_elems, w.O, pi, ll, w.rroot);
     PC_LAUNCH_CHECK();
     if (!edges) continue;
     if ((st = encode_maps(&ma, operand_view(w.Wop, prec, sA, G), prec, kBM)) != PC_OK) return st;
     if ((st = encode_maps(&mb, operand_view(w.Uop, prec, sA, G), prec, kHcltBN)) != PC_OK) return st;
-    EpiHcltFwd::Params ep{w.logD + static_cast<long long>(sA) * B * H, H, B};
+    EpiHcltFwd::Params ep{w.D + static_cast<long long>(sA) * B * H, H, B};
     if ((st = launch_gemm<P, kHcltBN, EpiHcltFwd>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi,
                                                   mb.lo, num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD,
                                                   2ll * G * H * H * B)) != PC_OK)
@@ -517,7 +540,7 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       const int G = sB - sA;
       if (G <= 0) continue;
       k_hclt_scaled_flows<P><<<dim3(cdiv(H, 32), cdiv(B, 32), G), dim3(32, 8), 0, s>>>(
-          sA, H, B, d_pslot, w.F32, w.logD, w.Gbm.ptr, w.Gbm.ld, w.Gbm.lo_elems, w.Gnm.ptr, w.Gnm.ld,
+          sA, H, B, d_pslot, w.F32, w.D, w.Gbm.ptr, w.Gbm.ld, w.Gbm.lo_elems, w.Gnm.ptr, w.Gnm.ld,
           w.Gnm.lo_elems);
       PC_LAUNCH_CHECK();
       // element flows of the level's children

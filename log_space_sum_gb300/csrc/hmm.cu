@@ -308,6 +308,7 @@ struct EpiHmmFwd {
     float* U0;               // u_0 float32 [B][H] (t = 0 only)
   };
   static constexpr bool kTranspose = false;
+  static constexpr int kSliceBF16 = 0;
   // the 3xTF32 ring needs the room: it gathers emissions directly instead
   static constexpr bool kStageE = P != kTF32x3;
   static constexpr int kSmemBytes = kChainBN * 4 * 2 + (kStageE ? kChainBN * kBM * 4 : 0);

@@ -38,6 +38,21 @@ struct GemmShape {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
 };
 
+// Accumulation slices, in MMA k-steps (1, or a multiple of the k-steps of one ring
+// slot); see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
+// (Epi::kSliceBF16 k-steps; 0 = one accumulation over all of K).
+constexpr int kSliceK3x = 1;
+constexpr int kSliceK1 = 8;
+
+// The tensor core's float32 accumulator truncates toward zero. A slice of one 3xTF32
+// k-step ends in one such truncation at the slice's own magnitude, which drops the bits
+// below one ulp of the result: on average half an ulp when the dropped fraction is
+// uniform. half_ulp(v) = sign(v) 2^e 2^-24 for v = m 2^e (1 <= m < 2), the exponent and
+// sign bits of v scaled by 2^-24 (0 for zero and subnormal v).
+__device__ __forceinline__ float half_ulp(float v) {
+  return __uint_as_float(__float_as_uint(v) & 0xFF800000u) * 5.9604644775390625e-8f;
+}
+
 // Per epilogue warp: a padded 32 x 33 float tile for warp_transpose32.
 constexpr int kTBufFloats = 32 * 33;
 
@@ -99,23 +114,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 int num_kb, unsigned* status, const typename Epi::Params ep) {
   using S = GemmShape<P, BN>;
   constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
-  // TF32 modes: every K slice (kSliceKB ring slots) is accumulated from zero in one
-  // of two TMEM buffers and added into registers by the epilogue with round-to-
-  // nearest adds. The tensor-core accumulator truncates on every accumulation, so
-  // its bias grows with the number of MMAs summed into one value; slicing bounds
-  // that number whatever K is (3xTF32: one slot = 4 k-steps x 3 products, issued
-  // small cross terms first; TF32: four slots = 16 MMAs).
-  constexpr int kSliceKB = (P == kTF32x3) ? 1 : (P == kTF32 ? 4 : 0);
-  constexpr bool kSliced = kSliceKB > 0;
-  constexpr uint32_t kTmemCols = kSliced ? 2 * BN : BN;
+  // Sliced modes: every K slice (kSliceK k-steps of the MMA) is accumulated from zero in
+  // one of kAccBufs TMEM buffers and added into registers by the epilogue with round-to-
+  // nearest adds. The tensor-core accumulator truncates on every accumulation, so its
+  // bias grows with the number of MMAs summed into one value; slicing bounds that number
+  // whatever K is. A slice of one k-step (3xTF32: lo*hi, hi*lo, then hi*hi) ends in a
+  // single truncation at the slice's own magnitude, whose expected loss (half_ulp of the
+  // slice) the epilogue adds back to each slice.
+  constexpr int kSliceK = (P == kTF32x3) ? kSliceK3x : (P == kTF32 ? kSliceK1 : Epi::kSliceBF16);
+  constexpr bool kSliced = kSliceK > 0;
+  constexpr bool kStepSliced = kSliced && kSliceK < static_cast<int>(S::kKSteps);
+  static_assert(!kSliced || kStepSliced ? kSliceK <= 1 : kSliceK % S::kKSteps == 0,
+                "slices are one k-step or whole ring slots");
+  constexpr int kAccBufs = !kSliced ? 1 : (kStepSliced && 4 * BN <= 512 ? 4 : 2);
+  constexpr uint32_t kTmemCols = kAccBufs * BN;
+  static_assert(kTmemCols <= 512, "TMEM columns");
+  constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * S::kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;  // [2]
-  uint64_t* acc_empty = acc_full + 2;    // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_full = empty + kStages;  // [4]
+  uint64_t* acc_empty = acc_full + 4;    // [4]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 4);
   float* tbuf_base = reinterpret_cast<float*>(smem + kStages * S::kStageBytes + 256);
   uint8_t* epi_smem = reinterpret_cast<uint8_t*>(tbuf_base) + GemmPlan<P, BN, Epi>::kTBufBytes;
 
@@ -136,7 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);
       }
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < 4; ++b) {
         mbar_init(&acc_full[b], 1);
         mbar_init(&acc_empty[b], 1);
       }
@@ -183,26 +205,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       // -------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = umma_idesc(P == kBF16 ? 1u : 2u, kBM, BN);
+      const int total_q = num_kb * static_cast<int>(S::kKSteps);
+      int q = 0;  // k-steps issued so far
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = (kb / kStages) & 1;
-        const int slice = kSliced ? kb / (kSliceKB > 0 ? kSliceKB : 1) : 0;
-        const bool first = kSliced ? (kb % (kSliceKB > 0 ? kSliceKB : 1)) == 0 : kb == 0;
-        const bool last = kSliced && ((kb % (kSliceKB > 0 ? kSliceKB : 1)) == kSliceKB - 1 || kb == num_kb - 1);
+        // slot-granular slices: wait for this slice's buffer before the slot
+        const int slice = kSliced && !kStepSliced ? q / kSliceK : 0;
+        const bool first = kSliced ? (q % (kSliceK > 0 ? kSliceK : 1)) == 0 : kb == 0;
+        const bool last = kSliced && !kStepSliced &&
+                          ((q + static_cast<int>(S::kKSteps)) % (kSliceK > 0 ? kSliceK : 1) == 0 ||
+                           q + static_cast<int>(S::kKSteps) == total_q);
         uint32_t d = tmem;
-        if constexpr (kSliced) {
-          const int buf = slice & 1;
-          if (first && !mbar_wait(&acc_empty[buf], ((slice >> 1) & 1) ^ 1, status, kErrTimeoutMma)) break;
+        if constexpr (kSliced && !kStepSliced) {
+          const int buf = slice % kAccBufs;
+          if (first && !mbar_wait(&acc_empty[buf], ((slice / kAccBufs) & 1) ^ 1, status, kErrTimeoutMma)) break;
           d = tmem + static_cast<uint32_t>(buf * BN);
         }
         if (!mbar_wait(&full[s], ph, status, kErrTimeoutMma)) break;
         tc_fence_after();
         const uint32_t a0 = smem_addr(a_tile(s, 0));
         const uint32_t b0 = smem_addr(b_tile(s, 0));
-        if constexpr (P == kTF32x3) {
-          const uint32_t a1 = smem_addr(a_tile(s, 1));
-          const uint32_t b1 = smem_addr(b_tile(s, 1));
-          // the small cross terms first, then hi*hi, into the zeroed buffer
+        const uint32_t a1 = smem_addr(a_tile(s, P == kTF32x3 ? 1 : 0));
+        const uint32_t b1 = smem_addr(b_tile(s, P == kTF32x3 ? 1 : 0));
+        bool timed_out = false;
+        if constexpr (kStepSliced) {
+          // one slice per k-step, each into the next of kAccBufs buffers
+#pragma unroll
+          for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
+            const int sl = q + static_cast<int>(kk);
+            const int buf = sl % kAccBufs;
+            if (!mbar_wait(&acc_empty[buf], ((sl / kAccBufs) & 1) ^ 1, status, kErrTimeoutMma)) {
+              timed_out = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ds = tmem + static_cast<uint32_t>(buf * BN);
+            const uint32_t off = kk * 32;
+            if constexpr (P == kTF32x3) {
+              umma_tf32(ds, umma_desc_sw128(a1 + off), umma_desc_sw128(b0 + off), idesc, 0u);
+              umma_tf32(ds, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, 1u);
+              umma_tf32(ds, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, 1u);
+            } else {
+              umma_tf32(ds, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, 0u);
+            }
+            umma_commit(&acc_full[buf]);
+          }
+        } else if constexpr (P == kTF32x3) {
+          // the small cross terms of the slot first, then hi*hi
 #pragma unroll
           for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
             const uint32_t off = kk * 32;
@@ -228,7 +278,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         umma_commit(&empty[s]);
-        if (last) umma_commit(&acc_full[slice & 1]);
+        if (timed_out) break;
+        if (last) umma_commit(&acc_full[slice % kAccBufs]);
+        q += static_cast<int>(S::kKSteps);
       }
       // also on a timeout: the epilogue must not wait forever
       if constexpr (!kSliced) umma_commit(&acc_full[0]);
@@ -249,11 +301,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[c][i] = 0.f;
-      const int num_slices = (num_kb + kSliceKB - 1) / kSliceKB;
+      const int total_q = num_kb * static_cast<int>(S::kKSteps);
+      const int num_slices = (total_q + kSliceK - 1) / kSliceK;
       for (int sl = 0; sl < num_slices; ++sl) {
-        const int buf = sl & 1;
+        const int buf = sl % kAccBufs;
         // all 128 epilogue threads agree on whether the slice arrived
-        ok = epilogue_bar_and(mbar_wait(&acc_full[buf], (sl >> 1) & 1, status, kErrTimeoutEpilogue));
+        ok = epilogue_bar_and(
+            mbar_wait(&acc_full[buf], (sl / kAccBufs) & 1, status, kErrTimeoutEpilogue));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -261,7 +315,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float v[32];
           tmem_ld_32x32(lane_base + static_cast<uint32_t>(buf * BN + c * 32), v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c][i] += v[i];
+          for (int i = 0; i < 32; ++i) acc[c][i] += kHalfUlp ? v[i] + half_ulp(v[i]) : v[i];
         }
         tc_fence_before();
         epilogue_bar_sync();
@@ -269,7 +323,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) Epi::apply(ep, g, m0, n0, row, c * 32, acc[c], epi_smem, tbuf);
+        for (int c = 0; c < BN / 32; ++c) {
+          Epi::apply(ep, g, m0, n0, row, c * 32, acc[c], epi_smem, tbuf);
+        }
       }
     } else {
       ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue));
@@ -297,6 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Default hooks for epilogues that need no per-CTA set-up or reduction.
 struct EpiNoHooks {
   static constexpr int kSmemBytes = 0;
+  static constexpr int kSliceBF16 = 0;       // bf16 accumulation slice in k-steps (0 = none)
   static constexpr bool kTranspose = false;  // true: apply() uses warp_transpose32
   template <class Params>
   __device__ static void prepare(const Params&, int, int, int, int, uint8_t*) {}

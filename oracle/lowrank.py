@@ -64,7 +64,11 @@ def lowrank_exp_sum_fwd(theta, A, Bm, x):
 
 
 def lowrank_exp_sum_bwd(theta, A, Bm, x, f):
-    """Returns dA [B,M,K], dB [B,K,N], e [N,B], Fplus [M,N], W [M,N] (and out, logZ)."""
+    """Returns dA [B,M,K], dB [B,K,N], e [N,B], Fplus [M,N], W [M,N] (and out, logZ),
+    plus absdA = |f| (p + q) |B_b|^T and absdB = |A_b|^T |f| (p + q): the sums of the
+    absolute terms behind each gradient entry before any cancellation (D = f (p - q)
+    cancels within each entry and D's rows sum to zero), the scale against which the
+    error of a rounded evaluation is measured."""
     theta = np.asarray(theta, dtype=np.float64)
     A = np.asarray(A, dtype=np.float64)
     Bm = np.asarray(Bm, dtype=np.float64)
@@ -78,6 +82,8 @@ def lowrank_exp_sum_bwd(theta, A, Bm, x, f):
     e = np.empty((N, B))
     Fplus = np.zeros((M, N))
     Wst = np.zeros((M, N))
+    absdA = np.empty((B, M, K))
+    absdB = np.empty((B, K, N))
     out = np.empty((M, B))
     logZ = np.empty((B, M))
     for b in range(B):
@@ -90,7 +96,10 @@ def lowrank_exp_sum_bwd(theta, A, Bm, x, f):
         D = fb * (p - q)
         dA[b] = D @ Bm[b].T
         dB[b] = A[b].T @ D
+        Dmag = np.abs(fb) * (p + q)
+        absdA[b] = Dmag @ np.abs(Bm[b]).T
+        absdB[b] = np.abs(A[b]).T @ Dmag
         e[:, b] = (fb * p).sum(axis=0)
         Fplus += fb * p
         Wst += fb * g / Z[:, None]
-    return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=Wst, out=out, logZ=logZ)
+    return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=Wst, out=out, logZ=logZ, absdA=absdA, absdB=absdB)

@@ -86,7 +86,7 @@ def test_hclt_768_sampled_and_invariants(hclt_full, mode):
     d = hclt_full
     ll, dpi, dW, dE = _gpu_run(d, mode)
     B, n = d["data"].shape
-    pick = np.random.default_rng(210).choice(B, size=4, replace=False)
+    pick = np.random.default_rng(210).choice(B, size=16, replace=False)
     ref = hclt_ll(d["parent"], d["data"][pick], d["pi"], d["W"], d["E"])
     err = ll_err(ll[pick], ref)
     print(f"hclt 768 {mode}: sampled ll err {err:.3e}")
@@ -97,6 +97,14 @@ def test_hclt_768_sampled_and_invariants(hclt_full, mode):
     np.testing.assert_allclose(dE.astype(np.float64).sum(axis=(1, 2)), B, rtol=tol)
 
 
+# With uniform emissions every node's values are equal across the latents up to rounding,
+# so u = n / max n sits just below 1, where rounding the operand to bf16 or TF32 is
+# one-sided: a value within half a spacing below 1 (2^-9 for bf16, 2^-12 for TF32) becomes
+# 1. Each of the n - 1 edges can gain that much relative mass at most; fp32 (3xTF32) keeps
+# the stated bar.
+UNIFORM_EDGE_BOUND = {"auto": 2.0 ** -9, "tf32": 2.0 ** -12, "fp32": 0.0}
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_hclt_768_uniform_emissions(hclt_full, mode):
     d = dict(hclt_full)
@@ -104,6 +112,9 @@ def test_hclt_768_uniform_emissions(hclt_full, mode):
     ll, *_ = _gpu_run(d, mode, flows=False)
     W = d["W"].astype(np.float64)
     pi = d["pi"].astype(np.float64)
+    n = len(d["parent"])
     # the float32 rows of W and pi sum to 1 only to ~1e-7; bound their effect on LL
     slack = np.abs(np.log(W[1:].sum(-1))).max(axis=1).sum() + abs(np.log(pi.sum()))
-    assert np.abs(ll + 768 * np.log(512)).max() <= LL_TOL[mode] + slack
+    err = np.abs(ll + n * np.log(512)).max()
+    print(f"hclt 768 uniform {mode}: ll err {err:.3e}")
+    assert err <= LL_TOL[mode] + (n - 1) * UNIFORM_EDGE_BOUND[mode] + slack

@@ -102,3 +102,13 @@ def test_spread_recipe():
     d = lowrank_inputs(256, 256, 16, 4, 4.0, seed=8)
     S = np.einsum("bik,bkj->bij", d["A"].astype(np.float64), d["Bm"].astype(np.float64))
     assert 3.6 < S.std() < 4.4
+
+
+def test_gradient_magnitudes_bound_gradients():
+    th, A, Bm, x, f = _inputs(6, 7, 3, 2, 1.0, seed=44)
+    r = lowrank_exp_sum_bwd(th, A, Bm, x, f)
+    assert np.all(np.abs(r["dA"]) <= r["absdA"] * (1 + 1e-12))
+    assert np.all(np.abs(r["dB"]) <= r["absdB"] * (1 + 1e-12))
+    # with A = 0, |A|^T |f| (p + q) vanishes with dB
+    r0 = lowrank_exp_sum_bwd(th, np.zeros_like(A), Bm, x, f)
+    assert np.all(r0["absdB"] == 0)
