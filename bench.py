@@ -1,18 +1,25 @@
-"""Benchmark of the HMM circuit forward + backward (log-likelihood and EM flows).
+"""Benchmark of the hot path: forward + backward of the HMM circuit (the headline), and
+of the single sum layer, the HCLT circuit and the LowRank exp_sum layer.
 
-Workload: HMM with 4096 latent states, 32 positions, vocabulary 1024, batch 512
-(pyjuice PR #62, Results table), synthetic seeded inputs (workloads.hmm(512)).
-One step = one pc_hmm_fwd_bwd call: 31 tied 4096x4096 sum layers forward, the 31
-element-flow contractions backward and the depth-15872 parameter-flow contraction.
+Workloads (synthetic, seeded; see workloads/):
+  hmm      HMM with 4096 latent states, 32 positions, vocabulary 1024, batch 512
+           (pyjuice PR #62, Results table). One step = one pc_hmm_fwd_bwd call: 31 tied
+           4096x4096 sum layers forward, the 31 element-flow contractions backward and
+           the depth-15872 parameter-flow contraction.
+  layer    one dense sum layer M = N = 1024, batch 128: pc_sum_layer_fwd + _bwd.
+  hclt     HCLT, 768 variables, 1024 latents, 512 categories, batch 512: pc_hclt_fwd_bwd.
+  lowrank  LowRank exp_sum layer M = N = 1024, rank 16, batch 64, scale spread 1 nat:
+           pc_lowrank_exp_sum_fwd + _bwd (dA, dB, e, F+, W).
 
-python bench.py [--gpus N --steps K --warmup W --precision auto|tf32|fp32 --impl ours|reference]
+python bench.py [--gpus N --steps K --warmup W --precision auto|tf32|fp32
+                 --impl ours|reference --workload hmm|layer|hclt|lowrank]
 
-Prints one JSON line (rank 0). Under torchrun each rank runs its own batch of 512
-(weak scaling; no data-path collective). Between timed steps a 256 MiB buffer is
-written to flush the 126 MB L2. The roofline entry times every tensor-core
-contraction of the timed region with CUDA events recorded by the library on the
-launching stream (pc_profile_start/stop). ``--impl reference`` times the float64
-CPU oracle on a bounded sample of the same workload.
+Prints one JSON line (rank 0). Under torchrun each rank runs its own batch (weak
+scaling; no data-path collective). Between timed steps a 256 MiB buffer is written to
+flush the 126 MB L2. The roofline entry times the dominant kernel kind of the timed
+region with CUDA events recorded by the library on the launching stream
+(pc_profile_start/stop). ``--impl reference`` times the float64 CPU oracle on a
+bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -29,16 +36,16 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "HMM 4096x32 fwd+bwd samples/s @batch 512 (1 GB300); % tensor/HBM roofline"
 UNIT = "samples/s"
-H, T, V, B = 4096, 32, 1024, 512
-# pages' RTX PRO 6000 figures for this exact workload (context, other hardware)
+HMM_METRIC = "HMM 4096x32 fwd+bwd samples/s @batch 512 (1 GB300); % tensor/HBM roofline"
+# pages' RTX PRO 6000 figures for the HMM workload (context, other hardware)
 PAGES_SAMPLES_PER_S = {"auto": 512 / 32.1e-3, "fp32": 512 / 49.9e-3}
-WORKLOAD = "HMM 4096 latents x 32 positions, vocab 1024, batch 512: forward LL + backward flows dpi, dA, dE"
 DTYPE = {"auto": "bf16", "tf32": "tf32", "fp32": "3xtf32"}
 # nominal dense tensor rates relative to bf16 (2.25 PF bf16, 1.1 PF tf32)
 TF32_OVER_BF16 = 1.1 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# special-function unit: 16 exp2 results per SM per clock, 152 SMs (GB300)
+MUFU_PER_SM_CLK, N_SMS = 16, 152
 
 
 def parse():
@@ -49,6 +56,7 @@ def parse():
     ap.add_argument("--precision", default="auto", choices=["auto", "tf32", "fp32"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="hmm", choices=["hmm", "layer", "hclt", "lowrank"])
     return ap.parse_args()
 
 
@@ -68,26 +76,203 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# ------------------------------------------------------------------ CPU oracle
-def oracle_sample_rate(target_s: float = 12.0):
-    """The float64 oracle on a bounded sample of the workload: returns (samples/s,
-    description, cores). The sample is the first b samples of the batch, b grown
-    until one run takes about target_s seconds (capped at 64 samples)."""
-    import numpy as np  # noqa: F401
-    from oracle.hmm import hmm_fwd_bwd
-    from workloads import hmm
+# ------------------------------------------------------------------ workloads
+class Workload:
+    """One benchmarked call sequence: its inputs (numpy, seeded), the GPU step through
+    the public API on device-resident tensors, and the oracle on the first b samples."""
 
-    d = hmm(512)
-    b = 4
+    name = metric = desc = ""
+    batch = 0
+    roofline_bound = "tensor"
+
+    def config(self):
+        return {}
+
+
+class HmmWorkload(Workload):
+    name, metric, batch = "hmm", HMM_METRIC, 512
+    desc = "HMM 4096 latents x 32 positions, vocab 1024, batch 512: forward LL + backward flows dpi, dA, dE"
+    data = "synthetic (seeded: softmax N(0,1) rows for pi, A, E; uniform tokens)"
+
+    def inputs(self):
+        from workloads import hmm
+        return hmm(512)
+
+    def config(self):
+        return {"H": 4096, "T": 32, "V": 1024, "B": 512}
+
+    def oracle(self, d, b):
+        from oracle.hmm import hmm_fwd_bwd
+        hmm_fwd_bwd(d["pi"], d["A"], d["E"], d["tokens"][:b])
+
+    def device(self, pc, d, dev, prec):
+        import torch
+        t = {k: torch.from_numpy(d[k]).to(dev) for k in ("tokens", "pi", "A", "E")}
+        H, V = d["E"].shape
+        out = dict(ll=torch.empty(self.batch, dtype=torch.float64, device=dev),
+                   dpi=torch.empty(H, device=dev), dA=torch.empty(H, H, device=dev), dE=torch.empty(H, V, device=dev))
+
+        def step(tok=None):
+            pc.hmm_fwd_bwd(t["tokens"] if tok is None else tok, t["pi"], t["A"], t["E"], precision=prec, **out)
+        host_in = torch.from_numpy(d["tokens"]).pin_memory()
+        host_out = torch.empty(self.batch, dtype=torch.float64).pin_memory()
+        dev_in = torch.empty_like(t["tokens"])
+
+        def e2e():
+            dev_in.copy_(host_in, non_blocking=True)
+            step(dev_in)
+            host_out.copy_(out["ll"], non_blocking=True)
+        return step, e2e, host_in.numel() * 4, host_out.numel() * 8
+
+
+class LayerWorkload(Workload):
+    name, batch = "layer", 128
+    metric = "sum layer 1024x1024 fwd+bwd samples/s @batch 128 (1 GB300)"
+    desc = "dense sum layer M = N = 1024, batch 128: forward out + backward element flows e and parameter flows F"
+    data = "synthetic (seeded: softmax N(0,1) theta rows; x log-softmax of N(0,9) logits; f = 1)"
+
+    def inputs(self):
+        from workloads import layer
+        return layer()
+
+    def config(self):
+        return {"M": 1024, "N": 1024, "B": 128}
+
+    def oracle(self, d, b):
+        from oracle.sum_layer import sum_layer_bwd, sum_layer_fwd
+        th = d["theta"].astype("float64")
+        x = d["x"][:, :b].astype("float64")
+        out = sum_layer_fwd(th, x)
+        sum_layer_bwd(th, x, 0, out, d["f"][:, :, :b].astype("float64"))
+
+    def device(self, pc, d, dev, prec):
+        import torch
+        th = torch.from_numpy(d["theta"]).to(dev)
+        x = torch.from_numpy(d["x"]).to(dev)
+        f = torch.from_numpy(d["f"]).to(dev)
+        out = torch.empty(1, 1024, self.batch, device=dev)
+        e = torch.zeros_like(x)
+        F = torch.empty_like(th)
+
+        def step(xin=None):
+            xx = x if xin is None else xin
+            pc.sum_layer_fwd(th, xx, precision=prec, out=out)
+            pc.sum_layer_bwd(th, xx, out, f, precision=prec, e=e, F=F)
+        host_in = torch.from_numpy(d["x"]).pin_memory()
+        host_out = torch.empty(1024, self.batch).pin_memory()
+        dev_in = torch.empty_like(x)
+
+        def e2e():
+            dev_in.copy_(host_in, non_blocking=True)
+            step(dev_in)
+            host_out.copy_(out[0], non_blocking=True)
+        return step, e2e, host_in.numel() * 4, host_out.numel() * 4
+
+
+class HcltWorkload(Workload):
+    name, batch = "hclt", 512
+    metric = "HCLT 768 vars x 1024 latents fwd+bwd samples/s @batch 512 (1 GB300)"
+    desc = ("HCLT 768 variables, 1024 latents, 512 categories, random tree, batch 512: forward LL + backward "
+            "flows dpi, dW, dE")
+    data = "synthetic (seeded: parent[i] ~ U[0, i); softmax N(0,1) rows for pi, W, E; uniform categories)"
+
+    def inputs(self):
+        from workloads import hclt
+        return hclt()
+
+    def config(self):
+        return {"nvars": 768, "H": 1024, "C": 512, "B": 512}
+
+    def oracle(self, d, b):
+        from oracle.hclt import hclt_fwd_bwd
+        hclt_fwd_bwd(d["parent"], d["data"][:b], d["pi"], d["W"], d["E"])
+
+    def device(self, pc, d, dev, prec):
+        import torch
+        t = {k: torch.from_numpy(d[k]).to(dev) for k in ("data", "pi", "W", "E")}
+        n, H, C = d["E"].shape
+        out = dict(ll=torch.empty(self.batch, dtype=torch.float64, device=dev), dpi=torch.empty(H, device=dev),
+                   dW=torch.empty(n, H, H, device=dev), dE=torch.empty(n, H, C, device=dev))
+
+        def step(data=None):
+            pc.hclt_fwd_bwd(d["parent"], t["data"] if data is None else data, t["pi"], t["W"], t["E"],
+                            precision=prec, **out)
+        host_in = torch.from_numpy(d["data"]).pin_memory()
+        host_out = torch.empty(self.batch, dtype=torch.float64).pin_memory()
+        dev_in = torch.empty_like(t["data"])
+
+        def e2e():
+            dev_in.copy_(host_in, non_blocking=True)
+            step(dev_in)
+            host_out.copy_(out["ll"], non_blocking=True)
+        return step, e2e, host_in.numel() * 4, host_out.numel() * 8
+
+
+class LowRankWorkload(Workload):
+    name, batch = "lowrank", 64
+    metric = "LowRank exp_sum 1024x1024 rank 16 fwd+bwd samples/s @batch 64 (1 GB300); % exp-unit roofline"
+    desc = ("LowRank exp_sum layer M = N = 1024, rank 16, batch 64, scale spread 1 nat: forward out, logZ + "
+            "backward dA, dB, e, F+, W")
+    data = "synthetic (seeded: softmax N(0,1) theta rows; A, B ~ N(0, s^2); x log-softmax of N(0,9) logits; f = 1)"
+    roofline_bound = "alu"
+
+    def inputs(self):
+        from workloads import lowrank
+        return lowrank(1.0)
+
+    def config(self):
+        return {"M": 1024, "N": 1024, "K": 16, "B": 64, "spread": 1.0}
+
+    def oracle(self, d, b):
+        from oracle.lowrank import lowrank_exp_sum_bwd
+        lowrank_exp_sum_bwd(d["theta"], d["A"][:b], d["Bm"][:b], d["x"][:, :b], d["f"][:, :b])
+
+    def device(self, pc, d, dev, prec):
+        import torch
+        t = {k: torch.from_numpy(d[k]).to(dev) for k in ("theta", "A", "Bm", "x", "f")}
+        M, N = d["theta"].shape
+        Bs, _, K = d["A"].shape
+        out = torch.empty(M, Bs, device=dev)
+        logZ = torch.empty(Bs, M, device=dev)
+        g = dict(dA=torch.empty(Bs, M, K, device=dev), dB=torch.empty(Bs, K, N, device=dev),
+                 e=torch.empty(N, Bs, device=dev), Fplus=torch.empty(M, N, device=dev), W=torch.empty(M, N, device=dev))
+
+        def step(A=None, Bm=None):
+            A = t["A"] if A is None else A
+            Bm = t["Bm"] if Bm is None else Bm
+            pc.lowrank_exp_sum_fwd(t["theta"], A, Bm, t["x"], precision=prec, out=out, logZ=logZ)
+            pc.lowrank_exp_sum_bwd(t["theta"], A, Bm, t["x"], out, logZ, t["f"], precision=prec, **g)
+        hA = torch.from_numpy(d["A"]).pin_memory()
+        hB = torch.from_numpy(d["Bm"]).pin_memory()
+        h_out = torch.empty(M, Bs).pin_memory()
+        dA_in, dB_in = torch.empty_like(t["A"]), torch.empty_like(t["Bm"])
+
+        def e2e():
+            dA_in.copy_(hA, non_blocking=True)
+            dB_in.copy_(hB, non_blocking=True)
+            step(dA_in, dB_in)
+            h_out.copy_(out, non_blocking=True)
+        return step, e2e, (hA.numel() + hB.numel()) * 4, h_out.numel() * 4
+
+
+WORKLOADS = {w.name: w for w in (HmmWorkload(), LayerWorkload(), HcltWorkload(), LowRankWorkload())}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample_rate(w, d, target_s: float = 12.0):
+    """The float64 oracle on a bounded sample of the workload: returns (samples/s,
+    description, cores, b, seconds). The sample is the first b samples of the batch, b
+    grown until one run takes about target_s seconds (at most the whole batch)."""
+    b = 1
     while True:
         t0 = time.perf_counter()
-        hmm_fwd_bwd(d["pi"], d["A"], d["E"], d["tokens"][:b])
+        w.oracle(d, b)
         dt = time.perf_counter() - t0
-        if dt >= target_s / 2 or b >= 64:
+        if dt >= target_s / 2 or b >= w.batch:
             break
-        b = min(64, max(b * 2, int(b * target_s / max(dt, 1e-3))))
-    desc = (f"float64 NumPy oracle (oracle.hmm.hmm_fwd_bwd): LL + dpi, dA, dE for the first {b} "
-            f"of the 512 samples of the same workload, {dt:.1f} s")
+        b = min(w.batch, max(b * 2, int(b * target_s / max(dt, 1e-3))))
+    desc = (f"float64 NumPy oracle ({w.name}): the same forward + backward for the first {b} of the "
+            f"{w.batch} samples of the workload, {dt:.1f} s")
     return b / dt, desc, os.cpu_count(), b, dt
 
 
@@ -95,26 +280,21 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    from oracle.hmm import hmm_fwd_bwd
-    from workloads import hmm
-
-    d = hmm(512)
-    rate, desc, cores, b, _ = oracle_sample_rate(target_s=8.0)
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; the sizing run above served as one
+    w = WORKLOADS[args.workload]
+    d = w.inputs()
+    rate, desc, cores, b, _ = oracle_sample_rate(w, d, target_s=8.0)
     times = []
-    for _ in range(args.steps):
+    for _ in range(args.steps):  # the sizing run above served as the warm-up
         t0 = time.perf_counter()
-        hmm_fwd_bwd(d["pi"], d["A"], d["E"], d["tokens"][:b])
+        w.oracle(d, b)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     value = b / (ms / 1e3)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": w.metric, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD + f" (oracle on {b}-sample slices)", "H": H, "T": T, "V": V,
-                   "B": B, "sample_batch": b},
+        "config": {"workload": w.desc + f" (oracle on {b}-sample slices)", **w.config(), "sample_batch": b},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -195,14 +375,12 @@ def recorded_traffic(kind: str, precision: str):
 
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
     import log_space_sum_gb300 as pc
-    from log_space_sum_gb300 import _native as N
-    from workloads import hmm
 
+    w = WORKLOADS[args.workload]
     rank, world, local = dist_env()
     if world > 1:
         torch.cuda.set_device(local)
@@ -211,20 +389,10 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     lib = pc.load()
 
-    d = hmm(512)
-    tok = torch.from_numpy(d["tokens"]).to(dev)
-    pi = torch.from_numpy(d["pi"]).to(dev)
-    A = torch.from_numpy(d["A"]).to(dev)
-    E = torch.from_numpy(d["E"]).to(dev)
-    ll = torch.empty(B, dtype=torch.float64, device=dev)
-    dpi = torch.empty(H, dtype=torch.float32, device=dev)
-    dA = torch.empty(H, H, dtype=torch.float32, device=dev)
-    dE = torch.empty(H, V, dtype=torch.float32, device=dev)
+    d = w.inputs()
+    step, e2e_step, h2d_bytes, d2h_bytes = w.device(pc, d, dev, args.precision)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        pc.hmm_fwd_bwd(tok, pi, A, E, precision=args.precision, ll=ll, dpi=dpi, dA=dA, dE=dE)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -245,28 +413,30 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     launches0 = lib.pc_launch_count()
-    pc.profile_start(200 * args.steps)
+    cap = 2000 * args.steps
+    pc.profile_start(cap)
     for i in range(args.steps):
         flush.random_(0, 255) if i == 0 else flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
-    prof = pc.profile_stop(200 * args.steps)
+    prof = pc.profile_stop(cap)
     torch.cuda.synchronize(dev)
     launches = lib.pc_launch_count() - launches0
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
+    pc.device_status(dev)
     ms_steps = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(ms_steps)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    total_ms = float(tt.item())
     ms_per_step = total_ms / args.steps
-    value = world * B * args.steps / (total_ms / 1e3)
+    value = world * w.batch * args.steps / (total_ms / 1e3)
 
-    # ---- roofline of the dominant contraction (by total time in the timed region)
+    # ---- roofline of the dominant kernel kind (by total time in the timed region)
     peaks, peak_src = load_peaks()
     by_kind = {}
     for kind, ms, fl in prof:
@@ -276,64 +446,75 @@ def run_ours(args):
         k[2] += 1
     dom = max(by_kind, key=lambda k: by_kind[k][0])
     dms, dfl, dn = by_kind[dom]
-    achieved = dfl / (dms / 1e3) / 1e12
-    bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    peak = bf16_peak if args.precision == "auto" else bf16_peak * TF32_OVER_BF16
-    roofline = {
-        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-        "traffic": recorded_traffic(dom, args.precision), "kernel": f"k_umma_gemm ({dom})",
-        "launches_timed": dn, "ms_per_launch": dms / dn,
-        "peak_source": f"{peak_src} bf16 sustained" + ("" if args.precision == "auto" else " x 1.1/2.25 (nominal tf32/bf16)"),
-        "all_contractions_frac": sum(v[1] for v in by_kind.values()) / (sum(v[0] for v in by_kind.values()) / 1e3) / 1e12 / peak,
-        "share_of_step": sum(v[0] for v in by_kind.values()) / total_ms if world == 1 else None,
-    }
-    if args.precision == "fp32":
-        roofline["issued_frac"] = 3 * achieved / peak
+    if w.roofline_bound == "alu":
+        # one exp per (sample, node, child) in every LowRank pass
+        cfg = w.config()
+        exps = cfg["M"] * cfg["N"] * cfg["B"]
+        mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+        peak = N_SMS * MUFU_PER_SM_CLK * mhz * 1e6 / 1e12
+        achieved = exps * dn / (dms / 1e3) / 1e12
+        roofline = {
+            "bound": "alu", "achieved": achieved, "peak": peak, "unit": "Texp/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(dom, args.precision), "kernel": f"k_lowrank* ({dom})",
+            "launches_timed": dn, "ms_per_launch": dms / dn,
+            "peak_source": f"derived: {N_SMS} SMs x {MUFU_PER_SM_CLK} exp/clk x {mhz:.0f} MHz",
+            "share_of_step": sum(v[0] for v in by_kind.values()) / total_ms if world == 1 else None,
+        }
+    else:
+        achieved = dfl / (dms / 1e3) / 1e12
+        bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        peak = bf16_peak if args.precision == "auto" else bf16_peak * TF32_OVER_BF16
+        roofline = {
+            "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(dom, args.precision), "kernel": f"k_umma_gemm ({dom})",
+            "launches_timed": dn, "ms_per_launch": dms / dn,
+            "peak_source": f"{peak_src} bf16 sustained" + ("" if args.precision == "auto"
+                                                           else " x 1.1/2.25 (nominal tf32/bf16)"),
+            "all_contractions_frac": sum(v[1] for v in by_kind.values()) / (sum(v[0] for v in by_kind.values())
+                                                                           / 1e3) / 1e12 / peak,
+            "share_of_step": sum(v[0] for v in by_kind.values()) / total_ms if world == 1 else None,
+        }
+        if args.precision == "fp32":
+            roofline["issued_frac"] = 3 * achieved / peak
 
-    # ---- end to end through the public API with host buffers
-    tok_host = torch.from_numpy(d["tokens"]).pin_memory()
-    ll_host = torch.empty(B, dtype=torch.float64).pin_memory()
-    tok_dev = torch.empty_like(tok)
+    # ---- end to end through the public API with pinned host buffers
     e2e_ms = []
     for i in range(max(3, min(args.steps, 10))):
         flush.fill_(i & 0xFF)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        tok_dev.copy_(tok_host, non_blocking=True)
-        pc.hmm_fwd_bwd(tok_dev, pi, A, E, precision=args.precision, ll=ll, dpi=dpi, dA=dA, dE=dE)
-        ll_host.copy_(ll, non_blocking=True)
+        e2e_step()
         torch.cuda.synchronize(dev)
         e2e_ms.append(1e3 * (time.perf_counter() - t0))
     e2e_t = torch.tensor([statistics.mean(e2e_ms)], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = world * B / (float(e2e_t.item()) / 1e3)
+    e2e_value = world * w.batch / (float(e2e_t.item()) / 1e3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, cores, b, dt = oracle_sample_rate()
+        rate, desc, cores, b, dt = oracle_sample_rate(w, d)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
-        ref = PAGES_SAMPLES_PER_S.get(args.precision)
+        ref = PAGES_SAMPLES_PER_S.get(args.precision) if w.name == "hmm" else None
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": w.metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": (value / world / ref) if ref else None,
-            "dtype": DTYPE[args.precision],
-            "data": "synthetic (seeded: softmax N(0,1) rows for pi, A, E; uniform tokens)",
-            "config": {"workload": WORKLOAD, "H": H, "T": T, "V": V, "B": B, "precision": args.precision,
+            "dtype": DTYPE[args.precision], "data": w.data,
+            "config": {"workload": w.desc, **w.config(), "precision": args.precision,
                        "l2": "flushed between timed steps (256 MiB write)", "launch": "eager stream",
                        "parallelism": f"replicas x{world}"},
             "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(tok_host.numel() * 4),
-                    "d2h_bytes_per_step": int(ll_host.numel() * 8)},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d_bytes),
+                    "d2h_bytes_per_step": int(d2h_bytes)},
             "gpu_launches": int(launches),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "step_ms": {"min": min(ms_steps), "median": statistics.median(ms_steps), "max": max(ms_steps)},
-            "contractions": {k: {"launches": v[2], "ms": v[0], "tflops": v[1] / (v[0] / 1e3) / 1e12}
-                             for k, v in by_kind.items()},
+            "kernels": {k: {"launches": v[2], "ms": v[0], "tflops": v[1] / (v[0] / 1e3) / 1e12}
+                        for k, v in by_kind.items()},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -34,6 +34,7 @@ constexpr int kLrRows = 128;   // own rows per CTA (TMEM lanes)
 constexpr int kLrChunk = 32;   // sweep columns per MMA group
 constexpr int kLrThreads = 128;
 constexpr int kLrMaxRank = 64;
+constexpr int kGradAccs = 4;   // TMEM accumulators of the gradient contractions
 
 enum LrMode : int { kLrFwd = 0, kLrGradA = 1, kLrGradB = 2 };
 
@@ -275,6 +276,12 @@ __global__ void __launch_bounds__(kLrThreads, 1)
   const TileGeo gd = tile_geo(GF, kLrRows, kLrChunk), gg = tile_geo(GF, Kp, kLrChunk);
   const int kf = go.ksteps * fmt_kstep(SF);  // K padded to whole k-steps (zeros)
   const LrSmem L = lr_smem(P, kGrad, K, 1);
+  // TMEM: two 32-column S slots, then (gradients) kGradAccs accumulators of gstride
+  // columns that the chunks take in turn: each sums a quarter of the sweep, which keeps
+  // the accumulator's truncations to a quarter; the epilogue adds them up.
+  const int gstride = (Kp + 31) & ~31;
+  const uint32_t tcols = !kGrad ? 64u : (64 + kGradAccs * gstride <= 128 ? 128u
+                                         : (64 + kGradAccs * gstride <= 256 ? 256u : 512u));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(kLrThreads, 1)
       tma_prefetch_map(&tmTheta);
     }
     __syncwarp();
-    tmem_alloc(tslot, 128);
+    tmem_alloc(tslot, tcols);
   }
   // own operand: A_b rows (forward, grad A) or B_b^T rows (grad B)
   for (int idx = t; idx < kLrRows * kf; idx += kLrThreads) {
@@ -489,7 +496,8 @@ __global__ void __launch_bounds__(kLrThreads, 1)
     if (!ok) break;
     if (kGrad && t == 0) {
       tc_fence_after();
-      lr_mma<GF>(tmem + 64u, d_tile(sl), gd, gb_tile(sl), gg, Kp, c > 0);
+      lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(sl), gd, gb_tile(sl), gg,
+                 Kp, c >= kGradAccs);
       umma_commit(&mbG[sl]);
       g_issued = c;
     }
@@ -511,8 +519,15 @@ __global__ void __launch_bounds__(kLrThreads, 1)
     } else {
       tc_fence_after();
       float acc[64];
-      tmem_ld_32x32(lane_base + 64u, *reinterpret_cast<float(*)[32]>(acc));
-      if (Kp > 32) tmem_ld_32x32(lane_base + 96u, *reinterpret_cast<float(*)[32]>(acc + 32));
+      for (int r = 0; r < 64; ++r) acc[r] = 0.f;
+      for (int q = 0; q < kGradAccs && q < nch; ++q) {
+        for (int c0 = 0; c0 < Kp; c0 += 32) {
+          float v[32];
+          tmem_ld_32x32(lane_base + static_cast<uint32_t>(64 + q * gstride + c0), v);
+#pragma unroll
+          for (int r = 0; r < 32; ++r) acc[c0 + r] += v[r];
+        }
+      }
       if (own < own_n) {
         if constexpr (Mode == kLrGradA) {
           float* dst = a.dA + (static_cast<long long>(b) * a.M + own) * K;
@@ -543,7 +558,7 @@ __global__ void __launch_bounds__(kLrThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, tcols);
   }
 }
 
