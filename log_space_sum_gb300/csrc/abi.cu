@@ -97,7 +97,7 @@ unsigned* device_status_word() {
 }
 
 pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision_t p,
-                               int box_rows, int part) {
+                               int box_rows, int part, bool swizzle) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -116,7 +116,8 @@ pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision
   const CUresult r = g_encode(map, p == PC_PREC_AUTO ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                               3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return set_error(PC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %lldx%lldx%lld operand",

@@ -23,6 +23,7 @@
 //   grad B   own j, sweep i:  S^T = B^T A^T, D^T row-tile, dB^T += D^T A, e_j in registers
 //   stats    own i, fixed 32 columns, sweep the samples: F+ and W in registers
 // No pass needs an atomic: every output element is written by exactly one thread.
+#include <algorithm>
 #include <cmath>
 
 #include "pc_launch.cuh"
@@ -136,10 +137,10 @@ __device__ __forceinline__ void lr_mma(uint32_t d, const uint8_t* a, const TileG
 }
 
 // ------------------------------------------------------------------ set-up kernels
-// Per sample b: m_b = max_j x[j,b] and u[b][j] = exp(x[j,b] - m_b) (sample-major). One
-// block per sample.
+// Per sample b: m_b = max_j x[j,b] and u[b][j] = exp(x[j,b] - m_b) (sample-major, rows
+// ldu apart). One block per sample.
 __global__ void k_lr_colmax_u(int N, int B, const float* __restrict__ x, float* __restrict__ m,
-                              float* __restrict__ u) {
+                              float* __restrict__ u, long long ldu) {
   __shared__ float red[32];
   const int b = blockIdx.x;
   float mx = -INFINITY;
@@ -156,7 +157,7 @@ __global__ void k_lr_colmax_u(int N, int B, const float* __restrict__ x, float* 
   mx = red[0];
   if (threadIdx.x == 0) m[b] = mx;
   for (int j = threadIdx.x; j < N; j += blockDim.x)
-    u[static_cast<long long>(b) * N + j] =
+    u[static_cast<long long>(b) * ldu + j] =
         mx > -INFINITY ? expf(x[static_cast<long long>(j) * B + b] - mx) : 0.f;
 }
 
@@ -185,10 +186,11 @@ __global__ void k_lr_theta_copy(int M, int N, const float* __restrict__ theta, f
 }
 
 // Per (b, i): the backward's row factors lz = log Z_b[i], f_i and fc = f_i exp(m_b - out_i)
-// (0 where out or log Z is -inf: such a node passes no flow), sample-major [B][M].
+// (0 where out or log Z is -inf: such a node passes no flow), sample-major [B][ldm].
 __global__ void k_lr_row_factors(int M, int B, const float* __restrict__ out, const float* __restrict__ f,
                                  const float* __restrict__ logZ, const float* __restrict__ m,
-                                 float* __restrict__ rf_lz, float* __restrict__ rf_f, float* __restrict__ rf_fc) {
+                                 float* __restrict__ rf_lz, float* __restrict__ rf_f, float* __restrict__ rf_fc,
+                                 long long ldm) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(M) * B) return;
   const int b = static_cast<int>(idx / M), i = static_cast<int>(idx % M);
@@ -196,52 +198,120 @@ __global__ void k_lr_row_factors(int M, int B, const float* __restrict__ out, co
   const float lz = logZ[idx];
   const float fi = f[static_cast<long long>(i) * B + b];
   const bool live = o > -INFINITY && lz > -INFINITY && m[b] > -INFINITY;
-  rf_lz[idx] = lz;
-  rf_f[idx] = live ? fi : 0.f;
-  rf_fc[idx] = live ? fi * expf(m[b] - o) : 0.f;
+  const long long dst = static_cast<long long>(b) * ldm + i;
+  rf_lz[dst] = lz;
+  rf_f[dst] = live ? fi : 0.f;
+  rf_fc[dst] = live ? fi * expf(m[b] - o) : 0.f;
+}
+
+// Operand copy in format F: dst[g][r][c] (rows ld elements apart, zero beyond C) =
+// src[g*sg + r*sr + c*sc], rounded to bf16 / TF32 (hi, and lo = the rounded remainder).
+template <int F>
+__global__ void k_lr_to_op(const float* __restrict__ src, long long sg, long long sr, long long sc, int G, int R,
+                           int C, void* __restrict__ hi, void* __restrict__ lo, long long ld) {
+  const long long n = static_cast<long long>(G) * R * ld;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long c = idx % ld, gr = idx / ld;
+    const long long r = gr % R, g = gr / R;
+    const float v = c < C ? src[g * sg + r * sr + c * sc] : 0.f;
+    if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(v);
+      static_cast<__nv_bfloat16*>(hi)[idx] = h;
+      if constexpr (F == kFmtBF16x2) static_cast<__nv_bfloat16*>(lo)[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
+    } else {
+      const float h = tf32_rna(v);
+      static_cast<float*>(hi)[idx] = h;
+      if constexpr (F == kFmtTF32x2) static_cast<float*>(lo)[idx] = tf32_rna(v - h);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ shared memory plan
-// Byte offsets inside the (1024-aligned) dynamic shared memory of the LowRank kernels.
-struct LrSmem {
-  int own, sw, sw_bytes, theta, d, d_bytes, gb, gb_bytes, small, total;
-};
+enum : int { kLrStats = 3 };
 constexpr int kThetaTileBytes = kLrRows * 128;  // 128 rows x 32 floats
-__host__ __device__ inline LrSmem lr_smem(int P, bool grad, int K, int own_bufs) {
+constexpr int kLrWarps = 8;                      // two warps per TMEM lane quarter
+constexpr int kLrThreadsAll = kLrWarps * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ constexpr int lr_stages(int mode) { return mode == kLrFwd ? 3 : 4; }
+__host__ __device__ constexpr int lr_nvec(int mode) { return mode == kLrGradB ? 3 : 1; }
+
+// Byte offsets inside the (1024-aligned) dynamic shared memory. Every TMA destination
+// and every operand tile starts on a 1024-byte boundary.
+struct LrSmem {
+  int own, own_bytes;              // resident own tile (not the statistics pass)
+  int stage, stage_bytes, nstage;  // ring of TMA stages
+  int sw_off, th_off, gb_off, vec_off;
+  int sw_bytes, gb_bytes, tx_bytes;
+  int d, d_bytes, nd;              // ring of nd D tiles (gradient passes)
+  int bars, total;
+};
+__host__ __device__ inline int up1024(int v) { return (v + 1023) & ~1023; }
+__host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstage, int nd) {
   const int SF = s_fmt(P), GF = g_fmt(P);
   const int Kp = (K + 15) & ~15;
+  const bool grad = mode == kLrGradA || mode == kLrGradB;
   LrSmem s;
-  int off = 0;
-  s.own = off;
-  off += own_bufs * tile_bytes(SF, kLrRows, K);
+  s.own_bytes = tile_bytes(SF, kLrRows, K);
   s.sw_bytes = tile_bytes(SF, kLrChunk, K);
-  s.sw = off;
-  off += 2 * s.sw_bytes;
-  s.theta = off;
-  off += 2 * kThetaTileBytes;
+  s.gb_bytes = grad ? fmt_parts(GF) * Kp * 128 : 0;
+  s.nstage = nstage;
+  s.nd = nd;
+  int off = 0;
+  if (mode == kLrStats) off += s.own_bytes;  // the sample's own tile travels with its stage
+  s.sw_off = off;
+  off += s.sw_bytes;
+  s.th_off = off;
+  if (mode != kLrStats) off += kThetaTileBytes;
+  s.gb_off = off;
+  off += s.gb_bytes;
+  s.vec_off = off;
+  off += up1024(lr_nvec(mode) * 128);
+  s.stage_bytes = up1024(off);
+  s.tx_bytes = (mode == kLrStats ? s.own_bytes : 0) + s.sw_bytes + (mode != kLrStats ? kThetaTileBytes : 0) +
+               s.gb_bytes + lr_nvec(mode) * 128;
+  off = 0;
+  s.own = off;
+  if (mode != kLrStats) off += s.own_bytes;
+  s.stage = off;
+  off += s.nstage * s.stage_bytes;
   s.d_bytes = grad ? tile_bytes(GF, kLrRows, kLrChunk) : 0;
   s.d = off;
-  off += 2 * s.d_bytes;
-  s.gb_bytes = grad ? tile_bytes(GF, Kp, kLrChunk) : 0;
-  s.gb = off;
-  off += 2 * s.gb_bytes;
-  s.small = off;        // [0,256) staged u, [256,1024) staged row factors, then barriers
-  off += 2048;
+  off += nd * s.d_bytes;
+  s.bars = off;
+  off += 2048;  // barriers, the TMEM slot and the end-of-pass merge buffers
   s.total = off + 1024;  // alignment slack
   return s;
 }
+constexpr int kLrSmemLimit = 232448;
+// The deepest ring (and two D tiles) that fits the shared memory of one CTA: large ranks
+// in the TF32 formats take two 128-byte k-blocks per operand row.
+__host__ __device__ inline LrSmem lr_smem(int P, int mode, int K) {
+  int nstage = lr_stages(mode), nd = 2;
+  LrSmem s = lr_smem_plan(P, mode, K, nstage, nd);
+  while (s.total > kLrSmemLimit && nstage > 2) s = lr_smem_plan(P, mode, K, --nstage, nd);
+  if (s.total > kLrSmemLimit) s = lr_smem_plan(P, mode, K, nstage, nd = 1);
+  return s;
+}
+
+// Tensor maps of one pass: the own and sweep operand tiles (hi, lo), the gradient
+// B-operand (hi, lo), theta (or its transpose) and up to three 32-float vectors.
+struct LrMaps {
+  CUtensorMap own[2], sw[2], gb[2], th, vec[3];
+};
 
 struct LrArgs {
   int M, N, K, B;
-  const float* A;      // [B][M][K]
-  const float* Bm;     // [B][K][N]
-  const float* u;      // [B][N]  exp(x - m_b)
-  const float* m;      // [B]
-  const float* rf_lz;  // [B][M]  backward row factors
+  const float* rf_lz;  // [B][ldm]  backward row factors (padded rows)
   const float* rf_f;
   const float* rf_fc;
-  const float* theta_ld;  // row-padded theta copy (stats pass)
+  long long ldm;
+  const float* theta_ld;  // row-padded theta copy (statistics pass)
   long long theta_ld_stride;
+  const float* m;  // [B]
+  const float* u;  // [B][ldu]  exp(x - m_b) (grad B's own-row constant)
+  long long ldu;
   float* out;   // [M][B]
   float* logZ;  // [B][M]
   float* dA;    // [B][M][K]
@@ -253,17 +323,82 @@ struct LrArgs {
   unsigned* status;
 };
 
-__device__ __forceinline__ float theta_at(const uint8_t* tile, int row, int col) {
-  return *reinterpret_cast<const float*>(tile + row * 128 + ((((col >> 2) ^ (row & 7)) & 7) << 4) + (col & 3) * 4);
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_ld_32x16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive floats of row `row` of a 128-byte-swizzled tile of 32-float rows
+// (theta tiles): four 16-byte loads.
+__device__ __forceinline__ void tile_row16_f32(const uint8_t* tile, int row, int col0, float (&v)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int chunk = (col0 >> 2) + q;
+    const float4 x =
+        *reinterpret_cast<const float4*>(tile + row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
+    v[4 * q] = x.x;
+    v[4 * q + 1] = x.y;
+    v[4 * q + 2] = x.z;
+    v[4 * q + 3] = x.w;
+  }
+}
+
+// Writes 16 values at (row, col0 .. col0+15) of a one-k-block operand tile of format F
+// with 16-byte stores (col0 a multiple of 16; the row's bytes fit one 128-byte block).
+template <int F>
+__device__ __forceinline__ void tile_put_row16(uint8_t* tile, const TileGeo& g, int row, int col0,
+                                               const float (&v)[16]) {
+  uint8_t* base = tile + (row >> 3) * 1024 + (row & 7) * 128;
+  if constexpr (F == kFmtBF16) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int chunk = (col0 >> 3) + q;
+      *reinterpret_cast<uint4*>(base + (((chunk ^ (row & 7)) & 7) << 4)) =
+          make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                     pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = (col0 >> 2) + q;
+      const uint32_t off = (((chunk ^ (row & 7)) & 7) << 4);
+      const float4 h = make_float4(tf32_rna(v[4 * q]), tf32_rna(v[4 * q + 1]), tf32_rna(v[4 * q + 2]),
+                                   tf32_rna(v[4 * q + 3]));
+      *reinterpret_cast<float4*>(base + off) = h;
+      if constexpr (F == kFmtTF32x2)
+        *reinterpret_cast<float4*>(base + g.bytes_part() + off) =
+            make_float4(tf32_rna(v[4 * q] - h.x), tf32_rna(v[4 * q + 1] - h.y), tf32_rna(v[4 * q + 2] - h.z),
+                        tf32_rna(v[4 * q + 3] - h.w));
+    }
+  }
 }
 
 // One pass (forward, grad A or grad B) over the tile of 128 own rows of sample
-// blockIdx.y; see the file comment.
+// blockIdx.y; see the file comment. Eight warps: warp w reads TMEM lane quarter w & 3 and
+// handles columns 16 (w >> 2) .. +15 of every 32-column chunk. Thread 0 issues the TMA
+// loads (a ring of kStages chunks) and the MMAs.
 template <int P, int Mode>
-__global__ void __launch_bounds__(kLrThreads, 1)
-    k_lowrank(const __grid_constant__ CUtensorMap tmTheta, const LrArgs a) {
+__global__ void __launch_bounds__(kLrThreadsAll, 1)
+    k_lowrank(const __grid_constant__ LrMaps maps, const LrArgs a) {
   constexpr int SF = s_fmt(P), GF = g_fmt(P);
   constexpr bool kGrad = Mode != kLrFwd;
+  constexpr int kNvec = lr_nvec(Mode);
+  constexpr int esS = fmt_bytes(SF);
   const int K = a.K;
   const int Kp = (K + 15) & ~15;
   const int own_n = Mode == kLrGradB ? a.N : a.M;
@@ -271,11 +406,14 @@ __global__ void __launch_bounds__(kLrThreads, 1)
   const int b = blockIdx.y;
   const int o0 = blockIdx.x * kLrRows;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int own = o0 + t;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane;  // own row in the tile (TMEM lane)
+  const int col0 = half * 16;           // this thread's columns of a chunk
+  const int own = o0 + row;
   const TileGeo go = tile_geo(SF, kLrRows, K), gs = tile_geo(SF, kLrChunk, K);
   const TileGeo gd = tile_geo(GF, kLrRows, kLrChunk), gg = tile_geo(GF, Kp, kLrChunk);
-  const int kf = go.ksteps * fmt_kstep(SF);  // K padded to whole k-steps (zeros)
-  const LrSmem L = lr_smem(P, kGrad, K, 1);
+  const LrSmem L = lr_smem(P, Mode, K);
+  const int R = L.nstage, ND = L.nd;
   // TMEM: two 32-column S slots, then (gradients) kGradAccs accumulators of gstride
   // columns that the chunks take in turn: each sums a quarter of the sweep, which keeps
   // the accumulator's truncations to a quarter; the epilogue adds them up.
@@ -286,272 +424,269 @@ __global__ void __launch_bounds__(kLrThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* own_tile = smem + L.own;
-  float* uS = reinterpret_cast<float*>(smem + L.small);  // [2][32]
-  float* rfS = uS + 64;                                    // [2][3][32]
-  uint64_t* mbS = reinterpret_cast<uint64_t*>(smem + L.small + 1024);
-  uint64_t* mbT = mbS + 2;
-  uint64_t* mbG = mbS + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbS + 6);
-  auto sw_tile = [&](int s) { return smem + L.sw + s * L.sw_bytes; };
-  auto th_tile = [&](int s) { return smem + L.theta + s * kThetaTileBytes; };
+  uint64_t* mbT = reinterpret_cast<uint64_t*>(smem + L.bars);  // [R <= 4] stage landed
+  uint64_t* mbS = mbT + 4;                                      // [2] S MMA done
+  uint64_t* mbG = mbS + 2;                                      // [2] grad MMA done
+  uint64_t* mbO = mbG + 2;                                      // own tile landed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbO + 1);
+  float* merge = reinterpret_cast<float*>(smem + L.bars + 256);  // [3][128]
+  auto stage = [&](int c) { return smem + L.stage + (c % R) * L.stage_bytes; };
   auto d_tile = [&](int s) { return smem + L.d + s * L.d_bytes; };
-  auto gb_tile = [&](int s) { return smem + L.gb + s * L.gb_bytes; };
 
   if (warp == 0) {
     if (lane == 0) {
+      for (int i = 0; i < R; ++i) mbar_init(&mbT[i], 1);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&mbS[i], 1);
-        mbar_init(&mbT[i], 1);
         mbar_init(&mbG[i], 1);
       }
+      mbar_init(mbO, 1);
       fence_barrier_init();
-      tma_prefetch_map(&tmTheta);
     }
     __syncwarp();
     tmem_alloc(tslot, tcols);
   }
-  // own operand: A_b rows (forward, grad A) or B_b^T rows (grad B)
-  for (int idx = t; idx < kLrRows * kf; idx += kLrThreads) {
-    int o, k;
-    if constexpr (Mode == kLrGradB) {
-      o = idx % kLrRows;
-      k = idx / kLrRows;
-    } else {
-      k = idx % kf;
-      o = idx / kf;
-    }
-    const int gi = o0 + o;
-    float v = 0.f;
-    if (gi < own_n && k < K)
-      v = Mode == kLrGradB ? a.Bm[(static_cast<long long>(b) * K + k) * a.N + gi]
-                           : a.A[(static_cast<long long>(b) * a.M + gi) * K + k];
-    tile_put<SF>(own_tile, go, o, k, v);
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const int nch = (sw_n + kLrChunk - 1) / kLrChunk;
+
+  // TMA of chunk c into its stage (thread 0)
+  auto issue_tma = [&](int c) {
+    uint8_t* st = stage(c);
+    uint64_t* bar = &mbT[c % R];
+    const int w0 = c * kLrChunk;
+    mbar_arrive_expect_tx(bar, L.tx_bytes);
+    for (int part = 0; part < fmt_parts(SF); ++part)
+      for (int kb = 0; kb < gs.kblocks; ++kb)
+        tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
+                    kb * (128 / esS), w0, b);
+    tma_load_3d(st + L.th_off, &maps.th, bar, w0, o0, 0);
+    if constexpr (kGrad)
+      for (int part = 0; part < fmt_parts(GF); ++part)
+        tma_load_3d(st + L.gb_off + part * gg.bytes_part(), &maps.gb[part], bar, w0, 0, b);
+    for (int v = 0; v < kNvec; ++v) tma_load_3d(st + L.vec_off + v * 128, &maps.vec[v], bar, w0, b, 0);
+  };
+  auto issue_s = [&](int c) {
+    tc_fence_after();
+    lr_mma<SF>(tmem + static_cast<uint32_t>((c & 1) * kLrChunk), own_tile, go, stage(c) + L.sw_off, gs, kLrChunk,
+               false);
+    umma_commit(&mbS[c & 1]);
+  };
+
+  bool ok = true;
+  int issued = -1, s_issued = -1, g_issued = -1;  // thread 0's bookkeeping
+  if (t == 0) {
+    mbar_arrive_expect_tx(mbO, L.own_bytes);
+    for (int part = 0; part < fmt_parts(SF); ++part)
+      for (int kb = 0; kb < go.kblocks; ++kb)
+        tma_load_3d(own_tile + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], mbO,
+                    kb * (128 / esS), o0, b);
+    for (int c = 0; c < R && c < nch; ++c) {
+      issue_tma(c);
+      issued = c;
+    }
+    ok = mbar_wait(mbO, 0, a.status, kErrTimeoutMma) && mbar_wait(&mbT[0], 0, a.status, kErrTimeoutMma);
+    if (ok) {
+      issue_s(0);
+      s_issued = 0;
+    }
+  }
 
   // per-row constants
   float lz = 0.f, fi = 0.f, fc = 0.f, uj = 0.f;
+  if constexpr (Mode == kLrGradB) uj = own < a.N ? a.u[static_cast<long long>(b) * a.ldu + own] : 0.f;
   if constexpr (Mode == kLrGradA) {
     if (own < a.M) {
-      const long long r = static_cast<long long>(b) * a.M + own;
+      const long long r = static_cast<long long>(b) * a.ldm + own;
       lz = a.rf_lz[r];
       fi = a.rf_f[r];
       fc = a.rf_fc[r];
     }
   }
-  if constexpr (Mode == kLrGradB) uj = own < a.N ? a.u[static_cast<long long>(b) * a.N + own] : 0.f;
   const bool row_live = lz > -INFINITY;
-  const float mb = a.m[b];
+  float run = -INFINITY, Z = 0.f, num = 0.f;  // forward
+  float e_acc = 0.f;                          // grad B
 
-  // fills of chunk c (all threads)
-  auto stage = [&](int c) {
-    const int sl = c & 1, w0 = c * kLrChunk;
-    uint8_t* st = sw_tile(sl);
-    for (int idx = t; idx < kLrChunk * kf; idx += kLrThreads) {
-      int w, k;
-      if constexpr (Mode == kLrGradB) {
-        k = idx % kf;
-        w = idx / kf;
-      } else {
-        w = idx % kLrChunk;
-        k = idx / kLrChunk;
-      }
-      const int gw = w0 + w;
-      float v = 0.f;
-      if (gw < sw_n && k < K)
-        v = Mode == kLrGradB ? a.A[(static_cast<long long>(b) * a.M + gw) * K + k]
-                             : a.Bm[(static_cast<long long>(b) * K + k) * a.N + gw];
-      tile_put<SF>(st, gs, w, k, v);
-    }
-    if constexpr (kGrad) {
-      uint8_t* gt = gb_tile(sl);
-      for (int idx = t; idx < Kp * kLrChunk; idx += kLrThreads) {
-        int r, kk;
-        if constexpr (Mode == kLrGradA) {
-          kk = idx % kLrChunk;
-          r = idx / kLrChunk;
-        } else {
-          r = idx % Kp;
-          kk = idx / Kp;
-        }
-        const int gw = w0 + kk;
-        float v = 0.f;
-        if (r < K && gw < sw_n)
-          v = Mode == kLrGradA ? a.Bm[(static_cast<long long>(b) * K + r) * a.N + gw]
-                               : a.A[(static_cast<long long>(b) * a.M + gw) * K + r];
-        tile_put<GF>(gt, gg, r, kk, v);
-      }
-    }
-    if (t < kLrChunk) {
-      const int gw = w0 + t;
-      if constexpr (Mode == kLrGradB) {
-        const long long r = static_cast<long long>(b) * a.M + gw;
-        rfS[(sl * 3 + 0) * 32 + t] = gw < a.M ? a.rf_lz[r] : -INFINITY;
-        rfS[(sl * 3 + 1) * 32 + t] = gw < a.M ? a.rf_f[r] : 0.f;
-        rfS[(sl * 3 + 2) * 32 + t] = gw < a.M ? a.rf_fc[r] : 0.f;
-      } else {
-        uS[sl * 32 + t] = gw < a.N ? a.u[static_cast<long long>(b) * a.N + gw] : 0.f;
-      }
-    }
-    fence_proxy_async_smem();
-  };
-  // theta tile and S = own * sweep^T of chunk c (thread 0, after the fills are visible)
-  auto issue = [&](int c) {
-    const int sl = c & 1;
-    mbar_arrive_expect_tx(&mbT[sl], kThetaTileBytes);
-    tma_load_3d(th_tile(sl), &tmTheta, &mbT[sl], c * kLrChunk, o0, 0);
-    tc_fence_after();
-    lr_mma<SF>(tmem + static_cast<uint32_t>(sl * kLrChunk), own_tile, go, sw_tile(sl), gs, kLrChunk, false);
-    umma_commit(&mbS[sl]);
-  };
-
-  const int nch = (sw_n + kLrChunk - 1) / kLrChunk;
-  bool ok = true;
-  int issued = -1, consumed = -1, g_issued = -1;  // chunk indices (thread 0's view)
-  float run = -INFINITY, Z = 0.f, num = 0.f;       // forward
-  float e_acc = 0.f;                               // grad B
-  stage(0);
-  __syncthreads();
-  if (t == 0) {
-    issue(0);
-    issued = 0;
-  }
+  // With a ring of two stages the next chunk's copy is issued only at the end of this
+  // iteration, so its S is issued there too; deeper rings issue it here, ahead.
+  const bool late_s = R == 2;
   for (int c = 0; c < nch; ++c) {
     const int sl = c & 1;
-    const uint32_t ph = (c >> 1) & 1;
-    if (c + 1 < nch) {
-      // the grad B-operand slot of chunk c+1 was read by the grad MMA of chunk c-1
-      if (kGrad && c >= 1) ok = ok && mbar_wait(&mbG[(c - 1) & 1], ((c - 1) >> 1) & 1, a.status, kErrTimeoutMma);
-      stage(c + 1);
+    if (t == 0 && ok && !late_s && c + 1 < nch) {
+      ok = mbar_wait(&mbT[(c + 1) % R], ((c + 1) / R) & 1, a.status, kErrTimeoutMma);
+      if (ok) {
+        issue_s(c + 1);
+        s_issued = c + 1;
+      }
     }
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    if (t == 0 && c + 1 < nch) {
-      issue(c + 1);
-      issued = c + 1;
-    }
-    bool w = mbar_wait(&mbS[sl], ph, a.status, kErrTimeoutEpilogue) &&
-             mbar_wait(&mbT[sl], ph, a.status, kErrTimeoutEpilogue);
+    bool w = mbar_wait(&mbS[sl], (c >> 1) & 1, a.status, kErrTimeoutEpilogue) &&
+             mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutEpilogue);
     w = __all_sync(0xffffffffu, w);
-    consumed = c;
     tc_fence_after();
-    float v[32];
     if (w) {
-      tmem_ld_32x32(lane_base + static_cast<uint32_t>(sl * kLrChunk), v);
-      const uint8_t* th = th_tile(sl);
-      const int w0 = c * kLrChunk;
+      float v[16], th[16];
+      tmem_ld_32x16(lane_base + static_cast<uint32_t>(sl * kLrChunk + col0), v);
+      const uint8_t* st = stage(c);
+      tile_row16_f32(st + L.th_off, row, col0, th);
+      const float* vec = reinterpret_cast<const float*>(st + L.vec_off);
+      const int w0 = c * kLrChunk + col0;
       if constexpr (Mode == kLrFwd) {
         float cm = -INFINITY;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
+        for (int jj = 0; jj < 16; ++jj)
           if (w0 + jj < a.N) cm = fmaxf(cm, v[jj]);
         if (cm > run) {
-          const float sc = run > -INFINITY ? expf(run - cm) : 0.f;
+          const float sc = run > -INFINITY ? ex2_approx((run - cm) * kLog2e) : 0.f;
           Z *= sc;
           num *= sc;
           run = cm;
         }
-        const float* us = uS + sl * 32;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const float tg = w0 + jj < a.N ? theta_at(th, t, jj) * expf(v[jj] - run) : 0.f;
+        for (int jj = 0; jj < 16; ++jj) {
+          const float tg = w0 + jj < a.N ? th[jj] * ex2_approx((v[jj] - run) * kLog2e) : 0.f;
           Z += tg;
-          num = fmaf(tg, us[jj], num);
+          num = fmaf(tg, vec[col0 + jj], num);
         }
       } else {
-        // D (grad A: row i over columns j; grad B: row j over columns i)
+        float dv[16];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          float q, dv;
+        for (int jj = 0; jj < 16; ++jj) {
           if constexpr (Mode == kLrGradA) {
-            const float tj = theta_at(th, t, jj);
-            q = (row_live && tj > 0.f) ? tj * expf(v[jj] - lz) : 0.f;
-            dv = q * fmaf(uS[sl * 32 + jj], fc, -fi);
+            const float q = (row_live && th[jj] > 0.f) ? th[jj] * ex2_approx((v[jj] - lz) * kLog2e) : 0.f;
+            dv[jj] = q * fmaf(vec[col0 + jj], fc, -fi);
           } else {
-            const float lzi = rfS[(sl * 3 + 0) * 32 + jj];
-            const float fci = rfS[(sl * 3 + 2) * 32 + jj];
-            const float tj = theta_at(th, t, jj);
-            q = (lzi > -INFINITY && tj > 0.f) ? tj * expf(v[jj] - lzi) : 0.f;
-            const float pf = q * uj * fci;
+            const float lzi = vec[col0 + jj];
+            const float q = (lzi > -INFINITY && th[jj] > 0.f) ? th[jj] * ex2_approx((v[jj] - lzi) * kLog2e) : 0.f;
+            const float pf = q * uj * vec[64 + col0 + jj];
             e_acc += pf;
-            dv = pf - q * rfS[(sl * 3 + 1) * 32 + jj];
+            dv[jj] = pf - q * vec[32 + col0 + jj];
           }
-          v[jj] = own < own_n ? dv : 0.f;
+          if (own >= own_n) dv[jj] = 0.f;
         }
-        // the D slot was read by the grad MMA of chunk c-2
-        if (c >= 2) w = w && mbar_wait(&mbG[sl], ((c - 2) >> 1) & 1, a.status, kErrTimeoutMma);
-        uint8_t* dt = d_tile(sl);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) tile_put<GF>(dt, gd, t, jj, v[jj]);
+        // the D slot was read by the grad MMA of chunk c - ND
+        if (c >= ND) {
+          const int pc = c - ND;
+          w = w && mbar_wait(&mbG[pc & 1], (pc >> 1) & 1, a.status, kErrTimeoutMma);
+        }
+        tile_put_row16<GF>(d_tile(c % ND), gd, row, col0, dv);
         fence_proxy_async_smem();
       }
     }
     tc_fence_before();
     ok = __syncthreads_and(ok && w);
     if (!ok) break;
-    if (kGrad && t == 0) {
-      tc_fence_after();
-      lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(sl), gd, gb_tile(sl), gg,
-                 Kp, c >= kGradAccs);
-      umma_commit(&mbG[sl]);
-      g_issued = c;
+    if (t == 0) {
+      if constexpr (kGrad) {
+        tc_fence_after();
+        lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(c % ND), gd,
+                   stage(c) + L.gb_off, gg, Kp, c >= kGradAccs);
+        umma_commit(&mbG[sl]);
+        g_issued = c;
+      }
+      // refill the stage of chunk c-1: its S and grad MMAs have completed
+      const int nc = c - 1 + R;
+      if (c >= 1 && nc < nch) {
+        if (kGrad) ok = mbar_wait(&mbG[(c - 1) & 1], ((c - 1) >> 1) & 1, a.status, kErrTimeoutMma);
+        if (ok) {
+          issue_tma(nc);
+          issued = nc;
+        }
+      }
+      if (ok && late_s && c + 1 < nch) {
+        ok = mbar_wait(&mbT[(c + 1) % R], ((c + 1) / R) & 1, a.status, kErrTimeoutMma);
+        if (ok) {
+          issue_s(c + 1);
+          s_issued = c + 1;
+        }
+      }
     }
   }
 
   if (ok && kGrad && nch > 0) {
     bool w = mbar_wait(&mbG[(nch - 1) & 1], ((nch - 1) >> 1) & 1, a.status, kErrTimeoutEpilogue);
     ok = __syncthreads_and(w);
+  } else {
+    ok = __syncthreads_and(ok);
   }
   if (ok) {
     if constexpr (Mode == kLrFwd) {
-      if (own < a.M) {
-        const bool live = Z > 0.f && num > 0.f && mb > -INFINITY;
-        const float o = live ? mb + logf(num / Z) : -INFINITY;
-        const float lzv = Z > 0.f ? logf(Z) + run : -INFINITY;
-        a.out[static_cast<long long>(own) * a.B + b] = o;
-        a.logZ[static_cast<long long>(b) * a.M + own] = lzv;
+      // merge the two column halves of every row
+      if (half == 1) {
+        merge[row] = run;
+        merge[128 + row] = Z;
+        merge[256 + row] = num;
+      }
+      __syncthreads();
+      if (half == 0 && own < a.M) {
+        const float r1 = merge[row], z1 = merge[128 + row], n1 = merge[256 + row];
+        const float r = fmaxf(run, r1);
+        float zt = 0.f, nt = 0.f;
+        if (r > -INFINITY) {
+          const float s0 = run > -INFINITY ? ex2_approx((run - r) * kLog2e) : 0.f;
+          const float s1 = r1 > -INFINITY ? ex2_approx((r1 - r) * kLog2e) : 0.f;
+          zt = Z * s0 + z1 * s1;
+          nt = num * s0 + n1 * s1;
+        }
+        const float mb = a.m[b];
+        const bool live = zt > 0.f && nt > 0.f && mb > -INFINITY;
+        a.out[static_cast<long long>(own) * a.B + b] = live ? mb + logf(nt / zt) : -INFINITY;
+        a.logZ[static_cast<long long>(b) * a.M + own] = zt > 0.f ? logf(zt) + r : -INFINITY;
       }
     } else {
-      tc_fence_after();
-      float acc[64];
-      for (int r = 0; r < 64; ++r) acc[r] = 0.f;
-      for (int q = 0; q < kGradAccs && q < nch; ++q) {
-        for (int c0 = 0; c0 < Kp; c0 += 32) {
-          float v[32];
-          tmem_ld_32x32(lane_base + static_cast<uint32_t>(64 + q * gstride + c0), v);
-#pragma unroll
-          for (int r = 0; r < 32; ++r) acc[c0 + r] += v[r];
-        }
+      if constexpr (Mode == kLrGradB) {
+        if (half == 1) merge[row] = e_acc;
       }
-      if (own < own_n) {
-        if constexpr (Mode == kLrGradA) {
-          float* dst = a.dA + (static_cast<long long>(b) * a.M + own) * K;
-          for (int r = 0; r < K; ++r) dst[r] = a.accumulate ? dst[r] + acc[r] : acc[r];
-        } else {
-          if (a.dB) {
-            for (int r = 0; r < K; ++r) {
-              float* dst = a.dB + (static_cast<long long>(b) * K + r) * a.N + own;
-              *dst = a.accumulate ? *dst + acc[r] : acc[r];
+      __syncthreads();
+      if (half == 0) {
+        tc_fence_after();
+        float acc[64];  // static indices only: kept in registers
+#pragma unroll
+        for (int r = 0; r < 64; ++r) acc[r] = 0.f;
+        for (int q = 0; q < kGradAccs && q < nch; ++q) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            if (h2 * 32 < Kp) {
+              float v[32];
+              tmem_ld_32x32(lane_base + static_cast<uint32_t>(64 + q * gstride + h2 * 32), v);
+#pragma unroll
+              for (int r = 0; r < 32; ++r) acc[h2 * 32 + r] += v[r];
             }
           }
-          if (a.e) {
-            float* de = a.e + static_cast<long long>(own) * a.B + b;
-            *de = a.accumulate ? *de + e_acc : e_acc;
+        }
+        if (own < own_n) {
+          if constexpr (Mode == kLrGradA) {
+            float* dst = a.dA + (static_cast<long long>(b) * a.M + own) * K;
+#pragma unroll
+            for (int r = 0; r < 64; ++r)
+              if (r < K) dst[r] = a.accumulate ? dst[r] + acc[r] : acc[r];
+          } else {
+            if (a.dB) {
+#pragma unroll
+              for (int r = 0; r < 64; ++r) {
+                if (r < K) {
+                  float* dst = a.dB + (static_cast<long long>(b) * K + r) * a.N + own;
+                  *dst = a.accumulate ? *dst + acc[r] : acc[r];
+                }
+              }
+            }
+            if (a.e) {
+              const float ev = e_acc + merge[row];
+              float* de = a.e + static_cast<long long>(own) * a.B + b;
+              *de = a.accumulate ? *de + ev : ev;
+            }
           }
         }
       }
     }
   } else if (t == 0) {
     // a wait gave up: let the copies and MMAs in flight finish before TMEM is freed
-    for (int c = consumed + 1; c <= issued; ++c) {
-      mbar_wait(&mbT[c & 1], (c >> 1) & 1, a.status, kErrTimeoutDrain);
-      mbar_wait(&mbS[c & 1], (c >> 1) & 1, a.status, kErrTimeoutDrain);
-    }
+    // (the latest phase of every barrier: earlier phases are long complete)
+    mbar_wait(mbO, 0, a.status, kErrTimeoutDrain);
+    for (int c = issued; c >= 0 && c > issued - R; --c) mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutDrain);
+    if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
     if (g_issued >= 0) mbar_wait(&mbG[g_issued & 1], (g_issued >> 1) & 1, a.status, kErrTimeoutDrain);
   }
   tc_fence_before();
@@ -563,31 +698,34 @@ __global__ void __launch_bounds__(kLrThreads, 1)
 }
 
 // Parameter-flow statistics F+ and W over all samples for the 128 x 32 tile (blockIdx.x,
-// blockIdx.y) of [M, N]: own rows i, the 32 columns j fixed, a sweep over the samples;
-// each sample's S chunk is one MMA group, its own A_b tile double-buffered.
+// blockIdx.y) of [M, N]: own rows i, the 32 columns j fixed, a sweep over the samples.
+// Each stage of the TMA ring holds one sample's A_b tile, its B_b^T chunk and u_b.
 template <int P>
-__global__ void __launch_bounds__(kLrThreads, 1)
-    k_lowrank_stats(const LrArgs a) {
+__global__ void __launch_bounds__(kLrThreadsAll, 1)
+    k_lowrank_stats(const __grid_constant__ LrMaps maps, const LrArgs a) {
   constexpr int SF = s_fmt(P);
+  constexpr int esS = fmt_bytes(SF);
   const int K = a.K;
   const int i0 = blockIdx.x * kLrRows, j0 = blockIdx.y * kLrChunk;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int i = i0 + t;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane;
+  const int col0 = half * 16;
+  const int i = i0 + row;
   const TileGeo go = tile_geo(SF, kLrRows, K), gs = tile_geo(SF, kLrChunk, K);
-  const int kf = go.ksteps * fmt_kstep(SF);
-  const LrSmem L = lr_smem(P, false, K, 2);
-  const int own_bytes = tile_bytes(SF, kLrRows, K);
+  const LrSmem L = lr_smem(P, kLrStats, K);
+  const int R = L.nstage;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* uS = reinterpret_cast<float*>(smem + L.small);  // [2][32]
-  uint64_t* mbS = reinterpret_cast<uint64_t*>(smem + L.small + 1024);
+  uint64_t* mbT = reinterpret_cast<uint64_t*>(smem + L.bars);  // [R <= 4]
+  uint64_t* mbS = mbT + 4;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mbS + 2);
-  auto own_tile = [&](int s) { return smem + L.own + s * own_bytes; };
-  auto sw_tile = [&](int s) { return smem + L.sw + s * L.sw_bytes; };
+  auto stage = [&](int b) { return smem + L.stage + (b % R) * L.stage_bytes; };
 
   if (warp == 0) {
     if (lane == 0) {
+      for (int s = 0; s < R; ++s) mbar_init(&mbT[s], 1);
       mbar_init(&mbS[0], 1);
       mbar_init(&mbS[1], 1);
       fence_barrier_init();
@@ -595,95 +733,118 @@ __global__ void __launch_bounds__(kLrThreads, 1)
     __syncwarp();
     tmem_alloc(tslot, 64);
   }
-  // theta[i][j0 .. j0+31] in registers, from the row-padded copy
-  float th[32];
+  // theta[i][j0 + col0 .. +15] in registers, from the row-padded copy
+  float th[16];
 #pragma unroll
-  for (int jj = 0; jj < 32; ++jj)
-    th[jj] = (i < a.M && j0 + jj < a.N) ? a.theta_ld[static_cast<long long>(i) * a.theta_ld_stride + j0 + jj] : 0.f;
-
-  auto stage = [&](int b) {
-    const int sl = b & 1;
-    uint8_t* ot = own_tile(sl);
-    for (int idx = t; idx < kLrRows * kf; idx += kLrThreads) {
-      const int k = idx % kf, o = idx / kf;
-      const int gi = i0 + o;
-      const float v = (gi < a.M && k < K) ? a.A[(static_cast<long long>(b) * a.M + gi) * K + k] : 0.f;
-      tile_put<SF>(ot, go, o, k, v);
-    }
-    uint8_t* st = sw_tile(sl);
-    for (int idx = t; idx < kLrChunk * kf; idx += kLrThreads) {
-      const int w = idx % kLrChunk, k = idx / kLrChunk;
-      const int gj = j0 + w;
-      const float v = (gj < a.N && k < K) ? a.Bm[(static_cast<long long>(b) * K + k) * a.N + gj] : 0.f;
-      tile_put<SF>(st, gs, w, k, v);
-    }
-    if (t < kLrChunk) uS[sl * 32 + t] = j0 + t < a.N ? a.u[static_cast<long long>(b) * a.N + j0 + t] : 0.f;
-    fence_proxy_async_smem();
-  };
-
+  for (int jj = 0; jj < 16; ++jj) {
+    const int j = j0 + col0 + jj;
+    th[jj] = (i < a.M && j < a.N) ? a.theta_ld[static_cast<long long>(i) * a.theta_ld_stride + j] : 0.f;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  float fp[32], wst[32];
-#pragma unroll
-  for (int jj = 0; jj < 32; ++jj) fp[jj] = wst[jj] = 0.f;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+
+  auto issue_tma = [&](int b) {
+    uint8_t* st = stage(b);
+    uint64_t* bar = &mbT[b % R];
+    mbar_arrive_expect_tx(bar, L.tx_bytes);
+    for (int part = 0; part < fmt_parts(SF); ++part) {
+      for (int kb = 0; kb < go.kblocks; ++kb)
+        tma_load_3d(st + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], bar, kb * (128 / esS), i0, b);
+      for (int kb = 0; kb < gs.kblocks; ++kb)
+        tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
+                    kb * (128 / esS), j0, b);
+    }
+    tma_load_3d(st + L.vec_off, &maps.vec[0], bar, j0, b, 0);
+  };
+  auto issue_s = [&](int b) {
+    tc_fence_after();
+    lr_mma<SF>(tmem + static_cast<uint32_t>((b & 1) * kLrChunk), stage(b), go, stage(b) + L.sw_off, gs, kLrChunk,
+               false);
+    umma_commit(&mbS[b & 1]);
+  };
 
   bool ok = true;
-  int issued = -1, consumed = -1;
-  stage(0);
-  __syncthreads();
+  int issued = -1, s_issued = -1;
   if (t == 0) {
-    tc_fence_after();
-    lr_mma<SF>(tmem, own_tile(0), go, sw_tile(0), gs, kLrChunk, false);
-    umma_commit(&mbS[0]);
-    issued = 0;
-  }
-  for (int b = 0; b < a.B; ++b) {
-    const int sl = b & 1;
-    if (b + 1 < a.B) stage(b + 1);  // slot (b+1)&1 was read by the MMA of sample b-1 (waited)
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    if (t == 0 && b + 1 < a.B) {
-      tc_fence_after();
-      lr_mma<SF>(tmem + static_cast<uint32_t>(((b + 1) & 1) * kLrChunk), own_tile((b + 1) & 1), go,
-                 sw_tile((b + 1) & 1), gs, kLrChunk, false);
-      umma_commit(&mbS[(b + 1) & 1]);
-      issued = b + 1;
+    for (int b = 0; b < R && b < a.B; ++b) {
+      issue_tma(b);
+      issued = b;
     }
-    // row factors of sample b
-    float lz = -INFINITY, fi = 0.f, fc = 0.f;
-    if (i < a.M) {
-      const long long r = static_cast<long long>(b) * a.M + i;
+    ok = mbar_wait(&mbT[0], 0, a.status, kErrTimeoutMma);
+    if (ok) {
+      issue_s(0);
+      s_issued = 0;
+    }
+  }
+  float fp[16], wst[16];
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) fp[jj] = wst[jj] = 0.f;
+  auto row_factors = [&](int b, float& lz, float& fi, float& fc) {
+    lz = -INFINITY;
+    fi = fc = 0.f;
+    if (i < a.M && b < a.B) {
+      const long long r = static_cast<long long>(b) * a.ldm + i;
       lz = a.rf_lz[r];
       fi = a.rf_f[r];
       fc = a.rf_fc[r];
     }
-    bool w = __all_sync(0xffffffffu, mbar_wait(&mbS[sl], (b >> 1) & 1, a.status, kErrTimeoutEpilogue));
-    consumed = b;
+  };
+  float lz, fi, fc;
+  row_factors(0, lz, fi, fc);
+  const bool late_s = R == 2;  // as in k_lowrank
+  for (int b = 0; b < a.B; ++b) {
+    const int sl = b & 1;
+    if (t == 0 && ok && !late_s && b + 1 < a.B) {
+      ok = mbar_wait(&mbT[(b + 1) % R], ((b + 1) / R) & 1, a.status, kErrTimeoutMma);
+      if (ok) {
+        issue_s(b + 1);
+        s_issued = b + 1;
+      }
+    }
+    float nlz, nfi, nfc;  // the next sample's row factors, loaded while this one computes
+    row_factors(b + 1, nlz, nfi, nfc);
+    bool w = mbar_wait(&mbS[sl], (b >> 1) & 1, a.status, kErrTimeoutEpilogue) &&
+             mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutEpilogue);
+    w = __all_sync(0xffffffffu, w);
     tc_fence_after();
     if (w) {
-      float v[32];
-      tmem_ld_32x32(lane_base + static_cast<uint32_t>(sl * kLrChunk), v);
+      float v[16];
+      tmem_ld_32x16(lane_base + static_cast<uint32_t>(sl * kLrChunk + col0), v);
       if (lz > -INFINITY) {
-        const float* us = uS + sl * 32;
+        const float* us = reinterpret_cast<const float*>(stage(b) + L.vec_off) + col0;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const float gz = expf(v[jj] - lz);  // g_b / Z_b
+        for (int jj = 0; jj < 16; ++jj) {
+          const float gz = ex2_approx((v[jj] - lz) * kLog2e);  // g_b / Z_b
           fp[jj] = fmaf(th[jj] * gz, us[jj] * fc, fp[jj]);
           wst[jj] = fmaf(fi, gz, wst[jj]);
         }
       }
     }
+    lz = nlz;
+    fi = nfi;
+    fc = nfc;
     tc_fence_before();
     ok = __syncthreads_and(ok && w);
     if (!ok) break;
+    if (t == 0 && b >= 1 && b - 1 + R < a.B) {  // refill the stage of sample b-1
+      issue_tma(b - 1 + R);
+      issued = b - 1 + R;
+    }
+    if (t == 0 && late_s && b + 1 < a.B) {
+      ok = mbar_wait(&mbT[(b + 1) % R], ((b + 1) / R) & 1, a.status, kErrTimeoutMma);
+      if (ok) {
+        issue_s(b + 1);
+        s_issued = b + 1;
+      }
+    }
   }
   if (ok) {
     if (i < a.M) {
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = j0 + jj;
+      for (int jj = 0; jj < 16; ++jj) {
+        const int j = j0 + col0 + jj;
         if (j >= a.N) break;
         const long long idx = static_cast<long long>(i) * a.N + j;
         if (a.Fp) a.Fp[idx] = a.accumulate ? a.Fp[idx] + fp[jj] : fp[jj];
@@ -691,7 +852,8 @@ __global__ void __launch_bounds__(kLrThreads, 1)
       }
     }
   } else if (t == 0) {
-    for (int b = consumed + 1; b <= issued; ++b) mbar_wait(&mbS[b & 1], (b >> 1) & 1, a.status, kErrTimeoutDrain);
+    for (int b = issued; b >= 0 && b > issued - R; --b) mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutDrain);
+    if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
   }
   tc_fence_before();
   __syncthreads();
@@ -707,22 +869,45 @@ __global__ void k_lr_fill(float* __restrict__ p, long long n, float v) {
   if (i < n) p[i] = v;
 }
 
+// An operand matrix in format F: one Operand per part (hi, lo), element type bf16 or fp32.
+struct LrOp {
+  Operand part[2];
+  int parts = 0;
+  pc_precision_t ety = PC_PREC_TF32;
+};
+LrOp carve_op(Carver& c, int F, long long groups, long long rows, long long cols) {
+  LrOp o;
+  o.parts = fmt_parts(F);
+  o.ety = fmt_bytes(F) == 2 ? PC_PREC_AUTO : PC_PREC_TF32;
+  for (int p = 0; p < o.parts; ++p) o.part[p] = c.operand(o.ety, groups, rows, cols);
+  return o;
+}
+
 struct LrWs {
-  float *m, *u, *rf_lz, *rf_f, *rf_fc;
-  Operand theta, thetaT;  // plain float32 copies, rows padded to 64 elements
+  float* m;
+  Operand u;                            // [B][N] exp(x - m_b), padded rows
+  Operand theta, thetaT;                // plain float32 copies, padded rows
+  Operand rf_lz, rf_f, rf_fc;           // [B][M] backward row factors
+  LrOp Aop, BTop;                       // A_b rows, B_b^T rows (format of S)
+  LrOp Bg, AgT;                         // B_b rows, A_b^T rows (format of the gradients)
 };
 
-size_t carve_lr(void* base, int M, int N, int B, bool bwd, LrWs* w) {
+size_t carve_lr(void* base, pc_precision_t prec, int M, int N, int K, int B, bool bwd, LrWs* w) {
+  const int P = prec == PC_PREC_AUTO ? kBF16 : (prec == PC_PREC_TF32 ? kTF32 : kTF32x3);
   Carver c(base);
   *w = LrWs{};
   w->m = static_cast<float*>(c.take(size_t(B) * 4));
-  w->u = static_cast<float*>(c.take(size_t(B) * N * 4));
+  w->u = c.operand(PC_PREC_TF32, 1, B, N);
   w->theta = c.operand(PC_PREC_TF32, 1, M, N);
+  w->Aop = carve_op(c, s_fmt(P), B, M, K);
+  w->BTop = carve_op(c, s_fmt(P), B, N, K);
   if (bwd) {
     w->thetaT = c.operand(PC_PREC_TF32, 1, N, M);
-    w->rf_lz = static_cast<float*>(c.take(size_t(B) * M * 4));
-    w->rf_f = static_cast<float*>(c.take(size_t(B) * M * 4));
-    w->rf_fc = static_cast<float*>(c.take(size_t(B) * M * 4));
+    w->rf_lz = c.operand(PC_PREC_TF32, 1, B, M);
+    w->rf_f = c.operand(PC_PREC_TF32, 1, B, M);
+    w->rf_fc = c.operand(PC_PREC_TF32, 1, B, M);
+    w->Bg = carve_op(c, g_fmt(P), B, K, N);
+    w->AgT = carve_op(c, g_fmt(P), B, K, M);
   }
   return c.used + 256;
 }
@@ -746,20 +931,44 @@ pc_status_t lr_attr(Kern kern, int smem) {
   return PC_OK;
 }
 
-pc_status_t lr_prepare(const float* theta, const float* x, int M, int N, int B, bool bwd, LrWs& w,
-                       cudaStream_t s) {
-  if (B > 0 && N > 0) {
-    k_lr_colmax_u<<<B, 256, 0, s>>>(N, B, x, w.m, w.u);
-    PC_LAUNCH_CHECK();
+template <int F>
+pc_status_t to_op(const float* src, long long sg, long long sr, long long sc, int G, int R, int C, const LrOp& o,
+                  cudaStream_t s) {
+  const long long n = static_cast<long long>(G) * R * o.part[0].ld;
+  const int blocks = static_cast<int>(std::min<long long>(cdiv(n, 256), 4096));
+  k_lr_to_op<F><<<blocks, 256, 0, s>>>(src, sg, sr, sc, G, R, C, o.part[0].ptr, o.parts > 1 ? o.part[1].ptr : nullptr,
+                                       o.part[0].ld);
+  PC_LAUNCH_CHECK();
+  return PC_OK;
+}
+
+pc_status_t encode_op(CUtensorMap (&maps)[2], const LrOp& o, int box_rows) {
+  for (int p = 0; p < o.parts; ++p) {
+    const pc_status_t st = encode_operand_map(&maps[p], o.part[p], o.ety, box_rows, 0);
+    if (st != PC_OK) return st;
   }
-  if (M > 0 && N > 0) {
-    const dim3 g(cdiv(N, 32), cdiv(M, 32));
-    k_lr_theta_copy<<<g, dim3(32, 8), 0, s>>>(M, N, theta, static_cast<float*>(w.theta.ptr), w.theta.ld, 0);
+  if (o.parts == 1) maps[1] = maps[0];
+  return PC_OK;
+}
+
+// Set-up shared by both passes: m, u, the theta copies and the operand copies of A, B.
+template <int P>
+pc_status_t lr_prepare(const float* theta, const float* A, const float* Bm, const float* x, int M, int N, int K,
+                       int B, bool bwd, LrWs& w, cudaStream_t s) {
+  k_lr_colmax_u<<<B, 256, 0, s>>>(N, B, x, w.m, static_cast<float*>(w.u.ptr), w.u.ld);
+  PC_LAUNCH_CHECK();
+  const dim3 g(cdiv(N, 32), cdiv(M, 32));
+  k_lr_theta_copy<<<g, dim3(32, 8), 0, s>>>(M, N, theta, static_cast<float*>(w.theta.ptr), w.theta.ld, 0);
+  PC_LAUNCH_CHECK();
+  const long long MK = static_cast<long long>(M) * K, KN = static_cast<long long>(K) * N;
+  pc_status_t st;
+  if ((st = to_op<s_fmt(P)>(A, MK, K, 1, B, M, K, w.Aop, s)) != PC_OK) return st;    // A_b[i][k]
+  if ((st = to_op<s_fmt(P)>(Bm, KN, 1, N, B, N, K, w.BTop, s)) != PC_OK) return st;  // B_b[k][j] as [j][k]
+  if (bwd) {
+    k_lr_theta_copy<<<g, dim3(32, 8), 0, s>>>(M, N, theta, static_cast<float*>(w.thetaT.ptr), w.thetaT.ld, 1);
     PC_LAUNCH_CHECK();
-    if (bwd) {
-      k_lr_theta_copy<<<g, dim3(32, 8), 0, s>>>(M, N, theta, static_cast<float*>(w.thetaT.ptr), w.thetaT.ld, 1);
-      PC_LAUNCH_CHECK();
-    }
+    if ((st = to_op<g_fmt(P)>(Bm, KN, N, 1, B, K, N, w.Bg, s)) != PC_OK) return st;   // B_b[k][j]
+    if ((st = to_op<g_fmt(P)>(A, MK, 1, K, B, K, M, w.AgT, s)) != PC_OK) return st;   // A_b[i][k] as [k][i]
   }
   return PC_OK;
 }
@@ -768,7 +977,8 @@ template <int P>
 pc_status_t lr_fwd(int M, int N, int K, int B, const float* theta, const float* A, const float* Bm, const float* x,
                    float* out, float* logZ, void* ws, cudaStream_t s) {
   LrWs w;
-  carve_lr(ws, M, N, B, false, &w);
+  carve_lr(ws, static_cast<pc_precision_t>(P == kBF16 ? PC_PREC_AUTO : (P == kTF32 ? PC_PREC_TF32 : PC_PREC_FP32)),
+           M, N, K, B, false, &w);
   if (M == 0 || B == 0) return PC_OK;
   if (N == 0) {  // no children: every node's sum is empty
     k_lr_fill<<<cdiv(static_cast<long long>(M) * B, 256), 256, 0, s>>>(out, static_cast<long long>(M) * B, -INFINITY);
@@ -777,19 +987,24 @@ pc_status_t lr_fwd(int M, int N, int K, int B, const float* theta, const float* 
     PC_LAUNCH_CHECK();
     return PC_OK;
   }
-  pc_status_t st = lr_prepare(theta, x, M, N, B, false, w, s);
+  pc_status_t st = lr_prepare<P>(theta, A, Bm, x, M, N, K, B, false, w, s);
   if (st != PC_OK) return st;
-  CUtensorMap tm;
-  if ((st = encode_operand_map(&tm, w.theta, PC_PREC_TF32, kLrRows, 0)) != PC_OK) return st;
+  LrMaps maps;
+  if ((st = encode_op(maps.own, w.Aop, kLrRows)) != PC_OK) return st;
+  if ((st = encode_op(maps.sw, w.BTop, kLrChunk)) != PC_OK) return st;
+  maps.gb[0] = maps.gb[1] = maps.sw[0];  // unused
+  if ((st = encode_operand_map(&maps.th, w.theta, PC_PREC_TF32, kLrRows, 0)) != PC_OK) return st;
+  if ((st = encode_operand_map(&maps.vec[0], w.u, PC_PREC_TF32, 1, 0, false)) != PC_OK) return st;
+  maps.vec[1] = maps.vec[2] = maps.vec[0];
   LrArgs a{};
   a.M = M; a.N = N; a.K = K; a.B = B;
-  a.A = A; a.Bm = Bm; a.u = w.u; a.m = w.m;
+  a.m = w.m;
   a.out = out; a.logZ = logZ;
   a.status = device_status_word();
-  const int smem = lr_smem(P, false, K, 1).total;
+  const int smem = lr_smem(P, kLrFwd, K).total;
   if ((st = lr_attr(k_lowrank<P, kLrFwd>, smem)) != PC_OK) return st;
   const int slot = profile_begin(s);
-  k_lowrank<P, kLrFwd><<<dim3(cdiv(M, kLrRows), B), kLrThreads, smem, s>>>(tm, a);
+  k_lowrank<P, kLrFwd><<<dim3(cdiv(M, kLrRows), B), kLrThreadsAll, smem, s>>>(maps, a);
   PC_LAUNCH_CHECK();
   profile_end(slot, s, PC_KIND_LOWRANK_FWD, 2LL * M * N * K * B);
   return PC_OK;
@@ -800,7 +1015,8 @@ pc_status_t lr_bwd(int M, int N, int K, int B, const float* theta, const float* 
                    const float* out, const float* logZ, const float* f, float* dA, float* dB, float* e, float* Fp,
                    float* W, int accumulate, void* ws, cudaStream_t s) {
   LrWs w;
-  carve_lr(ws, M, N, B, true, &w);
+  carve_lr(ws, static_cast<pc_precision_t>(P == kBF16 ? PC_PREC_AUTO : (P == kTF32 ? PC_PREC_TF32 : PC_PREC_FP32)),
+           M, N, K, B, true, &w);
   if (!accumulate) {  // outputs that no pass writes when a size is zero
     if (dA && N == 0) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(B) * M * K * 4, s));
     if (dB && M == 0) PC_CUDA(cudaMemsetAsync(dB, 0, size_t(B) * K * N * 4, s));
@@ -809,46 +1025,70 @@ pc_status_t lr_bwd(int M, int N, int K, int B, const float* theta, const float* 
     if (W && B == 0) PC_CUDA(cudaMemsetAsync(W, 0, size_t(M) * N * 4, s));
   }
   if (M == 0 || N == 0 || B == 0) return PC_OK;
-  pc_status_t st = lr_prepare(theta, x, M, N, B, true, w, s);
+  pc_status_t st = lr_prepare<P>(theta, A, Bm, x, M, N, K, B, true, w, s);
   if (st != PC_OK) return st;
-  k_lr_row_factors<<<cdiv(static_cast<long long>(M) * B, 256), 256, 0, s>>>(M, B, out, f, logZ, w.m, w.rf_lz,
-                                                                             w.rf_f, w.rf_fc);
+  k_lr_row_factors<<<cdiv(static_cast<long long>(M) * B, 256), 256, 0, s>>>(
+      M, B, out, f, logZ, w.m, static_cast<float*>(w.rf_lz.ptr), static_cast<float*>(w.rf_f.ptr),
+      static_cast<float*>(w.rf_fc.ptr), w.rf_lz.ld);
   PC_LAUNCH_CHECK();
   LrArgs a{};
   a.M = M; a.N = N; a.K = K; a.B = B;
-  a.A = A; a.Bm = Bm; a.u = w.u; a.m = w.m;
-  a.rf_lz = w.rf_lz; a.rf_f = w.rf_f; a.rf_fc = w.rf_fc;
+  a.m = w.m;
+  a.rf_lz = static_cast<const float*>(w.rf_lz.ptr);
+  a.rf_f = static_cast<const float*>(w.rf_f.ptr);
+  a.rf_fc = static_cast<const float*>(w.rf_fc.ptr);
+  a.ldm = w.rf_lz.ld;
   a.theta_ld = static_cast<const float*>(w.theta.ptr);
   a.theta_ld_stride = w.theta.ld;
+  a.u = static_cast<const float*>(w.u.ptr);
+  a.ldu = w.u.ld;
   a.dA = dA; a.dB = dB; a.e = e; a.Fp = Fp; a.W = W;
   a.accumulate = accumulate;
   a.status = device_status_word();
   const long long flops = 2LL * M * N * K * B;
+  const int Kp = (K + 15) & ~15;
   if (dA) {
-    CUtensorMap tm;
-    if ((st = encode_operand_map(&tm, w.theta, PC_PREC_TF32, kLrRows, 0)) != PC_OK) return st;
-    const int smem = lr_smem(P, true, K, 1).total;
+    LrMaps maps;
+    if ((st = encode_op(maps.own, w.Aop, kLrRows)) != PC_OK) return st;
+    if ((st = encode_op(maps.sw, w.BTop, kLrChunk)) != PC_OK) return st;
+    if ((st = encode_op(maps.gb, w.Bg, Kp)) != PC_OK) return st;
+    if ((st = encode_operand_map(&maps.th, w.theta, PC_PREC_TF32, kLrRows, 0)) != PC_OK) return st;
+    if ((st = encode_operand_map(&maps.vec[0], w.u, PC_PREC_TF32, 1, 0, false)) != PC_OK) return st;
+    maps.vec[1] = maps.vec[2] = maps.vec[0];
+    const int smem = lr_smem(P, kLrGradA, K).total;
     if ((st = lr_attr(k_lowrank<P, kLrGradA>, smem)) != PC_OK) return st;
     const int slot = profile_begin(s);
-    k_lowrank<P, kLrGradA><<<dim3(cdiv(M, kLrRows), B), kLrThreads, smem, s>>>(tm, a);
+    k_lowrank<P, kLrGradA><<<dim3(cdiv(M, kLrRows), B), kLrThreadsAll, smem, s>>>(maps, a);
     PC_LAUNCH_CHECK();
     profile_end(slot, s, PC_KIND_LOWRANK_BWD, 2 * flops);
   }
   if (dB || e) {
-    CUtensorMap tm;
-    if ((st = encode_operand_map(&tm, w.thetaT, PC_PREC_TF32, kLrRows, 0)) != PC_OK) return st;
-    const int smem = lr_smem(P, true, K, 1).total;
+    LrMaps maps;
+    if ((st = encode_op(maps.own, w.BTop, kLrRows)) != PC_OK) return st;
+    if ((st = encode_op(maps.sw, w.Aop, kLrChunk)) != PC_OK) return st;
+    if ((st = encode_op(maps.gb, w.AgT, Kp)) != PC_OK) return st;
+    if ((st = encode_operand_map(&maps.th, w.thetaT, PC_PREC_TF32, kLrRows, 0)) != PC_OK) return st;
+    if ((st = encode_operand_map(&maps.vec[0], w.rf_lz, PC_PREC_TF32, 1, 0, false)) != PC_OK) return st;
+    if ((st = encode_operand_map(&maps.vec[1], w.rf_f, PC_PREC_TF32, 1, 0, false)) != PC_OK) return st;
+    if ((st = encode_operand_map(&maps.vec[2], w.rf_fc, PC_PREC_TF32, 1, 0, false)) != PC_OK) return st;
+    const int smem = lr_smem(P, kLrGradB, K).total;
     if ((st = lr_attr(k_lowrank<P, kLrGradB>, smem)) != PC_OK) return st;
     const int slot = profile_begin(s);
-    k_lowrank<P, kLrGradB><<<dim3(cdiv(N, kLrRows), B), kLrThreads, smem, s>>>(tm, a);
+    k_lowrank<P, kLrGradB><<<dim3(cdiv(N, kLrRows), B), kLrThreadsAll, smem, s>>>(maps, a);
     PC_LAUNCH_CHECK();
     profile_end(slot, s, PC_KIND_LOWRANK_BWD, 2 * flops);
   }
   if (Fp || W) {
-    const int smem = lr_smem(P, false, K, 2).total;
+    LrMaps maps;
+    if ((st = encode_op(maps.own, w.Aop, kLrRows)) != PC_OK) return st;
+    if ((st = encode_op(maps.sw, w.BTop, kLrChunk)) != PC_OK) return st;
+    maps.gb[0] = maps.gb[1] = maps.th = maps.sw[0];  // unused
+    if ((st = encode_operand_map(&maps.vec[0], w.u, PC_PREC_TF32, 1, 0, false)) != PC_OK) return st;
+    maps.vec[1] = maps.vec[2] = maps.vec[0];
+    const int smem = lr_smem(P, kLrStats, K).total;
     if ((st = lr_attr(k_lowrank_stats<P>, smem)) != PC_OK) return st;
     const int slot = profile_begin(s);
-    k_lowrank_stats<P><<<dim3(cdiv(M, kLrRows), cdiv(N, kLrChunk)), kLrThreads, smem, s>>>(a);
+    k_lowrank_stats<P><<<dim3(cdiv(M, kLrRows), cdiv(N, kLrChunk)), kLrThreadsAll, smem, s>>>(maps, a);
     PC_LAUNCH_CHECK();
     profile_end(slot, s, PC_KIND_LOWRANK_BWD, flops);
   }
@@ -869,7 +1109,7 @@ pc_status_t pc_lowrank_exp_sum_workspace(int M, int N, int K, int B, int with_ba
   pc_status_t st = check_lr_shape(M, N, K, B, prec);
   if (st != PC_OK) return st;
   LrWs w;
-  *bytes = carve_lr(nullptr, M, N, B, with_backward != 0, &w);
+  *bytes = carve_lr(nullptr, prec, M, N, K, B, with_backward != 0, &w);
   return PC_OK;
 }
 
@@ -885,7 +1125,7 @@ pc_status_t pc_lowrank_exp_sum_fwd(int M, int N, int K, int B, const float* thet
   PC_CHECK(ws || !work, PC_ERR_NULL, "workspace is NULL");
   PC_CHECK(!ws || aligned16(ws), PC_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
   LrWs w;
-  const size_t need = carve_lr(nullptr, M, N, B, false, &w);
+  const size_t need = carve_lr(nullptr, prec, M, N, K, B, false, &w);
   PC_CHECK(!work || ws_bytes >= need, PC_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (prec) {
@@ -908,7 +1148,7 @@ pc_status_t pc_lowrank_exp_sum_bwd(int M, int N, int K, int B, const float* thet
   PC_CHECK(ws || !work, PC_ERR_NULL, "workspace is NULL");
   PC_CHECK(!ws || aligned16(ws), PC_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
   LrWs w;
-  const size_t need = carve_lr(nullptr, M, N, B, true, &w);
+  const size_t need = carve_lr(nullptr, prec, M, N, K, B, true, &w);
   PC_CHECK(!work || ws_bytes >= need, PC_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (prec) {

@@ -100,8 +100,9 @@ struct Carver {
 };
 
 // 3-D tensor map over an Operand: dims {cols (K), rows, groups}, box {128 bytes of K,
-// box_rows, 1}, 128-byte swizzle, zero fill outside the tensor. part 1 = the lo half.
+// box_rows, 1}, 128-byte swizzle (or none), zero fill outside the tensor. part 1 = the lo
+// half.
 pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision_t p,
-                               int box_rows, int part);
+                               int box_rows, int part, bool swizzle = true);
 
 }  // namespace pc
