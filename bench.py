@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="hmm", choices=["hmm", "layer", "hclt", "lowrank"])
+    ap.add_argument("--hclt-nvars", type=int, default=768,
+                    help="HCLT variables (768 = the workload; fewer for a profiler-sized case)")
     return ap.parse_args()
 
 
@@ -176,12 +178,14 @@ class HcltWorkload(Workload):
             "flows dpi, dW, dE")
     data = "synthetic (seeded: parent[i] ~ U[0, i); softmax N(0,1) rows for pi, W, E; uniform categories)"
 
+    nvars = 768
+
     def inputs(self):
-        from workloads import hclt
-        return hclt()
+        from workloads import hclt, hclt_inputs
+        return hclt() if self.nvars == 768 else hclt_inputs(self.nvars, 1024, 512, 512, seed=5)
 
     def config(self):
-        return {"nvars": 768, "H": 1024, "C": 512, "B": 512}
+        return {"nvars": self.nvars, "H": 1024, "C": 512, "B": 512}
 
     def oracle(self, d, b):
         from oracle.hclt import hclt_fwd_bwd
@@ -276,11 +280,19 @@ def oracle_sample_rate(w, d, target_s: float = 12.0):
     return b / dt, desc, os.cpu_count(), b, dt
 
 
+def pick_workload(args):
+    w = WORKLOADS[args.workload]
+    if w.name == "hclt" and args.hclt_nvars != 768:
+        w.nvars = args.hclt_nvars
+        w.desc = w.desc.replace("768 variables", f"{args.hclt_nvars} variables")
+    return w
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = pick_workload(args)
     d = w.inputs()
     rate, desc, cores, b, _ = oracle_sample_rate(w, d, target_s=8.0)
     times = []
@@ -380,7 +392,7 @@ def run_ours(args):
 
     import log_space_sum_gb300 as pc
 
-    w = WORKLOADS[args.workload]
+    w = pick_workload(args)
     rank, world, local = dist_env()
     if world > 1:
         torch.cuda.set_device(local)

@@ -275,10 +275,11 @@ __global__ void k_transpose_add_groups(const float* __restrict__ src, int R, int
 // columns without touching global memory. Runs in the epilogue warps during the K loop.
 __device__ __forceinline__ void stage_block(const float* __restrict__ src, int H, int B, int m0, int n0,
                                             float* S, int et) {
+  constexpr int kCols = kBM / kEpiWarps;  // columns staged by one epilogue warp
   const int lane = et & 31;
-  const int c_begin = (et >> 5) * 32;
+  const int c_begin = (et >> 5) * kCols;
 #pragma unroll 1
-  for (int cb = c_begin; cb < c_begin + 32; cb += 8) {
+  for (int cb = c_begin; cb < c_begin + kCols; cb += 8) {
     float vals[8][4];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {

@@ -262,13 +262,15 @@ __global__ void k_dE_gather(const float* __restrict__ fbm, int H, const int* __r
 // Stages the CTA's emission block Es[c][r] = E[m0 + r, x_{t,b}] (b = n0 + c) into shared
 // memory: rows and columns outside the problem read 0. The epilogue warps do this
 // while the contraction's K loop runs, so the gathers are off the critical path.
-// Each warp owns 32 columns and issues 8 columns x 4 rows of loads per batch.
+// Each epilogue warp owns kBM / kEpiWarps columns and issues 8 columns x 4 rows of loads
+// per batch.
 __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, int H, int B, int m0, int n0,
                                                 const int* tok_s, float* Es, int et) {
+  constexpr int kCols = kBM / kEpiWarps;  // columns staged by one epilogue warp
   const int lane = et & 31;
-  const int c_begin = (et >> 5) * 32;
+  const int c_begin = (et >> 5) * kCols;
 #pragma unroll 1
-  for (int cb = c_begin; cb < c_begin + 32; cb += 8) {
+  for (int cb = c_begin; cb < c_begin + kCols; cb += 8) {
     float vals[8][4];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -316,7 +318,7 @@ struct EpiHmmFwd {
   __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
     float* c_s = reinterpret_cast<float*>(smem) + kChainBN;
-    for (int c = et; c < kChainBN; c += 128) {
+    for (int c = et; c < kChainBN; c += kEpiThreads) {
       const int b = n0 + c;
       int tok = 0;
       float cv = 0.f;
@@ -466,7 +468,7 @@ struct EpiHmmBwd : EpiNoHooks {
   __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
     float* c_s = reinterpret_cast<float*>(smem) + kChainBN;
-    for (int c = et; c < kChainBN; c += 128) {
+    for (int c = et; c < kChainBN; c += kEpiThreads) {
       const int b = n0 + c;
       tok_s[c] = b < p.B ? p.tokens[static_cast<long long>(b) * p.T + p.t + 1] : 0;
       c_s[c] = b < p.B ? p.cf[static_cast<long long>(p.t + 1) * p.B + b] : 0.f;

@@ -22,7 +22,13 @@
 
 namespace pc {
 
-constexpr int kGemmThreads = 192;
+// Warp 0: TMA producer; warp 1: MMA issuer; warps 2 .. 9: epilogue, two warps per TMEM
+// lane quarter, each taking every other 32-column chunk of the tile.
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kGemmThreads = 64 + kEpiThreads;
+// (Ten warps place three on some SM sub-partitions, whose 16K registers then allow 168
+// per thread; the launch bounds let the compiler plan for that.)
 constexpr int kBM = 128;
 
 template <int P, int BN>
@@ -35,7 +41,7 @@ struct GemmShape {
   static constexpr uint32_t kStageBytes = kParts * (kABytes + kBBytes);
   static constexpr uint32_t kUmmaK = (P == kBF16) ? 16 : 8;  // K per MMA instruction
   static constexpr uint32_t kKSteps = kBK / kUmmaK;          // MMAs per ring slot (4)
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: two epilogue warps split the 32-column chunks");
 };
 
 // Accumulation slices, in MMA k-steps (1, or a multiple of the k-steps of one ring
@@ -62,7 +68,7 @@ constexpr size_t kSmemPerCta = 232448;  // opt-in maximum dynamic shared memory 
 template <int P, int BN, class Epi>
 struct GemmPlan {
   using S = GemmShape<P, BN>;
-  static constexpr size_t kTBufBytes = Epi::kTranspose ? 4 * kTBufFloats * sizeof(float) : 0;
+  static constexpr size_t kTBufBytes = Epi::kTranspose ? kEpiWarps * kTBufFloats * sizeof(float) : 0;
   static constexpr size_t kEpiBytes = ((Epi::kSmemBytes + 15) / 16) * 16;
   static constexpr size_t kFixed = 1024 /* alignment slack */ + 256 /* barriers */ + kTBufBytes + kEpiBytes;
   static constexpr int kFit = static_cast<int>((kSmemPerCta - kFixed) / S::kStageBytes);
@@ -90,19 +96,19 @@ __device__ __forceinline__ void warp_transpose32(const float (&v)[32], float (&w
 }
 
 __device__ __forceinline__ void epilogue_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
-// Named barrier of the 128 epilogue threads that also ANDs a predicate over them.
+// Named barrier of the epilogue threads that also ANDs a predicate over them.
 __device__ __forceinline__ bool epilogue_bar_and(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred pi, po;\n\t"
       "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, 1, 128, pi;\n\t"
+      "bar.red.and.pred po, 1, %2, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
+      : "r"(static_cast<uint32_t>(v)), "n"(kEpiThreads)
       : "memory");
   return r != 0;
 }
@@ -287,33 +293,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------- epilogue
-    const int et = threadIdx.x - 64;  // 0..127
+    const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
+    const int ew = warp - 2;          // epilogue warp 0 .. 7
     Epi::prepare(ep, g, m0, n0, et, epi_smem);
     epilogue_bar_sync();
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    const int half = ew >> 2;     // chunks c with (c & 1) == half
     const int row = q * 32 + lane;
-    float* tbuf = Epi::kTranspose ? tbuf_base + q * kTBufFloats : nullptr;
+    float* tbuf = Epi::kTranspose ? tbuf_base + ew * kTBufFloats : nullptr;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    constexpr int kChunks = BN / 64;  // 32-column chunks per epilogue warp
     bool ok = true;
     if constexpr (kSliced) {
-      float acc[BN / 32][32];
+      float acc[kChunks][32];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
+      for (int c = 0; c < kChunks; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[c][i] = 0.f;
       const int total_q = num_kb * static_cast<int>(S::kKSteps);
       const int num_slices = (total_q + kSliceK - 1) / kSliceK;
       for (int sl = 0; sl < num_slices; ++sl) {
         const int buf = sl % kAccBufs;
-        // all 128 epilogue threads agree on whether the slice arrived
+        // all epilogue threads agree on whether the slice arrived
         ok = epilogue_bar_and(
             mbar_wait(&acc_full[buf], (sl / kAccBufs) & 1, status, kErrTimeoutEpilogue));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < kChunks; ++c) {
           float v[32];
-          tmem_ld_32x32(lane_base + static_cast<uint32_t>(buf * BN + c * 32), v);
+          tmem_ld_32x32(lane_base + static_cast<uint32_t>(buf * BN + (2 * c + half) * 32), v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[c][i] += kHalfUlp ? v[i] + half_ulp(v[i]) : v[i];
         }
@@ -323,8 +332,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          Epi::apply(ep, g, m0, n0, row, c * 32, acc[c], epi_smem, tbuf);
+        for (int c = 0; c < kChunks; ++c) {
+          Epi::apply(ep, g, m0, n0, row, (2 * c + half) * 32, acc[c], epi_smem, tbuf);
         }
       }
     } else {
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       if (ok) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = half * 32; c < BN; c += 64) {
           float v[32];
           tmem_ld_32x32(lane_base + static_cast<uint32_t>(c), v);
           Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
