@@ -12,15 +12,16 @@
 // last), so the edges whose child has height L form one contiguous run of slots: one
 // grouped contraction per level, the groups evenly strided in every operand.
 //
-// Values. Every node keeps u_v[b][z] = n_v(z) / max_z n_v(z) (so max_z u_v = 1) and a
-// per-sample log-offset O_v[b] = log max_z n_v in double. Each edge's sum layer
+// Values. Every node keeps u_v[b][z] = n_v(z) / max_z n_v(z) (so max_z u_v = 1) and its
+// own log max as an integer exponent and a float32 log-mantissa. Each edge's sum layer
 //   D_c[b][z] = sum_{z'} W_c[z,z'] u_c[b][z']
 // is kept linear, and the product layer multiplies in float32 with an exact power-of-two
 // exponent carried beside every running product, so a node with many children cannot
 // underflow and no rounding but the multiplies' own round-to-nearest enters:
 //   n'_v[b][z] = E_v[z, x_v] * prod_c D_c[b][z] = m_z 2^{e_z}   (m_z in [1/2, 1)),
-//   u_v = n'_v / max_z n'_v,   O_v = log max_z n'_v + sum_c O_c,
-//   LL_b = O_0[b] + log sum_z pi[z] u_0[b][z].
+//   u_v = n'_v / max_z n'_v,
+//   LL_b = sum over all nodes v of log max_z n'_v[b]  +  log sum_z pi[z] u_0[b][z]
+// (every node lies under the root), summed in double once per sample at the end.
 // (Taking logs instead would round every y = log E + sum log D to float32 at |y| of
 // several nats, an error of ~1e-7 per node that a 768-node tree accumulates.)
 // Backward (root flow 1; product nodes pass their flow to every child):
@@ -42,40 +43,69 @@ namespace {
 constexpr int kHcltBN = 128;
 
 // ------------------------------------------------------------------ set-up
-// Et[v][k][z] = E[v][z][k]: per-variable transpose, so that the emissions of one category
-// are a contiguous row over the latents.
-__global__ void k_hclt_et(const float* __restrict__ E, int H, int C, float* __restrict__ Et) {
-  __shared__ float tile[32][33];
-  const long long v = blockIdx.z;
-  const int k0 = blockIdx.x * 32, z0 = blockIdx.y * 32;
-  const float* src = E + v * H * C;
-  float* dst = Et + v * H * C;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int z = z0 + i, k = k0 + threadIdx.x;
-    tile[i][threadIdx.x] = (z < H && k < C) ? src[static_cast<long long>(z) * C + k] : 0.f;
+
+// m 2^e with m in [1/2, 1) and the exponent added to e, for p >= 0 (0 stays 0). Normal
+// values by their bit fields; zero and subnormal products through frexpf.
+__device__ __forceinline__ float renorm(float p, int& e) {
+  const uint32_t bits = __float_as_uint(p);
+  const uint32_t f = bits >> 23;
+  if (f == 0u) {
+    if (bits == 0u) return 0.f;
+    int k;
+    const float r = frexpf(p, &k);
+    e += k;
+    return r;
   }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int k = k0 + i, z = z0 + threadIdx.x;
-    if (z < H && k < C) dst[static_cast<long long>(k) * H + z] = tile[threadIdx.x][i];
+  e += static_cast<int>(f) - 126;
+  return __uint_as_float((bits & 0x007FFFFFu) | (126u << 23));
+}
+
+// 2^d for d <= 0 (0 below the subnormal range).
+__device__ __forceinline__ float pow2_nonpos(int d) {
+  if (d >= -126) return __uint_as_float(static_cast<uint32_t>(d + 127) << 23);
+  return d >= -149 ? ldexpf(1.f, d) : 0.f;
+}
+
+// Four operand values at idx (idx % 4 == 0, rows 64-element aligned).
+template <int P>
+__device__ __forceinline__ void store_operand4(void* base, size_t idx, size_t lo, float4 v) {
+  if constexpr (P == kBF16) {
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + idx) =
+        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  } else {
+    const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx) = h;
+    if constexpr (P == kTF32x3)
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx + lo) =
+          make_float4(tf32_rna(v.x - h.x), tf32_rna(v.y - h.y), tf32_rna(v.z - h.z), tf32_rna(v.w - h.w));
   }
 }
 
 // Product layer of the nodes in slots [s0, s0 + gridDim.x), one block per (node, sample):
 // n' = E_v[., x_v] * prod_children D as float32 mantissas in [1/2, 1) with int exponents,
-// u = n' / max n' (float32 and operand copies), O = log max n' + sum_children O. For the
-// root it also forms LL and 1 / sum pi u.
-template <int P>
-__global__ void k_hclt_product(int s0, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
-                               const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr,
-                               const int* __restrict__ child_slots, const float* __restrict__ Et,
-                               const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
-                               long long uop_ld, size_t uop_lo, double* __restrict__ O, const float* __restrict__ pi,
-                               double* __restrict__ ll, float* __restrict__ rroot) {
-  extern __shared__ float mant[];  // H mantissas, then H exponents
-  int* expo = reinterpret_cast<int*>(mant + H);
+// u = n' / max n' (float32 and operand copies), and the node's own log max n' as its
+// exponent Ex and float32 log-mantissa Lm; for the root also sum_z pi u (rdot). Each
+// thread takes runs of four latents: 16-byte loads and stores when H % 4 == 0 (kVec),
+// element by element otherwise. No double-precision arithmetic: this GPU's FP64 pipe is
+// narrow, and the log-likelihood's double sum is formed once per sample (k_hclt_ll).
+template <bool kVec>
+__device__ __forceinline__ float4 load_run4(const float* row, int q, int H) {
+  if constexpr (kVec) return reinterpret_cast<const float4*>(row)[q];
+  const int z = 4 * q;
+  return make_float4(row[z], z + 1 < H ? row[z + 1] : 0.f, z + 2 < H ? row[z + 2] : 0.f, z + 3 < H ? row[z + 3] : 0.f);
+}
+
+template <int P, bool kVec>
+__global__ void __launch_bounds__(256) k_hclt_product(
+    int s0, int root_slot, int nvars, int H, int B, const int* __restrict__ data, const int* __restrict__ var_of_slot,
+    const int* __restrict__ child_ptr, const int* __restrict__ child_slots, const float* __restrict__ Et,
+    const float* __restrict__ D, int C, float* __restrict__ U32, void* uop, long long uop_ld, size_t uop_lo,
+    int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi, float* __restrict__ rdot) {
+  extern __shared__ float4 mant4[];  // ceil(H/4) mantissa runs, then as many exponent runs
+  const int H4 = (H + 3) / 4;
+  int4* expo4 = reinterpret_cast<int4*>(mant4 + H4);
   __shared__ long long red[32];
-  __shared__ double redd[32];
+  __shared__ float redf[32];
   constexpr long long kNone = -0x7fffffffffffffffLL - 1;  // key of a zero product
   const int s = s0 + blockIdx.x;
   const int b = blockIdx.y;
@@ -86,24 +116,32 @@ __global__ void k_hclt_product(int s0, int root_slot, int nvars, int H, int B, c
   const float* er = Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H;
   // key = e * 2^32 + bits(m) orders the nonzero products m 2^e (m in [1/2, 1)) by value
   long long best = kNone;
-  for (int z = threadIdx.x; z < H; z += blockDim.x) {
-    int e, k;
-    float m = frexpf(xin ? er[z] : 0.f, &e);
+  for (int q = threadIdx.x; q < H4; q += blockDim.x) {
+    const float4 ev = xin ? load_run4<kVec>(er, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float m[4] = {ev.x, ev.y, ev.z, ev.w};
+    int e[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = renorm(m[k], e[k]);
     for (int c = c0; c < c1; ++c) {
-      m = frexpf(m * D[(static_cast<long long>(child_slots[c]) * B + b) * H + z], &k);
-      e += k;
+      const float4 d = load_run4<kVec>(D + (static_cast<long long>(child_slots[c]) * B + b) * H, q, H);
+      m[0] = renorm(m[0] * d.x, e[0]);
+      m[1] = renorm(m[1] * d.y, e[1]);
+      m[2] = renorm(m[2] * d.z, e[2]);
+      m[3] = renorm(m[3] * d.w, e[3]);
     }
-    mant[z] = m;
-    expo[z] = e;
-    if (m > 0.f) best = max(best, static_cast<long long>(e) * 4294967296LL + __float_as_uint(m));
+    mant4[q] = make_float4(m[0], m[1], m[2], m[3]);
+    expo4[q] = make_int4(e[0], e[1], e[2], e[3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (m[k] > 0.f) best = max(best, static_cast<long long>(e[k]) * 4294967296LL + __float_as_uint(m[k]));
   }
   for (int o = 16; o; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
   __syncthreads();
   if (threadIdx.x < 32) {
-    long long m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : kNone;
-    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (threadIdx.x == 0) red[0] = m;
+    long long mx = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : kNone;
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (threadIdx.x == 0) red[0] = mx;
   }
   __syncthreads();
   best = red[0];
@@ -111,33 +149,177 @@ __global__ void k_hclt_product(int s0, int root_slot, int nvars, int H, int B, c
   const unsigned mbits = static_cast<unsigned>(best & 0xffffffffLL);
   const int emax = live ? static_cast<int>((best - static_cast<long long>(mbits)) / 4294967296LL) : 0;
   const float mmax = live ? __uint_as_float(mbits) : 1.f;
+  const float rinv = 1.f / mmax;
   const long long row = static_cast<long long>(s) * B + b;
-  double dot = 0.0;
-  for (int z = threadIdx.x; z < H; z += blockDim.x) {
-    const float m = mant[z];
-    const float u = (live && m > 0.f) ? ldexpf(m / mmax, expo[z] - emax) : 0.f;
-    U32[row * H + z] = u;
-    if (uop) store_operand<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
-    if (s == root_slot) dot += static_cast<double>(pi[z]) * u;
+  float* u32 = U32 + row * H;
+  float dot = 0.f;
+  for (int q = threadIdx.x; q < H4; q += blockDim.x) {
+    const float4 m = mant4[q];
+    const int4 e = expo4[q];
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      u.x = m.x > 0.f ? (m.x * rinv) * pow2_nonpos(e.x - emax) : 0.f;
+      u.y = m.y > 0.f ? (m.y * rinv) * pow2_nonpos(e.y - emax) : 0.f;
+      u.z = m.z > 0.f ? (m.z * rinv) * pow2_nonpos(e.z - emax) : 0.f;
+      u.w = m.w > 0.f ? (m.w * rinv) * pow2_nonpos(e.w - emax) : 0.f;
+    }
+    const int z = 4 * q;
+    if constexpr (kVec) {
+      reinterpret_cast<float4*>(u32)[q] = u;
+      if (uop) store_operand4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
+    } else {
+      const float uu[4] = {u.x, u.y, u.z, u.w};
+      for (int k = 0; k < 4 && z + k < H; ++k) {
+        u32[z + k] = uu[k];
+        if (uop) store_operand<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
+      }
+    }
+    if (s == root_slot) {
+      const float4 pz = load_run4<kVec>(pi, q, H);  // zero beyond H, where u is zero too
+      dot += (pz.x * u.x + pz.y * u.y) + (pz.z * u.z + pz.w * u.w);
+    }
   }
   if (threadIdx.x == 0) {
-    double off = live ? static_cast<double>(emax) * 0.69314718055994530942 + log(static_cast<double>(mmax))
-                      : -static_cast<double>(INFINITY);
-    for (int c = c0; c < c1; ++c) off += O[static_cast<long long>(child_slots[c]) * B + b];
-    O[row] = off;
+    Ex[row] = live ? emax : 0;
+    Lm[row] = live ? logf(mmax) : -INFINITY;
   }
   if (s != root_slot) return;
   for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-  if ((threadIdx.x & 31) == 0) redd[threadIdx.x >> 5] = dot;
+  if ((threadIdx.x & 31) == 0) redf[threadIdx.x >> 5] = dot;
   __syncthreads();
   if (threadIdx.x == 0) {
-    double t = 0.0;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += redd[w];
-    const double off = O[row];
-    const bool zero = !(t > 0.0) || !(off > -static_cast<double>(INFINITY));
-    ll[b] = zero ? -static_cast<double>(INFINITY) : off + log(t);
-    rroot[b] = zero ? 0.f : static_cast<float>(1.0 / t);
+    float tt = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tt += redf[w];
+    rdot[b] = tt;
   }
+}
+
+// The same product layer with one warp per (node, sample) for H <= 1024: every lane keeps
+// its runs of four latents in registers (eight runs at most), the maximum is a warp
+// reduction, and a lane's loads of one child row are independent, so they are all in
+// flight together. Warp w of the launch takes node s0 + w / B, sample w % B.
+constexpr int kWarpRuns = 8;  // runs of four latents per lane: H <= 4 * 32 * 8
+template <int P, bool kVec>
+__global__ void __launch_bounds__(256) k_hclt_product_warp(
+    int s0, int G, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
+    const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr, const int* __restrict__ child_slots,
+    const float* __restrict__ Et, const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
+    long long uop_ld, size_t uop_lo, int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi,
+    float* __restrict__ rdot) {
+  constexpr long long kNone = -0x7fffffffffffffffLL - 1;
+  const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (wid >= static_cast<long long>(G) * B) return;  // the whole warp leaves together
+  const int lane = threadIdx.x & 31;
+  const int s = s0 + static_cast<int>(wid / B);
+  const int b = static_cast<int>(wid % B);
+  const int v = var_of_slot[s];
+  const int x = data[static_cast<long long>(b) * nvars + v];
+  const bool xin = x >= 0 && x < C;
+  const int c0 = child_ptr[s], c1 = child_ptr[s + 1];
+  const float* er = Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H;
+  float m[kWarpRuns][4];
+  int e[kWarpRuns][4];
+#pragma unroll
+  for (int r = 0; r < kWarpRuns; ++r) {
+    const int q = lane + 32 * r;
+    const float4 ev = (xin && 4 * q < H) ? load_run4<kVec>(er, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
+    m[r][0] = ev.x;
+    m[r][1] = ev.y;
+    m[r][2] = ev.z;
+    m[r][3] = ev.w;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      e[r][k] = 0;
+      m[r][k] = renorm(m[r][k], e[r][k]);
+    }
+  }
+  for (int c = c0; c < c1; ++c) {
+    const float* drow = D + (static_cast<long long>(child_slots[c]) * B + b) * H;
+    float4 d[kWarpRuns];
+#pragma unroll
+    for (int r = 0; r < kWarpRuns; ++r) {
+      const int q = lane + 32 * r;
+      d[r] = 4 * q < H ? load_run4<kVec>(drow, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < kWarpRuns; ++r) {
+      m[r][0] = renorm(m[r][0] * d[r].x, e[r][0]);
+      m[r][1] = renorm(m[r][1] * d[r].y, e[r][1]);
+      m[r][2] = renorm(m[r][2] * d[r].z, e[r][2]);
+      m[r][3] = renorm(m[r][3] * d[r].w, e[r][3]);
+    }
+  }
+  long long best = kNone;
+#pragma unroll
+  for (int r = 0; r < kWarpRuns; ++r)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (m[r][k] > 0.f) best = max(best, static_cast<long long>(e[r][k]) * 4294967296LL + __float_as_uint(m[r][k]));
+  for (int o = 16; o; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  const bool live = best != kNone;
+  const unsigned mbits = static_cast<unsigned>(best & 0xffffffffLL);
+  const int emax = live ? static_cast<int>((best - static_cast<long long>(mbits)) / 4294967296LL) : 0;
+  const float mmax = live ? __uint_as_float(mbits) : 1.f;
+  const float rinv = 1.f / mmax;
+  const long long row = static_cast<long long>(s) * B + b;
+  float* u32 = U32 + row * H;
+  float dot = 0.f;
+#pragma unroll
+  for (int r = 0; r < kWarpRuns; ++r) {
+    const int q = lane + 32 * r;
+    const int z = 4 * q;
+    if (z >= H) continue;
+    float uu[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      uu[k] = (live && m[r][k] > 0.f) ? (m[r][k] * rinv) * pow2_nonpos(e[r][k] - emax) : 0.f;
+    const float4 u = make_float4(uu[0], uu[1], uu[2], uu[3]);
+    if constexpr (kVec) {
+      reinterpret_cast<float4*>(u32)[q] = u;
+      if (uop) store_operand4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
+    } else {
+      for (int k = 0; k < 4 && z + k < H; ++k) {
+        u32[z + k] = uu[k];
+        if (uop) store_operand<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
+      }
+    }
+    if (s == root_slot) {
+      const float4 pz = load_run4<kVec>(pi, q, H);
+      dot += (pz.x * u.x + pz.y * u.y) + (pz.z * u.z + pz.w * u.w);
+    }
+  }
+  if (lane == 0) {
+    Ex[row] = live ? emax : 0;
+    Lm[row] = live ? logf(mmax) : -INFINITY;
+  }
+  if (s != root_slot) return;
+  for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  if (lane == 0) rdot[b] = dot;
+}
+
+// The log-likelihood. Every node lies under the root, so the root's offset is the sum over
+// all nodes of their own log max: LL_b = ln 2 sum_v e_v[b] + sum_v log m_v[b] +
+// log sum_z pi u_0[b][z], summed in double (the exponents exactly, as integers); also
+// 1 / sum_z pi u_0 for the root flows. One thread per sample.
+__global__ void k_hclt_ll(int nslots, int B, const int* __restrict__ Ex, const float* __restrict__ Lm,
+                          const float* __restrict__ rdot, double* __restrict__ ll, float* __restrict__ rroot) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  long long esum = 0;
+  double lsum = 0.0;
+  bool live = true;
+  for (int s = 0; s < nslots; ++s) {
+    const long long idx = static_cast<long long>(s) * B + b;
+    const float l = Lm[idx];
+    live = live && l > -INFINITY;
+    esum += Ex[idx];
+    lsum += static_cast<double>(l);
+  }
+  const float dot = rdot[b];
+  live = live && dot > 0.f;
+  ll[b] = live ? static_cast<double>(esum) * 0.69314718055994530942 + lsum + log(static_cast<double>(dot))
+               : -static_cast<double>(INFINITY);
+  rroot[b] = live ? 1.f / dot : 0.f;
 }
 
 // Root flows f_0[b][z] = pi[z] u_0[b][z] / sum_z pi u_0 (batch-major) and dpi += sum_b f_0.
@@ -160,32 +342,50 @@ __global__ void k_hclt_root_flows(int root_slot, int H, int B, const float* __re
 
 // The layer's scaled flows of the edges in slots [s0, s0 + G): g[b][z] = f_parent[b][z] /
 // D[b][z] (0 where D = 0), written batch-major (element contraction operand) and
-// node-major (parameter contraction operand) through a 32 x 32 shared-memory tile.
-template <int P>
-__global__ void k_hclt_scaled_flows(int s0, int H, int B, const int* __restrict__ parent_slot,
-                                    const float* __restrict__ F32, const float* __restrict__ D, void* gbm,
-                                    long long gbm_ld, size_t gbm_lo, void* gnm, long long gnm_ld, size_t gnm_lo) {
-  __shared__ float tile[32][33];
+// node-major (parameter contraction operand) through a 64 x 64 shared-memory tile; runs of
+// four latents per load (16-byte accesses when kVec), runs of eight samples per
+// node-major store.
+template <int P, bool kVec>
+__global__ void __launch_bounds__(256) k_hclt_scaled_flows(int s0, int H, int B, const int* __restrict__ parent_slot,
+                                                           const float* __restrict__ F32, const float* __restrict__ D,
+                                                           void* gbm, long long gbm_ld, size_t gbm_lo, void* gnm,
+                                                           long long gnm_ld, size_t gnm_lo) {
+  __shared__ float tile[64][65];
   const int g = blockIdx.z;
   const int s = s0 + g;
   const int ps = parent_slot[s];
-  const int z0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int b = b0 + i, z = z0 + threadIdx.x;
-    float w = 0.f;
+  const int z0 = blockIdx.x * 64, b0 = blockIdx.y * 64;
+  for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+    const int bb = i >> 4, zq = (i & 15) * 4;
+    const int b = b0 + bb, z = z0 + zq;
+    float w[4] = {0.f, 0.f, 0.f, 0.f};
     if (b < B && z < H) {
-      const float d = D[(static_cast<long long>(s) * B + b) * H + z];
-      w = d > 0.f ? F32[(static_cast<long long>(ps) * B + b) * H + z] / d : 0.f;
-      store_operand<P>(gbm, static_cast<size_t>((static_cast<long long>(g) * B + b) * gbm_ld + z), gbm_lo, w);
+      const float4 d = load_run4<kVec>(D + (static_cast<long long>(s) * B + b) * H, z >> 2, H);
+      const float4 f = load_run4<kVec>(F32 + (static_cast<long long>(ps) * B + b) * H, z >> 2, H);
+      w[0] = d.x > 0.f ? f.x / d.x : 0.f;
+      w[1] = d.y > 0.f ? f.y / d.y : 0.f;
+      w[2] = d.z > 0.f ? f.z / d.z : 0.f;
+      w[3] = d.w > 0.f ? f.w / d.w : 0.f;
+      const size_t idx = static_cast<size_t>((static_cast<long long>(g) * B + b) * gbm_ld + z);
+      if constexpr (kVec) {
+        store_operand4<P>(gbm, idx, gbm_lo, make_float4(w[0], w[1], w[2], w[3]));
+      } else {
+        for (int k = 0; k < 4 && z + k < H; ++k) store_operand<P>(gbm, idx + k, gbm_lo, w[k]);
+      }
     }
-    tile[i][threadIdx.x] = w;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tile[bb][zq + k] = w[k];
   }
   __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int z = z0 + i, b = b0 + threadIdx.x;
-    if (b < B && z < H)
-      store_operand<P>(gnm, static_cast<size_t>((static_cast<long long>(g) * H + z) * gnm_ld + b), gnm_lo,
-                       tile[threadIdx.x][i]);
+  const StoreOperand<P> st{gnm, gnm_ld, gnm_lo, static_cast<long long>(H)};
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int zz = i >> 3, bq = (i & 7) * 8;
+    const int z = z0 + zz, b = b0 + bq;
+    if (z >= H || b >= B) continue;
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = tile[bq + k][zz];
+    st(g, z, b, v, min(8, B - b));
   }
 }
 
@@ -248,27 +448,6 @@ __global__ void k_hclt_dE_gather(int H, int B, int C, const int* __restrict__ va
   }
 }
 
-// dst[g][c][r] (+)= src[g][r][c] for G matrices of R x C.
-__global__ void k_transpose_add_groups(const float* __restrict__ src, int R, int C, float* __restrict__ dst,
-                                       int accumulate) {
-  __shared__ float tile[32][33];
-  const long long g = blockIdx.z;
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  const float* sg = src + g * R * C;
-  float* dg = dst + g * R * C;
-  for (int k = threadIdx.y; k < 32; k += 8) {
-    const int r = r0 + k, c = c0 + threadIdx.x;
-    tile[k][threadIdx.x] = (r < R && c < C) ? sg[static_cast<long long>(r) * C + c] : 0.f;
-  }
-  __syncthreads();
-  for (int k = threadIdx.y; k < 32; k += 8) {
-    const int c = c0 + k, r = r0 + threadIdx.x;
-    if (r < R && c < C) {
-      float* d = dg + static_cast<long long>(c) * R + r;
-      *d = accumulate ? *d + tile[threadIdx.x][k] : tile[threadIdx.x][k];
-    }
-  }
-}
 
 // Copies a 128 x 128 block rows[n0 + c][m0 + r] of a row-major [B][H] array into
 // shared memory as S[c][r] (0 outside), so an epilogue thread owning row r reads its 32
@@ -427,8 +606,8 @@ Operand operand_view(const Operand& op, pc_precision_t p, long long first, long 
 struct HcltWs {
   int* plan;
   Operand Wop, WopT, Uop, Gbm, Gnm, Unm;
-  float *Et, *U32, *D, *rroot, *F32, *dEt;
-  double* O;
+  float *Et, *U32, *D, *rroot, *rdot, *Lm, *F32, *dEt;
+  int* Ex;
   int *cat_order, *cat_off;
 };
 
@@ -442,8 +621,10 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
   w->U32 = static_cast<float*>(c.take(size_t(n) * B * H * 4));
   w->Uop = c.operand(p, E1, B, H);
   w->D = static_cast<float*>(c.take(size_t(E1) * B * H * 4));
-  w->O = static_cast<double*>(c.take(size_t(n) * B * 8));
+  w->Ex = static_cast<int*>(c.take(size_t(n) * B * 4));
+  w->Lm = static_cast<float*>(c.take(size_t(n) * B * 4));
   w->rroot = static_cast<float*>(c.take(size_t(B) * 4));
+  w->rdot = static_cast<float*>(c.take(size_t(B) * 4));
   if (flows) {
     w->WopT = c.operand(p, E1, H, H);
     w->F32 = static_cast<float*>(c.take(size_t(n) * B * H * 4));
@@ -499,25 +680,36 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dW && !accumulate) PC_CUDA(cudaMemsetAsync(dW, 0, size_t(H) * H * 4, s));  // W[0] has no edge
 
-  k_hclt_et<<<dim3(cdiv(C, 32), cdiv(H, 32), n), dim3(32, 8), 0, s>>>(Em, H, C, w.Et);
-  PC_LAUNCH_CHECK();
+  // Et[v][k][z] = E[v][z][k]: the emissions of one category are a contiguous row
+  if ((st = transpose_f32(Em, C, static_cast<long long>(H) * C, n, H, C, w.Et, H, 0, s)) != PC_OK) return st;
   if (E > 0 && (st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, d_var)) != PC_OK)
     return st;
 
   // -------------------------------------------------------------- forward
-  const size_t prod_smem = size_t(H) * 8;  // mantissas and exponents, up to 64 KB
-  if (prod_smem > 48 * 1024)
-    PC_CUDA(cudaFuncSetAttribute(k_hclt_product<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t prod_smem = size_t((H + 3) / 4) * 32;  // mantissa and exponent runs, up to 64 KB
+  const bool prod_vec = H % 4 == 0 && aligned16(pi);
+  if (prod_smem > 48 * 1024) {
+    PC_CUDA(cudaFuncSetAttribute(k_hclt_product<P, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(prod_smem)));
+    PC_CUDA(cudaFuncSetAttribute(k_hclt_product<P, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prod_smem)));
+  }
   OperandMaps ma, mb;
   for (int L = 0; L <= pl.maxh; ++L) {
     const int sA = pl.level_start[L], sB = pl.level_start[L + 1];
     const int G = sB - sA;
     if (G <= 0) continue;
     const bool edges = L < pl.maxh;
-    k_hclt_product<P><<<dim3(G, B), 256, prod_smem, s>>>(
-        sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, w.U32, edges ? w.Uop.ptr : nullptr,
-        w.Uop.ld, w.Uop.lo_elems, w.O, pi, ll, w.rroot);
+    if (H <= 4 * 32 * kWarpRuns) {
+      const unsigned blocks = static_cast<unsigned>(cdiv(static_cast<long long>(G) * B, 8));
+      (prod_vec ? k_hclt_product_warp<P, true> : k_hclt_product_warp<P, false>)<<<blocks, 256, 0, s>>>(
+          sA, G, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, w.U32, edges ? w.Uop.ptr : nullptr,
+          w.Uop.ld, w.Uop.lo_elems, w.Ex, w.Lm, pi, w.rdot);
+    } else {
+      (prod_vec ? k_hclt_product<P, true> : k_hclt_product<P, false>)<<<dim3(G, B), 256, prod_smem, s>>>(
+          sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, w.U32, edges ? w.Uop.ptr : nullptr,
+          w.Uop.ld, w.Uop.lo_elems, w.Ex, w.Lm, pi, w.rdot);
+    }
     PC_LAUNCH_CHECK();
     if (!edges) continue;
     if ((st = encode_maps(&ma, operand_view(w.Wop, prec, sA, G), prec, kBM)) != PC_OK) return st;
@@ -528,6 +720,8 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
                                                   2ll * G * H * H * B)) != PC_OK)
       return st;
   }
+  k_hclt_ll<<<cdiv(B, 128), 128, 0, s>>>(n, B, w.Ex, w.Lm, w.rdot, ll, w.rroot);
+  PC_LAUNCH_CHECK();
   if (!flows) return PC_OK;
 
   // ------------------------------------------------------------- backward
@@ -540,7 +734,8 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       const int sA = pl.level_start[L], sB = pl.level_start[L + 1];
       const int G = sB - sA;
       if (G <= 0) continue;
-      k_hclt_scaled_flows<P><<<dim3(cdiv(H, 32), cdiv(B, 32), G), dim3(32, 8), 0, s>>>(
+      (prod_vec ? k_hclt_scaled_flows<P, true> : k_hclt_scaled_flows<P, false>)<<<dim3(cdiv(H, 64), cdiv(B, 64), G),
+                                                                                 256, 0, s>>>(
           sA, H, B, d_pslot, w.F32, w.D, w.Gbm.ptr, w.Gbm.ld, w.Gbm.lo_elems, w.Gnm.ptr, w.Gnm.ld,
           w.Gnm.lo_elems);
       PC_LAUNCH_CHECK();
@@ -572,8 +767,8 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     PC_LAUNCH_CHECK();
     k_hclt_dE_gather<<<dim3(n, C), 256, 0, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, w.dEt);
     PC_LAUNCH_CHECK();
-    k_transpose_add_groups<<<dim3(cdiv(H, 32), cdiv(C, 32), n), dim3(32, 8), 0, s>>>(w.dEt, C, H, dE, accumulate);
-    PC_LAUNCH_CHECK();
+    if ((st = transpose_f32(w.dEt, H, static_cast<long long>(C) * H, n, C, H, dE, C, accumulate, s)) != PC_OK)
+      return st;
   }
   return PC_OK;
 }

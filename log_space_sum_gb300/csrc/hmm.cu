@@ -40,38 +40,6 @@ namespace {
 constexpr int kChainBN = 128;
 
 // ------------------------------------------------------------------ set-up
-__global__ void k_transpose_f32(const float* __restrict__ src, int R, int C, float* __restrict__ dst) {
-  __shared__ float tile[32][33];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  for (int k = threadIdx.y; k < 32; k += 8) {
-    const int r = r0 + k, c = c0 + threadIdx.x;
-    tile[k][threadIdx.x] = (r < R && c < C) ? src[static_cast<long long>(r) * C + c] : 0.f;
-  }
-  __syncthreads();
-  for (int k = threadIdx.y; k < 32; k += 8) {
-    const int c = c0 + k, r = r0 + threadIdx.x;
-    if (r < R && c < C) dst[static_cast<long long>(c) * R + r] = tile[threadIdx.x][k];
-  }
-}
-
-// dst[c][r] (+)= src[r][c]
-__global__ void k_transpose_add_f32(const float* __restrict__ src, int R, int C, float* __restrict__ dst,
-                                    int accumulate) {
-  __shared__ float tile[32][33];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  for (int k = threadIdx.y; k < 32; k += 8) {
-    const int r = r0 + k, c = c0 + threadIdx.x;
-    tile[k][threadIdx.x] = (r < R && c < C) ? src[static_cast<long long>(r) * C + c] : 0.f;
-  }
-  __syncthreads();
-  for (int k = threadIdx.y; k < 32; k += 8) {
-    const int c = c0 + k, r = r0 + threadIdx.x;
-    if (r < R && c < C) {
-      float* d = dst + static_cast<long long>(c) * R + r;
-      *d = accumulate ? *d + tile[threadIdx.x][k] : tile[threadIdx.x][k];
-    }
-  }
-}
 
 // rs[k] = sum_l A[k,l], one warp per row (float: it only feeds an upper bound).
 __global__ void k_rowsum(const float* __restrict__ A, int H, float* __restrict__ rs) {
@@ -605,8 +573,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   if (dA && !accumulate && T < 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
 
   // set-up: E transposed, row sums of A, emission bounds, operand copies of A
-  k_transpose_f32<<<dim3(cdiv(V, 32), cdiv(H, 32)), dim3(32, 8), 0, s>>>(E, H, V, w.Et);
-  PC_LAUNCH_CHECK();
+  if ((st = transpose_f32(E, V, 0, 1, H, V, w.Et, H, 0, s)) != PC_OK) return st;  // Et[v][k] = E[k][v]
   k_rowsum<<<cdiv(H, 8), 256, 0, s>>>(A, H, w.rs);
   PC_LAUNCH_CHECK();
   k_emission_bounds<<<V, 256, 0, s>>>(w.Et, w.rs, H, w.emax, w.emax_rs);
@@ -703,8 +670,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   if (dE) {
     k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
     PC_LAUNCH_CHECK();
-    k_transpose_add_f32<<<dim3(cdiv(H, 32), cdiv(V, 32)), dim3(32, 8), 0, s>>>(w.dEt, V, H, dE, accumulate);
-    PC_LAUNCH_CHECK();
+    if ((st = transpose_f32(w.dEt, H, 0, 1, V, H, dE, V, accumulate, s)) != PC_OK) return st;
   }
   return PC_OK;
 }

@@ -72,29 +72,6 @@ __global__ void k_rows_to_operand(const float* __restrict__ src, long long src_l
   }
 }
 
-// dst[g][c][r] = op(src[g][r][c]) through 32x32 shared-memory tiles.
-template <int P>
-__global__ void k_transpose_to_operand(const float* __restrict__ src, long long src_ld,
-                                       long long src_gs, int R, int C, void* dst,
-                                       long long dst_ld, size_t lo, const int* gmap) {
-  __shared__ float tile[32][33];
-  const int g = blockIdx.z;
-  const long long gs = gmap ? gmap[g] : g;
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  for (int k = ty; k < 32; k += 8) {
-    const int r = r0 + k, c = c0 + tx;
-    tile[k][tx] = (r < R && c < C) ? src[gs * src_gs + static_cast<long long>(r) * src_ld + c] : 0.f;
-  }
-  __syncthreads();
-  for (int k = ty; k < 32; k += 8) {
-    const int c = c0 + k, r = r0 + tx;
-    if (r < R && c < C)
-      store_operand<P>(dst, static_cast<size_t>((static_cast<long long>(g) * C + c) * dst_ld + r),
-                       lo, tile[tx][k]);
-  }
-}
-
 // Four consecutive columns per thread, blockIdx.x = matrix row (16-byte loads).
 template <int P>
 __global__ void k_rows_to_operand4(const float* __restrict__ src, long long src_ld, long long src_gs, int R,
@@ -136,15 +113,134 @@ pc_status_t rows_to_operand(const float* src, long long src_ld, long long src_gs
   return PC_OK;
 }
 
+// ---------------------------------------------------------------- transposes
+// dst(g, c, r) = src(g, r, c) over 64 x 64 tiles, 256 threads: the loads are 16-byte row
+// segments of src (c contiguous), the stores are runs of 8 consecutive r of one output
+// row per thread (16 or 32 bytes), both through a padded shared tile.
+// Store functors write n <= 8 values v[0 .. n) at (g, c, r .. r+n-1).
+template <int P>
+struct StoreOperand {  // an operand matrix [g][c][ld] in precision P
+  void* dst;
+  long long ld;
+  size_t lo;
+  __device__ void operator()(int g, int c, int r, const float (&v)[8], int n) const {
+    const size_t idx = static_cast<size_t>((static_cast<long long>(g) * rows_per_group + c) * ld + r);
+    if (n == 8) {
+      if constexpr (P == kBF16) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst) + idx) =
+            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                       pack_bf16x2(v[6], v[7]));
+      } else {
+        float* d = reinterpret_cast<float*>(dst) + idx;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float4 x = make_float4(tf32_rna(v[4 * h]), tf32_rna(v[4 * h + 1]), tf32_rna(v[4 * h + 2]),
+                                       tf32_rna(v[4 * h + 3]));
+          *reinterpret_cast<float4*>(d + 4 * h) = x;
+          if constexpr (P == kTF32x3)
+            *reinterpret_cast<float4*>(d + lo + 4 * h) =
+                make_float4(tf32_rna(v[4 * h] - x.x), tf32_rna(v[4 * h + 1] - x.y), tf32_rna(v[4 * h + 2] - x.z),
+                            tf32_rna(v[4 * h + 3] - x.w));
+        }
+      }
+    } else {
+      for (int k = 0; k < n; ++k) store_operand<P>(dst, idx + k, lo, v[k]);
+    }
+  }
+  long long rows_per_group;
+};
+
+struct StoreF32 {  // a float32 matrix [g][c][ld], overwritten or accumulated into
+  float* dst;
+  long long ld, rows_per_group;
+  int accumulate;
+  __device__ void operator()(int g, int c, int r, const float (&v)[8], int n) const {
+    float* d = dst + (static_cast<long long>(g) * rows_per_group + c) * ld + r;
+    if (n == 8 && (reinterpret_cast<uintptr_t>(d) & 15) == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 x = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
+        if (accumulate) {
+          const float4 o = *reinterpret_cast<const float4*>(d + 4 * h);
+          x.x += o.x;
+          x.y += o.y;
+          x.z += o.z;
+          x.w += o.w;
+        }
+        *reinterpret_cast<float4*>(d + 4 * h) = x;
+      }
+    } else {
+      for (int k = 0; k < n; ++k) d[k] = accumulate ? d[k] + v[k] : v[k];
+    }
+  }
+};
+
+template <class Store>
+__global__ void __launch_bounds__(256) k_transpose64(const float* __restrict__ src, long long src_ld,
+                                                      long long src_gs, int R, int C, const int* gmap, Store st) {
+  __shared__ float tile[64][65];
+  const int g = blockIdx.z;
+  const long long gs = gmap ? gmap[g] : g;
+  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+  const float* s = src + gs * src_gs;
+  const int t = threadIdx.x;
+  const bool vec = (src_ld & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+#pragma unroll
+  for (int i = t; i < 64 * 16; i += 256) {
+    const int rr = i >> 4, cq = (i & 15) * 4;
+    const int r = r0 + rr, c = c0 + cq;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < R) {
+      const float* p = s + static_cast<long long>(r) * src_ld + c;
+      if (vec && c + 3 < C) {
+        v = *reinterpret_cast<const float4*>(p);
+      } else {
+        if (c < C) v.x = p[0];
+        if (c + 1 < C) v.y = p[1];
+        if (c + 2 < C) v.z = p[2];
+        if (c + 3 < C) v.w = p[3];
+      }
+    }
+    tile[rr][cq] = v.x;
+    tile[rr][cq + 1] = v.y;
+    tile[rr][cq + 2] = v.z;
+    tile[rr][cq + 3] = v.w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = t; i < 64 * 8; i += 256) {
+    const int cc = i >> 3, rq = (i & 7) * 8;
+    const int c = c0 + cc, r = r0 + rq;
+    if (c >= C || r >= R) continue;
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = tile[rq + k][cc];
+    st(g, c, r, v, min(8, R - r));
+  }
+}
+
+template <class Store>
+pc_status_t launch_transpose64(const float* src, long long src_ld, long long src_gs, int G, int R, int C,
+                               const int* gmap, const Store& st, cudaStream_t s) {
+  if (G == 0 || R == 0 || C == 0) return PC_OK;
+  k_transpose64<Store><<<dim3(cdiv(C, 64), cdiv(R, 64), G), 256, 0, s>>>(src, src_ld, src_gs, R, C, gmap, st);
+  PC_LAUNCH_CHECK();
+  return PC_OK;
+}
+
 template <int P>
 pc_status_t transpose_to_operand(const float* src, long long src_ld, long long src_gs, int G,
                                  int R, int C, const Operand& dst, cudaStream_t s, const int* gmap = nullptr) {
-  if (G == 0 || R == 0 || C == 0) return PC_OK;
-  dim3 grid(cdiv(C, 32), cdiv(R, 32), G);
-  k_transpose_to_operand<P><<<grid, dim3(32, 8), 0, s>>>(src, src_ld, src_gs, R, C, dst.ptr, dst.ld,
-                                                         dst.lo_elems, gmap);
-  PC_LAUNCH_CHECK();
-  return PC_OK;
+  // operand rows are 64-element aligned, so full runs of 8 are 16-byte aligned
+  return launch_transpose64(src, src_ld, src_gs, G, R, C, gmap,
+                            StoreOperand<P>{dst.ptr, dst.ld, dst.lo_elems, static_cast<long long>(C)}, s);
+}
+
+// dst[g][c][r] (+)= src[g][r][c] in float32, dst rows ld apart.
+inline pc_status_t transpose_f32(const float* src, long long src_ld, long long src_gs, int G, int R, int C,
+                                 float* dst, long long dst_ld, int accumulate, cudaStream_t s) {
+  return launch_transpose64(src, src_ld, src_gs, G, R, C, nullptr,
+                            StoreF32{dst, dst_ld, static_cast<long long>(C), accumulate}, s);
 }
 
 // Shared with the circuits: F[g][i][j] (+)= theta[g][i][j] * D[i,j].

@@ -118,3 +118,14 @@ def test_hclt_768_uniform_emissions(hclt_full, mode):
     err = np.abs(ll + n * np.log(512)).max()
     print(f"hclt 768 uniform {mode}: ll err {err:.3e}")
     assert err <= LL_TOL[mode] + (n - 1) * UNIFORM_EDGE_BOUND[mode] + slack
+
+
+def test_more_than_1024_latents():
+    # H > 1024 takes the block-per-(node, sample) product layer instead of the warp one
+    d = hclt_inputs(6, 1100, 7, 9, seed=203, parent=np.array([-1, 0, 0, 1, 1, 2], dtype=np.int32))
+    rl, rpi, rW, rE = _oracle(d)
+    ll, dpi, dW, dE = _gpu_run(d, "fp32")
+    assert ll_err(ll, rl) <= LL_TOL["fp32"]
+    assert flow_err(dpi, rpi) <= FLOW_TOL["fp32"]
+    assert flow_err(dW[1:], rW[1:]) <= FLOW_TOL["fp32"]
+    assert flow_err(dE, rE) <= FLOW_TOL["fp32"]
