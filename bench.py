@@ -385,6 +385,23 @@ def recorded_traffic(kind: str, precision: str):
     return ent.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (the slowest rank's time); x itself for one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, batch: int, steps: int, total_ms: float) -> float:
+    """Whole-job samples/s: every rank processes its own batch per step (weak scaling)."""
+    return world * batch * steps / (total_ms / 1e3)
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args):
     import torch
@@ -441,12 +458,9 @@ def run_ours(args):
     pc.device_status(dev)
     ms_steps = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(ms_steps)
-    tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-    total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.batch * args.steps / (total_ms / 1e3)
+    value = job_rate(world, w.batch, args.steps, total_ms)
 
     # ---- roofline of the dominant kernel kind (by total time in the timed region)
     peaks, peak_src = load_peaks()
@@ -498,10 +512,7 @@ def run_ours(args):
         e2e_step()
         torch.cuda.synchronize(dev)
         e2e_ms.append(1e3 * (time.perf_counter() - t0))
-    e2e_t = torch.tensor([statistics.mean(e2e_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = world * w.batch / (float(e2e_t.item()) / 1e3)
+    e2e_value = job_rate(world, w.batch, 1, max_over_ranks(statistics.mean(e2e_ms), world, dev))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
