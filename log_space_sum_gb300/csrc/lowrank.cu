@@ -230,8 +230,8 @@ __global__ void k_lr_to_op(const float* __restrict__ src, long long sg, long lon
 // ------------------------------------------------------------------ shared memory plan
 enum : int { kLrStats = 3 };
 constexpr int kThetaTileBytes = kLrRows * 128;  // 128 rows x 32 floats
-constexpr int kLrWarps = 8;                      // two warps per TMEM lane quarter
-constexpr int kLrThreadsAll = kLrWarps * 32;
+constexpr int kLrWarps = 8;                      // consumers: two warps per TMEM lane quarter
+constexpr int kLrThreadsAll = (kLrWarps + 1) * 32;  // + one issuer warp (TMA and MMAs)
 constexpr float kLog2e = 1.4426950408889634f;
 
 __host__ __device__ constexpr int lr_stages(int mode) { return mode == kLrFwd ? 3 : 4; }
@@ -389,11 +389,17 @@ __device__ __forceinline__ void tile_put_row16(uint8_t* tile, const TileGeo& g, 
 }
 
 // One pass (forward, grad A or grad B) over the tile of 128 own rows of sample
-// blockIdx.y; see the file comment. Eight warps: warp w reads TMEM lane quarter w & 3 and
-// handles columns 16 (w >> 2) .. +15 of every 32-column chunk. Thread 0 issues the TMA
-// loads (a ring of kStages chunks) and the MMAs.
+// blockIdx.y; see the file comment. Warp specialised, with mbarrier hand-offs only:
+//   warp 8, one thread: the TMA loads (a ring of R chunk stages) and every MMA;
+//   warps 0..7: consumers; warp w reads TMEM lane quarter w & 3 and handles columns
+//   16 (w >> 2) .. +15 of every 32-column chunk.
+// Barriers: mbT[stage] chunk landed; mbS[c & 1] S of chunk c in TMEM; mbF[c & 1] all eight
+// consumer warps are done with chunk c's S slot and stage; mbDf[c & 1] chunk c's D tile is
+// written; mbG[c & 1] the gradient MMA of chunk c is done.
+// (The forward's shared memory leaves room for two CTAs per SM; its launch bounds ask the
+// compiler for registers that allow two as well.)
 template <int P, int Mode>
-__global__ void __launch_bounds__(kLrThreadsAll, 1)
+__global__ void __launch_bounds__(kLrThreadsAll, Mode == kLrFwd ? 2 : 1)
     k_lowrank(const __grid_constant__ LrMaps maps, const LrArgs a) {
   constexpr int SF = s_fmt(P), GF = g_fmt(P);
   constexpr bool kGrad = Mode != kLrFwd;
@@ -406,7 +412,8 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
   const int b = blockIdx.y;
   const int o0 = blockIdx.x * kLrRows;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int quarter = warp & 3, half = warp >> 2;
+  const bool issuer = warp == kLrWarps;
+  const int quarter = warp & 3, half = (warp >> 2) & 1;
   const int row = quarter * 32 + lane;  // own row in the tile (TMEM lane)
   const int col0 = half * 16;           // this thread's columns of a chunk
   const int own = o0 + row;
@@ -424,20 +431,24 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* own_tile = smem + L.own;
-  uint64_t* mbT = reinterpret_cast<uint64_t*>(smem + L.bars);  // [R <= 4] stage landed
-  uint64_t* mbS = mbT + 4;                                      // [2] S MMA done
-  uint64_t* mbG = mbS + 2;                                      // [2] grad MMA done
+  uint64_t* mbT = reinterpret_cast<uint64_t*>(smem + L.bars);  // [R <= 4]
+  uint64_t* mbS = mbT + 4;                                      // [2]
+  uint64_t* mbF = mbS + 2;                                      // [2]
+  uint64_t* mbDf = mbF + 2;                                     // [2]
+  uint64_t* mbG = mbDf + 2;                                     // [2]
   uint64_t* mbO = mbG + 2;                                      // own tile landed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mbO + 1);
   float* merge = reinterpret_cast<float*>(smem + L.bars + 256);  // [3][128]
   auto stage = [&](int c) { return smem + L.stage + (c % R) * L.stage_bytes; };
-  auto d_tile = [&](int s) { return smem + L.d + s * L.d_bytes; };
+  auto d_tile = [&](int c) { return smem + L.d + (c % ND) * L.d_bytes; };
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < R; ++i) mbar_init(&mbT[i], 1);
+      for (int i = 0; i < 4; ++i) mbar_init(&mbT[i], 1);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&mbS[i], 1);
+        mbar_init(&mbF[i], kLrWarps);
+        mbar_init(&mbDf[i], kLrWarps);
         mbar_init(&mbG[i], 1);
       }
       mbar_init(mbO, 1);
@@ -450,88 +461,126 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int nch = (sw_n + kLrChunk - 1) / kLrChunk;
-
-  // TMA of chunk c into its stage (thread 0)
-  auto issue_tma = [&](int c) {
-    uint8_t* st = stage(c);
-    uint64_t* bar = &mbT[c % R];
-    const int w0 = c * kLrChunk;
-    mbar_arrive_expect_tx(bar, L.tx_bytes);
-    for (int part = 0; part < fmt_parts(SF); ++part)
-      for (int kb = 0; kb < gs.kblocks; ++kb)
-        tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
-                    kb * (128 / esS), w0, b);
-    tma_load_3d(st + L.th_off, &maps.th, bar, w0, o0, 0);
-    if constexpr (kGrad)
-      for (int part = 0; part < fmt_parts(GF); ++part)
-        tma_load_3d(st + L.gb_off + part * gg.bytes_part(), &maps.gb[part], bar, w0, 0, b);
-    for (int v = 0; v < kNvec; ++v) tma_load_3d(st + L.vec_off + v * 128, &maps.vec[v], bar, w0, b, 0);
-  };
-  auto issue_s = [&](int c) {
-    tc_fence_after();
-    lr_mma<SF>(tmem + static_cast<uint32_t>((c & 1) * kLrChunk), own_tile, go, stage(c) + L.sw_off, gs, kLrChunk,
-               false);
-    umma_commit(&mbS[c & 1]);
-  };
-
   bool ok = true;
-  int issued = -1, s_issued = -1, g_issued = -1;  // thread 0's bookkeeping
-  if (t == 0) {
-    mbar_arrive_expect_tx(mbO, L.own_bytes);
-    for (int part = 0; part < fmt_parts(SF); ++part)
-      for (int kb = 0; kb < go.kblocks; ++kb)
-        tma_load_3d(own_tile + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], mbO,
-                    kb * (128 / esS), o0, b);
-    for (int c = 0; c < R && c < nch; ++c) {
-      issue_tma(c);
-      issued = c;
-    }
-    ok = mbar_wait(mbO, 0, a.status, kErrTimeoutMma) && mbar_wait(&mbT[0], 0, a.status, kErrTimeoutMma);
-    if (ok) {
-      issue_s(0);
-      s_issued = 0;
-    }
-  }
 
-  // per-row constants
-  float lz = 0.f, fi = 0.f, fc = 0.f, uj = 0.f;
-  if constexpr (Mode == kLrGradB) uj = own < a.N ? a.u[static_cast<long long>(b) * a.ldu + own] : 0.f;
-  if constexpr (Mode == kLrGradA) {
-    if (own < a.M) {
-      const long long r = static_cast<long long>(b) * a.ldm + own;
-      lz = a.rf_lz[r];
-      fi = a.rf_f[r];
-      fc = a.rf_fc[r];
-    }
-  }
-  const bool row_live = lz > -INFINITY;
-  float run = -INFINITY, Z = 0.f, num = 0.f;  // forward
-  float e_acc = 0.f;                          // grad B
-
-  // With a ring of two stages the next chunk's copy is issued only at the end of this
-  // iteration, so its S is issued there too; deeper rings issue it here, ahead.
-  const bool late_s = R == 2;
-  for (int c = 0; c < nch; ++c) {
-    const int sl = c & 1;
-    if (t == 0 && ok && !late_s && c + 1 < nch) {
-      ok = mbar_wait(&mbT[(c + 1) % R], ((c + 1) / R) & 1, a.status, kErrTimeoutMma);
-      if (ok) {
-        issue_s(c + 1);
-        s_issued = c + 1;
+  if (issuer) {
+    if (lane == 0) {
+      int issued = -1, s_issued = -1, g_issued = -1;
+      auto issue_tma = [&](int c) {
+        uint8_t* st = stage(c);
+        uint64_t* bar = &mbT[c % R];
+        const int w0 = c * kLrChunk;
+        mbar_arrive_expect_tx(bar, L.tx_bytes);
+        for (int part = 0; part < fmt_parts(SF); ++part)
+          for (int kb = 0; kb < gs.kblocks; ++kb)
+            tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
+                        kb * (128 / esS), w0, b);
+        tma_load_3d(st + L.th_off, &maps.th, bar, w0, o0, 0);
+        if constexpr (kGrad)
+          for (int part = 0; part < fmt_parts(GF); ++part)
+            tma_load_3d(st + L.gb_off + part * gg.bytes_part(), &maps.gb[part], bar, w0, 0, b);
+        for (int v = 0; v < kNvec; ++v) tma_load_3d(st + L.vec_off + v * 128, &maps.vec[v], bar, w0, b, 0);
+        issued = c;
+      };
+      auto issue_grad = [&](int c) {  // the D tile of chunk c is written
+        ok = ok && mbar_wait(&mbDf[c & 1], (c >> 1) & 1, a.status, kErrTimeoutMma);
+        if (!ok) return;
+        tc_fence_after();
+        lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(c), gd, stage(c) + L.gb_off,
+                   gg, Kp, c >= kGradAccs);
+        umma_commit(&mbG[c & 1]);
+        g_issued = c;
+      };
+      const int lag = R >= 3 ? 2 : 1;  // refill the stage of chunk c - lag
+      mbar_arrive_expect_tx(mbO, L.own_bytes);
+      for (int part = 0; part < fmt_parts(SF); ++part)
+        for (int kb = 0; kb < go.kblocks; ++kb)
+          tma_load_3d(own_tile + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], mbO,
+                      kb * (128 / esS), o0, b);
+      for (int c = 0; c < R && c < nch; ++c) issue_tma(c);
+      ok = mbar_wait(mbO, 0, a.status, kErrTimeoutMma);
+      // Waits once for the consumers to be done with chunk p. A parity wait must not be
+      // repeated: by then the barrier may have completed the next chunk's phase too.
+      int f_seen = -1;
+      auto wait_consumed = [&](int p) {
+        if (p <= f_seen) return;
+        ok = ok && mbar_wait(&mbF[p & 1], (p >> 1) & 1, a.status, kErrTimeoutMma);
+        if (ok) f_seen = p;
+      };
+      for (int c = 0; c < nch && ok; ++c) {
+        ok = mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutMma);
+        // the TMEM slot of chunk c - 2 is free once its consumers are done
+        if (ok && c >= 2) wait_consumed(c - 2);
+        if (!ok) break;
+        tc_fence_after();
+        lr_mma<SF>(tmem + static_cast<uint32_t>((c & 1) * kLrChunk), own_tile, go, stage(c) + L.sw_off, gs, kLrChunk,
+                   false);
+        umma_commit(&mbS[c & 1]);
+        s_issued = c;
+        if constexpr (kGrad) {
+          if (c >= 1) issue_grad(c - 1);
+        }
+        const int p = c - lag;
+        if (ok && p >= 0 && p + R < nch) {
+          wait_consumed(p);
+          if (kGrad && ok) ok = mbar_wait(&mbG[p & 1], (p >> 1) & 1, a.status, kErrTimeoutMma);
+          if (ok) issue_tma(p + R);
+        }
+      }
+      if (kGrad && ok && nch > 0) issue_grad(nch - 1);
+      if (!ok) {
+        // a wait gave up: let the copies and MMAs in flight finish before TMEM is freed
+        mbar_wait(mbO, 0, a.status, kErrTimeoutDrain);
+        for (int c = issued; c >= 0 && c > issued - R; --c)
+          mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutDrain);
+        if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
+        if (g_issued >= 0) mbar_wait(&mbG[g_issued & 1], (g_issued >> 1) & 1, a.status, kErrTimeoutDrain);
       }
     }
-    bool w = mbar_wait(&mbS[sl], (c >> 1) & 1, a.status, kErrTimeoutEpilogue) &&
-             mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutEpilogue);
-    w = __all_sync(0xffffffffu, w);
-    tc_fence_after();
-    if (w) {
-      float v[16], th[16];
-      tmem_ld_32x16(lane_base + static_cast<uint32_t>(sl * kLrChunk + col0), v);
+    ok = __all_sync(0xffffffffu, ok);
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float lz = 0.f, fi = 0.f, fc = 0.f, uj = 0.f;
+    if constexpr (Mode == kLrGradB) uj = own < a.N ? a.u[static_cast<long long>(b) * a.ldu + own] : 0.f;
+    if constexpr (Mode == kLrGradA) {
+      if (own < a.M) {
+        const long long r = static_cast<long long>(b) * a.ldm + own;
+        lz = a.rf_lz[r];
+        fi = a.rf_f[r];
+        fc = a.rf_fc[r];
+      }
+    }
+    const bool row_live = lz > -INFINITY;
+    float run = -INFINITY, Z = 0.f, num = 0.f;  // forward
+    float e_acc = 0.f;                          // grad B
+    for (int c = 0; c < nch; ++c) {
+      bool w = mbar_wait(&mbS[c & 1], (c >> 1) & 1, a.status, kErrTimeoutEpilogue) &&
+               mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutEpilogue);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[16], th[16], va[16], vb[16], vc[16];
+      tmem_ld_32x16(lane_base + static_cast<uint32_t>((c & 1) * kLrChunk + col0), v);
       const uint8_t* st = stage(c);
       tile_row16_f32(st + L.th_off, row, col0, th);
       const float* vec = reinterpret_cast<const float*>(st + L.vec_off);
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        va[jj] = vec[col0 + jj];
+        if constexpr (Mode == kLrGradB) {
+          vb[jj] = vec[32 + col0 + jj];
+          vc[jj] = vec[64 + col0 + jj];
+        }
+      }
+      // chunk c's S slot and stage are no longer read by this warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mbF[c & 1]);
       const int w0 = c * kLrChunk + col0;
       if constexpr (Mode == kLrFwd) {
         float cm = -INFINITY;
@@ -548,7 +597,7 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
         for (int jj = 0; jj < 16; ++jj) {
           const float tg = w0 + jj < a.N ? th[jj] * ex2_approx((v[jj] - run) * kLog2e) : 0.f;
           Z += tg;
-          num = fmaf(tg, vec[col0 + jj], num);
+          num = fmaf(tg, va[jj], num);
         }
       } else {
         float dv[16];
@@ -556,91 +605,60 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
         for (int jj = 0; jj < 16; ++jj) {
           if constexpr (Mode == kLrGradA) {
             const float q = (row_live && th[jj] > 0.f) ? th[jj] * ex2_approx((v[jj] - lz) * kLog2e) : 0.f;
-            dv[jj] = q * fmaf(vec[col0 + jj], fc, -fi);
+            dv[jj] = q * fmaf(va[jj], fc, -fi);
           } else {
-            const float lzi = vec[col0 + jj];
+            const float lzi = va[jj];
             const float q = (lzi > -INFINITY && th[jj] > 0.f) ? th[jj] * ex2_approx((v[jj] - lzi) * kLog2e) : 0.f;
-            const float pf = q * uj * vec[64 + col0 + jj];
+            const float pf = q * uj * vc[jj];
             e_acc += pf;
-            dv[jj] = pf - q * vec[32 + col0 + jj];
+            dv[jj] = pf - q * vb[jj];
           }
           if (own >= own_n) dv[jj] = 0.f;
         }
-        // the D slot was read by the grad MMA of chunk c - ND
+        // the D slot was read by the gradient MMA of chunk c - ND
         if (c >= ND) {
           const int pc = c - ND;
-          w = w && mbar_wait(&mbG[pc & 1], (pc >> 1) & 1, a.status, kErrTimeoutMma);
+          w = __all_sync(0xffffffffu, mbar_wait(&mbG[pc & 1], (pc >> 1) & 1, a.status, kErrTimeoutEpilogue));
+          if (!w) {
+            ok = false;
+            break;
+          }
         }
-        tile_put_row16<GF>(d_tile(c % ND), gd, row, col0, dv);
+        tile_put_row16<GF>(d_tile(c), gd, row, col0, dv);
         fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mbDf[c & 1]);
       }
     }
-    tc_fence_before();
-    ok = __syncthreads_and(ok && w);
-    if (!ok) break;
-    if (t == 0) {
-      if constexpr (kGrad) {
-        tc_fence_after();
-        lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(c % ND), gd,
-                   stage(c) + L.gb_off, gg, Kp, c >= kGradAccs);
-        umma_commit(&mbG[sl]);
-        g_issued = c;
-      }
-      // refill the stage of chunk c-1: its S and grad MMAs have completed
-      const int nc = c - 1 + R;
-      if (c >= 1 && nc < nch) {
-        if (kGrad) ok = mbar_wait(&mbG[(c - 1) & 1], ((c - 1) >> 1) & 1, a.status, kErrTimeoutMma);
-        if (ok) {
-          issue_tma(nc);
-          issued = nc;
-        }
-      }
-      if (ok && late_s && c + 1 < nch) {
-        ok = mbar_wait(&mbT[(c + 1) % R], ((c + 1) / R) & 1, a.status, kErrTimeoutMma);
-        if (ok) {
-          issue_s(c + 1);
-          s_issued = c + 1;
-        }
-      }
+    if (ok && kGrad && nch > 0) {
+      const int lc = nch - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&mbG[lc & 1], (lc >> 1) & 1, a.status, kErrTimeoutEpilogue));
     }
-  }
-
-  if (ok && kGrad && nch > 0) {
-    bool w = mbar_wait(&mbG[(nch - 1) & 1], ((nch - 1) >> 1) & 1, a.status, kErrTimeoutEpilogue);
-    ok = __syncthreads_and(w);
-  } else {
-    ok = __syncthreads_and(ok);
-  }
-  if (ok) {
-    if constexpr (Mode == kLrFwd) {
-      // merge the two column halves of every row
-      if (half == 1) {
-        merge[row] = run;
-        merge[128 + row] = Z;
-        merge[256 + row] = num;
-      }
-      __syncthreads();
-      if (half == 0 && own < a.M) {
-        const float r1 = merge[row], z1 = merge[128 + row], n1 = merge[256 + row];
-        const float r = fmaxf(run, r1);
-        float zt = 0.f, nt = 0.f;
-        if (r > -INFINITY) {
-          const float s0 = run > -INFINITY ? ex2_approx((run - r) * kLog2e) : 0.f;
-          const float s1 = r1 > -INFINITY ? ex2_approx((r1 - r) * kLog2e) : 0.f;
-          zt = Z * s0 + z1 * s1;
-          nt = num * s0 + n1 * s1;
+    // merge the two column halves of each row (consumer warps only)
+    if (half == 1) {
+      merge[row] = run;
+      merge[128 + row] = Z;
+      merge[256 + row] = Mode == kLrGradB ? e_acc : num;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kLrWarps * 32) : "memory");
+    if (ok && half == 0) {
+      if constexpr (Mode == kLrFwd) {
+        if (own < a.M) {
+          const float r1 = merge[row], z1 = merge[128 + row], n1 = merge[256 + row];
+          const float r = fmaxf(run, r1);
+          float zt = 0.f, nt = 0.f;
+          if (r > -INFINITY) {
+            const float s0 = run > -INFINITY ? ex2_approx((run - r) * kLog2e) : 0.f;
+            const float s1 = r1 > -INFINITY ? ex2_approx((r1 - r) * kLog2e) : 0.f;
+            zt = Z * s0 + z1 * s1;
+            nt = num * s0 + n1 * s1;
+          }
+          const float mb = a.m[b];
+          const bool live = zt > 0.f && nt > 0.f && mb > -INFINITY;
+          a.out[static_cast<long long>(own) * a.B + b] = live ? mb + logf(nt / zt) : -INFINITY;
+          a.logZ[static_cast<long long>(b) * a.M + own] = zt > 0.f ? logf(zt) + r : -INFINITY;
         }
-        const float mb = a.m[b];
-        const bool live = zt > 0.f && nt > 0.f && mb > -INFINITY;
-        a.out[static_cast<long long>(own) * a.B + b] = live ? mb + logf(nt / zt) : -INFINITY;
-        a.logZ[static_cast<long long>(b) * a.M + own] = zt > 0.f ? logf(zt) + r : -INFINITY;
-      }
-    } else {
-      if constexpr (Mode == kLrGradB) {
-        if (half == 1) merge[row] = e_acc;
-      }
-      __syncthreads();
-      if (half == 0) {
+      } else {
         tc_fence_after();
         float acc[64];  // static indices only: kept in registers
 #pragma unroll
@@ -673,7 +691,7 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
               }
             }
             if (a.e) {
-              const float ev = e_acc + merge[row];
+              const float ev = e_acc + merge[256 + row];
               float* de = a.e + static_cast<long long>(own) * a.B + b;
               *de = a.accumulate ? *de + ev : ev;
             }
@@ -681,13 +699,6 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
         }
       }
     }
-  } else if (t == 0) {
-    // a wait gave up: let the copies and MMAs in flight finish before TMEM is freed
-    // (the latest phase of every barrier: earlier phases are long complete)
-    mbar_wait(mbO, 0, a.status, kErrTimeoutDrain);
-    for (int c = issued; c >= 0 && c > issued - R; --c) mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutDrain);
-    if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
-    if (g_issued >= 0) mbar_wait(&mbG[g_issued & 1], (g_issued >> 1) & 1, a.status, kErrTimeoutDrain);
   }
   tc_fence_before();
   __syncthreads();
@@ -699,7 +710,8 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
 
 // Parameter-flow statistics F+ and W over all samples for the 128 x 32 tile (blockIdx.x,
 // blockIdx.y) of [M, N]: own rows i, the 32 columns j fixed, a sweep over the samples.
-// Each stage of the TMA ring holds one sample's A_b tile, its B_b^T chunk and u_b.
+// Each stage of the TMA ring holds one sample's A_b tile, its B_b^T chunk and u_b. Warp
+// specialised as k_lowrank: warp 8 issues the copies and the MMAs, warps 0..7 consume.
 template <int P>
 __global__ void __launch_bounds__(kLrThreadsAll, 1)
     k_lowrank_stats(const __grid_constant__ LrMaps maps, const LrArgs a) {
@@ -708,7 +720,8 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
   const int K = a.K;
   const int i0 = blockIdx.x * kLrRows, j0 = blockIdx.y * kLrChunk;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int quarter = warp & 3, half = warp >> 2;
+  const bool issuer = warp == kLrWarps;
+  const int quarter = warp & 3, half = (warp >> 2) & 1;
   const int row = quarter * 32 + lane;
   const int col0 = half * 16;
   const int i = i0 + row;
@@ -719,102 +732,120 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* mbT = reinterpret_cast<uint64_t*>(smem + L.bars);  // [R <= 4]
-  uint64_t* mbS = mbT + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbS + 2);
+  uint64_t* mbS = mbT + 4;                                      // [2]
+  uint64_t* mbF = mbS + 2;                                      // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbF + 2);
   auto stage = [&](int b) { return smem + L.stage + (b % R) * L.stage_bytes; };
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int s = 0; s < R; ++s) mbar_init(&mbT[s], 1);
-      mbar_init(&mbS[0], 1);
-      mbar_init(&mbS[1], 1);
+      for (int s = 0; s < 4; ++s) mbar_init(&mbT[s], 1);
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&mbS[s], 1);
+        mbar_init(&mbF[s], kLrWarps);
+      }
       fence_barrier_init();
     }
     __syncwarp();
     tmem_alloc(tslot, 64);
   }
-  // theta[i][j0 + col0 .. +15] in registers, from the row-padded copy
-  float th[16];
-#pragma unroll
-  for (int jj = 0; jj < 16; ++jj) {
-    const int j = j0 + col0 + jj;
-    th[jj] = (i < a.M && j < a.N) ? a.theta_ld[static_cast<long long>(i) * a.theta_ld_stride + j] : 0.f;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-
-  auto issue_tma = [&](int b) {
-    uint8_t* st = stage(b);
-    uint64_t* bar = &mbT[b % R];
-    mbar_arrive_expect_tx(bar, L.tx_bytes);
-    for (int part = 0; part < fmt_parts(SF); ++part) {
-      for (int kb = 0; kb < go.kblocks; ++kb)
-        tma_load_3d(st + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], bar, kb * (128 / esS), i0, b);
-      for (int kb = 0; kb < gs.kblocks; ++kb)
-        tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
-                    kb * (128 / esS), j0, b);
-    }
-    tma_load_3d(st + L.vec_off, &maps.vec[0], bar, j0, b, 0);
-  };
-  auto issue_s = [&](int b) {
-    tc_fence_after();
-    lr_mma<SF>(tmem + static_cast<uint32_t>((b & 1) * kLrChunk), stage(b), go, stage(b) + L.sw_off, gs, kLrChunk,
-               false);
-    umma_commit(&mbS[b & 1]);
-  };
-
   bool ok = true;
-  int issued = -1, s_issued = -1;
-  if (t == 0) {
-    for (int b = 0; b < R && b < a.B; ++b) {
-      issue_tma(b);
-      issued = b;
-    }
-    ok = mbar_wait(&mbT[0], 0, a.status, kErrTimeoutMma);
-    if (ok) {
-      issue_s(0);
-      s_issued = 0;
-    }
-  }
-  float fp[16], wst[16];
-#pragma unroll
-  for (int jj = 0; jj < 16; ++jj) fp[jj] = wst[jj] = 0.f;
-  auto row_factors = [&](int b, float& lz, float& fi, float& fc) {
-    lz = -INFINITY;
-    fi = fc = 0.f;
-    if (i < a.M && b < a.B) {
-      const long long r = static_cast<long long>(b) * a.ldm + i;
-      lz = a.rf_lz[r];
-      fi = a.rf_f[r];
-      fc = a.rf_fc[r];
-    }
-  };
-  float lz, fi, fc;
-  row_factors(0, lz, fi, fc);
-  const bool late_s = R == 2;  // as in k_lowrank
-  for (int b = 0; b < a.B; ++b) {
-    const int sl = b & 1;
-    if (t == 0 && ok && !late_s && b + 1 < a.B) {
-      ok = mbar_wait(&mbT[(b + 1) % R], ((b + 1) / R) & 1, a.status, kErrTimeoutMma);
-      if (ok) {
-        issue_s(b + 1);
-        s_issued = b + 1;
+
+  if (issuer) {
+    if (lane == 0) {
+      int issued = -1, s_issued = -1;
+      auto issue_tma = [&](int b) {
+        uint8_t* st = stage(b);
+        uint64_t* bar = &mbT[b % R];
+        mbar_arrive_expect_tx(bar, L.tx_bytes);
+        for (int part = 0; part < fmt_parts(SF); ++part) {
+          for (int kb = 0; kb < go.kblocks; ++kb)
+            tma_load_3d(st + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], bar, kb * (128 / esS), i0,
+                        b);
+          for (int kb = 0; kb < gs.kblocks; ++kb)
+            tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
+                        kb * (128 / esS), j0, b);
+        }
+        tma_load_3d(st + L.vec_off, &maps.vec[0], bar, j0, b, 0);
+        issued = b;
+      };
+      const int lag = R >= 3 ? 2 : 1;
+      for (int b = 0; b < R && b < a.B; ++b) issue_tma(b);
+      int f_seen = -1;  // as in k_lowrank: one wait per sample's consumer phase
+      auto wait_consumed = [&](int p) {
+        if (p <= f_seen) return;
+        ok = ok && mbar_wait(&mbF[p & 1], (p >> 1) & 1, a.status, kErrTimeoutMma);
+        if (ok) f_seen = p;
+      };
+      for (int b = 0; b < a.B && ok; ++b) {
+        ok = mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutMma);
+        if (ok && b >= 2) wait_consumed(b - 2);
+        if (!ok) break;
+        tc_fence_after();
+        lr_mma<SF>(tmem + static_cast<uint32_t>((b & 1) * kLrChunk), stage(b), go, stage(b) + L.sw_off, gs,
+                   kLrChunk, false);
+        umma_commit(&mbS[b & 1]);
+        s_issued = b;
+        const int p = b - lag;
+        if (p >= 0 && p + R < a.B) {
+          wait_consumed(p);
+          if (ok) issue_tma(p + R);
+        }
+      }
+      if (!ok) {
+        for (int b = issued; b >= 0 && b > issued - R; --b)
+          mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutDrain);
+        if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
       }
     }
-    float nlz, nfi, nfc;  // the next sample's row factors, loaded while this one computes
-    row_factors(b + 1, nlz, nfi, nfc);
-    bool w = mbar_wait(&mbS[sl], (b >> 1) & 1, a.status, kErrTimeoutEpilogue) &&
-             mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutEpilogue);
-    w = __all_sync(0xffffffffu, w);
-    tc_fence_after();
-    if (w) {
-      float v[16];
-      tmem_ld_32x16(lane_base + static_cast<uint32_t>(sl * kLrChunk + col0), v);
+    ok = __all_sync(0xffffffffu, ok);
+  } else {
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    // theta[i][j0 + col0 .. +15] in registers, from the row-padded copy
+    float th[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int j = j0 + col0 + jj;
+      th[jj] = (i < a.M && j < a.N) ? a.theta_ld[static_cast<long long>(i) * a.theta_ld_stride + j] : 0.f;
+    }
+    float fp[16], wst[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) fp[jj] = wst[jj] = 0.f;
+    auto row_factors = [&](int b, float& lz, float& fi, float& fc) {
+      lz = -INFINITY;
+      fi = fc = 0.f;
+      if (i < a.M && b < a.B) {
+        const long long r = static_cast<long long>(b) * a.ldm + i;
+        lz = a.rf_lz[r];
+        fi = a.rf_f[r];
+        fc = a.rf_fc[r];
+      }
+    };
+    float lz, fi, fc;
+    row_factors(0, lz, fi, fc);
+    for (int b = 0; b < a.B; ++b) {
+      float nlz, nfi, nfc;  // the next sample's row factors, loaded while this one computes
+      row_factors(b + 1, nlz, nfi, nfc);
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&mbS[b & 1], (b >> 1) & 1, a.status, kErrTimeoutEpilogue) &&
+                                                 mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutEpilogue));
+      if (!w) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[16], us[16];
+      tmem_ld_32x16(lane_base + static_cast<uint32_t>((b & 1) * kLrChunk + col0), v);
+      const float* uv = reinterpret_cast<const float*>(stage(b) + L.vec_off) + col0;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) us[jj] = uv[jj];
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mbF[b & 1]);
       if (lz > -INFINITY) {
-        const float* us = reinterpret_cast<const float*>(stage(b) + L.vec_off) + col0;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const float gz = ex2_approx((v[jj] - lz) * kLog2e);  // g_b / Z_b
@@ -822,27 +853,11 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
           wst[jj] = fmaf(fi, gz, wst[jj]);
         }
       }
+      lz = nlz;
+      fi = nfi;
+      fc = nfc;
     }
-    lz = nlz;
-    fi = nfi;
-    fc = nfc;
-    tc_fence_before();
-    ok = __syncthreads_and(ok && w);
-    if (!ok) break;
-    if (t == 0 && b >= 1 && b - 1 + R < a.B) {  // refill the stage of sample b-1
-      issue_tma(b - 1 + R);
-      issued = b - 1 + R;
-    }
-    if (t == 0 && late_s && b + 1 < a.B) {
-      ok = mbar_wait(&mbT[(b + 1) % R], ((b + 1) / R) & 1, a.status, kErrTimeoutMma);
-      if (ok) {
-        issue_s(b + 1);
-        s_issued = b + 1;
-      }
-    }
-  }
-  if (ok) {
-    if (i < a.M) {
+    if (ok && i < a.M) {
       for (int jj = 0; jj < 16; ++jj) {
         const int j = j0 + col0 + jj;
         if (j >= a.N) break;
@@ -851,9 +866,6 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
         if (a.W) a.W[idx] = a.accumulate ? a.W[idx] + wst[jj] : wst[jj];
       }
     }
-  } else if (t == 0) {
-    for (int b = issued; b >= 0 && b > issued - R; --b) mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutDrain);
-    if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
   }
   tc_fence_before();
   __syncthreads();
