@@ -715,9 +715,10 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     if ((st = encode_maps(&ma, operand_view(w.Wop, prec, sA, G), prec, kBM)) != PC_OK) return st;
     if ((st = encode_maps(&mb, operand_view(w.Uop, prec, sA, G), prec, kHcltBN)) != PC_OK) return st;
     EpiHcltFwd::Params ep{w.D + static_cast<long long>(sA) * B * H, H, B};
+    // a_early: W's operand copy was written before the first product layer
     if ((st = launch_gemm<P, kHcltBN, EpiHcltFwd>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi,
                                                   mb.lo, num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD,
-                                                  2ll * G * H * H * B)) != PC_OK)
+                                                  2ll * G * H * H * B, true)) != PC_OK)
       return st;
   }
   k_hclt_ll<<<cdiv(B, 128), 128, 0, s>>>(n, B, w.Ex, w.Lm, w.rdot, ll, w.rroot);
@@ -744,9 +745,10 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       if ((st = encode_maps(&mb, operand_view(w.Gbm, prec, 0, G), prec, kHcltBN)) != PC_OK) return st;
       typename EpiHcltElem<P>::Params ee{w.U32 + static_cast<long long>(sA) * B * H,
                                          w.F32 + static_cast<long long>(sA) * B * H, H, B};
+      // a_early: Wᵀ's operand copy was written before the first scaled-flow kernel
       if ((st = launch_gemm<P, kHcltBN, EpiHcltElem<P>>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo,
                                                         mb.hi, mb.lo, num_k_blocks(H, prec), ee, s,
-                                                        PC_KIND_HCLT_ELEM, 2ll * G * H * H * B)) != PC_OK)
+                                                        PC_KIND_HCLT_ELEM, 2ll * G * H * H * B, true)) != PC_OK)
         return st;
       if (!dW) continue;
       // parameter flows of the level's edges

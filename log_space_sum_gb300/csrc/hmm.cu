@@ -615,8 +615,10 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
         ep.U0 = w.U0;
       }
       const OperandMaps& b = mb[(t + 1) & 1];
+      // a_early: the A operand was converted before k_hmm_leaf, the kernel that precedes
+      // the first layer, so no kernel still running when a layer starts writes it.
       if ((st = launch_gemm<P, kChainBN, EpiHmmFwd<P>>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
-                                                        PC_KIND_HMM_FWD, 2ll * H * H * B)) != PC_OK)
+                                                        PC_KIND_HMM_FWD, 2ll * H * H * B, true)) != PC_OK)
         return st;
     }
   }
@@ -649,8 +651,9 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
         if (dA) { ep.wn = w.wn.ptr; ep.wn_ld = w.wn.ld; ep.wn_lo = w.wn.lo_elems; }
       }
       const OperandMaps& b = mb[t & 1];
+      // a_early: the transposed A operand was converted before the forward chain
       if ((st = launch_gemm<P, kChainBN, EpiHmmBwd<P>>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
-                                                        PC_KIND_HMM_ELEM, 2ll * H * H * B)) != PC_OK)
+                                                        PC_KIND_HMM_ELEM, 2ll * H * H * B, true)) != PC_OK)
         return st;
     }
     if (dA) {

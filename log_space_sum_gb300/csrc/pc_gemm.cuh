@@ -8,8 +8,12 @@
 //              STAGES-deep shared-memory ring, completion counted in transaction bytes
 //   warp 1     MMA issuer (one thread): tcgen05.mma (kind::f16 or kind::tf32, M = 128,
 //              N = BN) into a TMEM accumulator; tcgen05.commit frees each ring slot
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, one TMEM lane (row of D) per
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator, one TMEM lane (row of D) per
 //              thread, 32 columns at a time, into the pass's epilogue functor
+// Launched as a programmatic dependent of the previous kernel in the stream: everything
+// up to the first global access (barrier set-up, TMEM allocation, and with a_early the
+// first ring slots' A tiles) overlaps that kernel's tail; griddepcontrol.wait precedes
+// every other global access.
 // Precision kTF32x3 forms each product from three TF32 MMAs (lo*hi + hi*lo + hi*hi)
 // into the same accumulator (pyjuice PR #62, Summary 3, "tf32x3").
 //
@@ -117,7 +121,7 @@ template <int P, int BN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
-                int num_kb, unsigned* status, const typename Epi::Params ep) {
+                int num_kb, unsigned* status, const typename Epi::Params ep, int a_early) {
   using S = GemmShape<P, BN>;
   constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
   // Sliced modes: every K slice (kSliceK k-steps of the MMA) is accumulated from zero in
@@ -187,19 +191,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
+      // a_early: the A operand was complete before the previous kernel started, so the
+      // first (still empty) ring slots' A tiles are fetched before waiting for it.
+      const int early = a_early ? (num_kb < kStages ? num_kb : kStages) : 0;
+      for (int kb = 0; kb < early; ++kb) {
+        mbar_arrive_expect_tx(&full[kb], S::kStageBytes);
+        tma_load_3d(a_tile(kb, 0), &tmA, &full[kb], kb * S::kBK, m0, g);
+        if constexpr (P == kTF32x3) tma_load_3d(a_tile(kb, 1), &tmA_lo, &full[kb], kb * S::kBK, m0, g);
+      }
+      grid_dependency_wait();
+      grid_dependents_launch();
       int issued = 0;
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = (kb / kStages) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, status, kErrTimeoutProducer)) break;
-        mbar_arrive_expect_tx(&full[s], S::kStageBytes);
         const int kx = kb * S::kBK;
-        tma_load_3d(a_tile(s, 0), &tmA, &full[s], kx, m0, g);
-        tma_load_3d(b_tile(s, 0), &tmB, &full[s], kx, n0, g);
-        if constexpr (P == kTF32x3) {
-          tma_load_3d(a_tile(s, 1), &tmA_lo, &full[s], kx, m0, g);
-          tma_load_3d(b_tile(s, 1), &tmB_lo, &full[s], kx, n0, g);
+        if (kb >= early) {
+          if (!mbar_wait(&empty[s], ph ^ 1, status, kErrTimeoutProducer)) break;
+          mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+          tma_load_3d(a_tile(s, 0), &tmA, &full[s], kx, m0, g);
+          if constexpr (P == kTF32x3) tma_load_3d(a_tile(s, 1), &tmA_lo, &full[s], kx, m0, g);
         }
+        tma_load_3d(b_tile(s, 0), &tmB, &full[s], kx, n0, g);
+        if constexpr (P == kTF32x3) tma_load_3d(b_tile(s, 1), &tmB_lo, &full[s], kx, n0, g);
         issued = kb + 1;
       }
       // Drain: every slot's most recent fill must have landed before the CTA exits.
@@ -295,6 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------- epilogue
     const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
     const int ew = warp - 2;          // epilogue warp 0 .. 7
+    grid_dependency_wait();           // the epilogue reads and writes global memory
     Epi::prepare(ep, g, m0, n0, et, epi_smem);
     epilogue_bar_sync();
     const int q = warp & 3;       // TMEM lane quarter this warp may access

@@ -7,11 +7,12 @@
 
 namespace pc {
 
+// a_early: the A operand was written before the previous kernel in the stream started.
 template <int P, int BN, class Epi>
 pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo,
                         const CUtensorMap& b, const CUtensorMap& b_lo, int num_kb,
                         const typename Epi::Params& ep, cudaStream_t stream, int kind,
-                        long long flops) {
+                        long long flops, bool a_early = false) {
   constexpr size_t smem = gemm_smem_bytes<P, BN, Epi>();
   static_assert(smem <= 232448, "shared memory per CTA");
   static bool attr_set[64] = {};
@@ -25,8 +26,19 @@ pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo
   }
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return PC_OK;
   const int slot = profile_begin(stream);
-  k_umma_gemm<P, BN, Epi><<<grid, kGemmThreads, smem, stream>>>(a, a_lo, b, b_lo, num_kb,
-                                                                device_status_word(), ep);
+  // A programmatic dependent of the previous kernel in the stream (see k_umma_gemm).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  PC_CUDA(cudaLaunchKernelEx(&cfg, k_umma_gemm<P, BN, Epi>, a, a_lo, b, b_lo, num_kb, device_status_word(), ep,
+                             a_early ? 1 : 0));
   PC_LAUNCH_CHECK();
   profile_end(slot, stream, kind, flops);
   return PC_OK;
