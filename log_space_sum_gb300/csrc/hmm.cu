@@ -593,13 +593,19 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
     PC_LAUNCH_CHECK();
   }
 
+  // The bf16 chain contractions run as split-K pairs of 128 x 256 tiles (k_umma_gemm,
+  // kSplit); each CTA's epilogue still finishes 128 x kChainBN.
+  constexpr bool kSplitChain = P == kBF16;
+  constexpr int kTileBN = kSplitChain ? 2 * kChainBN : kChainBN;
+  const dim3 chain_grid((kSplitChain ? 2 : 1) * cdiv(H, kBM), cdiv(B, kTileBN), 1);
+
   // forward chain: S_t for t = T-2 .. 0
   if (T >= 2) {
     OperandMaps ma, mb[2];
     if ((st = encode_maps(&ma, w.Aop, prec, kBM)) != PC_OK) return st;
     for (int i = 0; i < 2; ++i)
-      if ((st = encode_maps(&mb[i], w.ubm[i], prec, kChainBN)) != PC_OK) return st;
-    const dim3 grid(cdiv(H, kBM), cdiv(B, kChainBN), 1);
+      if ((st = encode_maps(&mb[i], w.ubm[i], prec, kTileBN)) != PC_OK) return st;
+    const dim3 grid = chain_grid;
     const int nkb = num_k_blocks(H, prec);
     for (int t = T - 2; t >= 0; --t) {
       typename EpiHmmFwd<P>::Params ep{};
@@ -617,8 +623,8 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       const OperandMaps& b = mb[(t + 1) & 1];
       // a_early: the A operand was converted before k_hmm_leaf, the kernel that precedes
       // the first layer, so no kernel still running when a layer starts writes it.
-      if ((st = launch_gemm<P, kChainBN, EpiHmmFwd<P>>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
-                                                        PC_KIND_HMM_FWD, 2ll * H * H * B, true)) != PC_OK)
+      if ((st = launch_gemm<P, kTileBN, EpiHmmFwd<P>, kSplitChain>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                                    PC_KIND_HMM_FWD, 2ll * H * H * B, true)) != PC_OK)
         return st;
     }
   }
@@ -636,8 +642,8 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
     OperandMaps ma, mb[2];
     if ((st = encode_maps(&ma, w.Atop, prec, kBM)) != PC_OK) return st;
     for (int i = 0; i < 2; ++i)
-      if ((st = encode_maps(&mb[i], w.wbm[i], prec, kChainBN)) != PC_OK) return st;
-    const dim3 grid(cdiv(H, kBM), cdiv(B, kChainBN), 1);
+      if ((st = encode_maps(&mb[i], w.wbm[i], prec, kTileBN)) != PC_OK) return st;
+    const dim3 grid = chain_grid;
     const int nkb = num_k_blocks(H, prec);
     for (int t = 0; t <= T - 2; ++t) {
       typename EpiHmmBwd<P>::Params ep{};
@@ -652,8 +658,8 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       }
       const OperandMaps& b = mb[t & 1];
       // a_early: the transposed A operand was converted before the forward chain
-      if ((st = launch_gemm<P, kChainBN, EpiHmmBwd<P>>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
-                                                        PC_KIND_HMM_ELEM, 2ll * H * H * B, true)) != PC_OK)
+      if ((st = launch_gemm<P, kTileBN, EpiHmmBwd<P>, kSplitChain>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                                    PC_KIND_HMM_ELEM, 2ll * H * H * B, true)) != PC_OK)
         return st;
     }
     if (dA) {

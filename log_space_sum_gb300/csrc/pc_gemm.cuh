@@ -117,11 +117,17 @@ __device__ __forceinline__ bool epilogue_bar_and(bool v) {
   return r != 0;
 }
 
-template <int P, int BN, class Epi>
+// kSplit: a 2-CTA cluster (consecutive blockIdx.x) computes one 128 x BN tile with
+// BN-wide MMAs, each CTA over half of K; after both K loops each CTA sends the partial
+// sums of the other half of the columns to its partner through distributed shared memory
+// and finishes its own 128 x BN/2 sub-tile. (A 128 x 128 MMA leaves half of the tensor
+// core's width idle; at batch 512 there are too few 128 x 256 tiles to fill the GPU
+// without splitting K.)
+template <int P, int BN, class Epi, bool kSplit = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
-                int num_kb, unsigned* status, const typename Epi::Params ep, int a_early) {
+                int num_kb_total, unsigned* status, const typename Epi::Params ep, int a_early) {
   using S = GemmShape<P, BN>;
   constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
   // Sliced modes: every K slice (kSliceK k-steps of the MMA) is accumulated from zero in
@@ -140,6 +146,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr uint32_t kTmemCols = kAccBufs * BN;
   static_assert(kTmemCols <= 512, "TMEM columns");
   constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
+  static_assert(!kSplit || (!kSliced && BN == 256 && kStages * S::kStageBytes >= 128 * 128 * 4),
+                "split K: unsliced 128 x 256 tiles, the ring holds the 64 KB exchange buffer");
+  constexpr int kEpiBN = kSplit ? BN / 2 : BN;  // columns this CTA's epilogue finishes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -153,9 +162,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM;
+  const int rank = kSplit ? static_cast<int>(cluster_ctarank()) : 0;
+  const int m0 = (kSplit ? blockIdx.x >> 1 : blockIdx.x) * kBM;
   const int n0 = blockIdx.y * BN;
   const int g = blockIdx.z;
+  // this CTA's share of K (in ring blocks) and the first columns of its epilogue
+  const int kb_first = kSplit && rank == 1 ? (num_kb_total + 1) / 2 : 0;
+  const int num_kb = kSplit ? (rank == 1 ? num_kb_total - kb_first : (num_kb_total + 1) / 2) : num_kb_total;
+  const int n0_epi = n0 + rank * kEpiBN;
 
   auto a_tile = [&](int s, int part) { return smem + s * S::kStageBytes + part * S::kABytes; };
   auto b_tile = [&](int s, int part) {
@@ -195,9 +209,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // first (still empty) ring slots' A tiles are fetched before waiting for it.
       const int early = a_early ? (num_kb < kStages ? num_kb : kStages) : 0;
       for (int kb = 0; kb < early; ++kb) {
+        const int kx = (kb_first + kb) * S::kBK;
         mbar_arrive_expect_tx(&full[kb], S::kStageBytes);
-        tma_load_3d(a_tile(kb, 0), &tmA, &full[kb], kb * S::kBK, m0, g);
-        if constexpr (P == kTF32x3) tma_load_3d(a_tile(kb, 1), &tmA_lo, &full[kb], kb * S::kBK, m0, g);
+        tma_load_3d(a_tile(kb, 0), &tmA, &full[kb], kx, m0, g);
+        if constexpr (P == kTF32x3) tma_load_3d(a_tile(kb, 1), &tmA_lo, &full[kb], kx, m0, g);
       }
       grid_dependency_wait();
       grid_dependents_launch();
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % kStages;
         const uint32_t ph = (kb / kStages) & 1;
-        const int kx = kb * S::kBK;
+        const int kx = (kb_first + kb) * S::kBK;
         if (kb >= early) {
           if (!mbar_wait(&empty[s], ph ^ 1, status, kErrTimeoutProducer)) break;
           mbar_arrive_expect_tx(&full[s], S::kStageBytes);
@@ -220,6 +235,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb) {
         mbar_wait(&full[kb % kStages], (kb / kStages) & 1, status, kErrTimeoutDrain);
       }
+    }
+    if constexpr (kSplit) {  // the epilogue's two cluster barriers
+      __syncwarp();
+      cluster_sync();
+      cluster_sync();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -305,19 +325,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // also on a timeout: the epilogue must not wait forever
       if constexpr (!kSliced) umma_commit(&acc_full[0]);
     }
+    if constexpr (kSplit) {  // the epilogue's two cluster barriers
+      __syncwarp();
+      cluster_sync();
+      cluster_sync();
+    }
   } else {
     // ------------------------------------------------------------------- epilogue
     const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
     const int ew = warp - 2;          // epilogue warp 0 .. 7
     grid_dependency_wait();           // the epilogue reads and writes global memory
-    Epi::prepare(ep, g, m0, n0, et, epi_smem);
+    Epi::prepare(ep, g, m0, n0_epi, et, epi_smem);
     epilogue_bar_sync();
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     const int half = ew >> 2;     // chunks c with (c & 1) == half
     const int row = q * 32 + lane;
     float* tbuf = Epi::kTranspose ? tbuf_base + ew * kTBufFloats : nullptr;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    constexpr int kChunks = BN / 64;  // 32-column chunks per epilogue warp
+    constexpr int kChunks = kEpiBN / 64;  // 32-column chunks per epilogue warp
     bool ok = true;
     if constexpr (kSliced) {
       float acc[kChunks][32];
@@ -348,24 +373,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (ok) {
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
-          Epi::apply(ep, g, m0, n0, row, (2 * c + half) * 32, acc[c], epi_smem, tbuf);
+          Epi::apply(ep, g, m0, n0_epi, row, (2 * c + half) * 32, acc[c], epi_smem, tbuf);
         }
       }
     } else {
       ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue));
       tc_fence_after();
-      if (ok) {
+      if constexpr (kSplit) {
+        // Exchange buffer: 128 rows x 128 floats in the (now idle) ring, 16-byte chunks of a
+        // row swizzled by the row so that 32 rows' accesses spread over the banks.
+        auto xoff = [&](int r, int chunk) { return static_cast<uint32_t>(r * 512 + (((chunk ^ r) & 31) << 4)); };
+        cluster_sync();  // both accumulators are final and both rings idle
+        if (ok) {
+          const uint32_t peer = cluster_map(smem_addr(smem), static_cast<uint32_t>(rank ^ 1));
+#pragma unroll 1
+          for (int c = half * 32; c < kEpiBN; c += 64) {
+            float v[32];
+            tmem_ld_32x32(lane_base + static_cast<uint32_t>((rank ^ 1) * kEpiBN + c), v);
+            if (num_kb == 0) {  // a share of no k-blocks: the accumulator was never written
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_cluster_v4(peer + xoff(row, (c >> 2) + j), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+        cluster_sync();  // the partner's partial sums of this CTA's columns have landed
+        if (ok) {
+#pragma unroll 1
+          for (int c = half * 32; c < kEpiBN; c += 64) {
+            float v[32];
+            tmem_ld_32x32(lane_base + static_cast<uint32_t>(rank * kEpiBN + c), v);
+            if (num_kb == 0) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 x = *reinterpret_cast<const float4*>(smem + xoff(row, (c >> 2) + j));
+              v[4 * j] += x.x;
+              v[4 * j + 1] += x.y;
+              v[4 * j + 2] += x.z;
+              v[4 * j + 3] += x.w;
+            }
+            Epi::apply(ep, g, m0, n0_epi, row, c, v, epi_smem, tbuf);
+          }
+        }
+      } else if (ok) {
 #pragma unroll 1
         for (int c = half * 32; c < BN; c += 64) {
           float v[32];
           tmem_ld_32x32(lane_base + static_cast<uint32_t>(c), v);
-          Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+          Epi::apply(ep, g, m0, n0_epi, row, c, v, epi_smem, tbuf);
         }
       }
     }
     tc_fence_before();
     ok = epilogue_bar_and(ok);
-    if (ok) Epi::finish(ep, g, m0, n0, et, epi_smem);
+    if (ok) Epi::finish(ep, g, m0, n0_epi, et, epi_smem);
   }
   __syncthreads();
   if (warp == 0) {

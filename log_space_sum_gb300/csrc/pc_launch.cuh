@@ -8,7 +8,8 @@
 namespace pc {
 
 // a_early: the A operand was written before the previous kernel in the stream started.
-template <int P, int BN, class Epi>
+// kSplit: grid.x counts CTAs (two per 128-row tile), launched as 2-CTA clusters.
+template <int P, int BN, class Epi, bool kSplit = false>
 pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo,
                         const CUtensorMap& b, const CUtensorMap& b_lo, int num_kb,
                         const typename Epi::Params& ep, cudaStream_t stream, int kind,
@@ -20,25 +21,29 @@ pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo
   PC_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return set_error(PC_ERR_CUDA, "device index %d out of range", dev);
   if (!attr_set[dev]) {
-    PC_CUDA(cudaFuncSetAttribute(k_umma_gemm<P, BN, Epi>,
+    PC_CUDA(cudaFuncSetAttribute(k_umma_gemm<P, BN, Epi, kSplit>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
     attr_set[dev] = true;
   }
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return PC_OK;
   const int slot = profile_begin(stream);
   // A programmatic dependent of the previous kernel in the stream (see k_umma_gemm).
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kSplit ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  PC_CUDA(cudaLaunchKernelEx(&cfg, k_umma_gemm<P, BN, Epi>, a, a_lo, b, b_lo, num_kb, device_status_word(), ep,
-                             a_early ? 1 : 0));
+  cfg.numAttrs = kSplit ? 2 : 1;
+  PC_CUDA(cudaLaunchKernelEx(&cfg, k_umma_gemm<P, BN, Epi, kSplit>, a, a_lo, b, b_lo, num_kb, device_status_word(),
+                             ep, a_early ? 1 : 0));
   PC_LAUNCH_CHECK();
   profile_end(slot, stream, kind, flops);
   return PC_OK;
