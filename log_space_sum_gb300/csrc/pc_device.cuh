@@ -299,7 +299,10 @@ __device__ __forceinline__ void store_operand_run(void* base, size_t idx, size_t
       }
     }
   } else {
-    for (int i = 0; i < n; ++i) store_operand<P>(base, idx + i, lo, v[i]);
+    // unrolled with a predicate: a runtime index would place v in local memory
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < n) store_operand<P>(base, idx + i, lo, v[i]);
   }
 }
 
@@ -340,6 +343,7 @@ __device__ __forceinline__ void load_operand_run(const void* base, size_t idx, s
       }
     }
   } else {
+#pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = i < n ? load_operand<P>(base, idx + i, lo) : 0.f;
   }
 }
