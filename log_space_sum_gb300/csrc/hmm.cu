@@ -257,6 +257,29 @@ __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, in
   }
 }
 
+// Split-K chain epilogues (bf16) stage their node-major tile [k][b] (row pitch 272
+// bytes: the 16-byte runs of 32 consecutive rows spread over all banks) and their
+// batch-major tile [b][k] in the idle ring; store_staged then writes both out with
+// coalesced 16-byte accesses (stage_tile_store_bf16).
+constexpr int kNodePitch = 272;
+constexpr int kBatchPitch = 256;
+constexpr int kNodeTileBytes = kBM * kNodePitch;
+constexpr int kBatchTileBytes = kChainBN * kBatchPitch;
+
+__device__ __forceinline__ void stage_node_run(uint8_t* stage, int row, int col0, const float (&v)[32]) {
+  uint4* nt = reinterpret_cast<uint4*>(stage + row * kNodePitch + col0 * 2);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    nt[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+
+__device__ __forceinline__ void stage_batch_col(uint8_t* stage, int row, int col0, const float (&v)[32]) {
+  __nv_bfloat16* bt = reinterpret_cast<__nv_bfloat16*>(stage + kNodeTileBytes);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) bt[(col0 + c) * (kBatchPitch / 2) + row] = __float2bfloat16_rn(v[c]);
+}
+
 // ----------------------------------------------------------- forward epilogue
 template <int P>
 struct EpiHmmFwd {
@@ -342,6 +365,43 @@ struct EpiHmmFwd {
     const float mx = warp_transpose_max(v);
     const int b = n0 + col0 + (threadIdx.x & 31);
     if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
+  }
+
+  // Split-K form of apply: u_t goes to the staged tiles instead of global memory.
+  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes;
+  static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
+  __device__ static void after_mma(const Params&, int, int, int, int, uint8_t*) {}
+  __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
+                                      float (&v)[32], uint8_t* smem, uint8_t* stage) {
+    static_assert(P == kBF16 && kStageE, "staged chain tiles hold bf16 operands");
+    const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
+    const float* Es = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
+    const int k = m0 + row;
+    const int nvalid = k < p.H ? min(32, p.B - (n0 + col0)) : 0;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? Es[(col0 + c) * kBM + row] * v[c] * c_s[col0 + c] : 0.f;
+    if (p.ubm) stage_batch_col(stage, row, col0, v);
+    if (p.U0) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) p.U0[static_cast<long long>(n0 + col0 + c) * p.H + k] = v[c];
+    }
+    if (p.un) stage_node_run(stage, row, col0, v);
+    const float mx = warp_transpose_max(v);
+    const int b = n0 + col0 + (threadIdx.x & 31);
+    if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
+  }
+  __device__ static void store_staged(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
+    const int nr = min(kBM, p.H - m0), nc = min(kChainBN, p.B - n0);
+    if (p.ubm)
+      stage_tile_store_bf16(stage + kNodeTileBytes, kBatchPitch,
+                            static_cast<__nv_bfloat16*>(p.ubm) + static_cast<long long>(n0) * p.ubm_ld + m0,
+                            p.ubm_ld, nc, nr, et);
+    if (p.un)
+      stage_tile_store_bf16(stage, kNodePitch,
+                            static_cast<__nv_bfloat16*>(p.un) + static_cast<long long>(m0) * p.un_ld +
+                                static_cast<long long>(p.t - 1) * p.B + n0,
+                            p.un_ld, nr, nc, et);
   }
 
   __device__ static void finish(const Params&, int, int, int, int, uint8_t*) {}
@@ -488,6 +548,60 @@ struct EpiHmmBwd : EpiNoHooks {
     if (p.wn)
       store_operand_run<P>(p.wn, static_cast<size_t>(j * p.wn_ld + static_cast<long long>(p.t + 1) * p.B + n0 + col0),
                            p.wn_lo, v, nvalid);
+  }
+
+  // Split-K form of apply: u_{t+1} is staged (coalesced) while the partner CTA finishes;
+  // w_{t+1} goes to the staged tiles, the node-major one in place of u.
+  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes;
+  static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
+  __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
+    if (p.fbm)
+      stage_tile_load_bf16(stage, kNodePitch,
+                           static_cast<const __nv_bfloat16*>(p.un) + static_cast<long long>(m0) * p.un_ld +
+                               static_cast<long long>(p.t) * p.B + n0,
+                           p.un_ld, min(kBM, p.H - m0), min(kChainBN, p.B - n0), et);
+  }
+  __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
+                                      float (&v)[32], uint8_t* smem, uint8_t* stage) {
+    static_assert(P == kBF16 && kStageE, "staged chain tiles hold bf16 operands");
+    const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
+    const float* Es = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
+    const int j = m0 + row;
+    const int nvalid = j < p.H ? min(32, p.B - (n0 + col0)) : 0;
+    if (p.fbm) {
+      const uint4* nt = reinterpret_cast<const uint4*>(stage + row * kNodePitch + col0 * 2);
+      float u[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = nt[q];
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          u[8 * q + 2 * r] = __uint_as_float(ww[r] << 16);
+          u[8 * q + 2 * r + 1] = __uint_as_float(ww[r] & 0xFFFF0000u);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) p.fbm[static_cast<long long>(n0 + col0 + c) * p.H + j] = u[c] * v[c];
+    }
+    if (!p.wbm) return;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? Es[(col0 + c) * kBM + row] * c_s[col0 + c] * v[c] : 0.f;
+    stage_batch_col(stage, row, col0, v);
+    if (p.wn) stage_node_run(stage, row, col0, v);
+  }
+  __device__ static void store_staged(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
+    if (!p.wbm) return;
+    const int nr = min(kBM, p.H - m0), nc = min(kChainBN, p.B - n0);
+    stage_tile_store_bf16(stage + kNodeTileBytes, kBatchPitch,
+                          static_cast<__nv_bfloat16*>(p.wbm) + static_cast<long long>(n0) * p.wbm_ld + m0,
+                          p.wbm_ld, nc, nr, et);
+    if (p.wn)
+      stage_tile_store_bf16(stage, kNodePitch,
+                            static_cast<__nv_bfloat16*>(p.wn) + static_cast<long long>(m0) * p.wn_ld +
+                                static_cast<long long>(p.t + 1) * p.B + n0,
+                            p.wn_ld, nr, nc, et);
   }
 };
 

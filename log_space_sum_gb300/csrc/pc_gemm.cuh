@@ -117,6 +117,64 @@ __device__ __forceinline__ bool epilogue_bar_and(bool v) {
   return r != 0;
 }
 
+// Staged bf16 tiles of 128 rows x 128 values in shared memory (row pitch `pitch` bytes,
+// a multiple of 16), moved to and from a row-major global matrix by all epilogue
+// threads: two 256-byte row segments per warp instruction instead of one scattered
+// 16-byte run per lane. Only rows < nrows and columns < ncols touch global memory; a
+// row whose start is not 16-byte aligned goes element by element.
+constexpr int kStageTileRows = 128;
+constexpr int kStageChunks = 16;  // 16-byte chunks of a 128-value bf16 row
+constexpr int kStageIters = kStageTileRows * kStageChunks / kEpiThreads;
+
+__device__ __forceinline__ void stage_tile_store_bf16(const uint8_t* tile, int pitch, __nv_bfloat16* dst,
+                                                      long long ld, int nrows, int ncols, int et) {
+#pragma unroll 4
+  for (int it = 0; it < kStageIters; ++it) {
+    const int i = et + it * kEpiThreads;
+    const int r = i / kStageChunks, c0 = (i % kStageChunks) * 8;
+    if (r >= nrows || c0 >= ncols) continue;
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + r * pitch + c0 * 2);
+    __nv_bfloat16* g = dst + r * ld + c0;
+    if (c0 + 8 <= ncols && (reinterpret_cast<uintptr_t>(g) & 15) == 0) {
+      *reinterpret_cast<uint4*>(g) = v;
+    } else {
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < ncols) g[j] = __ushort_as_bfloat16(static_cast<unsigned short>(w[j >> 1] >> (16 * (j & 1))));
+    }
+  }
+}
+
+// The inverse: global rows into the staged tile; elements outside nrows x ncols read 0.
+__device__ __forceinline__ void stage_tile_load_bf16(uint8_t* tile, int pitch, const __nv_bfloat16* src,
+                                                     long long ld, int nrows, int ncols, int et) {
+  uint4 v[kStageIters];
+#pragma unroll
+  for (int it = 0; it < kStageIters; ++it) {
+    const int i = et + it * kEpiThreads;
+    const int r = i / kStageChunks, c0 = (i % kStageChunks) * 8;
+    v[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (r >= nrows || c0 >= ncols) continue;
+    const __nv_bfloat16* g = src + r * ld + c0;
+    if (c0 + 8 <= ncols && (reinterpret_cast<uintptr_t>(g) & 15) == 0) {
+      v[it] = *reinterpret_cast<const uint4*>(g);
+    } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < ncols)
+          w[j >> 1] |= static_cast<uint32_t>(__bfloat16_as_ushort(g[j])) << (16 * (j & 1));
+      v[it] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < kStageIters; ++it) {
+    const int i = et + it * kEpiThreads;
+    *reinterpret_cast<uint4*>(tile + (i / kStageChunks) * pitch + (i % kStageChunks) * 16) = v[it];
+  }
+}
+
 // kSplit: a 2-CTA cluster (consecutive blockIdx.x) computes one 128 x BN tile with
 // BN-wide MMAs, each CTA over half of K; after both K loops each CTA sends the partial
 // sums of the other half of the columns to its partner through distributed shared memory
@@ -146,8 +204,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr uint32_t kTmemCols = kAccBufs * BN;
   static_assert(kTmemCols <= 512, "TMEM columns");
   constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
-  static_assert(!kSplit || (!kSliced && BN == 256 && kStages * S::kStageBytes >= 128 * 128 * 4),
-                "split K: unsliced 128 x 256 tiles, the ring holds the 64 KB exchange buffer");
+  // split K: the idle ring holds the 64 KB exchange buffer, then the epilogue's staged tiles
+  constexpr int kXchgBytes = 128 * 128 * 4;
+  if constexpr (kSplit)
+    static_assert(!kSliced && BN == 256 && kStages * S::kStageBytes >= kXchgBytes + Epi::kSplitStageBytes,
+                  "split K: unsliced 128 x 256 tiles, the ring holds the exchange buffer and the staged tiles");
   constexpr int kEpiBN = kSplit ? BN / 2 : BN;  // columns this CTA's epilogue finishes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -380,6 +441,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue));
       tc_fence_after();
       if constexpr (kSplit) {
+        // the MMAs are complete: this CTA's ring is idle; inputs of the epilogue are
+        // staged behind the exchange buffer while the partner finishes
+        if (ok) Epi::after_mma(ep, g, m0, n0_epi, et, smem + kXchgBytes);
         // Exchange buffer: 128 rows x 128 floats in the (now idle) ring, 16-byte chunks of a
         // row swizzled by the row so that 32 rows' accesses spread over the banks.
         auto xoff = [&](int r, int chunk) { return static_cast<uint32_t>(r * 512 + (((chunk ^ r) & 31) << 4)); };
@@ -417,7 +481,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               v[4 * j + 2] += x.z;
               v[4 * j + 3] += x.w;
             }
-            Epi::apply(ep, g, m0, n0_epi, row, c, v, epi_smem, tbuf);
+            Epi::apply_staged(ep, g, m0, n0_epi, row, c, v, epi_smem, smem + kXchgBytes);
           }
         }
       } else if (ok) {
@@ -431,6 +495,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc_fence_before();
     ok = epilogue_bar_and(ok);
+    if constexpr (kSplit) {
+      if (ok) Epi::store_staged(ep, g, m0, n0_epi, et, smem + kXchgBytes);
+    }
     if (ok) Epi::finish(ep, g, m0, n0_epi, et, epi_smem);
   }
   __syncthreads();
