@@ -370,6 +370,8 @@ struct EpiHmmFwd {
   // Split-K form of apply: u_t goes to the staged tiles instead of global memory.
   static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes;
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
+  // the batch-major tile is written only in apply_staged: the exchange's scratch until then
+  static constexpr int kSplitScratchOffset = kNodeTileBytes;
   __device__ static void after_mma(const Params&, int, int, int, int, uint8_t*) {}
   __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
                                       float (&v)[32], uint8_t* smem, uint8_t* stage) {
@@ -554,6 +556,8 @@ struct EpiHmmBwd : EpiNoHooks {
   // w_{t+1} goes to the staged tiles, the node-major one in place of u.
   static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes;
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
+  // the batch-major tile is written only in apply_staged: the exchange's scratch until then
+  static constexpr int kSplitScratchOffset = kNodeTileBytes;
   __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
     if (p.fbm)
       stage_tile_load_bf16(stage, kNodePitch,

@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // split K: the idle ring holds the 64 KB exchange buffer, then the epilogue's staged tiles
   constexpr int kXchgBytes = 128 * 128 * 4;
   if constexpr (kSplit)
-    static_assert(!kSliced && BN == 256 && kStages * S::kStageBytes >= kXchgBytes + Epi::kSplitStageBytes,
+    static_assert(!kSliced && BN == 256 && kStages * S::kStageBytes >= kXchgBytes + Epi::kSplitStageBytes &&
+                      Epi::kSplitScratchOffset + kEpiWarps * 4096 <= Epi::kSplitStageBytes,
                   "split K: unsliced 128 x 256 tiles, the ring holds the exchange buffer and the staged tiles");
   constexpr int kEpiBN = kSplit ? BN / 2 : BN;  // columns this CTA's epilogue finishes
   extern __shared__ uint8_t smem_raw[];
@@ -444,9 +445,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the MMAs are complete: this CTA's ring is idle; inputs of the epilogue are
         // staged behind the exchange buffer while the partner finishes
         if (ok) Epi::after_mma(ep, g, m0, n0_epi, et, smem + kXchgBytes);
-        // Exchange buffer: 128 rows x 128 floats in the (now idle) ring, 16-byte chunks of a
-        // row swizzled by the row so that 32 rows' accesses spread over the banks.
-        auto xoff = [&](int r, int chunk) { return static_cast<uint32_t>(r * 512 + (((chunk ^ r) & 31) << 4)); };
+        // Exchange buffer: 128 rows x 128 floats in the (now idle) ring, stored by 32-column
+        // chunk, then row, then 16-byte piece (swizzled by the row so that 32 rows' reads of
+        // one piece spread over the banks). A warp's 32 x 32 block is contiguous, so each
+        // remote store instruction writes 512 consecutive bytes: the block is first turned
+        // around in a 4 KB per-warp scratch buffer that the epilogue leaves free until
+        // apply_staged (Epi::kSplitScratchOffset).
+        auto xoff = [&](int chunk, int r, int piece) {
+          return static_cast<uint32_t>(((chunk * 128 + r) * 8 + (piece ^ (r & 7))) * 16);
+        };
+        uint8_t* scratch = smem + kXchgBytes + Epi::kSplitScratchOffset + ew * 4096;
         cluster_sync();  // both accumulators are final and both rings idle
         if (ok) {
           const uint32_t peer = cluster_map(smem_addr(smem), static_cast<uint32_t>(rank ^ 1));
@@ -460,7 +468,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              st_cluster_v4(peer + xoff(row, (c >> 2) + j), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              *reinterpret_cast<float4*>(scratch + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // rows 4i .. 4i+3 of the block, 8 pieces each
+              const int r = i * 4 + (lane >> 3), piece = lane & 7;
+              const float4 x = *reinterpret_cast<const float4*>(scratch + r * 128 + ((piece ^ (r & 7)) << 4));
+              st_cluster_v4(peer + xoff(c >> 5, q * 32 + r, piece), x.x, x.y, x.z, x.w);
+            }
+            __syncwarp();
           }
         }
         cluster_sync();  // the partner's partial sums of this CTA's columns have landed
@@ -475,7 +492,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float4 x = *reinterpret_cast<const float4*>(smem + xoff(row, (c >> 2) + j));
+              const float4 x = *reinterpret_cast<const float4*>(smem + xoff(c >> 5, row, j));
               v[4 * j] += x.x;
               v[4 * j + 1] += x.y;
               v[4 * j + 2] += x.z;
