@@ -372,6 +372,7 @@ struct EpiHmmFwd {
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
   // the batch-major tile is written only in apply_staged: the exchange's scratch until then
   static constexpr int kSplitScratchOffset = kNodeTileBytes;
+  static_assert(kSplitScratchOffset % 16 == 0, "16-byte scratch rows");
   __device__ static void after_mma(const Params&, int, int, int, int, uint8_t*) {}
   __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
                                       float (&v)[32], uint8_t* smem, uint8_t* stage) {
@@ -552,15 +553,17 @@ struct EpiHmmBwd : EpiNoHooks {
                            p.wn_lo, v, nvalid);
   }
 
-  // Split-K form of apply: u_{t+1} is staged (coalesced) while the partner CTA finishes;
+  // Split-K form of apply: u_{t+1} is staged (coalesced, asynchronous: the copies complete
+  // while the partial sums are exchanged);
   // w_{t+1} goes to the staged tiles, the node-major one in place of u.
   static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes;
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
   // the batch-major tile is written only in apply_staged: the exchange's scratch until then
   static constexpr int kSplitScratchOffset = kNodeTileBytes;
+  static_assert(kSplitScratchOffset % 16 == 0, "16-byte scratch rows");
   __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
     if (p.fbm)
-      stage_tile_load_bf16(stage, kNodePitch,
+      stage_tile_load_bf16_async(stage, kNodePitch,
                            static_cast<const __nv_bfloat16*>(p.un) + static_cast<long long>(m0) * p.un_ld +
                                static_cast<long long>(p.t) * p.B + n0,
                            p.un_ld, min(kBM, p.H - m0), min(kChainBN, p.B - n0), et);

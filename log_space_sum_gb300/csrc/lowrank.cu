@@ -33,7 +33,6 @@ namespace {
 
 constexpr int kLrRows = 128;   // own rows per CTA (TMEM lanes)
 constexpr int kLrChunk = 32;   // sweep columns per MMA group
-constexpr int kLrThreads = 128;
 constexpr int kLrMaxRank = 64;
 constexpr int kGradAccs = 4;   // TMEM accumulators of the gradient contractions
 
@@ -69,34 +68,6 @@ __host__ __device__ inline TileGeo tile_geo(int F, int rows, int K) {
 __host__ __device__ inline int tile_bytes(int F, int rows, int K) {
   const TileGeo g = tile_geo(F, rows, K);
   return fmt_parts(F) * g.bytes_part();
-}
-
-// Byte offset of element (row, k) inside one part of a tile: 128-byte swizzle of the
-// 16-byte chunk index by the row within its 8-row core group.
-__device__ __forceinline__ uint32_t tile_off(const TileGeo& g, int es, int row, int k) {
-  const int byte = k * es;
-  const int blk = byte >> 7;
-  const int in = byte & 127;
-  return static_cast<uint32_t>(blk * g.rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
-                               ((((in >> 4) ^ (row & 7)) & 7) << 4) + (in & 15));
-}
-
-// Writes v at (row, k) in format F (both parts for the split formats).
-template <int F>
-__device__ __forceinline__ void tile_put(uint8_t* tile, const TileGeo& g, int row, int k, float v) {
-  constexpr int es = fmt_bytes(F);
-  const uint32_t off = tile_off(g, es, row, k);
-  if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    *reinterpret_cast<__nv_bfloat16*>(tile + off) = hi;
-    if constexpr (F == kFmtBF16x2)
-      *reinterpret_cast<__nv_bfloat16*>(tile + g.bytes_part() + off) =
-          __float2bfloat16_rn(v - __bfloat162float(hi));
-  } else {
-    const float hi = tf32_rna(v);
-    *reinterpret_cast<float*>(tile + off) = hi;
-    if constexpr (F == kFmtTF32x2) *reinterpret_cast<float*>(tile + g.bytes_part() + off) = tf32_rna(v - hi);
-  }
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -146,32 +146,38 @@ __device__ __forceinline__ void stage_tile_store_bf16(const uint8_t* tile, int p
   }
 }
 
-// The inverse: global rows into the staged tile; elements outside nrows x ncols read 0.
-__device__ __forceinline__ void stage_tile_load_bf16(uint8_t* tile, int pitch, const __nv_bfloat16* src,
-                                                     long long ld, int nrows, int ncols, int et) {
-  uint4 v[kStageIters];
+// The inverse, global rows into the staged tile (zero outside nrows x ncols), issued as
+// asynchronous copies (cp.async) so that it overlaps other work; the issuing thread
+// completes them with cp_async_wait_all before a barrier that publishes the tile. Rows
+// whose start is not 16-byte aligned are loaded element by element on the spot.
+__device__ __forceinline__ void cp_async_16(uint8_t* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void stage_tile_load_bf16_async(uint8_t* tile, int pitch, const __nv_bfloat16* src,
+                                                           long long ld, int nrows, int ncols, int et) {
 #pragma unroll
   for (int it = 0; it < kStageIters; ++it) {
     const int i = et + it * kEpiThreads;
     const int r = i / kStageChunks, c0 = (i % kStageChunks) * 8;
-    v[it] = make_uint4(0u, 0u, 0u, 0u);
-    if (r >= nrows || c0 >= ncols) continue;
+    uint8_t* dst = tile + r * pitch + c0 * 2;
+    const int n = (r < nrows && c0 < ncols) ? min(8, ncols - c0) : 0;
+    if (n == 0) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
     const __nv_bfloat16* g = src + r * ld + c0;
-    if (c0 + 8 <= ncols && (reinterpret_cast<uintptr_t>(g) & 15) == 0) {
-      v[it] = *reinterpret_cast<const uint4*>(g);
+    if ((reinterpret_cast<uintptr_t>(g) & 15) == 0) {
+      cp_async_16(dst, g, static_cast<uint32_t>(n * 2));  // zero-fills beyond n values
     } else {
       uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (c0 + j < ncols)
-          w[j >> 1] |= static_cast<uint32_t>(__bfloat16_as_ushort(g[j])) << (16 * (j & 1));
-      v[it] = make_uint4(w[0], w[1], w[2], w[3]);
+        if (j < n) w[j >> 1] |= static_cast<uint32_t>(__bfloat16_as_ushort(g[j])) << (16 * (j & 1));
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-  }
-#pragma unroll
-  for (int it = 0; it < kStageIters; ++it) {
-    const int i = et + it * kEpiThreads;
-    *reinterpret_cast<uint4*>(tile + (i / kStageChunks) * pitch + (i % kStageChunks) * 16) = v[it];
   }
 }
 
@@ -480,6 +486,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
           }
         }
+        cp_async_wait_all();  // this thread's share of after_mma's staged inputs
         cluster_sync();  // the partner's partial sums of this CTA's columns have landed
         if (ok) {
 #pragma unroll 1
