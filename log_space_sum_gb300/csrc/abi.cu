@@ -17,6 +17,20 @@ __device__ unsigned g_device_status = 0;
 constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
+cudaStream_t g_side[kMaxDevices] = {};
+std::mutex g_side_mu;
+
+// Records an event on `from` and makes `to` wait for it (the event is released once it
+// has completed).
+pc_status_t stream_after(cudaStream_t to, cudaStream_t from) {
+  cudaEvent_t ev = nullptr;
+  PC_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+  const cudaError_t e1 = cudaEventRecord(ev, from);
+  const cudaError_t e2 = e1 == cudaSuccess ? cudaStreamWaitEvent(to, ev, 0) : e1;
+  cudaEventDestroy(ev);
+  if (e2 != cudaSuccess) return pc::set_error(PC_ERR_CUDA, "side stream event: %s", cudaGetErrorString(e2));
+  return PC_OK;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -95,6 +109,20 @@ unsigned* device_status_word() {
   }
   return g_status_ptr[dev];
 }
+
+pc_status_t SideStream::fork(cudaStream_t main) {
+  int dev = 0;
+  PC_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return set_error(PC_ERR_CUDA, "device index %d out of range", dev);
+  {
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    if (!g_side[dev]) PC_CUDA(cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking));
+    s = g_side[dev];
+  }
+  return stream_after(s, main);
+}
+
+pc_status_t SideStream::join(cudaStream_t main) { return stream_after(main, s); }
 
 pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision_t p,
                                int box_rows, int part, bool swizzle) {

@@ -680,16 +680,24 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   pc_status_t st;
 
   PC_CUDA(cudaMemsetAsync(w.umax, 0, size_t(T) * B * 4, s));
+  // Work off the forward chain's path (the token buckets for dE, the transposed A operand
+  // of the backward chain) runs on a side stream, beside the forward contractions, which
+  // leave some SMs free; it joins the caller's stream before the backward chain.
+  SideStream side;
+  const bool use_side = w.dEt || chain;
+  if (use_side && (st = side.fork(s)) != PC_OK) return st;
+  const cudaStream_t sa = use_side ? side.s : s;
   if (w.dEt) {
     // token buckets of every (position, sample): dE is then a per-token gather-sum
-    PC_CUDA(cudaMemsetAsync(w.tok_count, 0, size_t(V + 1) * 4, s));
-    k_token_hist<<<cdiv(static_cast<long long>(T) * B, 256), 256, 0, s>>>(tokens, T * B, V, w.tok_count);
+    PC_CUDA(cudaMemsetAsync(w.tok_count, 0, size_t(V + 1) * 4, sa));
+    k_token_hist<<<cdiv(static_cast<long long>(T) * B, 256), 256, 0, sa>>>(tokens, T * B, V, w.tok_count);
     PC_LAUNCH_CHECK();
-    k_exclusive_scan<<<1, 1024, 0, s>>>(w.tok_count, V, w.tok_offset);
+    k_exclusive_scan<<<1, 1024, 0, sa>>>(w.tok_count, V, w.tok_offset);
     PC_LAUNCH_CHECK();
-    k_token_bucket<<<cdiv(V, kBucketSpan), 256, 0, s>>>(tokens, T, B, V, w.tok_offset, w.tok_order);
+    k_token_bucket<<<cdiv(V, kBucketSpan), 256, 0, sa>>>(tokens, T, B, V, w.tok_offset, w.tok_order);
     PC_LAUNCH_CHECK();
   }
+  if (chain && (st = transpose_to_operand<P>(A, H, 0, 1, H, H, w.Atop, sa)) != PC_OK) return st;
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dA && !accumulate && T < 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
 
@@ -700,7 +708,6 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   k_emission_bounds<<<V, 256, 0, s>>>(w.Et, w.rs, H, w.emax, w.emax_rs);
   PC_LAUNCH_CHECK();
   if (T >= 2 && (st = rows_to_operand<P>(A, H, 0, 1, H, H, w.Aop, s)) != PC_OK) return st;
-  if (chain && (st = transpose_to_operand<P>(A, H, 0, 1, H, H, w.Atop, s)) != PC_OK) return st;
 
   // leaf (position T-1)
   {
@@ -752,6 +759,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
 
   k_hmm_root<<<B, 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, ll, w.rroot);
   PC_LAUNCH_CHECK();
+  if (use_side && (st = side.join(s)) != PC_OK) return st;
   if (!flows) return PC_OK;
 
   k_hmm_root_flows<P><<<dim3(cdiv(H, 32), cdiv(B, 32)), dim3(32, 8), 0, s>>>(
@@ -783,6 +791,14 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
                                                                     PC_KIND_HMM_ELEM, 2ll * H * H * B, true)) != PC_OK)
         return st;
     }
+    // dE's gather reads the flows of every position: it runs on the side stream beside
+    // the stacked dA contraction (which is bound by the tensor cores)
+    if (dE) {
+      if ((st = side.fork(s)) != PC_OK) return st;
+      k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, side.s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
+      PC_LAUNCH_CHECK();
+      if ((st = transpose_f32(w.dEt, H, 0, 1, V, H, dE, V, accumulate, side.s)) != PC_OK) return st;
+    }
     if (dA) {
       OperandMaps pa, pb;
       if ((st = encode_maps(&pa, w.wn, prec, kBM)) != PC_OK) return st;
@@ -794,13 +810,14 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
                                                         2ll * H * H * (T - 1) * B)) != PC_OK)
         return st;
     }
-  } else if (dA && !accumulate && T >= 2) {
-    PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
-  }
-  if (dE) {
-    k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
-    PC_LAUNCH_CHECK();
-    if ((st = transpose_f32(w.dEt, H, 0, 1, V, H, dE, V, accumulate, s)) != PC_OK) return st;
+    if (dE && (st = side.join(s)) != PC_OK) return st;
+  } else {
+    if (dA && !accumulate && T >= 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
+    if (dE) {
+      k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
+      PC_LAUNCH_CHECK();
+      if ((st = transpose_f32(w.dEt, H, 0, 1, V, H, dE, V, accumulate, s)) != PC_OK) return st;
+    }
   }
   return PC_OK;
 }

@@ -22,6 +22,16 @@ void clear_error();
 // looked up once per device).
 unsigned* device_status_word();
 
+// A library-owned stream of the current device for work that runs beside the caller's
+// stream within one call: fork() makes it wait for everything issued on `main` so far,
+// join() makes `main` wait for everything issued on it since. Both are event waits, so a
+// call stays asynchronous and can be captured into a CUDA graph.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  pc_status_t fork(cudaStream_t main);
+  pc_status_t join(cudaStream_t main);
+};
+
 // Contraction profiler hooks (no-ops unless pc_profile_start is active).
 int profile_begin(cudaStream_t s);
 void profile_end(int slot, cudaStream_t s, int kind, long long flops);
