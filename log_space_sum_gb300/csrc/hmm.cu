@@ -227,11 +227,37 @@ __global__ void k_dE_gather(const float* __restrict__ fbm, int H, const int* __r
   dEt[static_cast<long long>(v) * H + k] = acc;
 }
 
-// Stages the CTA's emission block Es[c][r] = E[m0 + r, x_{t,b}] (b = n0 + c) into shared
-// memory: rows and columns outside the problem read 0. The epilogue warps do this
-// while the contraction's K loop runs, so the gathers are off the critical path.
-// Each epilogue warp owns kBM / kEpiWarps columns and issues 8 columns x 4 rows of loads
-// per batch.
+// The staged emission block holds row r (a state) as 128 floats whose 16-byte pieces are
+// swizzled by r: an epilogue thread reads its row's 32 columns with 8 vector loads, and
+// the 32 rows of a warp spread over all banks.
+__device__ __forceinline__ int es_index(int r, int c) { return r * kChainBN + (((c >> 2) ^ (r & 7)) << 2) + (c & 3); }
+__device__ __forceinline__ void es_run(const float* Es, int row, int col0, float (&e)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 x = *reinterpret_cast<const float4*>(Es + es_index(row, col0 + 4 * j));
+    e[4 * j] = x.x;
+    e[4 * j + 1] = x.y;
+    e[4 * j + 2] = x.z;
+    e[4 * j + 3] = x.w;
+  }
+}
+// The per-column factors c_s[col0 .. col0+31] (the same for every thread: broadcast loads).
+__device__ __forceinline__ void cs_run(const float* c_s, int col0, float (&cv)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 x = *reinterpret_cast<const float4*>(c_s + col0 + 4 * j);
+    cv[4 * j] = x.x;
+    cv[4 * j + 1] = x.y;
+    cv[4 * j + 2] = x.z;
+    cv[4 * j + 3] = x.w;
+  }
+}
+
+// Stages the CTA's emission block Es(r, c) = E[m0 + r, x_{t,b}] (b = n0 + c) into shared
+// memory (es_index layout): rows and columns outside the problem read 0. The epilogue
+// warps do this while the contraction's K loop runs, so the gathers are off the critical
+// path. Each epilogue warp owns kBM / kEpiWarps columns and issues 8 columns x 4 rows of
+// loads per batch.
 __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, int H, int B, int m0, int n0,
                                                 const int* tok_s, float* Es, int et) {
   constexpr int kCols = kBM / kEpiWarps;  // columns staged by one epilogue warp
@@ -253,8 +279,22 @@ __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, in
 #pragma unroll
     for (int c = 0; c < 8; ++c)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) Es[(cb + c) * kBM + lane + 32 * i] = vals[c][i];
+      for (int i = 0; i < 4; ++i) Es[es_index(lane + 32 * i, cb + c)] = vals[c][i];
   }
+}
+
+// Column maxima of the warp's 32 x 32 block of non-negative values (thread = row, v[c] =
+// column c): lane l returns the maximum of column l. Non-negative floats order like
+// their bit patterns, so each column is one integer warp reduction.
+__device__ __forceinline__ float warp_column_max(const float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+  unsigned mx = 0;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(v[c]) & 0x7FFFFFFFu);  // -0 as +0
+    if (lane == c) mx = m;
+  }
+  return __uint_as_float(mx);
 }
 
 // Split-K chain epilogues (bf16) stage their node-major tile [k][b] (row pitch 272
@@ -337,16 +377,16 @@ struct EpiHmmFwd {
     const int k = m0 + row;
     const bool kin = k < p.H;
     const int nvalid = kin ? min(32, p.B - (n0 + col0)) : 0;
-    float e[32];
+    float e[32], cv[32];
+    if constexpr (kStageE) {
+      es_run(Es, row, col0, e);
+    } else {
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      if constexpr (kStageE)
-        e[c] = Es[(col0 + c) * kBM + row];
-      else
-        e[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + k] : 0.f;
+      for (int c = 0; c < 32; ++c) e[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + k] : 0.f;
     }
+    cs_run(c_s, col0, cv);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * v[c] * c_s[col0 + c] : 0.f;
+    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * v[c] * cv[c] : 0.f;
     if (p.ubm) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
@@ -361,9 +401,8 @@ struct EpiHmmFwd {
     if (p.un && nvalid > 0)
       store_operand_run<P>(p.un, static_cast<size_t>(k * p.un_ld + static_cast<long long>(p.t - 1) * p.B + n0 + col0),
                            p.un_lo, v, nvalid);
-    // column maxima: lane l ends with the warp's maximum of column col0 + l
-    const float mx = warp_transpose_max(v);
     const int b = n0 + col0 + (threadIdx.x & 31);
+    const float mx = warp_column_max(v);
     if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
   }
 
@@ -381,8 +420,11 @@ struct EpiHmmFwd {
     const float* Es = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
     const int k = m0 + row;
     const int nvalid = k < p.H ? min(32, p.B - (n0 + col0)) : 0;
+    float e[32], cv[32];
+    es_run(Es, row, col0, e);
+    cs_run(c_s, col0, cv);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? Es[(col0 + c) * kBM + row] * v[c] * c_s[col0 + c] : 0.f;
+    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * v[c] * cv[c] : 0.f;
     if (p.ubm) stage_batch_col(stage, row, col0, v);
     if (p.U0) {
 #pragma unroll
@@ -390,8 +432,8 @@ struct EpiHmmFwd {
         if (c < nvalid) p.U0[static_cast<long long>(n0 + col0 + c) * p.H + k] = v[c];
     }
     if (p.un) stage_node_run(stage, row, col0, v);
-    const float mx = warp_transpose_max(v);
     const int b = n0 + col0 + (threadIdx.x & 31);
+    const float mx = warp_column_max(v);
     if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
   }
   __device__ static void store_staged(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
@@ -528,12 +570,11 @@ struct EpiHmmBwd : EpiNoHooks {
       load_operand_run<P>(p.un, static_cast<size_t>(j * p.un_ld + static_cast<long long>(p.t) * p.B + n0 + col0),
                           p.un_lo, u, nvalid);
     if (p.wbm) {
+      if constexpr (kStageE) {
+        es_run(Es, row, col0, e);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if constexpr (kStageE)
-          e[c] = Es[(col0 + c) * kBM + row];
-        else
-          e[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + j] : 0.f;
+        for (int c = 0; c < 32; ++c) e[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + j] : 0.f;
       }
     }
     if (p.fbm) {
@@ -593,8 +634,11 @@ struct EpiHmmBwd : EpiNoHooks {
         if (c < nvalid) p.fbm[static_cast<long long>(n0 + col0 + c) * p.H + j] = u[c] * v[c];
     }
     if (!p.wbm) return;
+    float e[32], cv[32];
+    es_run(Es, row, col0, e);
+    cs_run(c_s, col0, cv);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? Es[(col0 + c) * kBM + row] * c_s[col0 + c] * v[c] : 0.f;
+    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * cv[c] * v[c] : 0.f;
     stage_batch_col(stage, row, col0, v);
     if (p.wn) stage_node_run(stage, row, col0, v);
   }

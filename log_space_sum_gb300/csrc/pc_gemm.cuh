@@ -542,21 +542,4 @@ struct EpiNoHooks {
   __device__ static void finish(const Params&, int, int, int, int, uint8_t*) {}
 };
 
-// Lane l of the warp ends with the maximum over the 32 lanes of v[l] (v is clobbered).
-__device__ __forceinline__ float warp_transpose_max(float (&v)[32]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool upper = (lane & w) != 0;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = upper ? v[i] : v[i + w];
-      const float keep = upper ? v[i + w] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
-      v[i] = fmaxf(keep, recv);
-    }
-  }
-  return v[0];
-}
-
 }  // namespace pc
