@@ -6,13 +6,15 @@ Workloads (synthetic, seeded; see workloads/):
            (pyjuice PR #62, Results table). One step = one pc_hmm_fwd_bwd call: 31 tied
            4096x4096 sum layers forward, the 31 element-flow contractions backward and
            the depth-15872 parameter-flow contraction.
+  hmm1024  the table's second HMM: 1024 latent states, 64 positions, batch 512
+           (vocabulary 1024): 63 + 63 tied 1024x1024 layers, depth-32256 dA.
   layer    one dense sum layer M = N = 1024, batch 128: pc_sum_layer_fwd + _bwd.
   hclt     HCLT, 768 variables, 1024 latents, 512 categories, batch 512: pc_hclt_fwd_bwd.
   lowrank  LowRank exp_sum layer M = N = 1024, rank 16, batch 64, scale spread 1 nat:
            pc_lowrank_exp_sum_fwd + _bwd (dA, dB, e, F+, W).
 
 python bench.py [--gpus N --steps K --warmup W --precision auto|tf32|fp32
-                 --impl ours|reference --workload hmm|layer|hclt|lowrank]
+                 --impl ours|reference --workload hmm|hmm1024|layer|hclt|lowrank]
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own batch (weak
 scaling; no data-path collective). Between timed steps a 256 MiB buffer is written to
@@ -41,7 +43,13 @@ sys.path.insert(0, ROOT)
 UNIT = "samples/s"
 HMM_METRIC = "HMM 4096x32 fwd+bwd samples/s @batch 512 (1 GB300); % tensor/HBM roofline"
 # pages' RTX PRO 6000 figures for the HMM workload (context, other hardware)
-PAGES_SAMPLES_PER_S = {"auto": 512 / 32.1e-3, "fp32": 512 / 49.9e-3}
+# The pages' whole-circuit figures (RTX PRO 6000, batch 512, forward + backward): another
+# machine's numbers, the denominators of vs_baseline only.
+PAGES_SAMPLES_PER_S = {
+    "hmm": {"auto": 512 / 32.1e-3, "fp32": 512 / 49.9e-3},
+    "hmm1024": {"auto": 512 / 10.2e-3, "fp32": 512 / 12.3e-3},
+    "hclt": {"auto": 512 / 48.1e-3, "fp32": 512 / 64.3e-3},
+}
 DTYPE = {"auto": "bf16", "tf32": "tf32", "fp32": "3xtf32"}
 # nominal dense tensor rates relative to bf16 (2.25 PF bf16, 1.1 PF tf32)
 TF32_OVER_BF16 = 1.1 / 2.25
@@ -58,7 +66,7 @@ def parse():
     ap.add_argument("--precision", default="auto", choices=["auto", "tf32", "fp32"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="hmm", choices=["hmm", "layer", "hclt", "lowrank"])
+    ap.add_argument("--workload", default="hmm", choices=["hmm", "hmm1024", "layer", "hclt", "lowrank"])
     ap.add_argument("--hclt-nvars", type=int, default=768,
                     help="HCLT variables (768 = the workload; fewer for a profiler-sized case)")
     return ap.parse_args()
@@ -95,6 +103,7 @@ class Workload:
 
 class HmmWorkload(Workload):
     name, metric, batch = "hmm", HMM_METRIC, 512
+    H, T, V = 4096, 32, 1024
     desc = "HMM 4096 latents x 32 positions, vocab 1024, batch 512: forward LL + backward flows dpi, dA, dE"
     data = "synthetic (seeded: softmax N(0,1) rows for pi, A, E; uniform tokens)"
 
@@ -103,7 +112,7 @@ class HmmWorkload(Workload):
         return hmm(512)
 
     def config(self):
-        return {"H": 4096, "T": 32, "V": 1024, "B": 512}
+        return {"H": self.H, "T": self.T, "V": self.V, "B": self.batch}
 
     def oracle(self, d, b):
         from oracle.hmm import hmm_fwd_bwd
@@ -127,6 +136,17 @@ class HmmWorkload(Workload):
             step(dev_in)
             host_out.copy_(out["ll"], non_blocking=True)
         return step, e2e, host_in.numel() * 4, host_out.numel() * 8
+
+
+class Hmm1024Workload(HmmWorkload):
+    name, batch = "hmm1024", 512
+    H, T, V = 1024, 64, 1024
+    metric = "HMM 1024x64 fwd+bwd samples/s @batch 512 (1 GB300); % tensor/HBM roofline"
+    desc = "HMM 1024 latents x 64 positions, vocab 1024, batch 512: forward LL + backward flows dpi, dA, dE"
+
+    def inputs(self):
+        from workloads import hmm_1024x64
+        return hmm_1024x64()
 
 
 class LayerWorkload(Workload):
@@ -261,7 +281,7 @@ class LowRankWorkload(Workload):
         return step, e2e, (hA.numel() + hB.numel()) * 4, h_out.numel() * 4
 
 
-WORKLOADS = {w.name: w for w in (HmmWorkload(), LayerWorkload(), HcltWorkload(), LowRankWorkload())}
+WORKLOADS = {w.name: w for w in (HmmWorkload(), Hmm1024Workload(), LayerWorkload(), HcltWorkload(), LowRankWorkload())}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -373,16 +393,19 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kind: str, precision: str):
-    """DRAM bytes per launch of a contraction from a committed ncu capture, or None
-    when there is none or the kernel sources changed since it was taken."""
+def recorded_traffic(kind: str, precision: str, workload: str):
+    """DRAM bytes per launch of a contraction from a committed ncu capture of this
+    workload, or None when there is none or the kernel sources changed since it was
+    taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
     ent = d.get(f"{kind}:{precision}")
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("workload", "hmm" if kind.startswith("hmm") else kind.split("_")[0]) != workload:
+        return None
+    if ent.get("source_hash") != kernel_source_hash():
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -495,7 +518,7 @@ def run_ours(args):
         achieved = exps * dn / (dms / 1e3) / 1e12
         roofline = {
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "Texp/s", "frac": achieved / peak,
-            "traffic": recorded_traffic(dom, args.precision), "kernel": f"k_lowrank* ({dom})",
+            "traffic": recorded_traffic(dom, args.precision, w.name), "kernel": f"k_lowrank* ({dom})",
             "launches_timed": dn, "ms_per_launch": dms / dn,
             "peak_source": f"derived: {N_SMS} SMs x {MUFU_PER_SM_CLK} exp/clk x {mhz:.0f} MHz",
             "share_of_step": sum(v[0] for v in by_kind.values()) / sum(ms_steps_prof) if world == 1 else None,
@@ -506,7 +529,7 @@ def run_ours(args):
         peak = bf16_peak if args.precision == "auto" else bf16_peak * TF32_OVER_BF16
         roofline = {
             "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": recorded_traffic(dom, args.precision), "kernel": f"k_umma_gemm ({dom})",
+            "traffic": recorded_traffic(dom, args.precision, w.name), "kernel": f"k_umma_gemm ({dom})",
             "launches_timed": dn, "ms_per_launch": dms / dn,
             "peak_source": f"{peak_src} bf16 sustained" + ("" if args.precision == "auto"
                                                            else " x 1.1/2.25 (nominal tf32/bf16)"),
@@ -534,7 +557,9 @@ def run_ours(args):
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
-        ref = PAGES_SAMPLES_PER_S.get(args.precision) if w.name == "hmm" else None
+        ref = PAGES_SAMPLES_PER_S.get(w.name, {}).get(args.precision)
+        if w.name == "hclt" and w.nvars != 768:
+            ref = None
         line = {
             "metric": w.metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,

@@ -1,7 +1,8 @@
 """GPU parity of the whole HMM circuit (pc_hmm_fwd_bwd through the C ABI) against the
 float64 oracle: the tiny workload in every mode, ragged and degenerate shapes, the
 4096-state workload at batch 128 (every output) and 512 (sampled log-likelihoods,
-flow invariants), and the uniform-emission closed form."""
+flow invariants), the 1024-state, 64-position workload at batch 512 (every output), and
+the uniform-emission closed form."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,7 @@ import torch
 import log_space_sum_gb300 as pc
 from oracle.hmm import hmm_fwd_bwd, hmm_ll
 from tolerances import FLOW_TOL, LL_TOL, MODES, flow_err, ll_err
-from workloads import hmm, hmm_inputs, tiny_hmm
+from workloads import hmm, hmm_1024x64, hmm_inputs, tiny_hmm
 
 pytestmark = pytest.mark.gpu
 
@@ -94,6 +95,22 @@ def test_hmm_4096_batch128_every_output(hmm128, mode):
     ll, dpi, dA, dE = _gpu_run(d, mode)
     errs = ll_err(ll, rl), flow_err(dpi, rpi), flow_err(dA, rA), flow_err(dE, rE)
     print(f"hmm4096 B128 {mode}: ll {errs[0]:.3e} dpi {errs[1]:.3e} dA {errs[2]:.3e} dE {errs[3]:.3e}")
+    assert errs[0] <= LL_TOL[mode]
+    assert max(errs[1:]) <= FLOW_TOL[mode]
+
+
+@pytest.fixture(scope="module")
+def hmm1024():
+    d = hmm_1024x64()
+    return d, _oracle(d)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_hmm_1024x64_batch512_every_output(hmm1024, mode):
+    d, (rl, rpi, rA, rE) = hmm1024
+    ll, dpi, dA, dE = _gpu_run(d, mode)
+    errs = ll_err(ll, rl), flow_err(dpi, rpi), flow_err(dA, rA), flow_err(dE, rE)
+    print(f"hmm1024x64 B512 {mode}: ll {errs[0]:.3e} dpi {errs[1]:.3e} dA {errs[2]:.3e} dE {errs[3]:.3e}")
     assert errs[0] <= LL_TOL[mode]
     assert max(errs[1:]) <= FLOW_TOL[mode]
 

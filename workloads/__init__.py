@@ -65,6 +65,12 @@ def hmm(B: int = 512):
     return hmm_inputs(4096, 32, 1024, B, seed=3 if B == 128 else 4)
 
 
+def hmm_1024x64():
+    """The second HMM workload of the pages' timing table: 1024 latents, 64 positions,
+    batch 512 (the vocabulary is not stated there: 1024, as in the 4096-latent one)."""
+    return hmm_inputs(1024, 64, 1024, 512, seed=9)
+
+
 # ------------------------------------------------------- single dense layer
 def layer_inputs(G: int, M: int, N: int, B: int, seed: int, child_stride: int | None = None,
                  x_scale: float = 3.0, f_kind: str = "ones"):
