@@ -12,9 +12,11 @@ Workloads (synthetic, seeded; see workloads/):
   hclt     HCLT, 768 variables, 1024 latents, 512 categories, batch 512: pc_hclt_fwd_bwd.
   lowrank  LowRank exp_sum layer M = N = 1024, rank 16, batch 64, scale spread 1 nat:
            pc_lowrank_exp_sum_fwd + _bwd (dA, dB, e, F+, W).
+  mstep    the EM M-step (pc_em_normalize) of the HMM 4096x32 parameters (dpi, dA, dE)
+           and of the LowRank 1024x1024 layer (normalize F+ / W); unit: nodes/s.
 
 python bench.py [--gpus N --steps K --warmup W --precision auto|tf32|fp32
-                 --impl ours|reference --workload hmm|hmm1024|layer|hclt|lowrank]
+                 --impl ours|reference --workload hmm|hmm1024|layer|hclt|lowrank|mstep]
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own batch (weak
 scaling; no data-path collective). Between timed steps a 256 MiB buffer is written to
@@ -66,7 +68,7 @@ def parse():
     ap.add_argument("--precision", default="auto", choices=["auto", "tf32", "fp32"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="hmm", choices=["hmm", "hmm1024", "layer", "hclt", "lowrank"])
+    ap.add_argument("--workload", default="hmm", choices=["hmm", "hmm1024", "layer", "hclt", "lowrank", "mstep"])
     ap.add_argument("--hclt-nvars", type=int, default=768,
                     help="HCLT variables (768 = the workload; fewer for a profiler-sized case)")
     return ap.parse_args()
@@ -95,7 +97,12 @@ class Workload:
 
     name = metric = desc = ""
     batch = 0
+    unit = UNIT  # a "sample" is one unit of the workload's batch
+    unit_noun, oracle_what = "samples", "forward + backward"
     roofline_bound = "tensor"
+
+    def dtype(self, prec):
+        return DTYPE[prec]
 
     def config(self):
         return {}
@@ -281,7 +288,68 @@ class LowRankWorkload(Workload):
         return step, e2e, (hA.numel() + hB.numel()) * 4, h_out.numel() * 4
 
 
-WORKLOADS = {w.name: w for w in (HmmWorkload(), Hmm1024Workload(), LayerWorkload(), HcltWorkload(), LowRankWorkload())}
+class MstepWorkload(Workload):
+    """The EM M-step after a backward: every node's parameters normalized over its
+    children (plain, for the HMM's dpi, dA, dE) or the LowRank conditional update
+    normalize(F+ / W). A step updates all 9217 nodes; the unit is nodes/s."""
+    name, unit, roofline_bound = "mstep", "nodes/s", "hbm"
+    unit_noun, oracle_what = "nodes", "M-step"
+    PARTS = (("pi", 1, 4096), ("A", 4096, 4096), ("E", 4096, 1024), ("lowrank", 1024, 1024))
+    batch = sum(m for _, m, _ in PARTS)
+    metric = "EM M-step nodes/s (HMM 4096x32 + LowRank 1024x1024 parameters, 1 GB300); % HBM roofline"
+    desc = ("EM M-step: normalize dpi [1x4096], dA [4096x4096], dE [4096x1024] of the HMM 4096x32 workload "
+            "and the LowRank 1024x1024 conditional update normalize(F+/W)")
+    data = "synthetic (seeded: flows Gamma(0.5,1), W Gamma(2,1), previous parameters U[0,1))"
+
+    def inputs(self):
+        from workloads import em_statistics
+        return em_statistics()
+
+    def dtype(self, prec):
+        return "f32"  # the M-step has no precision modes
+
+    def config(self):
+        return {"parts": {k: [m, n] for k, m, n in self.PARTS}, "nodes": self.batch}
+
+    def oracle(self, d, b):
+        from oracle.em import em_conditional, em_plain
+        left = b
+        for k, m, _ in self.PARTS:
+            r = min(left, m)
+            if r <= 0:
+                break
+            if k == "lowrank":
+                em_conditional(d["F_lowrank"][:r], d["W_lowrank"][:r], d["theta_lowrank"][:r])
+            else:
+                em_plain(d["F_" + k][:r], d["theta_" + k][:r])
+            left -= r
+
+    def device(self, pc, d, dev, prec):
+        import torch
+        t = {k: torch.from_numpy(v).to(dev) for k, v in d.items()}
+        names = [k for k, _, _ in self.PARTS]
+
+        def step(src=None):
+            s = t if src is None else src
+            for k in names:
+                pc.em_normalize(s["F_" + k], t["theta_" + k], s["W_lowrank"] if k == "lowrank" else None)
+        host_in = {k: torch.from_numpy(d[k]).pin_memory() for k in d if k.startswith(("F_", "W_"))}
+        dev_in = {k: torch.empty_like(t[k]) for k in host_in}
+        host_out = {k: torch.empty(t["theta_" + k].shape, dtype=torch.float32).pin_memory() for k in names}
+
+        def e2e():
+            for k in host_in:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            step(dev_in)
+            for k in names:
+                host_out[k].copy_(t["theta_" + k], non_blocking=True)
+        h2d = sum(v.numel() * 4 for v in host_in.values())
+        d2h = sum(v.numel() * 4 for v in host_out.values())
+        return step, e2e, h2d, d2h
+
+
+WORKLOADS = {w.name: w for w in (HmmWorkload(), Hmm1024Workload(), LayerWorkload(), HcltWorkload(), LowRankWorkload(),
+                                 MstepWorkload())}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -297,8 +365,8 @@ def oracle_sample_rate(w, d, target_s: float = 12.0):
         if dt >= target_s / 2 or b >= w.batch:
             break
         b = min(w.batch, max(b * 2, int(b * target_s / max(dt, 1e-3))))
-    desc = (f"float64 NumPy oracle ({w.name}): the same forward + backward for the first {b} of the "
-            f"{w.batch} samples of the workload, {dt:.1f} s")
+    desc = (f"float64 NumPy oracle ({w.name}): the same {w.oracle_what} for the first {b} of the "
+            f"{w.batch} {w.unit_noun} of the workload, {dt:.1f} s")
     return b / dt, desc, os.cpu_count(), b, dt
 
 
@@ -325,12 +393,12 @@ def run_reference(args):
     ms = 1e3 * statistics.mean(times)
     value = b / (ms / 1e3)
     line = {
-        "impl": "reference", "metric": w.metric, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": w.metric, "value": value, "unit": w.unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.desc + f" (oracle on {b}-sample slices)", **w.config(), "sample_batch": b},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": w.unit, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": w.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -509,7 +577,18 @@ def run_ours(args):
         k[2] += 1
     dom = max(by_kind, key=lambda k: by_kind[k][0])
     dms, dfl, dn = by_kind[dom]
-    if w.roofline_bound == "alu":
+    if w.roofline_bound == "hbm":
+        # the kind's recorded count is its algorithmic bytes (read once, written once)
+        achieved = dfl / (dms / 1e3) / 1e9
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        roofline = {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(dom, args.precision, w.name), "kernel": f"k_em_normalize ({dom})",
+            "launches_timed": dn, "ms_per_launch": dms / dn,
+            "peak_source": f"{peak_src} copy bandwidth",
+            "share_of_step": sum(v[0] for v in by_kind.values()) / sum(ms_steps_prof) if world == 1 else None,
+        }
+    elif w.roofline_bound == "alu":
         # one exp per (sample, node, child) in every LowRank pass
         cfg = w.config()
         exps = cfg["M"] * cfg["N"] * cfg["B"]
@@ -554,22 +633,22 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, desc, cores, b, dt = oracle_sample_rate(w, d)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": rate, "unit": w.unit, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
         ref = PAGES_SAMPLES_PER_S.get(w.name, {}).get(args.precision)
         if w.name == "hclt" and w.nvars != 768:
             ref = None
         line = {
-            "metric": w.metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": w.metric, "value": value, "unit": w.unit, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": (value / world / ref) if ref else None,
-            "dtype": DTYPE[args.precision], "data": w.data,
+            "dtype": w.dtype(args.precision), "data": w.data,
             "config": {"workload": w.desc, **w.config(), "precision": args.precision,
                        "l2": "flushed between timed steps (256 MiB write)", "launch": "eager stream",
                        "parallelism": f"replicas x{world}"},
             "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d_bytes),
+            "e2e": {"value": e2e_value, "unit": w.unit, "h2d_bytes_per_step": int(h2d_bytes),
                     "d2h_bytes_per_step": int(d2h_bytes)},
             "gpu_launches": int(launches),
             "roofline": roofline,

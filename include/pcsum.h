@@ -98,13 +98,14 @@ PCSUM_API pc_status_t pc_device_status(pc_stream_t stream);
  * launches records a CUDA event pair on its stream (at most `capacity` launches).
  * pc_profile_stop synchronises the device, then writes for each recorded launch i
  * (i < *count <= capacity): ms[i] = elapsed device time, kind[i] = which contraction
- * (PC_KIND_*), flops[i] = its algorithmic flops 2*M*N*K (each product counted once).
+ * (PC_KIND_*), flops[i] = its algorithmic flops 2*M*N*K (each product counted once);
+ * for PC_KIND_EM_MSTEP (memory-bound) flops[i] holds the algorithmic bytes instead.
  * Not thread-safe; host-side event objects only, no device memory. */
 typedef enum {
   PC_KIND_LAYER_FWD = 0, PC_KIND_LAYER_ELEM = 1, PC_KIND_LAYER_PARAM = 2,
   PC_KIND_HMM_FWD = 3, PC_KIND_HMM_ELEM = 4, PC_KIND_HMM_PARAM = 5,
   PC_KIND_HCLT_FWD = 6, PC_KIND_HCLT_ELEM = 7, PC_KIND_HCLT_PARAM = 8,
-  PC_KIND_LOWRANK_FWD = 9, PC_KIND_LOWRANK_BWD = 10
+  PC_KIND_LOWRANK_FWD = 9, PC_KIND_LOWRANK_BWD = 10, PC_KIND_EM_MSTEP = 11
 } pc_kind_t;
 PCSUM_API pc_status_t pc_profile_start(int capacity);
 PCSUM_API pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long long* flops,
@@ -251,6 +252,25 @@ PCSUM_API pc_status_t pc_lowrank_exp_sum_bwd(int M, int N, int K, int B, const f
                                              float* dA, float* dB, float* e, float* Fplus,
                                              float* Wstat, int accumulate, pc_precision_t prec,
                                              void* ws, size_t ws_bytes, pc_stream_t stream);
+
+/* ---------------------------------------------------------------- EM M-step
+ * The M-step that follows the backward (pyjuice LowRank API doc, Training): for each of
+ * the G*M nodes (rows), over its N children,
+ *
+ *   theta[g][i][j] = r[g][i][j] / sum_j' r[g][i][j'],
+ *   r = F                          (W == NULL: the plain normalize(F) of the parameter
+ *                                   flows of a sum layer, HMM or HCLT; Baum-Welch)
+ *   r = F / W, 0 where W <= 0      (W != NULL: the LowRank conditional update
+ *                                   normalize(theta * F+ / F-) with F- = theta * W)
+ *
+ * F, W, theta: device, row-major [G][M][N] float32, caller-owned; theta is read only
+ * where a row's sum of r is zero or not finite (no flow reached the node): that row keeps
+ * its parameters (the pages are silent there). Rows are independent; F and W are not
+ * modified and may not alias theta. Asynchronous on `stream`, no workspace, capturable.
+ * Errors: PC_ERR_NULL (F or theta NULL), PC_ERR_SHAPE (G, M, N < 1 or G*M >= 2^31);
+ * nothing is launched then. */
+PCSUM_API pc_status_t pc_em_normalize(int G, int M, int N, const float* F, const float* W, float* theta,
+                                      pc_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -9,6 +9,7 @@ from ._native import PCError, declared_symbols, load  # noqa: F401
 from .api import (  # noqa: F401
     PRECISIONS,
     device_status,
+    em_normalize,
     hclt_fwd_bwd,
     hmm_fwd_bwd,
     lowrank_exp_sum_bwd,

@@ -22,7 +22,7 @@ STATUS = {
 KINDS = {
     0: "layer_fwd", 1: "layer_elem", 2: "layer_param", 3: "hmm_fwd", 4: "hmm_elem",
     5: "hmm_param", 6: "hclt_fwd", 7: "hclt_elem", 8: "hclt_param", 9: "lowrank_fwd",
-    10: "lowrank_bwd",
+    10: "lowrank_bwd", 11: "em_mstep",
 }
 
 _i, _ll, _sz, _p, _f, _d = C.c_int, C.c_longlong, C.c_size_t, C.c_void_p, C.c_float, C.c_double
@@ -46,6 +46,7 @@ SIGNATURES = {
     "pc_hclt_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
     "pc_lowrank_exp_sum_workspace": [_i, _i, _i, _i, _i, _i, _p],
     "pc_lowrank_exp_sum_fwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p],
+    "pc_em_normalize": [_i, _i, _i, _p, _p, _p, _p],
     "pc_lowrank_exp_sum_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz,
                                _p],
 }

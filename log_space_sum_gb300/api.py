@@ -264,6 +264,25 @@ def lowrank_exp_sum_bwd(theta, A, Bm, x, out, logZ, f, precision="auto", grads=T
     return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=W)
 
 
+# -------------------------------------------------------------------- EM M-step
+def em_normalize(F: torch.Tensor, theta: torch.Tensor, W: torch.Tensor | None = None) -> torch.Tensor:
+    """EM M-step (pc_em_normalize), in place on ``theta`` (shape [..., N], rows = nodes):
+    theta = normalize(F) over the last axis, or with ``W`` the LowRank conditional update
+    normalize(F / W) (0 where W <= 0). A row whose statistic sums to 0 keeps theta."""
+    _check(F, "F")
+    _check(theta, "theta", device=F.device)
+    if W is not None:
+        _check(W, "W", device=F.device)
+    if F.shape != theta.shape or (W is not None and W.shape != F.shape):
+        raise ValueError(f"F {tuple(F.shape)}, theta {tuple(theta.shape)} and W must have one shape")
+    if F.dim() < 1 or F.numel() == 0:
+        raise ValueError("F must have at least one element")
+    Nn = F.shape[-1]
+    rows = F.numel() // Nn
+    N.call("pc_em_normalize", 1, rows, Nn, _ptr(F), _ptr(W), _ptr(theta), _stream(F.device))
+    return theta
+
+
 # -------------------------------------------------------------------- diagnostics
 def device_status(device=None) -> None:
     """Synchronises the current stream and raises PCError if a kernel gave up a bounded wait."""

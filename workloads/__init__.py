@@ -161,3 +161,20 @@ def lowrank_inputs(M: int, N: int, K: int, B: int, spread: float, seed: int,
 
 def lowrank(spread: float = 1.0):
     return lowrank_inputs(1024, 1024, 16, 64, spread, seed=SPREAD_SEEDS[spread])
+
+
+# ------------------------------------------------------------------- EM M-step
+def em_statistics(seed: int = 10):
+    """Synthetic parameter statistics of the M-step at the HMM 4096 x 32 workload's
+    parameter shapes (initial dpi [1, 4096], transitions dA [4096, 4096], emissions
+    dE [4096, 1024]) and of the LowRank 1024 x 1024 layer (F+ and W): flows drawn
+    Gamma(0.5, 1) (many small entries, a few large ones, as expected counts are), W
+    drawn Gamma(2, 1), and previous parameters uniform in [0, 1)."""
+    rng = np.random.default_rng(seed)
+    shapes = {"pi": (1, 4096), "A": (4096, 4096), "E": (4096, 1024), "lowrank": (1024, 1024)}
+    out = {}
+    for k, shp in shapes.items():
+        out["F_" + k] = rng.gamma(0.5, 1.0, size=shp).astype(np.float32)
+        out["theta_" + k] = rng.random(shp).astype(np.float32)
+    out["W_lowrank"] = rng.gamma(2.0, 1.0, size=shapes["lowrank"]).astype(np.float32)
+    return out
