@@ -7,8 +7,10 @@
 // update normalize(theta * F+ / F-) with F- = theta * W. A row whose r sums to zero or to
 // a non-finite value keeps its parameters.
 //
-// Memory-bound: one CTA per row reads F (and W) once from DRAM, sums r, then reads the
-// row again (now in L1/L2) and writes theta once: 8 (12 with W) bytes per parameter.
+// Memory-bound: one CTA per row reads F (and W) once and writes theta once, 8 (12 with
+// W) bytes per parameter. Rows of up to 8192 aligned values are held in registers
+// (every load of a thread issued before the first use); longer or unaligned rows are
+// summed in a first pass and re-read (from L1/L2) in a second.
 #include "pc_device.cuh"
 #include "pc_host.h"
 
@@ -73,9 +75,56 @@ __global__ void __launch_bounds__(kEmThreads) k_em_normalize(int N, const float*
   }
 }
 
+// Register-resident rows: N % 4 == 0, 16-byte aligned, N <= 4 * kItems * kEmThreads.
+template <bool kRatio, int kItems>
+__global__ void __launch_bounds__(kEmThreads) k_em_normalize_reg(int N, const float* __restrict__ F,
+                                                                 const float* __restrict__ W,
+                                                                 float* __restrict__ theta) {
+  __shared__ float red[kEmThreads / 32];
+  const long long row0 = static_cast<long long>(blockIdx.x) * N;
+  const float4* f = reinterpret_cast<const float4*>(F + row0);
+  const float4* w = kRatio ? reinterpret_cast<const float4*>(W + row0) : nullptr;
+  const int n4 = N >> 2;
+  float4 r[kItems];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int i = threadIdx.x + k * kEmThreads;
+    r[k] = i < n4 ? f[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if constexpr (kRatio) {
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int i = threadIdx.x + k * kEmThreads;
+      const float4 b = i < n4 ? w[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      r[k] = make_float4(em_ratio(r[k].x, b.x), em_ratio(r[k].y, b.y), em_ratio(r[k].z, b.z), em_ratio(r[k].w, b.w));
+    }
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) acc += (r[k].x + r[k].y) + (r[k].z + r[k].w);
+  const float s = block_sum(acc, red);
+  if (!(s > 0.f) || !isfinite(s)) return;  // no flow reached the node: it keeps theta
+  const float inv = 1.f / s;                // r * (1 / s): within 1.5 ulp of r / s
+  float4* th = reinterpret_cast<float4*>(theta + row0);
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int i = threadIdx.x + k * kEmThreads;
+    if (i < n4) th[i] = make_float4(r[k].x * inv, r[k].y * inv, r[k].z * inv, r[k].w * inv);
+  }
+}
+
 template <bool kRatio>
 void launch_em(int rows, int N, const float* F, const float* W, float* theta, bool vec, cudaStream_t s) {
-  if (vec)
+  const int items = vec ? (N / 4 + kEmThreads - 1) / kEmThreads : 0;
+  if (vec && items <= 1)
+    k_em_normalize_reg<kRatio, 1><<<rows, kEmThreads, 0, s>>>(N, F, W, theta);
+  else if (vec && items <= 2)
+    k_em_normalize_reg<kRatio, 2><<<rows, kEmThreads, 0, s>>>(N, F, W, theta);
+  else if (vec && items <= 4)
+    k_em_normalize_reg<kRatio, 4><<<rows, kEmThreads, 0, s>>>(N, F, W, theta);
+  else if (vec && items <= 8)
+    k_em_normalize_reg<kRatio, 8><<<rows, kEmThreads, 0, s>>>(N, F, W, theta);
+  else if (vec)
     k_em_normalize<kRatio, true><<<rows, kEmThreads, 0, s>>>(N, F, W, theta);
   else
     k_em_normalize<kRatio, false><<<rows, kEmThreads, 0, s>>>(N, F, W, theta);
