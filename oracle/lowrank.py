@@ -103,3 +103,88 @@ def lowrank_exp_sum_bwd(theta, A, Bm, x, f):
         Fplus += fb * p
         Wst += fb * g / Z[:, None]
     return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=Wst, out=out, logZ=logZ, absdA=absdA, absdB=absdB)
+
+
+# ----------------------------------------------------------------- "sum_exp" form
+# pyjuice LowRank API doc (intro formulas): the second form of the scale,
+#     g_b[i,j] = sum_r exp(A_b[i,r]) exp(B_b[r,j])          ("sum_exp": a mixture of
+# k rank-one scales), with Z_b and theta_b as above. The layer, its flows and the
+# Z-correction statistic are the same functions of theta_b and g_b as for "exp_sum";
+# only the chain rule into the factors differs: with D = f (p - q) as above,
+#     d(sum f out)/d g_b[i,j] = D[i,j] / g_b[i,j]
+#     dA_b[i,r] = exp(A_b[i,r]) sum_j (D / g)[i,j] exp(B_b[r,j])
+#     dB_b[r,j] = exp(B_b[r,j]) sum_i exp(A_b[i,r]) (D / g)[i,j].
+# Each row of A_b is shifted by its maximum and each row of B_b by its maximum before the
+# exponentials (the shift of a row of A scales g's row and cancels in theta_b; the shift
+# of a row r of B is folded into column r of A), so float64 holds every term.
+
+
+def _per_sample_sum_exp(theta, A, Bm, x, b):
+    beta = Bm[b].max(axis=1)                                 # [K]
+    c = np.exp(Bm[b] - beta[:, None])                        # exp(B) / exp(beta_r)
+    Ab = A[b] + beta[None, :]
+    alpha = Ab.max(axis=1)                                   # [M]
+    a = np.exp(Ab - alpha[:, None])                          # exp(A) exp(beta) / exp(alpha_i)
+    g = a @ c                                                # g_b / exp(alpha_i)
+    tg = theta * g
+    Z = tg.sum(axis=1)
+    m = x[:, b].max()
+    u = np.exp(x[:, b] - m)
+    num = tg @ u
+    with np.errstate(divide="ignore"):
+        out = m + np.log(num) - np.log(Z)
+        logZ = np.log(Z) + alpha
+    return a, c, g, Z, u, out, logZ
+
+
+def lowrank_sum_exp_fwd(theta, A, Bm, x):
+    """Returns out [M,B] and logZ [B,M] of the "sum_exp" form."""
+    theta, A, Bm, x = (np.asarray(v, dtype=np.float64) for v in (theta, A, Bm, x))
+    M, N = theta.shape
+    B = x.shape[1]
+    out = np.empty((M, B))
+    logZ = np.empty((B, M))
+    for b in range(B):
+        _, _, _, _, _, o, lz = _per_sample_sum_exp(theta, A, Bm, x, b)
+        out[:, b] = o
+        logZ[b] = lz
+    return out, logZ
+
+
+def lowrank_sum_exp_bwd(theta, A, Bm, x, f):
+    """Returns dA [B,M,K], dB [B,K,N], e [N,B], Fplus [M,N], W [M,N], out, logZ of the
+    "sum_exp" form, and absdA, absdB: the sums of the absolute terms behind each gradient
+    entry before cancellation (as for "exp_sum")."""
+    theta, A, Bm, x, f = (np.asarray(v, dtype=np.float64) for v in (theta, A, Bm, x, f))
+    M, N = theta.shape
+    B = x.shape[1]
+    K = A.shape[2]
+    dA = np.empty((B, M, K))
+    dB = np.empty((B, K, N))
+    absdA = np.empty((B, M, K))
+    absdB = np.empty((B, K, N))
+    e = np.empty((N, B))
+    Fplus = np.zeros((M, N))
+    Wst = np.zeros((M, N))
+    out = np.empty((M, B))
+    logZ = np.empty((B, M))
+    for b in range(B):
+        a, c, g, Z, u, o, lz = _per_sample_sum_exp(theta, A, Bm, x, b)
+        out[:, b] = o
+        logZ[b] = lz
+        q = theta * g / Z[:, None]
+        p = q * np.exp(x[:, b][None, :] - o[:, None])
+        fb = f[:, b][:, None]
+        D = fb * (p - q)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            R = np.where(g > 0, D / np.where(g > 0, g, 1.0), 0.0)        # d/dg (up to exp(alpha_i))
+            Rabs = np.where(g > 0, np.abs(fb) * (p + q) / np.where(g > 0, g, 1.0), 0.0)
+        # the exp(alpha_i) of g's row cancels against the same factor of a_ir c_rj
+        dA[b] = a * (R @ c.T)
+        dB[b] = c * (a.T @ R)
+        absdA[b] = a * (Rabs @ c.T)
+        absdB[b] = c * (a.T @ Rabs)
+        e[:, b] = (fb * p).sum(axis=0)
+        Fplus += fb * p
+        Wst += fb * g / Z[:, None]
+    return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=Wst, out=out, logZ=logZ, absdA=absdA, absdB=absdB)
