@@ -12,11 +12,12 @@ Workloads (synthetic, seeded; see workloads/):
   hclt     HCLT, 768 variables, 1024 latents, 512 categories, batch 512: pc_hclt_fwd_bwd.
   lowrank  LowRank exp_sum layer M = N = 1024, rank 16, batch 64, scale spread 1 nat:
            pc_lowrank_exp_sum_fwd + _bwd (dA, dB, e, F+, W).
+  lowrank_sum_exp  the same factors in the LowRank sum_exp form (pc_lowrank_sum_exp_*).
   mstep    the EM M-step (pc_em_normalize) of the HMM 4096x32 parameters (dpi, dA, dE)
            and of the LowRank 1024x1024 layer (normalize F+ / W); unit: nodes/s.
 
 python bench.py [--gpus N --steps K --warmup W --precision auto|tf32|fp32
-                 --impl ours|reference --workload hmm|hmm1024|layer|hclt|lowrank|mstep]
+                 --impl ours|reference --workload hmm|hmm1024|layer|hclt|lowrank|lowrank_sum_exp|mstep]
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own batch (weak
 scaling; no data-path collective). Between timed steps a 256 MiB buffer is written to
@@ -68,7 +69,8 @@ def parse():
     ap.add_argument("--precision", default="auto", choices=["auto", "tf32", "fp32"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="hmm", choices=["hmm", "hmm1024", "layer", "hclt", "lowrank", "mstep"])
+    ap.add_argument("--workload", default="hmm",
+                    choices=["hmm", "hmm1024", "layer", "hclt", "lowrank", "lowrank_sum_exp", "mstep"])
     ap.add_argument("--hclt-nvars", type=int, default=768,
                     help="HCLT variables (768 = the workload; fewer for a profiler-sized case)")
     return ap.parse_args()
@@ -288,6 +290,48 @@ class LowRankWorkload(Workload):
         return step, e2e, (hA.numel() + hB.numel()) * 4, h_out.numel() * 4
 
 
+class LowRankSumExpWorkload(LowRankWorkload):
+    """The second form of the LowRank scale, g_b = sum_r exp(A_b[:, r]) exp(B_b[r, :]), on
+    the same factors: every pass is tensor-core contractions over the (sample, rank)
+    virtual batch, so the roofline is the tensor pipe's."""
+    name = "lowrank_sum_exp"
+    metric = "LowRank sum_exp 1024x1024 rank 16 fwd+bwd samples/s @batch 64 (1 GB300); % tensor roofline"
+    desc = ("LowRank sum_exp layer M = N = 1024, rank 16, batch 64 (the exp_sum workload's factors): forward "
+            "out, logZ + backward dA, dB, e, F+, W")
+    roofline_bound = "tensor"
+
+    def oracle(self, d, b):
+        from oracle.lowrank import lowrank_sum_exp_bwd
+        lowrank_sum_exp_bwd(d["theta"], d["A"][:b], d["Bm"][:b], d["x"][:, :b], d["f"][:, :b])
+
+    def device(self, pc, d, dev, prec):
+        import torch
+        t = {k: torch.from_numpy(d[k]).to(dev) for k in ("theta", "A", "Bm", "x", "f")}
+        M, N = d["theta"].shape
+        Bs, _, K = d["A"].shape
+        out = torch.empty(M, Bs, device=dev)
+        logZ = torch.empty(Bs, M, device=dev)
+        g = dict(dA=torch.empty(Bs, M, K, device=dev), dB=torch.empty(Bs, K, N, device=dev),
+                 e=torch.empty(N, Bs, device=dev), Fplus=torch.empty(M, N, device=dev), W=torch.empty(M, N, device=dev))
+
+        def step(A=None, Bm=None):
+            A = t["A"] if A is None else A
+            Bm = t["Bm"] if Bm is None else Bm
+            pc.lowrank_sum_exp_fwd(t["theta"], A, Bm, t["x"], precision=prec, out=out, logZ=logZ)
+            pc.lowrank_sum_exp_bwd(t["theta"], A, Bm, t["x"], t["f"], precision=prec, **g)
+        hA = torch.from_numpy(d["A"]).pin_memory()
+        hB = torch.from_numpy(d["Bm"]).pin_memory()
+        h_out = torch.empty(M, Bs).pin_memory()
+        dA_in, dB_in = torch.empty_like(t["A"]), torch.empty_like(t["Bm"])
+
+        def e2e():
+            dA_in.copy_(hA, non_blocking=True)
+            dB_in.copy_(hB, non_blocking=True)
+            step(dA_in, dB_in)
+            h_out.copy_(out, non_blocking=True)
+        return step, e2e, (hA.numel() + hB.numel()) * 4, h_out.numel() * 4
+
+
 class MstepWorkload(Workload):
     """The EM M-step after a backward: every node's parameters normalized over its
     children (plain, for the HMM's dpi, dA, dE) or the LowRank conditional update
@@ -349,7 +393,7 @@ class MstepWorkload(Workload):
 
 
 WORKLOADS = {w.name: w for w in (HmmWorkload(), Hmm1024Workload(), LayerWorkload(), HcltWorkload(), LowRankWorkload(),
-                                 MstepWorkload())}
+                                 LowRankSumExpWorkload(), MstepWorkload())}
 
 
 # ------------------------------------------------------------------ CPU oracle

@@ -253,6 +253,40 @@ PCSUM_API pc_status_t pc_lowrank_exp_sum_bwd(int M, int N, int K, int B, const f
                                              float* Wstat, int accumulate, pc_precision_t prec,
                                              void* ws, size_t ws_bytes, pc_stream_t stream);
 
+/* ------------------------------------------------------------------------------
+ * LowRank "sum_exp" per-sample scale (pyjuice LowRank API doc: intro formulas, the second
+ * form of the scale; Note: "sum_exp" through the plain sum-layer kernels on a virtual
+ * batch). Per sample b
+ *   g_b[i,j] = sum_r exp(A_b[i,r]) exp(B_b[r,j]),  Z_b[i] = sum_j theta[i,j] g_b[i,j],
+ *   theta_b = theta g_b / Z_b,                     out[i,b] = log sum_j theta_b[i,j] exp(x[j,b]).
+ * Arguments, layouts and outputs as for "exp_sum" above (theta [M][N], A [B][M][K],
+ * Bm [B][K][N], x [N][B], out [M][B], logZ [B][M]; backward for node flows f [M][B]: dA,
+ * dB = the gradients of sum f out, e, Fplus, Wstat, each optional, accumulate adds). The
+ * backward recomputes what it needs from the forward's inputs (it takes no out or logZ).
+ * Every pass runs as dense tensor-core contractions over the virtual batch of the B*K
+ * (sample, rank) pairs with the exponentials and rank reductions in element-wise kernels;
+ * row maxima of A, B and x are taken out of every exponential (they cancel), so any
+ * finite factors are in range. Precision: every contraction's products in the mode's
+ * format (bf16 / TF32 / 3xTF32), float32 accumulation.
+ * Limits: K >= 1, B <= 65535, B*K <= 2^22, M, N <= 2^24 (PC_ERR_SHAPE). M, N or B may
+ * be 0. Workspace: pc_lowrank_sum_exp_workspace(..., with_backward, ...) bytes, 16-byte
+ * aligned.
+ * ---------------------------------------------------------------------------- */
+PCSUM_API pc_status_t pc_lowrank_sum_exp_workspace(int M, int N, int K, int B, int with_backward,
+                                                   pc_precision_t prec, size_t* bytes);
+
+PCSUM_API pc_status_t pc_lowrank_sum_exp_fwd(int M, int N, int K, int B, const float* theta,
+                                             const float* A, const float* Bm, const float* x,
+                                             float* out, float* logZ, pc_precision_t prec,
+                                             void* ws, size_t ws_bytes, pc_stream_t stream);
+
+PCSUM_API pc_status_t pc_lowrank_sum_exp_bwd(int M, int N, int K, int B, const float* theta,
+                                             const float* A, const float* Bm, const float* x,
+                                             const float* f, float* dA, float* dB, float* e,
+                                             float* Fplus, float* Wstat, int accumulate,
+                                             pc_precision_t prec, void* ws, size_t ws_bytes,
+                                             pc_stream_t stream);
+
 /* ---------------------------------------------------------------- EM M-step
  * The M-step that follows the backward (pyjuice LowRank API doc, Training): for each of
  * the G*M nodes (rows), over its N children,

@@ -14,6 +14,8 @@ from .api import (  # noqa: F401
     hmm_fwd_bwd,
     lowrank_exp_sum_bwd,
     lowrank_exp_sum_fwd,
+    lowrank_sum_exp_bwd,
+    lowrank_sum_exp_fwd,
     precision_code,
     profile_start,
     profile_stop,

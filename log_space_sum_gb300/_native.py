@@ -45,6 +45,9 @@ SIGNATURES = {
     "pc_hclt_workspace": [_i, _i, _i, _i, _i, _p],
     "pc_hclt_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
     "pc_lowrank_exp_sum_workspace": [_i, _i, _i, _i, _i, _i, _p],
+    "pc_lowrank_sum_exp_workspace": [_i, _i, _i, _i, _i, _i, _p],
+    "pc_lowrank_sum_exp_fwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p],
+    "pc_lowrank_sum_exp_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
     "pc_lowrank_exp_sum_fwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p],
     "pc_em_normalize": [_i, _i, _i, _p, _p, _p, _p],
     "pc_lowrank_exp_sum_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz,

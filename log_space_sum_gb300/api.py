@@ -264,6 +264,48 @@ def lowrank_exp_sum_bwd(theta, A, Bm, x, out, logZ, f, precision="auto", grads=T
     return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=W)
 
 
+def lowrank_sum_exp_fwd(theta, A, Bm, x, precision="auto", out=None, logZ=None, **removed):
+    """LowRank sum_exp layer forward (pc_lowrank_sum_exp_fwd), the scale g_b = exp(A_b)
+    exp(B_b) summed over the rank: returns out [M,B] and logZ [B,M] = log Z_b[i]."""
+    _removed_flags(removed, "lowrank_sum_exp_fwd")
+    prec = precision_code(precision)
+    dev, M, Nn, K, Bs = _lowrank_shapes(theta, A, Bm, x)
+    out = torch.empty(M, Bs, dtype=torch.float32, device=dev) if out is None else out
+    logZ = torch.empty(Bs, M, dtype=torch.float32, device=dev) if logZ is None else logZ
+    _check(out, "out", device=dev)
+    _check(logZ, "logZ", device=dev)
+    nb = _query("pc_lowrank_sum_exp_workspace", M, Nn, K, Bs, 0, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_lowrank_sum_exp_fwd", M, Nn, K, Bs, _ptr(theta), _ptr(A), _ptr(Bm), _ptr(x), _ptr(out), _ptr(logZ),
+           prec, _ptr(ws), ws.numel(), _stream(dev))
+    return out, logZ
+
+
+def lowrank_sum_exp_bwd(theta, A, Bm, x, f, precision="auto", grads=True, element_flows=True, param_flows=True,
+                        z_correction=True, dA=None, dB=None, e=None, Fplus=None, W=None, accumulate=False,
+                        **removed):
+    """LowRank sum_exp layer backward (pc_lowrank_sum_exp_bwd): the same outputs as
+    lowrank_exp_sum_bwd (dA, dB, e, Fplus, W; what is switched off is None)."""
+    _removed_flags(removed, "lowrank_sum_exp_bwd")
+    prec = precision_code(precision)
+    dev, M, Nn, K, Bs = _lowrank_shapes(theta, A, Bm, x)
+    _check(f, "f", device=dev)
+    new = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)  # noqa: E731
+    dA = (new(Bs, M, K) if dA is None else dA) if grads else None
+    dB = (new(Bs, K, Nn) if dB is None else dB) if grads else None
+    e = (new(Nn, Bs) if e is None else e) if element_flows else None
+    Fplus = (new(M, Nn) if Fplus is None else Fplus) if param_flows else None
+    W = (new(M, Nn) if W is None else W) if z_correction else None
+    for t, n in ((dA, "dA"), (dB, "dB"), (e, "e"), (Fplus, "Fplus"), (W, "W")):
+        if t is not None:
+            _check(t, n, device=dev)
+    nb = _query("pc_lowrank_sum_exp_workspace", M, Nn, K, Bs, 1, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_lowrank_sum_exp_bwd", M, Nn, K, Bs, _ptr(theta), _ptr(A), _ptr(Bm), _ptr(x), _ptr(f), _ptr(dA),
+           _ptr(dB), _ptr(e), _ptr(Fplus), _ptr(W), int(bool(accumulate)), prec, _ptr(ws), ws.numel(), _stream(dev))
+    return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=W)
+
+
 # -------------------------------------------------------------------- EM M-step
 def em_normalize(F: torch.Tensor, theta: torch.Tensor, W: torch.Tensor | None = None) -> torch.Tensor:
     """EM M-step (pc_em_normalize), in place on ``theta`` (shape [..., N], rows = nodes):

@@ -301,4 +301,35 @@ struct EpiThetaScale : EpiNoHooks {
   }
 };
 
+// D[i][j] (+)= the accumulator: the contraction's result as a float32 matrix (rows ld
+// apart, M x N valid). Transposed per warp as EpiThetaScale, so that each store of the
+// warp is one contiguous row segment.
+struct EpiStoreF32 : EpiNoHooks {
+  static constexpr bool kTranspose = true;
+  struct Params {
+    float* D;
+    long long ld;
+    int M, N, accumulate;
+  };
+  __device__ static void apply(const Params& p, int, int m0, int n0, int row, int col0, float (&v)[32], uint8_t*,
+                               float* tbuf) {
+    float w[32];
+    warp_transpose32(v, w, tbuf);
+    const int lane = threadIdx.x & 31;
+    const int i0 = m0 + row - lane;
+    const int j = n0 + col0 + lane;
+    if (j >= p.N) return;
+    float* Dp = p.D + static_cast<long long>(i0) * p.ld + j;
+#pragma unroll
+    for (int h = 0; h < 32; h += 16) {
+      float f[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) f[r] = (i0 + h + r < p.M && p.accumulate) ? Dp[(h + r) * p.ld] : 0.f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (i0 + h + r < p.M) Dp[(h + r) * p.ld] = f[r] + w[h + r];
+    }
+  }
+};
+
 }  // namespace pc
