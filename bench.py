@@ -514,10 +514,8 @@ def recorded_traffic(kind: str, precision: str, workload: str):
         return None
     with open(p) as fh:
         d = json.load(fh)
-    ent = d.get(f"{kind}:{precision}")
-    if not ent or ent.get("workload", "hmm" if kind.startswith("hmm") else kind.split("_")[0]) != workload:
-        return None
-    if ent.get("source_hash") != kernel_source_hash():
+    ent = d.get(f"{workload}/{kind}:{precision}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
     return ent.get("dram_bytes_per_launch")
 
