@@ -499,16 +499,18 @@ struct EpiHcltFwd : EpiNoHooks {
 };
 
 // Element-flow epilogue: f[g][b][z'] = u[g][b][z'] * D[z', b]; thread = child latent z'.
-// The u block is staged in shared memory during the K loop (not in 3xTF32, whose ring
-// needs the room).
-template <int P>
+// For 128-wide tiles the u block is staged in shared memory during the K loop (not in
+// 3xTF32, whose ring needs the room); 256-wide tiles read it directly (a 128 KB block
+// would leave the ring two slots).
+struct HcltElemParams {
+  const float* U32;  // at the level's first slot, [G][B][H]
+  float* F32;        // idem
+  int H, B;
+};
+template <int P, int BN = kHcltBN>
 struct EpiHcltElem : EpiNoHooks {
-  struct Params {
-    const float* U32;  // at the level's first slot, [G][B][H]
-    float* F32;        // idem
-    int H, B;
-  };
-  static constexpr bool kStage = P != kTF32x3;
+  using Params = HcltElemParams;
+  static constexpr bool kStage = P != kTF32x3 && BN == kHcltBN;
   static constexpr int kSmemBytes = kStage ? kHcltBN * kBM * 4 : 0;
 
   __device__ static void prepare(const Params& p, int g, int m0, int n0, int et, uint8_t* smem) {
@@ -740,16 +742,26 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
           sA, H, B, d_pslot, w.F32, w.D, w.Gbm.ptr, w.Gbm.ld, w.Gbm.lo_elems, w.Gnm.ptr, w.Gnm.ld,
           w.Gnm.lo_elems);
       PC_LAUNCH_CHECK();
-      // element flows of the level's children
+      // element flows of the level's children; 256-wide tiles (full-rate MMAs) where the
+      // level has enough of them to fill the GPU
       if ((st = encode_maps(&ma, operand_view(w.WopT, prec, sA, G), prec, kBM)) != PC_OK) return st;
-      if ((st = encode_maps(&mb, operand_view(w.Gbm, prec, 0, G), prec, kHcltBN)) != PC_OK) return st;
-      typename EpiHcltElem<P>::Params ee{w.U32 + static_cast<long long>(sA) * B * H,
-                                         w.F32 + static_cast<long long>(sA) * B * H, H, B};
+      const bool wide = P == kBF16 && static_cast<long long>(cdiv(H, kBM)) * cdiv(B, 2 * kHcltBN) * G >= 148;
+      const int ebn = wide ? 2 * kHcltBN : kHcltBN;
+      if ((st = encode_maps(&mb, operand_view(w.Gbm, prec, 0, G), prec, ebn)) != PC_OK) return st;
+      HcltElemParams ee{w.U32 + static_cast<long long>(sA) * B * H, w.F32 + static_cast<long long>(sA) * B * H, H,
+                        B};
       // a_early: Wᵀ's operand copy was written before the first scaled-flow kernel
-      if ((st = launch_gemm<P, kHcltBN, EpiHcltElem<P>>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo,
-                                                        mb.hi, mb.lo, num_k_blocks(H, prec), ee, s,
-                                                        PC_KIND_HCLT_ELEM, 2ll * G * H * H * B, true)) != PC_OK)
-        return st;
+      if constexpr (P == kBF16) {
+        if (wide)
+          st = launch_gemm<P, 2 * kHcltBN, EpiHcltElem<P, 2 * kHcltBN>>(
+              dim3(cdiv(H, kBM), cdiv(B, 2 * kHcltBN), G), ma.hi, ma.lo, mb.hi, mb.lo, num_k_blocks(H, prec), ee, s,
+              PC_KIND_HCLT_ELEM, 2ll * G * H * H * B, true);
+      }
+      if (!wide)
+        st = launch_gemm<P, kHcltBN, EpiHcltElem<P>>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi,
+                                                     mb.lo, num_k_blocks(H, prec), ee, s, PC_KIND_HCLT_ELEM,
+                                                     2ll * G * H * H * B, true);
+      if (st != PC_OK) return st;
       if (!dW) continue;
       // parameter flows of the level's edges
       if ((st = transpose_to_operand<P>(w.U32 + static_cast<long long>(sA) * B * H, H,

@@ -22,9 +22,19 @@
 // TMEM and returns.
 #pragma once
 
+#include <type_traits>
+
 #include "pc_device.cuh"
 
 namespace pc {
+
+// Epi::kPrefetchTile (optional, default false): after the K loop the epilogue fetches a
+// per-tile input into the idle ring (Epi::prefetch<BN>) and applies from there
+// (Epi::apply_prefetched<BN>).
+template <class E, class = void>
+struct EpiPrefetch : std::false_type {};
+template <class E>
+struct EpiPrefetch<E, std::void_t<decltype(E::kPrefetchTile)>> : std::bool_constant<E::kPrefetchTile> {};
 
 // Warp 0: TMA producer; warp 1: MMA issuer; warps 2 .. 9: epilogue, two warps per TMEM
 // lane quarter, each taking every other 32-column chunk of the tile.
@@ -508,12 +518,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             Epi::apply_staged(ep, g, m0, n0_epi, row, c, v, epi_smem, smem + kXchgBytes);
           }
         }
-      } else if (ok) {
+      } else {
+        constexpr bool kPre = EpiPrefetch<Epi>::value;
+        if constexpr (kPre) {
+          static_assert(kStages * S::kStageBytes >= static_cast<uint32_t>(kBM) * BN * 4, "the ring holds the tile");
+          ok = epilogue_bar_and(ok);  // every epilogue thread takes the same branch
+          if (ok) {
+            Epi::template prefetch<BN>(ep, g, m0, n0_epi, et, smem);  // the MMAs are done: the ring is idle
+            cp_async_wait_all();
+          }
+          epilogue_bar_sync();
+        }
+        if (ok) {
 #pragma unroll 1
-        for (int c = half * 32; c < BN; c += 64) {
-          float v[32];
-          tmem_ld_32x32(lane_base + static_cast<uint32_t>(c), v);
-          Epi::apply(ep, g, m0, n0_epi, row, c, v, epi_smem, tbuf);
+          for (int c = half * 32; c < BN; c += 64) {
+            float v[32];
+            tmem_ld_32x32(lane_base + static_cast<uint32_t>(c), v);
+            if constexpr (kPre)
+              Epi::template apply_prefetched<BN>(ep, g, m0, n0_epi, row, c, v, smem, tbuf);
+            else
+              Epi::apply(ep, g, m0, n0_epi, row, c, v, epi_smem, tbuf);
+          }
         }
       }
     }

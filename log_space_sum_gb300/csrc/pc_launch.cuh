@@ -263,6 +263,10 @@ inline pc_status_t transpose_f32(const float* src, long long src_ld, long long s
 // Shared with the circuits: F[g][i][j] (+)= theta[g][i][j] * D[i,j].
 struct EpiThetaScale : EpiNoHooks {
   static constexpr bool kTranspose = true;
+  // Unsliced contractions fetch the tile's theta block into the idle ring with
+  // asynchronous copies (32 in flight per thread) once the MMAs are done, instead of 16
+  // dependent-free global loads at a time per thread in apply.
+  static constexpr bool kPrefetchTile = true;
   struct Params {
     float* F;
     const float* theta;
@@ -297,6 +301,59 @@ struct EpiThetaScale : EpiNoHooks {
 #pragma unroll
       for (int r = 0; r < 16; ++r)
         if (i0 + h + r < p.M) Fp[(h + r) * ld] = f[r] + t[r] * w[h + r];
+    }
+  }
+
+  // theta block [kBM][BN] of the tile, float32 row-major in `stage` (0 outside theta).
+  template <int BN>
+  __device__ static void prefetch(const Params& p, int g, int m0, int n0, int et, uint8_t* stage) {
+    constexpr int kPieces = BN / 4;  // 16-byte pieces of a tile row
+    const long long gm = p.gmap ? p.gmap[g] : g;
+    const float* src = p.theta + (gm * p.M + m0) * static_cast<long long>(p.N) + n0;
+    const int nrows = min(kBM, p.M - m0), ncols = min(BN, p.N - n0);
+#pragma unroll 4
+    for (int i = et; i < kBM * kPieces; i += kEpiThreads) {
+      const int r = i / kPieces, c0 = (i % kPieces) * 4;
+      uint8_t* dst = stage + (static_cast<long long>(r) * BN + c0) * 4;
+      const int n = (r < nrows && c0 < ncols) ? min(4, ncols - c0) : 0;
+      if (n == 0) {
+        *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+        continue;
+      }
+      const float* gp = src + static_cast<long long>(r) * p.N + c0;
+      if ((reinterpret_cast<uintptr_t>(gp) & 15) == 0) {
+        cp_async_16(dst, gp, static_cast<uint32_t>(n * 4));  // zero-fills beyond n values
+      } else {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (k < n) x[k] = gp[k];
+        *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+      }
+    }
+  }
+
+  template <int BN>
+  __device__ static void apply_prefetched(const Params& p, int g, int m0, int n0, int row, int col0,
+                                          float (&v)[32], const uint8_t* stage, float* tbuf) {
+    float w[32];
+    warp_transpose32(v, w, tbuf);
+    const int lane = threadIdx.x & 31;
+    const int i0 = m0 + row - lane;  // the warp's first row
+    const int j = n0 + col0 + lane;
+    if (j >= p.N) return;
+    const long long ld = p.N;
+    const long long gm = p.gmap ? p.gmap[g] : g;
+    const float* ts = reinterpret_cast<const float*>(stage) + static_cast<long long>(i0 - m0) * BN + col0 + lane;
+    float* Fp = p.F + (gm * p.M + i0) * ld + j;
+#pragma unroll
+    for (int h = 0; h < 32; h += 16) {
+      float f[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) f[r] = (i0 + h + r < p.M && p.accumulate) ? Fp[(h + r) * ld] : 0.f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (i0 + h + r < p.M) Fp[(h + r) * ld] = f[r] + ts[(h + r) * BN] * w[h + r];
     }
   }
 };
