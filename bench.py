@@ -13,11 +13,12 @@ Workloads (synthetic, seeded; see workloads/):
   lowrank  LowRank exp_sum layer M = N = 1024, rank 16, batch 64, scale spread 1 nat:
            pc_lowrank_exp_sum_fwd + _bwd (dA, dB, e, F+, W).
   lowrank_sum_exp  the same factors in the LowRank sum_exp form (pc_lowrank_sum_exp_*).
+  hmm_lowrank  HMM 1024x64, batch 64, with LowRank rank-16 transitions (pc_hmm_lowrank_fwd_bwd).
   mstep    the EM M-step (pc_em_normalize) of the HMM 4096x32 parameters (dpi, dA, dE)
            and of the LowRank 1024x1024 layer (normalize F+ / W); unit: nodes/s.
 
 python bench.py [--gpus N --steps K --warmup W --precision auto|tf32|fp32
-                 --impl ours|reference --workload hmm|hmm1024|layer|hclt|lowrank|lowrank_sum_exp|mstep]
+                 --impl ours|reference --workload hmm|hmm1024|layer|hclt|lowrank|lowrank_sum_exp|hmm_lowrank|mstep]
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own batch (weak
 scaling; no data-path collective). Between timed steps a 256 MiB buffer is written to
@@ -70,7 +71,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="hmm",
-                    choices=["hmm", "hmm1024", "layer", "hclt", "lowrank", "lowrank_sum_exp", "mstep"])
+                    choices=["hmm", "hmm1024", "layer", "hclt", "lowrank", "lowrank_sum_exp", "hmm_lowrank", "mstep"])
     ap.add_argument("--hclt-nvars", type=int, default=768,
                     help="HCLT variables (768 = the workload; fewer for a profiler-sized case)")
     return ap.parse_args()
@@ -156,6 +157,50 @@ class Hmm1024Workload(HmmWorkload):
     def inputs(self):
         from workloads import hmm_1024x64
         return hmm_1024x64()
+
+
+class HmmLowRankWorkload(Workload):
+    """An HMM whose 63 transition copies each carry the LowRank exp_sum scale with their own
+    per-sample factors: every transition layer is the fused exp_sum layer."""
+    name, batch = "hmm_lowrank", 64
+    metric = "HMM 1024x64 with LowRank rank-16 transitions fwd+bwd samples/s @batch 64 (1 GB300)"
+    desc = ("HMM 1024 latents x 64 positions, vocab 1024, batch 64, LowRank exp_sum rank 16 (spread 1 nat) on each "
+            "transition copy: forward LL + backward dpi, dA (F+), W, dE and the factor gradients")
+    data = "synthetic (seeded: softmax N(0,1) rows for pi, A, E; uniform tokens; factors N(0, s^2))"
+    roofline_bound = "alu"
+
+    def inputs(self):
+        from workloads import hmm_lowrank
+        return hmm_lowrank()
+
+    def config(self):
+        # M, N, B: the exp unit's work per transition layer (one exp per sample, node, child)
+        return {"H": 1024, "T": 64, "V": 1024, "B": 64, "K": 16, "spread": 1.0, "M": 1024, "N": 1024}
+
+    def oracle(self, d, b):
+        from oracle.hmm_lowrank import hmm_lowrank_fwd_bwd
+        hmm_lowrank_fwd_bwd(d["pi"], d["A"], d["E"], d["tokens"][:b], d["FA"][:, :b], d["FB"][:, :b])
+
+    def device(self, pc, d, dev, prec):
+        import torch
+        t = {k: torch.from_numpy(d[k]).to(dev) for k in ("tokens", "pi", "A", "E", "FA", "FB")}
+        out = pc.hmm_lowrank_fwd_bwd(t["tokens"], t["pi"], t["A"], t["E"], t["FA"], t["FB"], precision=prec)
+        bufs = {k: v for k, v in out.items()}
+
+        def step(FA=None, FB=None):
+            pc.hmm_lowrank_fwd_bwd(t["tokens"], t["pi"], t["A"], t["E"], t["FA"] if FA is None else FA,
+                                   t["FB"] if FB is None else FB, precision=prec, **bufs)
+        hA = torch.from_numpy(d["FA"]).pin_memory()
+        hB = torch.from_numpy(d["FB"]).pin_memory()
+        h_ll = torch.empty(self.batch, dtype=torch.float64).pin_memory()
+        dA_in, dB_in = torch.empty_like(t["FA"]), torch.empty_like(t["FB"])
+
+        def e2e():
+            dA_in.copy_(hA, non_blocking=True)
+            dB_in.copy_(hB, non_blocking=True)
+            step(dA_in, dB_in)
+            h_ll.copy_(bufs["ll"], non_blocking=True)
+        return step, e2e, (hA.numel() + hB.numel()) * 4, h_ll.numel() * 8
 
 
 class LayerWorkload(Workload):
@@ -393,7 +438,7 @@ class MstepWorkload(Workload):
 
 
 WORKLOADS = {w.name: w for w in (HmmWorkload(), Hmm1024Workload(), LayerWorkload(), HcltWorkload(), LowRankWorkload(),
-                                 LowRankSumExpWorkload(), MstepWorkload())}
+                                 LowRankSumExpWorkload(), HmmLowRankWorkload(), MstepWorkload())}
 
 
 # ------------------------------------------------------------------ CPU oracle

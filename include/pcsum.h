@@ -287,6 +287,36 @@ PCSUM_API pc_status_t pc_lowrank_sum_exp_bwd(int M, int N, int K, int B, const f
                                              pc_precision_t prec, void* ws, size_t ws_bytes,
                                              pc_stream_t stream);
 
+/* ------------------------------------------------------------------------------
+ * HMM circuit with LowRank "exp_sum" transitions (pyjuice LowRank API doc: intro
+ * formulas; Parameters: tie_external off, one pair of factor tensors per copy of the
+ * tied transition node vector). The HMM of pc_hmm_fwd_bwd, except that the transition
+ * layer of position t (t = 0 .. T-2) uses per-sample parameters
+ *   A_b^(t)[k,l] = A[k,l] exp((FA[t][b] FB[t][b])[k,l]) / Z_b^(t)[k]
+ * (Z normalizes each row over its children).
+ *   tokens [B][T] int32, pi [H], A [H][H], E [H][V]      as for pc_hmm_fwd_bwd (device)
+ *   FA [T-1][B][H][K], FB [T-1][B][K][H]                 the copies' factors, K <= 64
+ *   ll [B] (double)                                      per-sample log-likelihood
+ *   dpi [H], dE [H][V]                                   flows as for pc_hmm_fwd_bwd
+ *   dA [H][H] = sum_t F+_t, Wstat [H][H] = sum_t W_t     the tied A's statistics (the
+ *                                                        M-step's F+ and W, F- = A W)
+ *   dFA, dFB (shaped as FA, FB)                          gradients of sum_b ll[b]
+ * Each flow output may be NULL; with accumulate != 0 they are added to. Every transition
+ * layer runs as pc_lowrank_exp_sum_fwd / _bwd (the scale is never stored); the results
+ * are deterministic. Precision as for the LowRank layer. Errors: PC_ERR_SHAPE,
+ * PC_ERR_UNSUPPORTED (K > 64), PC_ERR_NULL, PC_ERR_WORKSPACE, PC_ERR_ALIGNMENT.
+ * Workspace: pc_hmm_lowrank_workspace bytes, 16-byte aligned.
+ * ---------------------------------------------------------------------------- */
+PCSUM_API pc_status_t pc_hmm_lowrank_workspace(int H, int T, int V, int B, int K, pc_precision_t prec,
+                                               size_t* bytes);
+
+PCSUM_API pc_status_t pc_hmm_lowrank_fwd_bwd(int H, int T, int V, int B, int K, const int32_t* tokens,
+                                             const float* pi, const float* A, const float* E,
+                                             const float* FA, const float* FB, double* ll, float* dpi,
+                                             float* dA, float* Wstat, float* dE, float* dFA, float* dFB,
+                                             int accumulate, pc_precision_t prec, void* ws,
+                                             size_t ws_bytes, pc_stream_t stream);
+
 /* ---------------------------------------------------------------- EM M-step
  * The M-step that follows the backward (pyjuice LowRank API doc, Training): for each of
  * the G*M nodes (rows), over its N children,

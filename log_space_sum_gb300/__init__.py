@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     em_normalize,
     hclt_fwd_bwd,
     hmm_fwd_bwd,
+    hmm_lowrank_fwd_bwd,
     lowrank_exp_sum_bwd,
     lowrank_exp_sum_fwd,
     lowrank_sum_exp_bwd,

@@ -165,6 +165,43 @@ def hmm_fwd_bwd(tokens, pi, A, E, precision="auto", flows=True, ll=None, dpi=Non
     return ll, dpi, dA, dE
 
 
+def hmm_lowrank_fwd_bwd(tokens, pi, A, E, FA, FB, precision="auto", flows=True, accumulate=False, ll=None, dpi=None,
+                        dA=None, W=None, dE=None, dFA=None, dFB=None, **removed):
+    """HMM circuit with LowRank exp_sum transitions (pc_hmm_lowrank_fwd_bwd): FA
+    [T-1,B,H,K], FB [T-1,B,K,H] the copies' factors. Returns a dict with ll [B] float64
+    and, when ``flows``, dpi [H], dA [H,H] (sum of the copies' F+), W [H,H] (sum of their
+    Z-correction statistics), dE [H,V], dFA, dFB (gradients of sum ll). Output tensors may
+    be passed in (with ``accumulate`` the flows are added to them)."""
+    _removed_flags(removed, "hmm_lowrank_fwd_bwd")
+    prec = precision_code(precision)
+    _check(A, "A")
+    dev = A.device
+    _check(tokens, "tokens", dtype=torch.int32, device=dev)
+    for t, n in ((pi, "pi"), (E, "E"), (FA, "FA"), (FB, "FB")):
+        _check(t, n, device=dev)
+    B, T = tokens.shape
+    H, V = E.shape
+    K = FA.shape[-1]
+    if tuple(FA.shape) != (max(T - 1, 0), B, H, K) or tuple(FB.shape) != (max(T - 1, 0), B, K, H):
+        raise ValueError(f"FA {tuple(FA.shape)} and FB {tuple(FB.shape)}: expected [T-1,B,H,K] and [T-1,B,K,H]")
+    out = dict(ll=torch.empty(B, dtype=torch.float64, device=dev) if ll is None else ll)
+    _check(out["ll"], "ll", dtype=torch.float64, device=dev)
+    if flows:
+        new = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)  # noqa: E731
+        given = dict(dpi=dpi, dA=dA, W=W, dE=dE, dFA=dFA, dFB=dFB)
+        fresh = dict(dpi=lambda: new(H), dA=lambda: new(H, H), W=lambda: new(H, H), dE=lambda: new(H, V),
+                     dFA=lambda: torch.empty_like(FA), dFB=lambda: torch.empty_like(FB))
+        for k, v in given.items():
+            out[k] = fresh[k]() if v is None else _check(v, k, device=dev)
+    g = lambda k: _ptr(out.get(k))  # noqa: E731
+    nb = _query("pc_hmm_lowrank_workspace", H, T, V, B, K, prec)
+    ws = workspace(nb, dev)
+    N.call("pc_hmm_lowrank_fwd_bwd", H, T, V, B, K, _ptr(tokens), _ptr(pi), _ptr(A), _ptr(E), _ptr(FA), _ptr(FB),
+           g("ll"), g("dpi"), g("dA"), g("W"), g("dE"), g("dFA"), g("dFB"), int(bool(accumulate)), prec, _ptr(ws),
+           ws.numel(), _stream(dev))
+    return out
+
+
 # -------------------------------------------------------------------------- HCLT
 def hclt_fwd_bwd(parent, data, pi, W, E, precision="auto", flows=True, ll=None, dpi=None, dW=None, dE=None,
                  accumulate=False, **removed):

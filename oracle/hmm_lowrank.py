@@ -50,8 +50,9 @@ def hmm_lowrank_forward(pi, A, E, tokens, FA, FB):
 
 def hmm_lowrank_fwd_bwd(pi, A, E, tokens, FA, FB):
     """Returns dict(ll, dpi, dA = sum_t F+_t, W = sum_t W_t, dE, dFA [T-1,B,H,K],
-    dFB [T-1,B,K,H]): the root flow is 1 per sample, so the factor gradients are those of
-    sum_b LL_b."""
+    dFB [T-1,B,K,H], absdFA, absdFB): the root flow is 1 per sample, so the factor
+    gradients are those of sum_b LL_b; absdF* are the layers' sums of absolute terms
+    before cancellation (lowrank_exp_sum_bwd's absdA, absdB)."""
     pi = np.asarray(pi, dtype=np.float64)
     A = np.asarray(A, dtype=np.float64)
     tokens = np.asarray(tokens)
@@ -68,6 +69,8 @@ def hmm_lowrank_fwd_bwd(pi, A, E, tokens, FA, FB):
     K = np.asarray(FA).shape[-1]
     dFA = np.zeros((T - 1, B, H, K))
     dFB = np.zeros((T - 1, B, K, H))
+    absdFA = np.zeros_like(dFA)
+    absdFB = np.zeros_like(dFB)
     for t in range(T):
         np.add.at(dE.T, tokens[:, t], f.T)                        # dE[:, x_{t,b}] += f[:, b]
         if t == T - 1:
@@ -77,5 +80,7 @@ def hmm_lowrank_fwd_bwd(pi, A, E, tokens, FA, FB):
         W += r["W"]
         dFA[t] = r["dA"]
         dFB[t] = r["dB"]
+        absdFA[t] = r["absdA"]
+        absdFB[t] = r["absdB"]
         f = r["e"]                                                # the flows of P_{t+1}
-    return dict(ll=ll, dpi=dpi, dA=dA, W=W, dE=dE, dFA=dFA, dFB=dFB)
+    return dict(ll=ll, dpi=dpi, dA=dA, W=W, dE=dE, dFA=dFA, dFB=dFB, absdFA=absdFA, absdFB=absdFB)

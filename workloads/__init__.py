@@ -163,6 +163,24 @@ def lowrank(spread: float = 1.0):
     return lowrank_inputs(1024, 1024, 16, 64, spread, seed=SPREAD_SEEDS[spread])
 
 
+def hmm_lowrank_inputs(H: int, T: int, V: int, B: int, K: int, spread: float, seed: int):
+    """An HMM (as hmm_inputs) plus one pair of LowRank factors per transition copy:
+    FA [T-1,B,H,K], FB [T-1,B,K,H] drawn N(0, s^2) with s = sqrt(spread / sqrt(K)), so
+    that an entry of FA[t][b] FB[t][b] has standard deviation ``spread`` nats."""
+    d = hmm_inputs(H, T, V, B, seed)
+    rng = np.random.default_rng(seed + 500)
+    s = float(np.sqrt(spread / np.sqrt(K)))
+    d["FA"] = _f32(s * rng.standard_normal((T - 1, B, H, K)))
+    d["FB"] = _f32(s * rng.standard_normal((T - 1, B, K, H)))
+    return d
+
+
+def hmm_lowrank():
+    """The pages' LowRank measurement setting: an HMM of 1024 states, rank 16, batch 64
+    (64 positions and vocabulary 1024, as the pages' 1024-state HMM), spread 1 nat."""
+    return hmm_lowrank_inputs(1024, 64, 1024, 64, 16, 1.0, seed=11)
+
+
 # ------------------------------------------------------------------- EM M-step
 def em_statistics(seed: int = 10):
     """Synthetic parameter statistics of the M-step at the HMM 4096 x 32 workload's
