@@ -102,3 +102,48 @@ def test_hmm_argument_errors_before_launch(lib):
 
 def test_profile_capacity_check(lib):
     assert N.STATUS[lib.pc_profile_start(0)] == "PC_ERR_SHAPE"
+
+
+def test_em_normalize_argument_errors_before_launch(lib):
+    fake = C.c_void_p(0x1000)
+    assert N.STATUS[lib.pc_em_normalize(1, 4, 4, None, None, fake, None)] == "PC_ERR_NULL"
+    assert N.STATUS[lib.pc_em_normalize(1, 4, 4, fake, None, None, None)] == "PC_ERR_NULL"
+    assert N.STATUS[lib.pc_em_normalize(0, 4, 4, fake, None, fake, None)] == "PC_ERR_SHAPE"
+    assert N.STATUS[lib.pc_em_normalize(1, 4, 0, fake, fake, fake, None)] == "PC_ERR_SHAPE"
+    assert N.STATUS[lib.pc_em_normalize(1 << 16, 1 << 16, 4, fake, None, fake, None)] == "PC_ERR_SHAPE"
+
+
+def test_lowrank_sum_exp_argument_errors_before_launch(lib):
+    fake = C.c_void_p(0x1000)
+    nb = _size()
+    assert lib.pc_lowrank_sum_exp_workspace(1024, 1024, 16, 64, 1, 0, C.byref(nb)) == 0
+    fwd_only = _size()
+    assert lib.pc_lowrank_sum_exp_workspace(1024, 1024, 16, 64, 0, 0, C.byref(fwd_only)) == 0
+    assert 0 < fwd_only.value < nb.value
+    assert N.STATUS[lib.pc_lowrank_sum_exp_workspace(8, 8, 0, 4, 0, 0, C.byref(nb))] == "PC_ERR_SHAPE"
+    assert N.STATUS[lib.pc_lowrank_sum_exp_workspace(8, 8, 4, 4, 0, 9, C.byref(nb))] == "PC_ERR_UNKNOWN_PRECISION"
+    st = lib.pc_lowrank_sum_exp_fwd(8, 8, 4, 4, fake, fake, fake, fake, None, fake, 0, fake, 1 << 30, None)
+    assert N.STATUS[st] == "PC_ERR_NULL"
+    st = lib.pc_lowrank_sum_exp_fwd(8, 8, 4, 4, fake, fake, fake, fake, fake, fake, 0, fake, 16, None)
+    assert N.STATUS[st] == "PC_ERR_WORKSPACE"
+    st = lib.pc_lowrank_sum_exp_bwd(8, 8, 4, 4, fake, fake, fake, fake, None, None, None, None, None, None, 0, 0,
+                                    fake, 1 << 30, None)
+    assert N.STATUS[st] == "PC_ERR_NULL"
+
+
+def test_hmm_lowrank_argument_errors_before_launch(lib):
+    fake = C.c_void_p(0x1000)
+    nb = _size()
+    assert lib.pc_hmm_lowrank_workspace(1024, 64, 1024, 64, 16, 0, C.byref(nb)) == 0
+    assert N.STATUS[lib.pc_hmm_lowrank_workspace(64, 4, 8, 4, 65, 0, C.byref(nb))] == "PC_ERR_UNSUPPORTED"
+    assert N.STATUS[lib.pc_hmm_lowrank_workspace(64, 0, 8, 4, 4, 0, C.byref(nb))] == "PC_ERR_SHAPE"
+    args = [None] * 13
+    st = lib.pc_hmm_lowrank_fwd_bwd(64, 4, 8, 4, 4, None, fake, fake, fake, fake, fake, fake, *args[:6], 0, 0,
+                                    fake, 1 << 30, None)
+    assert N.STATUS[st] == "PC_ERR_NULL"
+    st = lib.pc_hmm_lowrank_fwd_bwd(64, 4, 8, 4, 4, fake, fake, fake, fake, None, None, fake, *args[:6], 0, 0,
+                                    fake, 1 << 30, None)
+    assert N.STATUS[st] == "PC_ERR_NULL"                 # factors required when T > 1
+    st = lib.pc_hmm_lowrank_fwd_bwd(64, 4, 8, 4, 4, fake, fake, fake, fake, fake, fake, fake, *args[:6], 0, 0,
+                                    fake, 64, None)
+    assert N.STATUS[st] == "PC_ERR_WORKSPACE"
