@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="hmm",
                     choices=["hmm", "hmm1024", "layer", "hclt", "lowrank", "lowrank_sum_exp", "hmm_lowrank", "mstep"])
+    ap.add_argument("--flow-fp8", action="store_true",
+                    help="lowrank_sum_exp: e4m3 operands for the two flow contractions (precision auto)")
     ap.add_argument("--hclt-nvars", type=int, default=768,
                     help="HCLT variables (768 = the workload; fewer for a profiler-sized case)")
     return ap.parse_args()
@@ -349,6 +351,11 @@ class LowRankSumExpWorkload(LowRankWorkload):
         from oracle.lowrank import lowrank_sum_exp_bwd
         lowrank_sum_exp_bwd(d["theta"], d["A"][:b], d["Bm"][:b], d["x"][:, :b], d["f"][:, :b])
 
+    flow_precision = "bf16"
+
+    def config(self):
+        return {**super().config(), "flow_precision": self.flow_precision}
+
     def device(self, pc, d, dev, prec):
         import torch
         t = {k: torch.from_numpy(d[k]).to(dev) for k in ("theta", "A", "Bm", "x", "f")}
@@ -358,12 +365,13 @@ class LowRankSumExpWorkload(LowRankWorkload):
         logZ = torch.empty(Bs, M, device=dev)
         g = dict(dA=torch.empty(Bs, M, K, device=dev), dB=torch.empty(Bs, K, N, device=dev),
                  e=torch.empty(N, Bs, device=dev), Fplus=torch.empty(M, N, device=dev), W=torch.empty(M, N, device=dev))
+        fp = self.flow_precision
 
         def step(A=None, Bm=None):
             A = t["A"] if A is None else A
             Bm = t["Bm"] if Bm is None else Bm
             pc.lowrank_sum_exp_fwd(t["theta"], A, Bm, t["x"], precision=prec, out=out, logZ=logZ)
-            pc.lowrank_sum_exp_bwd(t["theta"], A, Bm, t["x"], t["f"], precision=prec, **g)
+            pc.lowrank_sum_exp_bwd(t["theta"], A, Bm, t["x"], t["f"], precision=prec, flow_precision=fp, **g)
         hA = torch.from_numpy(d["A"]).pin_memory()
         hB = torch.from_numpy(d["Bm"]).pin_memory()
         h_out = torch.empty(M, Bs).pin_memory()
@@ -461,6 +469,9 @@ def oracle_sample_rate(w, d, target_s: float = 12.0):
 
 def pick_workload(args):
     w = WORKLOADS[args.workload]
+    if w.name == "lowrank_sum_exp" and args.flow_fp8:
+        w.flow_precision = "fp8"
+        w.desc += " (flow contractions on e4m3 operands)"
     if w.name == "hclt" and args.hclt_nvars != 768:
         w.nvars = args.hclt_nvars
         w.desc = w.desc.replace("768 variables", f"{args.hclt_nvars} variables")

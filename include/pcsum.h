@@ -267,7 +267,11 @@ PCSUM_API pc_status_t pc_lowrank_exp_sum_bwd(int M, int N, int K, int B, const f
  * (sample, rank) pairs with the exponentials and rank reductions in element-wise kernels;
  * row maxima of A, B and x are taken out of every exponential (they cancel), so any
  * finite factors are in range. Precision: every contraction's products in the mode's
- * format (bf16 / TF32 / 3xTF32), float32 accumulation.
+ * format (bf16 / TF32 / 3xTF32), float32 accumulation. flow_fp8 != 0 (the doc's opt-in
+ * flow_precision "fp8"; precision auto only, ignored otherwise): the two flow
+ * contractions (Fplus and Wstat) take e4m3 operands with a power-of-two scale per operand
+ * row (largest magnitude within 448), float32 accumulation; the gradients and element
+ * flows are not affected. The doc measures such statistics about 16x less accurate.
  * Limits: K >= 1, B <= 65535, B*K <= 2^22, M, N <= 2^24 (PC_ERR_SHAPE). M, N or B may
  * be 0. Workspace: pc_lowrank_sum_exp_workspace(..., with_backward, ...) bytes, 16-byte
  * aligned.
@@ -283,7 +287,7 @@ PCSUM_API pc_status_t pc_lowrank_sum_exp_fwd(int M, int N, int K, int B, const f
 PCSUM_API pc_status_t pc_lowrank_sum_exp_bwd(int M, int N, int K, int B, const float* theta,
                                              const float* A, const float* Bm, const float* x,
                                              const float* f, float* dA, float* dB, float* e,
-                                             float* Fplus, float* Wstat, int accumulate,
+                                             float* Fplus, float* Wstat, int accumulate, int flow_fp8,
                                              pc_precision_t prec, void* ws, size_t ws_bytes,
                                              pc_stream_t stream);
 

@@ -47,7 +47,7 @@ SIGNATURES = {
     "pc_lowrank_exp_sum_workspace": [_i, _i, _i, _i, _i, _i, _p],
     "pc_lowrank_sum_exp_workspace": [_i, _i, _i, _i, _i, _i, _p],
     "pc_lowrank_sum_exp_fwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p],
-    "pc_lowrank_sum_exp_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
+    "pc_lowrank_sum_exp_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _p, _sz, _p],
     "pc_lowrank_exp_sum_fwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p],
     "pc_em_normalize": [_i, _i, _i, _p, _p, _p, _p],
     "pc_hmm_lowrank_workspace": [_i, _i, _i, _i, _i, _i, _p],

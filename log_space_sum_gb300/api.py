@@ -320,10 +320,13 @@ def lowrank_sum_exp_fwd(theta, A, Bm, x, precision="auto", out=None, logZ=None, 
 
 def lowrank_sum_exp_bwd(theta, A, Bm, x, f, precision="auto", grads=True, element_flows=True, param_flows=True,
                         z_correction=True, dA=None, dB=None, e=None, Fplus=None, W=None, accumulate=False,
-                        **removed):
+                        flow_precision="bf16", **removed):
     """LowRank sum_exp layer backward (pc_lowrank_sum_exp_bwd): the same outputs as
-    lowrank_exp_sum_bwd (dA, dB, e, Fplus, W; what is switched off is None)."""
+    lowrank_exp_sum_bwd (dA, dB, e, Fplus, W; what is switched off is None).
+    ``flow_precision="fp8"`` (precision "auto"): Fplus and W from e4m3 products."""
     _removed_flags(removed, "lowrank_sum_exp_bwd")
+    if flow_precision not in ("bf16", "fp8"):
+        raise ValueError(f"flow_precision must be 'bf16' or 'fp8', got {flow_precision!r}")
     prec = precision_code(precision)
     dev, M, Nn, K, Bs = _lowrank_shapes(theta, A, Bm, x)
     _check(f, "f", device=dev)
@@ -339,7 +342,8 @@ def lowrank_sum_exp_bwd(theta, A, Bm, x, f, precision="auto", grads=True, elemen
     nb = _query("pc_lowrank_sum_exp_workspace", M, Nn, K, Bs, 1, prec)
     ws = workspace(nb, dev)
     N.call("pc_lowrank_sum_exp_bwd", M, Nn, K, Bs, _ptr(theta), _ptr(A), _ptr(Bm), _ptr(x), _ptr(f), _ptr(dA),
-           _ptr(dB), _ptr(e), _ptr(Fplus), _ptr(W), int(bool(accumulate)), prec, _ptr(ws), ws.numel(), _stream(dev))
+           _ptr(dB), _ptr(e), _ptr(Fplus), _ptr(W), int(bool(accumulate)), int(flow_precision == "fp8"), prec,
+           _ptr(ws), ws.numel(), _stream(dev))
     return dict(dA=dA, dB=dB, e=e, Fplus=Fplus, W=W)
 
 

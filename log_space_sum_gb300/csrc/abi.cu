@@ -141,8 +141,10 @@ pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision
   const cuuint64_t strides[2] = {cuuint64_t(op.ld) * es, cuuint64_t(op.ld) * op.rows * es};
   const cuuint32_t box[3] = {cuuint32_t(128 / es), cuuint32_t(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, p == PC_PREC_AUTO ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  const CUtensorMapDataType dt = p == PC_PREC_AUTO  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : p == kPrecFp8Ops ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUresult r = g_encode(map, dt,
                               3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -29,6 +29,13 @@
 //   W[i,j]     = sum_(b,r) (a t)[i,(b,r)] c[j,(b,r)].
 //
 // Contractions: P|Q (M x 2BK x N), U|U' (N x 2BK x M), F+ and W (M x N x BK).
+//
+// Opt-in fp8 flow products (the doc's flow_precision "fp8", precision auto only): the two
+// flow contractions take e4m3 operands, each operand row scaled by a power of two that
+// brings its largest magnitude within the e4m3 range (448), accumulated in float32; the
+// epilogue multiplies by the inverse row scales of both operands.
+#include <cuda_fp8.h>
+
 #include "pc_launch.cuh"
 
 namespace pc {
@@ -131,6 +138,28 @@ __global__ void k_se_children(int N, int K, int B, long long V, const float* __r
   }
 }
 
+// dst[r][c] = e4m3(src[r][c] * 2^e_r) with 2^e_r the largest power of two for which the
+// row's largest magnitude stays within 448; inv[r] = 2^-e_r. One block per row.
+__global__ void k_se_rows_to_fp8(const float* __restrict__ src, long long ld_src, int C, uint8_t* __restrict__ dst,
+                                 long long ld_dst, float* __restrict__ inv) {
+  __shared__ float red[32];
+  const long long r = blockIdx.x;
+  const float* row = src + r * ld_src;
+  float m = 0.f;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) m = fmaxf(m, fabsf(row[c]));
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = m;
+  __syncthreads();
+  m = 0.f;
+  for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) m = fmaxf(m, red[w]);
+  int k = 0;
+  if (m > 0.f) frexpf(448.f / m, &k);  // 448 / m = f 2^k, f in [0.5, 1): floor(log2) = k - 1
+  const float sc = m > 0.f ? ldexpf(1.f, k - 1) : 1.f;
+  uint8_t* out = dst + r * ld_dst;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) out[c] = __nv_fp8_e4m3(row[c] * sc).__x;
+  if (threadIdx.x == 0) inv[r] = 1.f / sc;
+}
+
 __global__ void k_se_fill(float* __restrict__ p, long long n, float v) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < n) p[i] = v;
@@ -139,6 +168,8 @@ __global__ void k_se_fill(float* __restrict__ p, long long n, float v) {
 struct SeWs {
   float *xT, *m, *beta, *CV, *PQ, *L, *U;
   Operand th, thT, Vop, Lop, LsT, LtT, RvT, RcT;
+  float *T8a, *T8b, *inv_a, *inv_b;  // fp8 flow products: float32 transposes, inverse row scales
+  Operand A8, B8;                     // and the e4m3 operands
 };
 
 size_t carve_se(void* base, pc_precision_t p, int M, int N, int K, int B, bool bwd, SeWs* w) {
@@ -161,6 +192,14 @@ size_t carve_se(void* base, pc_precision_t p, int M, int N, int K, int B, bool b
     w->LtT = c.operand(p, 1, M, V);
     w->RvT = c.operand(p, 1, N, V);
     w->RcT = c.operand(p, 1, N, V);
+    if (p == PC_PREC_AUTO) {
+      w->T8a = static_cast<float*>(c.take(size_t(M) * V * 4));
+      w->T8b = static_cast<float*>(c.take(size_t(N) * V * 4));
+      w->inv_a = static_cast<float*>(c.take(size_t(M) * 4));
+      w->inv_b = static_cast<float*>(c.take(size_t(N) * 4));
+      w->A8 = c.operand(kPrecFp8Ops, 1, M, V);
+      w->B8 = c.operand(kPrecFp8Ops, 1, N, V);
+    }
   }
   return c.used + 256;
 }
@@ -226,7 +265,7 @@ pc_status_t se_fwd(int M, int N, int K, int B, const float* theta, const float* 
 template <int P>
 pc_status_t se_bwd(int M, int N, int K, int B, const float* theta, const float* A, const float* Bm, const float* x,
                    const float* f, float* dA, float* dB, float* e, float* Fp, float* W, int accumulate,
-                   pc_precision_t prec, void* ws, cudaStream_t s) {
+                   bool flow_fp8, pc_precision_t prec, void* ws, cudaStream_t s) {
   if (!accumulate) {  // outputs that no pass writes when a size is zero
     if (dA && N == 0) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(B) * M * K * 4, s));
     if (dB && M == 0) PC_CUDA(cudaMemsetAsync(dB, 0, size_t(B) * K * N * 4, s));
@@ -256,6 +295,40 @@ pc_status_t se_bwd(int M, int N, int K, int B, const float* theta, const float* 
       return st;
     k_se_children<<<dim3(cdiv(N, 256), B), 256, 0, s>>>(N, K, B, V, w.CV, w.U, dB, e, accumulate);
     PC_LAUNCH_CHECK();
+  }
+  if constexpr (P == kBF16) {
+    if (flow_fp8) {  // both flow contractions on e4m3 operands
+      for (int kind = 0; kind < 2; ++kind) {
+        float* out = kind == 0 ? Fp : W;
+        if (!out) continue;
+        if ((st = transpose_f32(w.L + kind * V * M, M, 0, 1, static_cast<int>(V), M, w.T8a, V, 0, s)) != PC_OK)
+          return st;
+        if ((st = transpose_f32(w.CV + kind * V * N, N, 0, 1, static_cast<int>(V), N, w.T8b, V, 0, s)) != PC_OK)
+          return st;
+        k_se_rows_to_fp8<<<M, 256, 0, s>>>(w.T8a, V, static_cast<int>(V), static_cast<uint8_t*>(w.A8.ptr), w.A8.ld,
+                                           w.inv_a);
+        PC_LAUNCH_CHECK();
+        k_se_rows_to_fp8<<<N, 256, 0, s>>>(w.T8b, V, static_cast<int>(V), static_cast<uint8_t*>(w.B8.ptr), w.B8.ld,
+                                           w.inv_b);
+        PC_LAUNCH_CHECK();
+        OperandMaps ma, mb;
+        if ((st = encode_maps(&ma, w.A8, kPrecFp8Ops, kBM)) != PC_OK) return st;
+        if ((st = encode_maps(&mb, w.B8, kPrecFp8Ops, kSeBN)) != PC_OK) return st;
+        const dim3 grid(cdiv(M, kBM), cdiv(N, kSeBN), 1);
+        const int nkb = num_k_blocks(V, kPrecFp8Ops);
+        if (kind == 0) {
+          EpiThetaScale::Params ep{Fp, theta, M, N, accumulate, nullptr, w.inv_a, w.inv_b};
+          st = launch_gemm<kFP8, kSeBN, EpiThetaScale>(grid, ma.hi, ma.lo, mb.hi, mb.lo, nkb, ep, s,
+                                                        PC_KIND_LOWRANK_BWD, 2ll * M * N * V);
+        } else {
+          EpiStoreF32::Params ep{W, N, M, N, accumulate, w.inv_a, w.inv_b};
+          st = launch_gemm<kFP8, kSeBN, EpiStoreF32>(grid, ma.hi, ma.lo, mb.hi, mb.lo, nkb, ep, s,
+                                                      PC_KIND_LOWRANK_BWD, 2ll * M * N * V);
+        }
+        if (st != PC_OK) return st;
+      }
+      return PC_OK;
+    }
   }
   if (Fp) {  // F+ = theta * ((a s) (c v)^T) over the virtual batch
     if ((st = transpose_to_operand<P>(w.L, M, 0, 1, static_cast<int>(V), M, w.LsT, s)) != PC_OK) return st;
@@ -326,8 +399,8 @@ pc_status_t pc_lowrank_sum_exp_fwd(int M, int N, int K, int B, const float* thet
 
 pc_status_t pc_lowrank_sum_exp_bwd(int M, int N, int K, int B, const float* theta, const float* A, const float* Bm,
                                    const float* x, const float* f, float* dA, float* dB, float* e, float* Fplus,
-                                   float* Wstat, int accumulate, pc_precision_t prec, void* ws, size_t ws_bytes,
-                                   pc_stream_t stream) {
+                                   float* Wstat, int accumulate, int flow_fp8, pc_precision_t prec, void* ws,
+                                   size_t ws_bytes, pc_stream_t stream) {
   clear_error();
   pc_status_t st = check_se_shape(M, N, K, B, prec);
   if (st != PC_OK) return st;
@@ -341,11 +414,13 @@ pc_status_t pc_lowrank_sum_exp_bwd(int M, int N, int K, int B, const float* thet
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (prec) {
     case PC_PREC_AUTO:
-      return se_bwd<kBF16>(M, N, K, B, theta, A, Bm, x, f, dA, dB, e, Fplus, Wstat, accumulate, prec, ws, s);
+      return se_bwd<kBF16>(M, N, K, B, theta, A, Bm, x, f, dA, dB, e, Fplus, Wstat, accumulate, flow_fp8 != 0, prec,
+                           ws, s);
     case PC_PREC_TF32:
-      return se_bwd<kTF32>(M, N, K, B, theta, A, Bm, x, f, dA, dB, e, Fplus, Wstat, accumulate, prec, ws, s);
+      return se_bwd<kTF32>(M, N, K, B, theta, A, Bm, x, f, dA, dB, e, Fplus, Wstat, accumulate, false, prec, ws, s);
     default:
-      return se_bwd<kTF32x3>(M, N, K, B, theta, A, Bm, x, f, dA, dB, e, Fplus, Wstat, accumulate, prec, ws, s);
+      return se_bwd<kTF32x3>(M, N, K, B, theta, A, Bm, x, f, dA, dB, e, Fplus, Wstat, accumulate, false, prec, ws,
+                             s);
   }
 }
 

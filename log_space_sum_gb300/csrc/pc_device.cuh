@@ -197,6 +197,17 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t 
       : "memory");
 }
 
+// e4m3 x e4m3 products (instruction descriptor formats 0), K = 32 per instruction.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
@@ -227,7 +238,8 @@ __device__ __forceinline__ void tmem_ld_32x32(uint32_t taddr, float (&v)[32]) {
 
 // --------------------------------------------------------------- operand formats
 // Precision modes of the contractions (pyjuice PR #62, Summary 1 table).
-enum Prec : int { kBF16 = 0, kTF32 = 1, kTF32x3 = 2 };
+// kFP8: e4m3 operands (kind::f8f6f4), used internally by the opt-in fp8 flow contractions.
+enum Prec : int { kBF16 = 0, kTF32 = 1, kTF32x3 = 2, kFP8 = 3 };
 
 __device__ __forceinline__ float tf32_rna(float v) {
   uint32_t r;
@@ -265,7 +277,7 @@ __device__ __forceinline__ float load_operand(const void* base, size_t idx, size
 }
 
 template <int P>
-constexpr int operand_bytes() { return P == kBF16 ? 2 : 4; }
+constexpr int operand_bytes() { return P == kBF16 ? 2 : (P == kFP8 ? 1 : 4); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);

@@ -53,7 +53,7 @@ struct GemmShape {
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
   static constexpr uint32_t kStageBytes = kParts * (kABytes + kBBytes);
-  static constexpr uint32_t kUmmaK = (P == kBF16) ? 16 : 8;  // K per MMA instruction
+  static constexpr uint32_t kUmmaK = (P == kBF16) ? 16 : (P == kFP8 ? 32 : 8);  // K per MMA instruction
   static constexpr uint32_t kKSteps = kBK / kUmmaK;          // MMAs per ring slot (4)
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: two epilogue warps split the 32-column chunks");
 };
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // -------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = umma_idesc(P == kBF16 ? 1u : 2u, kBM, BN);
+      constexpr uint32_t idesc = umma_idesc(P == kBF16 ? 1u : (P == kFP8 ? 0u : 2u), kBM, BN);
       const int total_q = num_kb * static_cast<int>(S::kKSteps);
       int q = 0;  // k-steps issued so far
       for (int kb = 0; kb < num_kb; ++kb) {
@@ -390,6 +390,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t acc = (first && kk == 0) ? 0u : 1u;
             if constexpr (P == kBF16) {
               umma_bf16(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+            } else if constexpr (P == kFP8) {
+              umma_f8(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
             } else {
               umma_tf32(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
             }

@@ -70,7 +70,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 
 // Bytes of one stored operand element, and the number of stored parts (hi, lo).
-inline int operand_elem_bytes(pc_precision_t p) { return p == PC_PREC_AUTO ? 2 : 4; }
+// Internal operand format of the opt-in fp8 flow contractions (not a public mode: the
+// public calls reject it): e4m3, one byte per element.
+constexpr pc_precision_t kPrecFp8Ops = static_cast<pc_precision_t>(3);
+inline int operand_elem_bytes(pc_precision_t p) { return p == PC_PREC_AUTO ? 2 : (p == kPrecFp8Ops ? 1 : 4); }
 inline int operand_parts(pc_precision_t p) { return p == PC_PREC_FP32 ? 2 : 1; }
 
 // An operand matrix [groups][rows][ld] in a precision's storage format. For 3xTF32

@@ -260,6 +260,14 @@ inline pc_status_t transpose_f32(const float* src, long long src_ld, long long s
                             StoreF32{dst, dst_ld, static_cast<long long>(C), accumulate}, s);
 }
 
+// w[r] (rows i0 + r of column j, one lane per column) *= rs[i0 + r] * cs[j] (NULL: 1).
+__device__ __forceinline__ void scale_rows(const float* rs, const float* cs, int i0, int j, int M,
+                                           float (&w)[32]) {
+  const float c = cs ? cs[j] : 1.f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) w[r] *= (rs && i0 + r < M) ? rs[i0 + r] * c : c;
+}
+
 // Shared with the circuits: F[g][i][j] (+)= theta[g][i][j] * D[i,j].
 struct EpiThetaScale : EpiNoHooks {
   static constexpr bool kTranspose = true;
@@ -272,6 +280,10 @@ struct EpiThetaScale : EpiNoHooks {
     const float* theta;
     int M, N, accumulate;
     const int* gmap;  // group g reads theta / writes F at matrix gmap[g] (NULL: g)
+    // D is scaled by rscale[i] * cscale[j] (NULL: 1): the inverse operand row scales of
+    // the fp8 flow contractions
+    const float* rscale = nullptr;
+    const float* cscale = nullptr;
   };
   // Transposed so that lane l owns column col0 + l of the warp's 32 rows: every theta
   // load and F store of the warp covers one contiguous row segment. All loads of the
@@ -288,6 +300,7 @@ struct EpiThetaScale : EpiNoHooks {
     const long long gm = p.gmap ? p.gmap[g] : g;
     const float* tp = p.theta + (gm * p.M + i0) * ld + j;
     float* Fp = p.F + (gm * p.M + i0) * ld + j;
+    if (p.rscale || p.cscale) scale_rows(p.rscale, p.cscale, i0, j, p.M, w);
     // two halves of 16 rows keep the loads-before-stores batch within the register budget
 #pragma unroll
     for (int h = 0; h < 32; h += 16) {
@@ -346,6 +359,7 @@ struct EpiThetaScale : EpiNoHooks {
     const long long gm = p.gmap ? p.gmap[g] : g;
     const float* ts = reinterpret_cast<const float*>(stage) + static_cast<long long>(i0 - m0) * BN + col0 + lane;
     float* Fp = p.F + (gm * p.M + i0) * ld + j;
+    if (p.rscale || p.cscale) scale_rows(p.rscale, p.cscale, i0, j, p.M, w);
 #pragma unroll
     for (int h = 0; h < 32; h += 16) {
       float f[16];
@@ -367,6 +381,8 @@ struct EpiStoreF32 : EpiNoHooks {
     float* D;
     long long ld;
     int M, N, accumulate;
+    const float* rscale = nullptr;  // as EpiThetaScale's
+    const float* cscale = nullptr;
   };
   __device__ static void apply(const Params& p, int, int m0, int n0, int row, int col0, float (&v)[32], uint8_t*,
                                float* tbuf) {
@@ -377,6 +393,7 @@ struct EpiStoreF32 : EpiNoHooks {
     const int j = n0 + col0 + lane;
     if (j >= p.N) return;
     float* Dp = p.D + static_cast<long long>(i0) * p.ld + j;
+    if (p.rscale || p.cscale) scale_rows(p.rscale, p.cscale, i0, j, p.M, w);
 #pragma unroll
     for (int h = 0; h < 32; h += 16) {
       float f[16];

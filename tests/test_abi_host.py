@@ -126,7 +126,7 @@ def test_lowrank_sum_exp_argument_errors_before_launch(lib):
     assert N.STATUS[st] == "PC_ERR_NULL"
     st = lib.pc_lowrank_sum_exp_fwd(8, 8, 4, 4, fake, fake, fake, fake, fake, fake, 0, fake, 16, None)
     assert N.STATUS[st] == "PC_ERR_WORKSPACE"
-    st = lib.pc_lowrank_sum_exp_bwd(8, 8, 4, 4, fake, fake, fake, fake, None, None, None, None, None, None, 0, 0,
+    st = lib.pc_lowrank_sum_exp_bwd(8, 8, 4, 4, fake, fake, fake, fake, None, None, None, None, None, None, 0, 0, 0,
                                     fake, 1 << 30, None)
     assert N.STATUS[st] == "PC_ERR_NULL"
 

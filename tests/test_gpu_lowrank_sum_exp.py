@@ -141,3 +141,30 @@ def test_edge_cases():
     out, logZ, g = _run(d2, "fp32")
     assert np.all(np.isneginf(out[:, 1])) and np.all(np.isfinite(out[:, 0]))
     assert np.all(g["e"][:, 1] == 0) and np.all(g["dA"][1] == 0) and np.all(g["dB"][1] == 0)
+
+
+@pytest.mark.parametrize("spread", [0.3, 1.0, 4.0])
+def test_fp8_flow_products(spread):
+    # F+ and W are sums of positive terms, each the product of two operands rounded to e4m3
+    # (3 mantissa bits: within 2^-4 relative), so every entry is within 2 * 2^-4 (+ float32
+    # rounding) of the exact sum; the gradients and element flows do not change.
+    d = lowrank(spread)
+    r = _oracle(d)
+    t = _cuda(d)
+    g = pc.lowrank_sum_exp_bwd(t["theta"], t["A"], t["Bm"], t["x"], t["f"], precision="auto")
+    q = pc.lowrank_sum_exp_bwd(t["theta"], t["A"], t["Bm"], t["x"], t["f"], precision="auto", flow_precision="fp8")
+    torch.cuda.synchronize()
+    pc.device_status()
+    for k in ("dA", "dB", "e"):
+        assert torch.equal(q[k], g[k]), k
+    rel = {}
+    for k in ("Fplus", "W"):
+        ref = r[k]
+        got = q[k].cpu().numpy().astype(np.float64)
+        rel[k] = np.abs(got - ref) / np.abs(ref)
+        assert rel[k].max() <= 2 * 2.0 ** -4 * (1 + 1e-3), (k, rel[k].max())
+    th = d["theta"].astype(np.float64)
+    ratio = (q["Fplus"].cpu().numpy() / (th * q["W"].cpu().numpy())) / (r["Fplus"] / (th * r["W"]))
+    print(f"fp8 flows spread {spread}: F+ median {np.median(rel['Fplus']):.2e} max {rel['Fplus'].max():.2e}; "
+          f"W median {np.median(rel['W']):.2e} max {rel['W'].max():.2e}; F+/F- median "
+          f"{np.median(np.abs(ratio - 1)):.2e} max {np.abs(ratio - 1).max():.2e}")
