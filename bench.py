@@ -24,9 +24,9 @@ Prints one JSON line (rank 0). Under torchrun each rank runs its own batch (weak
 scaling; no data-path collective). Between timed steps a 256 MiB buffer is written to
 flush the 126 MB L2. The value comes from a timed pass with only the step events;
 the roofline entry from a second timed pass of the same steps in which the library
-records a CUDA event pair around every contraction on the launching stream
-(pc_profile_start/stop) — such events between kernels serialise them, so they stay out
-of the first pass. ``--impl reference`` times the float64 CPU oracle on a
+records a CUDA event pair around every contraction on the launching stream, or around
+each HMM chain of same-kind contractions as a whole (pc_profile_start/stop) — events
+between kernels serialise them, so they stay out of the first pass. ``--impl reference`` times the float64 CPU oracle on a
 bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -668,11 +668,11 @@ def run_ours(args):
     # ---- roofline of the dominant kernel kind (by total time in the timed region)
     peaks, peak_src = load_peaks()
     by_kind = {}
-    for kind, ms, fl in prof:
+    for kind, ms, fl, nl in prof:
         k = by_kind.setdefault(kind, [0.0, 0, 0])
         k[0] += ms
         k[1] += fl
-        k[2] += 1
+        k[2] += nl
     dom = max(by_kind, key=lambda k: by_kind[k][0])
     dms, dfl, dn = by_kind[dom]
     if w.roofline_bound == "hbm":

@@ -93,14 +93,18 @@ PCSUM_API unsigned long long pc_launch_count(void);
  * the last read, or PC_ERR_CUDA. Diagnostic; not for the hot path. */
 PCSUM_API pc_status_t pc_device_status(pc_stream_t stream);
 
-/* Per-launch timing of the tensor-core contractions, for measurement. Between
+/* Timing of the tensor-core contractions, for measurement. Between
  * pc_profile_start(capacity) and pc_profile_stop, every contraction the library
- * launches records a CUDA event pair on its stream (at most `capacity` launches).
- * pc_profile_stop synchronises the device, then writes for each recorded launch i
+ * launches records a CUDA event pair on its stream (at most `capacity` records), except
+ * the HMM's chain contractions: each chain of T-1 consecutive launches of one kind is
+ * one record (events between them would break their programmatic overlap).
+ * pc_profile_stop synchronises the device, then writes for each record i
  * (i < *count <= capacity): ms[i] = elapsed device time, kind[i] = which contraction
- * (PC_KIND_*), flops[i] = its algorithmic flops 2*M*N*K (each product counted once);
- * for PC_KIND_EM_MSTEP (memory-bound) flops[i] holds the algorithmic bytes instead.
- * Not thread-safe; host-side event objects only, no device memory. */
+ * (PC_KIND_*), flops[i] = the algorithmic flops of its launches, 2*M*N*K each (each
+ * product counted once), launches[i] = how many launches the record spans; for
+ * PC_KIND_EM_MSTEP (memory-bound) flops[i] holds the algorithmic bytes instead. Any
+ * output pointer may be NULL. Not thread-safe; host-side event objects only, no device
+ * memory. */
 typedef enum {
   PC_KIND_LAYER_FWD = 0, PC_KIND_LAYER_ELEM = 1, PC_KIND_LAYER_PARAM = 2,
   PC_KIND_HMM_FWD = 3, PC_KIND_HMM_ELEM = 4, PC_KIND_HMM_PARAM = 5,
@@ -109,7 +113,7 @@ typedef enum {
 } pc_kind_t;
 PCSUM_API pc_status_t pc_profile_start(int capacity);
 PCSUM_API pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long long* flops,
-                                      int capacity);
+                                      int* launches, int capacity);
 
 /* ------------------------------------------------------------------------------
  * Dense sum layer, G groups (pyjuice PR #62, Summary 2: shared-children layers

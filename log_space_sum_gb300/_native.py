@@ -35,7 +35,7 @@ SIGNATURES = {
     "pc_device_status": [_p],
     "pc_launch_count": [],
     "pc_profile_start": [_i],
-    "pc_profile_stop": [_p, _p, _p, _p, _i],
+    "pc_profile_stop": [_p, _p, _p, _p, _p, _i],
     "pc_sum_layer_workspace": [_i, _i, _i, _i, _i, _p],
     "pc_sum_layer_fwd": [_i, _i, _i, _i, _p, _p, _ll, _p, _i, _p, _sz, _p],
     "pc_sum_layer_bwd": [_i, _i, _i, _i, _p, _p, _ll, _p, _p, _p, _p, _i, _i, _p, _sz, _p],

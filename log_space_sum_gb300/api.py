@@ -378,10 +378,13 @@ def profile_start(capacity: int = 4096) -> None:
 
 
 def profile_stop(capacity: int = 4096):
-    """Returns [(kind, ms, flops)] for every contraction launched since profile_start."""
+    """Returns [(kind, ms, flops, launches)] for every record since profile_start: one
+    contraction launch, or a chain of consecutive launches of one kind timed together."""
     cnt = C.c_int(0)
     ms = (C.c_float * capacity)()
     kind = (C.c_int * capacity)()
     flops = (C.c_longlong * capacity)()
-    N.call("pc_profile_stop", C.byref(cnt), ms, kind, flops, int(capacity))
-    return [(N.KINDS.get(kind[i], str(kind[i])), float(ms[i]), int(flops[i])) for i in range(cnt.value)]
+    launches = (C.c_int * capacity)()
+    N.call("pc_profile_stop", C.byref(cnt), ms, kind, flops, launches, int(capacity))
+    return [(N.KINDS.get(kind[i], str(kind[i])), float(ms[i]), int(flops[i]), int(launches[i]))
+            for i in range(cnt.value)]

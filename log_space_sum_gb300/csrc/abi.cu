@@ -39,15 +39,17 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 
-// Per-launch event pairs of the contraction profiler.
+// Event pairs of the contraction profiler: one per launch, or one per group of launches.
 struct Profiler {
   std::mutex mu;
   bool active = false;
+  bool group_open = false;  // inside profile_group_begin .. _end: launches add no record
   int capacity = 0, count = 0;
   cudaEvent_t* begin = nullptr;
   cudaEvent_t* end = nullptr;
   int* kind = nullptr;
   long long* flops = nullptr;
+  int* launches = nullptr;
   void release() {
     for (int i = 0; i < capacity; ++i) {
       if (begin && begin[i]) cudaEventDestroy(begin[i]);
@@ -57,11 +59,14 @@ struct Profiler {
     delete[] end;
     delete[] kind;
     delete[] flops;
+    delete[] launches;
     begin = end = nullptr;
     kind = nullptr;
     flops = nullptr;
+    launches = nullptr;
     capacity = count = 0;
     active = false;
+    group_open = false;
   }
 } g_prof;
 
@@ -70,7 +75,7 @@ struct Profiler {
 namespace pc {
 
 int profile_begin(cudaStream_t s) {
-  if (!g_prof.active) return -1;
+  if (!g_prof.active || g_prof.group_open) return -1;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   if (!g_prof.active || g_prof.count >= g_prof.capacity) return -1;
   const int i = g_prof.count++;
@@ -82,7 +87,21 @@ void profile_end(int i, cudaStream_t s, int kind, long long flops) {
   if (i < 0) return;
   g_prof.kind[i] = kind;
   g_prof.flops[i] = flops;
+  g_prof.launches[i] = 1;
   cudaEventRecord(g_prof.end[i], s);
+}
+
+int profile_group_begin(cudaStream_t s) {
+  const int i = profile_begin(s);
+  if (i >= 0) g_prof.group_open = true;
+  return i;
+}
+
+void profile_group_end(int i, cudaStream_t s, int kind, long long flops, int launches) {
+  if (i < 0) return;
+  g_prof.group_open = false;
+  profile_end(i, s, kind, flops);
+  g_prof.launches[i] = launches;
 }
 
 pc_status_t set_error(pc_status_t st, const char* fmt, ...) {
@@ -204,6 +223,7 @@ pc_status_t pc_profile_start(int capacity) {
   g_prof.end = new cudaEvent_t[capacity]();
   g_prof.kind = new int[capacity]();
   g_prof.flops = new long long[capacity]();
+  g_prof.launches = new int[capacity]();
   g_prof.capacity = capacity;
   for (int i = 0; i < capacity; ++i) {
     if (cudaEventCreate(&g_prof.begin[i]) != cudaSuccess || cudaEventCreate(&g_prof.end[i]) != cudaSuccess) {
@@ -215,7 +235,7 @@ pc_status_t pc_profile_start(int capacity) {
   return PC_OK;
 }
 
-pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long long* flops, int capacity) {
+pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long long* flops, int* launches, int capacity) {
   pc::clear_error();
   PC_CHECK(count != nullptr, PC_ERR_NULL, "count is NULL");
   std::lock_guard<std::mutex> lock(g_prof.mu);
@@ -228,6 +248,7 @@ pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long long* flops, 
     if (ms) ms[i] = t;
     if (kind) kind[i] = g_prof.kind[i];
     if (flops) flops[i] = g_prof.flops[i];
+    if (launches) launches[i] = g_prof.launches[i];
   }
   *count = n;
   g_prof.release();

@@ -692,6 +692,8 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       if ((st = encode_maps(&mb[i], w.ubm[i], prec, kTileBN)) != PC_OK) return st;
     const dim3 grid = chain_grid;
     const int nkb = num_k_blocks(H, prec);
+    // the chain is one profiler record: events between its launches would break their overlap
+    const int prof = profile_group_begin(s);
     for (int t = T - 2; t >= 0; --t) {
       typename EpiHmmFwd<P>::Params ep{};
       ep.H = H; ep.B = B; ep.T = T; ep.t = t;
@@ -712,6 +714,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
                                                                     PC_KIND_HMM_FWD, 2ll * H * H * B, true)) != PC_OK)
         return st;
     }
+    profile_group_end(prof, s, PC_KIND_HMM_FWD, 2ll * H * H * B * (T - 1), T - 1);
   }
 
   k_hmm_root<<<B, 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, ll, w.rroot);
@@ -731,6 +734,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       if ((st = encode_maps(&mb[i], w.wbm[i], prec, kTileBN)) != PC_OK) return st;
     const dim3 grid = chain_grid;
     const int nkb = num_k_blocks(H, prec);
+    const int prof = profile_group_begin(s);
     for (int t = 0; t <= T - 2; ++t) {
       typename EpiHmmBwd<P>::Params ep{};
       ep.H = H; ep.B = B; ep.T = T; ep.t = t;
@@ -748,6 +752,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
                                                                     PC_KIND_HMM_ELEM, 2ll * H * H * B, true)) != PC_OK)
         return st;
     }
+    profile_group_end(prof, s, PC_KIND_HMM_ELEM, 2ll * H * H * B * (T - 1), T - 1);
     // dE's gather reads the flows of every position: it runs on the side stream beside
     // the stacked dA contraction (which is bound by the tensor cores)
     if (dE) {

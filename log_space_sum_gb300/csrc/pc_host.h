@@ -35,6 +35,10 @@ struct SideStream {
 // Contraction profiler hooks (no-ops unless pc_profile_start is active).
 int profile_begin(cudaStream_t s);
 void profile_end(int slot, cudaStream_t s, int kind, long long flops);
+// One record for a run of `launches` consecutive launches of one kind on stream s (no
+// record of their own): events between them would serialise their programmatic overlap.
+int profile_group_begin(cudaStream_t s);
+void profile_group_end(int slot, cudaStream_t s, int kind, long long flops, int launches);
 
 #define PC_CHECK(cond, st, ...)                 \
   do {                                          \
