@@ -256,9 +256,19 @@ __host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstag
   return s;
 }
 constexpr int kLrSmemLimit = 232448;
-// The deepest ring (and two D tiles) that fits the shared memory of one CTA: large ranks
-// in the TF32 formats take two 128-byte k-blocks per operand row.
+constexpr int kLrSmemHalf = 113 * 1024;  // two CTAs per SM
+// The gradient passes run two CTAs per SM (their consumer warps are latency-bound, so a
+// second CTA's warps fill the issue slots) when a ring of two or more stages fits half the
+// shared memory; otherwise, and for the other passes, the deepest ring (and two D tiles)
+// that fits the shared memory of one CTA: large ranks in the TF32 formats take two
+// 128-byte k-blocks per operand row.
 __host__ __device__ inline LrSmem lr_smem(int P, int mode, int K) {
+  if (mode == kLrGradA || mode == kLrGradB)
+    for (int ns = 3; ns >= 2; --ns)
+      for (int d = 2; d >= 1; --d) {
+        const LrSmem h = lr_smem_plan(P, mode, K, ns, d);
+        if (h.total <= kLrSmemHalf) return h;
+      }
   int nstage = lr_stages(mode), nd = 2;
   LrSmem s = lr_smem_plan(P, mode, K, nstage, nd);
   while (s.total > kLrSmemLimit && nstage > 2) s = lr_smem_plan(P, mode, K, --nstage, nd);
@@ -370,7 +380,7 @@ __device__ __forceinline__ void tile_put_row16(uint8_t* tile, const TileGeo& g, 
 // (The forward's shared memory leaves room for two CTAs per SM; its launch bounds ask the
 // compiler for registers that allow two as well.)
 template <int P, int Mode>
-__global__ void __launch_bounds__(kLrThreadsAll, Mode == kLrFwd ? 2 : 1)
+__global__ void __launch_bounds__(kLrThreadsAll, 2)
     k_lowrank(const __grid_constant__ LrMaps maps, const LrArgs a) {
   constexpr int SF = s_fmt(P), GF = g_fmt(P);
   constexpr bool kGrad = Mode != kLrFwd;
