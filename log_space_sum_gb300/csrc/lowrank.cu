@@ -257,13 +257,13 @@ __host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstag
 }
 constexpr int kLrSmemLimit = 232448;
 constexpr int kLrSmemHalf = 113 * 1024;  // two CTAs per SM
-// The gradient passes run two CTAs per SM (their consumer warps are latency-bound, so a
+// The backward passes run two CTAs per SM (their consumer warps are latency-bound, so a
 // second CTA's warps fill the issue slots) when a ring of two or more stages fits half the
-// shared memory; otherwise, and for the other passes, the deepest ring (and two D tiles)
+// shared memory; otherwise, and for the forward pass, the deepest ring (and two D tiles)
 // that fits the shared memory of one CTA: large ranks in the TF32 formats take two
 // 128-byte k-blocks per operand row.
 __host__ __device__ inline LrSmem lr_smem(int P, int mode, int K) {
-  if (mode == kLrGradA || mode == kLrGradB)
+  if (mode != kLrFwd)
     for (int ns = 3; ns >= 2; --ns)
       for (int d = 2; d >= 1; --d) {
         const LrSmem h = lr_smem_plan(P, mode, K, ns, d);
@@ -558,10 +558,15 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
           vc[jj] = vec[64 + col0 + jj];
         }
       }
-      // chunk c's S slot and stage are no longer read by this warp
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&mbF[c & 1]);
+      // Chunk c's S slot and stage are released (mbF) only after the values read from them
+      // have been used: the stage's next fill is an async-proxy write, which the arrival
+      // alone does not order after these generic-proxy reads.
+      auto release_chunk = [&]() {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mbF[c & 1]);
+      };
       const int w0 = c * kLrChunk + col0;
       if constexpr (Mode == kLrFwd) {
         float cm = -INFINITY;
@@ -580,6 +585,7 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
           Z += tg;
           num = fmaf(tg, va[jj], num);
         }
+        release_chunk();
       } else {
         float dv[16];
 #pragma unroll
@@ -596,6 +602,7 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
           }
           if (own >= own_n) dv[jj] = 0.f;
         }
+        release_chunk();
         // the D slot was read by the gradient MMA of chunk c - ND
         if (c >= ND) {
           const int pc = c - ND;
@@ -694,7 +701,7 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
 // Each stage of the TMA ring holds one sample's A_b tile, its B_b^T chunk and u_b. Warp
 // specialised as k_lowrank: warp 8 issues the copies and the MMAs, warps 0..7 consume.
 template <int P>
-__global__ void __launch_bounds__(kLrThreadsAll, 1)
+__global__ void __launch_bounds__(kLrThreadsAll, 2)
     k_lowrank_stats(const __grid_constant__ LrMaps maps, const LrArgs a) {
   constexpr int SF = s_fmt(P);
   constexpr int esS = fmt_bytes(SF);
@@ -823,9 +830,6 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
       const float* uv = reinterpret_cast<const float*>(stage(b) + L.vec_off) + col0;
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) us[jj] = uv[jj];
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&mbF[b & 1]);
       if (lz > -INFINITY) {
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
@@ -834,6 +838,11 @@ __global__ void __launch_bounds__(kLrThreadsAll, 1)
           wst[jj] = fmaf(fi, gz, wst[jj]);
         }
       }
+      // the stage and S slot are released after their values are used (see k_lowrank)
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mbF[b & 1]);
       lz = nlz;
       fi = nfi;
       fc = nfc;
