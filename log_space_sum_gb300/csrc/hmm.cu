@@ -169,11 +169,13 @@ __device__ __forceinline__ void cs_run(const float* c_s, int col0, float (&cv)[3
 // Stages the CTA's emission block Es(r, c) = E[m0 + r, x_{t,b}] (b = n0 + c) into shared
 // memory (es_index layout): rows and columns outside the problem read 0. The epilogue
 // warps do this while the contraction's K loop runs, so the gathers are off the critical
-// path. Each epilogue warp owns kBM / kEpiWarps columns and issues 8 columns x 4 rows of
-// loads per batch.
+// path. The block is W columns wide (W <= kChainBN); each epilogue warp owns
+// W / kEpiWarps of them and issues 8 columns x 4 rows of loads per batch.
+template <int W>
 __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, int H, int B, int m0, int n0,
                                                 const int* tok_s, float* Es, int et) {
-  constexpr int kCols = kBM / kEpiWarps;  // columns staged by one epilogue warp
+  static_assert(W <= kChainBN && W % (8 * kEpiWarps) == 0, "whole batches of 8 columns per warp");
+  constexpr int kCols = W / kEpiWarps;  // columns staged by one epilogue warp
   const int lane = et & 31;
   const int c_begin = (et >> 5) * kCols;
 #pragma unroll 1
@@ -234,9 +236,7 @@ __device__ __forceinline__ void stage_batch_col(uint8_t* stage, int row, int col
 }
 
 // ----------------------------------------------------------- forward epilogue
-template <int P>
-struct EpiHmmFwd {
-  struct Params {
+struct HmmFwdParams {
     int H, B, T, t;
     const int* tokens;
     const float* Et;
@@ -252,7 +252,13 @@ struct EpiHmmFwd {
     long long un_ld;
     size_t un_lo;
     float* U0;               // u_0 float32 [B][H] (t = 0 only)
-  };
+};
+
+// W: the columns one CTA's epilogue finishes (kChainBN, or half of it for 128-wide
+// split-K tiles).
+template <int P, int W = kChainBN>
+struct EpiHmmFwd {
+  using Params = HmmFwdParams;
   static constexpr bool kTranspose = false;
   static constexpr int kSliceBF16 = 0;
   // the 3xTF32 ring needs the room: it gathers emissions directly instead
@@ -262,7 +268,7 @@ struct EpiHmmFwd {
   __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
     float* c_s = reinterpret_cast<float*>(smem) + kChainBN;
-    for (int c = et; c < kChainBN; c += kEpiThreads) {
+    for (int c = et; c < W; c += kEpiThreads) {
       const int b = n0 + c;
       int tok = 0;
       float cv = 0.f;
@@ -277,7 +283,7 @@ struct EpiHmmFwd {
     }
     if constexpr (kStageE) {
       epilogue_bar_sync();
-      stage_emissions(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
+      stage_emissions<W>(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
     }
   }
 
@@ -350,7 +356,7 @@ struct EpiHmmFwd {
     if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
   }
   __device__ static void store_staged(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
-    const int nr = min(kBM, p.H - m0), nc = min(kChainBN, p.B - n0);
+    const int nr = min(kBM, p.H - m0), nc = min(W, p.B - n0);
     if (p.ubm)
       stage_tile_store_bf16(stage + kNodeTileBytes, kBatchPitch,
                             static_cast<__nv_bfloat16*>(p.ubm) + static_cast<long long>(n0) * p.ubm_ld + m0,
@@ -430,9 +436,7 @@ __global__ void k_hmm_root_flows(int H, int B, int T, const int* __restrict__ to
 }
 
 // ---------------------------------------------------------- backward epilogue
-template <int P>
-struct EpiHmmBwd : EpiNoHooks {
-  struct Params {
+struct HmmBwdParams {
     int H, B, T, t;
     const int* tokens;
     const float* Et;
@@ -447,14 +451,19 @@ struct EpiHmmBwd : EpiNoHooks {
     void* wn;                // w_{t+1} node-major at column (t+1) B for dA (NULL if unused)
     long long wn_ld;
     size_t wn_lo;
-  };
+};
+
+// W as in EpiHmmFwd.
+template <int P, int W = kChainBN>
+struct EpiHmmBwd : EpiNoHooks {
+  using Params = HmmBwdParams;
   static constexpr bool kStageE = P != kTF32x3;
   static constexpr int kSmemBytes = kChainBN * 8 + (kStageE ? kChainBN * kBM * 4 : 0);
 
   __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
     float* c_s = reinterpret_cast<float*>(smem) + kChainBN;
-    for (int c = et; c < kChainBN; c += kEpiThreads) {
+    for (int c = et; c < W; c += kEpiThreads) {
       const int b = n0 + c;
       tok_s[c] = b < p.B ? p.tokens[static_cast<long long>(b) * p.T + p.t + 1] : 0;
       c_s[c] = b < p.B ? p.cf[static_cast<long long>(p.t + 1) * p.B + b] : 0.f;
@@ -462,7 +471,7 @@ struct EpiHmmBwd : EpiNoHooks {
     if constexpr (kStageE) {
       if (p.wbm) {
         epilogue_bar_sync();
-        stage_emissions(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
+        stage_emissions<W>(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
       }
     }
   }
@@ -520,7 +529,7 @@ struct EpiHmmBwd : EpiNoHooks {
       stage_tile_load_bf16_async(stage, kNodePitch,
                            static_cast<const __nv_bfloat16*>(p.un) + static_cast<long long>(m0) * p.un_ld +
                                static_cast<long long>(p.t) * p.B + n0,
-                           p.un_ld, min(kBM, p.H - m0), min(kChainBN, p.B - n0), et);
+                           p.un_ld, min(kBM, p.H - m0), min(W, p.B - n0), et);
   }
   __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
                                       float (&v)[32], uint8_t* smem, uint8_t* stage) {
@@ -557,7 +566,7 @@ struct EpiHmmBwd : EpiNoHooks {
   }
   __device__ static void store_staged(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
     if (!p.wbm) return;
-    const int nr = min(kBM, p.H - m0), nc = min(kChainBN, p.B - n0);
+    const int nr = min(kBM, p.H - m0), nc = min(W, p.B - n0);
     stage_tile_store_bf16(stage + kNodeTileBytes, kBatchPitch,
                           static_cast<__nv_bfloat16*>(p.wbm) + static_cast<long long>(n0) * p.wbm_ld + m0,
                           p.wbm_ld, nc, nr, et);
@@ -679,17 +688,23 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   }
 
   // The bf16 chain contractions run as split-K pairs of 128 x 256 tiles (k_umma_gemm,
-  // kSplit); each CTA's epilogue still finishes 128 x kChainBN.
+  // kSplit); each CTA's epilogue still finishes 128 x kChainBN. Where that gives fewer
+  // than kNarrowBelow CTAs (a small H: short K loops, the fixed costs dominate), the
+  // pairs take 128 x 128 tiles instead: twice the CTAs, half the exchange and epilogue
+  // per CTA.
   constexpr bool kSplitChain = P == kBF16;
   constexpr int kTileBN = kSplitChain ? 2 * kChainBN : kChainBN;
-  const dim3 chain_grid((kSplitChain ? 2 : 1) * cdiv(H, kBM), cdiv(B, kTileBN), 1);
+  constexpr long long kNarrowBelow = 96;
+  const bool narrow = kSplitChain && 2ll * cdiv(H, kBM) * cdiv(B, kTileBN) < kNarrowBelow;
+  const int tile_bn = narrow ? kChainBN : kTileBN;
+  const dim3 chain_grid((kSplitChain ? 2 : 1) * cdiv(H, kBM), cdiv(B, tile_bn), 1);
 
   // forward chain: S_t for t = T-2 .. 0
   if (T >= 2) {
     OperandMaps ma, mb[2];
     if ((st = encode_maps(&ma, w.Aop, prec, kBM)) != PC_OK) return st;
     for (int i = 0; i < 2; ++i)
-      if ((st = encode_maps(&mb[i], w.ubm[i], prec, kTileBN)) != PC_OK) return st;
+      if ((st = encode_maps(&mb[i], w.ubm[i], prec, tile_bn)) != PC_OK) return st;
     const dim3 grid = chain_grid;
     const int nkb = num_k_blocks(H, prec);
     // the chain is one profiler record: events between its launches would break their overlap
@@ -710,9 +725,18 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       const OperandMaps& b = mb[(t + 1) & 1];
       // a_early: the A operand was converted before k_hmm_leaf, the kernel that precedes
       // the first layer, so no kernel still running when a layer starts writes it.
-      if ((st = launch_gemm<P, kTileBN, EpiHmmFwd<P>, kSplitChain>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
-                                                                    PC_KIND_HMM_FWD, 2ll * H * H * B, true)) != PC_OK)
-        return st;
+      if constexpr (kSplitChain) {
+        if (narrow)
+          st = launch_gemm<P, kChainBN, EpiHmmFwd<P, kChainBN / 2>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                                          PC_KIND_HMM_FWD, 2ll * H * H * B, true);
+        else
+          st = launch_gemm<P, kTileBN, EpiHmmFwd<P>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                            PC_KIND_HMM_FWD, 2ll * H * H * B, true);
+      } else {
+        st = launch_gemm<P, kTileBN, EpiHmmFwd<P>, false>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                           PC_KIND_HMM_FWD, 2ll * H * H * B, true);
+      }
+      if (st != PC_OK) return st;
     }
     profile_group_end(prof, s, PC_KIND_HMM_FWD, 2ll * H * H * B * (T - 1), T - 1);
   }
@@ -731,7 +755,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
     OperandMaps ma, mb[2];
     if ((st = encode_maps(&ma, w.Atop, prec, kBM)) != PC_OK) return st;
     for (int i = 0; i < 2; ++i)
-      if ((st = encode_maps(&mb[i], w.wbm[i], prec, kTileBN)) != PC_OK) return st;
+      if ((st = encode_maps(&mb[i], w.wbm[i], prec, tile_bn)) != PC_OK) return st;
     const dim3 grid = chain_grid;
     const int nkb = num_k_blocks(H, prec);
     const int prof = profile_group_begin(s);
@@ -748,9 +772,18 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       }
       const OperandMaps& b = mb[t & 1];
       // a_early: the transposed A operand was converted before the forward chain
-      if ((st = launch_gemm<P, kTileBN, EpiHmmBwd<P>, kSplitChain>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
-                                                                    PC_KIND_HMM_ELEM, 2ll * H * H * B, true)) != PC_OK)
-        return st;
+      if constexpr (kSplitChain) {
+        if (narrow)
+          st = launch_gemm<P, kChainBN, EpiHmmBwd<P, kChainBN / 2>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                                          PC_KIND_HMM_ELEM, 2ll * H * H * B, true);
+        else
+          st = launch_gemm<P, kTileBN, EpiHmmBwd<P>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                            PC_KIND_HMM_ELEM, 2ll * H * H * B, true);
+      } else {
+        st = launch_gemm<P, kTileBN, EpiHmmBwd<P>, false>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
+                                                           PC_KIND_HMM_ELEM, 2ll * H * H * B, true);
+      }
+      if (st != PC_OK) return st;
     }
     profile_group_end(prof, s, PC_KIND_HMM_ELEM, 2ll * H * H * B * (T - 1), T - 1);
     // dE's gather reads the flows of every position: it runs on the side stream beside
