@@ -144,7 +144,7 @@ pc_status_t SideStream::fork(cudaStream_t main) {
 pc_status_t SideStream::join(cudaStream_t main) { return stream_after(main, s); }
 
 pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision_t p,
-                               int box_rows, int part, bool swizzle) {
+                               int box_rows, int part, bool swizzle, long long group_stride) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -157,7 +157,8 @@ pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision
   const int es = operand_elem_bytes(p);
   uint8_t* base = static_cast<uint8_t*>(op.ptr) + (part ? op.lo_elems * size_t(es) : 0);
   const cuuint64_t dims[3] = {cuuint64_t(op.cols), cuuint64_t(op.rows), cuuint64_t(op.groups)};
-  const cuuint64_t strides[2] = {cuuint64_t(op.ld) * es, cuuint64_t(op.ld) * op.rows * es};
+  const cuuint64_t strides[2] = {cuuint64_t(op.ld) * es,
+                                 cuuint64_t(group_stride > 0 ? group_stride : op.ld * op.rows) * es};
   const cuuint32_t box[3] = {cuuint32_t(128 / es), cuuint32_t(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = p == PC_PREC_AUTO  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16

@@ -578,12 +578,64 @@ struct EpiHmmBwd : EpiNoHooks {
   }
 };
 
+// ------------------------------------------------------- dA over K ranges
+// The stacked dA contraction has K = (T-1) B but only cdiv(H,128) x cdiv(H,BN) output
+// tiles: for a small H too few CTAs for the GPU. It then runs over S consecutive K ranges
+// (blockIdx.z; the operands' tensor maps take the ranges as groups) into S float32
+// partial products, which k_dA_reduce adds in range order and scales by A.
+constexpr int kParamSplitMax = 4;
+constexpr long long kParamSplitCtas = 148;  // CTAs the split may bring the launch to
+
+int param_split(int H, int T, int B, pc_precision_t prec) {
+  if (T < 2) return 1;
+  const long long K = static_cast<long long>(T - 1) * B;
+  const int kb = 128 / operand_elem_bytes(prec);  // K elements per ring block
+  const long long tiles = static_cast<long long>(cdiv(H, kBM)) * cdiv(H, prec == PC_PREC_AUTO ? 256 : 128);
+  for (int S = kParamSplitMax; S >= 2; S /= 2)
+    if (tiles * S <= kParamSplitCtas && K % (static_cast<long long>(S) * kb) == 0 && K / S >= 8ll * kb) return S;
+  return 1;
+}
+
+// dA[i] = (accumulate ? dA[i] : 0) + A[i] (part[0][i] + part[1][i] + ...), float4 runs
+// where n is a multiple of 4.
+__global__ void k_dA_reduce(int S, long long n, const float* __restrict__ part, const float* __restrict__ A,
+                            float* __restrict__ dA, int accumulate) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  if ((n & 3) == 0) {
+    const long long n4 = n >> 2;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+      float4 sum = reinterpret_cast<const float4*>(part)[i];
+      for (int g = 1; g < S; ++g) {
+        const float4 x = reinterpret_cast<const float4*>(part + g * n)[i];
+        sum.x += x.x;
+        sum.y += x.y;
+        sum.z += x.z;
+        sum.w += x.w;
+      }
+      const float4 a = reinterpret_cast<const float4*>(A)[i];
+      float4 r = make_float4(a.x * sum.x, a.y * sum.y, a.z * sum.z, a.w * sum.w);
+      if (accumulate) {
+        const float4 d = reinterpret_cast<const float4*>(dA)[i];
+        r = make_float4(d.x + r.x, d.y + r.y, d.z + r.z, d.w + r.w);
+      }
+      reinterpret_cast<float4*>(dA)[i] = r;
+    }
+  } else {
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+      float sum = part[i];
+      for (int g = 1; g < S; ++g) sum += part[g * n + i];
+      dA[i] = (accumulate ? dA[i] : 0.f) + A[i] * sum;
+    }
+  }
+}
+
 // -------------------------------------------------------------- workspace
 struct HmmWs {
   Operand Aop, Atop, ubm[2], wbm[2], un, wn;
   float *Et, *rs, *emax, *emax_rs, *U0, *umax, *cf, *rroot, *dEt, *fbm;
   int *tok_count, *tok_offset, *tok_order;
   double* logc;
+  float* dA_part;  // param_split > 1: the K ranges' partial products [S][H][H]
 };
 
 size_t carve_hmm(void* base, pc_precision_t p, int H, int T, int V, int B, bool flows, bool chain,
@@ -608,6 +660,8 @@ size_t carve_hmm(void* base, pc_precision_t p, int H, int T, int V, int B, bool 
     w->wbm[1] = c.operand(p, 1, B, H);
     w->un = c.operand(p, 1, H, static_cast<long long>(T - 1) * B);
     w->wn = c.operand(p, 1, H, static_cast<long long>(T - 1) * B);
+    const int S = param_split(H, T, B, p);
+    if (S > 1) w->dA_part = static_cast<float*>(c.take(size_t(S) * H * H * 4));
   }
   if (flows && want_dE) {
     w->dEt = static_cast<float*>(c.take(size_t(V) * H * 4));
@@ -798,12 +852,39 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       OperandMaps pa, pb;
       if ((st = encode_maps(&pa, w.wn, prec, kBM)) != PC_OK) return st;
       if ((st = encode_maps(&pb, w.un, prec, kParamBN)) != PC_OK) return st;
-      EpiThetaScale::Params ep{dA, A, H, H, accumulate};
-      if ((st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), 1), pa.hi, pa.lo,
-                                                        pb.hi, pb.lo, num_k_blocks(static_cast<long long>(T - 1) * B, prec),
-                                                        ep, s, PC_KIND_HMM_PARAM,
-                                                        2ll * H * H * (T - 1) * B)) != PC_OK)
-        return st;
+      const int S = param_split(H, T, B, prec);
+      const long long K = static_cast<long long>(T - 1) * B;
+      if (S > 1) {
+        // K-range views of the two operands: S groups of K/S columns, K/S elements apart
+        OperandMaps va, vb;
+        Operand oa = w.wn, ob = w.un;
+        oa.cols = ob.cols = K / S;
+        oa.groups = ob.groups = S;
+        for (int part = 0; part < (prec == PC_PREC_FP32 ? 2 : 1); ++part) {
+          if ((st = encode_operand_map(part ? &va.lo : &va.hi, oa, prec, kBM, part, true, K / S)) != PC_OK) return st;
+          if ((st = encode_operand_map(part ? &vb.lo : &vb.hi, ob, prec, kParamBN, part, true, K / S)) != PC_OK)
+            return st;
+        }
+        if (prec != PC_PREC_FP32) {
+          va.lo = va.hi;
+          vb.lo = vb.hi;
+        }
+        EpiStoreF32::Params ep{w.dA_part, H, H, H, 0, nullptr, nullptr, static_cast<long long>(H) * H};
+        if ((st = launch_gemm<P, kParamBN, EpiStoreF32>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), S), va.hi, va.lo, vb.hi,
+                                                        vb.lo, num_k_blocks(K / S, prec), ep, s, PC_KIND_HMM_PARAM,
+                                                        2ll * H * H * K)) != PC_OK)
+          return st;
+        const long long n = static_cast<long long>(H) * H;
+        k_dA_reduce<<<static_cast<unsigned>(std::min<long long>(cdiv(n, 4 * 256), 4 * 148)), 256, 0, s>>>(
+            S, n, w.dA_part, A, dA, accumulate);
+        PC_LAUNCH_CHECK();
+      } else {
+        EpiThetaScale::Params ep{dA, A, H, H, accumulate};
+        if ((st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), 1), pa.hi, pa.lo,
+                                                          pb.hi, pb.lo, num_k_blocks(K, prec), ep, s, PC_KIND_HMM_PARAM,
+                                                          2ll * H * H * K)) != PC_OK)
+          return st;
+      }
     }
     if (dE && (st = side.join(s)) != PC_OK) return st;
   } else {

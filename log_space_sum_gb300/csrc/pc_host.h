@@ -118,8 +118,10 @@ struct Carver {
 
 // 3-D tensor map over an Operand: dims {cols (K), rows, groups}, box {128 bytes of K,
 // box_rows, 1}, 128-byte swizzle (or none), zero fill outside the tensor. part 1 = the lo
-// half.
+// half. group_stride: elements between groups (0: rows x ld); a K-split view takes
+// groups that are consecutive K ranges of the same rows (op.cols = the range's length,
+// group_stride = op.cols).
 pc_status_t encode_operand_map(CUtensorMap* map, const Operand& op, pc_precision_t p,
-                               int box_rows, int part, bool swizzle = true);
+                               int box_rows, int part, bool swizzle = true, long long group_stride = 0);
 
 }  // namespace pc

@@ -383,8 +383,9 @@ struct EpiStoreF32 : EpiNoHooks {
     int M, N, accumulate;
     const float* rscale = nullptr;  // as EpiThetaScale's
     const float* cscale = nullptr;
+    long long gstride = 0;          // elements between the outputs of groups (blockIdx.z)
   };
-  __device__ static void apply(const Params& p, int, int m0, int n0, int row, int col0, float (&v)[32], uint8_t*,
+  __device__ static void apply(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32], uint8_t*,
                                float* tbuf) {
     float w[32];
     warp_transpose32(v, w, tbuf);
@@ -392,7 +393,7 @@ struct EpiStoreF32 : EpiNoHooks {
     const int i0 = m0 + row - lane;
     const int j = n0 + col0 + lane;
     if (j >= p.N) return;
-    float* Dp = p.D + static_cast<long long>(i0) * p.ld + j;
+    float* Dp = p.D + g * p.gstride + static_cast<long long>(i0) * p.ld + j;
     if (p.rscale || p.cscale) scale_rows(p.rscale, p.cscale, i0, j, p.M, w);
 #pragma unroll
     for (int h = 0; h < 32; h += 16) {
