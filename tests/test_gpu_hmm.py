@@ -83,6 +83,37 @@ def test_accumulate_adds_flows():
         torch.testing.assert_close(b, 2 * a, rtol=1e-6, atol=0)
 
 
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("H", [300, 129])
+def test_small_state_space_paths(H, mode):
+    # H = 300 or 129 at batch 256: 128 x 128 split-K tiles on the chain (too few 128 x 256
+    # pairs), and the dA contraction over K ranges (K = 8 x 256 divides into 4 ranges of
+    # whole ring blocks); H = 129 leaves H^2 odd for the range sum's scalar path. Then
+    # accumulation through the range sum doubles dA.
+    d = hmm_inputs(H, 9, 23, 256, seed=90 + H)
+    rl, rpi, rA, rE = _oracle(d)
+    ll, dpi, dA, dE = _gpu_run(d, mode)
+    errs = (ll_err(ll, rl), flow_err(dpi, rpi), flow_err(dA, rA), flow_err(dE, rE))
+    print(f"hmm {H}x9 B256 {mode}: ll {errs[0]:.3e} dpi {errs[1]:.3e} dA {errs[2]:.3e} dE {errs[3]:.3e}")
+    assert errs[0] <= LL_TOL[mode] and max(errs[1:]) <= FLOW_TOL[mode], errs
+    t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda() for k in ("tokens", "pi", "A", "E")}
+    base = torch.from_numpy(dA).cuda()
+    _, _, dA2, _ = pc.hmm_fwd_bwd(t["tokens"], t["pi"], t["A"], t["E"], precision=mode, dA=base.clone(),
+                                  accumulate=True)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(dA2, 2 * base, rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("mode", ["auto", "fp32"])
+def test_small_state_space_ragged_batch(mode):
+    # 128 x 128 split-K tiles with a ragged last sample tile (B = 200)
+    d = hmm_inputs(256, 4, 17, 200, seed=95)
+    rl, rpi, rA, rE = _oracle(d)
+    ll, dpi, dA, dE = _gpu_run(d, mode)
+    assert ll_err(ll, rl) <= LL_TOL[mode]
+    assert max(flow_err(dpi, rpi), flow_err(dA, rA), flow_err(dE, rE)) <= FLOW_TOL[mode]
+
+
 @pytest.fixture(scope="module")
 def hmm128():
     d = hmm(128)
