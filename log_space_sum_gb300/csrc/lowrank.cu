@@ -177,23 +177,28 @@ __global__ void k_lr_row_factors(int M, int B, const float* __restrict__ out, co
 
 // Operand copy in format F: dst[g][r][c] (rows ld elements apart, zero beyond C) =
 // src[g*sg + r*sr + c*sc], rounded to bf16 / TF32 (hi, and lo = the rounded remainder).
+// One row (g, r) per warp row of the block: the row's index is split once per row, not
+// per element.
 template <int F>
 __global__ void k_lr_to_op(const float* __restrict__ src, long long sg, long long sr, long long sc, int G, int R,
                            int C, void* __restrict__ hi, void* __restrict__ lo, long long ld) {
-  const long long n = static_cast<long long>(G) * R * ld;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long c = idx % ld, gr = idx / ld;
-    const long long r = gr % R, g = gr / R;
-    const float v = c < C ? src[g * sg + r * sr + c * sc] : 0.f;
-    if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(v);
-      static_cast<__nv_bfloat16*>(hi)[idx] = h;
-      if constexpr (F == kFmtBF16x2) static_cast<__nv_bfloat16*>(lo)[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
-    } else {
-      const float h = tf32_rna(v);
-      static_cast<float*>(hi)[idx] = h;
-      if constexpr (F == kFmtTF32x2) static_cast<float*>(lo)[idx] = tf32_rna(v - h);
+  const long long rows = static_cast<long long>(G) * R;
+  for (long long gr = static_cast<long long>(blockIdx.x) * blockDim.y + threadIdx.y; gr < rows;
+       gr += static_cast<long long>(gridDim.x) * blockDim.y) {
+    const long long g = gr / R, r = gr - g * R;
+    const float* s0 = src + g * sg + r * sr;
+    for (long long c = threadIdx.x; c < ld; c += blockDim.x) {
+      const long long idx = gr * ld + c;
+      const float v = c < C ? s0[c * sc] : 0.f;
+      if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        static_cast<__nv_bfloat16*>(hi)[idx] = h;
+        if constexpr (F == kFmtBF16x2) static_cast<__nv_bfloat16*>(lo)[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
+      } else {
+        const float h = tf32_rna(v);
+        static_cast<float*>(hi)[idx] = h;
+        if constexpr (F == kFmtTF32x2) static_cast<float*>(lo)[idx] = tf32_rna(v - h);
+      }
     }
   }
 }
@@ -936,10 +941,10 @@ pc_status_t lr_attr(Kern kern, int smem) {
 template <int F>
 pc_status_t to_op(const float* src, long long sg, long long sr, long long sc, int G, int R, int C, const LrOp& o,
                   cudaStream_t s) {
-  const long long n = static_cast<long long>(G) * R * o.part[0].ld;
-  const int blocks = static_cast<int>(std::min<long long>(cdiv(n, 256), 4096));
-  k_lr_to_op<F><<<blocks, 256, 0, s>>>(src, sg, sr, sc, G, R, C, o.part[0].ptr, o.parts > 1 ? o.part[1].ptr : nullptr,
-                                       o.part[0].ld);
+  const long long rows = static_cast<long long>(G) * R;
+  const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, 8), 8192));
+  k_lr_to_op<F><<<blocks, dim3(32, 8), 0, s>>>(src, sg, sr, sc, G, R, C, o.part[0].ptr,
+                                               o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
   PC_LAUNCH_CHECK();
   return PC_OK;
 }
