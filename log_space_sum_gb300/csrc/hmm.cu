@@ -140,14 +140,16 @@ __global__ void k_hmm_leaf(int H, int B, int T, const int* __restrict__ tokens,
   }
 }
 
-// The staged emission block holds row r (a state) as 128 floats whose 16-byte pieces are
-// swizzled by r: an epilogue thread reads its row's 32 columns with 8 vector loads, and
-// the 32 rows of a warp spread over all banks.
-__device__ __forceinline__ int es_index(int r, int c) { return r * kChainBN + (((c >> 2) ^ (r & 7)) << 2) + (c & 3); }
+// The staged emission block holds row r (a state) as Pitch floats whose 16-byte pieces
+// are swizzled by r: an epilogue thread reads its row's 32 columns with 8 vector loads,
+// and the 32 rows of a warp spread over all banks.
+template <int Pitch = kChainBN>
+__device__ __forceinline__ int es_index(int r, int c) { return r * Pitch + (((c >> 2) ^ (r & 7)) << 2) + (c & 3); }
+template <int Pitch = kChainBN>
 __device__ __forceinline__ void es_run(const float* Es, int row, int col0, float (&e)[32]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float4 x = *reinterpret_cast<const float4*>(Es + es_index(row, col0 + 4 * j));
+    const float4 x = *reinterpret_cast<const float4*>(Es + es_index<Pitch>(row, col0 + 4 * j));
     e[4 * j] = x.x;
     e[4 * j + 1] = x.y;
     e[4 * j + 2] = x.z;
@@ -171,7 +173,7 @@ __device__ __forceinline__ void cs_run(const float* c_s, int col0, float (&cv)[3
 // warps do this while the contraction's K loop runs, so the gathers are off the critical
 // path. The block is W columns wide (W <= kChainBN); each epilogue warp owns
 // W / kEpiWarps of them and issues 8 columns x 4 rows of loads per batch.
-template <int W>
+template <int W, int Pitch = kChainBN>
 __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, int H, int B, int m0, int n0,
                                                 const int* tok_s, float* Es, int et) {
   static_assert(W <= kChainBN && W % (8 * kEpiWarps) == 0, "whole batches of 8 columns per warp");
@@ -194,9 +196,42 @@ __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, in
 #pragma unroll
     for (int c = 0; c < 8; ++c)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) Es[es_index(lane + 32 * i, cb + c)] = vals[c][i];
+      for (int i = 0; i < 4; ++i) Es[es_index<Pitch>(lane + 32 * i, cb + c)] = vals[c][i];
   }
 }
+
+// The same block gathered with asynchronous 4-byte copies (zero-filled outside the
+// problem), which the issuing thread completes with cp_async_wait_all before a barrier.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+template <int W, int Pitch>
+__device__ __forceinline__ void stage_emissions_async(const float* __restrict__ Et, int H, int B, int m0, int n0,
+                                                      const int* tok_s, float* Es, int et) {
+  static_assert(W % kEpiWarps == 0, "whole columns per warp");
+  constexpr int kCols = W / kEpiWarps;
+  const int lane = et & 31;
+  const int c_begin = (et >> 5) * kCols;
+#pragma unroll 1
+  for (int c = c_begin; c < c_begin + kCols; ++c) {
+    const bool bin = n0 + c < B;
+    const float* src = Et + static_cast<long long>(tok_s[c]) * H + m0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = lane + 32 * i;
+      const bool in = bin && m0 + r < H;
+      cp_async_4(Es + es_index<Pitch>(r, c), in ? src + r : Et, in ? 4u : 0u);
+    }
+  }
+}
+
+// The wide bf16 split-K tiles (128 x 256, epilogue width kChainBN) stage only the first
+// kEsLoCols columns of the emission block before the K loop, so that the ring keeps four
+// stages; the other columns are gathered into the idle ring behind the staged tiles
+// while the partial sums are exchanged.
+constexpr int kEsLoCols = kChainBN / 2;
+constexpr int kEsHiBytes = (kChainBN - kEsLoCols) * kBM * 4;
 
 // Column maxima of the warp's 32 x 32 block of non-negative values (thread = row, v[c] =
 // column c): lane l returns the maximum of column l. Non-negative floats order like
@@ -263,7 +298,10 @@ struct EpiHmmFwd {
   static constexpr int kSliceBF16 = 0;
   // the 3xTF32 ring needs the room: it gathers emissions directly instead
   static constexpr bool kStageE = P != kTF32x3;
-  static constexpr int kSmemBytes = kChainBN * 4 * 2 + (kStageE ? kChainBN * kBM * 4 : 0);
+  static constexpr bool kEsSplit = P == kBF16 && W == kChainBN;  // see kEsLoCols
+  static constexpr int kEsLo = kEsSplit ? kEsLoCols : W;         // columns staged before the K loop
+  static constexpr int kEsPitch = kEsSplit ? kEsLoCols : kChainBN;
+  static constexpr int kSmemBytes = kChainBN * 4 * 2 + (kStageE ? kEsPitch * kBM * 4 : 0);
 
   __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
@@ -283,7 +321,8 @@ struct EpiHmmFwd {
     }
     if constexpr (kStageE) {
       epilogue_bar_sync();
-      stage_emissions<W>(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
+      stage_emissions<kEsLo, kEsPitch>(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN,
+                                       et);
     }
   }
 
@@ -296,6 +335,7 @@ struct EpiHmmFwd {
     const int k = m0 + row;
     const bool kin = k < p.H;
     const int nvalid = kin ? min(32, p.B - (n0 + col0)) : 0;
+    static_assert(!kEsSplit, "the split emission block is read by apply_staged");
     float e[32], cv[32];
     if constexpr (kStageE) {
       es_run(Es, row, col0, e);
@@ -326,12 +366,20 @@ struct EpiHmmFwd {
   }
 
   // Split-K form of apply: u_t goes to the staged tiles instead of global memory.
-  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes;
+  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes + (kEsSplit ? kEsHiBytes : 0);
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
   // the batch-major tile is written only in apply_staged: the exchange's scratch until then
   static constexpr int kSplitScratchOffset = kNodeTileBytes;
   static_assert(kSplitScratchOffset % 16 == 0, "16-byte scratch rows");
-  __device__ static void after_mma(const Params&, int, int, int, int, uint8_t*) {}
+  __device__ static float* es_hi(uint8_t* stage) {
+    return reinterpret_cast<float*>(stage + kNodeTileBytes + kBatchTileBytes);
+  }
+  __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* smem, uint8_t* stage) {
+    if constexpr (kEsSplit)
+      stage_emissions_async<kChainBN - kEsLoCols, kEsLoCols>(p.Et, p.H, p.B, m0, n0 + kEsLoCols,
+                                                             reinterpret_cast<const int*>(smem) + kEsLoCols,
+                                                             es_hi(stage), et);
+  }
   __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
                                       float (&v)[32], uint8_t* smem, uint8_t* stage) {
     static_assert(P == kBF16 && kStageE, "staged chain tiles hold bf16 operands");
@@ -340,7 +388,10 @@ struct EpiHmmFwd {
     const int k = m0 + row;
     const int nvalid = k < p.H ? min(32, p.B - (n0 + col0)) : 0;
     float e[32], cv[32];
-    es_run(Es, row, col0, e);
+    if (col0 < kEsLo)
+      es_run<kEsPitch>(Es, row, col0, e);
+    else
+      es_run<kEsLoCols>(es_hi(stage), row, col0 - kEsLoCols, e);
     cs_run(c_s, col0, cv);
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * v[c] * cv[c] : 0.f;
@@ -458,7 +509,10 @@ template <int P, int W = kChainBN>
 struct EpiHmmBwd : EpiNoHooks {
   using Params = HmmBwdParams;
   static constexpr bool kStageE = P != kTF32x3;
-  static constexpr int kSmemBytes = kChainBN * 8 + (kStageE ? kChainBN * kBM * 4 : 0);
+  static constexpr bool kEsSplit = P == kBF16 && W == kChainBN;  // see kEsLoCols
+  static constexpr int kEsLo = kEsSplit ? kEsLoCols : W;
+  static constexpr int kEsPitch = kEsSplit ? kEsLoCols : kChainBN;
+  static constexpr int kSmemBytes = kChainBN * 8 + (kStageE ? kEsPitch * kBM * 4 : 0);
 
   __device__ static void prepare(const Params& p, int, int m0, int n0, int et, uint8_t* smem) {
     int* tok_s = reinterpret_cast<int*>(smem);
@@ -471,7 +525,8 @@ struct EpiHmmBwd : EpiNoHooks {
     if constexpr (kStageE) {
       if (p.wbm) {
         epilogue_bar_sync();
-        stage_emissions<W>(p.Et, p.H, p.B, m0, n0, tok_s, reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
+        stage_emissions<kEsLo, kEsPitch>(p.Et, p.H, p.B, m0, n0, tok_s,
+                                         reinterpret_cast<float*>(smem) + 2 * kChainBN, et);
       }
     }
   }
@@ -491,6 +546,7 @@ struct EpiHmmBwd : EpiNoHooks {
     if (p.fbm)
       load_operand_run<P>(p.un, static_cast<size_t>(j * p.un_ld + static_cast<long long>(p.t) * p.B + n0 + col0),
                           p.un_lo, u, nvalid);
+    static_assert(!kEsSplit, "the split emission block is read by apply_staged");
     if (p.wbm) {
       if constexpr (kStageE) {
         es_run(Es, row, col0, e);
@@ -519,12 +575,20 @@ struct EpiHmmBwd : EpiNoHooks {
   // Split-K form of apply: u_{t+1} is staged (coalesced, asynchronous: the copies complete
   // while the partial sums are exchanged);
   // w_{t+1} goes to the staged tiles, the node-major one in place of u.
-  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes;
+  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes + (kEsSplit ? kEsHiBytes : 0);
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
   // the batch-major tile is written only in apply_staged: the exchange's scratch until then
   static constexpr int kSplitScratchOffset = kNodeTileBytes;
   static_assert(kSplitScratchOffset % 16 == 0, "16-byte scratch rows");
-  __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
+  __device__ static float* es_hi(uint8_t* stage) {
+    return reinterpret_cast<float*>(stage + kNodeTileBytes + kBatchTileBytes);
+  }
+  __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* smem, uint8_t* stage) {
+    if constexpr (kEsSplit)
+      if (p.wbm)
+        stage_emissions_async<kChainBN - kEsLoCols, kEsLoCols>(p.Et, p.H, p.B, m0, n0 + kEsLoCols,
+                                                               reinterpret_cast<const int*>(smem) + kEsLoCols,
+                                                               es_hi(stage), et);
     if (p.fbm)
       stage_tile_load_bf16_async(stage, kNodePitch,
                            static_cast<const __nv_bfloat16*>(p.un) + static_cast<long long>(m0) * p.un_ld +
@@ -557,7 +621,10 @@ struct EpiHmmBwd : EpiNoHooks {
     }
     if (!p.wbm) return;
     float e[32], cv[32];
-    es_run(Es, row, col0, e);
+    if (col0 < kEsLo)
+      es_run<kEsPitch>(Es, row, col0, e);
+    else
+      es_run<kEsLoCols>(es_hi(stage), row, col0 - kEsLoCols, e);
     cs_run(c_s, col0, cv);
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * cv[c] * v[c] : 0.f;
