@@ -10,6 +10,7 @@
 //                   e      = exp(x - m_b) * D
 //        parameter  D[i,j] = sum_b w[i,b] u[j,b]
 //                   F      = theta * D
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -176,13 +177,71 @@ struct EpiLayerElem : EpiNoHooks {
 
 constexpr int kLayerBN = 128;
 
+// ------------------------------------------------- contraction over K ranges
+// A single group's forward and element-flow contractions have cdiv(rows,128) x
+// cdiv(B,128) output tiles: at M = N = 1024, B = 128 eight CTAs, each over all of K. They
+// then run over S consecutive K ranges (blockIdx.z; the operands' tensor maps take the
+// ranges as groups) into S float32 partial sums, and the pass's elementwise epilogue
+// runs in a reduction kernel that adds them in range order.
+constexpr int kLayerSplitMax = 8;
+constexpr long long kLayerSplitCtas = 148;  // CTAs the split may bring a launch to
+
+int layer_split(int G, int rows, int K, int B, pc_precision_t prec) {
+  if (G != 1) return 1;
+  const int kb = 128 / operand_elem_bytes(prec);  // K elements per ring block
+  const long long tiles = static_cast<long long>(cdiv(rows, kBM)) * cdiv(B, kLayerBN);
+  if (tiles * B > (1ll << 24)) return 1;
+  for (int S = kLayerSplitMax; S >= 2; S /= 2)
+    if (tiles * S <= kLayerSplitCtas && K % (S * kb) == 0 && K / S >= 2 * kb) return S;
+  return 1;
+}
+
+// Tensor maps of an operand's K-range view: S groups of K/S columns, K/S elements apart.
+pc_status_t encode_krange_maps(OperandMaps* m, const Operand& op, pc_precision_t p, int box_rows, int S) {
+  Operand v = op;
+  v.cols = op.cols / S;
+  v.groups = S;
+  pc_status_t st = encode_operand_map(&m->hi, v, p, box_rows, 0, true, v.cols);
+  if (st != PC_OK) return st;
+  if (p == PC_PREC_FP32) return encode_operand_map(&m->lo, v, p, box_rows, 1, true, v.cols);
+  m->lo = m->hi;
+  return PC_OK;
+}
+
+// out[i][b] = m_b + log(sum_s part[s][i][b]) (-inf where m_b is -inf or the sum is 0).
+__global__ void k_layer_fwd_reduce(int S, int M, int B, const float* __restrict__ part,
+                                   const float* __restrict__ colmax, float* __restrict__ out) {
+  const int n = M * B;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += gridDim.x * blockDim.x) {
+    float sum = part[idx];
+    for (int k = 1; k < S; ++k) sum += part[static_cast<long long>(k) * n + idx];
+    const float m = colmax[idx % B];
+    out[idx] = (m > -INFINITY && sum > 0.f) ? m + logf(sum) : -INFINITY;
+  }
+}
+
+// e[j][b] = (accumulate ? e : 0) + exp(x[j][b] - m_b) sum_s part[s][j][b].
+__global__ void k_layer_elem_reduce(int S, int N, int B, const float* __restrict__ part, const float* __restrict__ x,
+                                    const float* __restrict__ colmax, float* __restrict__ e, int accumulate) {
+  const int n = N * B;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += gridDim.x * blockDim.x) {
+    float sum = part[idx];
+    for (int k = 1; k < S; ++k) sum += part[static_cast<long long>(k) * n + idx];
+    const float m = colmax[idx % B];
+    const float u = m > -INFINITY ? expf(x[idx] - m) : 0.f;
+    e[idx] = (accumulate ? e[idx] : 0.f) + u * sum;
+  }
+}
+
 struct LayerFwdWs {
   float* colmax;
   Operand th, ubm;
+  float* part;  // layer_split > 1: the K ranges' partial sums
 };
 struct LayerBwdWs {
   float* colmax;
   Operand thT, gbm, gnm, unm;
+  float* part;
 };
 
 size_t carve_fwd(void* base, pc_precision_t p, int G, int M, int N, int B, LayerFwdWs* w) {
@@ -190,6 +249,8 @@ size_t carve_fwd(void* base, pc_precision_t p, int G, int M, int N, int B, Layer
   w->colmax = static_cast<float*>(c.take(size_t(G) * B * sizeof(float)));
   w->th = c.operand(p, G, M, N);
   w->ubm = c.operand(p, G, B, N);
+  const int S = layer_split(G, M, N, B, p);
+  w->part = S > 1 ? static_cast<float*>(c.take(size_t(S) * M * B * sizeof(float))) : nullptr;
   return c.used;
 }
 
@@ -200,6 +261,8 @@ size_t carve_bwd(void* base, pc_precision_t p, int G, int M, int N, int B, Layer
   w->gbm = c.operand(p, G, B, M);
   w->gnm = c.operand(p, G, M, B);
   w->unm = c.operand(p, G, N, B);
+  const int S = layer_split(G, N, M, B, p);
+  w->part = S > 1 ? static_cast<float*>(c.take(size_t(S) * N * B * sizeof(float))) : nullptr;
   return c.used;
 }
 
@@ -239,6 +302,20 @@ pc_status_t layer_fwd(int G, int M, int N, int B, const float* theta, const floa
   if ((st = rows_to_operand<P>(theta, N, static_cast<long long>(M) * N, G, M, N, w.th, s)) != PC_OK) return st;
   if ((st = make_operands<P>(ExpChildren{x, w.colmax, cs, B}, G, N, B, nullptr, &w.ubm, s)) != PC_OK) return st;
   OperandMaps ma, mb;
+  const int S = layer_split(G, M, N, B, prec);
+  if (S > 1) {
+    if ((st = encode_krange_maps(&ma, w.th, prec, kBM, S)) != PC_OK) return st;
+    if ((st = encode_krange_maps(&mb, w.ubm, prec, kLayerBN, S)) != PC_OK) return st;
+    EpiStoreF32::Params ep{w.part, B, M, B, 0, nullptr, nullptr, static_cast<long long>(M) * B};
+    if ((st = launch_gemm<P, kLayerBN, EpiStoreF32>(dim3(cdiv(M, kBM), cdiv(B, kLayerBN), S), ma.hi, ma.lo, mb.hi,
+                                                    mb.lo, num_k_blocks(N / S, prec), ep, s, PC_KIND_LAYER_FWD,
+                                                    2ll * M * N * B)) != PC_OK)
+      return st;
+    k_layer_fwd_reduce<<<static_cast<unsigned>(std::min<long long>(cdiv(static_cast<long long>(M) * B, 256), 1184)),
+                         256, 0, s>>>(S, M, B, w.part, w.colmax, out);
+    PC_LAUNCH_CHECK();
+    return PC_OK;
+  }
   if ((st = encode_maps(&ma, w.th, prec, kBM)) != PC_OK) return st;
   if ((st = encode_maps(&mb, w.ubm, prec, kLayerBN)) != PC_OK) return st;
   EpiLayerFwd::Params ep{out, w.colmax, M, B};
@@ -262,13 +339,27 @@ pc_status_t layer_bwd(int G, int M, int N, int B, const float* theta, const floa
   if (e) {
     if ((st = transpose_to_operand<P>(theta, N, static_cast<long long>(M) * N, G, M, N, w.thT, s)) != PC_OK) return st;
     OperandMaps ma, mb;
-    if ((st = encode_maps(&ma, w.thT, prec, kBM)) != PC_OK) return st;
-    if ((st = encode_maps(&mb, w.gbm, prec, kLayerBN)) != PC_OK) return st;
-    EpiLayerElem::Params ep{e, x, w.colmax, cs, N, B, accumulate};
-    if ((st = launch_gemm<P, kLayerBN, EpiLayerElem>(dim3(cdiv(N, kBM), cdiv(B, kLayerBN), G), ma.hi,
-                                                     ma.lo, mb.hi, mb.lo, num_k_blocks(M, prec), ep,
-                                                     s, PC_KIND_LAYER_ELEM, 2ll * G * M * N * B)) != PC_OK)
-      return st;
+    const int S = layer_split(G, N, M, B, prec);
+    if (S > 1) {
+      if ((st = encode_krange_maps(&ma, w.thT, prec, kBM, S)) != PC_OK) return st;
+      if ((st = encode_krange_maps(&mb, w.gbm, prec, kLayerBN, S)) != PC_OK) return st;
+      EpiStoreF32::Params ep{w.part, B, N, B, 0, nullptr, nullptr, static_cast<long long>(N) * B};
+      if ((st = launch_gemm<P, kLayerBN, EpiStoreF32>(dim3(cdiv(N, kBM), cdiv(B, kLayerBN), S), ma.hi, ma.lo, mb.hi,
+                                                      mb.lo, num_k_blocks(M / S, prec), ep, s, PC_KIND_LAYER_ELEM,
+                                                      2ll * M * N * B)) != PC_OK)
+        return st;
+      k_layer_elem_reduce<<<static_cast<unsigned>(std::min<long long>(cdiv(static_cast<long long>(N) * B, 256), 1184)),
+                            256, 0, s>>>(S, N, B, w.part, x, w.colmax, e, accumulate);
+      PC_LAUNCH_CHECK();
+    } else {
+      if ((st = encode_maps(&ma, w.thT, prec, kBM)) != PC_OK) return st;
+      if ((st = encode_maps(&mb, w.gbm, prec, kLayerBN)) != PC_OK) return st;
+      EpiLayerElem::Params ep{e, x, w.colmax, cs, N, B, accumulate};
+      if ((st = launch_gemm<P, kLayerBN, EpiLayerElem>(dim3(cdiv(N, kBM), cdiv(B, kLayerBN), G), ma.hi,
+                                                       ma.lo, mb.hi, mb.lo, num_k_blocks(M, prec), ep,
+                                                       s, PC_KIND_LAYER_ELEM, 2ll * G * M * N * B)) != PC_OK)
+        return st;
+    }
   }
   if (F) {
     if ((st = make_operands<P>(ExpChildren{x, w.colmax, cs, B}, G, N, B, &w.unm, nullptr, s)) != PC_OK) return st;
