@@ -203,6 +203,39 @@ __global__ void k_lr_to_op(const float* __restrict__ src, long long sg, long lon
   }
 }
 
+// The same copy where the source is contiguous along r (sr = 1) and strided along c: a
+// 32 x 32 tile goes through shared memory, so that both the reads (along r) and the
+// writes (along c) are coalesced.
+template <int F>
+__global__ void k_lr_to_op_t(const float* __restrict__ src, long long sg, long long sc, int G, int R, int C,
+                             void* __restrict__ hi, void* __restrict__ lo, long long ld) {
+  __shared__ float tile[32][33];
+  const int g = blockIdx.z;
+  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const float* s0 = src + g * sg;
+  for (int i = threadIdx.y; i < 32; i += 8) {  // i: column c0 + i, lane: row r0 + lane
+    const int r = r0 + threadIdx.x, c = c0 + i;
+    tile[i][threadIdx.x] = (r < R && c < C) ? s0[r + c * sc] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {  // i: row r0 + i, lane: column c0 + lane
+    const int r = r0 + i;
+    const long long c = c0 + threadIdx.x;
+    if (r >= R || c >= ld) continue;
+    const long long idx = (static_cast<long long>(g) * R + r) * ld + c;
+    const float v = tile[threadIdx.x][i];  // 0 beyond C
+    if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(v);
+      static_cast<__nv_bfloat16*>(hi)[idx] = h;
+      if constexpr (F == kFmtBF16x2) static_cast<__nv_bfloat16*>(lo)[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
+    } else {
+      const float h = tf32_rna(v);
+      static_cast<float*>(hi)[idx] = h;
+      if constexpr (F == kFmtTF32x2) static_cast<float*>(lo)[idx] = tf32_rna(v - h);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ shared memory plan
 enum : int { kLrStats = 3 };
 constexpr int kThetaTileBytes = kLrRows * 128;  // 128 rows x 32 floats
@@ -941,6 +974,13 @@ pc_status_t lr_attr(Kern kern, int smem) {
 template <int F>
 pc_status_t to_op(const float* src, long long sg, long long sr, long long sc, int G, int R, int C, const LrOp& o,
                   cudaStream_t s) {
+  if (sr == 1 && sc != 1 && G <= 65535) {  // a transpose: tiled through shared memory
+    const dim3 grid(cdiv(R, 32), cdiv(o.part[0].ld, 32), G);
+    k_lr_to_op_t<F><<<grid, dim3(32, 8), 0, s>>>(src, sg, sc, G, R, C, o.part[0].ptr,
+                                                 o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
+    PC_LAUNCH_CHECK();
+    return PC_OK;
+  }
   const long long rows = static_cast<long long>(G) * R;
   const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, 8), 8192));
   k_lr_to_op<F><<<blocks, dim3(32, 8), 0, s>>>(src, sg, sr, sc, G, R, C, o.part[0].ptr,
