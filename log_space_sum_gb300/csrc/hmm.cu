@@ -664,11 +664,12 @@ int param_split(int H, int T, int B, pc_precision_t prec) {
 }
 
 // dA[i] = (accumulate ? dA[i] : 0) + A[i] (part[0][i] + part[1][i] + ...), float4 runs
-// where n is a multiple of 4.
+// where n is a multiple of 4 and the caller's A and dA are 16-byte aligned.
 __global__ void k_dA_reduce(int S, long long n, const float* __restrict__ part, const float* __restrict__ A,
                             float* __restrict__ dA, int accumulate) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  if ((n & 3) == 0) {
+  const bool vec = (n & 3) == 0 && ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(dA)) & 15) == 0;
+  if (vec) {
     const long long n4 = n >> 2;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
       float4 sum = reinterpret_cast<const float4*>(part)[i];

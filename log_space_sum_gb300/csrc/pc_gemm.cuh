@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the MMAs are complete: this CTA's ring is idle; inputs of the epilogue are
         // staged behind the exchange buffer while the partner finishes
         if (ok) Epi::after_mma(ep, g, m0, n0_epi, et, epi_smem, smem + kXchgBytes);
-        // Exchange buffer: 128 rows x 128 floats in the (now idle) ring, stored by 32-column
+        // Exchange buffer: 128 rows x BN/2 floats in the (now idle) ring, stored by 32-column
         // chunk, then row, then 16-byte piece (swizzled by the row so that 32 rows' reads of
         // one piece spread over the banks). A warp's 32 x 32 block is contiguous, so each
         // remote store instruction writes 512 consecutive bytes: the block is first turned
