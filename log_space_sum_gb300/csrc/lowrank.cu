@@ -175,10 +175,11 @@ __global__ void k_lr_row_factors(int M, int B, const float* __restrict__ out, co
   rf_fc[dst] = live ? fi * expf(m[b] - o) : 0.f;
 }
 
-// Operand copy in format F: dst[g][r][c] (rows ld elements apart, zero beyond C) =
-// src[g*sg + r*sr + c*sc], rounded to bf16 / TF32 (hi, and lo = the rounded remainder).
-// One row (g, r) per warp row of the block: the row's index is split once per row, not
-// per element.
+// Operand copy in format F: dst[g][r][c] (rows ld elements apart) = src[g*sg + r*sr +
+// c*sc] for c < C, rounded to bf16 / TF32 (hi, and lo = the rounded remainder). The row
+// padding [C, ld) is left unwritten: the operand's tensor maps end at C, so the TMA fills
+// those columns of a tile with zeros and never reads them. One row (g, r) per warp row of
+// the block: the row's index is split once per row, not per element.
 template <int F>
 __global__ void k_lr_to_op(const float* __restrict__ src, long long sg, long long sr, long long sc, int G, int R,
                            int C, void* __restrict__ hi, void* __restrict__ lo, long long ld) {
@@ -187,9 +188,9 @@ __global__ void k_lr_to_op(const float* __restrict__ src, long long sg, long lon
        gr += static_cast<long long>(gridDim.x) * blockDim.y) {
     const long long g = gr / R, r = gr - g * R;
     const float* s0 = src + g * sg + r * sr;
-    for (long long c = threadIdx.x; c < ld; c += blockDim.x) {
+    for (long long c = threadIdx.x; c < C; c += blockDim.x) {
       const long long idx = gr * ld + c;
-      const float v = c < C ? s0[c * sc] : 0.f;
+      const float v = s0[c * sc];
       if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
         const __nv_bfloat16 h = __float2bfloat16_rn(v);
         static_cast<__nv_bfloat16*>(hi)[idx] = h;
@@ -221,9 +222,9 @@ __global__ void k_lr_to_op_t(const float* __restrict__ src, long long sg, long l
   for (int i = threadIdx.y; i < 32; i += 8) {  // i: row r0 + i, lane: column c0 + lane
     const int r = r0 + i;
     const long long c = c0 + threadIdx.x;
-    if (r >= R || c >= ld) continue;
+    if (r >= R || c >= C) continue;
     const long long idx = (static_cast<long long>(g) * R + r) * ld + c;
-    const float v = tile[threadIdx.x][i];  // 0 beyond C
+    const float v = tile[threadIdx.x][i];
     if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
       const __nv_bfloat16 h = __float2bfloat16_rn(v);
       static_cast<__nv_bfloat16*>(hi)[idx] = h;
@@ -975,7 +976,7 @@ template <int F>
 pc_status_t to_op(const float* src, long long sg, long long sr, long long sc, int G, int R, int C, const LrOp& o,
                   cudaStream_t s) {
   if (sr == 1 && sc != 1 && G <= 65535) {  // a transpose: tiled through shared memory
-    const dim3 grid(cdiv(R, 32), cdiv(o.part[0].ld, 32), G);
+    const dim3 grid(cdiv(R, 32), cdiv(C, 32), G);
     k_lr_to_op_t<F><<<grid, dim3(32, 8), 0, s>>>(src, sg, sc, G, R, C, o.part[0].ptr,
                                                  o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
     PC_LAUNCH_CHECK();
