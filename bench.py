@@ -38,6 +38,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -511,12 +512,12 @@ class ClockSampler:
 
     def __init__(self, device_uuid):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="pcsum_clocks_", suffix=".csv")
+        os.close(fd)
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
         if device_uuid:
             cmd += ["-i", device_uuid]
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
@@ -546,6 +547,10 @@ class ClockSampler:
                 for n, v in zip(names, f[4:8]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),

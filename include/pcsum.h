@@ -69,7 +69,7 @@ typedef enum {
   PC_ERR_ALIGNMENT = 3,         /* a pointer is not 16-byte aligned */
   PC_ERR_UNKNOWN_PRECISION = 4, /* precision is not one of pc_precision_t */
   PC_ERR_WORKSPACE = 5,         /* workspace NULL or smaller than the query's size */
-  PC_ERR_UNSUPPORTED = 6,       /* a valid request outside this build's limits */
+  PC_ERR_UNSUPPORTED = 6,       /* a valid request outside the library's limits */
   PC_ERR_CUDA = 7,              /* a CUDA call failed (launch or device query) */
   PC_ERR_TIMEOUT = 8            /* a device-side wait ran out (see pc_device_status) */
 } pc_status_t;

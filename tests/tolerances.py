@@ -3,7 +3,7 @@
 Per-sample log-likelihood (for a single layer: every entry of ``out``), absolute:
 fp32 1e-5, tf32 1e-3, auto (bf16 products) 8e-3.
 Flows, elementwise relative with a floor: |gpu - ref| <= tol * (|ref| + 1e-6 max|ref|);
-fp32 1e-5 is the stated bar; tf32 1e-3 and auto 3e-2 are this build's reading for
+fp32 1e-5 is the stated bar; tf32 1e-3 and auto 3e-2 are the library's reading for
 modes whose flow error the pages do not bound (the pages measured TF32 flows at
 5e-5 / 3e-4 on one HMM layer, pyjuice PR #62 Summary 3).
 """
