@@ -176,15 +176,16 @@ __device__ __forceinline__ void cs_run(const float* c_s, int col0, float (&cv)[3
 template <int W, int Pitch = kChainBN>
 __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, int H, int B, int m0, int n0,
                                                 const int* tok_s, float* Es, int et) {
-  static_assert(W <= kChainBN && W % (8 * kEpiWarps) == 0, "whole batches of 8 columns per warp");
   constexpr int kCols = W / kEpiWarps;  // columns staged by one epilogue warp
+  constexpr int kBatch = kCols < 8 ? kCols : 8;
+  static_assert(W <= kChainBN && W % kEpiWarps == 0 && kCols % kBatch == 0, "whole batches of columns per warp");
   const int lane = et & 31;
   const int c_begin = (et >> 5) * kCols;
 #pragma unroll 1
-  for (int cb = c_begin; cb < c_begin + kCols; cb += 8) {
-    float vals[8][4];
+  for (int cb = c_begin; cb < c_begin + kCols; cb += kBatch) {
+    float vals[kBatch][4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < kBatch; ++c) {
       const bool bin = n0 + cb + c < B;
       const float* src = Et + static_cast<long long>(tok_s[cb + c]) * H + m0;
 #pragma unroll
@@ -194,7 +195,7 @@ __device__ __forceinline__ void stage_emissions(const float* __restrict__ Et, in
       }
     }
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
+    for (int c = 0; c < kBatch; ++c)
 #pragma unroll
       for (int i = 0; i < 4; ++i) Es[es_index<Pitch>(lane + 32 * i, cb + c)] = vals[c][i];
   }
@@ -812,13 +813,15 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   // The bf16 chain contractions run as split-K pairs of 128 x 256 tiles (k_umma_gemm,
   // kSplit); each CTA's epilogue still finishes 128 x kChainBN. Where that gives fewer
   // than kNarrowBelow CTAs (a small H: short K loops, the fixed costs dominate), the
-  // pairs take 128 x 128 tiles instead: twice the CTAs, half the exchange and epilogue
-  // per CTA.
+  // pairs take 128 x 128 (or 128 x 64) tiles instead: twice (four times) the CTAs, a half
+  // (a quarter) of the exchange and epilogue per CTA.
   constexpr bool kSplitChain = P == kBF16;
   constexpr int kTileBN = kSplitChain ? 2 * kChainBN : kChainBN;
   constexpr long long kNarrowBelow = 96;
-  const bool narrow = kSplitChain && 2ll * cdiv(H, kBM) * cdiv(B, kTileBN) < kNarrowBelow;
-  const int tile_bn = narrow ? kChainBN : kTileBN;
+  // split-K tiles 128 x 256, else 128 x 128, else 128 x 64: the widest with enough CTAs
+  int tile_bn = kTileBN;
+  if (kSplitChain)
+    while (tile_bn > 64 && 2ll * cdiv(H, kBM) * cdiv(B, tile_bn) < kNarrowBelow) tile_bn /= 2;
   const dim3 chain_grid((kSplitChain ? 2 : 1) * cdiv(H, kBM), cdiv(B, tile_bn), 1);
 
   // forward chain: S_t for t = T-2 .. 0
@@ -848,7 +851,11 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       // a_early: the A operand was converted before k_hmm_leaf, the kernel that precedes
       // the first layer, so no kernel still running when a layer starts writes it.
       if constexpr (kSplitChain) {
-        if (narrow)
+        if (tile_bn == kChainBN / 2)
+          st = launch_gemm<P, kChainBN / 2, EpiHmmFwd<P, kChainBN / 4>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep,
+                                                                              s, PC_KIND_HMM_FWD, 2ll * H * H * B,
+                                                                              true);
+        else if (tile_bn == kChainBN)
           st = launch_gemm<P, kChainBN, EpiHmmFwd<P, kChainBN / 2>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
                                                                           PC_KIND_HMM_FWD, 2ll * H * H * B, true);
         else
@@ -895,7 +902,11 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
       const OperandMaps& b = mb[t & 1];
       // a_early: the transposed A operand was converted before the forward chain
       if constexpr (kSplitChain) {
-        if (narrow)
+        if (tile_bn == kChainBN / 2)
+          st = launch_gemm<P, kChainBN / 2, EpiHmmBwd<P, kChainBN / 4>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep,
+                                                                              s, PC_KIND_HMM_ELEM, 2ll * H * H * B,
+                                                                              true);
+        else if (tile_bn == kChainBN)
           st = launch_gemm<P, kChainBN, EpiHmmBwd<P, kChainBN / 2>, true>(grid, ma.hi, ma.lo, b.hi, b.lo, nkb, ep, s,
                                                                           PC_KIND_HMM_ELEM, 2ll * H * H * B, true);
         else

@@ -196,8 +196,8 @@ __device__ __forceinline__ void stage_tile_load_bf16_async(uint8_t* tile, int pi
 // sums of the other half of the columns to its partner through distributed shared memory
 // and finishes its own 128 x BN/2 sub-tile. (A 128 x 128 MMA leaves half of the tensor
 // core's width idle; at batch 512 there are too few 128 x 256 tiles to fill the GPU
-// without splitting K. Where even those are too few, 128 x 128 tiles split the same way
-// trade MMA width for twice the CTAs and half the exchange.)
+// without splitting K. Where even those are too few, 128 x 128 or 128 x 64 tiles split the
+// same way trade MMA width for more CTAs and a smaller exchange.)
 template <int P, int BN, class Epi, bool kSplit = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
@@ -225,11 +225,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // epilogue's staged tiles
   constexpr int kXchgBytes = kBM * (BN / 2) * 4;
   if constexpr (kSplit)
-    static_assert(!kSliced && (BN == 256 || BN == 128) &&
+    static_assert(!kSliced && (BN == 256 || BN == 128 || BN == 64) &&
                       kStages * S::kStageBytes >= kXchgBytes + Epi::kSplitStageBytes &&
                       Epi::kSplitScratchOffset + kEpiWarps * 4096 <= Epi::kSplitStageBytes,
-                  "split K: unsliced 128 x 256 or 128 x 128 tiles, the ring holds the exchange buffer and the "
-                  "staged tiles");
+                  "split K: unsliced 128 x 256, 128 x 128 or 128 x 64 tiles, the ring holds the exchange buffer "
+                  "and the staged tiles");
   constexpr int kEpiBN = kSplit ? BN / 2 : BN;  // columns this CTA's epilogue finishes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &

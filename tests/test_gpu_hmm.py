@@ -86,7 +86,7 @@ def test_accumulate_adds_flows():
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("H", [300, 129])
 def test_small_state_space_paths(H, mode):
-    # H = 300 or 129 at batch 256: 128 x 128 split-K tiles on the chain (too few 128 x 256
+    # H = 300 or 129 at batch 256: 128 x 64 split-K tiles on the chain (too few wider
     # pairs), and the dA contraction over K ranges (K = 8 x 256 divides into 4 ranges of
     # whole ring blocks); H = 129 leaves H^2 odd for the range sum's scalar path. Then
     # accumulation through the range sum doubles dA.
@@ -104,9 +104,18 @@ def test_small_state_space_paths(H, mode):
     torch.testing.assert_close(dA2, 2 * base, rtol=1e-6, atol=0)
 
 
+def test_128_wide_split_tiles():
+    # H = 1024, B = 768: 128 x 256 split-K pairs would give 48 CTAs, 128 x 128 pairs 96
+    d = hmm_inputs(1024, 4, 19, 768, seed=97)
+    rl, rpi, rA, rE = _oracle(d)
+    ll, dpi, dA, dE = _gpu_run(d, "auto")
+    assert ll_err(ll, rl) <= LL_TOL["auto"]
+    assert max(flow_err(dpi, rpi), flow_err(dA, rA), flow_err(dE, rE)) <= FLOW_TOL["auto"]
+
+
 @pytest.mark.parametrize("mode", ["auto", "fp32"])
 def test_small_state_space_ragged_batch(mode):
-    # 128 x 128 split-K tiles with a ragged last sample tile (B = 200)
+    # 128 x 64 split-K tiles with a ragged last sample tile (B = 200)
     d = hmm_inputs(256, 4, 17, 200, seed=95)
     rl, rpi, rA, rE = _oracle(d)
     ll, dpi, dA, dE = _gpu_run(d, mode)
