@@ -102,6 +102,23 @@ def test_hmm_argument_errors_before_launch(lib):
 
 def test_profile_capacity_check(lib):
     assert N.STATUS[lib.pc_profile_start(0)] == "PC_ERR_SHAPE"
+    # every output but the count may be NULL; a NULL count is refused before any CUDA call
+    assert N.STATUS[lib.pc_profile_stop(None, None, None, None, None, 4)] == "PC_ERR_NULL"
+
+
+def test_split_workspaces_hold_the_partial_products(lib):
+    # the single-group layer at M = N = 1024, B = 128 runs its forward over 8 K ranges: the
+    # workspace holds the 8 x M x B float32 partial sums that G = 2 groups do not need
+    one, two = _size(), _size()
+    assert lib.pc_sum_layer_workspace(1, 1024, 1024, 128, 0, C.byref(one)) == 0
+    assert lib.pc_sum_layer_workspace(2, 1024, 1024, 128, 0, C.byref(two)) == 0
+    assert one.value - two.value / 2 >= 8 * 1024 * 128 * 4 - 4096  # two groups: twice the rest
+    # the HMM with H = 1024, T = 64, B = 512 runs its stacked dA contraction over 4 K ranges
+    # (4 x H x H float32 partial products); with B = 500 the ranges do not divide K evenly
+    small, odd = _size(), _size()
+    assert lib.pc_hmm_workspace(1024, 64, 1024, 512, 0, C.byref(small)) == 0
+    assert lib.pc_hmm_workspace(1024, 64, 1024, 500, 0, C.byref(odd)) == 0
+    assert small.value - odd.value >= 4 * 1024 * 1024 * 4 - (1 << 20)
 
 
 def test_em_normalize_argument_errors_before_launch(lib):
