@@ -93,6 +93,18 @@ PCSUM_API unsigned long long pc_launch_count(void);
  * the last read, or PC_ERR_CUDA. Diagnostic; not for the hot path. */
 PCSUM_API pc_status_t pc_device_status(pc_stream_t stream);
 
+/* Limit, in nanoseconds, of the first waits of the tensor-core contraction kernel on the
+ * current device (a free ring slot, a filled slot, a free or complete accumulator);
+ * 0 restores the default of 2 s. A kernel whose wait runs out records PC_ERR_TIMEOUT
+ * for pc_device_status, skips the rest of its tile and exits cleanly: waits for work it
+ * has already issued (copies landing, MMAs completing before tensor memory is freed)
+ * always keep the default limit, so no copy or MMA is left in flight. The limit is a
+ * device-wide watchdog setting for failure detection and its tests: a limit shorter
+ * than a tile's K loop makes calls give up and return garbage outputs. Synchronous
+ * (a host-to-device copy); takes effect for kernels launched after it returns; call it
+ * while no library kernel is running. Errors: PC_ERR_CUDA. */
+PCSUM_API pc_status_t pc_set_wait_limit_ns(unsigned long long ns);
+
 /* Timing of the tensor-core contractions, for measurement. Between
  * pc_profile_start(capacity) and pc_profile_stop, every contraction the library
  * launches records a CUDA event pair on its stream (at most `capacity` records), except
@@ -101,15 +113,19 @@ PCSUM_API pc_status_t pc_device_status(pc_stream_t stream);
  * pc_profile_stop synchronises the device, then writes for each record i
  * (i < *count <= capacity): ms[i] = elapsed device time, kind[i] = which contraction
  * (PC_KIND_*), flops[i] = the algorithmic flops of its launches, 2*M*N*K each (each
- * product counted once), launches[i] = how many launches the record spans; for
- * PC_KIND_EM_MSTEP (memory-bound) flops[i] holds the algorithmic bytes instead. Any
- * output pointer may be NULL. Not thread-safe; host-side event objects only, no device
- * memory. */
+ * product counted once), launches[i] = how many launches the record spans. For the
+ * memory-bound kinds (PC_KIND_EM_MSTEP and the *_MEM kinds: every launch of the HMM and
+ * HCLT calls that is not a contraction, i.e. operand copies and transposes, emission
+ * gathers, product layers, root and scaled flows, token buckets and dE gathers) flops[i]
+ * holds the launch's algorithmic bytes instead (each input read once, each output written
+ * once). Any output pointer may be NULL. Not thread-safe; host-side event objects only,
+ * no device memory. */
 typedef enum {
   PC_KIND_LAYER_FWD = 0, PC_KIND_LAYER_ELEM = 1, PC_KIND_LAYER_PARAM = 2,
   PC_KIND_HMM_FWD = 3, PC_KIND_HMM_ELEM = 4, PC_KIND_HMM_PARAM = 5,
   PC_KIND_HCLT_FWD = 6, PC_KIND_HCLT_ELEM = 7, PC_KIND_HCLT_PARAM = 8,
-  PC_KIND_LOWRANK_FWD = 9, PC_KIND_LOWRANK_BWD = 10, PC_KIND_EM_MSTEP = 11
+  PC_KIND_LOWRANK_FWD = 9, PC_KIND_LOWRANK_BWD = 10, PC_KIND_EM_MSTEP = 11,
+  PC_KIND_HMM_MEM = 12, PC_KIND_HCLT_MEM = 13
 } pc_kind_t;
 PCSUM_API pc_status_t pc_profile_start(int capacity);
 PCSUM_API pc_status_t pc_profile_stop(int* count, float* ms, int* kind, long long* flops,

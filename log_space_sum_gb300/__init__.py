@@ -19,6 +19,7 @@ from .api import (  # noqa: F401
     lowrank_sum_exp_fwd,
     precision_code,
     profile_start,
+    set_wait_limit_ns,
     profile_stop,
     sum_layer_bwd,
     sum_layer_fwd,

@@ -22,8 +22,10 @@ STATUS = {
 KINDS = {
     0: "layer_fwd", 1: "layer_elem", 2: "layer_param", 3: "hmm_fwd", 4: "hmm_elem",
     5: "hmm_param", 6: "hclt_fwd", 7: "hclt_elem", 8: "hclt_param", 9: "lowrank_fwd",
-    10: "lowrank_bwd", 11: "em_mstep",
+    10: "lowrank_bwd", 11: "em_mstep", 12: "hmm_mem", 13: "hclt_mem",
 }
+# kinds whose flops field holds algorithmic bytes
+MEMORY_KINDS = {"em_mstep", "hmm_mem", "hclt_mem"}
 
 _i, _ll, _sz, _p, _f, _d = C.c_int, C.c_longlong, C.c_size_t, C.c_void_p, C.c_float, C.c_double
 
@@ -33,6 +35,7 @@ SIGNATURES = {
     "pc_status_string": [_i],
     "pc_last_error": [],
     "pc_device_status": [_p],
+    "pc_set_wait_limit_ns": [C.c_ulonglong],
     "pc_launch_count": [],
     "pc_profile_start": [_i],
     "pc_profile_stop": [_p, _p, _p, _p, _p, _i],

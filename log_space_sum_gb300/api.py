@@ -373,6 +373,12 @@ def device_status(device=None) -> None:
     N.call("pc_device_status", _stream(dev))
 
 
+def set_wait_limit_ns(ns: int = 0) -> None:
+    """Limit of the contraction kernel's first device-side waits on the current device
+    (0 restores the 2 s default); a wait that runs out is reported by device_status()."""
+    N.call("pc_set_wait_limit_ns", int(ns))
+
+
 def profile_start(capacity: int = 4096) -> None:
     N.call("pc_profile_start", int(capacity))
 

@@ -11,8 +11,9 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
-// Set by kernels that give up a bounded wait (bits pc::kErrTimeout*).
-__device__ unsigned g_device_status = 0;
+// Word 0: set by kernels that give up a bounded wait (bits pc::kErrTimeout*). Words 2..3:
+// the contraction kernel's first-wait limit in ns (pc::first_wait_limit; 0 = default).
+__device__ __align__(16) unsigned g_device_status[4] = {0u, 0u, 0u, 0u};
 
 constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices] = {};
@@ -129,6 +130,24 @@ unsigned* device_status_word() {
   return g_status_ptr[dev];
 }
 
+int num_sms() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 148;
+  }
+  const int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 148;
+  }
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 pc_status_t SideStream::fork(cudaStream_t main) {
   int dev = 0;
   PC_CUDA(cudaGetDevice(&dev));
@@ -212,6 +231,14 @@ pc_status_t pc_device_status(pc_stream_t stream) {
     PC_CUDA(cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice));
     return pc::set_error(PC_ERR_TIMEOUT, "a kernel gave up a bounded wait (status bits 0x%x)", v);
   }
+  return PC_OK;
+}
+
+pc_status_t pc_set_wait_limit_ns(unsigned long long ns) {
+  pc::clear_error();
+  unsigned* word = pc::device_status_word();
+  if (!word) return pc::set_error(PC_ERR_CUDA, "device status word unavailable");
+  PC_CUDA(cudaMemcpy(word + 2, &ns, sizeof(ns), cudaMemcpyHostToDevice));
   return PC_OK;
 }
 

@@ -81,6 +81,32 @@ __device__ __forceinline__ void store_operand4(void* base, size_t idx, size_t lo
   }
 }
 
+// The forward contraction's children operand: hi + lo in every mode (3xTF32's own pair,
+// or EpiHcltFwd::kBLo's for bf16 and TF32).
+template <int P>
+__device__ __forceinline__ void store_child4(void* base, size_t idx, size_t lo, float4 v) {
+  if constexpr (P == kTF32x3) {
+    store_operand4<P>(base, idx, lo, v);
+  } else if constexpr (P == kBF16) {
+    const float4 h = make_float4(round_operand<P>(v.x), round_operand<P>(v.y), round_operand<P>(v.z),
+                                 round_operand<P>(v.w));
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + idx) =
+        make_uint2(pack_bf16x2(h.x, h.y), pack_bf16x2(h.z, h.w));
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + idx + lo) =
+        make_uint2(pack_bf16x2(v.x - h.x, v.y - h.y), pack_bf16x2(v.z - h.z, v.w - h.w));
+  } else {
+    const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx) = h;
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx + lo) =
+        make_float4(tf32_rna(v.x - h.x), tf32_rna(v.y - h.y), tf32_rna(v.z - h.z), tf32_rna(v.w - h.w));
+  }
+}
+template <int P>
+__device__ __forceinline__ void store_child(void* base, size_t idx, size_t lo, float v) {
+  if constexpr (P == kTF32x3) store_operand<P>(base, idx, lo, v);
+  else store_operand_hilo<P>(base, idx, lo, v);
+}
+
 // Product layer of the nodes in slots [s0, s0 + gridDim.x), one block per (node, sample):
 // n' = E_v[., x_v] * prod_children D as float32 mantissas in [1/2, 1) with int exponents,
 // u = n' / max n' (float32 and operand copies), and the node's own log max n' as its
@@ -166,12 +192,12 @@ __global__ void __launch_bounds__(256) k_hclt_product(
     const int z = 4 * q;
     if constexpr (kVec) {
       reinterpret_cast<float4*>(u32)[q] = u;
-      if (uop) store_operand4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
+      if (uop) store_child4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
     } else {
       const float uu[4] = {u.x, u.y, u.z, u.w};
       for (int k = 0; k < 4 && z + k < H; ++k) {
         u32[z + k] = uu[k];
-        if (uop) store_operand<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
+        if (uop) store_child<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
       }
     }
     if (s == root_slot) {
@@ -276,11 +302,11 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
     const float4 u = make_float4(uu[0], uu[1], uu[2], uu[3]);
     if constexpr (kVec) {
       reinterpret_cast<float4*>(u32)[q] = u;
-      if (uop) store_operand4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
+      if (uop) store_child4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
     } else {
       for (int k = 0; k < 4 && z + k < H; ++k) {
         u32[z + k] = uu[k];
-        if (uop) store_operand<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
+        if (uop) store_child<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
       }
     }
     if (s == root_slot) {
@@ -483,6 +509,11 @@ struct EpiHcltFwd : EpiNoHooks {
   // mode accumulates K in slices of 16 k-steps so that the accumulator's truncation acts
   // on partial sums a fraction of D's size.
   static constexpr int kSliceBF16 = 16;
+  // With uniform emissions every latent of a node is within a rounding step of the node's
+  // maximum, where one bf16 / TF32 rounding would take them all to exactly 1 and each
+  // edge would gain its largest row sum error instead of an average: the children
+  // operand keeps a lo part (EpiBLo).
+  static constexpr bool kBLo = true;
   struct Params {
     float* D;  // at the level's first slot, [G][B][H]
     int H, B;
@@ -621,7 +652,7 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
   w->Wop = c.operand(p, E1, H, H);
   w->Et = static_cast<float*>(c.take(size_t(n) * C * H * 4));
   w->U32 = static_cast<float*>(c.take(size_t(n) * B * H * 4));
-  w->Uop = c.operand(p, E1, B, H);
+  w->Uop = c.operand(p, E1, B, H, 2);  // hi + lo in every mode (EpiHcltFwd::kBLo)
   w->D = static_cast<float*>(c.take(size_t(E1) * B * H * 4));
   w->Ex = static_cast<int*>(c.take(size_t(n) * B * 4));
   w->Lm = static_cast<float*>(c.take(size_t(n) * B * 4));
@@ -677,15 +708,25 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
   const int* d_cslots = w.plan + pl.off_cslots;
   const int* d_pslot = w.plan + pl.off_pslot;
 
+  // algorithmic bytes of the memory-bound launches (profiler records, PC_KIND_HCLT_MEM)
+  const long long eb = operand_elem_bytes(prec) * operand_parts(prec);  // stored bytes per operand value
+  const long long eb2 = 2ll * operand_elem_bytes(prec);                  // the children operand's hi + lo
+  const long long HH = static_cast<long long>(H) * H, BH = static_cast<long long>(B) * H;
+  const long long CH = static_cast<long long>(C) * H;
   // the tree plan is a few KB of host data
   PC_CUDA(cudaMemcpyAsync(w.plan, pl.blob.data(), pl.blob.size() * sizeof(int), cudaMemcpyHostToDevice, s));
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dW && !accumulate) PC_CUDA(cudaMemsetAsync(dW, 0, size_t(H) * H * 4, s));  // W[0] has no edge
 
   // Et[v][k][z] = E[v][z][k]: the emissions of one category are a contiguous row
-  if ((st = transpose_f32(Em, C, static_cast<long long>(H) * C, n, H, C, w.Et, H, 0, s)) != PC_OK) return st;
-  if (E > 0 && (st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, d_var)) != PC_OK)
-    return st;
+  {
+    ProfileScope ps(s, PC_KIND_HCLT_MEM, 2ll * n * CH * 4);
+    if ((st = transpose_f32(Em, C, static_cast<long long>(H) * C, n, H, C, w.Et, H, 0, s)) != PC_OK) return st;
+  }
+  if (E > 0) {
+    ProfileScope ps(s, PC_KIND_HCLT_MEM, E * HH * (4 + eb));
+    if ((st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, d_var)) != PC_OK) return st;
+  }
 
   // -------------------------------------------------------------- forward
   const size_t prod_smem = size_t((H + 3) / 4) * 32;  // mantissa and exponent runs, up to 64 KB
@@ -702,6 +743,9 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     const int G = sB - sA;
     if (G <= 0) continue;
     const bool edges = L < pl.maxh;
+    const long long kids = pl.child_ptr[sB] - pl.child_ptr[sA];
+    ProfileScope ps(s, PC_KIND_HCLT_MEM,
+                    G * B * 4ll + G * BH * 8 + kids * BH * 4 + (edges ? G * BH * eb2 : H * 4ll + B * 4ll));
     if (H <= 4 * 32 * kWarpRuns) {
       const unsigned blocks = static_cast<unsigned>(cdiv(static_cast<long long>(G) * B, 8));
       (prod_vec ? k_hclt_product_warp<P, true> : k_hclt_product_warp<P, false>)<<<blocks, 256, 0, s>>>(
@@ -715,7 +759,7 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     PC_LAUNCH_CHECK();
     if (!edges) continue;
     if ((st = encode_maps(&ma, operand_view(w.Wop, prec, sA, G), prec, kBM)) != PC_OK) return st;
-    if ((st = encode_maps(&mb, operand_view(w.Uop, prec, sA, G), prec, kHcltBN)) != PC_OK) return st;
+    if ((st = encode_maps_hilo(&mb, operand_view(w.Uop, prec, sA, G), prec, kHcltBN)) != PC_OK) return st;
     EpiHcltFwd::Params ep{w.D + static_cast<long long>(sA) * B * H, H, B};
     // a_early: W's operand copy was written before the first product layer
     if ((st = launch_gemm<P, kHcltBN, EpiHcltFwd>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi,
@@ -723,29 +767,41 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
                                                   2ll * G * H * H * B, true)) != PC_OK)
       return st;
   }
-  k_hclt_ll<<<cdiv(B, 128), 128, 0, s>>>(n, B, w.Ex, w.Lm, w.rdot, ll, w.rroot);
-  PC_LAUNCH_CHECK();
+  {
+    ProfileScope ps(s, PC_KIND_HCLT_MEM, n * B * 8ll + B * 16ll);
+    k_hclt_ll<<<cdiv(B, 128), 128, 0, s>>>(n, B, w.Ex, w.Lm, w.rdot, ll, w.rroot);
+    PC_LAUNCH_CHECK();
+  }
   if (!flows) return PC_OK;
 
   // ------------------------------------------------------------- backward
-  k_hclt_root_flows<<<dim3(cdiv(H, 256), cdiv(B, 32)), 256, 0, s>>>(root, H, B, pi, w.U32, w.rroot, w.F32, dpi);
-  PC_LAUNCH_CHECK();
+  {
+    ProfileScope ps(s, PC_KIND_HCLT_MEM, 2 * BH * 4 + H * 4ll + B * 4ll);
+    k_hclt_root_flows<<<dim3(cdiv(H, 256), cdiv(B, 32)), 256, 0, s>>>(root, H, B, pi, w.U32, w.rroot, w.F32, dpi);
+    PC_LAUNCH_CHECK();
+  }
   if (down) {
-    if ((st = transpose_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.WopT, s, d_var)) != PC_OK)
-      return st;
+    {
+      ProfileScope ps(s, PC_KIND_HCLT_MEM, E * HH * (4 + eb));
+      if ((st = transpose_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.WopT, s, d_var)) != PC_OK)
+        return st;
+    }
     for (int L = pl.maxh - 1; L >= 0; --L) {
       const int sA = pl.level_start[L], sB = pl.level_start[L + 1];
       const int G = sB - sA;
       if (G <= 0) continue;
-      (prod_vec ? k_hclt_scaled_flows<P, true> : k_hclt_scaled_flows<P, false>)<<<dim3(cdiv(H, 64), cdiv(B, 64), G),
-                                                                                 256, 0, s>>>(
-          sA, H, B, d_pslot, w.F32, w.D, w.Gbm.ptr, w.Gbm.ld, w.Gbm.lo_elems, w.Gnm.ptr, w.Gnm.ld,
-          w.Gnm.lo_elems);
-      PC_LAUNCH_CHECK();
+      {
+        ProfileScope ps(s, PC_KIND_HCLT_MEM, G * BH * (8 + 2 * eb));
+        (prod_vec ? k_hclt_scaled_flows<P, true> : k_hclt_scaled_flows<P, false>)<<<dim3(cdiv(H, 64), cdiv(B, 64), G),
+                                                                                   256, 0, s>>>(
+            sA, H, B, d_pslot, w.F32, w.D, w.Gbm.ptr, w.Gbm.ld, w.Gbm.lo_elems, w.Gnm.ptr, w.Gnm.ld,
+            w.Gnm.lo_elems);
+        PC_LAUNCH_CHECK();
+      }
       // element flows of the level's children; 256-wide tiles (full-rate MMAs) where the
       // level has enough of them to fill the GPU
       if ((st = encode_maps(&ma, operand_view(w.WopT, prec, sA, G), prec, kBM)) != PC_OK) return st;
-      const bool wide = P == kBF16 && static_cast<long long>(cdiv(H, kBM)) * cdiv(B, 2 * kHcltBN) * G >= 148;
+      const bool wide = P == kBF16 && static_cast<long long>(cdiv(H, kBM)) * cdiv(B, 2 * kHcltBN) * G >= num_sms();
       const int ebn = wide ? 2 * kHcltBN : kHcltBN;
       if ((st = encode_maps(&mb, operand_view(w.Gbm, prec, 0, G), prec, ebn)) != PC_OK) return st;
       HcltElemParams ee{w.U32 + static_cast<long long>(sA) * B * H, w.F32 + static_cast<long long>(sA) * B * H, H,
@@ -764,9 +820,12 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       if (st != PC_OK) return st;
       if (!dW) continue;
       // parameter flows of the level's edges
-      if ((st = transpose_to_operand<P>(w.U32 + static_cast<long long>(sA) * B * H, H,
-                                        static_cast<long long>(B) * H, G, B, H, w.Unm, s)) != PC_OK)
-        return st;
+      {
+        ProfileScope ps(s, PC_KIND_HCLT_MEM, G * BH * (4 + eb));
+        if ((st = transpose_to_operand<P>(w.U32 + static_cast<long long>(sA) * B * H, H,
+                                          static_cast<long long>(B) * H, G, B, H, w.Unm, s)) != PC_OK)
+          return st;
+      }
       if ((st = encode_maps(&ma, operand_view(w.Gnm, prec, 0, G), prec, kBM)) != PC_OK) return st;
       if ((st = encode_maps(&mb, operand_view(w.Unm, prec, 0, G), prec, kParamBN)) != PC_OK) return st;
       EpiThetaScale::Params ep{dW, W, H, H, accumulate, d_var + sA};
@@ -777,10 +836,17 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     }
   }
   if (dE) {
-    k_hclt_cat_bucket<<<n, 32, size_t(C + 1) * 4, s>>>(n, B, C, data, d_var, w.cat_order, w.cat_off);
-    PC_LAUNCH_CHECK();
-    k_hclt_dE_gather<<<dim3(n, C), 256, 0, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, w.dEt);
-    PC_LAUNCH_CHECK();
+    {
+      ProfileScope ps(s, PC_KIND_HCLT_MEM, n * B * 8ll + n * (C + 1) * 4ll);
+      k_hclt_cat_bucket<<<n, 32, size_t(C + 1) * 4, s>>>(n, B, C, data, d_var, w.cat_order, w.cat_off);
+      PC_LAUNCH_CHECK();
+    }
+    {
+      ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + n * CH * 4);
+      k_hclt_dE_gather<<<dim3(n, C), 256, 0, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, w.dEt);
+      PC_LAUNCH_CHECK();
+    }
+    ProfileScope ps(s, PC_KIND_HCLT_MEM, (accumulate ? 3ll : 2ll) * n * CH * 4);
     if ((st = transpose_f32(w.dEt, H, static_cast<long long>(C) * H, n, C, H, dE, C, accumulate, s)) != PC_OK)
       return st;
   }

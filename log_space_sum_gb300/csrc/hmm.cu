@@ -652,7 +652,6 @@ struct EpiHmmBwd : EpiNoHooks {
 // (blockIdx.z; the operands' tensor maps take the ranges as groups) into S float32
 // partial products, which k_dA_reduce adds in range order and scales by A.
 constexpr int kParamSplitMax = 4;
-constexpr long long kParamSplitCtas = 148;  // CTAs the split may bring the launch to
 
 int param_split(int H, int T, int B, pc_precision_t prec) {
   if (T < 2) return 1;
@@ -660,7 +659,7 @@ int param_split(int H, int T, int B, pc_precision_t prec) {
   const int kb = 128 / operand_elem_bytes(prec);  // K elements per ring block
   const long long tiles = static_cast<long long>(cdiv(H, kBM)) * cdiv(H, prec == PC_PREC_AUTO ? 256 : 128);
   for (int S = kParamSplitMax; S >= 2; S /= 2)
-    if (tiles * S <= kParamSplitCtas && K % (static_cast<long long>(S) * kb) == 0 && K / S >= 8ll * kb) return S;
+    if (tiles * S <= num_sms() && K % (static_cast<long long>(S) * kb) == 0 && K / S >= 8ll * kb) return S;
   return 1;
 }
 
@@ -769,6 +768,10 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   pc_status_t st;
 
   PC_CUDA(cudaMemsetAsync(w.umax, 0, size_t(T) * B * 4, s));
+  // algorithmic bytes of the memory-bound launches (profiler records, PC_KIND_HMM_MEM)
+  const long long eb = operand_elem_bytes(prec) * operand_parts(prec);  // stored bytes per operand value
+  const long long HH = static_cast<long long>(H) * H, BH = static_cast<long long>(B) * H;
+  const long long TB = static_cast<long long>(T) * B, VH = static_cast<long long>(V) * H;
   // Work off the forward chain's path (the token buckets for dE, the transposed A operand
   // of the backward chain) runs on a side stream, beside the forward contractions, which
   // leave some SMs free; it joins the caller's stream before the backward chain.
@@ -779,30 +782,56 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   if (w.dEt) {
     // token buckets of every (position, sample): dE is then a per-token gather-sum
     PC_CUDA(cudaMemsetAsync(w.tok_count, 0, size_t(V + 1) * 4, sa));
-    k_token_hist<<<cdiv(static_cast<long long>(T) * B, 256), 256, 0, sa>>>(tokens, T * B, V, w.tok_count);
-    PC_LAUNCH_CHECK();
-    k_exclusive_scan<<<1, 1024, 0, sa>>>(w.tok_count, V, w.tok_offset);
-    PC_LAUNCH_CHECK();
-    k_token_bucket<<<cdiv(V, kBucketSpan), 256, 0, sa>>>(tokens, T, B, V, w.tok_offset, w.tok_order);
-    PC_LAUNCH_CHECK();
+    {
+      ProfileScope ps(sa, PC_KIND_HMM_MEM, TB * 4 + (V + 1) * 4ll);
+      k_token_hist<<<cdiv(static_cast<long long>(T) * B, 256), 256, 0, sa>>>(tokens, T * B, V, w.tok_count);
+      PC_LAUNCH_CHECK();
+    }
+    {
+      ProfileScope ps(sa, PC_KIND_HMM_MEM, (V + 1) * 8ll);
+      k_exclusive_scan<<<1, 1024, 0, sa>>>(w.tok_count, V, w.tok_offset);
+      PC_LAUNCH_CHECK();
+    }
+    {
+      ProfileScope ps(sa, PC_KIND_HMM_MEM, TB * 8 + (V + 1) * 4ll);
+      k_token_bucket<<<cdiv(V, kBucketSpan), 256, 0, sa>>>(tokens, T, B, V, w.tok_offset, w.tok_order);
+      PC_LAUNCH_CHECK();
+    }
   }
-  if (chain && (st = transpose_to_operand<P>(A, H, 0, 1, H, H, w.Atop, sa)) != PC_OK) return st;
+  if (chain) {
+    ProfileScope ps(sa, PC_KIND_HMM_MEM, HH * (4 + eb));
+    if ((st = transpose_to_operand<P>(A, H, 0, 1, H, H, w.Atop, sa)) != PC_OK) return st;
+  }
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dA && !accumulate && T < 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
 
   // set-up: E transposed, row sums of A, emission bounds, operand copies of A
-  if ((st = transpose_f32(E, V, 0, 1, H, V, w.Et, H, 0, s)) != PC_OK) return st;  // Et[v][k] = E[k][v]
-  k_rowsum<<<cdiv(H, 8), 256, 0, s>>>(A, H, w.rs);
-  PC_LAUNCH_CHECK();
-  k_emission_bounds<<<V, 256, 0, s>>>(w.Et, w.rs, H, w.emax, w.emax_rs);
-  PC_LAUNCH_CHECK();
-  if (T >= 2 && (st = rows_to_operand<P>(A, H, 0, 1, H, H, w.Aop, s)) != PC_OK) return st;
+  {
+    ProfileScope ps(s, PC_KIND_HMM_MEM, 2 * VH * 4);
+    if ((st = transpose_f32(E, V, 0, 1, H, V, w.Et, H, 0, s)) != PC_OK) return st;  // Et[v][k] = E[k][v]
+  }
+  {
+    ProfileScope ps(s, PC_KIND_HMM_MEM, HH * 4 + H * 4ll);
+    k_rowsum<<<cdiv(H, 8), 256, 0, s>>>(A, H, w.rs);
+    PC_LAUNCH_CHECK();
+  }
+  {
+    ProfileScope ps(s, PC_KIND_HMM_MEM, VH * 4 + H * 4ll + V * 8ll);
+    k_emission_bounds<<<V, 256, 0, s>>>(w.Et, w.rs, H, w.emax, w.emax_rs);
+    PC_LAUNCH_CHECK();
+  }
+  if (T >= 2) {
+    ProfileScope ps(s, PC_KIND_HMM_MEM, HH * (4 + eb));
+    if ((st = rows_to_operand<P>(A, H, 0, 1, H, H, w.Aop, s)) != PC_OK) return st;
+  }
 
   // leaf (position T-1)
   {
     const int t = T - 1;
     const bool has_next = T >= 2;
     const Operand& ub = w.ubm[t & 1];
+    ProfileScope ps(s, PC_KIND_HMM_MEM,
+                    B * 4ll + V * 4ll + BH * 4 + (has_next ? BH * eb : 0) + (chain ? BH * eb : 0) + (T == 1 ? BH * 4 : 0));
     k_hmm_leaf<P><<<dim3(cdiv(H, 32), cdiv(B, 32)), dim3(32, 8), 0, s>>>(
         H, B, T, tokens, w.Et, w.emax, has_next ? ub.ptr : nullptr, ub.ld, ub.lo_elems,
         chain ? w.un.ptr : nullptr, w.un.ld, w.un.lo_elems, static_cast<long long>(T - 2) * B,
@@ -870,15 +899,22 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
     profile_group_end(prof, s, PC_KIND_HMM_FWD, 2ll * H * H * B * (T - 1), T - 1);
   }
 
-  k_hmm_root<<<B, 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, ll, w.rroot);
-  PC_LAUNCH_CHECK();
+  {
+    ProfileScope ps(s, PC_KIND_HMM_MEM, BH * 4 + H * 4ll + TB * 8 + B * 12ll);
+    k_hmm_root<<<B, 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, ll, w.rroot);
+    PC_LAUNCH_CHECK();
+  }
   if (use_side && (st = side.join(s)) != PC_OK) return st;
   if (!flows) return PC_OK;
 
+  {
+  ProfileScope ps(s, PC_KIND_HMM_MEM,
+                  2 * BH * 4 + H * 4ll + (w.fbm ? BH * 4 : 0) + (chain ? BH * eb : 0) + (chain && dA ? BH * eb : 0));
   k_hmm_root_flows<P><<<dim3(cdiv(H, 32), cdiv(B, 32)), dim3(32, 8), 0, s>>>(
       H, B, T, tokens, pi, w.U0, w.Et, w.cf, w.rroot, chain ? w.wbm[0].ptr : nullptr, w.wbm[0].ld,
       w.wbm[0].lo_elems, (chain && dA) ? w.wn.ptr : nullptr, w.wn.ld, w.wn.lo_elems, w.fbm, dpi);
   PC_LAUNCH_CHECK();
+  }
 
   if (chain) {
     OperandMaps ma, mb[2];
@@ -923,9 +959,15 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
     // the stacked dA contraction (which is bound by the tensor cores)
     if (dE) {
       if ((st = side.fork(s)) != PC_OK) return st;
-      k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, side.s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
-      PC_LAUNCH_CHECK();
-      if ((st = transpose_f32(w.dEt, H, 0, 1, V, H, dE, V, accumulate, side.s)) != PC_OK) return st;
+      {
+        ProfileScope ps(side.s, PC_KIND_HMM_MEM, TB * H * 4 + TB * 4 + VH * 4);
+        k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, side.s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
+        PC_LAUNCH_CHECK();
+      }
+      {
+        ProfileScope ps(side.s, PC_KIND_HMM_MEM, (accumulate ? 3 : 2) * VH * 4);
+        if ((st = transpose_f32(w.dEt, H, 0, 1, V, H, dE, V, accumulate, side.s)) != PC_OK) return st;
+      }
     }
     if (dA) {
       OperandMaps pa, pb;
@@ -954,7 +996,8 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
                                                         2ll * H * H * K)) != PC_OK)
           return st;
         const long long n = static_cast<long long>(H) * H;
-        k_dA_reduce<<<static_cast<unsigned>(std::min<long long>(cdiv(n, 4 * 256), 4 * 148)), 256, 0, s>>>(
+        ProfileScope ps(s, PC_KIND_HMM_MEM, (S + 2 + (accumulate ? 1 : 0)) * n * 4);
+        k_dA_reduce<<<static_cast<unsigned>(std::min<long long>(cdiv(n, 4 * 256), 4ll * num_sms())), 256, 0, s>>>(
             S, n, w.dA_part, A, dA, accumulate);
         PC_LAUNCH_CHECK();
       } else {
@@ -969,8 +1012,12 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   } else {
     if (dA && !accumulate && T >= 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
     if (dE) {
-      k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
-      PC_LAUNCH_CHECK();
+      {
+        ProfileScope ps(s, PC_KIND_HMM_MEM, TB * H * 4 + TB * 4 + VH * 4);
+        k_dE_gather<<<dim3(V, cdiv(H, 256)), 256, 0, s>>>(w.fbm, H, w.tok_offset, w.tok_order, w.dEt);
+        PC_LAUNCH_CHECK();
+      }
+      ProfileScope ps(s, PC_KIND_HMM_MEM, (accumulate ? 3 : 2) * VH * 4);
       if ((st = transpose_f32(w.dEt, H, 0, 1, V, H, dE, V, accumulate, s)) != PC_OK) return st;
     }
   }

@@ -184,7 +184,6 @@ constexpr int kLayerBN = 128;
 // ranges as groups) into S float32 partial sums, and the pass's elementwise epilogue
 // runs in a reduction kernel that adds them in range order.
 constexpr int kLayerSplitMax = 8;
-constexpr long long kLayerSplitCtas = 148;  // CTAs the split may bring a launch to
 
 int layer_split(int G, int rows, int K, int B, pc_precision_t prec) {
   if (G != 1) return 1;
@@ -192,7 +191,7 @@ int layer_split(int G, int rows, int K, int B, pc_precision_t prec) {
   const long long tiles = static_cast<long long>(cdiv(rows, kBM)) * cdiv(B, kLayerBN);
   if (tiles * B > (1ll << 24)) return 1;
   for (int S = kLayerSplitMax; S >= 2; S /= 2)
-    if (tiles * S <= kLayerSplitCtas && K % (S * kb) == 0 && K / S >= 2 * kb) return S;
+    if (tiles * S <= num_sms() && K % (S * kb) == 0 && K / S >= 2 * kb) return S;
   return 1;
 }
 

@@ -20,6 +20,18 @@ enum : unsigned { kErrTimeoutProducer = 1u, kErrTimeoutMma = 2u, kErrTimeoutEpil
 // (an epilogue waiting for the full K loop of its tile).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// The status word is the first of four: words 2..3 hold the limit, in ns, of the
+// contraction kernel's first waits (the producer's wait for a free ring slot, the MMA
+// issuer's waits for a filled slot or a free accumulator, the epilogue's wait for the
+// accumulator), set by pc_set_wait_limit_ns; 0 means kWaitLimitNs. Waits for work
+// already issued (copies landing, MMAs completing before TMEM is freed) always take
+// kWaitLimitNs, so a kernel that gives up early never exits with work in flight.
+__device__ __forceinline__ unsigned long long first_wait_limit(const unsigned* status) {
+  if (!status) return kWaitLimitNs;
+  const unsigned long long v = *reinterpret_cast<const volatile unsigned long long*>(status + 2);
+  return v ? v : kWaitLimitNs;
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -62,15 +74,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Gives up after
-// kWaitLimitNs, sets `code` in the status word and returns false.
+// Waits for the phase with the given parity to complete. Gives up after limit_ns,
+// sets `code` in the status word and returns false. (A limit below the default is
+// checked on every iteration.)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status,
-                                          unsigned code) {
+                                          unsigned code, unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
+  const bool short_limit = limit_ns < kWaitLimitNs;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (((it & 63u) == 0 || short_limit) && globaltimer_ns() - t0 > limit_ns) {
       if (status) atomicOr(status, code);
       return false;
     }
@@ -260,6 +274,27 @@ __device__ __forceinline__ void store_operand(void* base, size_t idx, size_t lo_
     const float lo = tf32_rna(v - hi);
     reinterpret_cast<float*>(base)[idx] = hi;
     reinterpret_cast<float*>(base)[idx + lo_stride] = lo;
+  }
+}
+
+// A bf16 or TF32 operand stored as hi + lo: hi = the mode's rounding of v, lo = that of
+// v - hi (for kTF32x3, the same as store_operand). Read by contractions whose B operand
+// has a lo part (EpiBLo).
+template <int P>
+__device__ __forceinline__ float round_operand(float v) {
+  if constexpr (P == kBF16) return __bfloat162float(__float2bfloat16_rn(v));
+  else return tf32_rna(v);
+}
+template <int P>
+__device__ __forceinline__ void store_operand_hilo(void* base, size_t idx, size_t lo_stride, float v) {
+  if constexpr (P == kBF16) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    reinterpret_cast<__nv_bfloat16*>(base)[idx] = hi;
+    reinterpret_cast<__nv_bfloat16*>(base)[idx + lo_stride] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  } else {
+    const float hi = tf32_rna(v);
+    reinterpret_cast<float*>(base)[idx] = hi;
+    reinterpret_cast<float*>(base)[idx + lo_stride] = tf32_rna(v - hi);
   }
 }
 

@@ -36,6 +36,18 @@ struct EpiPrefetch : std::false_type {};
 template <class E>
 struct EpiPrefetch<E, std::void_t<decltype(E::kPrefetchTile)>> : std::bool_constant<E::kPrefetchTile> {};
 
+// Epi::kBLo (optional, default false; bf16 and TF32 only): the B operand (the layer's
+// children) is stored as hi + lo, hi = the mode's rounding of the value and lo = that of
+// the remainder, and every k-step adds A * B_lo into a separate TMEM accumulator that
+// spans all of K (its entries are 2^-9 / 2^-12 of the main ones, so its truncation is
+// negligible); the epilogue adds it to the sliced sum. For children that sit within a
+// rounding step of one another (every latent of an HCLT node near its maximum) a single
+// rounding would move them all the same way.
+template <class E, class = void>
+struct EpiBLo : std::false_type {};
+template <class E>
+struct EpiBLo<E, std::void_t<decltype(E::kBLo)>> : std::bool_constant<E::kBLo> {};
+
 // Warp 0: TMA producer; warp 1: MMA issuer; warps 2 .. 9: epilogue, two warps per TMEM
 // lane quarter, each taking every other 32-column chunk of the tile.
 constexpr int kEpiWarps = 8;
@@ -45,14 +57,15 @@ constexpr int kGemmThreads = 64 + kEpiThreads;
 // per thread; the launch bounds let the compiler plan for that.)
 constexpr int kBM = 128;
 
-template <int P, int BN>
+template <int P, int BN, bool kBLo = false>
 struct GemmShape {
   static constexpr int kElem = operand_bytes<P>();
-  static constexpr int kBK = 128 / kElem;                // K elements per 128-byte row
-  static constexpr int kParts = (P == kTF32x3) ? 2 : 1;  // hi (+ lo)
+  static constexpr int kBK = 128 / kElem;                 // K elements per 128-byte row
+  static constexpr int kAParts = (P == kTF32x3) ? 2 : 1;  // hi (+ lo)
+  static constexpr int kBParts = (P == kTF32x3 || kBLo) ? 2 : 1;
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
-  static constexpr uint32_t kStageBytes = kParts * (kABytes + kBBytes);
+  static constexpr uint32_t kStageBytes = kAParts * kABytes + kBParts * kBBytes;
   static constexpr uint32_t kUmmaK = (P == kBF16) ? 16 : (P == kFP8 ? 32 : 8);  // K per MMA instruction
   static constexpr uint32_t kKSteps = kBK / kUmmaK;          // MMAs per ring slot (4)
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: two epilogue warps split the 32-column chunks");
@@ -81,7 +94,7 @@ constexpr size_t kSmemPerCta = 232448;  // opt-in maximum dynamic shared memory 
 // Shared-memory plan of one instantiation: the ring gets what the epilogue leaves.
 template <int P, int BN, class Epi>
 struct GemmPlan {
-  using S = GemmShape<P, BN>;
+  using S = GemmShape<P, BN, EpiBLo<Epi>::value && P != kTF32x3>;
   static constexpr size_t kTBufBytes = Epi::kTranspose ? kEpiWarps * kTBufFloats * sizeof(float) : 0;
   static constexpr size_t kEpiBytes = ((Epi::kSmemBytes + 15) / 16) * 16;
   static constexpr size_t kFixed = 1024 /* alignment slack */ + 256 /* barriers */ + kTBufBytes + kEpiBytes;
@@ -203,7 +216,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
                 int num_kb_total, unsigned* status, const typename Epi::Params ep, int a_early) {
-  using S = GemmShape<P, BN>;
+  // B_lo products in their own accumulator (EpiBLo); 3xTF32 has its own lo terms
+  constexpr bool kBLo = EpiBLo<Epi>::value && P != kTF32x3;
+  static_assert(!kBLo || P == kBF16 || P == kTF32, "a B lo part in bf16 or TF32");
+  using S = GemmShape<P, BN, kBLo>;
   constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
   // Sliced modes: every K slice (kSliceK k-steps of the MMA) is accumulated from zero in
   // one of kAccBufs TMEM buffers and added into registers by the epilogue with round-to-
@@ -218,8 +234,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   static_assert(!kSliced || kStepSliced ? kSliceK <= 1 : kSliceK % S::kKSteps == 0,
                 "slices are one k-step or whole ring slots");
   constexpr int kAccBufs = !kSliced ? 1 : (kStepSliced && 4 * BN <= 512 ? 4 : 2);
-  constexpr uint32_t kTmemCols = kAccBufs * BN;
-  static_assert(kTmemCols <= 512, "TMEM columns");
+  static_assert(!kBLo || (kSliced && !kStepSliced), "B lo parts with slot-granular slices");
+  constexpr uint32_t kLoCol = kAccBufs * BN;  // the B_lo accumulator's first column
+  constexpr uint32_t kTmemUsed = kAccBufs * BN + (kBLo ? BN : 0);
+  // tcgen05.alloc takes a power of two
+  constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                 : kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM columns");
   constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
   // split K: the idle ring holds the exchange buffer (128 x BN/2 floats), then the
   // epilogue's staged tiles
@@ -238,13 +259,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;  // [4]
   uint64_t* acc_empty = acc_full + 4;    // [4]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 4);
+  uint64_t* mma_done = acc_empty + 4;    // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   float* tbuf_base = reinterpret_cast<float*>(smem + kStages * S::kStageBytes + 256);
   uint8_t* epi_smem = reinterpret_cast<uint8_t*>(tbuf_base) + GemmPlan<P, BN, Epi>::kTBufBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = kSplit ? static_cast<int>(cluster_ctarank()) : 0;
+  const unsigned long long wl = first_wait_limit(status);  // the first waits' limit
   const int m0 = (kSplit ? blockIdx.x >> 1 : blockIdx.x) * kBM;
   const int n0 = blockIdx.y * BN;
   const int g = blockIdx.z;
@@ -255,7 +278,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   auto a_tile = [&](int s, int part) { return smem + s * S::kStageBytes + part * S::kABytes; };
   auto b_tile = [&](int s, int part) {
-    return smem + s * S::kStageBytes + S::kParts * S::kABytes + part * S::kBBytes;
+    return smem + s * S::kStageBytes + S::kAParts * S::kABytes + part * S::kBBytes;
   };
 
   if (warp == 0) {
@@ -268,13 +291,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_init(&acc_full[b], 1);
         mbar_init(&acc_empty[b], 1);
       }
+      mbar_init(mma_done, 1);
       fence_barrier_init();
       tma_prefetch_map(&tmA);
       tma_prefetch_map(&tmB);
-      if constexpr (P == kTF32x3) {
-        tma_prefetch_map(&tmA_lo);
-        tma_prefetch_map(&tmB_lo);
-      }
+      if constexpr (P == kTF32x3) tma_prefetch_map(&tmA_lo);
+      if constexpr (S::kBParts == 2) tma_prefetch_map(&tmB_lo);
     }
     __syncwarp();
     tmem_alloc(tmem_slot, kTmemCols);
@@ -304,13 +326,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t ph = (kb / kStages) & 1;
         const int kx = (kb_first + kb) * S::kBK;
         if (kb >= early) {
-          if (!mbar_wait(&empty[s], ph ^ 1, status, kErrTimeoutProducer)) break;
+          if (!mbar_wait(&empty[s], ph ^ 1, status, kErrTimeoutProducer, wl)) break;
           mbar_arrive_expect_tx(&full[s], S::kStageBytes);
           tma_load_3d(a_tile(s, 0), &tmA, &full[s], kx, m0, g);
           if constexpr (P == kTF32x3) tma_load_3d(a_tile(s, 1), &tmA_lo, &full[s], kx, m0, g);
         }
         tma_load_3d(b_tile(s, 0), &tmB, &full[s], kx, n0, g);
-        if constexpr (P == kTF32x3) tma_load_3d(b_tile(s, 1), &tmB_lo, &full[s], kx, n0, g);
+        if constexpr (S::kBParts == 2) tma_load_3d(b_tile(s, 1), &tmB_lo, &full[s], kx, n0, g);
         issued = kb + 1;
       }
       // Drain: every slot's most recent fill must have landed before the CTA exits.
@@ -341,15 +363,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t d = tmem;
         if constexpr (kSliced && !kStepSliced) {
           const int buf = slice % kAccBufs;
-          if (first && !mbar_wait(&acc_empty[buf], ((slice / kAccBufs) & 1) ^ 1, status, kErrTimeoutMma)) break;
+          if (first && !mbar_wait(&acc_empty[buf], ((slice / kAccBufs) & 1) ^ 1, status, kErrTimeoutMma, wl)) break;
           d = tmem + static_cast<uint32_t>(buf * BN);
         }
-        if (!mbar_wait(&full[s], ph, status, kErrTimeoutMma)) break;
+        if (!mbar_wait(&full[s], ph, status, kErrTimeoutMma, wl)) break;
         tc_fence_after();
         const uint32_t a0 = smem_addr(a_tile(s, 0));
         const uint32_t b0 = smem_addr(b_tile(s, 0));
         const uint32_t a1 = smem_addr(a_tile(s, P == kTF32x3 ? 1 : 0));
-        const uint32_t b1 = smem_addr(b_tile(s, P == kTF32x3 ? 1 : 0));
+        const uint32_t b1 = smem_addr(b_tile(s, S::kBParts == 2 ? 1 : 0));
         bool timed_out = false;
         if constexpr (kStepSliced) {
           // one slice per k-step, each into the next of kAccBufs buffers
@@ -357,7 +379,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
             const int sl = q + static_cast<int>(kk);
             const int buf = sl % kAccBufs;
-            if (!mbar_wait(&acc_empty[buf], ((sl / kAccBufs) & 1) ^ 1, status, kErrTimeoutMma)) {
+            if (!mbar_wait(&acc_empty[buf], ((sl / kAccBufs) & 1) ^ 1, status, kErrTimeoutMma, wl)) {
               timed_out = true;
               break;
             }
@@ -392,6 +414,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
             const uint32_t off = kk * 32;  // 32 bytes of K per MMA
             const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+            if constexpr (kBLo) {  // A * B_lo into the lo accumulator, over all of K
+              const uint32_t lacc = (kb == 0 && kk == 0) ? 0u : 1u;
+              if constexpr (P == kBF16)
+                umma_bf16(tmem + kLoCol, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, lacc);
+              else
+                umma_tf32(tmem + kLoCol, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, lacc);
+            }
             if constexpr (P == kBF16) {
               umma_bf16(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
             } else if constexpr (P == kFP8) {
@@ -408,6 +437,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // also on a timeout: the epilogue must not wait forever
       if constexpr (!kSliced) umma_commit(&acc_full[0]);
+      // TMEM is freed (and, split, the ring handed to the partner) only once every MMA
+      // issued has completed, whether or not a wait gave up
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, status, kErrTimeoutDrain);
     }
     if constexpr (kSplit) {  // the epilogue's two cluster barriers
       __syncwarp();
@@ -440,7 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int buf = sl % kAccBufs;
         // all epilogue threads agree on whether the slice arrived
         ok = epilogue_bar_and(
-            mbar_wait(&acc_full[buf], (sl / kAccBufs) & 1, status, kErrTimeoutEpilogue));
+            mbar_wait(&acc_full[buf], (sl / kAccBufs) & 1, status, kErrTimeoutEpilogue, wl));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -454,6 +487,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epilogue_bar_sync();
         if (et == 0) mbar_arrive(&acc_empty[buf]);
       }
+      if constexpr (kBLo) {
+        // the last slice's commit covered every MMA, the B_lo ones included
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            float v[32];
+            tmem_ld_32x32(lane_base + static_cast<uint32_t>(kLoCol + (2 * c + half) * 32), v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c][i] += v[i];
+          }
+        }
+      }
       if (ok) {
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
@@ -461,7 +507,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     } else {
-      ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue));
+      ok = epilogue_bar_and(mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue, wl));
       tc_fence_after();
       if constexpr (kSplit) {
         // the MMAs are complete: this CTA's ring is idle; inputs of the epilogue are

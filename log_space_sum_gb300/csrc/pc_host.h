@@ -22,6 +22,10 @@ void clear_error();
 // looked up once per device).
 unsigned* device_status_word();
 
+// Streaming multiprocessors of the current device (cached per device; 148 if the device
+// cannot be queried). The planners size grids and K-range splits by it.
+int num_sms();
+
 // A library-owned stream of the current device for work that runs beside the caller's
 // stream within one call: fork() makes it wait for everything issued on `main` so far,
 // join() makes `main` wait for everything issued on it since. Both are event waits, so a
@@ -39,6 +43,19 @@ void profile_end(int slot, cudaStream_t s, int kind, long long flops);
 // record of their own): events between them would serialise their programmatic overlap.
 int profile_group_begin(cudaStream_t s);
 void profile_group_end(int slot, cudaStream_t s, int kind, long long flops, int launches);
+
+// One profiler record around the memory-bound launches of a scope (none unless
+// pc_profile_start is active): `bytes` = their algorithmic bytes.
+struct ProfileScope {
+  int slot;
+  cudaStream_t s;
+  int kind;
+  long long bytes;
+  ProfileScope(cudaStream_t s_, int kind_, long long bytes_) : slot(profile_begin(s_)), s(s_), kind(kind_), bytes(bytes_) {}
+  ~ProfileScope() { profile_end(slot, s, kind, bytes); }
+  ProfileScope(const ProfileScope&) = delete;
+  ProfileScope& operator=(const ProfileScope&) = delete;
+};
 
 #define PC_CHECK(cond, st, ...)                 \
   do {                                          \
@@ -86,9 +103,9 @@ struct Operand {
   void* ptr = nullptr;
   long long rows = 0, cols = 0, ld = 0, groups = 1;
   size_t lo_elems = 0;
-  static size_t bytes(pc_precision_t p, long long groups, long long rows, long long cols) {
+  static size_t bytes(pc_precision_t p, long long groups, long long rows, long long cols, int parts = 0) {
     const long long ld = round_up(cols > 0 ? cols : 1, 64);
-    return size_t(groups) * rows * ld * operand_elem_bytes(p) * operand_parts(p);
+    return size_t(groups) * rows * ld * operand_elem_bytes(p) * (parts > 0 ? parts : operand_parts(p));
   }
 };
 
@@ -103,15 +120,17 @@ struct Carver {
     used += n;
     return p;
   }
-  Operand operand(pc_precision_t p, long long groups, long long rows, long long cols) {
+  // parts = 2 gives a bf16 or TF32 operand a lo part (hi + lo, as 3xTF32 always has)
+  Operand operand(pc_precision_t p, long long groups, long long rows, long long cols, int parts = 0) {
     Operand o;
     o.groups = groups;
     o.rows = rows;
     o.cols = cols;
     o.ld = round_up(cols > 0 ? cols : 1, 64);
+    const int np = parts > 0 ? parts : operand_parts(p);
     const size_t part = size_t(groups) * rows * o.ld;
-    o.lo_elems = operand_parts(p) == 2 ? part : 0;
-    o.ptr = take(Operand::bytes(p, groups, rows, cols));
+    o.lo_elems = np == 2 ? part : 0;
+    o.ptr = take(Operand::bytes(p, groups, rows, cols, np));
     return o;
   }
 };

@@ -62,6 +62,14 @@ inline pc_status_t encode_maps(OperandMaps* m, const Operand& op, pc_precision_t
   return PC_OK;
 }
 
+// Both parts of an operand that has a lo part (Carver::operand with parts = 2).
+inline pc_status_t encode_maps_hilo(OperandMaps* m, const Operand& op, pc_precision_t p, int box_rows) {
+  if (op.lo_elems == 0) return set_error(PC_ERR_CUDA, "operand has no lo part");
+  pc_status_t st = encode_operand_map(&m->hi, op, p, box_rows, 0);
+  if (st != PC_OK) return st;
+  return encode_operand_map(&m->lo, op, p, box_rows, 1);
+}
+
 inline int num_k_blocks(long long K, pc_precision_t p) {
   const int bk = 128 / operand_elem_bytes(p);
   return static_cast<int>((K + bk - 1) / bk);
@@ -123,7 +131,7 @@ pc_status_t rows_to_operand(const float* src, long long src_ld, long long src_gs
     const dim3 grid(static_cast<unsigned>(static_cast<long long>(G) * R), cdiv(C / 4, 256));
     k_rows_to_operand4<P><<<grid, 256, 0, s>>>(src, src_ld, src_gs, R, C, dst.ptr, dst.ld, dst.lo_elems, gmap);
   } else {
-    const unsigned blocks = static_cast<unsigned>((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
+    const unsigned blocks = static_cast<unsigned>((total + 255) / 256 < 16ll * num_sms() ? (total + 255) / 256 : 16ll * num_sms());
     k_rows_to_operand<P><<<blocks, 256, 0, s>>>(src, src_ld, src_gs, G, R, C, dst.ptr, dst.ld, dst.lo_elems, gmap);
   }
   PC_LAUNCH_CHECK();

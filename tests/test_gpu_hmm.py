@@ -1,14 +1,13 @@
 """GPU parity of the whole HMM circuit (pc_hmm_fwd_bwd through the C ABI) against the
 float64 oracle: the tiny workload in every mode, ragged and degenerate shapes, the
-4096-state workload at batch 128 (every output) and 512 (sampled log-likelihoods,
-flow invariants), the 1024-state, 64-position workload at batch 512 (every output), and
-the uniform-emission closed form."""
+4096-state workload at batch 128 and 512 (every output), the 1024-state, 64-position
+workload at batch 512 (every output), and the uniform-emission closed form."""
 import numpy as np
 import pytest
 import torch
 
 import log_space_sum_gb300 as pc
-from oracle.hmm import hmm_fwd_bwd, hmm_ll
+from oracle.hmm import hmm_fwd_bwd
 from tolerances import FLOW_TOL, LL_TOL, MODES, flow_err, ll_err
 from workloads import hmm, hmm_1024x64, hmm_inputs, tiny_hmm
 
@@ -155,15 +154,24 @@ def test_hmm_1024x64_batch512_every_output(hmm1024, mode):
     assert max(errs[1:]) <= FLOW_TOL[mode]
 
 
-@pytest.mark.parametrize("mode", MODES)
-def test_hmm_4096_batch512_sampled_and_invariants(mode):
+@pytest.fixture(scope="module")
+def hmm512():
     d = hmm(512)
+    return d, _oracle(d)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_hmm_4096_batch512_every_output(hmm512, mode):
+    # the benchmarked configuration: in auto mode the chains take the 128 x 256 split-K
+    # pairs that stage half of the emission block during the exchange
+    d, (rl, rpi, rA, rE) = hmm512
     ll, dpi, dA, dE = _gpu_run(d, mode)
+    errs = ll_err(ll, rl), flow_err(dpi, rpi), flow_err(dA, rA), flow_err(dE, rE)
+    print(f"hmm4096 B512 {mode}: ll {errs[0]:.3e} dpi {errs[1]:.3e} dA {errs[2]:.3e} dE {errs[3]:.3e}")
+    assert errs[0] <= LL_TOL[mode]
+    assert max(errs[1:]) <= FLOW_TOL[mode]
+    # flows are posterior expected counts: their totals are exact at any size
     B, T = d["tokens"].shape
-    pick = np.random.default_rng(90).choice(B, size=6, replace=False)
-    ref = hmm_ll(d["pi"], d["A"], d["E"], d["tokens"][pick])
-    assert ll_err(ll[pick], ref) <= LL_TOL[mode]
-    # flows are posterior expected counts: exact totals at any size
     tol = {"auto": 1e-2, "tf32": 1e-3, "fp32": 1e-5}[mode]
     assert abs(dpi.astype(np.float64).sum() - B) <= tol * B
     assert abs(dA.astype(np.float64).sum() - B * (T - 1)) <= tol * B * (T - 1)
