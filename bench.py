@@ -59,8 +59,23 @@ DTYPE = {"auto": "bf16", "tf32": "tf32", "fp32": "3xtf32"}
 # nominal dense tensor rates relative to bf16 (2.25 PF bf16, 1.1 PF tf32)
 TF32_OVER_BF16 = 1.1 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# special-function unit: 16 exp2 results per SM per clock, 152 SMs (GB300)
-MUFU_PER_SM_CLK, N_SMS = 16, 152
+# special-function unit: 16 exp2 results per SM per clock (the SM count comes from the device)
+MUFU_PER_SM_CLK = 16
+MEMORY_KINDS = ("hmm_mem", "hclt_mem", "em_mstep")
+
+
+def choose_bf16_peak(peaks, clk):
+    """The measured bf16 peak that applies to this run: the burst figure (a kernel timed
+    at full clock), unless the clocks sampled during the timed region show a power-capped
+    run well below the maximum, where the sustained figure (measured under the power cap)
+    applies. Returns (TFLOP/s, which)."""
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    if clk and clk.get("sm_mhz") and clk.get("sm_max_mhz"):
+        capped = "sw_power_cap" in (clk.get("reasons") or [])
+        if capped and clk["sm_mhz"] < 0.9 * clk["sm_max_mhz"]:
+            return sustained, "bf16 sustained (power-capped clocks)"
+    return burst, "bf16 burst"
 
 
 def parse():
@@ -71,6 +86,8 @@ def parse():
     ap.add_argument("--precision", default="auto", choices=["auto", "tf32", "fp32"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--other-modes", type=int, default=1,
+                    help="with --precision auto, also time the tf32 and fp32 modes (extra keys)")
     ap.add_argument("--workload", default="hmm",
                     choices=["hmm", "hmm1024", "layer", "hclt", "lowrank", "lowrank_sum_exp", "hmm_lowrank", "mstep"])
     ap.add_argument("--flow-fp8", action="store_true",
@@ -148,6 +165,14 @@ class HmmWorkload(Workload):
             dev_in.copy_(host_in, non_blocking=True)
             step(dev_in)
             host_out.copy_(out["ll"], non_blocking=True)
+        # the same, reading the flows back too (an EM loop keeps them on the device)
+        host_flows = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items() if k != "ll"}
+
+        def e2e_flows():
+            e2e()
+            for k, h in host_flows.items():
+                h.copy_(out[k], non_blocking=True)
+        self.e2e_flows = (e2e_flows, host_out.numel() * 8 + sum(h.numel() * 4 for h in host_flows.values()))
         return step, e2e, host_in.numel() * 4, host_out.numel() * 8
 
 
@@ -678,7 +703,23 @@ def run_ours(args):
         k[0] += ms
         k[1] += fl
         k[2] += nl
-    dom = max(by_kind, key=lambda k: by_kind[k][0])
+    # the dominant contraction kind (memory-bound kinds are reported in the hbm block)
+    cands = [k for k in by_kind if k not in MEMORY_KINDS] or list(by_kind)
+    dom = max(cands, key=lambda k: by_kind[k][0])
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # the memory-bound passes of the step (operand copies, transposes, gathers, product
+    # and flow kernels): algorithmic bytes over their summed device time
+    mem = {k: v for k, v in by_kind.items() if k in MEMORY_KINDS and k != dom}
+    hbm = None
+    if mem:
+        mb = sum(v[1] for v in mem.values())
+        mms = sum(v[0] for v in mem.values())
+        hpeak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        hbm = {"kinds": sorted(mem), "launches_per_step": sum(v[2] for v in mem.values()) / args.steps,
+               "bytes_per_step": mb / args.steps, "ms_per_step": mms / args.steps,
+               "achieved": mb / (mms / 1e3) / 1e9, "peak": hpeak, "unit": "GB/s",
+               "frac": mb / (mms / 1e3) / 1e9 / hpeak, "peak_source": f"{peak_src} copy bandwidth",
+               "note": "summed event time of each memory-bound launch (side-stream ones overlap the chain)"}
     dms, dfl, dn = by_kind[dom]
     if w.roofline_bound == "hbm":
         # the kind's recorded count is its algorithmic bytes (read once, written once)
@@ -696,28 +737,30 @@ def run_ours(args):
         cfg = w.config()
         exps = cfg["M"] * cfg["N"] * cfg["B"]
         mhz = (clk or {}).get("sm_max_mhz") or 2070.0
-        peak = N_SMS * MUFU_PER_SM_CLK * mhz * 1e6 / 1e12
+        peak = n_sms * MUFU_PER_SM_CLK * mhz * 1e6 / 1e12
         achieved = exps * dn / (dms / 1e3) / 1e12
         roofline = {
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "Texp/s", "frac": achieved / peak,
             "traffic": recorded_traffic(dom, args.precision, w.name), "kernel": f"k_lowrank* ({dom})",
             "launches_timed": dn, "ms_per_launch": dms / dn,
-            "peak_source": f"derived: {N_SMS} SMs x {MUFU_PER_SM_CLK} exp/clk x {mhz:.0f} MHz",
+            "peak_source": f"derived: {n_sms} SMs x {MUFU_PER_SM_CLK} exp/clk x {mhz:.0f} MHz",
             "share_of_step": sum(v[0] for v in by_kind.values()) / sum(ms_steps_prof) if world == 1 else None,
         }
     else:
         achieved = dfl / (dms / 1e3) / 1e12
-        bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        bf16_peak, which = choose_bf16_peak(peaks, clk)
         peak = bf16_peak if args.precision == "auto" else bf16_peak * TF32_OVER_BF16
+        con = {k: v for k, v in by_kind.items() if k not in MEMORY_KINDS}
         roofline = {
             "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": recorded_traffic(dom, args.precision, w.name), "kernel": f"k_umma_gemm ({dom})",
             "launches_timed": dn, "ms_per_launch": dms / dn,
-            "peak_source": f"{peak_src} bf16 sustained" + ("" if args.precision == "auto"
-                                                           else " x 1.1/2.25 (nominal tf32/bf16)"),
-            "all_contractions_frac": sum(v[1] for v in by_kind.values()) / (sum(v[0] for v in by_kind.values())
-                                                                           / 1e3) / 1e12 / peak,
-            "share_of_step": sum(v[0] for v in by_kind.values()) / sum(ms_steps_prof) if world == 1 else None,
+            "peak_source": f"{peak_src} {which}" + ("" if args.precision == "auto"
+                                                     else " x 1.1/2.25 (nominal tf32/bf16)"),
+            "sm_mhz_during_timed_region": (clk or {}).get("sm_mhz"),
+            "all_contractions_frac": sum(v[1] for v in con.values()) / (sum(v[0] for v in con.values())
+                                                                       / 1e3) / 1e12 / peak,
+            "share_of_step": sum(v[0] for v in con.values()) / sum(ms_steps_prof) if world == 1 else None,
         }
         if args.precision == "fp32":
             roofline["issued_frac"] = 3 * achieved / peak
@@ -732,6 +775,45 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         e2e_ms.append(1e3 * (time.perf_counter() - t0))
     e2e_value = job_rate(world, w.batch, 1, max_over_ranks(statistics.mean(e2e_ms), world, dev))
+    e2e_flows = None
+    if getattr(w, "e2e_flows", None):
+        fn, fbytes = w.e2e_flows
+        fms = []
+        for i in range(max(3, min(args.steps, 10))):
+            flush.fill_(i & 0xFF)
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            fms.append(1e3 * (time.perf_counter() - t0))
+        e2e_flows = {"value": job_rate(world, w.batch, 1, max_over_ranks(statistics.mean(fms), world, dev)),
+                     "unit": w.unit, "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(fbytes)}
+
+    # the other precision modes of the same workload, same timing rules (value only)
+    modes = None
+    if args.precision == "auto" and args.other_modes and w.name in ("hmm", "hmm1024", "hclt"):
+        modes = {}
+        for prec in ("tf32", "fp32"):
+            mstep, *_ = w.device(pc, d, dev, prec)
+            for _ in range(3):
+                mstep()
+            torch.cuda.synchronize(dev)
+            k = max(3, min(args.steps, 10))
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            for i in range(k):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                mstep()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize(dev)
+            pc.device_status(dev)
+            tot = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
+            modes[prec] = {"value": job_rate(world, w.batch, k, tot), "ms_per_step": tot / k, "steps": k,
+                           "warmup": 3, "dtype": w.dtype(prec)}
+            del mstep
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -755,6 +837,9 @@ def run_ours(args):
                     "d2h_bytes_per_step": int(d2h_bytes)},
             "gpu_launches": int(launches),
             "roofline": roofline,
+            "hbm": hbm,
+            "e2e_with_flows": e2e_flows,
+            "modes": modes,
             "cpu_baseline": cpu,
             "step_ms": {"min": min(ms_steps), "median": statistics.median(ms_steps), "max": max(ms_steps),
                         "instrumented_median": statistics.median(ms_steps_prof)},
