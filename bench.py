@@ -313,6 +313,17 @@ class HcltWorkload(Workload):
             dev_in.copy_(host_in, non_blocking=True)
             step(dev_in)
             host_out.copy_(out["ll"], non_blocking=True)
+
+        # the same step with the parameters prepared once (pc_hclt_prepare): an EM
+        # iteration's batches share W and E
+        prep = {}
+
+        def prepare():
+            prep["p"] = pc.hclt_prepare(d["parent"], t["W"], t["E"], precision=prec)
+
+        def step_prepared():
+            pc.hclt_fwd_bwd(d["parent"], t["data"], t["pi"], t["W"], None, precision=prec, prepared=prep["p"], **out)
+        self.prepared = (prepare, step_prepared)
         return step, e2e, host_in.numel() * 4, host_out.numel() * 8
 
 
@@ -789,6 +800,36 @@ def run_ours(args):
         e2e_flows = {"value": job_rate(world, w.batch, 1, max_over_ranks(statistics.mean(fms), world, dev)),
                      "unit": w.unit, "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(fbytes)}
 
+    # a workload whose parameters can be prepared once per EM iteration (the HCLT): the
+    # per-batch step with prepared parameters, and the preparation's own time
+    prepared = None
+    if getattr(w, "prepared", None):
+        prep_fn, pstep = w.prepared
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        prep_fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        prep_ms = e0.elapsed_time(e1)
+        for _ in range(3):
+            pstep()
+        torch.cuda.synchronize(dev)
+        k = max(3, min(args.steps, 10))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        for i in range(k):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            pstep()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        pc.device_status(dev)
+        tot = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
+        prepared = {"value": job_rate(world, w.batch, k, tot), "ms_per_step": tot / k, "steps": k,
+                    "prepare_ms": prep_ms,
+                    "note": "W and E converted once per EM iteration (pc_hclt_prepare, prepare_ms) and read by "
+                            "every batch's pc_hclt_fwd_bwd_prepared; value = the per-batch step"}
+
     # the other precision modes of the same workload, same timing rules (value only)
     modes = None
     if args.precision == "auto" and args.other_modes and w.name in ("hmm", "hmm1024", "hclt"):
@@ -839,6 +880,7 @@ def run_ours(args):
             "roofline": roofline,
             "hbm": hbm,
             "e2e_with_flows": e2e_flows,
+            "prepared_parameters": prepared,
             "modes": modes,
             "cpu_baseline": cpu,
             "step_ms": {"min": min(ms_steps), "median": statistics.median(ms_steps), "max": max(ms_steps),

@@ -71,7 +71,8 @@ typedef enum {
   PC_ERR_WORKSPACE = 5,         /* workspace NULL or smaller than the query's size */
   PC_ERR_UNSUPPORTED = 6,       /* a valid request outside the library's limits */
   PC_ERR_CUDA = 7,              /* a CUDA call failed (launch or device query) */
-  PC_ERR_TIMEOUT = 8            /* a device-side wait ran out (see pc_device_status) */
+  PC_ERR_TIMEOUT = 8,           /* a device-side wait ran out (see pc_device_status) */
+  PC_ERR_RANGE = 9              /* an HMM sample left the exactly-scaled range (see pc_hmm_fwd_bwd) */
 } pc_status_t;
 
 /* Library version string, e.g. "pcsum 0.1 sm_103a". Static storage. */
@@ -89,8 +90,10 @@ PCSUM_API const char* pc_last_error(void);
 PCSUM_API unsigned long long pc_launch_count(void);
 
 /* Synchronises `stream`, then reads and clears the device status word of the current
- * device. Returns PC_OK, or PC_ERR_TIMEOUT if a kernel gave up a bounded wait since
- * the last read, or PC_ERR_CUDA. Diagnostic; not for the hot path. */
+ * device. Returns PC_OK; PC_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
+ * read; else PC_ERR_RANGE if an HMM call flagged a sample whose values left the range its
+ * per-layer scaling keeps exact (that sample's LL is NaN and it passed no flow); or
+ * PC_ERR_CUDA. Diagnostic; not for the hot path. */
 PCSUM_API pc_status_t pc_device_status(pc_stream_t stream);
 
 /* Limit, in nanoseconds, of the first waits of the tensor-core contraction kernel on the
@@ -194,10 +197,16 @@ PCSUM_API pc_status_t pc_sum_layer_fwd_noalloc(int G, int M, int N, int B, const
  *                                           expected counts); each may be NULL. When
  *                                           all three are NULL only ll is computed.
  * Limits: 1 <= H <= 16384, 1 <= T <= 4096, 1 <= V <= 65536, 1 <= B <= 65536.
- * Tokens outside [0, V) are undefined behaviour. Numerical range: the per-layer
- * rescaling keeps node values in float32 range when, at every position, the most
- * likely state's value is within e^-80 of max_k E[k,x_t] * sum_l A[k,l] times the
- * previous position's maximum; the per-sample log-offsets are accumulated in double.
+ * Tokens outside [0, V) are undefined behaviour. Numerical range: every layer scales
+ * a sample's values by 1 / (max_k E[k,x_t] * sum_l A[k,l] times the previous position's
+ * maximum) (at most 2^100), an upper bound of the largest value, and the per-sample
+ * log-offsets accumulate in double; exact zeros (in E, A or pi) give exact zeros, and a
+ * sequence of probability 0 gets ll = -inf and passes no flow. The results are exact
+ * (to the mode's rounding) while at every position the largest scaled value stays
+ * above 2^-80, i.e. the bound is looser than e^-55 nowhere. A sample for which that
+ * fails is flagged instead of returning a wrong value: its ll is NaN, it passes no
+ * flow (the other samples' flows are unaffected) and pc_device_status reports
+ * PC_ERR_RANGE.
  * ---------------------------------------------------------------------------- */
 PCSUM_API pc_status_t pc_hmm_workspace(int H, int T, int V, int B, pc_precision_t prec, size_t* bytes);
 
@@ -222,8 +231,10 @@ PCSUM_API pc_status_t pc_hmm_fwd_bwd(int H, int T, int V, int B, const int32_t* 
  *   dpi [H], dW [nvars][H][H] (dW[0] = 0), dE [nvars][H][C]   EM flows summed over
  *                                 the batch; each may be NULL; all NULL = ll only.
  * Limits: 1 <= nvars <= 65535, 1 <= H <= 8192, 1 <= C <= 8192, 1 <= B <= 65535.
- * The call copies a few KB of tree plan host->device with cudaMemcpyAsync from
- * pageable memory, so unlike the other entry points it is not stream-capturable.
+ * The tree plan the call derives from `parent` (a few KB) reaches the device inside
+ * kernel arguments, not through a host-to-device copy, so the call can be captured
+ * into a CUDA graph like the others; a captured graph replays the tree it was
+ * captured with.
  * ---------------------------------------------------------------------------- */
 PCSUM_API pc_status_t pc_hclt_workspace(int nvars, int H, int C, int B, pc_precision_t prec,
                                         size_t* bytes);
@@ -233,6 +244,37 @@ PCSUM_API pc_status_t pc_hclt_fwd_bwd(int nvars, int H, int C, int B, const int3
                                       const float* E, double* ll, float* dpi, float* dW, float* dE,
                                       int accumulate, pc_precision_t prec, void* ws,
                                       size_t ws_bytes, pc_stream_t stream);
+
+/* The HCLT's parameters prepared once for many calls. Within an EM iteration every batch
+ * reads the same W and E, and pc_hclt_fwd_bwd converts them on every call into the
+ * formats its contractions read: W's per-edge operand copy in the tree's level order and
+ * its transpose (2 x nvars x H x H values) and E transposed per variable. With
+ * pc_hclt_prepare run once after the parameters change, pc_hclt_fwd_bwd_prepared skips
+ * those conversions and computes the same results as pc_hclt_fwd_bwd.
+ *
+ * pc_hclt_prepare_bytes: the size of the prepared buffer for the tree size, H, C and
+ *   precision (errors as pc_hclt_workspace).
+ * pc_hclt_prepare: writes the prepared buffer `prep` (caller-owned device memory of at
+ *   least that size) from parent (HOST, as for pc_hclt_fwd_bwd), W and E; asynchronous
+ *   on `stream`, capturable. Errors: PC_ERR_NULL, PC_ERR_SHAPE (sizes or parent),
+ *   PC_ERR_WORKSPACE (prep NULL or too small), PC_ERR_UNKNOWN_PRECISION.
+ * pc_hclt_prepared_workspace: the workspace of pc_hclt_fwd_bwd_prepared (smaller than
+ *   pc_hclt_workspace's by the prepared data).
+ * pc_hclt_fwd_bwd_prepared: pc_hclt_fwd_bwd with `prep` in place of E. W is still read
+ *   (the parameter flows are W times the contraction). `prep` must have been written by
+ *   pc_hclt_prepare for the same parent, W, E, sizes and precision, and W and E must not
+ *   have changed since: the library cannot check that without reading device memory. */
+PCSUM_API pc_status_t pc_hclt_prepare_bytes(int nvars, int H, int C, pc_precision_t prec, size_t* bytes);
+PCSUM_API pc_status_t pc_hclt_prepare(int nvars, int H, int C, const int32_t* parent, const float* W,
+                                      const float* E, pc_precision_t prec, void* prep, size_t prep_bytes,
+                                      pc_stream_t stream);
+PCSUM_API pc_status_t pc_hclt_prepared_workspace(int nvars, int H, int C, int B, pc_precision_t prec,
+                                                 size_t* bytes);
+PCSUM_API pc_status_t pc_hclt_fwd_bwd_prepared(int nvars, int H, int C, int B, const int32_t* parent,
+                                               const int32_t* data, const float* pi, const float* W,
+                                               const void* prep, size_t prep_bytes, double* ll, float* dpi,
+                                               float* dW, float* dE, int accumulate, pc_precision_t prec,
+                                               void* ws, size_t ws_bytes, pc_stream_t stream);
 
 /* ------------------------------------------------------------------------------
  * LowRank "exp_sum" per-sample scale on a dense sum layer with shared children

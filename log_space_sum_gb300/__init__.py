@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     device_status,
     em_normalize,
     hclt_fwd_bwd,
+    hclt_prepare,
     hmm_fwd_bwd,
     hmm_lowrank_fwd_bwd,
     lowrank_exp_sum_bwd,

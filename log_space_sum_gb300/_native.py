@@ -16,7 +16,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "pcsum.h")
 STATUS = {
     0: "PC_OK", 1: "PC_ERR_NULL", 2: "PC_ERR_SHAPE", 3: "PC_ERR_ALIGNMENT",
     4: "PC_ERR_UNKNOWN_PRECISION", 5: "PC_ERR_WORKSPACE", 6: "PC_ERR_UNSUPPORTED",
-    7: "PC_ERR_CUDA", 8: "PC_ERR_TIMEOUT",
+    7: "PC_ERR_CUDA", 8: "PC_ERR_TIMEOUT", 9: "PC_ERR_RANGE",
 }
 
 KINDS = {
@@ -47,6 +47,10 @@ SIGNATURES = {
     "pc_hmm_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
     "pc_hclt_workspace": [_i, _i, _i, _i, _i, _p],
     "pc_hclt_fwd_bwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
+    "pc_hclt_prepare_bytes": [_i, _i, _i, _i, _p],
+    "pc_hclt_prepare": [_i, _i, _i, _p, _p, _p, _i, _p, _sz, _p],
+    "pc_hclt_prepared_workspace": [_i, _i, _i, _i, _i, _p],
+    "pc_hclt_fwd_bwd_prepared": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p, _p, _p, _p, _i, _i, _p, _sz, _p],
     "pc_lowrank_exp_sum_workspace": [_i, _i, _i, _i, _i, _i, _p],
     "pc_lowrank_sum_exp_workspace": [_i, _i, _i, _i, _i, _i, _p],
     "pc_lowrank_sum_exp_fwd": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p],

@@ -203,11 +203,42 @@ def hmm_lowrank_fwd_bwd(tokens, pi, A, E, FA, FB, precision="auto", flows=True, 
 
 
 # -------------------------------------------------------------------------- HCLT
+class HcltPrepared:
+    """The HCLT's parameters in its contractions' formats (pc_hclt_prepare): reusable by
+    every hclt_fwd_bwd call with the same tree, W, E and precision until they change."""
+
+    def __init__(self, buf, parent, nvars, H, C, prec):
+        self.buf, self.parent, self.nvars, self.H, self.C, self.prec = buf, parent, nvars, H, C, prec
+
+
+def _host_parent(parent):
+    import numpy as np
+    return np.ascontiguousarray(np.asarray(parent.cpu() if isinstance(parent, torch.Tensor) else parent,
+                                           dtype=np.int32))
+
+
+def hclt_prepare(parent, W, E, precision="auto"):
+    """Converts W and E once into the formats the HCLT's contractions read (pc_hclt_prepare)."""
+    prec = precision_code(precision)
+    _check(W, "W")
+    dev = W.device
+    _check(E, "E", device=dev)
+    par = _host_parent(parent)
+    n, H, Ccat = E.shape
+    nb = _query("pc_hclt_prepare_bytes", n, H, Ccat, prec)
+    buf = torch.empty(nb, dtype=torch.uint8, device=dev)
+    N.call("pc_hclt_prepare", n, H, Ccat, par.ctypes.data_as(C.c_void_p), _ptr(W), _ptr(E), prec, _ptr(buf),
+           buf.numel(), _stream(dev))
+    return HcltPrepared(buf, par, n, H, Ccat, prec)
+
+
 def hclt_fwd_bwd(parent, data, pi, W, E, precision="auto", flows=True, ll=None, dpi=None, dW=None, dE=None,
-                 accumulate=False, **removed):
+                 accumulate=False, prepared=None, **removed):
     """Whole HCLT circuit (pc_hclt_fwd_bwd). ``parent`` is a host int sequence
     (parent[0] = -1, parent[i] in [0, i)); data [B, nvars] int32 on the GPU; W
-    [nvars, H, H]; E [nvars, H, C]. Returns (ll [B] float64, dpi, dW, dE)."""
+    [nvars, H, H]; E [nvars, H, C]. Returns (ll [B] float64, dpi, dW, dE). With
+    ``prepared`` (from hclt_prepare for the same parent, W, E and precision) the call
+    uses pc_hclt_fwd_bwd_prepared and E may be None."""
     import numpy as np
 
     _removed_flags(removed, "hclt_fwd_bwd")
@@ -216,11 +247,15 @@ def hclt_fwd_bwd(parent, data, pi, W, E, precision="auto", flows=True, ll=None, 
     dev = W.device
     _check(data, "data", dtype=torch.int32, device=dev)
     _check(pi, "pi", device=dev)
-    _check(E, "E", device=dev)
-    par = np.ascontiguousarray(np.asarray(parent.cpu() if isinstance(parent, torch.Tensor) else parent,
-                                          dtype=np.int32))
+    par = _host_parent(parent)
     B, n = data.shape
-    _, H, Ccat = E.shape
+    if prepared is not None:
+        if prepared.prec != prec or prepared.nvars != n or not np.array_equal(prepared.parent, par):
+            raise ValueError("prepared parameters were made for another tree or precision")
+        H, Ccat = prepared.H, prepared.C
+    else:
+        _check(E, "E", device=dev)
+        _, H, Ccat = E.shape
     if par.shape != (n,):
         raise ValueError(f"parent has shape {par.shape}, expected ({n},)")
     if ll is None:
@@ -234,6 +269,13 @@ def hclt_fwd_bwd(parent, data, pi, W, E, precision="auto", flows=True, ll=None, 
             _check(t, nm, device=dev)
     else:
         dpi = dW = dE = None
+    if prepared is not None:
+        nb = _query("pc_hclt_prepared_workspace", n, H, Ccat, B, prec)
+        ws = workspace(nb, dev)
+        N.call("pc_hclt_fwd_bwd_prepared", n, H, Ccat, B, par.ctypes.data_as(C.c_void_p), _ptr(data), _ptr(pi),
+               _ptr(W), _ptr(prepared.buf), prepared.buf.numel(), _ptr(ll), _ptr(dpi), _ptr(dW), _ptr(dE),
+               int(bool(accumulate)), prec, _ptr(ws), ws.numel(), _stream(dev))
+        return ll, dpi, dW, dE
     nb = _query("pc_hclt_workspace", n, H, Ccat, B, prec)
     ws = workspace(nb, dev)
     N.call("pc_hclt_fwd_bwd", n, H, Ccat, B, par.ctypes.data_as(C.c_void_p), _ptr(data), _ptr(pi), _ptr(W), _ptr(E),

@@ -211,6 +211,7 @@ const char* pc_status_string(pc_status_t s) {
     case PC_ERR_UNSUPPORTED: return "PC_ERR_UNSUPPORTED";
     case PC_ERR_CUDA: return "PC_ERR_CUDA";
     case PC_ERR_TIMEOUT: return "PC_ERR_TIMEOUT";
+    case PC_ERR_RANGE: return "PC_ERR_RANGE";
   }
   return "PC_ERR_UNKNOWN_STATUS";
 }
@@ -229,7 +230,11 @@ pc_status_t pc_device_status(pc_stream_t stream) {
   if (v) {
     const unsigned zero = 0;
     PC_CUDA(cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice));
-    return pc::set_error(PC_ERR_TIMEOUT, "a kernel gave up a bounded wait (status bits 0x%x)", v);
+    if (v & pc::kErrTimeoutBits)
+      return pc::set_error(PC_ERR_TIMEOUT, "a kernel gave up a bounded wait (status bits 0x%x)", v);
+    return pc::set_error(PC_ERR_RANGE,
+                         "an HMM sample left the range its per-layer scaling keeps exact: its ll is NaN and it "
+                         "passed no flow (status bits 0x%x)", v);
   }
   return PC_OK;
 }

@@ -474,6 +474,64 @@ __global__ void k_hclt_dE_gather(int H, int B, int C, const int* __restrict__ va
   }
 }
 
+// dE[v][z][k] (+)= sum over the samples of node s with category k of f[s][b][z], written
+// directly in the caller's [nvars][H][C] layout: one block per (node, 32 latents), one
+// latent per lane. Warp w owns the categories [w C / 8, (w + 1) C / 8) and walks their
+// samples in bucket order (stable, so the sums are deterministic), 32 at a time: their
+// indices in one load, their 32 rows of f (128 bytes each) all in flight together, then a
+// running sum per category into a padded [32][C + 1] shared tile that the block writes
+// out as rows of C categories. For C <= kDEDirectMaxC.
+constexpr int kDEDirectMaxC = 1024;
+__global__ void __launch_bounds__(256) k_hclt_dE_direct(int H, int B, int C, const int* __restrict__ var_of_slot,
+                                                        const int* __restrict__ order, const int* __restrict__ off,
+                                                        const float* __restrict__ F32, float* __restrict__ dE,
+                                                        int accumulate) {
+  extern __shared__ float acc[];  // [32][C + 1], then C + 1 bucket offsets
+  int* offs = reinterpret_cast<int*>(acc + 32 * (C + 1));
+  const int s = blockIdx.x, z0 = blockIdx.y * 32;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int v = var_of_slot[s];
+  const int* ord = order + static_cast<long long>(s) * B;
+  for (int i = threadIdx.x; i <= C; i += blockDim.x) offs[i] = off[static_cast<long long>(s) * (C + 1) + i];
+  for (int i = threadIdx.x; i < 32 * (C + 1); i += blockDim.x) acc[i] = 0.f;
+  __syncthreads();
+  const float* fs = F32 + static_cast<long long>(s) * B * H + z0 + lane;
+  const bool zin = z0 + lane < H;
+  float* arow = acc + lane * (C + 1);
+  const int kb = w * C / 8, ke = (w + 1) * C / 8;
+  int k = kb, knext = offs[k + 1];
+  float run = 0.f;
+  for (int e0 = offs[kb]; e0 < offs[ke]; e0 += 32) {
+    const int n = min(32, offs[ke] - e0);
+    const int my = lane < n ? ord[e0 + lane] : 0;
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int b = __shfl_sync(0xffffffffu, my, j);
+      x[j] = (j < n && zin) ? fs[static_cast<long long>(b) * H] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < n) {
+        while (e0 + j >= knext) {  // the previous category is complete
+          arow[k] = run;
+          run = 0.f;
+          knext = offs[++k + 1];
+        }
+        run += x[j];
+      }
+    }
+  }
+  if (k < ke) arow[k] = run;  // the last non-empty category (later ones stay 0)
+  __syncthreads();
+  const int zmax = min(32, H - z0);
+  for (int i = threadIdx.x; i < zmax * C; i += blockDim.x) {
+    const int zz = i / C, kk = i - zz * C;
+    float* dst = dE + (static_cast<long long>(v) * H + z0 + zz) * C + kk;
+    const float y = acc[zz * (C + 1) + kk];
+    *dst = accumulate ? *dst + y : y;
+  }
+}
 
 // Copies a 128 x 128 block rows[n0 + c][m0 + r] of a row-major [B][H] array into
 // shared memory as S[c][r] (0 outside), so an epilogue thread owning row r reads its 32
@@ -569,6 +627,18 @@ struct EpiHcltElem : EpiNoHooks {
   }
 };
 
+// The host plan reaches the device inside kernel arguments (by value, up to kPlanChunk
+// ints per launch), so that a call issues no host-to-device copy from pageable memory and
+// can be captured into a CUDA graph: the graph keeps the arguments.
+constexpr int kPlanChunk = 6144;  // 24 KB of kernel parameters (the limit is 32 KB)
+struct PlanChunk {
+  int n;
+  int v[kPlanChunk];
+};
+__global__ void k_write_plan(int* __restrict__ dst, const __grid_constant__ PlanChunk c) {
+  for (int i = threadIdx.x; i < c.n; i += blockDim.x) dst[i] = c.v[i];
+}
+
 // ---------------------------------------------------------------- host plan
 struct HcltPlan {
   int n = 0, E = 0, maxh = 0;
@@ -644,13 +714,42 @@ struct HcltWs {
   int *cat_order, *cat_off;
 };
 
-size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool flows, bool want_dE, HcltWs* w) {
+// The parameters in the contractions' formats, prepared once for many calls (pc_hclt_prepare):
+// the slot order of the edges, W's per-edge operand copies in slot order (rows z_parent,
+// K = z_child) and transposed (rows z_child), and E transposed per variable [v][k][z].
+struct HcltPrep {
+  int* var_of_slot;
+  Operand Wop, WopT;
+  float* Et;
+};
+
+size_t carve_prep(void* base, pc_precision_t p, int n, int H, int C, HcltPrep* w) {
+  Carver c(base);
+  *w = HcltPrep{};
+  const long long E1 = n > 1 ? n - 1 : 1;
+  w->var_of_slot = static_cast<int*>(c.take(size_t(n) * 4));
+  w->Wop = c.operand(p, E1, H, H);
+  w->WopT = c.operand(p, E1, H, H);
+  w->Et = static_cast<float*>(c.take(size_t(n) * C * H * 4));
+  return c.used;
+}
+
+size_t hclt_prep_bytes(pc_precision_t p, int n, int H, int C) {
+  HcltPrep w;
+  return carve_prep(nullptr, p, n, H, C, &w) + 256;
+}
+
+// prepared = true: W's operand copies and E transposed come from a prepared buffer.
+size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool flows, bool want_dE, HcltWs* w,
+                  bool prepared = false) {
   Carver c(base);
   *w = HcltWs{};
   const long long E1 = n > 1 ? n - 1 : 1;
   w->plan = static_cast<int*>(c.take(size_t(4 * n + 2) * 4));
-  w->Wop = c.operand(p, E1, H, H);
-  w->Et = static_cast<float*>(c.take(size_t(n) * C * H * 4));
+  if (!prepared) {
+    w->Wop = c.operand(p, E1, H, H);
+    w->Et = static_cast<float*>(c.take(size_t(n) * C * H * 4));
+  }
   w->U32 = static_cast<float*>(c.take(size_t(n) * B * H * 4));
   w->Uop = c.operand(p, E1, B, H, 2);  // hi + lo in every mode (EpiHcltFwd::kBLo)
   w->D = static_cast<float*>(c.take(size_t(E1) * B * H * 4));
@@ -659,13 +758,13 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
   w->rroot = static_cast<float*>(c.take(size_t(B) * 4));
   w->rdot = static_cast<float*>(c.take(size_t(B) * 4));
   if (flows) {
-    w->WopT = c.operand(p, E1, H, H);
+    if (!prepared) w->WopT = c.operand(p, E1, H, H);
     w->F32 = static_cast<float*>(c.take(size_t(n) * B * H * 4));
     w->Gbm = c.operand(p, E1, B, H);
     w->Gnm = c.operand(p, E1, H, B);
     w->Unm = c.operand(p, E1, H, B);
     if (want_dE) {
-      w->dEt = static_cast<float*>(c.take(size_t(n) * C * H * 4));
+      if (C > kDEDirectMaxC) w->dEt = static_cast<float*>(c.take(size_t(n) * C * H * 4));
       w->cat_order = static_cast<int*>(c.take(size_t(n) * B * 4));
       w->cat_off = static_cast<int*>(c.take(size_t(n) * (C + 1) * 4));
     }
@@ -673,9 +772,9 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
   return c.used;
 }
 
-size_t hclt_ws_bytes(pc_precision_t p, int n, int H, int C, int B) {
+size_t hclt_ws_bytes(pc_precision_t p, int n, int H, int C, int B, bool prepared = false) {
   HcltWs w;
-  return carve_hclt(nullptr, p, n, H, C, B, true, true, &w) + 256;
+  return carve_hclt(nullptr, p, n, H, C, B, true, true, &w, prepared) + 256;
 }
 
 pc_status_t check_hclt_shape(int n, int H, int C, int B) {
@@ -688,10 +787,43 @@ pc_status_t check_hclt_shape(int n, int H, int C, int B) {
   return PC_OK;
 }
 
+void* align256(const void* p) {
+  return reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(p) + 255) & ~uintptr_t(255));
+}
+
+// W's operand copies (slot order of the tree) and E transposed, into a prepared buffer.
+template <int P>
+pc_status_t hclt_prepare(int n, int H, int C, const int32_t* parent, const float* W, const float* Em,
+                         pc_precision_t prec, void* prep, cudaStream_t s) {
+  HcltPlan pl;
+  pc_status_t st;
+  if ((st = make_plan(n, parent, &pl)) != PC_OK) return st;
+  HcltPrep w;
+  carve_prep(align256(prep), prec, n, H, C, &w);
+  for (int off = 0; off < n; off += kPlanChunk) {
+    PlanChunk ch;
+    ch.n = std::min(kPlanChunk, n - off);
+    std::copy(pl.var_of_slot.begin() + off, pl.var_of_slot.begin() + off + ch.n, ch.v);
+    k_write_plan<<<1, 256, 0, s>>>(w.var_of_slot + off, ch);
+    PC_LAUNCH_CHECK();
+  }
+  if ((st = transpose_f32(Em, C, static_cast<long long>(H) * C, n, H, C, w.Et, H, 0, s)) != PC_OK) return st;
+  const int E = n - 1;
+  if (E > 0) {
+    if ((st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, w.var_of_slot)) != PC_OK)
+      return st;
+    if ((st = transpose_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.WopT, s, w.var_of_slot)) !=
+        PC_OK)
+      return st;
+  }
+  return PC_OK;
+}
+
+// prep: NULL, or a buffer written by hclt_prepare for the same tree, sizes and precision.
 template <int P>
 pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const int32_t* data, const float* pi,
                      const float* W, const float* Em, double* ll, float* dpi, float* dW, float* dE, int accumulate,
-                     pc_precision_t prec, void* ws, cudaStream_t s) {
+                     pc_precision_t prec, void* ws, cudaStream_t s, const void* prep = nullptr) {
   constexpr int kParamBN = (P == kBF16) ? 256 : 128;
   HcltPlan pl;
   pc_status_t st;
@@ -699,8 +831,14 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
   const bool flows = dpi || dW || dE;
   const bool down = flows && (dW || dE) && n >= 2;  // flows below the root are needed
   HcltWs w;
-  void* base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
-  carve_hclt(base, prec, n, H, C, B, flows, dE != nullptr, &w);
+  carve_hclt(align256(ws), prec, n, H, C, B, flows, dE != nullptr, &w, prep != nullptr);
+  if (prep) {
+    HcltPrep pw;
+    carve_prep(align256(prep), prec, n, H, C, &pw);
+    w.Wop = pw.Wop;
+    w.WopT = pw.WopT;
+    w.Et = pw.Et;
+  }
   const int E = n - 1;
   const int root = n - 1;
   const int* d_var = w.plan + pl.off_var;
@@ -713,17 +851,23 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
   const long long eb2 = 2ll * operand_elem_bytes(prec);                  // the children operand's hi + lo
   const long long HH = static_cast<long long>(H) * H, BH = static_cast<long long>(B) * H;
   const long long CH = static_cast<long long>(C) * H;
-  // the tree plan is a few KB of host data
-  PC_CUDA(cudaMemcpyAsync(w.plan, pl.blob.data(), pl.blob.size() * sizeof(int), cudaMemcpyHostToDevice, s));
+  // the tree plan (a few KB of host data) travels in kernel arguments
+  for (size_t off = 0; off < pl.blob.size(); off += kPlanChunk) {
+    PlanChunk ch;
+    ch.n = static_cast<int>(std::min<size_t>(kPlanChunk, pl.blob.size() - off));
+    std::copy(pl.blob.begin() + off, pl.blob.begin() + off + ch.n, ch.v);
+    k_write_plan<<<1, 256, 0, s>>>(w.plan + off, ch);
+    PC_LAUNCH_CHECK();
+  }
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dW && !accumulate) PC_CUDA(cudaMemsetAsync(dW, 0, size_t(H) * H * 4, s));  // W[0] has no edge
 
   // Et[v][k][z] = E[v][z][k]: the emissions of one category are a contiguous row
-  {
+  if (!prep) {
     ProfileScope ps(s, PC_KIND_HCLT_MEM, 2ll * n * CH * 4);
     if ((st = transpose_f32(Em, C, static_cast<long long>(H) * C, n, H, C, w.Et, H, 0, s)) != PC_OK) return st;
   }
-  if (E > 0) {
+  if (E > 0 && !prep) {
     ProfileScope ps(s, PC_KIND_HCLT_MEM, E * HH * (4 + eb));
     if ((st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, d_var)) != PC_OK) return st;
   }
@@ -781,7 +925,7 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     PC_LAUNCH_CHECK();
   }
   if (down) {
-    {
+    if (!prep) {
       ProfileScope ps(s, PC_KIND_HCLT_MEM, E * HH * (4 + eb));
       if ((st = transpose_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.WopT, s, d_var)) != PC_OK)
         return st;
@@ -841,6 +985,17 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       k_hclt_cat_bucket<<<n, 32, size_t(C + 1) * 4, s>>>(n, B, C, data, d_var, w.cat_order, w.cat_off);
       PC_LAUNCH_CHECK();
     }
+    if (C <= kDEDirectMaxC) {
+      const size_t smem = size_t(33) * (C + 1) * 4;  // the tile and the bucket offsets
+      if (smem > 48 * 1024)
+        PC_CUDA(cudaFuncSetAttribute(k_hclt_dE_direct, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)));
+      ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + (accumulate ? 2 : 1) * n * CH * 4);
+      k_hclt_dE_direct<<<dim3(n, cdiv(H, 32)), 256, smem, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, dE,
+                                                               accumulate);
+      PC_LAUNCH_CHECK();
+      return PC_OK;
+    }
     {
       ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + n * CH * 4);
       k_hclt_dE_gather<<<dim3(n, C), 256, 0, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, w.dEt);
@@ -889,6 +1044,73 @@ pc_status_t pc_hclt_fwd_bwd(int nvars, int H, int C, int B, const int32_t* paren
     default:
       return pc::hclt_run<pc::kTF32x3>(nvars, H, C, B, parent, data, pi, W, E, ll, dpi, dW, dE, accumulate, prec, ws,
                                        s);
+  }
+}
+
+pc_status_t pc_hclt_prepare_bytes(int nvars, int H, int C, pc_precision_t prec, size_t* bytes) {
+  pc::clear_error();
+  PC_CHECK(bytes != nullptr, PC_ERR_NULL, "bytes is NULL");
+  pc_status_t st;
+  if ((st = pc::check_precision(prec)) != PC_OK) return st;
+  if ((st = pc::check_hclt_shape(nvars, H, C, 1)) != PC_OK) return st;
+  *bytes = pc::hclt_prep_bytes(prec, nvars, H, C);
+  return PC_OK;
+}
+
+pc_status_t pc_hclt_prepare(int nvars, int H, int C, const int32_t* parent, const float* W, const float* E,
+                            pc_precision_t prec, void* prep, size_t prep_bytes, pc_stream_t stream) {
+  pc::clear_error();
+  pc_status_t st;
+  if ((st = pc::check_precision(prec)) != PC_OK) return st;
+  if ((st = pc::check_hclt_shape(nvars, H, C, 1)) != PC_OK) return st;
+  PC_CHECK(parent && W && E, PC_ERR_NULL, "parent, W and E must not be NULL");
+  PC_CHECK(prep, PC_ERR_WORKSPACE, "prepared buffer is NULL");
+  const size_t need = pc::hclt_prep_bytes(prec, nvars, H, C);
+  PC_CHECK(prep_bytes >= need, PC_ERR_WORKSPACE, "prepared buffer of %zu bytes < %zu required", prep_bytes, need);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (prec) {
+    case PC_PREC_AUTO: return pc::hclt_prepare<pc::kBF16>(nvars, H, C, parent, W, E, prec, prep, s);
+    case PC_PREC_TF32: return pc::hclt_prepare<pc::kTF32>(nvars, H, C, parent, W, E, prec, prep, s);
+    default: return pc::hclt_prepare<pc::kTF32x3>(nvars, H, C, parent, W, E, prec, prep, s);
+  }
+}
+
+pc_status_t pc_hclt_prepared_workspace(int nvars, int H, int C, int B, pc_precision_t prec, size_t* bytes) {
+  pc::clear_error();
+  PC_CHECK(bytes != nullptr, PC_ERR_NULL, "bytes is NULL");
+  pc_status_t st;
+  if ((st = pc::check_precision(prec)) != PC_OK) return st;
+  if ((st = pc::check_hclt_shape(nvars, H, C, B)) != PC_OK) return st;
+  *bytes = pc::hclt_ws_bytes(prec, nvars, H, C, B, true);
+  return PC_OK;
+}
+
+pc_status_t pc_hclt_fwd_bwd_prepared(int nvars, int H, int C, int B, const int32_t* parent, const int32_t* data,
+                                     const float* pi, const float* W, const void* prep, size_t prep_bytes, double* ll,
+                                     float* dpi, float* dW, float* dE, int accumulate, pc_precision_t prec, void* ws,
+                                     size_t ws_bytes, pc_stream_t stream) {
+  pc::clear_error();
+  pc_status_t st;
+  if ((st = pc::check_precision(prec)) != PC_OK) return st;
+  if ((st = pc::check_hclt_shape(nvars, H, C, B)) != PC_OK) return st;
+  PC_CHECK(parent && data && pi && W && ll, PC_ERR_NULL, "parent, data, pi, W and ll must not be NULL");
+  PC_CHECK(prep, PC_ERR_WORKSPACE, "prepared buffer is NULL");
+  PC_CHECK(prep_bytes >= pc::hclt_prep_bytes(prec, nvars, H, C), PC_ERR_WORKSPACE,
+           "prepared buffer of %zu bytes is smaller than pc_hclt_prepare_bytes reports", prep_bytes);
+  PC_CHECK(ws, PC_ERR_WORKSPACE, "workspace is NULL");
+  const size_t need = pc::hclt_ws_bytes(prec, nvars, H, C, B, true);
+  PC_CHECK(ws_bytes >= need, PC_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, need);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (prec) {
+    case PC_PREC_AUTO:
+      return pc::hclt_run<pc::kBF16>(nvars, H, C, B, parent, data, pi, W, nullptr, ll, dpi, dW, dE, accumulate, prec,
+                                     ws, s, prep);
+    case PC_PREC_TF32:
+      return pc::hclt_run<pc::kTF32>(nvars, H, C, B, parent, data, pi, W, nullptr, ll, dpi, dW, dE, accumulate, prec,
+                                     ws, s, prep);
+    default:
+      return pc::hclt_run<pc::kTF32x3>(nvars, H, C, B, parent, data, pi, W, nullptr, ll, dpi, dW, dE, accumulate,
+                                       prec, ws, s, prep);
   }
 }
 

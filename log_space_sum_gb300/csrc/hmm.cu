@@ -62,35 +62,96 @@ __global__ void k_rowsum(const float* __restrict__ A, int H, float* __restrict__
   if (lane == 0) rs[row] = s;
 }
 
-// emax[v] = max_k E[k,v];  emax_rs[v] = max_k E[k,v] * rs[k]   (Et = E transposed)
-__global__ void k_emission_bounds(const float* __restrict__ Et, const float* __restrict__ rs, int H,
-                                  float* __restrict__ emax, float* __restrict__ emax_rs) {
-  __shared__ float r0[32], r1[32];
-  const int v = blockIdx.x;
-  const float* e = Et + static_cast<long long>(v) * H;
-  float m0 = 0.f, m1 = 0.f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    const float ev = e[k];
-    m0 = fmaxf(m0, ev);
-    m1 = fmaxf(m1, ev * rs[k]);
+// The transition operand and the row sums in one pass over A: one block per row, the
+// row read once with 16-byte loads (H % 4 == 0, A 16-byte aligned), its operand copy
+// written and its sum reduced in a fixed order (float: it only feeds an upper bound).
+template <int P>
+__global__ void __launch_bounds__(256) k_transition_operand(const float* __restrict__ A, int H, void* op,
+                                                            long long op_ld, size_t op_lo, float* __restrict__ rs) {
+  __shared__ float red[8];
+  const int row = blockIdx.x;
+  const float4* a4 = reinterpret_cast<const float4*>(A + static_cast<long long>(row) * H);
+  float sum = 0.f;
+  for (int q = threadIdx.x; q < H / 4; q += blockDim.x) {
+    const float4 v = a4[q];
+    sum += (v.x + v.y) + (v.z + v.w);
+    const size_t idx = static_cast<size_t>(row * op_ld + 4 * q);
+    if constexpr (P == kBF16) {
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(op) + idx) =
+          make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    } else {
+      const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+      *reinterpret_cast<float4*>(static_cast<float*>(op) + idx) = h;
+      if constexpr (P == kTF32x3)
+        *reinterpret_cast<float4*>(static_cast<float*>(op) + idx + op_lo) =
+            make_float4(tf32_rna(v.x - h.x), tf32_rna(v.y - h.y), tf32_rna(v.z - h.z), tf32_rna(v.w - h.w));
+    }
   }
-  for (int o = 16; o; o >>= 1) {
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-  }
-  if ((threadIdx.x & 31) == 0) {
-    r0[threadIdx.x / 32] = m0;
-    r1[threadIdx.x / 32] = m1;
-  }
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) {
-      m0 = fmaxf(m0, r0[w]);
-      m1 = fmaxf(m1, r1[w]);
-    }
-    emax[v] = m0;
-    emax_rs[v] = m1;
+    float t = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+    rs[row] = t;
   }
+}
+
+// Et[v][k] = E[k][v] over 64 x 64 tiles, and the emission bounds of every token from the
+// same tile: emax[v] = max_k E[k,v], emax_rs[v] = max_k E[k,v] * rs[k], reduced over the
+// tiles with atomic maxima on the bit patterns (non-negative values; zeroed beforehand;
+// the result does not depend on the order).
+__global__ void __launch_bounds__(256) k_emission_transpose(const float* __restrict__ E, int H, int V,
+                                                            const float* __restrict__ rs, float* __restrict__ Et,
+                                                            float* __restrict__ emax, float* __restrict__ emax_rs) {
+  __shared__ float tile[64][65];
+  __shared__ float rsk[64];
+  const int v0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
+  const int t = threadIdx.x;
+  if (t < 64) rsk[t] = k0 + t < H ? rs[k0 + t] : 0.f;
+  for (int i = t; i < 64 * 64; i += 256) {
+    const int kk = i >> 6, vv = i & 63;
+    const int k = k0 + kk, v = v0 + vv;
+    tile[kk][vv] = (k < H && v < V) ? E[static_cast<long long>(k) * V + v] : 0.f;
+  }
+  __syncthreads();
+  for (int i = t; i < 64 * 64; i += 256) {
+    const int vv = i >> 6, kk = i & 63;
+    const int k = k0 + kk, v = v0 + vv;
+    if (k < H && v < V) Et[static_cast<long long>(v) * H + k] = tile[kk][vv];
+  }
+  // bounds: four threads per token, 16 of the tile's states each
+  const int vv = t >> 2, part = t & 3;
+  float m0 = 0.f, m1 = 0.f;
+  for (int kk = part * 16; kk < part * 16 + 16; ++kk) {
+    const float e = tile[kk][vv];
+    m0 = fmaxf(m0, e);
+    m1 = fmaxf(m1, e * rsk[kk]);
+  }
+  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+  if (part == 0 && v0 + vv < V) {
+    atomic_max_nonneg(&emax[v0 + vv], m0);
+    atomic_max_nonneg(&emax_rs[v0 + vv], m1);
+  }
+}
+
+
+// The per-sample scale of a layer, 1 / (the bound of its values): clamped at 2^100, where
+// it is still exact as a power-of-two shift of the column, so that the products below
+// never overflow and a denormal emission is scaled into the normal range before it is
+// multiplied. A column whose largest value then falls below kRangeFloor (the bound was
+// looser than e^-55 at some position; values that matter would lose precision in the
+// operand formats) is reported by the root instead of giving a silently wrong LL.
+constexpr float kScaleMax = 0x1p100f;
+constexpr float kRangeFloor = 0x1p-80f;
+constexpr float kUnderflowMark = 0x1p-149f;  // column max of a column whose nonzero products underflowed
+// (The bound is formed in double: the product of a small previous maximum and a denormal
+// emission bound underflows float32.)
+__device__ __forceinline__ float layer_scale(double bound) {
+  return bound > 0.0 ? static_cast<float>(fmin(1.0 / bound, static_cast<double>(kScaleMax))) : 0.f;
 }
 
 __device__ __forceinline__ void write_scale(float c, float* cf, double* logc, long long idx) {
@@ -118,16 +179,17 @@ __global__ void k_hmm_leaf(int H, int B, int T, const int* __restrict__ tokens,
     if (b < B) {
       const int tok = tokens[static_cast<long long>(b) * T + t];
       const float em = emax[tok];
-      const float c = em > 0.f ? 1.f / em : 0.f;
+      const float c = layer_scale(em);
       if (k < H) {
         u = Et[static_cast<long long>(tok) * H + k] * c;
         if (ubm) store_operand<P>(ubm, static_cast<size_t>(b * ubm_ld + k), ubm_lo, u);
         if (U0) U0[static_cast<long long>(b) * H + k] = u;
       }
-      if (blockIdx.x == 0 && threadIdx.x == 0) write_scale(c, cf, logc, static_cast<long long>(t) * B + b);
-      float m = u;
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (threadIdx.x == 0) atomic_max_nonneg(&umax[static_cast<long long>(t) * B + b], m);
+      // the column maximum is em * c exactly (rounding is monotone): no reduction needed
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        write_scale(c, cf, logc, static_cast<long long>(t) * B + b);
+        umax[static_cast<long long>(t) * B + b] = em * c;
+      }
     }
     tile[i][threadIdx.x] = u;
   }
@@ -248,6 +310,28 @@ __device__ __forceinline__ float warp_column_max(const float (&v)[32]) {
   return __uint_as_float(mx);
 }
 
+// Columns whose product u = e (D c) is 0 although e, D and the column's scale c are
+// positive (the product underflowed).
+__device__ __forceinline__ uint32_t underflow_mask(const float (&u)[32], const float (&e)[32], const float (&d)[32],
+                                                   const float* c_s, int col0, int nvalid) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    if (c < nvalid && u[c] == 0.f && e[c] > 0.f && d[c] > 0.f && c_s[col0 + c] > 0.f) m |= 1u << c;
+  return m;
+}
+
+// After the values are stored: a column whose nonzero product underflowed to 0 takes the
+// smallest positive float into its maximum, so that the root can tell it from a column of
+// exact zeros (a sequence of probability 0).
+__device__ __forceinline__ void mark_underflow(float (&v)[32], uint32_t under) {
+  if (under) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      if ((under >> c) & 1u) v[c] = kUnderflowMark;
+  }
+}
+
 // Split-K chain epilogues (bf16) stage their node-major tile [k][b] (row pitch 272
 // bytes: the 16-byte runs of 32 consecutive rows spread over all banks) and their
 // batch-major tile [b][k] in the idle ring; store_staged then writes both out with
@@ -296,10 +380,17 @@ template <int P, int W = kChainBN>
 struct EpiHmmFwd {
   using Params = HmmFwdParams;
   static constexpr bool kTranspose = false;
+  // sliced 3xTF32 tiles: 16 epilogue warps (prepare strides by 256 threads and needs no
+  // more; apply takes one chunk per warp)
+  static constexpr int kEpiWarps = P == kTF32x3 ? 16 : 8;
   static constexpr int kSliceBF16 = 0;
+  static constexpr int kSliceTF32 = 0;  // the TF32 chain runs as split-K pairs: one accumulation
   // the 3xTF32 ring needs the room: it gathers emissions directly instead
   static constexpr bool kStageE = P != kTF32x3;
-  static constexpr bool kEsSplit = P == kBF16 && W == kChainBN;  // see kEsLoCols
+  static constexpr bool kEsSplit = P != kTF32x3 && W == kChainBN;  // see kEsLoCols
+  // split-K pairs stage their bf16 output tiles in the idle ring; TF32 values (4 bytes)
+  // would not fit beside the exchange buffer and go to global memory from registers
+  static constexpr bool kStageOut = P == kBF16;
   static constexpr int kEsLo = kEsSplit ? kEsLoCols : W;         // columns staged before the K loop
   static constexpr int kEsPitch = kEsSplit ? kEsLoCols : kChainBN;
   static constexpr int kSmemBytes = kChainBN * 4 * 2 + (kStageE ? kEsPitch * kBM * 4 : 0);
@@ -313,8 +404,7 @@ struct EpiHmmFwd {
       float cv = 0.f;
       if (b < p.B) {
         tok = p.tokens[static_cast<long long>(b) * p.T + p.t];
-        const float d = p.umax_prev[b] * p.emax_rs[tok];
-        cv = d > 0.f ? 1.f / d : 0.f;
+        cv = layer_scale(static_cast<double>(p.umax_prev[b]) * p.emax_rs[tok]);
         if (m0 == 0) write_scale(cv, p.cf, p.logc, static_cast<long long>(p.t) * p.B + b);
       }
       tok_s[c] = tok;
@@ -345,36 +435,49 @@ struct EpiHmmFwd {
       for (int c = 0; c < 32; ++c) e[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + k] : 0.f;
     }
     cs_run(c_s, col0, cv);
+    // u = e (D c) into e; v keeps D for the rare check below
 #pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * v[c] * cv[c] : 0.f;
+    for (int c = 0; c < 32; ++c) e[c] = c < nvalid ? e[c] * (v[c] * cv[c]) : 0.f;
     if (p.ubm) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
         if (c < nvalid)
-          store_operand<P>(p.ubm, static_cast<size_t>((n0 + col0 + c) * p.ubm_ld + k), p.ubm_lo, v[c]);
+          store_operand<P>(p.ubm, static_cast<size_t>((n0 + col0 + c) * p.ubm_ld + k), p.ubm_lo, e[c]);
     }
     if (p.U0) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
-        if (c < nvalid) p.U0[static_cast<long long>(n0 + col0 + c) * p.H + k] = v[c];
+        if (c < nvalid) p.U0[static_cast<long long>(n0 + col0 + c) * p.H + k] = e[c];
     }
     if (p.un && nvalid > 0)
       store_operand_run<P>(p.un, static_cast<size_t>(k * p.un_ld + static_cast<long long>(p.t - 1) * p.B + n0 + col0),
-                           p.un_lo, v, nvalid);
+                           p.un_lo, e, nvalid);
     const int b = n0 + col0 + (threadIdx.x & 31);
-    const float mx = warp_column_max(v);
+    float mx = warp_column_max(e);
+    if (__any_sync(0xffffffffu, mx == 0.f && b < p.B)) {
+      // a column of this warp's 32 states is all zero: tell an exact zero from products
+      // that underflowed (the emissions are gathered again into cv)
+      if constexpr (kStageE) {
+        es_run(Es, row, col0, cv);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          cv[c] = c < nvalid ? p.Et[static_cast<long long>(tok_s[col0 + c]) * p.H + k] : 0.f;
+      }
+      mark_underflow(e, underflow_mask(e, cv, v, c_s, col0, nvalid));
+      mx = warp_column_max(e);
+    }
     if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
   }
 
-  // Split-K form of apply: u_t goes to the staged tiles instead of global memory.
-  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes + (kEsSplit ? kEsHiBytes : 0);
+  // Split-K form of apply: u_t goes to the staged tiles (bf16) or straight to global memory.
+  static constexpr int kOutBytes = kStageOut ? kNodeTileBytes + kBatchTileBytes : kEpiWarps * 4096;
+  static constexpr int kSplitStageBytes = kOutBytes + (kEsSplit ? kEsHiBytes : 0);
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
   // the batch-major tile is written only in apply_staged: the exchange's scratch until then
-  static constexpr int kSplitScratchOffset = kNodeTileBytes;
+  static constexpr int kSplitScratchOffset = kStageOut ? kNodeTileBytes : 0;
   static_assert(kSplitScratchOffset % 16 == 0, "16-byte scratch rows");
-  __device__ static float* es_hi(uint8_t* stage) {
-    return reinterpret_cast<float*>(stage + kNodeTileBytes + kBatchTileBytes);
-  }
+  __device__ static float* es_hi(uint8_t* stage) { return reinterpret_cast<float*>(stage + kOutBytes); }
   __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* smem, uint8_t* stage) {
     if constexpr (kEsSplit)
       stage_emissions_async<kChainBN - kEsLoCols, kEsLoCols>(p.Et, p.H, p.B, m0, n0 + kEsLoCols,
@@ -383,7 +486,7 @@ struct EpiHmmFwd {
   }
   __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
                                       float (&v)[32], uint8_t* smem, uint8_t* stage) {
-    static_assert(P == kBF16 && kStageE, "staged chain tiles hold bf16 operands");
+    static_assert(P != kTF32x3 && kStageE, "split-K chain tiles in bf16 or TF32");
     const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
     const float* Es = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
     const int k = m0 + row;
@@ -394,20 +497,42 @@ struct EpiHmmFwd {
     else
       es_run<kEsLoCols>(es_hi(stage), row, col0 - kEsLoCols, e);
     cs_run(c_s, col0, cv);
+    // u = e (D c) into e; v keeps D for the rare check below
 #pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * v[c] * cv[c] : 0.f;
-    if (p.ubm) stage_batch_col(stage, row, col0, v);
+    for (int c = 0; c < 32; ++c) e[c] = c < nvalid ? e[c] * (v[c] * cv[c]) : 0.f;
+    if constexpr (kStageOut) {
+      if (p.ubm) stage_batch_col(stage, row, col0, e);
+    } else if (p.ubm) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid)
+          store_operand<P>(p.ubm, static_cast<size_t>((n0 + col0 + c) * p.ubm_ld + k), p.ubm_lo, e[c]);
+    }
     if (p.U0) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
-        if (c < nvalid) p.U0[static_cast<long long>(n0 + col0 + c) * p.H + k] = v[c];
+        if (c < nvalid) p.U0[static_cast<long long>(n0 + col0 + c) * p.H + k] = e[c];
     }
-    if (p.un) stage_node_run(stage, row, col0, v);
+    if constexpr (kStageOut) {
+      if (p.un) stage_node_run(stage, row, col0, e);
+    } else if (p.un && nvalid > 0) {
+      store_operand_run<P>(p.un, static_cast<size_t>(k * p.un_ld + static_cast<long long>(p.t - 1) * p.B + n0 + col0),
+                           p.un_lo, e, nvalid);
+    }
     const int b = n0 + col0 + (threadIdx.x & 31);
-    const float mx = warp_column_max(v);
+    float mx = warp_column_max(e);
+    if (__any_sync(0xffffffffu, mx == 0.f && b < p.B)) {  // as in apply
+      if (col0 < kEsLo)
+        es_run<kEsPitch>(Es, row, col0, cv);
+      else
+        es_run<kEsLoCols>(es_hi(stage), row, col0 - kEsLoCols, cv);
+      mark_underflow(e, underflow_mask(e, cv, v, c_s, col0, nvalid));
+      mx = warp_column_max(e);
+    }
     if (b < p.B) atomic_max_nonneg(&p.umax_cur[b], mx);
   }
   __device__ static void store_staged(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
+    if constexpr (!kStageOut) return;
     const int nr = min(kBM, p.H - m0), nc = min(W, p.B - n0);
     if (p.ubm)
       stage_tile_store_bf16(stage + kNodeTileBytes, kBatchPitch,
@@ -425,21 +550,49 @@ struct EpiHmmFwd {
 
 // ------------------------------------------------------------------- root
 // ll[b] = log sum_k pi[k] u_0[k,b] - sum_t log c_{t,b};  r[b] = 1 / sum_k pi u_0.
-__global__ void k_hmm_root(int H, int B, int T, const float* __restrict__ pi, const float* __restrict__ U0,
-                           const double* __restrict__ logc, double* __restrict__ ll, float* __restrict__ rroot) {
-  __shared__ double red[32];
-  const int b = blockIdx.x;
+// A sample whose column maximum fell into (0, kRangeFloor) at some position left the
+// range the per-layer shift keeps exact: its LL is NaN, it passes no flow (r = 0) and the
+// device status word records kErrRange. One warp per sample (16-byte loads when H % 4 == 0
+// and the rows are aligned), sums in double.
+__global__ void __launch_bounds__(256) k_hmm_root(int H, int B, int T, const float* __restrict__ pi,
+                                                  const float* __restrict__ U0, const double* __restrict__ logc,
+                                                  const float* __restrict__ umax, double* __restrict__ ll,
+                                                  float* __restrict__ rroot, unsigned* status) {
+  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (b >= B) return;
+  const int lane = threadIdx.x & 31;
   const float* u = U0 + static_cast<long long>(b) * H;
   double s = 0.0;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) s += static_cast<double>(pi[k]) * u[k];
-  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) s += red[w];
-    double off = 0.0;
-    for (int t = 0; t < T; ++t) off += logc[static_cast<long long>(t) * B + b];
-    const bool zero = !(s > 0.0) || !(off < INFINITY);
+  if ((H & 3) == 0 && ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(pi)) & 15) == 0) {
+    const float4* u4 = reinterpret_cast<const float4*>(u);
+    const float4* p4 = reinterpret_cast<const float4*>(pi);
+    for (int q = lane; q < H / 4; q += 32) {
+      const float4 x = u4[q], y = p4[q];
+      s += static_cast<double>(x.x) * y.x + static_cast<double>(x.y) * y.y + static_cast<double>(x.z) * y.z +
+           static_cast<double>(x.w) * y.w;
+    }
+  } else {
+    for (int k = lane; k < H; k += 32) s += static_cast<double>(pi[k]) * u[k];
+  }
+  double off = 0.0;
+  bool out_of_range = false;
+  for (int t = lane; t < T; t += 32) {
+    off += logc[static_cast<long long>(t) * B + b];
+    const float m = umax[static_cast<long long>(t) * B + b];
+    out_of_range |= m > 0.f && m < kRangeFloor;
+  }
+  for (int o = 16; o; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    off += __shfl_xor_sync(0xffffffffu, off, o);
+  }
+  out_of_range = __any_sync(0xffffffffu, out_of_range);
+  if (lane != 0) return;
+  const bool zero = !(s > 0.0) || !(off < INFINITY);
+  if (out_of_range) {
+    ll[b] = NAN;
+    rroot[b] = 0.f;
+    if (status) atomicOr(status, kErrRange);
+  } else {
     ll[b] = zero ? -INFINITY : log(s) - off;
     rroot[b] = zero ? 0.f : static_cast<float>(1.0 / s);
   }
@@ -509,8 +662,11 @@ struct HmmBwdParams {
 template <int P, int W = kChainBN>
 struct EpiHmmBwd : EpiNoHooks {
   using Params = HmmBwdParams;
+  static constexpr int kEpiWarps = P == kTF32x3 ? 16 : 8;  // as EpiHmmFwd
+  static constexpr int kSliceTF32 = 0;  // as EpiHmmFwd
   static constexpr bool kStageE = P != kTF32x3;
-  static constexpr bool kEsSplit = P == kBF16 && W == kChainBN;  // see kEsLoCols
+  static constexpr bool kEsSplit = P != kTF32x3 && W == kChainBN;  // see kEsLoCols
+  static constexpr bool kStageOut = P == kBF16;                    // as EpiHmmFwd
   static constexpr int kEsLo = kEsSplit ? kEsLoCols : W;
   static constexpr int kEsPitch = kEsSplit ? kEsLoCols : kChainBN;
   static constexpr int kSmemBytes = kChainBN * 8 + (kStageE ? kEsPitch * kBM * 4 : 0);
@@ -573,24 +729,23 @@ struct EpiHmmBwd : EpiNoHooks {
                            p.wn_lo, v, nvalid);
   }
 
-  // Split-K form of apply: u_{t+1} is staged (coalesced, asynchronous: the copies complete
-  // while the partial sums are exchanged);
-  // w_{t+1} goes to the staged tiles, the node-major one in place of u.
-  static constexpr int kSplitStageBytes = kNodeTileBytes + kBatchTileBytes + (kEsSplit ? kEsHiBytes : 0);
+  // Split-K form of apply: in bf16, u_{t+1} is staged (coalesced, asynchronous: the copies
+  // complete while the partial sums are exchanged) and w_{t+1} goes to the staged tiles, the
+  // node-major one in place of u; TF32 reads and writes global memory from registers.
+  static constexpr int kOutBytes = kStageOut ? kNodeTileBytes + kBatchTileBytes : kEpiWarps * 4096;
+  static constexpr int kSplitStageBytes = kOutBytes + (kEsSplit ? kEsHiBytes : 0);
   static_assert(kSplitStageBytes % 16 == 0, "16-byte staged rows");
   // the batch-major tile is written only in apply_staged: the exchange's scratch until then
-  static constexpr int kSplitScratchOffset = kNodeTileBytes;
+  static constexpr int kSplitScratchOffset = kStageOut ? kNodeTileBytes : 0;
   static_assert(kSplitScratchOffset % 16 == 0, "16-byte scratch rows");
-  __device__ static float* es_hi(uint8_t* stage) {
-    return reinterpret_cast<float*>(stage + kNodeTileBytes + kBatchTileBytes);
-  }
+  __device__ static float* es_hi(uint8_t* stage) { return reinterpret_cast<float*>(stage + kOutBytes); }
   __device__ static void after_mma(const Params& p, int, int m0, int n0, int et, uint8_t* smem, uint8_t* stage) {
     if constexpr (kEsSplit)
       if (p.wbm)
         stage_emissions_async<kChainBN - kEsLoCols, kEsLoCols>(p.Et, p.H, p.B, m0, n0 + kEsLoCols,
                                                                reinterpret_cast<const int*>(smem) + kEsLoCols,
                                                                es_hi(stage), et);
-    if (p.fbm)
+    if (kStageOut && p.fbm)
       stage_tile_load_bf16_async(stage, kNodePitch,
                            static_cast<const __nv_bfloat16*>(p.un) + static_cast<long long>(m0) * p.un_ld +
                                static_cast<long long>(p.t) * p.B + n0,
@@ -598,23 +753,28 @@ struct EpiHmmBwd : EpiNoHooks {
   }
   __device__ static void apply_staged(const Params& p, int, int m0, int n0, int row, int col0,
                                       float (&v)[32], uint8_t* smem, uint8_t* stage) {
-    static_assert(P == kBF16 && kStageE, "staged chain tiles hold bf16 operands");
+    static_assert(P != kTF32x3 && kStageE, "split-K chain tiles in bf16 or TF32");
     const float* c_s = reinterpret_cast<const float*>(smem) + kChainBN;
     const float* Es = reinterpret_cast<const float*>(smem) + 2 * kChainBN;
     const int j = m0 + row;
     const int nvalid = j < p.H ? min(32, p.B - (n0 + col0)) : 0;
     if (p.fbm) {
-      const uint4* nt = reinterpret_cast<const uint4*>(stage + row * kNodePitch + col0 * 2);
       float u[32];
+      if constexpr (kStageOut) {
+        const uint4* nt = reinterpret_cast<const uint4*>(stage + row * kNodePitch + col0 * 2);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = nt[q];
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = nt[q];
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          u[8 * q + 2 * r] = __uint_as_float(ww[r] << 16);
-          u[8 * q + 2 * r + 1] = __uint_as_float(ww[r] & 0xFFFF0000u);
+          for (int r = 0; r < 4; ++r) {
+            u[8 * q + 2 * r] = __uint_as_float(ww[r] << 16);
+            u[8 * q + 2 * r + 1] = __uint_as_float(ww[r] & 0xFFFF0000u);
+          }
         }
+      } else if (nvalid > 0) {
+        load_operand_run<P>(p.un, static_cast<size_t>(j * p.un_ld + static_cast<long long>(p.t) * p.B + n0 + col0),
+                            p.un_lo, u, nvalid);
       }
 #pragma unroll
       for (int c = 0; c < 32; ++c)
@@ -629,10 +789,21 @@ struct EpiHmmBwd : EpiNoHooks {
     cs_run(c_s, col0, cv);
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] = c < nvalid ? e[c] * cv[c] * v[c] : 0.f;
-    stage_batch_col(stage, row, col0, v);
-    if (p.wn) stage_node_run(stage, row, col0, v);
+    if constexpr (kStageOut) {
+      stage_batch_col(stage, row, col0, v);
+      if (p.wn) stage_node_run(stage, row, col0, v);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) store_operand<P>(p.wbm, static_cast<size_t>((n0 + col0 + c) * p.wbm_ld + j), p.wbm_lo, v[c]);
+      if (p.wn && nvalid > 0)
+        store_operand_run<P>(p.wn,
+                             static_cast<size_t>(j * p.wn_ld + static_cast<long long>(p.t + 1) * p.B + n0 + col0),
+                             p.wn_lo, v, nvalid);
+    }
   }
   __device__ static void store_staged(const Params& p, int, int m0, int n0, int et, uint8_t* stage) {
+    if constexpr (!kStageOut) return;
     if (!p.wbm) return;
     const int nr = min(kBM, p.H - m0), nc = min(W, p.B - n0);
     stage_tile_store_bf16(stage + kNodeTileBytes, kBatchPitch,
@@ -657,7 +828,7 @@ int param_split(int H, int T, int B, pc_precision_t prec) {
   if (T < 2) return 1;
   const long long K = static_cast<long long>(T - 1) * B;
   const int kb = 128 / operand_elem_bytes(prec);  // K elements per ring block
-  const long long tiles = static_cast<long long>(cdiv(H, kBM)) * cdiv(H, prec == PC_PREC_AUTO ? 256 : 128);
+  const long long tiles = static_cast<long long>(cdiv(H, kBM)) * cdiv(H, prec == PC_PREC_FP32 ? 128 : 256);
   for (int S = kParamSplitMax; S >= 2; S /= 2)
     if (tiles * S <= num_sms() && K % (static_cast<long long>(S) * kb) == 0 && K / S >= 8ll * kb) return S;
   return 1;
@@ -715,8 +886,8 @@ size_t carve_hmm(void* base, pc_precision_t p, int H, int T, int V, int B, bool 
   w->ubm[1] = c.operand(p, 1, B, H);
   w->Et = static_cast<float*>(c.take(size_t(V) * H * 4));
   w->rs = static_cast<float*>(c.take(size_t(H) * 4));
-  w->emax = static_cast<float*>(c.take(size_t(V) * 4));
-  w->emax_rs = static_cast<float*>(c.take(size_t(V) * 4));
+  w->emax = static_cast<float*>(c.take(size_t(V) * 8));  // emax, then emax_rs (cleared together)
+  w->emax_rs = w->emax + V;
   w->U0 = static_cast<float*>(c.take(size_t(B) * H * 4));
   w->umax = static_cast<float*>(c.take(size_t(T) * B * 4));
   w->cf = static_cast<float*>(c.take(size_t(T) * B * 4));
@@ -759,7 +930,7 @@ template <int P>
 pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const float* pi, const float* A,
                     const float* E, double* ll, float* dpi, float* dA, float* dE, int accumulate,
                     pc_precision_t prec, void* ws, cudaStream_t s) {
-  constexpr int kParamBN = (P == kBF16) ? 256 : 128;  // sliced modes hold BN sums per thread
+  constexpr int kParamBN = (P == kTF32x3) ? 128 : 256;  // 3xTF32 (sliced) holds BN sums per thread
   const bool flows = dpi || dA || dE;
   const bool chain = flows && (dA || dE) && T >= 2;
   HmmWs w;
@@ -805,24 +976,28 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   if (dpi && !accumulate) PC_CUDA(cudaMemsetAsync(dpi, 0, size_t(H) * 4, s));
   if (dA && !accumulate && T < 2) PC_CUDA(cudaMemsetAsync(dA, 0, size_t(H) * H * 4, s));
 
-  // set-up: E transposed, row sums of A, emission bounds, operand copies of A
-  {
-    ProfileScope ps(s, PC_KIND_HMM_MEM, 2 * VH * 4);
-    if ((st = transpose_f32(E, V, 0, 1, H, V, w.Et, H, 0, s)) != PC_OK) return st;  // Et[v][k] = E[k][v]
-  }
-  {
-    ProfileScope ps(s, PC_KIND_HMM_MEM, HH * 4 + H * 4ll);
-    k_rowsum<<<cdiv(H, 8), 256, 0, s>>>(A, H, w.rs);
+  // set-up: row sums of A with its operand copy, E transposed with the emission bounds
+  const bool fused_a = T >= 2 && (H & 3) == 0 && aligned16(A);
+  if (fused_a) {
+    ProfileScope ps(s, PC_KIND_HMM_MEM, HH * (4 + eb) + H * 4ll);
+    k_transition_operand<P><<<H, 256, 0, s>>>(A, H, w.Aop.ptr, w.Aop.ld, w.Aop.lo_elems, w.rs);
     PC_LAUNCH_CHECK();
+  } else {
+    {
+      ProfileScope ps(s, PC_KIND_HMM_MEM, HH * 4 + H * 4ll);
+      k_rowsum<<<cdiv(H, 8), 256, 0, s>>>(A, H, w.rs);
+      PC_LAUNCH_CHECK();
+    }
+    if (T >= 2) {
+      ProfileScope ps(s, PC_KIND_HMM_MEM, HH * (4 + eb));
+      if ((st = rows_to_operand<P>(A, H, 0, 1, H, H, w.Aop, s)) != PC_OK) return st;
+    }
   }
+  PC_CUDA(cudaMemsetAsync(w.emax, 0, size_t(V) * 8, s));  // emax and emax_rs are adjacent
   {
-    ProfileScope ps(s, PC_KIND_HMM_MEM, VH * 4 + H * 4ll + V * 8ll);
-    k_emission_bounds<<<V, 256, 0, s>>>(w.Et, w.rs, H, w.emax, w.emax_rs);
+    ProfileScope ps(s, PC_KIND_HMM_MEM, 2 * VH * 4 + H * 4ll + V * 8ll);
+    k_emission_transpose<<<dim3(cdiv(V, 64), cdiv(H, 64)), 256, 0, s>>>(E, H, V, w.rs, w.Et, w.emax, w.emax_rs);
     PC_LAUNCH_CHECK();
-  }
-  if (T >= 2) {
-    ProfileScope ps(s, PC_KIND_HMM_MEM, HH * (4 + eb));
-    if ((st = rows_to_operand<P>(A, H, 0, 1, H, H, w.Aop, s)) != PC_OK) return st;
   }
 
   // leaf (position T-1)
@@ -844,7 +1019,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
   // than kNarrowBelow CTAs (a small H: short K loops, the fixed costs dominate), the
   // pairs take 128 x 128 (or 128 x 64) tiles instead: twice (four times) the CTAs, a half
   // (a quarter) of the exchange and epilogue per CTA.
-  constexpr bool kSplitChain = P == kBF16;
+  constexpr bool kSplitChain = P != kTF32x3;
   constexpr int kTileBN = kSplitChain ? 2 * kChainBN : kChainBN;
   constexpr long long kNarrowBelow = 96;
   // split-K tiles 128 x 256, else 128 x 128, else 128 x 64: the widest with enough CTAs
@@ -901,7 +1076,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
 
   {
     ProfileScope ps(s, PC_KIND_HMM_MEM, BH * 4 + H * 4ll + TB * 8 + B * 12ll);
-    k_hmm_root<<<B, 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, ll, w.rroot);
+    k_hmm_root<<<cdiv(B, 8), 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, w.umax, ll, w.rroot, device_status_word());
     PC_LAUNCH_CHECK();
   }
   if (use_side && (st = side.join(s)) != PC_OK) return st;

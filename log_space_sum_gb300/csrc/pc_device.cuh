@@ -14,7 +14,8 @@ namespace pc {
 // ----------------------------------------------------------------- device status
 // Bits of the device status word a kernel sets when it gives up a bounded wait.
 enum : unsigned { kErrTimeoutProducer = 1u, kErrTimeoutMma = 2u, kErrTimeoutEpilogue = 4u,
-                  kErrTimeoutDrain = 8u };
+                  kErrTimeoutDrain = 8u, kErrRange = 16u };
+constexpr unsigned kErrTimeoutBits = 15u;
 
 // 2 s of wall time: three orders of magnitude above the longest legitimate wait here
 // (an epilogue waiting for the full K loop of its tile).
@@ -246,8 +247,64 @@ __device__ __forceinline__ void tmem_ld_32x32(uint32_t taddr, float (&v)[32]) {
       : "r"(taddr)
       : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  // the registers are read only after the wait (see tmem_wait_ld)
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i])::"memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The same load without the wait, so that several loads are in flight; complete them
+// with tmem_wait_ld before the registers are read.
+__device__ __forceinline__ void tmem_ld_32x32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The wait, then an empty volatile statement that rewrites the loaded registers, so that
+// every later use of them depends on a point after the wait (the load's own statement
+// names them as outputs and nothing else would keep their uses behind the wait).
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i])::"memory");
+}
+
+// Packed float32 pairs (sm_100 family): a += b and a += b + h * k, two lanes per instruction.
+__device__ __forceinline__ void add2(float& a0, float& a1, uint32_t b0, uint32_t b1) {
+  asm("{\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(b0), "r"(b1));
+}
+// a += b + (b's exponent and sign bits) * k: b plus half an ulp of b (see half_ulp) for
+// k = 2^-24 (bit pattern 0x33800000), or a multiple of it.
+__device__ __forceinline__ void add2_half_ulp(float& a0, float& a1, uint32_t b0, uint32_t b1,
+                                              uint32_t kbits = 0x33800000u) {
+  asm("{\n\t.reg .b64 a, b, h, k;\n\t.reg .b32 h0, h1;\n\t"
+      "and.b32 h0, %2, 0xFF800000;\n\t"
+      "and.b32 h1, %3, 0xFF800000;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "mov.b64 h, {h0, h1};\n\t"
+      "mov.b64 k, {%4, %4};\n\t"
+      "fma.rn.f32x2 b, h, k, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "add.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(b0), "r"(b1), "r"(kbits));
 }
 
 // --------------------------------------------------------------- operand formats

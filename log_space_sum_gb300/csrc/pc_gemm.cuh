@@ -36,6 +36,13 @@ struct EpiPrefetch : std::false_type {};
 template <class E>
 struct EpiPrefetch<E, std::void_t<decltype(E::kPrefetchTile)>> : std::bool_constant<E::kPrefetchTile> {};
 
+// Epi::kSliceTF32 (optional, default kSliceK1): the TF32 accumulation slice in k-steps
+// (0 = one accumulation over all of K, as the split-K chain tiles need).
+template <class E, class = void>
+struct EpiSliceTF32 : std::integral_constant<int, 8> {};
+template <class E>
+struct EpiSliceTF32<E, std::void_t<decltype(E::kSliceTF32)>> : std::integral_constant<int, E::kSliceTF32> {};
+
 // Epi::kBLo (optional, default false; bf16 and TF32 only): the B operand (the layer's
 // children) is stored as hi + lo, hi = the mode's rounding of the value and lo = that of
 // the remainder, and every k-step adds A * B_lo into a separate TMEM accumulator that
@@ -48,11 +55,19 @@ struct EpiBLo : std::false_type {};
 template <class E>
 struct EpiBLo<E, std::void_t<decltype(E::kBLo)>> : std::bool_constant<E::kBLo> {};
 
-// Warp 0: TMA producer; warp 1: MMA issuer; warps 2 .. 9: epilogue, two warps per TMEM
-// lane quarter, each taking every other 32-column chunk of the tile.
+// Warp 0: TMA producer; warp 1: MMA issuer; then the epilogue warps, kEpiWarps / 4 per
+// TMEM lane quarter, each taking every (kEpiWarps / 4)-th 32-column chunk of the tile.
+// Epi::kEpiWarps (optional) sets the count for one instantiation: 16 for the sliced
+// 3xTF32 tiles, whose accumulator slices arrive every k-step (more warps hide the TMEM
+// load latency, one chunk per warp leaves registers to keep the next slice's load in
+// flight); epilogues that opt in stride their own loops by their count.
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kGemmThreads = 64 + kEpiThreads;
+template <class E, class = void>
+struct EpiWarps : std::integral_constant<int, kEpiWarps> {};
+template <class E>
+struct EpiWarps<E, std::void_t<decltype(E::kEpiWarps)>> : std::integral_constant<int, E::kEpiWarps> {};
 // (Ten warps place three on some SM sub-partitions, whose 16K registers then allow 168
 // per thread; the launch bounds let the compiler plan for that.)
 constexpr int kBM = 128;
@@ -75,7 +90,7 @@ struct GemmShape {
 // slot); see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
 // (Epi::kSliceBF16 k-steps; 0 = one accumulation over all of K).
 constexpr int kSliceK3x = 1;
-constexpr int kSliceK1 = 8;
+constexpr int kSliceK1 = 8;  // the TF32 default (EpiSliceTF32)
 
 // The tensor core's float32 accumulator truncates toward zero. A slice of one 3xTF32
 // k-step ends in one such truncation at the slice's own magnitude, which drops the bits
@@ -95,7 +110,7 @@ constexpr size_t kSmemPerCta = 232448;  // opt-in maximum dynamic shared memory 
 template <int P, int BN, class Epi>
 struct GemmPlan {
   using S = GemmShape<P, BN, EpiBLo<Epi>::value && P != kTF32x3>;
-  static constexpr size_t kTBufBytes = Epi::kTranspose ? kEpiWarps * kTBufFloats * sizeof(float) : 0;
+  static constexpr size_t kTBufBytes = Epi::kTranspose ? EpiWarps<Epi>::value * kTBufFloats * sizeof(float) : 0;
   static constexpr size_t kEpiBytes = ((Epi::kSmemBytes + 15) / 16) * 16;
   static constexpr size_t kFixed = 1024 /* alignment slack */ + 256 /* barriers */ + kTBufBytes + kEpiBytes;
   static constexpr int kFit = static_cast<int>((kSmemPerCta - kFixed) / S::kStageBytes);
@@ -122,11 +137,13 @@ __device__ __forceinline__ void warp_transpose32(const float (&v)[32], float (&w
   __syncwarp();
 }
 
+template <int N = kEpiThreads>
 __device__ __forceinline__ void epilogue_bar_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
 // Named barrier of the epilogue threads that also ANDs a predicate over them.
+template <int N = kEpiThreads>
 __device__ __forceinline__ bool epilogue_bar_and(bool v) {
   uint32_t r;
   asm volatile(
@@ -135,7 +152,7 @@ __device__ __forceinline__ bool epilogue_bar_and(bool v) {
       "bar.red.and.pred po, 1, %2, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "n"(kEpiThreads)
+      : "r"(static_cast<uint32_t>(v)), "n"(N)
       : "memory");
   return r != 0;
 }
@@ -212,7 +229,7 @@ __device__ __forceinline__ void stage_tile_load_bf16_async(uint8_t* tile, int pi
 // without splitting K. Where even those are too few, 128 x 128 or 128 x 64 tiles split the
 // same way trade MMA width for more CTAs and a smaller exchange.)
 template <int P, int BN, class Epi, bool kSplit = false>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
                 int num_kb_total, unsigned* status, const typename Epi::Params ep, int a_early) {
@@ -220,6 +237,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr bool kBLo = EpiBLo<Epi>::value && P != kTF32x3;
   static_assert(!kBLo || P == kBF16 || P == kTF32, "a B lo part in bf16 or TF32");
   using S = GemmShape<P, BN, kBLo>;
+  constexpr int kEW = EpiWarps<Epi>::value;  // epilogue warps
+  constexpr int kET = kEW * 32;
+  constexpr int kWPQ = kEW / 4;              // epilogue warps per TMEM lane quarter
+  static_assert(kEW % 4 == 0 && (kEW == kEpiWarps || P == kTF32x3), "more epilogue warps: sliced 3xTF32 only");
   constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
   // Sliced modes: every K slice (kSliceK k-steps of the MMA) is accumulated from zero in
   // one of kAccBufs TMEM buffers and added into registers by the epilogue with round-to-
@@ -228,7 +249,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // whatever K is. A slice of one k-step (3xTF32: lo*hi, hi*lo, then hi*hi) ends in a
   // single truncation at the slice's own magnitude, whose expected loss (half_ulp of the
   // slice) the epilogue adds back to each slice.
-  constexpr int kSliceK = (P == kTF32x3) ? kSliceK3x : (P == kTF32 ? kSliceK1 : Epi::kSliceBF16);
+  constexpr int kSliceK = (P == kTF32x3) ? kSliceK3x : (P == kTF32 ? EpiSliceTF32<Epi>::value : Epi::kSliceBF16);
   constexpr bool kSliced = kSliceK > 0;
   constexpr bool kStepSliced = kSliced && kSliceK < static_cast<int>(S::kKSteps);
   static_assert(!kSliced || kStepSliced ? kSliceK <= 1 : kSliceK % S::kKSteps == 0,
@@ -248,7 +269,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if constexpr (kSplit)
     static_assert(!kSliced && (BN == 256 || BN == 128 || BN == 64) &&
                       kStages * S::kStageBytes >= kXchgBytes + Epi::kSplitStageBytes &&
-                      Epi::kSplitScratchOffset + kEpiWarps * 4096 <= Epi::kSplitStageBytes,
+                      Epi::kSplitScratchOffset + kEW * 4096 <= Epi::kSplitStageBytes,
                   "split K: unsliced 128 x 256, 128 x 128 or 128 x 64 tiles, the ring holds the exchange buffer "
                   "and the staged tiles");
   constexpr int kEpiBN = kSplit ? BN / 2 : BN;  // columns this CTA's epilogue finishes
@@ -289,7 +310,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       for (int b = 0; b < 4; ++b) {
         mbar_init(&acc_full[b], 1);
-        mbar_init(&acc_empty[b], 1);
+        mbar_init(&acc_empty[b], kSliced ? kEW : 1);  // sliced: every epilogue warp releases
       }
       mbar_init(mma_done, 1);
       fence_barrier_init();
@@ -449,19 +470,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------- epilogue
-    const int et = threadIdx.x - 64;  // 0 .. kEpiThreads-1
-    const int ew = warp - 2;          // epilogue warp 0 .. 7
+    const int et = threadIdx.x - 64;  // 0 .. kET-1
+    const int ew = warp - 2;          // epilogue warp 0 .. kEW-1
     grid_dependency_wait();           // the epilogue reads and writes global memory
     Epi::prepare(ep, g, m0, n0_epi, et, epi_smem);
-    epilogue_bar_sync();
+    epilogue_bar_sync<kET>();
     const int q = warp & 3;       // TMEM lane quarter this warp may access
-    const int half = ew >> 2;     // chunks c with (c & 1) == half
+    const int part = ew >> 2;     // the warp takes the chunks c with c % kWPQ == part
     const int row = q * 32 + lane;
     float* tbuf = Epi::kTranspose ? tbuf_base + ew * kTBufFloats : nullptr;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    constexpr int kChunks = kEpiBN / 64;  // 32-column chunks per epilogue warp
+    constexpr int kChunks = kEpiBN / (32 * kWPQ);  // 32-column chunks per epilogue warp (sliced path)
+    auto chunk_col = [&](int c) { return (kWPQ * c + part) * 32; };
     bool ok = true;
     if constexpr (kSliced) {
+      static_assert(kChunks >= 1 && kEpiBN % (32 * kWPQ) == 0, "whole chunks per epilogue warp");
       float acc[kChunks][32];
 #pragma unroll
       for (int c = 0; c < kChunks; ++c)
@@ -469,24 +492,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int i = 0; i < 32; ++i) acc[c][i] = 0.f;
       const int total_q = num_kb * static_cast<int>(S::kKSteps);
       const int num_slices = (total_q + kSliceK - 1) / kSliceK;
-      for (int sl = 0; sl < num_slices; ++sl) {
-        const int buf = sl % kAccBufs;
-        // all epilogue threads agree on whether the slice arrived
-        ok = epilogue_bar_and(
-            mbar_wait(&acc_full[buf], (sl / kAccBufs) & 1, status, kErrTimeoutEpilogue, wl));
-        if (!ok) break;
-        tc_fence_after();
+      // Each warp takes its slices on its own and releases a slice's buffer to the MMA
+      // issuer as soon as its loads have landed (acc_empty counts the epilogue warps), so
+      // no block-wide barrier sits between a slice's arrival and its release.
+      // The truncation correction (kHalfUlp) is sampled: every fourth slice adds four
+      // times its own half ulp. Its expectation is that of adding each slice's half ulp
+      // (the slices' magnitudes do not depend on their index modulo 4), its extra noise is
+      // of the order of 2^-24 / sqrt(slices) of the sum, and the epilogue's arithmetic per
+      // slice drops to about one packed add per two values.
+      auto add_slice = [&](float (&a)[32], const uint32_t (&v)[32], bool corr) {
+        if (kHalfUlp && corr) {
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-          float v[32];
-          tmem_ld_32x32(lane_base + static_cast<uint32_t>(buf * BN + (2 * c + half) * 32), v);
+          for (int i = 0; i < 32; i += 2) add2_half_ulp(a[i], a[i + 1], v[i], v[i + 1], 0x34800000u);  // 4 x 2^-24
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c][i] += kHalfUlp ? v[i] + half_ulp(v[i]) : v[i];
+          for (int i = 0; i < 32; i += 2) add2(a[i], a[i + 1], v[i], v[i + 1]);
         }
+      };
+      auto wait_slice = [&](int sl) {
+        return __all_sync(0xffffffffu, mbar_wait(&acc_full[sl % kAccBufs], (sl / kAccBufs) & 1, status,
+                                                  kErrTimeoutEpilogue, wl));
+      };
+      auto release = [&](int sl) {
         tc_fence_before();
-        epilogue_bar_sync();
-        if (et == 0) mbar_arrive(&acc_empty[buf]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[sl % kAccBufs]);
+      };
+      {
+        constexpr int kGroup = kChunks < 2 ? kChunks : 2;  // loads in flight at a time
+        // (with kEpiWarps = 16 a warp holds one chunk: four warps per SM sub-partition
+        // overlap one another's TMEM load latency)
+        for (int sl = 0; sl < num_slices; ++sl) {
+          const int buf = sl % kAccBufs;
+          ok = wait_slice(sl);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < kChunks; c0 += kGroup) {
+            uint32_t v[kGroup][32];
+#pragma unroll
+            for (int c = 0; c < kGroup; ++c)
+              tmem_ld_32x32_async(lane_base + static_cast<uint32_t>(buf * BN + chunk_col(c0 + c)), v[c]);
+#pragma unroll
+            for (int c = 0; c < kGroup; ++c) tmem_wait_ld(v[c]);
+            if (c0 + kGroup == kChunks) release(sl);
+#pragma unroll
+            for (int c = 0; c < kGroup; ++c) add_slice(acc[c0 + c], v[c], (sl & 3) == 0);
+          }
+        }
       }
+      ok = epilogue_bar_and<kET>(ok);  // every epilogue thread takes the same branch below
       if constexpr (kBLo) {
         // the last slice's commit covered every MMA, the B_lo ones included
         if (ok) {
@@ -494,7 +549,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) {
             float v[32];
-            tmem_ld_32x32(lane_base + static_cast<uint32_t>(kLoCol + (2 * c + half) * 32), v);
+            tmem_ld_32x32(lane_base + static_cast<uint32_t>(kLoCol + chunk_col(c)), v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[c][i] += v[i];
           }
@@ -503,11 +558,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (ok) {
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
-          Epi::apply(ep, g, m0, n0_epi, row, (2 * c + half) * 32, acc[c], epi_smem, tbuf);
+          Epi::apply(ep, g, m0, n0_epi, row, chunk_col(c), acc[c], epi_smem, tbuf);
         }
       }
     } else {
-      ok = epilogue_bar_and(mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue, wl));
+      ok = epilogue_bar_and<kET>(mbar_wait(&acc_full[0], 0, status, kErrTimeoutEpilogue, wl));
       tc_fence_after();
       if constexpr (kSplit) {
         // the MMAs are complete: this CTA's ring is idle; inputs of the epilogue are
@@ -527,7 +582,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (ok) {
           const uint32_t peer = cluster_map(smem_addr(smem), static_cast<uint32_t>(rank ^ 1));
 #pragma unroll 1
-          for (int c = half * 32; c < kEpiBN; c += 64) {
+          for (int c = part * 32; c < kEpiBN; c += 32 * kWPQ) {
             float v[32];
             tmem_ld_32x32(lane_base + static_cast<uint32_t>((rank ^ 1) * kEpiBN + c), v);
             if (num_kb == 0) {  // a share of no k-blocks: the accumulator was never written
@@ -552,7 +607,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         cluster_sync();  // the partner's partial sums of this CTA's columns have landed
         if (ok) {
 #pragma unroll 1
-          for (int c = half * 32; c < kEpiBN; c += 64) {
+          for (int c = part * 32; c < kEpiBN; c += 32 * kWPQ) {
             float v[32];
             tmem_ld_32x32(lane_base + static_cast<uint32_t>(rank * kEpiBN + c), v);
             if (num_kb == 0) {
@@ -574,16 +629,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         constexpr bool kPre = EpiPrefetch<Epi>::value;
         if constexpr (kPre) {
           static_assert(kStages * S::kStageBytes >= static_cast<uint32_t>(kBM) * BN * 4, "the ring holds the tile");
-          ok = epilogue_bar_and(ok);  // every epilogue thread takes the same branch
+          ok = epilogue_bar_and<kET>(ok);  // every epilogue thread takes the same branch
           if (ok) {
             Epi::template prefetch<BN>(ep, g, m0, n0_epi, et, smem);  // the MMAs are done: the ring is idle
             cp_async_wait_all();
           }
-          epilogue_bar_sync();
+          epilogue_bar_sync<kET>();
         }
         if (ok) {
 #pragma unroll 1
-          for (int c = half * 32; c < BN; c += 64) {
+          for (int c = part * 32; c < BN; c += 32 * kWPQ) {
             float v[32];
             tmem_ld_32x32(lane_base + static_cast<uint32_t>(c), v);
             if constexpr (kPre)
@@ -595,7 +650,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     tc_fence_before();
-    ok = epilogue_bar_and(ok);
+    ok = epilogue_bar_and<kET>(ok);
     if constexpr (kSplit) {
       if (ok) Epi::store_staged(ep, g, m0, n0_epi, et, smem + kXchgBytes);
     }

@@ -37,7 +37,7 @@ pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(64 + EpiWarps<Epi>::value * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -279,6 +279,10 @@ __device__ __forceinline__ void scale_rows(const float* rs, const float* cs, int
 // Shared with the circuits: F[g][i][j] (+)= theta[g][i][j] * D[i,j].
 struct EpiThetaScale : EpiNoHooks {
   static constexpr bool kTranspose = true;
+  // TF32 accumulates unsliced: a parameter-flow entry is one contraction, not a chain of
+  // them, and its truncation bias (at most ~4e-5 of the value at K = 15872) is far below
+  // the mode's rounding; 256-wide tiles would not hold sliced sums in registers.
+  static constexpr int kSliceTF32 = 0;
   // Unsliced contractions fetch the tile's theta block into the idle ring with
   // asynchronous copies (32 in flight per thread) once the MMAs are done, instead of 16
   // dependent-free global loads at a time per thread in apply.
@@ -385,6 +389,7 @@ struct EpiThetaScale : EpiNoHooks {
 // warp is one contiguous row segment.
 struct EpiStoreF32 : EpiNoHooks {
   static constexpr bool kTranspose = true;
+  static constexpr int kSliceTF32 = 0;  // as EpiThetaScale
   struct Params {
     float* D;
     long long ld;

@@ -126,3 +126,40 @@ def test_more_than_1024_latents():
     assert flow_err(dpi, rpi) <= FLOW_TOL["fp32"]
     assert flow_err(dW[1:], rW[1:]) <= FLOW_TOL["fp32"]
     assert flow_err(dE, rE) <= FLOW_TOL["fp32"]
+
+
+def test_more_than_1024_categories():
+    # C > 1024 takes the gather-then-transpose dE path instead of the direct one
+    d = hclt_inputs(5, 64, 1100, 20, seed=204, parent=np.array([-1, 0, 0, 1, 2], dtype=np.int32))
+    rl, rpi, rW, rE = _oracle(d)
+    for mode in ("auto", "fp32"):
+        ll, dpi, dW, dE = _gpu_run(d, mode)
+        assert ll_err(ll, rl) <= LL_TOL[mode]
+        assert max(flow_err(dpi, rpi), flow_err(dW[1:], rW[1:]), flow_err(dE, rE)) <= FLOW_TOL[mode]
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_prepared_parameters_match_the_plain_call(mode):
+    # one prepared buffer serves two batches; every output equals pc_hclt_fwd_bwd's
+    # (dpi within float-atomic rounding), and the prepared call matches the oracle
+    d = hclt_inputs(40, 130, 17, 45, seed=205)
+    t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda() for k in ("data", "pi", "W", "E")}
+    prep = pc.hclt_prepare(d["parent"], t["W"], t["E"], precision=mode)
+    rng = np.random.default_rng(206)
+    for batch in range(2):
+        data = t["data"] if batch == 0 else torch.from_numpy(
+            rng.integers(0, 17, size=d["data"].shape, dtype=np.int64).astype(np.int32)).cuda()
+        plain = pc.hclt_fwd_bwd(d["parent"], data, t["pi"], t["W"], t["E"], precision=mode)
+        fast = pc.hclt_fwd_bwd(d["parent"], data, t["pi"], t["W"], None, precision=mode, prepared=prep)
+        torch.cuda.synchronize()
+        pc.device_status()
+        for i, (a, b) in enumerate(zip(plain, fast)):
+            if i == 1:
+                torch.testing.assert_close(b, a, rtol=1e-6, atol=0)
+            else:
+                assert torch.equal(a, b)
+        if batch == 0:
+            rl, rpi, rW, rE = _oracle(d)
+            ll, dpi, dW, dE = (x.cpu().numpy() for x in fast)
+            assert ll_err(ll, rl) <= LL_TOL[mode]
+            assert max(flow_err(dpi, rpi), flow_err(dW[1:], rW[1:]), flow_err(dE, rE)) <= FLOW_TOL[mode]

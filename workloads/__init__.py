@@ -23,7 +23,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "softmax_rows", "hmm_inputs", "tiny_hmm", "hmm", "layer_inputs", "layer",
+    "softmax_rows", "hmm_inputs", "hmm_edge_inputs", "tiny_hmm", "hmm", "layer_inputs", "layer",
     "hclt_parents", "hclt_inputs", "hclt", "lowrank_inputs", "lowrank",
     "SPREAD_SEEDS",
 ]
@@ -51,6 +51,26 @@ def hmm_inputs(H: int, T: int, V: int, B: int, seed: int):
     pi = softmax_rows(rng.standard_normal(H))
     A = softmax_rows(rng.standard_normal((H, H)))
     E = softmax_rows(rng.standard_normal((H, V)))
+    tokens = rng.integers(0, V, size=(B, T), dtype=np.int64).astype(np.int32)
+    return dict(pi=_f32(pi), A=_f32(A), E=_f32(E), tokens=np.ascontiguousarray(tokens))
+
+
+def hmm_edge_inputs(H: int, T: int, V: int, B: int, seed: int, e_scale: float = 1.0, zero_A: float = 0.0,
+                    zero_E: float = 0.0):
+    """HMM inputs with the structure of the numerical edge cases: emission rows a softmax
+    of N(0, e_scale^2) logits (peaked for a large scale), and a fraction of exact zeros
+    in the rows of A and of E (each row keeps its largest entry; rows renormalised).
+    Tokens uniform in [0, V)."""
+    rng = np.random.default_rng(seed)
+    pi = softmax_rows(rng.standard_normal(H))
+    A = softmax_rows(rng.standard_normal((H, H)))
+    E = softmax_rows(e_scale * rng.standard_normal((H, V)))
+    for M, frac in ((A, zero_A), (E, zero_E)):
+        if frac > 0:
+            keep = rng.uniform(size=M.shape) >= frac
+            keep[np.arange(M.shape[0]), M.argmax(axis=1)] = True
+            M *= keep
+            M /= M.sum(axis=1, keepdims=True)
     tokens = rng.integers(0, V, size=(B, T), dtype=np.int64).astype(np.int32)
     return dict(pi=_f32(pi), A=_f32(A), E=_f32(E), tokens=np.ascontiguousarray(tokens))
 
