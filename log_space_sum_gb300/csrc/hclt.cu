@@ -950,12 +950,13 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       if ((st = encode_maps(&mb, operand_view(w.Gbm, prec, 0, G), prec, ebn)) != PC_OK) return st;
       HcltElemParams ee{w.U32 + static_cast<long long>(sA) * B * H, w.F32 + static_cast<long long>(sA) * B * H, H,
                         B};
-      // a_early: Wᵀ's operand copy was written before the first scaled-flow kernel
+      // a_early: Wᵀ's operand copy was written before the first scaled-flow kernel. Levels with
+      // more tiles than SMs run persistent (bf16: one tile's epilogue under the next's K loop).
       if constexpr (P == kBF16) {
         if (wide)
-          st = launch_gemm<P, 2 * kHcltBN, EpiHcltElem<P, 2 * kHcltBN>>(
-              dim3(cdiv(H, kBM), cdiv(B, 2 * kHcltBN), G), ma.hi, ma.lo, mb.hi, mb.lo, num_k_blocks(H, prec), ee, s,
-              PC_KIND_HCLT_ELEM, 2ll * G * H * H * B, true);
+          st = launch_gemm_persist<P, 2 * kHcltBN, EpiHcltElem<P, 2 * kHcltBN>>(
+              cdiv(H, kBM), cdiv(B, 2 * kHcltBN), G, ma.hi, ma.lo, mb.hi, mb.lo, num_k_blocks(H, prec), ee, s,
+              PC_KIND_HCLT_ELEM, 2ll * G * H * H * B);
       }
       if (!wide)
         st = launch_gemm<P, kHcltBN, EpiHcltElem<P>>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi,
@@ -973,10 +974,17 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       if ((st = encode_maps(&ma, operand_view(w.Gnm, prec, 0, G), prec, kBM)) != PC_OK) return st;
       if ((st = encode_maps(&mb, operand_view(w.Unm, prec, 0, G), prec, kParamBN)) != PC_OK) return st;
       EpiThetaScale::Params ep{dW, W, H, H, accumulate, d_var + sA};
-      if ((st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), G), ma.hi, ma.lo,
-                                                        mb.hi, mb.lo, num_k_blocks(B, prec), ep, s,
-                                                        PC_KIND_HCLT_PARAM, 2ll * G * H * H * B)) != PC_OK)
-        return st;
+      // short K (= B) and a theta block per tile: persistent (bf16, TF32), so the epilogue's
+      // theta reads and dW writes overlap the next tile's K loop
+      if constexpr (P != kTF32x3)
+        st = launch_gemm_persist<P, kParamBN, EpiThetaScaleDirect>(cdiv(H, kBM), cdiv(H, kParamBN), G, ma.hi, ma.lo,
+                                                                   mb.hi, mb.lo, num_k_blocks(B, prec), ep, s,
+                                                                   PC_KIND_HCLT_PARAM, 2ll * G * H * H * B);
+      else
+        st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), G), ma.hi, ma.lo, mb.hi,
+                                                     mb.lo, num_k_blocks(B, prec), ep, s, PC_KIND_HCLT_PARAM,
+                                                     2ll * G * H * H * B);
+      if (st != PC_OK) return st;
     }
   }
   if (dE) {

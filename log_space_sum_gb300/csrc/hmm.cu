@@ -148,10 +148,13 @@ __global__ void __launch_bounds__(256) k_emission_transpose(const float* __restr
 constexpr float kScaleMax = 0x1p100f;
 constexpr float kRangeFloor = 0x1p-80f;
 constexpr float kUnderflowMark = 0x1p-149f;  // column max of a column whose nonzero products underflowed
-// (The bound is formed in double: the product of a small previous maximum and a denormal
-// emission bound underflows float32.)
-__device__ __forceinline__ float layer_scale(double bound) {
-  return bound > 0.0 ? static_cast<float>(fmin(1.0 / bound, static_cast<double>(kScaleMax))) : 0.f;
+// The bound of a chain layer is a product a * b (the previous maximum and the emission
+// bound), whose float32 product can underflow for a denormal b: the scale is formed as
+// (1/a)(1/b), where an overflow only meets the clamp. (Float only: this GPU's FP64 pipe is
+// narrow.)
+__device__ __forceinline__ float layer_scale(float bound) { return bound > 0.f ? fminf(1.f / bound, kScaleMax) : 0.f; }
+__device__ __forceinline__ float layer_scale2(float a, float b) {
+  return (a > 0.f && b > 0.f) ? fminf((1.f / a) * (1.f / b), kScaleMax) : 0.f;
 }
 
 __device__ __forceinline__ void write_scale(float c, float* cf, double* logc, long long idx) {
@@ -404,7 +407,7 @@ struct EpiHmmFwd {
       float cv = 0.f;
       if (b < p.B) {
         tok = p.tokens[static_cast<long long>(b) * p.T + p.t];
-        cv = layer_scale(static_cast<double>(p.umax_prev[b]) * p.emax_rs[tok]);
+        cv = layer_scale2(p.umax_prev[b], p.emax_rs[tok]);
         if (m0 == 0) write_scale(cv, p.cf, p.logc, static_cast<long long>(p.t) * p.B + b);
       }
       tok_s[c] = tok;
@@ -553,12 +556,13 @@ struct EpiHmmFwd {
 // A sample whose column maximum fell into (0, kRangeFloor) at some position left the
 // range the per-layer shift keeps exact: its LL is NaN, it passes no flow (r = 0) and the
 // device status word records kErrRange. One warp per sample (16-byte loads when H % 4 == 0
-// and the rows are aligned), sums in double.
-__global__ void __launch_bounds__(256) k_hmm_root(int H, int B, int T, const float* __restrict__ pi,
+// and the rows are aligned): each run of four products is summed in float and the runs in
+// double (one FP64 add per four values: this GPU's FP64 pipe is narrow).
+__global__ void __launch_bounds__(128) k_hmm_root(int H, int B, int T, const float* __restrict__ pi,
                                                   const float* __restrict__ U0, const double* __restrict__ logc,
                                                   const float* __restrict__ umax, double* __restrict__ ll,
                                                   float* __restrict__ rroot, unsigned* status) {
-  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (b >= B) return;
   const int lane = threadIdx.x & 31;
   const float* u = U0 + static_cast<long long>(b) * H;
@@ -568,8 +572,7 @@ __global__ void __launch_bounds__(256) k_hmm_root(int H, int B, int T, const flo
     const float4* p4 = reinterpret_cast<const float4*>(pi);
     for (int q = lane; q < H / 4; q += 32) {
       const float4 x = u4[q], y = p4[q];
-      s += static_cast<double>(x.x) * y.x + static_cast<double>(x.y) * y.y + static_cast<double>(x.z) * y.z +
-           static_cast<double>(x.w) * y.w;
+      s += static_cast<double>(fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w))));
     }
   } else {
     for (int k = lane; k < H; k += 32) s += static_cast<double>(pi[k]) * u[k];
@@ -1076,7 +1079,7 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
 
   {
     ProfileScope ps(s, PC_KIND_HMM_MEM, BH * 4 + H * 4ll + TB * 8 + B * 12ll);
-    k_hmm_root<<<cdiv(B, 8), 256, 0, s>>>(H, B, T, pi, w.U0, w.logc, w.umax, ll, w.rroot, device_status_word());
+    k_hmm_root<<<cdiv(B, 4), 128, 0, s>>>(H, B, T, pi, w.U0, w.logc, w.umax, ll, w.rroot, device_status_word());
     PC_LAUNCH_CHECK();
   }
   if (use_side && (st = side.join(s)) != PC_OK) return st;

@@ -663,6 +663,178 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------
+// Persistent form for many short tiles (the HCLT's per-edge contractions: K = H or B, tens
+// of thousands of tiles per step): one CTA per SM takes the tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (t = (g * tiles_m + m) * tiles_n + n, so a CTA's consecutive
+// tiles share A's row panel), the producer's ring runs on across tile boundaries, and the
+// accumulator alternates between two TMEM buffers, so that one tile's epilogue runs while
+// the next tile's K loop does. Unsliced bf16 or TF32, no split, no prefetched tile (the
+// ring is never idle); Epi::prepare runs per tile (the epilogue warps own their shared
+// memory between tiles). Waits and drains as in k_umma_gemm.
+template <int P, int BN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_umma_gemm_persist(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
+                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
+                        int num_kb, int tiles_m, int tiles_n, int groups, unsigned* status,
+                        const typename Epi::Params ep) {
+  static_assert(P == kBF16 || P == kTF32, "persistent tiles: bf16 or TF32");
+  static_assert(EpiWarps<Epi>::value == kEpiWarps && !EpiPrefetch<Epi>::value && !EpiBLo<Epi>::value,
+                "persistent tiles: default epilogue warps, no prefetched tile, no B lo part");
+  using S = GemmShape<P, BN, false>;
+  constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
+  constexpr int kSliceK = (P == kTF32 ? EpiSliceTF32<Epi>::value : Epi::kSliceBF16);
+  static_assert(kSliceK == 0, "persistent tiles accumulate unsliced");
+  constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256 : 512;
+  constexpr int kWPQ = kEpiWarps / 4;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * S::kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;    // [2]
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  float* tbuf_base = reinterpret_cast<float*>(smem + kStages * S::kStageBytes + 256);
+  uint8_t* epi_smem = reinterpret_cast<uint8_t*>(tbuf_base) + GemmPlan<P, BN, Epi>::kTBufBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long wl = first_wait_limit(status);
+  const int num_tiles = tiles_m * tiles_n * groups;
+  auto tile_coords = [&](int t, int& m0, int& n0, int& g) {
+    const int mn = tiles_m * tiles_n;
+    g = t / mn;
+    const int r = t - g * mn;
+    m0 = (r / tiles_n) * kBM;
+    n0 = (r % tiles_n) * BN;
+  };
+  auto a_tile = [&](int s) { return smem + s * S::kStageBytes; };
+  auto b_tile = [&](int s) { return smem + s * S::kStageBytes + S::kABytes; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&acc_full[b], 1);
+        mbar_init(&acc_empty[b], kEpiWarps);
+      }
+      mbar_init(mma_done, 1);
+      fence_barrier_init();
+      tma_prefetch_map(&tmA);
+      tma_prefetch_map(&tmB);
+    }
+    __syncwarp();
+    tmem_alloc(tmem_slot, kTmemCols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      grid_dependency_wait();
+      grid_dependents_launch();
+      int it = 0, issued = 0;  // k-blocks issued over all tiles
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int m0, n0, g;
+        tile_coords(t, m0, n0, g);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, status, kErrTimeoutProducer, wl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+          tma_load_3d(a_tile(s), &tmA, &full[s], kb * S::kBK, m0, g);
+          tma_load_3d(b_tile(s), &tmB, &full[s], kb * S::kBK, n0, g);
+          issued = it + 1;
+        }
+      }
+      for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
+        mbar_wait(&full[k % kStages], (k / kStages) & 1, status, kErrTimeoutDrain);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = umma_idesc(P == kBF16 ? 1u : 2u, kBM, BN);
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++local) {
+        const int a = local & 1;
+        if (!mbar_wait(&acc_empty[a], ((local >> 1) & 1) ^ 1, status, kErrTimeoutMma, wl)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(a * BN);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&full[s], (it / kStages) & 1, status, kErrTimeoutMma, wl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(a_tile(s)), b0 = smem_addr(b_tile(s));
+#pragma unroll
+          for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
+            const uint32_t off = kk * 32;
+            const uint32_t acc = (kb == 0 && kk == 0) ? 0u : 1u;
+            if constexpr (P == kBF16)
+              umma_bf16(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+            else
+              umma_tf32(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+          }
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&acc_full[a]);  // also on a timeout: the epilogue must not wait forever
+      }
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, status, kErrTimeoutDrain);
+    }
+  } else {
+    // ------------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;
+    const int ew = warp - 2;
+    const int q = warp & 3, part = ew >> 2;
+    const int row = q * 32 + lane;
+    float* tbuf = Epi::kTranspose ? tbuf_base + ew * kTBufFloats : nullptr;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    grid_dependency_wait();
+    bool ok = true;
+    int local = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      int m0, n0, g;
+      tile_coords(t, m0, n0, g);
+      Epi::prepare(ep, g, m0, n0, et, epi_smem);
+      epilogue_bar_sync();
+      const int a = local & 1;
+      ok = epilogue_bar_and(ok && mbar_wait(&acc_full[a], (local >> 1) & 1, status, kErrTimeoutEpilogue, wl));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = part * 32; c < BN; c += 32 * kWPQ) {
+        float v[32];
+        tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * BN + c), v);
+        if (c + 32 * kWPQ >= BN) {  // this warp's last chunk of the tile: the buffer is free
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+        Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+      }
+      Epi::finish(ep, g, m0, n0, et, epi_smem);
+      epilogue_bar_sync();  // prepare of the next tile rewrites the epilogue's shared memory
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // Default hooks for epilogues that need no per-CTA set-up or reduction.
 struct EpiNoHooks {
   static constexpr int kSmemBytes = 0;

@@ -49,6 +49,43 @@ pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo
   return PC_OK;
 }
 
+// The persistent contraction over tiles_m x tiles_n x groups tiles (k_umma_gemm_persist):
+// one CTA per SM, or fewer when there are fewer tiles.
+template <int P, int BN, class Epi>
+pc_status_t launch_gemm_persist(int tiles_m, int tiles_n, int groups, const CUtensorMap& a, const CUtensorMap& a_lo,
+                                const CUtensorMap& b, const CUtensorMap& b_lo, int num_kb,
+                                const typename Epi::Params& ep, cudaStream_t stream, int kind, long long flops) {
+  constexpr size_t smem = gemm_smem_bytes<P, BN, Epi>();
+  static_assert(smem <= 232448, "shared memory per CTA");
+  static bool attr_set[64] = {};
+  int dev = 0;
+  PC_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return set_error(PC_ERR_CUDA, "device index %d out of range", dev);
+  if (!attr_set[dev]) {
+    PC_CUDA(cudaFuncSetAttribute(k_umma_gemm_persist<P, BN, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem)));
+    attr_set[dev] = true;
+  }
+  const long long tiles = static_cast<long long>(tiles_m) * tiles_n * groups;
+  if (tiles == 0) return PC_OK;
+  const int slot = profile_begin(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles < num_sms() ? tiles : num_sms()));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  PC_CUDA(cudaLaunchKernelEx(&cfg, k_umma_gemm_persist<P, BN, Epi>, a, a_lo, b, b_lo, num_kb, tiles_m, tiles_n,
+                             groups, device_status_word(), ep));
+  PC_LAUNCH_CHECK();
+  profile_end(slot, stream, kind, flops);
+  return PC_OK;
+}
+
 // Tensor maps of an operand's hi and (3xTF32) lo parts.
 struct OperandMaps {
   CUtensorMap hi, lo;
@@ -382,6 +419,12 @@ struct EpiThetaScale : EpiNoHooks {
         if (i0 + h + r < p.M) Fp[(h + r) * ld] = f[r] + ts[(h + r) * BN] * w[h + r];
     }
   }
+};
+
+// EpiThetaScale reading theta directly in apply (the persistent contraction's ring is never
+// idle, so no tile is prefetched into it).
+struct EpiThetaScaleDirect : EpiThetaScale {
+  static constexpr bool kPrefetchTile = false;
 };
 
 // D[i][j] (+)= the accumulator: the contraction's result as a float32 matrix (rows ld
