@@ -326,20 +326,41 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
 // The log-likelihood. Every node lies under the root, so the root's offset is the sum over
 // all nodes of their own log max: LL_b = ln 2 sum_v e_v[b] + sum_v log m_v[b] +
 // log sum_z pi u_0[b][z], summed in double (the exponents exactly, as integers); also
-// 1 / sum_z pi u_0 for the root flows. One thread per sample.
-__global__ void k_hclt_ll(int nslots, int B, const int* __restrict__ Ex, const float* __restrict__ Lm,
-                          const float* __restrict__ rdot, double* __restrict__ ll, float* __restrict__ rroot) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
+// 1 / sum_z pi u_0 for the root flows. A block per 32 samples, one per lane: warp w sums
+// the nodes w, w + 8, ... (128-byte loads, independent of one another), and the eight
+// partial sums are combined in warp order.
+constexpr int kLlWarps = 8;
+__global__ void __launch_bounds__(kLlWarps * 32) k_hclt_ll(int nslots, int B, const int* __restrict__ Ex,
+                                                          const float* __restrict__ Lm,
+                                                          const float* __restrict__ rdot, double* __restrict__ ll,
+                                                          float* __restrict__ rroot) {
+  __shared__ long long esum_w[kLlWarps][32];
+  __shared__ double lsum_w[kLlWarps][32];
+  __shared__ int live_w[kLlWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int b = blockIdx.x * 32 + lane;
   long long esum = 0;
   double lsum = 0.0;
   bool live = true;
-  for (int s = 0; s < nslots; ++s) {
-    const long long idx = static_cast<long long>(s) * B + b;
-    const float l = Lm[idx];
-    live = live && l > -INFINITY;
-    esum += Ex[idx];
-    lsum += static_cast<double>(l);
+  if (b < B) {
+#pragma unroll 4
+    for (int s = w; s < nslots; s += kLlWarps) {
+      const long long idx = static_cast<long long>(s) * B + b;
+      const float l = Lm[idx];
+      live = live && l > -INFINITY;
+      esum += Ex[idx];
+      lsum += static_cast<double>(l);
+    }
+  }
+  esum_w[w][lane] = esum;
+  lsum_w[w][lane] = lsum;
+  live_w[w][lane] = live;
+  __syncthreads();
+  if (w != 0 || b >= B) return;
+  for (int k = 1; k < kLlWarps; ++k) {
+    esum += esum_w[k][lane];
+    lsum += lsum_w[k][lane];
+    live = live && live_w[k][lane];
   }
   const float dot = rdot[b];
   live = live && dot > 0.f;
@@ -475,12 +496,13 @@ __global__ void k_hclt_dE_gather(int H, int B, int C, const int* __restrict__ va
 }
 
 // dE[v][z][k] (+)= sum over the samples of node s with category k of f[s][b][z], written
-// directly in the caller's [nvars][H][C] layout: one block per (node, 32 latents), one
-// latent per lane. Warp w owns the categories [w C / 8, (w + 1) C / 8) and walks their
-// samples in bucket order (stable, so the sums are deterministic), 32 at a time: their
-// indices in one load, their 32 rows of f (128 bytes each) all in flight together, then a
-// running sum per category into a padded [32][C + 1] shared tile that the block writes
-// out as rows of C categories. For C <= kDEDirectMaxC.
+// directly in the caller's [nvars][H][C] layout: one block per (32 latents, node), the
+// blocks of one node side by side (they read the same 4 KB rows of f), one latent per lane.
+// Warp w owns the categories [w C / 8, (w + 1) C / 8) and walks their samples in bucket
+// order (stable, so the sums are deterministic), 32 at a time: their indices in one load,
+// their 32 rows of f (128 bytes each) all in flight together, then a running sum per
+// category into a padded [32][C + 1] shared tile that the block writes out as rows of C
+// categories. For C <= kDEDirectMaxC.
 constexpr int kDEDirectMaxC = 1024;
 __global__ void __launch_bounds__(256) k_hclt_dE_direct(int H, int B, int C, const int* __restrict__ var_of_slot,
                                                         const int* __restrict__ order, const int* __restrict__ off,
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(256) k_hclt_dE_direct(int H, int B, int C, con
                                                         int accumulate) {
   extern __shared__ float acc[];  // [32][C + 1], then C + 1 bucket offsets
   int* offs = reinterpret_cast<int*>(acc + 32 * (C + 1));
-  const int s = blockIdx.x, z0 = blockIdx.y * 32;
+  const int s = blockIdx.y, z0 = blockIdx.x * 32;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int v = var_of_slot[s];
   const int* ord = order + static_cast<long long>(s) * B;
@@ -621,6 +643,25 @@ struct EpiHcltElem : EpiNoHooks {
       else
         u[c] = n0 + col0 + c < p.B ? p.U32[base + static_cast<long long>(c) * p.H] : 0.f;
     }
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      if (n0 + col0 + c < p.B) p.F32[base + static_cast<long long>(c) * p.H] = u[c] * v[c];
+  }
+
+  // persistent tiles (the unstaged 256-wide form): the chunk's node values one chunk ahead
+  static constexpr bool kLoadAhead = !kStage;
+  __device__ static void load(const Params& p, int g, int m0, int n0, int row, int col0, float (&u)[32]) {
+    const int z = m0 + row;
+    const long long base = (static_cast<long long>(g) * p.B + n0 + col0) * p.H + z;
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      u[c] = (z < p.H && n0 + col0 + c < p.B) ? p.U32[base + static_cast<long long>(c) * p.H] : 0.f;
+  }
+  __device__ static void apply_loaded(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
+                                      const float (&u)[32], float*) {
+    const int z = m0 + row;
+    if (z >= p.H) return;
+    const long long base = (static_cast<long long>(g) * p.B + n0 + col0) * p.H + z;
 #pragma unroll
     for (int c = 0; c < 32; ++c)
       if (n0 + col0 + c < p.B) p.F32[base + static_cast<long long>(c) * p.H] = u[c] * v[c];
@@ -809,13 +850,10 @@ pc_status_t hclt_prepare(int n, int H, int C, const int32_t* parent, const float
   }
   if ((st = transpose_f32(Em, C, static_cast<long long>(H) * C, n, H, C, w.Et, H, 0, s)) != PC_OK) return st;
   const int E = n - 1;
-  if (E > 0) {
-    if ((st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, w.var_of_slot)) != PC_OK)
-      return st;
-    if ((st = transpose_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.WopT, s, w.var_of_slot)) !=
-        PC_OK)
-      return st;
-  }
+  if (E > 0 &&
+      (st = operand_and_transpose<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, w.WopT, s, w.var_of_slot)) !=
+          PC_OK)
+    return st;
   return PC_OK;
 }
 
@@ -868,8 +906,11 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     if ((st = transpose_f32(Em, C, static_cast<long long>(H) * C, n, H, C, w.Et, H, 0, s)) != PC_OK) return st;
   }
   if (E > 0 && !prep) {
-    ProfileScope ps(s, PC_KIND_HCLT_MEM, E * HH * (4 + eb));
-    if ((st = rows_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.Wop, s, d_var)) != PC_OK) return st;
+    // W's two operand copies (Wᵀ's for the element flows) in one pass over W
+    ProfileScope ps(s, PC_KIND_HCLT_MEM, E * HH * (4 + (down ? 2 : 1) * eb));
+    if ((st = down ? operand_and_transpose<P>(W, H, HH, E, H, H, w.Wop, w.WopT, s, d_var)
+                   : rows_to_operand<P>(W, H, HH, E, H, H, w.Wop, s, d_var)) != PC_OK)
+      return st;
   }
 
   // -------------------------------------------------------------- forward
@@ -913,7 +954,7 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
   }
   {
     ProfileScope ps(s, PC_KIND_HCLT_MEM, n * B * 8ll + B * 16ll);
-    k_hclt_ll<<<cdiv(B, 128), 128, 0, s>>>(n, B, w.Ex, w.Lm, w.rdot, ll, w.rroot);
+    k_hclt_ll<<<cdiv(B, 32), kLlWarps * 32, 0, s>>>(n, B, w.Ex, w.Lm, w.rdot, ll, w.rroot);
     PC_LAUNCH_CHECK();
   }
   if (!flows) return PC_OK;
@@ -925,11 +966,6 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     PC_LAUNCH_CHECK();
   }
   if (down) {
-    if (!prep) {
-      ProfileScope ps(s, PC_KIND_HCLT_MEM, E * HH * (4 + eb));
-      if ((st = transpose_to_operand<P>(W, H, static_cast<long long>(H) * H, E, H, H, w.WopT, s, d_var)) != PC_OK)
-        return st;
-    }
     for (int L = pl.maxh - 1; L >= 0; --L) {
       const int sA = pl.level_start[L], sB = pl.level_start[L + 1];
       const int G = sB - sA;
@@ -977,9 +1013,9 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       // short K (= B) and a theta block per tile: persistent (bf16, TF32), so the epilogue's
       // theta reads and dW writes overlap the next tile's K loop
       if constexpr (P != kTF32x3)
-        st = launch_gemm_persist<P, kParamBN, EpiThetaScaleDirect>(cdiv(H, kBM), cdiv(H, kParamBN), G, ma.hi, ma.lo,
-                                                                   mb.hi, mb.lo, num_k_blocks(B, prec), ep, s,
-                                                                   PC_KIND_HCLT_PARAM, 2ll * G * H * H * B);
+        st = launch_gemm_persist<P, kParamBN, EpiThetaScaleAhead>(cdiv(H, kBM), cdiv(H, kParamBN), G, ma.hi, ma.lo,
+                                                                  mb.hi, mb.lo, num_k_blocks(B, prec), ep, s,
+                                                                  PC_KIND_HCLT_PARAM, 2ll * G * H * H * B);
       else
         st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), G), ma.hi, ma.lo, mb.hi,
                                                      mb.lo, num_k_blocks(B, prec), ep, s, PC_KIND_HCLT_PARAM,
@@ -999,7 +1035,7 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
         PC_CUDA(cudaFuncSetAttribute(k_hclt_dE_direct, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)));
       ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + (accumulate ? 2 : 1) * n * CH * 4);
-      k_hclt_dE_direct<<<dim3(n, cdiv(H, 32)), 256, smem, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, dE,
+      k_hclt_dE_direct<<<dim3(cdiv(H, 32), n), 256, smem, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, dE,
                                                                accumulate);
       PC_LAUNCH_CHECK();
       return PC_OK;

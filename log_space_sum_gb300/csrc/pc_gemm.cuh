@@ -55,6 +55,17 @@ struct EpiBLo : std::false_type {};
 template <class E>
 struct EpiBLo<E, std::void_t<decltype(E::kBLo)>> : std::bool_constant<E::kBLo> {};
 
+// Epi::kLoadAhead (optional, persistent tiles only): the epilogue's global operand of a
+// chunk (a theta block, a block of node values) is loaded into registers by
+// Epi::load(p, g, m0, n0, row, col0, t[32]) one chunk ahead, before the accumulator of that
+// chunk is waited for, and consumed by Epi::apply_loaded(p, g, m0, n0, row, col0, v, t,
+// tbuf): a warp keeps 32 loads per thread in flight through its stores, the TMEM loads and
+// the accumulator wait, which is what keeps a memory-bound epilogue near the HBM rate.
+template <class E, class = void>
+struct EpiLoadAhead : std::false_type {};
+template <class E>
+struct EpiLoadAhead<E, std::void_t<decltype(E::kLoadAhead)>> : std::bool_constant<E::kLoadAhead> {};
+
 // Warp 0: TMA producer; warp 1: MMA issuer; then the epilogue warps, kEpiWarps / 4 per
 // TMEM lane quarter, each taking every (kEpiWarps / 4)-th 32-column chunk of the tile.
 // Epi::kEpiWarps (optional) sets the count for one instantiation: 16 for the sliced
@@ -86,10 +97,13 @@ struct GemmShape {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: two epilogue warps split the 32-column chunks");
 };
 
-// Accumulation slices, in MMA k-steps (1, or a multiple of the k-steps of one ring
+// Accumulation slices, in MMA k-steps (1 or 2, or a multiple of the k-steps of one ring
 // slot); see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
 // (Epi::kSliceBF16 k-steps; 0 = one accumulation over all of K).
-constexpr int kSliceK3x = 1;
+#ifndef PC_SLICE_K3X
+#define PC_SLICE_K3X 1
+#endif
+constexpr int kSliceK3x = PC_SLICE_K3X;
 constexpr int kSliceK1 = 8;  // the TF32 default (EpiSliceTF32)
 
 // The tensor core's float32 accumulator truncates toward zero. A slice of one 3xTF32
@@ -252,8 +266,9 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
   constexpr int kSliceK = (P == kTF32x3) ? kSliceK3x : (P == kTF32 ? EpiSliceTF32<Epi>::value : Epi::kSliceBF16);
   constexpr bool kSliced = kSliceK > 0;
   constexpr bool kStepSliced = kSliced && kSliceK < static_cast<int>(S::kKSteps);
-  static_assert(!kSliced || kStepSliced ? kSliceK <= 1 : kSliceK % S::kKSteps == 0,
-                "slices are one k-step or whole ring slots");
+  static_assert(!kSliced || (kStepSliced ? S::kKSteps % kSliceK == 0 && (kSliceK == 1 || P == kTF32x3)
+                                           : kSliceK % S::kKSteps == 0),
+                "slices are k-steps that divide a ring slot (several: 3xTF32) or whole ring slots");
   constexpr int kAccBufs = !kSliced ? 1 : (kStepSliced && 4 * BN <= 512 ? 4 : 2);
   static_assert(!kBLo || (kSliced && !kStepSliced), "B lo parts with slot-granular slices");
   constexpr uint32_t kLoCol = kAccBufs * BN;  // the B_lo accumulator's first column
@@ -263,6 +278,10 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
                                  : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM columns");
   constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
+#ifndef PC_SLICE_CORR
+#define PC_SLICE_CORR (kSliceK == 1 ? 0x34800000u : 0x34C00000u)
+#endif
+  constexpr uint32_t kCorrBits = PC_SLICE_CORR;
   // split K: the idle ring holds the exchange buffer (128 x BN/2 floats), then the
   // epilogue's staged tiles
   constexpr int kXchgBytes = kBM * (BN / 2) * 4;
@@ -395,10 +414,11 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
         const uint32_t b1 = smem_addr(b_tile(s, S::kBParts == 2 ? 1 : 0));
         bool timed_out = false;
         if constexpr (kStepSliced) {
-          // one slice per k-step, each into the next of kAccBufs buffers
+          // one slice per kSliceK k-steps, each into the next of kAccBufs buffers; in
+          // 3xTF32 the small cross terms of the slice's k-steps first, then hi*hi
 #pragma unroll
-          for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
-            const int sl = q + static_cast<int>(kk);
+          for (uint32_t k0 = 0; k0 < S::kKSteps; k0 += kSliceK) {
+            const int sl = (q + static_cast<int>(k0)) / kSliceK;
             const int buf = sl % kAccBufs;
             if (!mbar_wait(&acc_empty[buf], ((sl / kAccBufs) & 1) ^ 1, status, kErrTimeoutMma, wl)) {
               timed_out = true;
@@ -406,13 +426,18 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
             }
             tc_fence_after();
             const uint32_t ds = tmem + static_cast<uint32_t>(buf * BN);
-            const uint32_t off = kk * 32;
             if constexpr (P == kTF32x3) {
-              umma_tf32(ds, umma_desc_sw128(a1 + off), umma_desc_sw128(b0 + off), idesc, 0u);
-              umma_tf32(ds, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, 1u);
-              umma_tf32(ds, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, 1u);
+#pragma unroll
+              for (uint32_t kk = k0; kk < k0 + kSliceK; ++kk) {
+                const uint32_t off = kk * 32;
+                umma_tf32(ds, umma_desc_sw128(a1 + off), umma_desc_sw128(b0 + off), idesc, kk == k0 ? 0u : 1u);
+                umma_tf32(ds, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, 1u);
+              }
+#pragma unroll
+              for (uint32_t kk = k0; kk < k0 + kSliceK; ++kk)
+                umma_tf32(ds, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc, 1u);
             } else {
-              umma_tf32(ds, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, 0u);
+              umma_tf32(ds, umma_desc_sw128(a0 + k0 * 32), umma_desc_sw128(b0 + k0 * 32), idesc, 0u);
             }
             umma_commit(&acc_full[buf]);
           }
@@ -503,7 +528,7 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
       auto add_slice = [&](float (&a)[32], const uint32_t (&v)[32], bool corr) {
         if (kHalfUlp && corr) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) add2_half_ulp(a[i], a[i + 1], v[i], v[i + 1], 0x34800000u);  // 4 x 2^-24
+          for (int i = 0; i < 32; i += 2) add2_half_ulp(a[i], a[i + 1], v[i], v[i + 1], kCorrBits);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) add2(a[i], a[i + 1], v[i], v[i + 1]);
@@ -804,28 +829,67 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     grid_dependency_wait();
     bool ok = true;
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      int m0, n0, g;
-      tile_coords(t, m0, n0, g);
-      Epi::prepare(ep, g, m0, n0, et, epi_smem);
-      epilogue_bar_sync();
-      const int a = local & 1;
-      ok = epilogue_bar_and(ok && mbar_wait(&acc_full[a], (local >> 1) & 1, status, kErrTimeoutEpilogue, wl));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int c = part * 32; c < BN; c += 32 * kWPQ) {
-        float v[32];
-        tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * BN + c), v);
-        if (c + 32 * kWPQ >= BN) {  // this warp's last chunk of the tile: the buffer is free
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[a]);
-        }
-        Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+    if constexpr (EpiLoadAhead<Epi>::value) {
+      static_assert(Epi::kSmemBytes == 0, "load-ahead epilogues keep no per-tile shared memory");
+      float tn[32];  // the next chunk's operand
+      if (static_cast<int>(blockIdx.x) < num_tiles) {
+        int m0, n0, g;
+        tile_coords(blockIdx.x, m0, n0, g);
+        Epi::load(ep, g, m0, n0, row, part * 32, tn);
       }
-      Epi::finish(ep, g, m0, n0, et, epi_smem);
-      epilogue_bar_sync();  // prepare of the next tile rewrites the epilogue's shared memory
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+        int m0, n0, g;
+        tile_coords(t, m0, n0, g);
+        const int a = local & 1;
+        ok = epilogue_bar_and(ok && mbar_wait(&acc_full[a], (local >> 1) & 1, status, kErrTimeoutEpilogue, wl));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = part * 32; c < BN; c += 32 * kWPQ) {
+          float tc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tc[i] = tn[i];
+          const bool last = c + 32 * kWPQ >= BN;  // this warp's last chunk of the tile
+          const int tx = last ? t + static_cast<int>(gridDim.x) : t;
+          if (tx < num_tiles) {
+            int mx, nx, gx;
+            tile_coords(tx, mx, nx, gx);
+            Epi::load(ep, gx, mx, nx, row, last ? part * 32 : c + 32 * kWPQ, tn);
+          }
+          float v[32];
+          tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * BN + c), v);
+          if (last) {  // the buffer is free
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+          }
+          Epi::apply_loaded(ep, g, m0, n0, row, c, v, tc, tbuf);
+        }
+      }
+    } else {
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+        int m0, n0, g;
+        tile_coords(t, m0, n0, g);
+        Epi::prepare(ep, g, m0, n0, et, epi_smem);
+        epilogue_bar_sync();
+        const int a = local & 1;
+        ok = epilogue_bar_and(ok && mbar_wait(&acc_full[a], (local >> 1) & 1, status, kErrTimeoutEpilogue, wl));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = part * 32; c < BN; c += 32 * kWPQ) {
+          float v[32];
+          tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * BN + c), v);
+          if (c + 32 * kWPQ >= BN) {  // this warp's last chunk of the tile: the buffer is free
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+          }
+          Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+        }
+        Epi::finish(ep, g, m0, n0, et, epi_smem);
+        epilogue_bar_sync();  // prepare of the next tile rewrites the epilogue's shared memory
+      }
     }
   }
   __syncthreads();

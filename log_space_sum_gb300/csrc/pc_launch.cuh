@@ -212,6 +212,37 @@ struct StoreOperand {  // an operand matrix [g][c][ld] in precision P
   long long rows_per_group;
 };
 
+// The untransposed copy (k_transpose64's Direct): the operand [g][r][ld] of the tile's own
+// rows, four consecutive columns per call (n <= 4 valid).
+template <int P>
+struct StoreOperandRows {
+  void* dst;
+  long long ld;
+  size_t lo;
+  long long rows_per_group;
+  __device__ void operator()(int g, int r, int c, const float4& v, int n) const {
+    const size_t idx = static_cast<size_t>((static_cast<long long>(g) * rows_per_group + r) * ld + c);
+    if (n == 4) {
+      if constexpr (P == kBF16) {
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(dst) + idx) =
+            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      } else {
+        const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(dst) + idx) = h;
+        if constexpr (P == kTF32x3)
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(dst) + idx + lo) =
+              make_float4(tf32_rna(v.x - h.x), tf32_rna(v.y - h.y), tf32_rna(v.z - h.z), tf32_rna(v.w - h.w));
+      }
+    } else {
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      for (int k = 0; k < n; ++k) store_operand<P>(dst, idx + k, lo, x[k]);
+    }
+  }
+};
+struct NoDirect {
+  __device__ void operator()(int, int, int, const float4&, int) const {}
+};
+
 struct StoreF32 {  // a float32 matrix [g][c][ld], overwritten or accumulated into
   float* dst;
   long long ld, rows_per_group;
@@ -237,9 +268,10 @@ struct StoreF32 {  // a float32 matrix [g][c][ld], overwritten or accumulated in
   }
 };
 
-template <class Store>
+template <class Store, class Direct = NoDirect>
 __global__ void __launch_bounds__(256) k_transpose64(const float* __restrict__ src, long long src_ld,
-                                                      long long src_gs, int R, int C, const int* gmap, Store st) {
+                                                      long long src_gs, int R, int C, const int* gmap, Store st,
+                                                      Direct direct = {}) {
   __shared__ float tile[64][65];
   const int g = blockIdx.z;
   const long long gs = gmap ? gmap[g] : g;
@@ -262,6 +294,7 @@ __global__ void __launch_bounds__(256) k_transpose64(const float* __restrict__ s
         if (c + 2 < C) v.z = p[2];
         if (c + 3 < C) v.w = p[3];
       }
+      if (c < C) direct(g, r, c, v, min(4, C - c));
     }
     tile[rr][cq] = v.x;
     tile[rr][cq + 1] = v.y;
@@ -296,6 +329,19 @@ pc_status_t transpose_to_operand(const float* src, long long src_ld, long long s
   // operand rows are 64-element aligned, so full runs of 8 are 16-byte aligned
   return launch_transpose64(src, src_ld, src_gs, G, R, C, gmap,
                             StoreOperand<P>{dst.ptr, dst.ld, dst.lo_elems, static_cast<long long>(C)}, s);
+}
+
+// Both operand copies of src in one pass over it: rows (dst[g][r][c], as rows_to_operand)
+// and transposed (dstT[g][c][r], as transpose_to_operand).
+template <int P>
+pc_status_t operand_and_transpose(const float* src, long long src_ld, long long src_gs, int G, int R, int C,
+                                  const Operand& dst, const Operand& dstT, cudaStream_t s, const int* gmap = nullptr) {
+  if (G == 0 || R == 0 || C == 0) return PC_OK;
+  k_transpose64<StoreOperand<P>, StoreOperandRows<P>><<<dim3(cdiv(C, 64), cdiv(R, 64), G), 256, 0, s>>>(
+      src, src_ld, src_gs, R, C, gmap, StoreOperand<P>{dstT.ptr, dstT.ld, dstT.lo_elems, static_cast<long long>(C)},
+      StoreOperandRows<P>{dst.ptr, dst.ld, dst.lo_elems, static_cast<long long>(R)});
+  PC_LAUNCH_CHECK();
+  return PC_OK;
 }
 
 // dst[g][c][r] (+)= src[g][r][c] in float32, dst rows ld apart.
@@ -425,6 +471,46 @@ struct EpiThetaScale : EpiNoHooks {
 // idle, so no tile is prefetched into it).
 struct EpiThetaScaleDirect : EpiThetaScale {
   static constexpr bool kPrefetchTile = false;
+};
+
+// EpiThetaScale on persistent tiles: the theta rows of a chunk are loaded one chunk ahead
+// (kLoadAhead; streaming loads, read once), and the flows are written with streaming
+// stores, or added by one reduction per element when accumulating (each element of F
+// has one writer per call).
+struct EpiThetaScaleAhead : EpiThetaScaleDirect {
+  static constexpr bool kLoadAhead = true;
+  __device__ static void load(const Params& p, int g, int m0, int n0, int row, int col0, float (&t)[32]) {
+    const int lane = threadIdx.x & 31;
+    const int i0 = m0 + row - lane;
+    const int j = n0 + col0 + lane;
+    const long long ld = p.N;
+    const long long gm = p.gmap ? p.gmap[g] : g;
+    const float* tp = p.theta + (gm * p.M + i0) * ld + j;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) t[r] = (j < p.N && i0 + r < p.M) ? __ldcs(tp + r * ld) : 0.f;
+  }
+  __device__ static void apply_loaded(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
+                                      const float (&t)[32], float* tbuf) {
+    float w[32];
+    warp_transpose32(v, w, tbuf);
+    const int lane = threadIdx.x & 31;
+    const int i0 = m0 + row - lane;
+    const int j = n0 + col0 + lane;
+    if (j >= p.N) return;
+    const long long ld = p.N;
+    const long long gm = p.gmap ? p.gmap[g] : g;
+    float* Fp = p.F + (gm * p.M + i0) * ld + j;
+    if (p.rscale || p.cscale) scale_rows(p.rscale, p.cscale, i0, j, p.M, w);
+    if (p.accumulate) {
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        if (i0 + r < p.M) atomicAdd(Fp + r * ld, t[r] * w[r]);
+    } else {
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        if (i0 + r < p.M) __stcs(Fp + r * ld, t[r] * w[r]);
+    }
+  }
 };
 
 // D[i][j] (+)= the accumulator: the contraction's result as a float32 matrix (rows ld
