@@ -496,13 +496,12 @@ __global__ void k_hclt_dE_gather(int H, int B, int C, const int* __restrict__ va
 }
 
 // dE[v][z][k] (+)= sum over the samples of node s with category k of f[s][b][z], written
-// directly in the caller's [nvars][H][C] layout: one block per (32 latents, node), the
-// blocks of one node side by side (they read the same 4 KB rows of f), one latent per lane.
-// Warp w owns the categories [w C / 8, (w + 1) C / 8) and walks their samples in bucket
-// order (stable, so the sums are deterministic), 32 at a time: their indices in one load,
-// their 32 rows of f (128 bytes each) all in flight together, then a running sum per
-// category into a padded [32][C + 1] shared tile that the block writes out as rows of C
-// categories. For C <= kDEDirectMaxC.
+// directly in the caller's [nvars][H][C] layout: one block per (node, 32 latents), one
+// latent per lane. Warp w owns the categories [w C / 8, (w + 1) C / 8) and walks their
+// samples in bucket order (stable, so the sums are deterministic), 32 at a time: their
+// indices in one load, their 32 rows of f (128 bytes each) all in flight together, then a
+// running sum per category into a padded [32][C + 1] shared tile that the block writes out
+// as rows of C categories. For C <= kDEDirectMaxC.
 constexpr int kDEDirectMaxC = 1024;
 __global__ void __launch_bounds__(256) k_hclt_dE_direct(int H, int B, int C, const int* __restrict__ var_of_slot,
                                                         const int* __restrict__ order, const int* __restrict__ off,
@@ -510,12 +509,13 @@ __global__ void __launch_bounds__(256) k_hclt_dE_direct(int H, int B, int C, con
                                                         int accumulate) {
   extern __shared__ float acc[];  // [32][C + 1], then C + 1 bucket offsets
   int* offs = reinterpret_cast<int*>(acc + 32 * (C + 1));
-  const int s = blockIdx.y, z0 = blockIdx.x * 32;
+  const int s = blockIdx.x, z0 = blockIdx.y * 32;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int v = var_of_slot[s];
   const int* ord = order + static_cast<long long>(s) * B;
   for (int i = threadIdx.x; i <= C; i += blockDim.x) offs[i] = off[static_cast<long long>(s) * (C + 1) + i];
-  for (int i = threadIdx.x; i < 32 * (C + 1); i += blockDim.x) acc[i] = 0.f;
+  for (int i = 4 * threadIdx.x; i < 32 * (C + 1); i += 4 * blockDim.x)  // 32 (C + 1) is a multiple of 4
+    *reinterpret_cast<float4*>(acc + i) = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   const float* fs = F32 + static_cast<long long>(s) * B * H + z0 + lane;
   const bool zin = z0 + lane < H;
@@ -547,11 +547,10 @@ __global__ void __launch_bounds__(256) k_hclt_dE_direct(int H, int B, int C, con
   if (k < ke) arow[k] = run;  // the last non-empty category (later ones stay 0)
   __syncthreads();
   const int zmax = min(32, H - z0);
-  for (int i = threadIdx.x; i < zmax * C; i += blockDim.x) {
-    const int zz = i / C, kk = i - zz * C;
-    float* dst = dE + (static_cast<long long>(v) * H + z0 + zz) * C + kk;
-    const float y = acc[zz * (C + 1) + kk];
-    *dst = accumulate ? *dst + y : y;
+  for (int zz = 0; zz < zmax; ++zz) {  // row by row: no division per element
+    float* drow = dE + (static_cast<long long>(v) * H + z0 + zz) * C;
+    const float* arow_z = acc + zz * (C + 1);
+    for (int kk = threadIdx.x; kk < C; kk += blockDim.x) drow[kk] = accumulate ? drow[kk] + arow_z[kk] : arow_z[kk];
   }
 }
 
@@ -609,6 +608,14 @@ struct EpiHcltFwd : EpiNoHooks {
   }
 };
 
+// The bf16 forward on persistent tiles: one accumulation over K (= H) per tile, hi and lo
+// parts of the children operand side by side. Unsliced, the accumulator's truncation
+// costs each edge at most about H / 16 half-ulps of D (K = 1024: ~2e-6 of D, far inside
+// the bf16 mode's rounding); in exchange one tile's stores run under the next tile's MMAs.
+struct EpiHcltFwdWhole : EpiHcltFwd {
+  static constexpr int kSliceBF16 = 0;
+};
+
 // Element-flow epilogue: f[g][b][z'] = u[g][b][z'] * D[z', b]; thread = child latent z'.
 // For 128-wide tiles the u block is staged in shared memory during the K loop (not in
 // 3xTF32, whose ring needs the room); 256-wide tiles read it directly (a 128 KB block
@@ -622,7 +629,9 @@ template <int P, int BN = kHcltBN>
 struct EpiHcltElem : EpiNoHooks {
   using Params = HcltElemParams;
   static constexpr bool kStage = P != kTF32x3 && BN == kHcltBN;
-  static constexpr int kSmemBytes = kStage ? kHcltBN * kBM * 4 : 0;
+  static constexpr bool kLoadAhead = BN == 2 * kHcltBN;  // the persistent 256-wide form, see issue
+  static constexpr int kAheadBufs = 2;  // as EpiThetaScaleAhead
+  static constexpr int kSmemBytes = kStage ? kHcltBN * kBM * 4 : (kLoadAhead ? kEpiWarps * kAheadBufs * 4096 : 0);
 
   __device__ static void prepare(const Params& p, int g, int m0, int n0, int et, uint8_t* smem) {
     if constexpr (kStage)
@@ -648,23 +657,30 @@ struct EpiHcltElem : EpiNoHooks {
       if (n0 + col0 + c < p.B) p.F32[base + static_cast<long long>(c) * p.H] = u[c] * v[c];
   }
 
-  // persistent tiles (the unstaged 256-wide form): the chunk's node values one chunk ahead
-  static constexpr bool kLoadAhead = !kStage;
-  __device__ static void load(const Params& p, int g, int m0, int n0, int row, int col0, float (&u)[32]) {
-    const int z = m0 + row;
-    const long long base = (static_cast<long long>(g) * p.B + n0 + col0) * p.H + z;
+  // persistent tiles (kLoadAhead): the chunk's node values u[b][z] (32 samples x 32
+  // latents) come through the warp's ring of shared-memory buffers; lane = latent z reads
+  // them conflict-free. Needs H % 4 == 0 (16-byte rows).
+  __device__ static void issue(const Params& p, int g, int m0, int n0, int q, int col0, float* buf) {
+    const int lane = threadIdx.x & 31;
+    const int z = m0 + q * 32 + 4 * (lane & 7);
 #pragma unroll
-    for (int c = 0; c < 32; ++c)
-      u[c] = (z < p.H && n0 + col0 + c < p.B) ? p.U32[base + static_cast<long long>(c) * p.H] : 0.f;
+    for (int k = 0; k < 8; ++k) {
+      const int c = 4 * k + (lane >> 3);
+      const int b = n0 + col0 + c;
+      const int n = (b < p.B && z < p.H) ? min(4, p.H - z) : 0;
+      const float* src = n ? p.U32 + (static_cast<long long>(g) * p.B + b) * p.H + z : p.U32;
+      cp_async_16(reinterpret_cast<uint8_t*>(buf + c * 32 + 4 * (lane & 7)), src, static_cast<uint32_t>(n * 4));
+    }
   }
-  __device__ static void apply_loaded(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
-                                      const float (&u)[32], float*) {
+  __device__ static void apply_buf(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
+                                   float* buf) {
     const int z = m0 + row;
     if (z >= p.H) return;
+    const int lane = threadIdx.x & 31;
     const long long base = (static_cast<long long>(g) * p.B + n0 + col0) * p.H + z;
 #pragma unroll
     for (int c = 0; c < 32; ++c)
-      if (n0 + col0 + c < p.B) p.F32[base + static_cast<long long>(c) * p.H] = u[c] * v[c];
+      if (n0 + col0 + c < p.B) p.F32[base + static_cast<long long>(c) * p.H] = buf[c * 32 + lane] * v[c];
   }
 };
 
@@ -947,10 +963,15 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     if ((st = encode_maps_hilo(&mb, operand_view(w.Uop, prec, sA, G), prec, kHcltBN)) != PC_OK) return st;
     EpiHcltFwd::Params ep{w.D + static_cast<long long>(sA) * B * H, H, B};
     // a_early: W's operand copy was written before the first product layer
-    if ((st = launch_gemm<P, kHcltBN, EpiHcltFwd>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi,
-                                                  mb.lo, num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD,
-                                                  2ll * G * H * H * B, true)) != PC_OK)
-      return st;
+    if constexpr (P == kBF16)
+      st = launch_gemm_persist<P, kHcltBN, EpiHcltFwdWhole>(cdiv(H, kBM), cdiv(B, kHcltBN), G, ma.hi, ma.lo, mb.hi,
+                                                            mb.lo, num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD,
+                                                            2ll * G * H * H * B);
+    else
+      st = launch_gemm<P, kHcltBN, EpiHcltFwd>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi, mb.lo,
+                                               num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD, 2ll * G * H * H * B,
+                                               true);
+    if (st != PC_OK) return st;
   }
   {
     ProfileScope ps(s, PC_KIND_HCLT_MEM, n * B * 8ll + B * 16ll);
@@ -981,7 +1002,8 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       // element flows of the level's children; 256-wide tiles (full-rate MMAs) where the
       // level has enough of them to fill the GPU
       if ((st = encode_maps(&ma, operand_view(w.WopT, prec, sA, G), prec, kBM)) != PC_OK) return st;
-      const bool wide = P == kBF16 && static_cast<long long>(cdiv(H, kBM)) * cdiv(B, 2 * kHcltBN) * G >= num_sms();
+      const bool wide = P == kBF16 && H % 4 == 0 &&
+                        static_cast<long long>(cdiv(H, kBM)) * cdiv(B, 2 * kHcltBN) * G >= num_sms();
       const int ebn = wide ? 2 * kHcltBN : kHcltBN;
       if ((st = encode_maps(&mb, operand_view(w.Gbm, prec, 0, G), prec, ebn)) != PC_OK) return st;
       HcltElemParams ee{w.U32 + static_cast<long long>(sA) * B * H, w.F32 + static_cast<long long>(sA) * B * H, H,
@@ -1012,11 +1034,17 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       EpiThetaScale::Params ep{dW, W, H, H, accumulate, d_var + sA};
       // short K (= B) and a theta block per tile: persistent (bf16, TF32), so the epilogue's
       // theta reads and dW writes overlap the next tile's K loop
-      if constexpr (P != kTF32x3)
-        st = launch_gemm_persist<P, kParamBN, EpiThetaScaleAhead>(cdiv(H, kBM), cdiv(H, kParamBN), G, ma.hi, ma.lo,
-                                                                  mb.hi, mb.lo, num_k_blocks(B, prec), ep, s,
-                                                                  PC_KIND_HCLT_PARAM, 2ll * G * H * H * B);
-      else
+      // (the theta blocks travel as 16-byte pieces: H % 4 == 0 and an aligned W)
+      bool persist = false;
+      if constexpr (P != kTF32x3) {
+        if (H % 4 == 0 && aligned16(W)) {
+          persist = true;
+          st = launch_gemm_persist<P, kParamBN, EpiThetaScaleAhead>(cdiv(H, kBM), cdiv(H, kParamBN), G, ma.hi, ma.lo,
+                                                                    mb.hi, mb.lo, num_k_blocks(B, prec), ep, s,
+                                                                    PC_KIND_HCLT_PARAM, 2ll * G * H * H * B);
+        }
+      }
+      if (!persist)
         st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), G), ma.hi, ma.lo, mb.hi,
                                                      mb.lo, num_k_blocks(B, prec), ep, s, PC_KIND_HCLT_PARAM,
                                                      2ll * G * H * H * B);
@@ -1035,7 +1063,7 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
         PC_CUDA(cudaFuncSetAttribute(k_hclt_dE_direct, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)));
       ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + (accumulate ? 2 : 1) * n * CH * 4);
-      k_hclt_dE_direct<<<dim3(cdiv(H, 32), n), 256, smem, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, dE,
+      k_hclt_dE_direct<<<dim3(n, cdiv(H, 32)), 256, smem, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, dE,
                                                                accumulate);
       PC_LAUNCH_CHECK();
       return PC_OK;

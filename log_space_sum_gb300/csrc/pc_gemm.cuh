@@ -56,11 +56,13 @@ template <class E>
 struct EpiBLo<E, std::void_t<decltype(E::kBLo)>> : std::bool_constant<E::kBLo> {};
 
 // Epi::kLoadAhead (optional, persistent tiles only): the epilogue's global operand of a
-// chunk (a theta block, a block of node values) is loaded into registers by
-// Epi::load(p, g, m0, n0, row, col0, t[32]) one chunk ahead, before the accumulator of that
-// chunk is waited for, and consumed by Epi::apply_loaded(p, g, m0, n0, row, col0, v, t,
-// tbuf): a warp keeps 32 loads per thread in flight through its stores, the TMEM loads and
-// the accumulator wait, which is what keeps a memory-bound epilogue near the HBM rate.
+// chunk (a 32 x 32 float block: theta, or node values) goes through a ring of
+// Epi::kAheadBufs 4 KB shared-memory buffers per epilogue warp. Epi::issue(p, g, m0, n0,
+// q, col0, buf) starts its asynchronous copy (cp.async, no registers held) kAheadBufs - 1
+// chunks ahead, across tile boundaries and before the accumulator of that chunk is
+// waited for; Epi::apply_buf(p, g, m0, n0, row, col0, v, buf) consumes it. A warp keeps
+// up to kAheadBufs - 1 blocks in flight through its stores, TMEM loads and waits: what a
+// memory-bound epilogue needs to run near the HBM rate.
 template <class E, class = void>
 struct EpiLoadAhead : std::false_type {};
 template <class E>
@@ -97,13 +99,15 @@ struct GemmShape {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: two epilogue warps split the 32-column chunks");
 };
 
-// Accumulation slices, in MMA k-steps (1 or 2, or a multiple of the k-steps of one ring
-// slot); see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
-// (Epi::kSliceBF16 k-steps; 0 = one accumulation over all of K).
-#ifndef PC_SLICE_K3X
-#define PC_SLICE_K3X 1
-#endif
-constexpr int kSliceK3x = PC_SLICE_K3X;
+// Accumulation slices, in MMA k-steps (1, or a multiple of the k-steps of one ring slot);
+// see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
+// (Epi::kSliceBF16 k-steps; 0 = one accumulation over all of K). 3xTF32 slices one k-step
+// at a time: with two k-steps per slice (half the slices, measured 11.25 against 14.56 ms
+// per HMM 4096 step) the second hi*hi product adds a truncation at the partial sum's own
+// magnitude, whose expected size depends on the data (the HCLT-768 LL error went to
+// 2.5e-5 with the one-step correction, to 1.9e-5 on uniform emissions with 1.5 times it):
+// no single correction keeps both inside the fp32 mode's 1e-5.
+constexpr int kSliceK3x = 1;
 constexpr int kSliceK1 = 8;  // the TF32 default (EpiSliceTF32)
 
 // The tensor core's float32 accumulator truncates toward zero. A slice of one 3xTF32
@@ -209,6 +213,11 @@ __device__ __forceinline__ void cp_async_16(uint8_t* dst, const void* src, uint3
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ void stage_tile_load_bf16_async(uint8_t* tile, int pitch, const __nv_bfloat16* src,
                                                            long long ld, int nrows, int ncols, int et) {
@@ -278,10 +287,8 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
                                  : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM columns");
   constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
-#ifndef PC_SLICE_CORR
-#define PC_SLICE_CORR (kSliceK == 1 ? 0x34800000u : 0x34C00000u)
-#endif
-  constexpr uint32_t kCorrBits = PC_SLICE_CORR;
+  static_assert(!kHalfUlp || kSliceK == 1, "the truncation correction is that of one-k-step slices");
+  constexpr uint32_t kCorrBits = 0x34800000u;  // 4 x 2^-24: four half ulps, every fourth slice
   // split K: the idle ring holds the exchange buffer (128 x BN/2 floats), then the
   // epilogue's staged tiles
   constexpr int kXchgBytes = kBM * (BN / 2) * 4;
@@ -704,13 +711,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         int num_kb, int tiles_m, int tiles_n, int groups, unsigned* status,
                         const typename Epi::Params ep) {
   static_assert(P == kBF16 || P == kTF32, "persistent tiles: bf16 or TF32");
-  static_assert(EpiWarps<Epi>::value == kEpiWarps && !EpiPrefetch<Epi>::value && !EpiBLo<Epi>::value,
-                "persistent tiles: default epilogue warps, no prefetched tile, no B lo part");
-  using S = GemmShape<P, BN, false>;
+  static_assert(EpiWarps<Epi>::value == kEpiWarps && !EpiPrefetch<Epi>::value,
+                "persistent tiles: default epilogue warps, no prefetched tile");
+  // B lo part (EpiBLo): A * B_lo accumulates beside A * B_hi, in the same TMEM buffer's
+  // upper BN columns, and the epilogue adds the two
+  constexpr bool kBLo = EpiBLo<Epi>::value;
+  using S = GemmShape<P, BN, kBLo>;
   constexpr int kStages = GemmPlan<P, BN, Epi>::kStages;
   constexpr int kSliceK = (P == kTF32 ? EpiSliceTF32<Epi>::value : Epi::kSliceBF16);
   static_assert(kSliceK == 0, "persistent tiles accumulate unsliced");
-  constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256 : 512;
+  constexpr uint32_t kAccCols = kBLo ? 2 * BN : BN;  // one accumulator buffer
+  static_assert(2 * kAccCols <= 512, "two accumulator buffers in TMEM");
+  constexpr uint32_t kTmemCols = 2 * kAccCols <= 256 ? 256 : 512;
   constexpr int kWPQ = kEpiWarps / 4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -733,7 +745,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     n0 = (r % tiles_n) * BN;
   };
   auto a_tile = [&](int s) { return smem + s * S::kStageBytes; };
-  auto b_tile = [&](int s) { return smem + s * S::kStageBytes + S::kABytes; };
+  auto b_tile = [&](int s, int part) { return smem + s * S::kStageBytes + S::kABytes + part * S::kBBytes; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -749,6 +761,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       fence_barrier_init();
       tma_prefetch_map(&tmA);
       tma_prefetch_map(&tmB);
+      if constexpr (kBLo) tma_prefetch_map(&tmB_lo);
     }
     __syncwarp();
     tmem_alloc(tmem_slot, kTmemCols);
@@ -776,7 +789,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           mbar_arrive_expect_tx(&full[s], S::kStageBytes);
           tma_load_3d(a_tile(s), &tmA, &full[s], kb * S::kBK, m0, g);
-          tma_load_3d(b_tile(s), &tmB, &full[s], kb * S::kBK, n0, g);
+          tma_load_3d(b_tile(s, 0), &tmB, &full[s], kb * S::kBK, n0, g);
+          if constexpr (kBLo) tma_load_3d(b_tile(s, 1), &tmB_lo, &full[s], kb * S::kBK, n0, g);
           issued = it + 1;
         }
       }
@@ -793,7 +807,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int a = local & 1;
         if (!mbar_wait(&acc_empty[a], ((local >> 1) & 1) ^ 1, status, kErrTimeoutMma, wl)) break;
         tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(a * BN);
+        const uint32_t d = tmem + static_cast<uint32_t>(a * kAccCols);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&full[s], (it / kStages) & 1, status, kErrTimeoutMma, wl)) {
@@ -801,15 +815,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_addr(a_tile(s)), b0 = smem_addr(b_tile(s));
+          const uint32_t a0 = smem_addr(a_tile(s)), b0 = smem_addr(b_tile(s, 0)), b1 = smem_addr(b_tile(s, 1));
 #pragma unroll
           for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
             const uint32_t off = kk * 32;
             const uint32_t acc = (kb == 0 && kk == 0) ? 0u : 1u;
-            if constexpr (P == kBF16)
+            if constexpr (P == kBF16) {
               umma_bf16(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
-            else
+              if constexpr (kBLo) umma_bf16(d + BN, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, acc);
+            } else {
               umma_tf32(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
+              if constexpr (kBLo) umma_tf32(d + BN, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, acc);
+            }
           }
           umma_commit(&empty[s]);
         }
@@ -826,46 +843,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;
     float* tbuf = Epi::kTranspose ? tbuf_base + ew * kTBufFloats : nullptr;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    // chunk c of accumulator buffer a (+ its B lo part)
+    auto load_acc = [&](int a, int c, float (&v)[32]) {
+      tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * kAccCols + c), v);
+      if constexpr (kBLo) {
+        float lo[32];
+        tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * kAccCols + BN + c), lo);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += lo[i];
+      }
+    };
     grid_dependency_wait();
     bool ok = true;
     int local = 0;
     if constexpr (EpiLoadAhead<Epi>::value) {
-      static_assert(Epi::kSmemBytes == 0, "load-ahead epilogues keep no per-tile shared memory");
-      float tn[32];  // the next chunk's operand
-      if (static_cast<int>(blockIdx.x) < num_tiles) {
-        int m0, n0, g;
-        tile_coords(blockIdx.x, m0, n0, g);
-        Epi::load(ep, g, m0, n0, row, part * 32, tn);
-      }
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-        int m0, n0, g;
-        tile_coords(t, m0, n0, g);
-        const int a = local & 1;
-        ok = epilogue_bar_and(ok && mbar_wait(&acc_full[a], (local >> 1) & 1, status, kErrTimeoutEpilogue, wl));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = part * 32; c < BN; c += 32 * kWPQ) {
-          float tc[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) tc[i] = tn[i];
-          const bool last = c + 32 * kWPQ >= BN;  // this warp's last chunk of the tile
-          const int tx = last ? t + static_cast<int>(gridDim.x) : t;
-          if (tx < num_tiles) {
-            int mx, nx, gx;
-            tile_coords(tx, mx, nx, gx);
-            Epi::load(ep, gx, mx, nx, row, last ? part * 32 : c + 32 * kWPQ, tn);
-          }
-          float v[32];
-          tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * BN + c), v);
-          if (last) {  // the buffer is free
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[a]);
-          }
-          Epi::apply_loaded(ep, g, m0, n0, row, c, v, tc, tbuf);
+      constexpr int kNB = Epi::kAheadBufs;
+      constexpr int kCPT = BN / (32 * kWPQ);  // chunks of one tile per warp
+      static_assert(kNB >= 2 && Epi::kSmemBytes >= kEpiWarps * kNB * 4096, "a ring of 4 KB blocks per warp");
+      float* ring = reinterpret_cast<float*>(epi_smem) + ew * kNB * 1024;
+      const int my_tiles =
+          static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+      const int items = my_tiles * kCPT;  // (tile, chunk) items of this warp, in order
+      auto item_tile = [&](int i) { return static_cast<int>(blockIdx.x) + (i / kCPT) * static_cast<int>(gridDim.x); };
+      auto item_col = [&](int i) { return part * 32 + (i % kCPT) * 32 * kWPQ; };
+      auto issue = [&](int i) {
+        if (i < items) {
+          int m0, n0, g;
+          tile_coords(item_tile(i), m0, n0, g);
+          Epi::issue(ep, g, m0, n0, q, item_col(i), ring + (i % kNB) * 1024);
         }
+        cp_async_commit();  // (an empty group past the end keeps the counting uniform)
+      };
+      for (int i = 0; i < kNB - 1; ++i) issue(i);
+      for (int i = 0; i < items; ++i) {
+        issue(i + kNB - 1);  // into the buffer item i - 1 left
+        int m0, n0, g;
+        tile_coords(item_tile(i), m0, n0, g);
+        const int local_i = i / kCPT, a = local_i & 1, c = item_col(i);
+        if (i % kCPT == 0) {
+          ok = epilogue_bar_and(ok && mbar_wait(&acc_full[a], (local_i >> 1) & 1, status, kErrTimeoutEpilogue, wl));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        cp_async_wait_group<kNB - 1>();  // item i's block has landed (this thread's share)
+        __syncwarp();                    // ... and every lane's
+        float v[32];
+        load_acc(a, c, v);
+        if (i % kCPT == kCPT - 1) {  // this warp's last chunk of the tile: the buffer is free
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+        Epi::apply_buf(ep, g, m0, n0, row, c, v, ring + (i % kNB) * 1024);
+        __syncwarp();  // every lane is done with the block before it is refilled
       }
+      cp_async_wait_all();  // no copy may land after the CTA has left
     } else {
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
         int m0, n0, g;
@@ -879,7 +911,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll 1
         for (int c = part * 32; c < BN; c += 32 * kWPQ) {
           float v[32];
-          tmem_ld_32x32(lane_base + static_cast<uint32_t>(a * BN + c), v);
+          load_acc(a, c, v);
           if (c + 32 * kWPQ >= BN) {  // this warp's last chunk of the tile: the buffer is free
             tc_fence_before();
             __syncwarp();

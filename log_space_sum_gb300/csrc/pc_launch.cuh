@@ -473,42 +473,71 @@ struct EpiThetaScaleDirect : EpiThetaScale {
   static constexpr bool kPrefetchTile = false;
 };
 
-// EpiThetaScale on persistent tiles: the theta rows of a chunk are loaded one chunk ahead
-// (kLoadAhead; streaming loads, read once), and the flows are written with streaming
-// stores, or added by one reduction per element when accumulating (each element of F
-// has one writer per call).
-struct EpiThetaScaleAhead : EpiThetaScaleDirect {
+// EpiThetaScale on persistent tiles (kLoadAhead): the theta block of a chunk (32 rows x
+// 32 columns) comes through the warp's ring of shared-memory buffers, its 16-byte pieces
+// swizzled by the row; the product theta * D is formed one row per lane, written back in
+// place and read out one column per lane, so that each global store of the warp is one
+// contiguous 128-byte row segment (the buffer doubles as the transpose). Flows are written
+// with streaming stores, or added by one reduction per element when accumulating (each
+// element of F has one writer per call). Needs N % 4 == 0 and a 16-byte aligned theta.
+struct EpiThetaScaleAhead : EpiThetaScale {
+  static constexpr bool kTranspose = false;
+  static constexpr bool kPrefetchTile = false;
   static constexpr bool kLoadAhead = true;
-  __device__ static void load(const Params& p, int g, int m0, int n0, int row, int col0, float (&t)[32]) {
+  // two blocks (one in flight while the other is consumed): deeper rings cost the
+  // contraction a ring stage, and measured slower (HCLT 768: 10.16 ms per step with two,
+  // 10.49 with three, 10.54 with four)
+  static constexpr int kAheadBufs = 2;
+  static constexpr int kSmemBytes = kEpiWarps * kAheadBufs * 4096;
+  __device__ static int piece(int r, int p) { return r * 32 + ((p ^ (r & 7)) << 2); }
+  __device__ static void issue(const Params& p, int g, int m0, int n0, int q, int col0, float* buf) {
     const int lane = threadIdx.x & 31;
-    const int i0 = m0 + row - lane;
-    const int j = n0 + col0 + lane;
-    const long long ld = p.N;
     const long long gm = p.gmap ? p.gmap[g] : g;
-    const float* tp = p.theta + (gm * p.M + i0) * ld + j;
+    const int pc = lane & 7;
+    const int j = n0 + col0 + 4 * pc;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) t[r] = (j < p.N && i0 + r < p.M) ? __ldcs(tp + r * ld) : 0.f;
+    for (int k = 0; k < 8; ++k) {
+      const int r = 4 * k + (lane >> 3);
+      const int i = m0 + q * 32 + r;
+      const int n = (i < p.M && j < p.N) ? min(4, p.N - j) : 0;
+      const float* src = n ? p.theta + (gm * p.M + i) * static_cast<long long>(p.N) + j : p.theta;
+      cp_async_16(reinterpret_cast<uint8_t*>(buf + piece(r, pc)), src, static_cast<uint32_t>(n * 4));
+    }
   }
-  __device__ static void apply_loaded(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
-                                      const float (&t)[32], float* tbuf) {
-    float w[32];
-    warp_transpose32(v, w, tbuf);
+  __device__ static void apply_buf(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
+                                   float* buf) {
     const int lane = threadIdx.x & 31;
+    const int i = m0 + row;
+    if (p.rscale || p.cscale) {
+      const float rs = (p.rscale && i < p.M) ? p.rscale[i] : 1.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int j = n0 + col0 + c;
+        v[c] *= rs * ((p.cscale && j < p.N) ? p.cscale[j] : 1.f);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // row lane: theta * D, in place
+      float4* t = reinterpret_cast<float4*>(buf + piece(lane, k));
+      const float4 x = *t;
+      *t = make_float4(x.x * v[4 * k], x.y * v[4 * k + 1], x.z * v[4 * k + 2], x.w * v[4 * k + 3]);
+    }
+    __syncwarp();
     const int i0 = m0 + row - lane;
     const int j = n0 + col0 + lane;
     if (j >= p.N) return;
-    const long long ld = p.N;
     const long long gm = p.gmap ? p.gmap[g] : g;
+    const long long ld = p.N;
     float* Fp = p.F + (gm * p.M + i0) * ld + j;
-    if (p.rscale || p.cscale) scale_rows(p.rscale, p.cscale, i0, j, p.M, w);
+    const int pl = lane >> 2, wl = lane & 3;
     if (p.accumulate) {
 #pragma unroll
       for (int r = 0; r < 32; ++r)
-        if (i0 + r < p.M) atomicAdd(Fp + r * ld, t[r] * w[r]);
+        if (i0 + r < p.M) atomicAdd(Fp + r * ld, buf[piece(r, pl) + wl]);
     } else {
 #pragma unroll
       for (int r = 0; r < 32; ++r)
-        if (i0 + r < p.M) __stcs(Fp + r * ld, t[r] * w[r]);
+        if (i0 + r < p.M) __stcs(Fp + r * ld, buf[piece(r, pl) + wl]);
     }
   }
 };
