@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(256) k_hclt_product(
   const float mmax = live ? __uint_as_float(mbits) : 1.f;
   const float rinv = 1.f / mmax;
   const long long row = static_cast<long long>(s) * B + b;
-  float* u32 = U32 + row * H;
+  float* u32 = U32 ? U32 + row * H : nullptr;  // NULL: the bf16 operand parts carry u
   float dot = 0.f;
   for (int q = threadIdx.x; q < H4; q += blockDim.x) {
     const float4 m = mant4[q];
@@ -191,12 +191,12 @@ __global__ void __launch_bounds__(256) k_hclt_product(
     }
     const int z = 4 * q;
     if constexpr (kVec) {
-      reinterpret_cast<float4*>(u32)[q] = u;
+      if (u32) reinterpret_cast<float4*>(u32)[q] = u;
       if (uop) store_child4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
     } else {
       const float uu[4] = {u.x, u.y, u.z, u.w};
       for (int k = 0; k < 4 && z + k < H; ++k) {
-        u32[z + k] = uu[k];
+        if (u32) u32[z + k] = uu[k];
         if (uop) store_child<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
       }
     }
@@ -225,26 +225,12 @@ __global__ void __launch_bounds__(256) k_hclt_product(
 // reduction, and a lane's loads of one child row are independent, so they are all in
 // flight together. Warp w of the launch takes node s0 + w / B, sample w % B.
 constexpr int kWarpRuns = 8;  // runs of four latents per lane: H <= 4 * 32 * 8
-template <int P, bool kVec>
-__global__ void __launch_bounds__(256) k_hclt_product_warp(
-    int s0, int G, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
-    const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr, const int* __restrict__ child_slots,
-    const float* __restrict__ Et, const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
-    long long uop_ld, size_t uop_lo, int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi,
-    float* __restrict__ rdot) {
-  constexpr long long kNone = -0x7fffffffffffffffLL - 1;
-  const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (wid >= static_cast<long long>(G) * B) return;  // the whole warp leaves together
-  const int lane = threadIdx.x & 31;
-  const int s = s0 + static_cast<int>(wid / B);
-  const int b = static_cast<int>(wid % B);
-  const int v = var_of_slot[s];
-  const int x = data[static_cast<long long>(b) * nvars + v];
-  const bool xin = x >= 0 && x < C;
-  const int c0 = child_ptr[s], c1 = child_ptr[s + 1];
-  const float* er = Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H;
-  float m[kWarpRuns][4];
-  int e[kWarpRuns][4];
+
+// Running products of one (node, sample) row, m 2^e per latent (lane's runs q = lane +
+// 32 r): the emission row, then every child's D row from child c_from on.
+template <bool kVec>
+__device__ __forceinline__ void product_start(const float* er, bool xin, int H, int lane,
+                                              float (&m)[kWarpRuns][4], int (&e)[kWarpRuns][4]) {
 #pragma unroll
   for (int r = 0; r < kWarpRuns; ++r) {
     const int q = lane + 32 * r;
@@ -259,22 +245,35 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
       m[r][k] = renorm(m[r][k], e[r][k]);
     }
   }
-  for (int c = c0; c < c1; ++c) {
-    const float* drow = D + (static_cast<long long>(child_slots[c]) * B + b) * H;
-    float4 d[kWarpRuns];
+}
+template <bool kVec>
+__device__ __forceinline__ void product_child(const float* drow, int H, int lane, float (&m)[kWarpRuns][4],
+                                              int (&e)[kWarpRuns][4]) {
+  float4 d[kWarpRuns];
 #pragma unroll
-    for (int r = 0; r < kWarpRuns; ++r) {
-      const int q = lane + 32 * r;
-      d[r] = 4 * q < H ? load_run4<kVec>(drow, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int r = 0; r < kWarpRuns; ++r) {
-      m[r][0] = renorm(m[r][0] * d[r].x, e[r][0]);
-      m[r][1] = renorm(m[r][1] * d[r].y, e[r][1]);
-      m[r][2] = renorm(m[r][2] * d[r].z, e[r][2]);
-      m[r][3] = renorm(m[r][3] * d[r].w, e[r][3]);
-    }
+  for (int r = 0; r < kWarpRuns; ++r) {
+    const int q = lane + 32 * r;
+    d[r] = 4 * q < H ? load_run4<kVec>(drow, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+#pragma unroll
+  for (int r = 0; r < kWarpRuns; ++r) {
+    m[r][0] = renorm(m[r][0] * d[r].x, e[r][0]);
+    m[r][1] = renorm(m[r][1] * d[r].y, e[r][1]);
+    m[r][2] = renorm(m[r][2] * d[r].z, e[r][2]);
+    m[r][3] = renorm(m[r][3] * d[r].w, e[r][3]);
+  }
+}
+
+// The row's maximum (a warp reduction on (exponent, mantissa) keys), u = m / m_max
+// 2^(e - e_max) into U32 (if kept) and the children operand, the offsets Ex / Lm, and at
+// the root the dot product with pi.
+template <int P, bool kVec>
+__device__ __forceinline__ void product_finish(float (&m)[kWarpRuns][4], int (&e)[kWarpRuns][4], int s, int b,
+                                               int lane, int root_slot, int H, int B, float* __restrict__ U32,
+                                               void* uop, long long uop_ld, size_t uop_lo, int* __restrict__ Ex,
+                                               float* __restrict__ Lm, const float* __restrict__ pi,
+                                               float* __restrict__ rdot) {
+  constexpr long long kNone = -0x7fffffffffffffffLL - 1;
   long long best = kNone;
 #pragma unroll
   for (int r = 0; r < kWarpRuns; ++r)
@@ -288,7 +287,7 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
   const float mmax = live ? __uint_as_float(mbits) : 1.f;
   const float rinv = 1.f / mmax;
   const long long row = static_cast<long long>(s) * B + b;
-  float* u32 = U32 + row * H;
+  float* u32 = U32 ? U32 + row * H : nullptr;  // NULL: the bf16 operand parts carry u
   float dot = 0.f;
 #pragma unroll
   for (int r = 0; r < kWarpRuns; ++r) {
@@ -301,11 +300,11 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
       uu[k] = (live && m[r][k] > 0.f) ? (m[r][k] * rinv) * pow2_nonpos(e[r][k] - emax) : 0.f;
     const float4 u = make_float4(uu[0], uu[1], uu[2], uu[3]);
     if constexpr (kVec) {
-      reinterpret_cast<float4*>(u32)[q] = u;
+      if (u32) reinterpret_cast<float4*>(u32)[q] = u;
       if (uop) store_child4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
     } else {
       for (int k = 0; k < 4 && z + k < H; ++k) {
-        u32[z + k] = uu[k];
+        if (u32) u32[z + k] = uu[k];
         if (uop) store_child<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
       }
     }
@@ -321,6 +320,30 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
   if (s != root_slot) return;
   for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
   if (lane == 0) rdot[b] = dot;
+}
+
+template <int P, bool kVec>
+__global__ void __launch_bounds__(256) k_hclt_product_warp(
+    int s0, int G, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
+    const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr, const int* __restrict__ child_slots,
+    const float* __restrict__ Et, const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
+    long long uop_ld, size_t uop_lo, int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi,
+    float* __restrict__ rdot) {
+  const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (wid >= static_cast<long long>(G) * B) return;  // the whole warp leaves together
+  const int lane = threadIdx.x & 31;
+  const int s = s0 + static_cast<int>(wid / B);
+  const int b = static_cast<int>(wid % B);
+  const int v = var_of_slot[s];
+  const int x = data[static_cast<long long>(b) * nvars + v];
+  const bool xin = x >= 0 && x < C;
+  const int c0 = child_ptr[s], c1 = child_ptr[s + 1];
+  float m[kWarpRuns][4];
+  int e[kWarpRuns][4];
+  product_start<kVec>(Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H, xin, H, lane, m, e);
+  for (int c = c0; c < c1; ++c)
+    product_child<kVec>(D + (static_cast<long long>(child_slots[c]) * B + b) * H, H, lane, m, e);
+  product_finish<P, kVec>(m, e, s, b, lane, root_slot, H, B, U32, uop, uop_ld, uop_lo, Ex, Lm, pi, rdot);
 }
 
 // The log-likelihood. Every node lies under the root, so the root's offset is the sum over
@@ -478,6 +501,57 @@ __global__ void k_hclt_cat_bucket(int nvars, int B, int C, const int* __restrict
   }
 }
 
+// dEt[v][k][z] = sum over the samples of node s with category k of f[s][b][z], one warp
+// per (node, category): every sample's row of f is read whole (4-byte runs of four
+// latents per lane, all of the warp's loads of a row in flight together) and the category's
+// row of dEt written whole, so both sides stream contiguous kilobytes; the transpose to
+// dE's [H][C] rows follows. Samples in bucket order (deterministic sums). H % 4 == 0.
+constexpr int kDERowWarps = 8;
+constexpr int kDERowRuns = 8;  // runs of four latents per lane and pass: 1024 latents
+__global__ void __launch_bounds__(kDERowWarps * 32) k_hclt_dE_rows(int n, int H, int B, int C,
+                                                                  const int* __restrict__ var_of_slot,
+                                                                  const int* __restrict__ order,
+                                                                  const int* __restrict__ off,
+                                                                  const float* __restrict__ F32,
+                                                                  float* __restrict__ dEt) {
+  const long long wid = static_cast<long long>(blockIdx.x) * kDERowWarps + (threadIdx.x >> 5);
+  if (wid >= static_cast<long long>(n) * C) return;
+  const int lane = threadIdx.x & 31;
+  const int s = static_cast<int>(wid / C), k = static_cast<int>(wid % C);
+  const int v = var_of_slot[s];
+  const long long ob = static_cast<long long>(s) * (C + 1);
+  const int e0 = off[ob + k], e1 = off[ob + k + 1];
+  const int* ord = order + static_cast<long long>(s) * B;
+  const int H4 = H / 4;
+  float4* dst = reinterpret_cast<float4*>(dEt + (static_cast<long long>(v) * C + k) * H);
+  for (int q0 = 0; q0 < H4; q0 += 32 * kDERowRuns) {
+    float4 acc[kDERowRuns];
+#pragma unroll
+    for (int r = 0; r < kDERowRuns; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = e0; e < e1; ++e) {
+      const float4* row = reinterpret_cast<const float4*>(F32 + (static_cast<long long>(s) * B + ord[e]) * H);
+      float4 x[kDERowRuns];
+#pragma unroll
+      for (int r = 0; r < kDERowRuns; ++r) {
+        const int q = q0 + lane + 32 * r;
+        x[r] = q < H4 ? row[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int r = 0; r < kDERowRuns; ++r) {
+        acc[r].x += x[r].x;
+        acc[r].y += x[r].y;
+        acc[r].z += x[r].z;
+        acc[r].w += x[r].w;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kDERowRuns; ++r) {
+      const int q = q0 + lane + 32 * r;
+      if (q < H4) dst[q] = acc[r];
+    }
+  }
+}
+
 // dEt[v][k][z] = sum over the samples of node s with category k of f[s][b][z].
 __global__ void k_hclt_dE_gather(int H, int B, int C, const int* __restrict__ var_of_slot,
                                  const int* __restrict__ order, const int* __restrict__ off,
@@ -495,64 +569,6 @@ __global__ void k_hclt_dE_gather(int H, int B, int C, const int* __restrict__ va
   }
 }
 
-// dE[v][z][k] (+)= sum over the samples of node s with category k of f[s][b][z], written
-// directly in the caller's [nvars][H][C] layout: one block per (node, 32 latents), one
-// latent per lane. Warp w owns the categories [w C / 8, (w + 1) C / 8) and walks their
-// samples in bucket order (stable, so the sums are deterministic), 32 at a time: their
-// indices in one load, their 32 rows of f (128 bytes each) all in flight together, then a
-// running sum per category into a padded [32][C + 1] shared tile that the block writes out
-// as rows of C categories. For C <= kDEDirectMaxC.
-constexpr int kDEDirectMaxC = 1024;
-__global__ void __launch_bounds__(256) k_hclt_dE_direct(int H, int B, int C, const int* __restrict__ var_of_slot,
-                                                        const int* __restrict__ order, const int* __restrict__ off,
-                                                        const float* __restrict__ F32, float* __restrict__ dE,
-                                                        int accumulate) {
-  extern __shared__ float acc[];  // [32][C + 1], then C + 1 bucket offsets
-  int* offs = reinterpret_cast<int*>(acc + 32 * (C + 1));
-  const int s = blockIdx.x, z0 = blockIdx.y * 32;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int v = var_of_slot[s];
-  const int* ord = order + static_cast<long long>(s) * B;
-  for (int i = threadIdx.x; i <= C; i += blockDim.x) offs[i] = off[static_cast<long long>(s) * (C + 1) + i];
-  for (int i = 4 * threadIdx.x; i < 32 * (C + 1); i += 4 * blockDim.x)  // 32 (C + 1) is a multiple of 4
-    *reinterpret_cast<float4*>(acc + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-  __syncthreads();
-  const float* fs = F32 + static_cast<long long>(s) * B * H + z0 + lane;
-  const bool zin = z0 + lane < H;
-  float* arow = acc + lane * (C + 1);
-  const int kb = w * C / 8, ke = (w + 1) * C / 8;
-  int k = kb, knext = offs[k + 1];
-  float run = 0.f;
-  for (int e0 = offs[kb]; e0 < offs[ke]; e0 += 32) {
-    const int n = min(32, offs[ke] - e0);
-    const int my = lane < n ? ord[e0 + lane] : 0;
-    float x[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int b = __shfl_sync(0xffffffffu, my, j);
-      x[j] = (j < n && zin) ? fs[static_cast<long long>(b) * H] : 0.f;
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < n) {
-        while (e0 + j >= knext) {  // the previous category is complete
-          arow[k] = run;
-          run = 0.f;
-          knext = offs[++k + 1];
-        }
-        run += x[j];
-      }
-    }
-  }
-  if (k < ke) arow[k] = run;  // the last non-empty category (later ones stay 0)
-  __syncthreads();
-  const int zmax = min(32, H - z0);
-  for (int zz = 0; zz < zmax; ++zz) {  // row by row: no division per element
-    float* drow = dE + (static_cast<long long>(v) * H + z0 + zz) * C;
-    const float* arow_z = acc + zz * (C + 1);
-    for (int kk = threadIdx.x; kk < C; kk += blockDim.x) drow[kk] = accumulate ? drow[kk] + arow_z[kk] : arow_z[kk];
-  }
-}
 
 // Copies a 128 x 128 block rows[n0 + c][m0 + r] of a row-major [B][H] array into
 // shared memory as S[c][r] (0 outside), so an epilogue thread owning row r reads its 32
@@ -582,12 +598,42 @@ __device__ __forceinline__ void stage_block(const float* __restrict__ src, int H
   }
 }
 
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+
+// stage_block of u given as the children operand's bf16 hi and lo parts (rows ld apart,
+// the lo part lo elements after the hi part): S[c][r] = hi + lo.
+__device__ __forceinline__ void stage_block_hilo(const uint16_t* __restrict__ src, long long ld, size_t lo, int H,
+                                                 int B, int m0, int n0, float* S, int et) {
+  constexpr int kCols = kBM / kEpiWarps;
+  const int lane = et & 31;
+  const int c_begin = (et >> 5) * kCols;
+#pragma unroll 1
+  for (int cb = c_begin; cb < c_begin + kCols; cb += 8) {
+    float vals[8][4];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const bool bin = n0 + cb + c < B;
+      const uint16_t* row = src + static_cast<long long>(n0 + cb + c) * ld + m0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        vals[c][i] = (bin && m0 + r < H) ? bf16_bits_to_float(row[r]) + bf16_bits_to_float(row[r + lo]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) S[(cb + c) * kBM + lane + 32 * i] = vals[c][i];
+  }
+}
+
 // Forward epilogue: D[g][b][z], the edge's sum layer kept linear; thread = parent latent z.
+// The bf16 forward runs on persistent tiles with one accumulation over K (= H) per tile:
+// the accumulator's truncation costs an edge at most H / 16 half ulps of D (K = 1024:
+// < 4e-6 of D, far inside the bf16 mode's rounding), and one tile's stores run under the
+// next tile's MMAs. (The TF32 mode slices K, EpiSliceTF32.)
 struct EpiHcltFwd : EpiNoHooks {
-  // Every edge's D feeds the log-likelihood, and a tree chains hundreds of them: the bf16
-  // mode accumulates K in slices of 16 k-steps so that the accumulator's truncation acts
-  // on partial sums a fraction of D's size.
-  static constexpr int kSliceBF16 = 16;
+  static constexpr int kSliceBF16 = 0;
   // With uniform emissions every latent of a node is within a rounding step of the node's
   // maximum, where one bf16 / TF32 rounding would take them all to exactly 1 and each
   // edge would gain its largest row sum error instead of an average: the children
@@ -608,22 +654,19 @@ struct EpiHcltFwd : EpiNoHooks {
   }
 };
 
-// The bf16 forward on persistent tiles: one accumulation over K (= H) per tile, hi and lo
-// parts of the children operand side by side. Unsliced, the accumulator's truncation
-// costs each edge at most about H / 16 half-ulps of D (K = 1024: ~2e-6 of D, far inside
-// the bf16 mode's rounding); in exchange one tile's stores run under the next tile's MMAs.
-struct EpiHcltFwdWhole : EpiHcltFwd {
-  static constexpr int kSliceBF16 = 0;
-};
-
 // Element-flow epilogue: f[g][b][z'] = u[g][b][z'] * D[z', b]; thread = child latent z'.
 // For 128-wide tiles the u block is staged in shared memory during the K loop (not in
 // 3xTF32, whose ring needs the room); 256-wide tiles read it directly (a 128 KB block
 // would leave the ring two slots).
 struct HcltElemParams {
-  const float* U32;  // at the level's first slot, [G][B][H]
+  const float* U32;  // at the level's first slot, [G][B][H] (TF32 modes)
   float* F32;        // idem
   int H, B;
+  // bf16 mode: u as the children operand's hi and lo parts (the forward's B operand; no
+  // float32 copy of u is kept below the root): [G][B][ld] at the level's first slot
+  const uint16_t* Uh;
+  long long uld;
+  size_t ulo;
 };
 template <int P, int BN = kHcltBN>
 struct EpiHcltElem : EpiNoHooks {
@@ -634,7 +677,10 @@ struct EpiHcltElem : EpiNoHooks {
   static constexpr int kSmemBytes = kStage ? kHcltBN * kBM * 4 : (kLoadAhead ? kEpiWarps * kAheadBufs * 4096 : 0);
 
   __device__ static void prepare(const Params& p, int g, int m0, int n0, int et, uint8_t* smem) {
-    if constexpr (kStage)
+    if constexpr (kStage && P == kBF16)
+      stage_block_hilo(p.Uh + static_cast<long long>(g) * p.B * p.uld, p.uld, p.ulo, p.H, p.B, m0, n0,
+                       reinterpret_cast<float*>(smem), et);
+    else if constexpr (kStage)
       stage_block(p.U32 + static_cast<long long>(g) * p.B * p.H, p.H, p.B, m0, n0, reinterpret_cast<float*>(smem),
                   et);
   }
@@ -647,29 +693,37 @@ struct EpiHcltElem : EpiNoHooks {
     float u[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      if constexpr (kStage)
+      if constexpr (kStage) {
         u[c] = reinterpret_cast<const float*>(smem)[(col0 + c) * kBM + row];
-      else
+      } else if constexpr (P == kBF16) {
+        const long long i = (static_cast<long long>(g) * p.B + n0 + col0 + c) * p.uld + z;
+        u[c] = n0 + col0 + c < p.B ? bf16_bits_to_float(p.Uh[i]) + bf16_bits_to_float(p.Uh[i + p.ulo]) : 0.f;
+      } else {
         u[c] = n0 + col0 + c < p.B ? p.U32[base + static_cast<long long>(c) * p.H] : 0.f;
+      }
     }
 #pragma unroll
     for (int c = 0; c < 32; ++c)
       if (n0 + col0 + c < p.B) p.F32[base + static_cast<long long>(c) * p.H] = u[c] * v[c];
   }
 
-  // persistent tiles (kLoadAhead): the chunk's node values u[b][z] (32 samples x 32
-  // latents) come through the warp's ring of shared-memory buffers; lane = latent z reads
-  // them conflict-free. Needs H % 4 == 0 (16-byte rows).
+  // persistent tiles (kLoadAhead, bf16): the chunk's node values u[b][z] (32 samples x 32
+  // latents, as 128-byte rows of 32 hi then 32 lo parts) come through the warp's ring of
+  // shared-memory buffers; lane = latent z reads them conflict-free. Needs H % 8 == 0
+  // (16-byte pieces of bf16 rows).
   __device__ static void issue(const Params& p, int g, int m0, int n0, int q, int col0, float* buf) {
+    static_assert(P == kBF16, "the persistent element-flow tiles are bf16");
     const int lane = threadIdx.x & 31;
-    const int z = m0 + q * 32 + 4 * (lane & 7);
+    const int pc = lane & 7;  // pieces 0-3: hi, 4-7: lo
+    const int z = m0 + q * 32 + 8 * (pc & 3);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int c = 4 * k + (lane >> 3);
       const int b = n0 + col0 + c;
-      const int n = (b < p.B && z < p.H) ? min(4, p.H - z) : 0;
-      const float* src = n ? p.U32 + (static_cast<long long>(g) * p.B + b) * p.H + z : p.U32;
-      cp_async_16(reinterpret_cast<uint8_t*>(buf + c * 32 + 4 * (lane & 7)), src, static_cast<uint32_t>(n * 4));
+      const int n = (b < p.B && z < p.H) ? min(8, p.H - z) : 0;
+      const uint16_t* src =
+          n ? p.Uh + (pc >= 4 ? p.ulo : 0) + (static_cast<long long>(g) * p.B + b) * p.uld + z : p.Uh;
+      cp_async_16(reinterpret_cast<uint8_t*>(buf) + c * 128 + pc * 16, src, static_cast<uint32_t>(n * 2));
     }
   }
   __device__ static void apply_buf(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
@@ -677,10 +731,13 @@ struct EpiHcltElem : EpiNoHooks {
     const int z = m0 + row;
     if (z >= p.H) return;
     const int lane = threadIdx.x & 31;
+    const uint16_t* hb = reinterpret_cast<const uint16_t*>(buf);
     const long long base = (static_cast<long long>(g) * p.B + n0 + col0) * p.H + z;
 #pragma unroll
     for (int c = 0; c < 32; ++c)
-      if (n0 + col0 + c < p.B) p.F32[base + static_cast<long long>(c) * p.H] = buf[c * 32 + lane] * v[c];
+      if (n0 + col0 + c < p.B)
+        p.F32[base + static_cast<long long>(c) * p.H] =
+            (bf16_bits_to_float(hb[c * 64 + lane]) + bf16_bits_to_float(hb[c * 64 + 32 + lane])) * v[c];
   }
 };
 
@@ -821,7 +878,7 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
     w->Gnm = c.operand(p, E1, H, B);
     w->Unm = c.operand(p, E1, H, B);
     if (want_dE) {
-      if (C > kDEDirectMaxC) w->dEt = static_cast<float*>(c.take(size_t(n) * C * H * 4));
+      w->dEt = static_cast<float*>(c.take(size_t(n) * C * H * 4));
       w->cat_order = static_cast<int*>(c.take(size_t(n) * B * 4));
       w->cat_off = static_cast<int*>(c.take(size_t(n) * (C + 1) * 4));
     }
@@ -945,16 +1002,19 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     if (G <= 0) continue;
     const bool edges = L < pl.maxh;
     const long long kids = pl.child_ptr[sB] - pl.child_ptr[sA];
+    // bf16: below the root u lives only in the children operand's hi and lo parts
+    float* u32_out = (P == kBF16 && edges) ? nullptr : w.U32;
     ProfileScope ps(s, PC_KIND_HCLT_MEM,
-                    G * B * 4ll + G * BH * 8 + kids * BH * 4 + (edges ? G * BH * eb2 : H * 4ll + B * 4ll));
+                    G * B * 4ll + G * BH * 4 + (u32_out ? G * BH * 4 : 0) + kids * BH * 4 +
+                        (edges ? G * BH * eb2 : H * 4ll + B * 4ll));
     if (H <= 4 * 32 * kWarpRuns) {
       const unsigned blocks = static_cast<unsigned>(cdiv(static_cast<long long>(G) * B, 8));
       (prod_vec ? k_hclt_product_warp<P, true> : k_hclt_product_warp<P, false>)<<<blocks, 256, 0, s>>>(
-          sA, G, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, w.U32, edges ? w.Uop.ptr : nullptr,
+          sA, G, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, u32_out, edges ? w.Uop.ptr : nullptr,
           w.Uop.ld, w.Uop.lo_elems, w.Ex, w.Lm, pi, w.rdot);
     } else {
       (prod_vec ? k_hclt_product<P, true> : k_hclt_product<P, false>)<<<dim3(G, B), 256, prod_smem, s>>>(
-          sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, w.U32, edges ? w.Uop.ptr : nullptr,
+          sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, u32_out, edges ? w.Uop.ptr : nullptr,
           w.Uop.ld, w.Uop.lo_elems, w.Ex, w.Lm, pi, w.rdot);
     }
     PC_LAUNCH_CHECK();
@@ -964,9 +1024,9 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     EpiHcltFwd::Params ep{w.D + static_cast<long long>(sA) * B * H, H, B};
     // a_early: W's operand copy was written before the first product layer
     if constexpr (P == kBF16)
-      st = launch_gemm_persist<P, kHcltBN, EpiHcltFwdWhole>(cdiv(H, kBM), cdiv(B, kHcltBN), G, ma.hi, ma.lo, mb.hi,
-                                                            mb.lo, num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD,
-                                                            2ll * G * H * H * B);
+      st = launch_gemm_persist<P, kHcltBN, EpiHcltFwd>(cdiv(H, kBM), cdiv(B, kHcltBN), G, ma.hi, ma.lo, mb.hi, mb.lo,
+                                                       num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD,
+                                                       2ll * G * H * H * B);
     else
       st = launch_gemm<P, kHcltBN, EpiHcltFwd>(dim3(cdiv(H, kBM), cdiv(B, kHcltBN), G), ma.hi, ma.lo, mb.hi, mb.lo,
                                                num_k_blocks(H, prec), ep, s, PC_KIND_HCLT_FWD, 2ll * G * H * H * B,
@@ -1002,12 +1062,13 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       // element flows of the level's children; 256-wide tiles (full-rate MMAs) where the
       // level has enough of them to fill the GPU
       if ((st = encode_maps(&ma, operand_view(w.WopT, prec, sA, G), prec, kBM)) != PC_OK) return st;
-      const bool wide = P == kBF16 && H % 4 == 0 &&
+      const bool wide = P == kBF16 && H % 8 == 0 &&
                         static_cast<long long>(cdiv(H, kBM)) * cdiv(B, 2 * kHcltBN) * G >= num_sms();
       const int ebn = wide ? 2 * kHcltBN : kHcltBN;
       if ((st = encode_maps(&mb, operand_view(w.Gbm, prec, 0, G), prec, ebn)) != PC_OK) return st;
       HcltElemParams ee{w.U32 + static_cast<long long>(sA) * B * H, w.F32 + static_cast<long long>(sA) * B * H, H,
-                        B};
+                        B, static_cast<const uint16_t*>(w.Uop.ptr) + static_cast<long long>(sA) * B * w.Uop.ld,
+                        w.Uop.ld, w.Uop.lo_elems};
       // a_early: Wᵀ's operand copy was written before the first scaled-flow kernel. Levels with
       // more tiles than SMs run persistent (bf16: one tile's epilogue under the next's K loop).
       if constexpr (P == kBF16) {
@@ -1023,7 +1084,13 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       if (st != PC_OK) return st;
       if (!dW) continue;
       // parameter flows of the level's edges
-      {
+      if constexpr (P == kBF16) {  // u's bf16 operand is its hi part
+        ProfileScope ps(s, PC_KIND_HCLT_MEM, G * BH * 4);
+        if ((st = transpose_bf16_to_operand(
+                 static_cast<const uint16_t*>(w.Uop.ptr) + static_cast<long long>(sA) * B * w.Uop.ld, w.Uop.ld,
+                 static_cast<long long>(B) * w.Uop.ld, G, B, H, w.Unm, s)) != PC_OK)
+          return st;
+      } else {
         ProfileScope ps(s, PC_KIND_HCLT_MEM, G * BH * (4 + eb));
         if ((st = transpose_to_operand<P>(w.U32 + static_cast<long long>(sA) * B * H, H,
                                           static_cast<long long>(B) * H, G, B, H, w.Unm, s)) != PC_OK)
@@ -1057,16 +1124,16 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       k_hclt_cat_bucket<<<n, 32, size_t(C + 1) * 4, s>>>(n, B, C, data, d_var, w.cat_order, w.cat_off);
       PC_LAUNCH_CHECK();
     }
-    if (C <= kDEDirectMaxC) {
-      const size_t smem = size_t(33) * (C + 1) * 4;  // the tile and the bucket offsets
-      if (smem > 48 * 1024)
-        PC_CUDA(cudaFuncSetAttribute(k_hclt_dE_direct, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)));
-      ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + (accumulate ? 2 : 1) * n * CH * 4);
-      k_hclt_dE_direct<<<dim3(n, cdiv(H, 32)), 256, smem, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, dE,
-                                                               accumulate);
-      PC_LAUNCH_CHECK();
-      return PC_OK;
+    if (H % 4 == 0) {
+      // whole rows in, whole rows out, then the transpose
+      {
+        ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + n * CH * 4);
+        k_hclt_dE_rows<<<cdiv(static_cast<long long>(n) * C, kDERowWarps), kDERowWarps * 32, 0, s>>>(
+            n, H, B, C, d_var, w.cat_order, w.cat_off, w.F32, w.dEt);
+        PC_LAUNCH_CHECK();
+      }
+      ProfileScope ps(s, PC_KIND_HCLT_MEM, (accumulate ? 3ll : 2ll) * n * CH * 4);
+      return transpose_f32(w.dEt, H, static_cast<long long>(C) * H, n, C, H, dE, C, accumulate, s);
     }
     {
       ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + n * CH * 4);

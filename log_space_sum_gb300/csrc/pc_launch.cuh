@@ -268,31 +268,41 @@ struct StoreF32 {  // a float32 matrix [g][c][ld], overwritten or accumulated in
   }
 };
 
-template <class Store, class Direct = NoDirect>
-__global__ void __launch_bounds__(256) k_transpose64(const float* __restrict__ src, long long src_ld,
+// Source elements: float32, or bf16 bit patterns (uint16_t, widened exactly).
+__device__ __forceinline__ float src_value(const float* p) { return *p; }
+__device__ __forceinline__ float src_value(const uint16_t* p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
+__device__ __forceinline__ float4 src_value4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 src_value4(const uint16_t* p) {
+  const uint2 x = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xFFFF0000u), __uint_as_float(x.y << 16),
+                     __uint_as_float(x.y & 0xFFFF0000u));
+}
+
+template <class Store, class Direct = NoDirect, class T = float>
+__global__ void __launch_bounds__(256) k_transpose64(const T* __restrict__ src, long long src_ld,
                                                       long long src_gs, int R, int C, const int* gmap, Store st,
                                                       Direct direct = {}) {
   __shared__ float tile[64][65];
   const int g = blockIdx.z;
   const long long gs = gmap ? gmap[g] : g;
   const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
-  const float* s = src + gs * src_gs;
+  const T* s = src + gs * src_gs;
   const int t = threadIdx.x;
-  const bool vec = (src_ld & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+  const bool vec = (src_ld & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & (4 * sizeof(T) - 1)) == 0;
 #pragma unroll
   for (int i = t; i < 64 * 16; i += 256) {
     const int rr = i >> 4, cq = (i & 15) * 4;
     const int r = r0 + rr, c = c0 + cq;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r < R) {
-      const float* p = s + static_cast<long long>(r) * src_ld + c;
+      const T* p = s + static_cast<long long>(r) * src_ld + c;
       if (vec && c + 3 < C) {
-        v = *reinterpret_cast<const float4*>(p);
+        v = src_value4(p);
       } else {
-        if (c < C) v.x = p[0];
-        if (c + 1 < C) v.y = p[1];
-        if (c + 2 < C) v.z = p[2];
-        if (c + 3 < C) v.w = p[3];
+        if (c < C) v.x = src_value(p);
+        if (c + 1 < C) v.y = src_value(p + 1);
+        if (c + 2 < C) v.z = src_value(p + 2);
+        if (c + 3 < C) v.w = src_value(p + 3);
       }
       if (c < C) direct(g, r, c, v, min(4, C - c));
     }
@@ -319,6 +329,17 @@ pc_status_t launch_transpose64(const float* src, long long src_ld, long long src
                                const int* gmap, const Store& st, cudaStream_t s) {
   if (G == 0 || R == 0 || C == 0) return PC_OK;
   k_transpose64<Store><<<dim3(cdiv(C, 64), cdiv(R, 64), G), 256, 0, s>>>(src, src_ld, src_gs, R, C, gmap, st);
+  PC_LAUNCH_CHECK();
+  return PC_OK;
+}
+
+// The same from a bf16 source (bit patterns): exact for a bf16 operand.
+inline pc_status_t transpose_bf16_to_operand(const uint16_t* src, long long src_ld, long long src_gs, int G, int R,
+                                             int C, const Operand& dst, cudaStream_t s) {
+  if (G == 0 || R == 0 || C == 0) return PC_OK;
+  k_transpose64<StoreOperand<kBF16>, NoDirect, uint16_t><<<dim3(cdiv(C, 64), cdiv(R, 64), G), 256, 0, s>>>(
+      src, src_ld, src_gs, R, C, nullptr,
+      StoreOperand<kBF16>{dst.ptr, dst.ld, dst.lo_elems, static_cast<long long>(C)});
   PC_LAUNCH_CHECK();
   return PC_OK;
 }
