@@ -225,12 +225,26 @@ __global__ void __launch_bounds__(256) k_hclt_product(
 // reduction, and a lane's loads of one child row are independent, so they are all in
 // flight together. Warp w of the launch takes node s0 + w / B, sample w % B.
 constexpr int kWarpRuns = 8;  // runs of four latents per lane: H <= 4 * 32 * 8
-
-// Running products of one (node, sample) row, m 2^e per latent (lane's runs q = lane +
-// 32 r): the emission row, then every child's D row from child c_from on.
-template <bool kVec>
-__device__ __forceinline__ void product_start(const float* er, bool xin, int H, int lane,
-                                              float (&m)[kWarpRuns][4], int (&e)[kWarpRuns][4]) {
+template <int P, bool kVec>
+__global__ void __launch_bounds__(256) k_hclt_product_warp(
+    int s0, int G, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
+    const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr, const int* __restrict__ child_slots,
+    const float* __restrict__ Et, const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
+    long long uop_ld, size_t uop_lo, int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi,
+    float* __restrict__ rdot) {
+  constexpr long long kNone = -0x7fffffffffffffffLL - 1;
+  const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (wid >= static_cast<long long>(G) * B) return;  // the whole warp leaves together
+  const int lane = threadIdx.x & 31;
+  const int s = s0 + static_cast<int>(wid / B);
+  const int b = static_cast<int>(wid % B);
+  const int v = var_of_slot[s];
+  const int x = data[static_cast<long long>(b) * nvars + v];
+  const bool xin = x >= 0 && x < C;
+  const int c0 = child_ptr[s], c1 = child_ptr[s + 1];
+  const float* er = Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H;
+  float m[kWarpRuns][4];
+  int e[kWarpRuns][4];
 #pragma unroll
   for (int r = 0; r < kWarpRuns; ++r) {
     const int q = lane + 32 * r;
@@ -245,35 +259,22 @@ __device__ __forceinline__ void product_start(const float* er, bool xin, int H, 
       m[r][k] = renorm(m[r][k], e[r][k]);
     }
   }
-}
-template <bool kVec>
-__device__ __forceinline__ void product_child(const float* drow, int H, int lane, float (&m)[kWarpRuns][4],
-                                              int (&e)[kWarpRuns][4]) {
-  float4 d[kWarpRuns];
+  for (int c = c0; c < c1; ++c) {
+    const float* drow = D + (static_cast<long long>(child_slots[c]) * B + b) * H;
+    float4 d[kWarpRuns];
 #pragma unroll
-  for (int r = 0; r < kWarpRuns; ++r) {
-    const int q = lane + 32 * r;
-    d[r] = 4 * q < H ? load_run4<kVec>(drow, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+    for (int r = 0; r < kWarpRuns; ++r) {
+      const int q = lane + 32 * r;
+      d[r] = 4 * q < H ? load_run4<kVec>(drow, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-  for (int r = 0; r < kWarpRuns; ++r) {
-    m[r][0] = renorm(m[r][0] * d[r].x, e[r][0]);
-    m[r][1] = renorm(m[r][1] * d[r].y, e[r][1]);
-    m[r][2] = renorm(m[r][2] * d[r].z, e[r][2]);
-    m[r][3] = renorm(m[r][3] * d[r].w, e[r][3]);
+    for (int r = 0; r < kWarpRuns; ++r) {
+      m[r][0] = renorm(m[r][0] * d[r].x, e[r][0]);
+      m[r][1] = renorm(m[r][1] * d[r].y, e[r][1]);
+      m[r][2] = renorm(m[r][2] * d[r].z, e[r][2]);
+      m[r][3] = renorm(m[r][3] * d[r].w, e[r][3]);
+    }
   }
-}
-
-// The row's maximum (a warp reduction on (exponent, mantissa) keys), u = m / m_max
-// 2^(e - e_max) into U32 (if kept) and the children operand, the offsets Ex / Lm, and at
-// the root the dot product with pi.
-template <int P, bool kVec>
-__device__ __forceinline__ void product_finish(float (&m)[kWarpRuns][4], int (&e)[kWarpRuns][4], int s, int b,
-                                               int lane, int root_slot, int H, int B, float* __restrict__ U32,
-                                               void* uop, long long uop_ld, size_t uop_lo, int* __restrict__ Ex,
-                                               float* __restrict__ Lm, const float* __restrict__ pi,
-                                               float* __restrict__ rdot) {
-  constexpr long long kNone = -0x7fffffffffffffffLL - 1;
   long long best = kNone;
 #pragma unroll
   for (int r = 0; r < kWarpRuns; ++r)
@@ -320,30 +321,6 @@ __device__ __forceinline__ void product_finish(float (&m)[kWarpRuns][4], int (&e
   if (s != root_slot) return;
   for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
   if (lane == 0) rdot[b] = dot;
-}
-
-template <int P, bool kVec>
-__global__ void __launch_bounds__(256) k_hclt_product_warp(
-    int s0, int G, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
-    const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr, const int* __restrict__ child_slots,
-    const float* __restrict__ Et, const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
-    long long uop_ld, size_t uop_lo, int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi,
-    float* __restrict__ rdot) {
-  const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (wid >= static_cast<long long>(G) * B) return;  // the whole warp leaves together
-  const int lane = threadIdx.x & 31;
-  const int s = s0 + static_cast<int>(wid / B);
-  const int b = static_cast<int>(wid % B);
-  const int v = var_of_slot[s];
-  const int x = data[static_cast<long long>(b) * nvars + v];
-  const bool xin = x >= 0 && x < C;
-  const int c0 = child_ptr[s], c1 = child_ptr[s + 1];
-  float m[kWarpRuns][4];
-  int e[kWarpRuns][4];
-  product_start<kVec>(Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H, xin, H, lane, m, e);
-  for (int c = c0; c < c1; ++c)
-    product_child<kVec>(D + (static_cast<long long>(child_slots[c]) * B + b) * H, H, lane, m, e);
-  product_finish<P, kVec>(m, e, s, b, lane, root_slot, H, B, U32, uop, uop_ld, uop_lo, Ex, Lm, pi, rdot);
 }
 
 // The log-likelihood. Every node lies under the root, so the root's offset is the sum over
