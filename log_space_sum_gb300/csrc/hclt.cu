@@ -125,7 +125,8 @@ template <int P, bool kVec>
 __global__ void __launch_bounds__(256) k_hclt_product(
     int s0, int root_slot, int nvars, int H, int B, const int* __restrict__ data, const int* __restrict__ var_of_slot,
     const int* __restrict__ child_ptr, const int* __restrict__ child_slots, const float* __restrict__ Et,
-    const float* __restrict__ D, int C, float* __restrict__ U32, void* uop, long long uop_ld, size_t uop_lo,
+    const float* __restrict__ D, int C, float* __restrict__ U32, long long u32_off, void* uop, long long uop_ld,
+    size_t uop_lo,
     int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi, float* __restrict__ rdot) {
   extern __shared__ float4 mant4[];  // ceil(H/4) mantissa runs, then as many exponent runs
   const int H4 = (H + 3) / 4;
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(256) k_hclt_product(
   const float mmax = live ? __uint_as_float(mbits) : 1.f;
   const float rinv = 1.f / mmax;
   const long long row = static_cast<long long>(s) * B + b;
-  float* u32 = U32 ? U32 + row * H : nullptr;  // NULL: the bf16 operand parts carry u
+  float* u32 = U32 ? U32 + row * H - u32_off : nullptr;  // NULL: the bf16 operand parts carry u
   float dot = 0.f;
   for (int q = threadIdx.x; q < H4; q += blockDim.x) {
     const float4 m = mant4[q];
@@ -229,8 +230,8 @@ template <int P, bool kVec>
 __global__ void __launch_bounds__(256) k_hclt_product_warp(
     int s0, int G, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
     const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr, const int* __restrict__ child_slots,
-    const float* __restrict__ Et, const float* __restrict__ D, int C, float* __restrict__ U32, void* uop,
-    long long uop_ld, size_t uop_lo, int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi,
+    const float* __restrict__ Et, const float* __restrict__ D, int C, float* __restrict__ U32, long long u32_off,
+    void* uop, long long uop_ld, size_t uop_lo, int* __restrict__ Ex, float* __restrict__ Lm, const float* __restrict__ pi,
     float* __restrict__ rdot) {
   constexpr long long kNone = -0x7fffffffffffffffLL - 1;
   const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
   const float mmax = live ? __uint_as_float(mbits) : 1.f;
   const float rinv = 1.f / mmax;
   const long long row = static_cast<long long>(s) * B + b;
-  float* u32 = U32 ? U32 + row * H : nullptr;  // NULL: the bf16 operand parts carry u
+  float* u32 = U32 ? U32 + row * H - u32_off : nullptr;  // NULL: the bf16 operand parts carry u
   float dot = 0.f;
 #pragma unroll
   for (int r = 0; r < kWarpRuns; ++r) {
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kLlWarps * 32) k_hclt_ll(int nslots, int B, co
 
 // Root flows f_0[b][z] = pi[z] u_0[b][z] / sum_z pi u_0 (batch-major) and dpi += sum_b f_0.
 __global__ void k_hclt_root_flows(int root_slot, int H, int B, const float* __restrict__ pi,
-                                  const float* __restrict__ U32, const float* __restrict__ rroot,
+                                  const float* __restrict__ U32, long long u32_off, const float* __restrict__ rroot,
                                   float* __restrict__ F32, float* dpi) {
   const int z = blockIdx.x * blockDim.x + threadIdx.x;
   if (z >= H) return;
@@ -380,7 +381,7 @@ __global__ void k_hclt_root_flows(int root_slot, int H, int B, const float* __re
   const int b0 = blockIdx.y * 32;
   for (int b = b0; b < b0 + 32 && b < B; ++b) {
     const long long idx = (static_cast<long long>(root_slot) * B + b) * H + z;
-    const float f = pz * U32[idx] * rroot[b];
+    const float f = pz * U32[idx - u32_off] * rroot[b];
     F32[idx] = f;
     acc += f;
   }
@@ -801,6 +802,7 @@ struct HcltWs {
   int* plan;
   Operand Wop, WopT, Uop, Gbm, Gnm, Unm;
   float *Et, *U32, *D, *rroot, *rdot, *Lm, *F32, *dEt;
+  long long u32_off = 0;  // elements between U32 and the first stored slot row
   int* Ex;
   int *cat_order, *cat_off;
 };
@@ -841,9 +843,15 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
     w->Wop = c.operand(p, E1, H, H);
     w->Et = static_cast<float*>(c.take(size_t(n) * C * H * 4));
   }
-  w->U32 = static_cast<float*>(c.take(size_t(n) * B * H * 4));
+  // bf16: u is kept in float32 for the root alone (below it the children operand's hi
+  // and lo parts carry it); U32 then holds the root's rows and u32_off shifts slot rows
+  const bool u32_root_only = p == PC_PREC_AUTO;
+  w->u32_off = u32_root_only ? static_cast<long long>(n - 1) * B * H : 0;
+  w->U32 = static_cast<float*>(c.take(size_t(u32_root_only ? 1 : n) * B * H * 4));
   w->Uop = c.operand(p, E1, B, H, 2);  // hi + lo in every mode (EpiHcltFwd::kBLo)
-  w->D = static_cast<float*>(c.take(size_t(E1) * B * H * 4));
+  // n slots (one more than the edges need), so that dE's category-major rows (n x C x H)
+  // can reuse D when C <= B: D is dead once the last level's scaled flows have run
+  w->D = static_cast<float*>(c.take(size_t(n) * B * H * 4));
   w->Ex = static_cast<int*>(c.take(size_t(n) * B * 4));
   w->Lm = static_cast<float*>(c.take(size_t(n) * B * 4));
   w->rroot = static_cast<float*>(c.take(size_t(B) * 4));
@@ -855,7 +863,7 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
     w->Gnm = c.operand(p, E1, H, B);
     w->Unm = c.operand(p, E1, H, B);
     if (want_dE) {
-      w->dEt = static_cast<float*>(c.take(size_t(n) * C * H * 4));
+      w->dEt = C <= B ? w->D : static_cast<float*>(c.take(size_t(n) * C * H * 4));
       w->cat_order = static_cast<int*>(c.take(size_t(n) * B * 4));
       w->cat_off = static_cast<int*>(c.take(size_t(n) * (C + 1) * 4));
     }
@@ -987,11 +995,11 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
     if (H <= 4 * 32 * kWarpRuns) {
       const unsigned blocks = static_cast<unsigned>(cdiv(static_cast<long long>(G) * B, 8));
       (prod_vec ? k_hclt_product_warp<P, true> : k_hclt_product_warp<P, false>)<<<blocks, 256, 0, s>>>(
-          sA, G, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, u32_out, edges ? w.Uop.ptr : nullptr,
+          sA, G, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, u32_out, w.u32_off, edges ? w.Uop.ptr : nullptr,
           w.Uop.ld, w.Uop.lo_elems, w.Ex, w.Lm, pi, w.rdot);
     } else {
       (prod_vec ? k_hclt_product<P, true> : k_hclt_product<P, false>)<<<dim3(G, B), 256, prod_smem, s>>>(
-          sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, u32_out, edges ? w.Uop.ptr : nullptr,
+          sA, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, u32_out, w.u32_off, edges ? w.Uop.ptr : nullptr,
           w.Uop.ld, w.Uop.lo_elems, w.Ex, w.Lm, pi, w.rdot);
     }
     PC_LAUNCH_CHECK();
@@ -1020,7 +1028,8 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
   // ------------------------------------------------------------- backward
   {
     ProfileScope ps(s, PC_KIND_HCLT_MEM, 2 * BH * 4 + H * 4ll + B * 4ll);
-    k_hclt_root_flows<<<dim3(cdiv(H, 256), cdiv(B, 32)), 256, 0, s>>>(root, H, B, pi, w.U32, w.rroot, w.F32, dpi);
+    k_hclt_root_flows<<<dim3(cdiv(H, 256), cdiv(B, 32)), 256, 0, s>>>(root, H, B, pi, w.U32, w.u32_off, w.rroot,
+                                                                       w.F32, dpi);
     PC_LAUNCH_CHECK();
   }
   if (down) {
