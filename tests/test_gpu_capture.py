@@ -102,6 +102,20 @@ def test_hclt(mode):
     _same(eager[1:2], graph[1:2], exact=False)  # dpi: float atomics
 
 
+@pytest.mark.parametrize("mode", ["auto", "tf32"])
+def test_hclt_prepared_and_persistent_tiles(mode):
+    # H a multiple of 8: the forward and parameter contractions run on persistent tiles;
+    # the prepared parameters are made outside the graph, the batch call is captured
+    d = hclt_inputs(24, 256, 9, 256, seed=604)
+    t = {k: _t(d[k]) for k in ("data", "pi", "W", "E")}
+    prep = pc.hclt_prepare(d["parent"], t["W"], t["E"], precision=mode)
+    torch.cuda.synchronize()
+    eager, graph = _capture(lambda: list(pc.hclt_fwd_bwd(d["parent"], t["data"], t["pi"], t["W"], None,
+                                                         precision=mode, prepared=prep)))
+    _same(eager[:1] + eager[2:], graph[:1] + graph[2:])
+    _same(eager[1:2], graph[1:2], exact=False)  # dpi: float atomics
+
+
 @pytest.mark.parametrize("form", ["exp_sum", "sum_exp"])
 def test_lowrank(form):
     d = lowrank_inputs(200, 150, 5, 24, spread=1.0, seed=604)

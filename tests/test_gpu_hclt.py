@@ -76,6 +76,42 @@ def test_forward_only_and_accumulate():
         torch.testing.assert_close(y, 2 * x, rtol=1e-6, atol=0)
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_latents_a_multiple_of_four(mode):
+    # H % 4 == 0 but H % 8 != 0 and off the tile sizes: the parameter flows take the
+    # persistent tiles with the theta ring (partial chunks), the element flows the staged
+    # 128-wide tiles (bf16: u from the operand's hi and lo parts), dE the whole-row sums;
+    # then accumulation, whose persistent epilogue adds with one reduction per element
+    d = hclt_inputs(40, 100, 17, 45, seed=207)
+    rl, rpi, rW, rE = _oracle(d)
+    ll, dpi, dW, dE = _gpu_run(d, mode)
+    errs = ll_err(ll, rl), flow_err(dpi, rpi), flow_err(dW[1:], rW[1:]), flow_err(dE, rE)
+    print(f"hclt 40x100 {mode}: ll {errs[0]:.3e} dpi {errs[1]:.3e} dW {errs[2]:.3e} dE {errs[3]:.3e}")
+    assert errs[0] <= LL_TOL[mode]
+    assert max(errs[1:]) <= FLOW_TOL[mode]
+    t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda() for k in ("data", "pi", "W", "E")}
+    first = [torch.from_numpy(x).cuda() for x in (dpi, dW, dE)]
+    _, dpi2, dW2, dE2 = pc.hclt_fwd_bwd(d["parent"], t["data"], t["pi"], t["W"], t["E"], precision=mode,
+                                        dpi=first[0].clone(), dW=first[1].clone(), dE=first[2].clone(),
+                                        accumulate=True)
+    torch.cuda.synchronize()
+    for x, y in zip(first, (dpi2, dW2, dE2)):
+        torch.testing.assert_close(y, 2 * x, rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("mode", ["auto", "fp32"])
+def test_wide_tiles_ragged(mode):
+    # enough edges on the lowest level for the 256-wide persistent element tiles, with H
+    # and B off the tile sizes (H = 1000, B = 600): partial row and sample tiles
+    d = hclt_inputs(24, 1000, 11, 600, seed=208)
+    rl, rpi, rW, rE = _oracle(d)
+    ll, dpi, dW, dE = _gpu_run(d, mode)
+    errs = ll_err(ll, rl), flow_err(dpi, rpi), flow_err(dW[1:], rW[1:]), flow_err(dE, rE)
+    print(f"hclt 24x1000 B600 {mode}: ll {errs[0]:.3e} dpi {errs[1]:.3e} dW {errs[2]:.3e} dE {errs[3]:.3e}")
+    assert errs[0] <= LL_TOL[mode]
+    assert max(errs[1:]) <= FLOW_TOL[mode]
+
+
 @pytest.fixture(scope="module")
 def hclt_full():
     d = hclt()
