@@ -388,6 +388,10 @@ struct EpiHmmFwd {
   static constexpr int kEpiWarps = P == kTF32x3 ? 16 : 8;
   static constexpr int kSliceBF16 = 0;
   static constexpr int kSliceTF32 = 0;  // the TF32 chain runs as split-K pairs: one accumulation
+  // 3xTF32: slices of two k-steps (see EpiSlice3x): the chain has T - 1 layers, whose
+  // residual truncation bias stays far below the fp32 mode's 1e-5 (the 4096 x 32 workload's
+  // LL error: 2.9e-7)
+  static constexpr int kSlice3x = 2;
   // the 3xTF32 ring needs the room: it gathers emissions directly instead
   static constexpr bool kStageE = P != kTF32x3;
   static constexpr bool kEsSplit = P != kTF32x3 && W == kChainBN;  // see kEsLoCols
@@ -667,6 +671,7 @@ struct EpiHmmBwd : EpiNoHooks {
   using Params = HmmBwdParams;
   static constexpr int kEpiWarps = P == kTF32x3 ? 16 : 8;  // as EpiHmmFwd
   static constexpr int kSliceTF32 = 0;  // as EpiHmmFwd
+  static constexpr int kSlice3x = 2;    // as EpiHmmFwd
   static constexpr bool kStageE = P != kTF32x3;
   static constexpr bool kEsSplit = P != kTF32x3 && W == kChainBN;  // see kEsLoCols
   static constexpr bool kStageOut = P == kBF16;                    // as EpiHmmFwd

@@ -99,15 +99,20 @@ struct GemmShape {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: two epilogue warps split the 32-column chunks");
 };
 
-// Accumulation slices, in MMA k-steps (1, or a multiple of the k-steps of one ring slot);
-// see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
+// Accumulation slices, in MMA k-steps (1 or 2, or a multiple of the k-steps of one ring
+// slot); see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
 // (Epi::kSliceBF16 k-steps; 0 = one accumulation over all of K). 3xTF32 slices one k-step
-// at a time: with two k-steps per slice (half the slices, measured 11.25 against 14.56 ms
-// per HMM 4096 step) the second hi*hi product adds a truncation at the partial sum's own
-// magnitude, whose expected size depends on the data (the HCLT-768 LL error went to
-// 2.5e-5 with the one-step correction, to 1.9e-5 on uniform emissions with 1.5 times it):
-// no single correction keeps both inside the fp32 mode's 1e-5.
+// at a time unless the epilogue asks for two (Epi::kSlice3x): half the slices (HMM 4096
+// step 11.25 against 14.56 ms), but the second hi*hi product adds a truncation at the
+// partial sum's own magnitude, whose expected size depends on the data; its correction
+// (1.5 half ulps per slice) leaves a residual bias per contraction of up to ~2.5e-8 of
+// the sum (the HCLT-768 LL, 767 chained edges, moved by 8e-6, and by 1.9e-5 on uniform
+// emissions): fine for a chain of tens of layers, not for hundreds.
 constexpr int kSliceK3x = 1;
+template <class E, class = void>
+struct EpiSlice3x : std::integral_constant<int, kSliceK3x> {};
+template <class E>
+struct EpiSlice3x<E, std::void_t<decltype(E::kSlice3x)>> : std::integral_constant<int, E::kSlice3x> {};
 constexpr int kSliceK1 = 8;  // the TF32 default (EpiSliceTF32)
 
 // The tensor core's float32 accumulator truncates toward zero. A slice of one 3xTF32
@@ -272,7 +277,8 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
   // whatever K is. A slice of one k-step (3xTF32: lo*hi, hi*lo, then hi*hi) ends in a
   // single truncation at the slice's own magnitude, whose expected loss (half_ulp of the
   // slice) the epilogue adds back to each slice.
-  constexpr int kSliceK = (P == kTF32x3) ? kSliceK3x : (P == kTF32 ? EpiSliceTF32<Epi>::value : Epi::kSliceBF16);
+  constexpr int kSliceK =
+      (P == kTF32x3) ? EpiSlice3x<Epi>::value : (P == kTF32 ? EpiSliceTF32<Epi>::value : Epi::kSliceBF16);
   constexpr bool kSliced = kSliceK > 0;
   constexpr bool kStepSliced = kSliced && kSliceK < static_cast<int>(S::kKSteps);
   static_assert(!kSliced || (kStepSliced ? S::kKSteps % kSliceK == 0 && (kSliceK == 1 || P == kTF32x3)
@@ -287,8 +293,10 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
                                  : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM columns");
   constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
-  static_assert(!kHalfUlp || kSliceK == 1, "the truncation correction is that of one-k-step slices");
-  constexpr uint32_t kCorrBits = 0x34800000u;  // 4 x 2^-24: four half ulps, every fourth slice
+  static_assert(!kHalfUlp || kSliceK <= 2, "the truncation correction is that of one- or two-k-step slices");
+  // every fourth slice adds 4 half ulps (one-k-step slices: one truncation at the slice's
+  // magnitude) or 6 (two k-steps: that one plus one at about half of it)
+  constexpr uint32_t kCorrBits = kSliceK == 1 ? 0x34800000u : 0x34C00000u;  // 4 or 6 x 2^-24
   // split K: the idle ring holds the exchange buffer (128 x BN/2 floats), then the
   // epilogue's staged tiles
   constexpr int kXchgBytes = kBM * (BN / 2) * 4;
