@@ -934,6 +934,18 @@ pc_status_t check_hmm_shape(int H, int T, int V, int B) {
   return PC_OK;
 }
 
+// The stacked dA contraction (one contraction over K = (T - 1) B, not a chain): in 3xTF32
+// it accumulates slices of one ring slot (4 k-steps, summed in registers, no correction),
+// whose truncation bias (~2.5e-7 of the result, measured on a layer) is far inside the
+// fp32 mode's 1e-5 flow bar for a single contraction, at a quarter of the one-k-step
+// slices' round trips.
+struct EpiThetaScaleStacked : EpiThetaScale {
+  static constexpr int kSlice3x = 4;
+};
+struct EpiStoreF32Stacked : EpiStoreF32 {
+  static constexpr int kSlice3x = 4;
+};
+
 template <int P>
 pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const float* pi, const float* A,
                     const float* E, double* ll, float* dpi, float* dA, float* dE, int accumulate,
@@ -1174,9 +1186,9 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
           vb.lo = vb.hi;
         }
         EpiStoreF32::Params ep{w.dA_part, H, H, H, 0, nullptr, nullptr, static_cast<long long>(H) * H};
-        if ((st = launch_gemm<P, kParamBN, EpiStoreF32>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), S), va.hi, va.lo, vb.hi,
-                                                        vb.lo, num_k_blocks(K / S, prec), ep, s, PC_KIND_HMM_PARAM,
-                                                        2ll * H * H * K)) != PC_OK)
+        if ((st = launch_gemm<P, kParamBN, EpiStoreF32Stacked>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), S), va.hi,
+                                                               va.lo, vb.hi, vb.lo, num_k_blocks(K / S, prec), ep, s,
+                                                               PC_KIND_HMM_PARAM, 2ll * H * H * K)) != PC_OK)
           return st;
         const long long n = static_cast<long long>(H) * H;
         ProfileScope ps(s, PC_KIND_HMM_MEM, (S + 2 + (accumulate ? 1 : 0)) * n * 4);
@@ -1185,9 +1197,9 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
         PC_LAUNCH_CHECK();
       } else {
         EpiThetaScale::Params ep{dA, A, H, H, accumulate};
-        if ((st = launch_gemm<P, kParamBN, EpiThetaScale>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), 1), pa.hi, pa.lo,
-                                                          pb.hi, pb.lo, num_k_blocks(K, prec), ep, s, PC_KIND_HMM_PARAM,
-                                                          2ll * H * H * K)) != PC_OK)
+        if ((st = launch_gemm<P, kParamBN, EpiThetaScaleStacked>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), 1), pa.hi,
+                                                                 pa.lo, pb.hi, pb.lo, num_k_blocks(K, prec), ep, s,
+                                                                 PC_KIND_HMM_PARAM, 2ll * H * H * K)) != PC_OK)
           return st;
       }
     }
