@@ -1197,10 +1197,30 @@ pc_status_t hmm_run(int H, int T, int V, int B, const int32_t* tokens, const flo
         PC_LAUNCH_CHECK();
       } else {
         EpiThetaScale::Params ep{dA, A, H, H, accumulate};
-        if ((st = launch_gemm<P, kParamBN, EpiThetaScaleStacked>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), 1), pa.hi,
-                                                                 pa.lo, pb.hi, pb.lo, num_k_blocks(K, prec), ep, s,
-                                                                 PC_KIND_HMM_PARAM, 2ll * H * H * K)) != PC_OK)
-          return st;
+        bool persist = false;
+        if constexpr (P != kTF32x3) {
+          // bf16 / TF32: persistent tiles (each tile's theta and dA traffic under the next
+          // tile's K loop); a last partial wave of at most half the SMs is split into K
+          // halves added into dA (zeroed first), which halves its length: 512 tiles on
+          // 152 SMs take 3.5 tile times instead of 4
+          const int tm = static_cast<int>(cdiv(H, kBM)), tn = static_cast<int>(cdiv(H, kParamBN));
+          const int tail = (tm * tn) % num_sms();
+          const int split =
+              (!accumulate && tail > 0 && 2 * tail <= num_sms() && num_k_blocks(K, prec) >= 2) ? tail : 0;
+          if (split) {
+            const long long row0 = static_cast<long long>((tm * tn - split) / tn) * kBM;
+            PC_CUDA(cudaMemsetAsync(dA + row0 * H, 0, size_t(H - row0) * H * 4, s));
+          }
+          persist = true;
+          st = launch_gemm_persist<P, kParamBN, EpiThetaScaleDirect>(tm, tn, 1, pa.hi, pa.lo, pb.hi, pb.lo,
+                                                                     num_k_blocks(K, prec), ep, s, PC_KIND_HMM_PARAM,
+                                                                     2ll * H * H * K, split);
+        }
+        if (!persist)
+          st = launch_gemm<P, kParamBN, EpiThetaScaleStacked>(dim3(cdiv(H, kBM), cdiv(H, kParamBN), 1), pa.hi, pa.lo,
+                                                              pb.hi, pb.lo, num_k_blocks(K, prec), ep, s,
+                                                              PC_KIND_HMM_PARAM, 2ll * H * H * K);
+        if (st != PC_OK) return st;
       }
     }
     if (dE && (st = side.join(s)) != PC_OK) return st;

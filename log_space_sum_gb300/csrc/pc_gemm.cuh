@@ -712,11 +712,20 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
 // the next tile's K loop does. Unsliced bf16 or TF32, no split, no prefetched tile (the
 // ring is never idle); Epi::prepare runs per tile (the epilogue warps own their shared
 // memory between tiles). Waits and drains as in k_umma_gemm.
+// Split tail (split_from < the tile count; epilogues with apply_add / accumulating load-
+// ahead only): the tiles from split_from on are taken as two units each, over the first
+// and the second half of K, whose epilogues add their partial products into the output
+// with one reduction per element. When the tiles leave a last partial wave of at most
+// half the CTAs, halving its tiles halves its length.
+template <class E, class = void>
+struct EpiHasAdd : std::false_type {};
+template <class E>
+struct EpiHasAdd<E, std::void_t<decltype(&E::apply_add)>> : std::true_type {};
 template <int P, int BN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_umma_gemm_persist(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_lo,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB_lo,
-                        int num_kb, int tiles_m, int tiles_n, int groups, unsigned* status,
+                        int num_kb, int tiles_m, int tiles_n, int groups, int split_from, unsigned* status,
                         const typename Epi::Params ep) {
   static_assert(P == kBF16 || P == kTF32, "persistent tiles: bf16 or TF32");
   static_assert(EpiWarps<Epi>::value == kEpiWarps && !EpiPrefetch<Epi>::value,
@@ -752,6 +761,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     m0 = (r / tiles_n) * kBM;
     n0 = (r % tiles_n) * BN;
   };
+  // work units: the tiles before split_from whole, then two K halves of each later tile
+  const int num_units = split_from + 2 * (num_tiles - split_from);
+  auto unit_info = [&](int u, int& t, int& kb0, int& kb1) {  // returns the tile's K-block range
+    if (u < split_from) {
+      t = u;
+      kb0 = 0;
+      kb1 = num_kb;
+    } else {
+      const int j = u - split_from;
+      t = split_from + j / 2;
+      kb0 = (j & 1) ? num_kb / 2 : 0;
+      kb1 = (j & 1) ? num_kb : num_kb / 2;
+    }
+    return u >= split_from;  // a partial product: the epilogue adds
+  };
   auto a_tile = [&](int s) { return smem + s * S::kStageBytes; };
   auto b_tile = [&](int s, int part) { return smem + s * S::kStageBytes + S::kABytes + part * S::kBBytes; };
 
@@ -786,10 +810,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       grid_dependents_launch();
       int it = 0, issued = 0;  // k-blocks issued over all tiles
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        int m0, n0, g;
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        int t, kb0, kb1, m0, n0, g;
+        unit_info(u, t, kb0, kb1);
         tile_coords(t, m0, n0, g);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, status, kErrTimeoutProducer, wl)) {
             ok = false;
@@ -811,12 +836,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       constexpr uint32_t idesc = umma_idesc(P == kBF16 ? 1u : 2u, kBM, BN);
       int it = 0, local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++local) {
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++local) {
+        int t, kb0, kb1;
+        unit_info(u, t, kb0, kb1);
         const int a = local & 1;
         if (!mbar_wait(&acc_empty[a], ((local >> 1) & 1) ^ 1, status, kErrTimeoutMma, wl)) break;
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(a * kAccCols);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&full[s], (it / kStages) & 1, status, kErrTimeoutMma, wl)) {
             ok = false;
@@ -827,7 +854,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (uint32_t kk = 0; kk < S::kKSteps; ++kk) {
             const uint32_t off = kk * 32;
-            const uint32_t acc = (kb == 0 && kk == 0) ? 0u : 1u;
+            const uint32_t acc = (kb == kb0 && kk == 0) ? 0u : 1u;
             if constexpr (P == kBF16) {
               umma_bf16(d, umma_desc_sw128(a0 + off), umma_desc_sw128(b0 + off), idesc, acc);
               if constexpr (kBLo) umma_bf16(d + BN, umma_desc_sw128(a0 + off), umma_desc_sw128(b1 + off), idesc, acc);
@@ -869,15 +896,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       constexpr int kCPT = BN / (32 * kWPQ);  // chunks of one tile per warp
       static_assert(kNB >= 2 && Epi::kSmemBytes >= kEpiWarps * kNB * 4096, "a ring of 4 KB blocks per warp");
       float* ring = reinterpret_cast<float*>(epi_smem) + ew * kNB * 1024;
-      const int my_tiles =
-          static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-      const int items = my_tiles * kCPT;  // (tile, chunk) items of this warp, in order
-      auto item_tile = [&](int i) { return static_cast<int>(blockIdx.x) + (i / kCPT) * static_cast<int>(gridDim.x); };
+      const int my_units =
+          static_cast<int>(blockIdx.x) < num_units ? (num_units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+      const int items = my_units * kCPT;  // (unit, chunk) items of this warp, in order
+      auto item_unit = [&](int i) { return static_cast<int>(blockIdx.x) + (i / kCPT) * static_cast<int>(gridDim.x); };
       auto item_col = [&](int i) { return part * 32 + (i % kCPT) * 32 * kWPQ; };
+      auto item_tile = [&](int i, bool& add) {
+        int t, kb0, kb1;
+        add = unit_info(item_unit(i), t, kb0, kb1);
+        return t;
+      };
       auto issue = [&](int i) {
         if (i < items) {
           int m0, n0, g;
-          tile_coords(item_tile(i), m0, n0, g);
+          bool add;
+          tile_coords(item_tile(i, add), m0, n0, g);
           Epi::issue(ep, g, m0, n0, q, item_col(i), ring + (i % kNB) * 1024);
         }
         cp_async_commit();  // (an empty group past the end keeps the counting uniform)
@@ -886,7 +919,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int i = 0; i < items; ++i) {
         issue(i + kNB - 1);  // into the buffer item i - 1 left
         int m0, n0, g;
-        tile_coords(item_tile(i), m0, n0, g);
+        bool add;
+        tile_coords(item_tile(i, add), m0, n0, g);
         const int local_i = i / kCPT, a = local_i & 1, c = item_col(i);
         if (i % kCPT == 0) {
           ok = epilogue_bar_and(ok && mbar_wait(&acc_full[a], (local_i >> 1) & 1, status, kErrTimeoutEpilogue, wl));
@@ -902,13 +936,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[a]);
         }
-        Epi::apply_buf(ep, g, m0, n0, row, c, v, ring + (i % kNB) * 1024);
+        if constexpr (EpiHasAdd<Epi>::value) {
+          if (add) {
+            typename Epi::Params pa = ep;
+            pa.accumulate = 1;  // a K half: added with one reduction per element
+            Epi::apply_buf(pa, g, m0, n0, row, c, v, ring + (i % kNB) * 1024);
+          } else {
+            Epi::apply_buf(ep, g, m0, n0, row, c, v, ring + (i % kNB) * 1024);
+          }
+        } else {
+          Epi::apply_buf(ep, g, m0, n0, row, c, v, ring + (i % kNB) * 1024);
+        }
         __syncwarp();  // every lane is done with the block before it is refilled
       }
       cp_async_wait_all();  // no copy may land after the CTA has left
     } else {
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-        int m0, n0, g;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++local) {
+        int t, kb0, kb1, m0, n0, g;
+        const bool add = unit_info(u, t, kb0, kb1);
         tile_coords(t, m0, n0, g);
         Epi::prepare(ep, g, m0, n0, et, epi_smem);
         epilogue_bar_sync();
@@ -925,7 +970,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[a]);
           }
-          Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+          if constexpr (EpiHasAdd<Epi>::value) {
+            if (add)
+              Epi::apply_add(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+            else
+              Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+          } else {
+            Epi::apply(ep, g, m0, n0, row, c, v, epi_smem, tbuf);
+          }
         }
         Epi::finish(ep, g, m0, n0, et, epi_smem);
         epilogue_bar_sync();  // prepare of the next tile rewrites the epilogue's shared memory

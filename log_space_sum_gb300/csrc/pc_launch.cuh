@@ -51,10 +51,13 @@ pc_status_t launch_gemm(dim3 grid, const CUtensorMap& a, const CUtensorMap& a_lo
 
 // The persistent contraction over tiles_m x tiles_n x groups tiles (k_umma_gemm_persist):
 // one CTA per SM, or fewer when there are fewer tiles.
+// split_tail: the last tiles taken as two K halves each (EpiHasAdd epilogues; the caller
+// zeroes their output first unless the epilogue accumulates).
 template <int P, int BN, class Epi>
 pc_status_t launch_gemm_persist(int tiles_m, int tiles_n, int groups, const CUtensorMap& a, const CUtensorMap& a_lo,
                                 const CUtensorMap& b, const CUtensorMap& b_lo, int num_kb,
-                                const typename Epi::Params& ep, cudaStream_t stream, int kind, long long flops) {
+                                const typename Epi::Params& ep, cudaStream_t stream, int kind, long long flops,
+                                int split_tail = 0) {
   constexpr size_t smem = gemm_smem_bytes<P, BN, Epi>();
   static_assert(smem <= 232448, "shared memory per CTA");
   static bool attr_set[64] = {};
@@ -68,19 +71,22 @@ pc_status_t launch_gemm_persist(int tiles_m, int tiles_n, int groups, const CUte
   }
   const long long tiles = static_cast<long long>(tiles_m) * tiles_n * groups;
   if (tiles == 0) return PC_OK;
+  if (split_tail < 0 || split_tail > tiles || (split_tail > 0 && (!EpiHasAdd<Epi>::value || num_kb < 2)))
+    return set_error(PC_ERR_UNSUPPORTED, "split tail of %d tiles not supported here", split_tail);
+  const long long units = tiles + split_tail;
   const int slot = profile_begin(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles < num_sms() ? tiles : num_sms()));
+  cfg.gridDim = dim3(static_cast<unsigned>(units < num_sms() ? units : num_sms()));
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   PC_CUDA(cudaLaunchKernelEx(&cfg, k_umma_gemm_persist<P, BN, Epi>, a, a_lo, b, b_lo, num_kb, tiles_m, tiles_n,
-                             groups, device_status_word(), ep));
+                             groups, static_cast<int>(tiles - split_tail), device_status_word(), ep));
   PC_LAUNCH_CHECK();
   profile_end(slot, stream, kind, flops);
   return PC_OK;
@@ -430,6 +436,33 @@ struct EpiThetaScale : EpiNoHooks {
 #pragma unroll
       for (int r = 0; r < 16; ++r)
         if (i0 + h + r < p.M) Fp[(h + r) * ld] = f[r] + t[r] * w[h + r];
+    }
+  }
+
+  // apply for a partial product (a K half of a split tile, k_umma_gemm_persist): F +=
+  // theta * D by one reduction per element, whatever accumulate says (F holds the other
+  // half's share, or zeros the caller wrote).
+  __device__ static void apply_add(const Params& p, int g, int m0, int n0, int row, int col0, float (&v)[32],
+                                   uint8_t*, float* tbuf) {
+    float w[32];
+    warp_transpose32(v, w, tbuf);
+    const int lane = threadIdx.x & 31;
+    const int i0 = m0 + row - lane;
+    const int j = n0 + col0 + lane;
+    if (j >= p.N) return;
+    const long long ld = p.N;
+    const long long gm = p.gmap ? p.gmap[g] : g;
+    const float* tp = p.theta + (gm * p.M + i0) * ld + j;
+    float* Fp = p.F + (gm * p.M + i0) * ld + j;
+    if (p.rscale || p.cscale) scale_rows(p.rscale, p.cscale, i0, j, p.M, w);
+#pragma unroll
+    for (int h = 0; h < 32; h += 16) {
+      float t[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) t[r] = i0 + h + r < p.M ? tp[(h + r) * ld] : 0.f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (i0 + h + r < p.M) atomicAdd(Fp + (h + r) * ld, t[r] * w[h + r]);
     }
   }
 
