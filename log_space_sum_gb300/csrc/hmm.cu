@@ -388,10 +388,10 @@ struct EpiHmmFwd {
   static constexpr int kEpiWarps = P == kTF32x3 ? 16 : 8;
   static constexpr int kSliceBF16 = 0;
   static constexpr int kSliceTF32 = 0;  // the TF32 chain runs as split-K pairs: one accumulation
-  // 3xTF32: slices of two k-steps (see EpiSlice3x): the chain has T - 1 layers, whose
-  // residual truncation bias stays far below the fp32 mode's 1e-5 (the 4096 x 32 workload's
-  // LL error: 2.9e-7)
-  static constexpr int kSlice3x = 2;
+  // 3xTF32: slices of a whole ring slot (4 k-steps; see EpiSlice3x): the chain has T - 1
+  // layers, whose residual truncation bias stays far below the fp32 mode's 1e-5 (LL
+  // errors 4.4e-7 and 8.6e-7 on the 4096 x 32 and 1024 x 64 workloads)
+  static constexpr int kSlice3x = 4;
   // the 3xTF32 ring needs the room: it gathers emissions directly instead
   static constexpr bool kStageE = P != kTF32x3;
   static constexpr bool kEsSplit = P != kTF32x3 && W == kChainBN;  // see kEsLoCols
@@ -671,7 +671,7 @@ struct EpiHmmBwd : EpiNoHooks {
   using Params = HmmBwdParams;
   static constexpr int kEpiWarps = P == kTF32x3 ? 16 : 8;  // as EpiHmmFwd
   static constexpr int kSliceTF32 = 0;  // as EpiHmmFwd
-  static constexpr int kSlice3x = 2;    // as EpiHmmFwd
+  static constexpr int kSlice3x = 4;  // as EpiHmmFwd
   static constexpr bool kStageE = P != kTF32x3;
   static constexpr bool kEsSplit = P != kTF32x3 && W == kChainBN;  // see kEsLoCols
   static constexpr bool kStageOut = P == kBF16;                    // as EpiHmmFwd
@@ -935,10 +935,8 @@ pc_status_t check_hmm_shape(int H, int T, int V, int B) {
 }
 
 // The stacked dA contraction (one contraction over K = (T - 1) B, not a chain): in 3xTF32
-// it accumulates slices of one ring slot (4 k-steps, summed in registers, no correction),
-// whose truncation bias (~2.5e-7 of the result, measured on a layer) is far inside the
-// fp32 mode's 1e-5 flow bar for a single contraction, at a quarter of the one-k-step
-// slices' round trips.
+// it accumulates slices of one ring slot (4 k-steps, corrected as every 3xTF32 slice), at a
+// quarter of the one-k-step slices' round trips.
 struct EpiThetaScaleStacked : EpiThetaScale {
   static constexpr int kSlice3x = 4;
 };

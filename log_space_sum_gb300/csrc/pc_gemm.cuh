@@ -102,12 +102,13 @@ struct GemmShape {
 // Accumulation slices, in MMA k-steps (1 or 2, or a multiple of the k-steps of one ring
 // slot); see k_umma_gemm. The bf16 mode slices only where the epilogue asks for it
 // (Epi::kSliceBF16 k-steps; 0 = one accumulation over all of K). 3xTF32 slices one k-step
-// at a time unless the epilogue asks for two (Epi::kSlice3x): half the slices (HMM 4096
-// step 11.25 against 14.56 ms), but the second hi*hi product adds a truncation at the
-// partial sum's own magnitude, whose expected size depends on the data; its correction
-// (1.5 half ulps per slice) leaves a residual bias per contraction of up to ~2.5e-8 of
-// the sum (the HCLT-768 LL, 767 chained edges, moved by 8e-6, and by 1.9e-5 on uniform
-// emissions): fine for a chain of tens of layers, not for hundreds.
+// at a time unless the epilogue asks for more (Epi::kSlice3x: 2, or 4 = a ring slot):
+// fewer slices (HMM 4096 step 14.6, 10.8, 9.4 ms with 1, 2, 4), but every hi*hi product
+// after the slice's first adds a truncation at the partial sum's own magnitude, whose
+// expected size depends on the data; the correction for it (kCorrBits) leaves a residual
+// bias per contraction of up to ~2.5e-8 of the sum with two k-steps (the HCLT-768 LL, 767
+// chained edges, moved by 8e-6, and by 1.9e-5 on uniform emissions): fine for a chain of
+// tens of layers, not for hundreds.
 constexpr int kSliceK3x = 1;
 template <class E, class = void>
 struct EpiSlice3x : std::integral_constant<int, kSliceK3x> {};
@@ -284,7 +285,8 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
   static_assert(!kSliced || (kStepSliced ? S::kKSteps % kSliceK == 0 && (kSliceK == 1 || P == kTF32x3)
                                            : kSliceK % S::kKSteps == 0),
                 "slices are k-steps that divide a ring slot (several: 3xTF32) or whole ring slots");
-  constexpr int kAccBufs = !kSliced ? 1 : (kStepSliced && 4 * BN <= 512 ? 4 : 2);
+  // four slice buffers where TMEM holds them (k-step slices; 3xTF32 slot slices), else two
+  constexpr int kAccBufs = !kSliced ? 1 : ((kStepSliced || P == kTF32x3) && 4 * BN <= 512 ? 4 : 2);
   static_assert(!kBLo || (kSliced && !kStepSliced), "B lo parts with slot-granular slices");
   constexpr uint32_t kLoCol = kAccBufs * BN;  // the B_lo accumulator's first column
   constexpr uint32_t kTmemUsed = kAccBufs * BN + (kBLo ? BN : 0);
@@ -292,11 +294,15 @@ __global__ void __launch_bounds__(64 + EpiWarps<Epi>::value * 32, 1)
   constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                  : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM columns");
-  constexpr bool kHalfUlp = kStepSliced && P == kTF32x3;
-  static_assert(!kHalfUlp || kSliceK <= 2, "the truncation correction is that of one- or two-k-step slices");
+  constexpr bool kHalfUlp = kSliced && P == kTF32x3;
+  static_assert(!kHalfUlp || kSliceK <= 4, "the truncation correction is that of slices of up to one ring slot");
   // every fourth slice adds 4 half ulps (one-k-step slices: one truncation at the slice's
-  // magnitude) or 6 (two k-steps: that one plus one at about half of it)
-  constexpr uint32_t kCorrBits = kSliceK == 1 ? 0x34800000u : 0x34C00000u;  // 4 or 6 x 2^-24
+  // magnitude), 6 (two k-steps: that one plus one at about half of it) or 12 (a slot of
+  // four k-steps, hi*hi after the slot's cross terms: truncations at about a quarter, half,
+  // three quarters and all of the slice; 12 measured the least biased on the HMM chains,
+  // with a mean LL error of -3e-7 and -6e-7 on the 4096 x 32 and 1024 x 64 workloads,
+  // against -1.0e-6 / -2.0e-6 with 10 and -1.7e-6 / -3.3e-6 with 8)
+  constexpr uint32_t kCorrBits = kSliceK == 1 ? 0x34800000u : kSliceK == 2 ? 0x34C00000u : 0x35400000u;
   // split K: the idle ring holds the exchange buffer (128 x BN/2 floats), then the
   // epilogue's staged tiles
   constexpr int kXchgBytes = kBM * (BN / 2) * 4;
