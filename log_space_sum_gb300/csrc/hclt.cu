@@ -479,71 +479,62 @@ __global__ void k_hclt_cat_bucket(int nvars, int B, int C, const int* __restrict
   }
 }
 
-// dEt[v][k][z] = sum over the samples of node s with category k of f[s][b][z], one warp
-// per (node, category): every sample's row of f is read whole (4-byte runs of four
-// latents per lane, all of the warp's loads of a row in flight together) and the category's
-// row of dEt written whole, so both sides stream contiguous kilobytes; the transpose to
-// dE's [H][C] rows follows. Samples in bucket order (deterministic sums). H % 4 == 0.
-constexpr int kDERowWarps = 8;
-constexpr int kDERowRuns = 8;  // runs of four latents per lane and pass: 1024 latents
-__global__ void __launch_bounds__(kDERowWarps * 32) k_hclt_dE_rows(int n, int H, int B, int C,
-                                                                  const int* __restrict__ var_of_slot,
-                                                                  const int* __restrict__ order,
-                                                                  const int* __restrict__ off,
-                                                                  const float* __restrict__ F32,
-                                                                  float* __restrict__ dEt) {
-  const long long wid = static_cast<long long>(blockIdx.x) * kDERowWarps + (threadIdx.x >> 5);
-  if (wid >= static_cast<long long>(n) * C) return;
-  const int lane = threadIdx.x & 31;
-  const int s = static_cast<int>(wid / C), k = static_cast<int>(wid % C);
-  const int v = var_of_slot[s];
+// dE[v][z][k] (+)= sum over the samples of node s with category k of f[s][b][z], written
+// in dE's own [H][C] layout in one pass. A block takes 32 categories and 256 latents of
+// one node: each warp sums its categories' sample rows (bucket order, so the sums are
+// deterministic; lane l takes latents l, l + 32, ..., 128-byte loads per row) into a
+// shared-memory tile, and the block then writes the tile out latent by latent, the 32
+// categories of a latent (128 contiguous bytes) per warp store. f is read once and dE
+// written once, with no category-major copy between them.
+constexpr int kDETileC = 32;   // categories per block (one per lane on the way out)
+constexpr int kDETileZ = 256;  // latents per block
+constexpr int kDEWarps = 8;
+__global__ void __launch_bounds__(kDEWarps * 32) k_hclt_dE_tiles(int n, int H, int B, int C, int accumulate,
+                                                                const int* __restrict__ var_of_slot,
+                                                                const int* __restrict__ order,
+                                                                const int* __restrict__ off,
+                                                                const float* __restrict__ F32,
+                                                                float* __restrict__ dE) {
+  __shared__ float tile[kDETileC][kDETileZ + 1];  // odd row length: both phases conflict-free
+  __shared__ int bounds[kDETileC + 1];
+  constexpr int kRuns = kDETileZ / 32;
+  const long long zt = (H + kDETileZ - 1) / kDETileZ, ct = (C + kDETileC - 1) / kDETileC;
+  const long long blk = blockIdx.x;
+  const int z0 = static_cast<int>(blk % zt) * kDETileZ;
+  const int k0 = static_cast<int>((blk / zt) % ct) * kDETileC;
+  const int s = static_cast<int>(blk / (zt * ct));
+  if (s >= n) return;  // the whole block leaves together
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long ob = static_cast<long long>(s) * (C + 1);
-  const int e0 = off[ob + k], e1 = off[ob + k + 1];
+  if (threadIdx.x <= kDETileC) bounds[threadIdx.x] = off[ob + min(k0 + static_cast<int>(threadIdx.x), C)];
+  __syncthreads();
   const int* ord = order + static_cast<long long>(s) * B;
-  const int H4 = H / 4;
-  float4* dst = reinterpret_cast<float4*>(dEt + (static_cast<long long>(v) * C + k) * H);
-  for (int q0 = 0; q0 < H4; q0 += 32 * kDERowRuns) {
-    float4 acc[kDERowRuns];
+  const float* fs = F32 + static_cast<long long>(s) * B * H + z0;
+  const int zn = min(kDETileZ, H - z0);
+  for (int c = warp; c < kDETileC; c += kDEWarps) {
+    float acc[kRuns];
 #pragma unroll
-    for (int r = 0; r < kDERowRuns; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int e = e0; e < e1; ++e) {
-      const float4* row = reinterpret_cast<const float4*>(F32 + (static_cast<long long>(s) * B + ord[e]) * H);
-      float4 x[kDERowRuns];
+    for (int r = 0; r < kRuns; ++r) acc[r] = 0.f;
+    const int e1 = bounds[c + 1];
+    for (int e = bounds[c]; e < e1; ++e) {
+      const float* row = fs + static_cast<long long>(ord[e]) * H;
+      float x[kRuns];
 #pragma unroll
-      for (int r = 0; r < kDERowRuns; ++r) {
-        const int q = q0 + lane + 32 * r;
-        x[r] = q < H4 ? row[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int r = 0; r < kRuns; ++r) x[r] = lane + 32 * r < zn ? row[lane + 32 * r] : 0.f;
 #pragma unroll
-      for (int r = 0; r < kDERowRuns; ++r) {
-        acc[r].x += x[r].x;
-        acc[r].y += x[r].y;
-        acc[r].z += x[r].z;
-        acc[r].w += x[r].w;
-      }
+      for (int r = 0; r < kRuns; ++r) acc[r] += x[r];
     }
 #pragma unroll
-    for (int r = 0; r < kDERowRuns; ++r) {
-      const int q = q0 + lane + 32 * r;
-      if (q < H4) dst[q] = acc[r];
-    }
+    for (int r = 0; r < kRuns; ++r) tile[c][lane + 32 * r] = acc[r];
   }
-}
-
-// dEt[v][k][z] = sum over the samples of node s with category k of f[s][b][z].
-__global__ void k_hclt_dE_gather(int H, int B, int C, const int* __restrict__ var_of_slot,
-                                 const int* __restrict__ order, const int* __restrict__ off,
-                                 const float* __restrict__ F32, float* __restrict__ dEt) {
-  const int s = blockIdx.x, k = blockIdx.y;
-  const int v = var_of_slot[s];
-  const long long ob = static_cast<long long>(s) * (C + 1);
-  const int e0 = off[ob + k], e1 = off[ob + k + 1];
-  float* dst = dEt + (static_cast<long long>(v) * C + k) * H;
-  for (int z = threadIdx.x; z < H; z += blockDim.x) {
-    float acc = 0.f;
-    for (int e = e0; e < e1; ++e)
-      acc += F32[(static_cast<long long>(s) * B + order[static_cast<long long>(s) * B + e]) * H + z];
-    dst[z] = acc;
+  __syncthreads();
+  const int k = k0 + lane;
+  if (k >= C) return;
+  float* out = dE + static_cast<long long>(var_of_slot[s]) * H * C + static_cast<long long>(z0) * C + k;
+  for (int z = warp; z < zn; z += kDEWarps) {
+    const float v = tile[lane][z];
+    float* p = out + static_cast<long long>(z) * C;
+    *p = accumulate ? *p + v : v;
   }
 }
 
@@ -801,7 +792,7 @@ Operand operand_view(const Operand& op, pc_precision_t p, long long first, long 
 struct HcltWs {
   int* plan;
   Operand Wop, WopT, Uop, Gbm, Gnm, Unm;
-  float *Et, *U32, *D, *rroot, *rdot, *Lm, *F32, *dEt;
+  float *Et, *U32, *D, *rroot, *rdot, *Lm, *F32;
   long long u32_off = 0;  // elements between U32 and the first stored slot row
   int* Ex;
   int *cat_order, *cat_off;
@@ -849,9 +840,7 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
   w->u32_off = u32_root_only ? static_cast<long long>(n - 1) * B * H : 0;
   w->U32 = static_cast<float*>(c.take(size_t(u32_root_only ? 1 : n) * B * H * 4));
   w->Uop = c.operand(p, E1, B, H, 2);  // hi + lo in every mode (EpiHcltFwd::kBLo)
-  // n slots (one more than the edges need), so that dE's category-major rows (n x C x H)
-  // can reuse D when C <= B: D is dead once the last level's scaled flows have run
-  w->D = static_cast<float*>(c.take(size_t(n) * B * H * 4));
+  w->D = static_cast<float*>(c.take(size_t(E1) * B * H * 4));
   w->Ex = static_cast<int*>(c.take(size_t(n) * B * 4));
   w->Lm = static_cast<float*>(c.take(size_t(n) * B * 4));
   w->rroot = static_cast<float*>(c.take(size_t(B) * 4));
@@ -863,7 +852,6 @@ size_t carve_hclt(void* base, pc_precision_t p, int n, int H, int C, int B, bool
     w->Gnm = c.operand(p, E1, H, B);
     w->Unm = c.operand(p, E1, H, B);
     if (want_dE) {
-      w->dEt = C <= B ? w->D : static_cast<float*>(c.take(size_t(n) * C * H * 4));
       w->cat_order = static_cast<int*>(c.take(size_t(n) * B * 4));
       w->cat_off = static_cast<int*>(c.take(size_t(n) * (C + 1) * 4));
     }
@@ -1110,25 +1098,12 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
       k_hclt_cat_bucket<<<n, 32, size_t(C + 1) * 4, s>>>(n, B, C, data, d_var, w.cat_order, w.cat_off);
       PC_LAUNCH_CHECK();
     }
-    if (H % 4 == 0) {
-      // whole rows in, whole rows out, then the transpose
-      {
-        ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + n * CH * 4);
-        k_hclt_dE_rows<<<cdiv(static_cast<long long>(n) * C, kDERowWarps), kDERowWarps * 32, 0, s>>>(
-            n, H, B, C, d_var, w.cat_order, w.cat_off, w.F32, w.dEt);
-        PC_LAUNCH_CHECK();
-      }
-      ProfileScope ps(s, PC_KIND_HCLT_MEM, (accumulate ? 3ll : 2ll) * n * CH * 4);
-      return transpose_f32(w.dEt, H, static_cast<long long>(C) * H, n, C, H, dE, C, accumulate, s);
-    }
-    {
-      ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + n * CH * 4);
-      k_hclt_dE_gather<<<dim3(n, C), 256, 0, s>>>(H, B, C, d_var, w.cat_order, w.cat_off, w.F32, w.dEt);
-      PC_LAUNCH_CHECK();
-    }
-    ProfileScope ps(s, PC_KIND_HCLT_MEM, (accumulate ? 3ll : 2ll) * n * CH * 4);
-    if ((st = transpose_f32(w.dEt, H, static_cast<long long>(C) * H, n, C, H, dE, C, accumulate, s)) != PC_OK)
-      return st;
+    ProfileScope ps(s, PC_KIND_HCLT_MEM, n * BH * 4 + n * B * 4ll + (accumulate ? 2ll : 1ll) * n * CH * 4);
+    // at most 65535 x 256 x 32 blocks (the shape limits)
+    const long long blocks = static_cast<long long>(n) * cdiv(C, kDETileC) * cdiv(H, kDETileZ);
+    k_hclt_dE_tiles<<<static_cast<unsigned>(blocks), kDEWarps * 32, 0, s>>>(n, H, B, C, accumulate, d_var,
+                                                                            w.cat_order, w.cat_off, w.F32, dE);
+    PC_LAUNCH_CHECK();
   }
   return PC_OK;
 }

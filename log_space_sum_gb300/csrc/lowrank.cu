@@ -204,6 +204,43 @@ __global__ void k_lr_to_op(const float* __restrict__ src, long long sg, long lon
   }
 }
 
+// The same copy for a source contiguous along c (sc = 1) with C, sr and sg multiples of
+// four and a 16-byte aligned base: four columns per thread (16-byte loads, 8- or 16-byte
+// stores), so a rank-16 row takes four threads rather than half a warp of scalar loads.
+// Rounds each value exactly as the element-wise copy does.
+template <int F>
+__global__ void k_lr_to_op4(const float* __restrict__ src, long long sg, long long sr, int R, int C4, long long rows,
+                            void* __restrict__ hi, void* __restrict__ lo, long long ld) {
+  const long long total = rows * C4;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long gr = i / C4;
+    const int q = static_cast<int>(i - gr * C4);
+    const long long g = gr / R, r = gr - g * R;
+    const float4 v4 = *reinterpret_cast<const float4*>(src + g * sg + r * sr + 4 * q);
+    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    const long long idx = gr * ld + 4 * q;
+    if constexpr (F == kFmtBF16 || F == kFmtBF16x2) {
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v[k]);
+        h[k] = __bfloat16_as_ushort(b);
+        l[k] = __bfloat16_as_ushort(__float2bfloat16_rn(v[k] - __bfloat162float(b)));
+      }
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(hi) + idx) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+      if constexpr (F == kFmtBF16x2)
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(lo) + idx) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+    } else {
+      const float4 h = make_float4(tf32_rna(v[0]), tf32_rna(v[1]), tf32_rna(v[2]), tf32_rna(v[3]));
+      *reinterpret_cast<float4*>(static_cast<float*>(hi) + idx) = h;
+      if constexpr (F == kFmtTF32x2)
+        *reinterpret_cast<float4*>(static_cast<float*>(lo) + idx) =
+            make_float4(tf32_rna(v[0] - h.x), tf32_rna(v[1] - h.y), tf32_rna(v[2] - h.z), tf32_rna(v[3] - h.w));
+    }
+  }
+}
+
 // The same copy where the source is contiguous along r (sr = 1) and strided along c: a
 // 32 x 32 tile goes through shared memory, so that both the reads (along r) and the
 // writes (along c) are coalesced.
@@ -927,7 +964,8 @@ LrOp carve_op(Carver& c, int F, long long groups, long long rows, long long cols
 struct LrWs {
   float* m;
   Operand u;                            // [B][N] exp(x - m_b), padded rows
-  Operand theta, thetaT;                // plain float32 copies, padded rows
+  Operand theta, thetaT;                // float32 theta (the caller's rows when 16-byte aligned,
+                                        // else a padded copy) and a padded transposed copy
   Operand rf_lz, rf_f, rf_fc;           // [B][M] backward row factors
   LrOp Aop, BTop;                       // A_b rows, B_b^T rows (format of S)
   LrOp Bg, AgT;                         // B_b rows, A_b^T rows (format of the gradients)
@@ -983,6 +1021,13 @@ pc_status_t to_op(const float* src, long long sg, long long sr, long long sc, in
     return PC_OK;
   }
   const long long rows = static_cast<long long>(G) * R;
+  if (sc == 1 && C % 4 == 0 && sr % 4 == 0 && sg % 4 == 0 && aligned16(src) && o.part[0].ld % 4 == 0) {
+    const int blocks = static_cast<int>(std::min<long long>(cdiv(rows * (C / 4), 256), 65535));
+    k_lr_to_op4<F><<<blocks, 256, 0, s>>>(src, sg, sr, R, C / 4, rows, o.part[0].ptr,
+                                          o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
+    PC_LAUNCH_CHECK();
+    return PC_OK;
+  }
   const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, 8), 8192));
   k_lr_to_op<F><<<blocks, dim3(32, 8), 0, s>>>(src, sg, sr, sc, G, R, C, o.part[0].ptr,
                                                o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
@@ -999,15 +1044,21 @@ pc_status_t encode_op(CUtensorMap (&maps)[2], const LrOp& o, int box_rows) {
   return PC_OK;
 }
 
-// Set-up shared by both passes: m, u, the theta copies and the operand copies of A, B.
+// Set-up shared by both passes: m, u, theta's tensor-map rows (and its transposed copy) and
+// the operand copies of A, B.
 template <int P>
 pc_status_t lr_prepare(const float* theta, const float* A, const float* Bm, const float* x, int M, int N, int K,
                        int B, bool bwd, LrWs& w, cudaStream_t s) {
   k_lr_colmax_u<<<B, 256, 0, s>>>(N, B, x, w.m, static_cast<float*>(w.u.ptr), w.u.ld);
   PC_LAUNCH_CHECK();
   const dim3 g(cdiv(N, 32), cdiv(M, 32));
-  k_lr_theta_copy<<<g, dim3(32, 8), 0, s>>>(M, N, theta, static_cast<float*>(w.theta.ptr), w.theta.ld, 0);
-  PC_LAUNCH_CHECK();
+  if (N % 4 == 0 && aligned16(theta)) {  // theta's own rows are a tensor map's rows: no copy
+    w.theta.ptr = const_cast<float*>(theta);
+    w.theta.ld = N;
+  } else {
+    k_lr_theta_copy<<<g, dim3(32, 8), 0, s>>>(M, N, theta, static_cast<float*>(w.theta.ptr), w.theta.ld, 0);
+    PC_LAUNCH_CHECK();
+  }
   const long long MK = static_cast<long long>(M) * K, KN = static_cast<long long>(K) * N;
   pc_status_t st;
   if ((st = to_op<s_fmt(P)>(A, MK, K, 1, B, M, K, w.Aop, s)) != PC_OK) return st;    // A_b[i][k]

@@ -80,7 +80,7 @@ def test_forward_only_and_accumulate():
 def test_latents_a_multiple_of_four(mode):
     # H % 4 == 0 but H % 8 != 0 and off the tile sizes: the parameter flows take the
     # persistent tiles with the theta ring (partial chunks), the element flows the staged
-    # 128-wide tiles (bf16: u from the operand's hi and lo parts), dE the whole-row sums;
+    # 128-wide tiles (bf16: u from the operand's hi and lo parts), dE a partial latent tile;
     # then accumulation, whose persistent epilogue adds with one reduction per element
     d = hclt_inputs(40, 100, 17, 45, seed=207)
     rl, rpi, rW, rE = _oracle(d)
@@ -165,7 +165,7 @@ def test_more_than_1024_latents():
 
 
 def test_more_than_1024_categories():
-    # C > 1024 takes the gather-then-transpose dE path instead of the direct one
+    # C > 1024: 35 category tiles of dE per variable, the last one partial (12 of 32)
     d = hclt_inputs(5, 64, 1100, 20, seed=204, parent=np.array([-1, 0, 0, 1, 2], dtype=np.int32))
     rl, rpi, rW, rE = _oracle(d)
     for mode in ("auto", "fp32"):

@@ -140,3 +140,27 @@ def test_edge_cases():
         pc.lowrank_exp_sum_fwd(t["theta"], t["A"][:, :, :0].contiguous(), t["Bm"][:, :0].contiguous(), t["x"])
     with pytest.raises(pc.PCError, match="UNKNOWN_PRECISION"):
         pc.lowrank_exp_sum_fwd(t["theta"], t["A"], t["Bm"], t["x"], precision=7)
+
+
+def test_theta_alignment_paths_agree():
+    # theta's own rows feed the passes' tensor maps when they are 16-byte aligned (N % 4
+    # == 0), through a padded copy otherwise: a theta stored 4 bytes off alignment takes
+    # the copy, and every output keeps the same bits
+    d = lowrank_inputs(130, 100, 16, 3, 1.0, seed=320, f_kind="uniform")
+    t = _cuda(d)
+    buf = torch.empty(t["theta"].numel() + 1, dtype=torch.float32, device="cuda")
+    shifted = buf[1:].view(t["theta"].shape)
+    shifted.copy_(t["theta"])
+    assert shifted.data_ptr() % 16 != 0 and t["theta"].data_ptr() % 16 == 0
+    for mode in MODES:
+        res = []
+        for th in (t["theta"], shifted):
+            out, logZ = pc.lowrank_exp_sum_fwd(th, t["A"], t["Bm"], t["x"], precision=mode)
+            g = pc.lowrank_exp_sum_bwd(th, t["A"], t["Bm"], t["x"], out, logZ, t["f"], precision=mode)
+            res.append((out, logZ, g))
+        torch.cuda.synchronize()
+        pc.device_status()
+        (o1, z1, g1), (o2, z2, g2) = res
+        assert torch.equal(o1, o2) and torch.equal(z1, z2), mode
+        for k in g1:
+            assert torch.equal(g1[k], g2[k]), (mode, k)
