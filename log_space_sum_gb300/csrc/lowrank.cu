@@ -278,7 +278,7 @@ __global__ void k_lr_to_op_t(const float* __restrict__ src, long long sg, long l
 enum : int { kLrStats = 3 };
 constexpr int kThetaTileBytes = kLrRows * 128;  // 128 rows x 32 floats
 constexpr int kLrWarps = 8;                      // consumers: two warps per TMEM lane quarter
-constexpr int kLrThreadsAll = (kLrWarps + 1) * 32;  // + one issuer warp (TMA and MMAs)
+constexpr int kLrThreadsFused = (kLrWarps + 2) * 32;  // + a TMA producer warp and an MMA warp
 constexpr float kLog2e = 1.4426950408889634f;
 
 __host__ __device__ constexpr int lr_stages(int mode) { return mode == kLrFwd ? 3 : 4; }
@@ -289,13 +289,15 @@ __host__ __device__ constexpr int lr_nvec(int mode) { return mode == kLrGradB ? 
 struct LrSmem {
   int own, own_bytes;              // resident own tile (not the statistics pass)
   int stage, stage_bytes, nstage;  // ring of TMA stages
-  int sw_off, th_off, gb_off, vec_off;
-  int sw_bytes, gb_bytes, tx_bytes;
+  int sw_off, th_off, vec_off;
+  int sw_bytes, tx_bytes;
+  int gbr, gb_bytes, ngb;          // ring of ngb gradient B-operand tiles (gradient passes)
   int d, d_bytes, nd;              // ring of nd D tiles (gradient passes)
   int bars, total;
 };
+constexpr int kGbSlots = 4;  // gradient B-operand tiles in flight at most
 __host__ __device__ inline int up1024(int v) { return (v + 1023) & ~1023; }
-__host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstage, int nd) {
+__host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstage, int nd, int ngb) {
   const int SF = s_fmt(P), GF = g_fmt(P);
   const int Kp = (K + 15) & ~15;
   const bool grad = mode == kLrGradA || mode == kLrGradB;
@@ -305,24 +307,25 @@ __host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstag
   s.gb_bytes = grad ? fmt_parts(GF) * Kp * 128 : 0;
   s.nstage = nstage;
   s.nd = nd;
+  s.ngb = grad ? ngb : 0;
   int off = 0;
   if (mode == kLrStats) off += s.own_bytes;  // the sample's own tile travels with its stage
   s.sw_off = off;
   off += s.sw_bytes;
   s.th_off = off;
   if (mode != kLrStats) off += kThetaTileBytes;
-  s.gb_off = off;
-  off += s.gb_bytes;
   s.vec_off = off;
   off += up1024(lr_nvec(mode) * 128);
   s.stage_bytes = up1024(off);
   s.tx_bytes = (mode == kLrStats ? s.own_bytes : 0) + s.sw_bytes + (mode != kLrStats ? kThetaTileBytes : 0) +
-               s.gb_bytes + lr_nvec(mode) * 128;
+               lr_nvec(mode) * 128;
   off = 0;
   s.own = off;
   if (mode != kLrStats) off += s.own_bytes;
   s.stage = off;
   off += s.nstage * s.stage_bytes;
+  s.gbr = off;  // gb_bytes is a multiple of 2048
+  off += s.ngb * s.gb_bytes;
   s.d_bytes = grad ? tile_bytes(GF, kLrRows, kLrChunk) : 0;
   s.d = off;
   off += nd * s.d_bytes;
@@ -342,13 +345,14 @@ __host__ __device__ inline LrSmem lr_smem(int P, int mode, int K) {
   if (mode != kLrFwd)
     for (int ns = 3; ns >= 2; --ns)
       for (int d = 2; d >= 1; --d) {
-        const LrSmem h = lr_smem_plan(P, mode, K, ns, d);
+        const LrSmem h = lr_smem_plan(P, mode, K, ns, d, kGbSlots);
         if (h.total <= kLrSmemHalf) return h;
       }
-  int nstage = lr_stages(mode), nd = 2;
-  LrSmem s = lr_smem_plan(P, mode, K, nstage, nd);
-  while (s.total > kLrSmemLimit && nstage > 2) s = lr_smem_plan(P, mode, K, --nstage, nd);
-  if (s.total > kLrSmemLimit) s = lr_smem_plan(P, mode, K, nstage, nd = 1);
+  int nstage = lr_stages(mode), nd = 2, ngb = kGbSlots;
+  LrSmem s = lr_smem_plan(P, mode, K, nstage, nd, ngb);
+  while (s.total > kLrSmemLimit && nstage > 2) s = lr_smem_plan(P, mode, K, --nstage, nd, ngb);
+  if (s.total > kLrSmemLimit) s = lr_smem_plan(P, mode, K, nstage, nd = 1, ngb);
+  while (s.total > kLrSmemLimit && ngb > 1) s = lr_smem_plan(P, mode, K, nstage, nd, ngb /= 2);
   return s;
 }
 
@@ -447,16 +451,21 @@ __device__ __forceinline__ void tile_put_row16(uint8_t* tile, const TileGeo& g, 
 
 // One pass (forward, grad A or grad B) over the tile of 128 own rows of sample
 // blockIdx.y; see the file comment. Warp specialised, with mbarrier hand-offs only:
-//   warp 8, one thread: the TMA loads (a ring of R chunk stages) and every MMA;
+//   warp 8, one thread: the TMA loads (a ring of R chunk stages), ahead of the MMAs;
+//   warp 9, one thread: every MMA;
 //   warps 0..7: consumers; warp w reads TMEM lane quarter w & 3 and handles columns
 //   16 (w >> 2) .. +15 of every 32-column chunk.
-// Barriers: mbT[stage] chunk landed; mbS[c & 1] S of chunk c in TMEM; mbF[c & 1] all eight
-// consumer warps are done with chunk c's S slot and stage; mbDf[c & 1] chunk c's D tile is
-// written; mbG[c & 1] the gradient MMA of chunk c is done.
+// (With one thread doing both, each chunk's copy was issued only after the previous
+// chunk's MMA and then waited for at once: copy, MMA and hand-off ran in series, and the
+// consumers sat idle half of every chunk.)
+// Barriers: mbT[stage] chunk landed; mbE[stage] the consumers are done with the stage;
+// mbGT / mbGE[slot] a gradient B-operand tile landed / read by its MMA; mbS[c & 1] S of
+// chunk c in TMEM; mbF[c & 1] all eight consumer warps are done with chunk c's S slot;
+// mbDf[c & 1] chunk c's D tile is written; mbG[c & 1] the gradient MMA of chunk c is done.
 // (The forward's shared memory leaves room for two CTAs per SM; its launch bounds ask the
 // compiler for registers that allow two as well.)
 template <int P, int Mode>
-__global__ void __launch_bounds__(kLrThreadsAll, 2)
+__global__ void __launch_bounds__(kLrThreadsFused, 2)
     k_lowrank(const __grid_constant__ LrMaps maps, const LrArgs a) {
   constexpr int SF = s_fmt(P), GF = g_fmt(P);
   constexpr bool kGrad = Mode != kLrFwd;
@@ -469,7 +478,6 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
   const int b = blockIdx.y;
   const int o0 = blockIdx.x * kLrRows;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const bool issuer = warp == kLrWarps;
   const int quarter = warp & 3, half = (warp >> 2) & 1;
   const int row = quarter * 32 + lane;  // own row in the tile (TMEM lane)
   const int col0 = half * 16;           // this thread's columns of a chunk
@@ -477,7 +485,7 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
   const TileGeo go = tile_geo(SF, kLrRows, K), gs = tile_geo(SF, kLrChunk, K);
   const TileGeo gd = tile_geo(GF, kLrRows, kLrChunk), gg = tile_geo(GF, Kp, kLrChunk);
   const LrSmem L = lr_smem(P, Mode, K);
-  const int R = L.nstage, ND = L.nd;
+  const int R = L.nstage, ND = L.nd, NG = L.ngb;
   // TMEM: two 32-column S slots, then (gradients) kGradAccs accumulators of gstride
   // columns that the chunks take in turn: each sums a quarter of the sweep, which keeps
   // the accumulator's truncations to a quarter; the epilogue adds them up.
@@ -494,14 +502,23 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
   uint64_t* mbDf = mbF + 2;                                     // [2]
   uint64_t* mbG = mbDf + 2;                                     // [2]
   uint64_t* mbO = mbG + 2;                                      // own tile landed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbO + 1);
+  uint64_t* mbE = mbO + 1;                                      // [R <= 4] stage free
+  uint64_t* mbGT = mbE + 4;                                     // [NG <= 4] B-operand tile landed
+  uint64_t* mbGE = mbGT + 4;                                    // [NG <= 4] B-operand tile free
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbGE + 4);
   float* merge = reinterpret_cast<float*>(smem + L.bars + 256);  // [3][128]
   auto stage = [&](int c) { return smem + L.stage + (c % R) * L.stage_bytes; };
   auto d_tile = [&](int c) { return smem + L.d + (c % ND) * L.d_bytes; };
+  auto gb_tile = [&](int c) { return smem + L.gbr + (c % NG) * L.gb_bytes; };
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < 4; ++i) mbar_init(&mbT[i], 1);
+      for (int i = 0; i < 4; ++i) {
+        mbar_init(&mbT[i], 1);
+        mbar_init(&mbE[i], kLrWarps);
+        mbar_init(&mbGT[i], 1);
+        mbar_init(&mbGE[i], 1);
+      }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&mbS[i], 1);
         mbar_init(&mbF[i], kLrWarps);
@@ -521,9 +538,17 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
   const int nch = (sw_n + kLrChunk - 1) / kLrChunk;
   bool ok = true;
 
-  if (issuer) {
+  // Each barrier below has one waiter role, and no role can fall two phases behind on a
+  // barrier it waits on (the phase after the one it waits for needs the waiter's own next
+  // step), so a parity wait never aliases onto a later phase.
+  if (warp == kLrWarps) {
+    // -------------------------------------------------------------- TMA producer
+    // Runs ahead of the MMAs as far as the rings allow: chunk c's stage is refilled as
+    // soon as the consumers of chunk c - R have released it (mbE), and its gradient
+    // B-operand tile, which only the gradient MMA reads, travels in a ring of its own
+    // (mbGT landed, mbGE read), so a stage never waits for a gradient MMA.
     if (lane == 0) {
-      int issued = -1, s_issued = -1, g_issued = -1;
+      int issued = -1, gb_issued = -1;
       auto issue_tma = [&](int c) {
         uint8_t* st = stage(c);
         uint64_t* bar = &mbT[c % R];
@@ -534,41 +559,61 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
             tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
                         kb * (128 / esS), w0, b);
         tma_load_3d(st + L.th_off, &maps.th, bar, w0, o0, 0);
-        if constexpr (kGrad)
-          for (int part = 0; part < fmt_parts(GF); ++part)
-            tma_load_3d(st + L.gb_off + part * gg.bytes_part(), &maps.gb[part], bar, w0, 0, b);
         for (int v = 0; v < kNvec; ++v) tma_load_3d(st + L.vec_off + v * 128, &maps.vec[v], bar, w0, b, 0);
         issued = c;
       };
-      auto issue_grad = [&](int c) {  // the D tile of chunk c is written
-        ok = ok && mbar_wait(&mbDf[c & 1], (c >> 1) & 1, a.status, kErrTimeoutMma);
-        if (!ok) return;
-        tc_fence_after();
-        lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(c), gd, stage(c) + L.gb_off,
-                   gg, Kp, c >= kGradAccs);
-        umma_commit(&mbG[c & 1]);
-        g_issued = c;
+      auto issue_gb = [&](int c) {
+        uint64_t* bar = &mbGT[c % NG];
+        mbar_arrive_expect_tx(bar, L.gb_bytes);
+        for (int part = 0; part < fmt_parts(GF); ++part)
+          tma_load_3d(gb_tile(c) + part * gg.bytes_part(), &maps.gb[part], bar, c * kLrChunk, 0, b);
+        gb_issued = c;
       };
-      const int lag = R >= 3 ? 2 : 1;  // refill the stage of chunk c - lag
       mbar_arrive_expect_tx(mbO, L.own_bytes);
       for (int part = 0; part < fmt_parts(SF); ++part)
         for (int kb = 0; kb < go.kblocks; ++kb)
           tma_load_3d(own_tile + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], mbO,
                       kb * (128 / esS), o0, b);
-      for (int c = 0; c < R && c < nch; ++c) issue_tma(c);
-      ok = mbar_wait(mbO, 0, a.status, kErrTimeoutMma);
-      // Waits once for the consumers to be done with chunk p. A parity wait must not be
-      // repeated: by then the barrier may have completed the next chunk's phase too.
-      int f_seen = -1;
-      auto wait_consumed = [&](int p) {
-        if (p <= f_seen) return;
-        ok = ok && mbar_wait(&mbF[p & 1], (p >> 1) & 1, a.status, kErrTimeoutMma);
-        if (ok) f_seen = p;
+      for (int c = 0; c < nch; ++c) {
+        if (c >= R) ok = mbar_wait(&mbE[c % R], ((c / R) - 1) & 1, a.status, kErrTimeoutMma);
+        if (!ok) break;
+        issue_tma(c);
+        if constexpr (kGrad) {
+          if (c >= NG) ok = mbar_wait(&mbGE[c % NG], ((c / NG) - 1) & 1, a.status, kErrTimeoutMma);
+          if (!ok) break;
+          issue_gb(c);
+        }
+      }
+      if (!ok) {
+        // a wait gave up: let the copies in flight land before the block exits
+        mbar_wait(mbO, 0, a.status, kErrTimeoutDrain);
+        for (int c = issued; c >= 0 && c > issued - R; --c)
+          mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutDrain);
+        for (int c = gb_issued; c >= 0 && c > gb_issued - NG; --c)
+          mbar_wait(&mbGT[c % NG], (c / NG) & 1, a.status, kErrTimeoutDrain);
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+  } else if (warp == kLrWarps + 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int s_issued = -1, g_issued = -1;
+      auto issue_grad = [&](int c) {  // the D tile of chunk c is written, its B-operand landed
+        ok = ok && mbar_wait(&mbDf[c & 1], (c >> 1) & 1, a.status, kErrTimeoutMma) &&
+             mbar_wait(&mbGT[c % NG], (c / NG) & 1, a.status, kErrTimeoutMma);
+        if (!ok) return;
+        tc_fence_after();
+        lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(c), gd, gb_tile(c), gg, Kp,
+                   c >= kGradAccs);
+        umma_commit(&mbG[c & 1]);
+        umma_commit(&mbGE[c % NG]);  // the B-operand tile has been read
+        g_issued = c;
       };
+      ok = mbar_wait(mbO, 0, a.status, kErrTimeoutMma);
       for (int c = 0; c < nch && ok; ++c) {
         ok = mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutMma);
         // the TMEM slot of chunk c - 2 is free once its consumers are done
-        if (ok && c >= 2) wait_consumed(c - 2);
+        if (ok && c >= 2) ok = mbar_wait(&mbF[c & 1], ((c - 2) >> 1) & 1, a.status, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         lr_mma<SF>(tmem + static_cast<uint32_t>((c & 1) * kLrChunk), own_tile, go, stage(c) + L.sw_off, gs, kLrChunk,
@@ -578,19 +623,10 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
         if constexpr (kGrad) {
           if (c >= 1) issue_grad(c - 1);
         }
-        const int p = c - lag;
-        if (ok && p >= 0 && p + R < nch) {
-          wait_consumed(p);
-          if (kGrad && ok) ok = mbar_wait(&mbG[p & 1], (p >> 1) & 1, a.status, kErrTimeoutMma);
-          if (ok) issue_tma(p + R);
-        }
       }
       if (kGrad && ok && nch > 0) issue_grad(nch - 1);
       if (!ok) {
-        // a wait gave up: let the copies and MMAs in flight finish before TMEM is freed
-        mbar_wait(mbO, 0, a.status, kErrTimeoutDrain);
-        for (int c = issued; c >= 0 && c > issued - R; --c)
-          mbar_wait(&mbT[c % R], (c / R) & 1, a.status, kErrTimeoutDrain);
+        // a wait gave up: let the MMAs in flight finish before TMEM is freed
         if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
         if (g_issued >= 0) mbar_wait(&mbG[g_issued & 1], (g_issued >> 1) & 1, a.status, kErrTimeoutDrain);
       }
@@ -641,7 +677,10 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&mbF[c & 1]);
+        if (lane == 0) {
+          mbar_arrive(&mbF[c & 1]);
+          mbar_arrive(&mbE[c % R]);
+        }
       };
       const int w0 = c * kLrChunk + col0;
       if constexpr (Mode == kLrFwd) {
@@ -775,16 +814,15 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
 // Parameter-flow statistics F+ and W over all samples for the 128 x 32 tile (blockIdx.x,
 // blockIdx.y) of [M, N]: own rows i, the 32 columns j fixed, a sweep over the samples.
 // Each stage of the TMA ring holds one sample's A_b tile, its B_b^T chunk and u_b. Warp
-// specialised as k_lowrank: warp 8 issues the copies and the MMAs, warps 0..7 consume.
+// specialised as k_lowrank: warp 8 issues the copies, warp 9 the MMAs, warps 0..7 consume.
 template <int P>
-__global__ void __launch_bounds__(kLrThreadsAll, 2)
+__global__ void __launch_bounds__(kLrThreadsFused, 2)
     k_lowrank_stats(const __grid_constant__ LrMaps maps, const LrArgs a) {
   constexpr int SF = s_fmt(P);
   constexpr int esS = fmt_bytes(SF);
   const int K = a.K;
   const int i0 = blockIdx.x * kLrRows, j0 = blockIdx.y * kLrChunk;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const bool issuer = warp == kLrWarps;
   const int quarter = warp & 3, half = (warp >> 2) & 1;
   const int row = quarter * 32 + lane;
   const int col0 = half * 16;
@@ -798,12 +836,16 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
   uint64_t* mbT = reinterpret_cast<uint64_t*>(smem + L.bars);  // [R <= 4]
   uint64_t* mbS = mbT + 4;                                      // [2]
   uint64_t* mbF = mbS + 2;                                      // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbF + 2);
+  uint64_t* mbE = mbF + 2;                                      // [R <= 4] stage free
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbE + 4);
   auto stage = [&](int b) { return smem + L.stage + (b % R) * L.stage_bytes; };
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int s = 0; s < 4; ++s) mbar_init(&mbT[s], 1);
+      for (int s = 0; s < 4; ++s) {
+        mbar_init(&mbT[s], 1);
+        mbar_init(&mbE[s], kLrWarps);
+      }
       for (int s = 0; s < 2; ++s) {
         mbar_init(&mbS[s], 1);
         mbar_init(&mbF[s], kLrWarps);
@@ -819,9 +861,11 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
   const uint32_t tmem = *tslot;
   bool ok = true;
 
-  if (issuer) {
+  // The same roles as k_lowrank: a TMA producer that refills a stage as soon as its
+  // consumers release it (mbE), and an MMA warp.
+  if (warp == kLrWarps) {
     if (lane == 0) {
-      int issued = -1, s_issued = -1;
+      int issued = -1;
       auto issue_tma = [&](int b) {
         uint8_t* st = stage(b);
         uint64_t* bar = &mbT[b % R];
@@ -837,34 +881,31 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
         tma_load_3d(st + L.vec_off, &maps.vec[0], bar, j0, b, 0);
         issued = b;
       };
-      const int lag = R >= 3 ? 2 : 1;
-      for (int b = 0; b < R && b < a.B; ++b) issue_tma(b);
-      int f_seen = -1;  // as in k_lowrank: one wait per sample's consumer phase
-      auto wait_consumed = [&](int p) {
-        if (p <= f_seen) return;
-        ok = ok && mbar_wait(&mbF[p & 1], (p >> 1) & 1, a.status, kErrTimeoutMma);
-        if (ok) f_seen = p;
-      };
+      for (int b = 0; b < a.B; ++b) {
+        if (b >= R) ok = mbar_wait(&mbE[b % R], ((b / R) - 1) & 1, a.status, kErrTimeoutMma);
+        if (!ok) break;
+        issue_tma(b);
+      }
+      if (!ok)
+        for (int b = issued; b >= 0 && b > issued - R; --b)
+          mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutDrain);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+  } else if (warp == kLrWarps + 1) {
+    if (lane == 0) {
+      int s_issued = -1;
       for (int b = 0; b < a.B && ok; ++b) {
         ok = mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutMma);
-        if (ok && b >= 2) wait_consumed(b - 2);
+        // the TMEM slot of sample b - 2 is free once its consumers are done
+        if (ok && b >= 2) ok = mbar_wait(&mbF[b & 1], ((b - 2) >> 1) & 1, a.status, kErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         lr_mma<SF>(tmem + static_cast<uint32_t>((b & 1) * kLrChunk), stage(b), go, stage(b) + L.sw_off, gs,
                    kLrChunk, false);
         umma_commit(&mbS[b & 1]);
         s_issued = b;
-        const int p = b - lag;
-        if (p >= 0 && p + R < a.B) {
-          wait_consumed(p);
-          if (ok) issue_tma(p + R);
-        }
       }
-      if (!ok) {
-        for (int b = issued; b >= 0 && b > issued - R; --b)
-          mbar_wait(&mbT[b % R], (b / R) & 1, a.status, kErrTimeoutDrain);
-        if (s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
-      }
+      if (!ok && s_issued >= 0) mbar_wait(&mbS[s_issued & 1], (s_issued >> 1) & 1, a.status, kErrTimeoutDrain);
     }
     ok = __all_sync(0xffffffffu, ok);
   } else {
@@ -918,7 +959,10 @@ __global__ void __launch_bounds__(kLrThreadsAll, 2)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&mbF[b & 1]);
+      if (lane == 0) {
+        mbar_arrive(&mbF[b & 1]);
+        mbar_arrive(&mbE[b % R]);
+      }
       lz = nlz;
       fi = nfi;
       fc = nfc;
@@ -1103,7 +1147,7 @@ pc_status_t lr_fwd(int M, int N, int K, int B, const float* theta, const float* 
   const int smem = lr_smem(P, kLrFwd, K).total;
   if ((st = lr_attr(k_lowrank<P, kLrFwd>, smem)) != PC_OK) return st;
   const int slot = profile_begin(s);
-  k_lowrank<P, kLrFwd><<<dim3(cdiv(M, kLrRows), B), kLrThreadsAll, smem, s>>>(maps, a);
+  k_lowrank<P, kLrFwd><<<dim3(cdiv(M, kLrRows), B), kLrThreadsFused, smem, s>>>(maps, a);
   PC_LAUNCH_CHECK();
   profile_end(slot, s, PC_KIND_LOWRANK_FWD, 2LL * M * N * K * B);
   return PC_OK;
@@ -1157,7 +1201,7 @@ pc_status_t lr_bwd(int M, int N, int K, int B, const float* theta, const float* 
     const int smem = lr_smem(P, kLrGradA, K).total;
     if ((st = lr_attr(k_lowrank<P, kLrGradA>, smem)) != PC_OK) return st;
     const int slot = profile_begin(s);
-    k_lowrank<P, kLrGradA><<<dim3(cdiv(M, kLrRows), B), kLrThreadsAll, smem, s>>>(maps, a);
+    k_lowrank<P, kLrGradA><<<dim3(cdiv(M, kLrRows), B), kLrThreadsFused, smem, s>>>(maps, a);
     PC_LAUNCH_CHECK();
     profile_end(slot, s, PC_KIND_LOWRANK_BWD, 2 * flops);
   }
@@ -1173,7 +1217,7 @@ pc_status_t lr_bwd(int M, int N, int K, int B, const float* theta, const float* 
     const int smem = lr_smem(P, kLrGradB, K).total;
     if ((st = lr_attr(k_lowrank<P, kLrGradB>, smem)) != PC_OK) return st;
     const int slot = profile_begin(s);
-    k_lowrank<P, kLrGradB><<<dim3(cdiv(N, kLrRows), B), kLrThreadsAll, smem, s>>>(maps, a);
+    k_lowrank<P, kLrGradB><<<dim3(cdiv(N, kLrRows), B), kLrThreadsFused, smem, s>>>(maps, a);
     PC_LAUNCH_CHECK();
     profile_end(slot, s, PC_KIND_LOWRANK_BWD, 2 * flops);
   }
@@ -1187,7 +1231,7 @@ pc_status_t lr_bwd(int M, int N, int K, int B, const float* theta, const float* 
     const int smem = lr_smem(P, kLrStats, K).total;
     if ((st = lr_attr(k_lowrank_stats<P>, smem)) != PC_OK) return st;
     const int slot = profile_begin(s);
-    k_lowrank_stats<P><<<dim3(cdiv(M, kLrRows), cdiv(N, kLrChunk)), kLrThreadsAll, smem, s>>>(maps, a);
+    k_lowrank_stats<P><<<dim3(cdiv(M, kLrRows), cdiv(N, kLrChunk)), kLrThreadsFused, smem, s>>>(maps, a);
     PC_LAUNCH_CHECK();
     profile_end(slot, s, PC_KIND_LOWRANK_BWD, flops);
   }
