@@ -328,7 +328,8 @@ __host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstag
   off += s.ngb * s.gb_bytes;
   s.d_bytes = grad ? tile_bytes(GF, kLrRows, kLrChunk) : 0;
   s.d = off;
-  off += nd * s.d_bytes;
+  // bf16 D tiles fill half of each 128-byte row: two share one tile (d_pair)
+  off += (GF == kFmtBF16 && nd == 2 ? 1 : nd) * s.d_bytes;
   s.bars = off;
   off += 2048;  // barriers, the TMEM slot and the end-of-pass merge buffers
   s.total = off + 1024;  // alignment slack
@@ -508,7 +509,14 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mbGE + 4);
   float* merge = reinterpret_cast<float*>(smem + L.bars + 256);  // [3][128]
   auto stage = [&](int c) { return smem + L.stage + (c % R) * L.stage_bytes; };
-  auto d_tile = [&](int c) { return smem + L.d + (c % ND) * L.d_bytes; };
+  // A bf16 D tile is 32 columns = 64 bytes of each 128-byte row: with two slots, slot 1
+  // takes the second half of the rows of the same tile (its k-steps 2 and 3), which the
+  // consumers address as columns 32 .. 63 and the MMA by a 64-byte start offset.
+  constexpr bool kDPair = GF == kFmtBF16;
+  auto d_tile = [&](int c) {
+    return kDPair ? smem + L.d + (c % ND) * 64 : smem + L.d + (c % ND) * L.d_bytes;
+  };
+  auto d_col = [&](int c) { return kDPair ? (c % ND) * 32 : 0; };
   auto gb_tile = [&](int c) { return smem + L.gbr + (c % NG) * L.gb_bytes; };
 
   if (warp == 0) {
@@ -727,7 +735,7 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
             break;
           }
         }
-        tile_put_row16<GF>(d_tile(c), gd, row, col0, dv);
+        tile_put_row16<GF>(smem + L.d + (kDPair ? 0 : (c % ND) * L.d_bytes), gd, row, col0 + d_col(c), dv);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&mbDf[c & 1]);
