@@ -69,21 +69,45 @@ __host__ __device__ inline int tile_bytes(int F, int rows, int K) {
   const TileGeo g = tile_geo(F, rows, K);
   return fmt_parts(F) * g.bytes_part();
 }
+// A split-format operand of K columns is "packed" when its hi and lo parts fit one
+// 128-byte row together and K fills whole k-steps (rank 16 or 32 in bf16, 8 or 16 in
+// TF32): the row holds the hi k-steps, then the lo k-steps, and no padding lies between.
+// Its copy is one [rows][2K] array and its tile one part; otherwise the lo part follows
+// all hi k-blocks.
+__host__ __device__ constexpr bool lr_packed(int F, int K) {
+  return fmt_parts(F) == 2 && K % fmt_kstep(F) == 0 && 2 * K * fmt_bytes(F) <= 128;
+}
+// The S operands' tiles: the parts loaded (each kblocks x rows x 128 bytes), the lo
+// part's byte offset inside the tile and the tile's bytes.
+struct STile {
+  TileGeo g;
+  int parts, lo_off, bytes;
+};
+__host__ __device__ inline STile s_tile(int F, int rows, int K) {
+  STile t;
+  t.g = tile_geo(F, rows, K);
+  const bool packed = lr_packed(F, K);
+  t.parts = packed ? 1 : fmt_parts(F);
+  t.lo_off = packed ? K * fmt_bytes(F) : t.g.bytes_part();
+  t.bytes = t.parts * t.g.bytes_part();
+  return t;
+}
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Issues D(tmem) (+)= A(tile a, M = 128 rows) * B(tile b, N rows)^T over the k-steps of
-// the tiles, in format F: split formats take lo*hi, hi*lo, then hi*hi per k-step.
+// the tiles, in format F: split formats take lo*hi, hi*lo, then hi*hi per k-step, the lo
+// parts a_lo and b_lo bytes after the hi parts.
 template <int F>
 __device__ __forceinline__ void lr_mma(uint32_t d, const uint8_t* a, const TileGeo& ga, const uint8_t* b,
-                                       const TileGeo& gb, int n, bool accumulate) {
+                                       const TileGeo& gb, int n, bool accumulate, uint32_t a_lo, uint32_t b_lo) {
   constexpr uint32_t kind = F <= kFmtBF16x2 ? 1u : 2u;
   const uint32_t idesc = umma_idesc(kind, kLrRows, static_cast<uint32_t>(n));
   const uint32_t a0 = smem_addr(a), b0 = smem_addr(b);
-  const uint32_t a1 = a0 + (fmt_parts(F) == 2 ? ga.bytes_part() : 0);
-  const uint32_t b1 = b0 + (fmt_parts(F) == 2 ? gb.bytes_part() : 0);
+  const uint32_t a1 = a0 + (fmt_parts(F) == 2 ? a_lo : 0);
+  const uint32_t b1 = b0 + (fmt_parts(F) == 2 ? b_lo : 0);
   uint32_t acc = accumulate ? 1u : 0u;
   for (int kk = 0; kk < ga.ksteps; ++kk) {
     const uint32_t oa = (kk >> 2) * ga.rows * 128 + (kk & 3) * 32;
@@ -302,8 +326,8 @@ __host__ __device__ inline LrSmem lr_smem_plan(int P, int mode, int K, int nstag
   const int Kp = (K + 15) & ~15;
   const bool grad = mode == kLrGradA || mode == kLrGradB;
   LrSmem s;
-  s.own_bytes = tile_bytes(SF, kLrRows, K);
-  s.sw_bytes = tile_bytes(SF, kLrChunk, K);
+  s.own_bytes = s_tile(SF, kLrRows, K).bytes;
+  s.sw_bytes = s_tile(SF, kLrChunk, K).bytes;
   s.gb_bytes = grad ? fmt_parts(GF) * Kp * 128 : 0;
   s.nstage = nstage;
   s.nd = nd;
@@ -344,7 +368,7 @@ constexpr int kLrSmemHalf = 113 * 1024;  // two CTAs per SM
 // 128-byte k-blocks per operand row.
 __host__ __device__ inline LrSmem lr_smem(int P, int mode, int K) {
   if (mode != kLrFwd)
-    for (int ns = 3; ns >= 2; --ns)
+    for (int ns = 4; ns >= 2; --ns)
       for (int d = 2; d >= 1; --d) {
         const LrSmem h = lr_smem_plan(P, mode, K, ns, d, kGbSlots);
         if (h.total <= kLrSmemHalf) return h;
@@ -483,7 +507,8 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
   const int row = quarter * 32 + lane;  // own row in the tile (TMEM lane)
   const int col0 = half * 16;           // this thread's columns of a chunk
   const int own = o0 + row;
-  const TileGeo go = tile_geo(SF, kLrRows, K), gs = tile_geo(SF, kLrChunk, K);
+  const STile so = s_tile(SF, kLrRows, K), ss = s_tile(SF, kLrChunk, K);
+  const TileGeo go = so.g, gs = ss.g;
   const TileGeo gd = tile_geo(GF, kLrRows, kLrChunk), gg = tile_geo(GF, Kp, kLrChunk);
   const LrSmem L = lr_smem(P, Mode, K);
   const int R = L.nstage, ND = L.nd, NG = L.ngb;
@@ -562,7 +587,7 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
         uint64_t* bar = &mbT[c % R];
         const int w0 = c * kLrChunk;
         mbar_arrive_expect_tx(bar, L.tx_bytes);
-        for (int part = 0; part < fmt_parts(SF); ++part)
+        for (int part = 0; part < ss.parts; ++part)
           for (int kb = 0; kb < gs.kblocks; ++kb)
             tma_load_3d(st + L.sw_off + part * gs.bytes_part() + kb * kLrChunk * 128, &maps.sw[part], bar,
                         kb * (128 / esS), w0, b);
@@ -578,7 +603,7 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
         gb_issued = c;
       };
       mbar_arrive_expect_tx(mbO, L.own_bytes);
-      for (int part = 0; part < fmt_parts(SF); ++part)
+      for (int part = 0; part < so.parts; ++part)
         for (int kb = 0; kb < go.kblocks; ++kb)
           tma_load_3d(own_tile + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], mbO,
                       kb * (128 / esS), o0, b);
@@ -612,7 +637,7 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
         if (!ok) return;
         tc_fence_after();
         lr_mma<GF>(tmem + static_cast<uint32_t>(64 + (c % kGradAccs) * gstride), d_tile(c), gd, gb_tile(c), gg, Kp,
-                   c >= kGradAccs);
+                   c >= kGradAccs, gd.bytes_part(), gg.bytes_part());
         umma_commit(&mbG[c & 1]);
         umma_commit(&mbGE[c % NG]);  // the B-operand tile has been read
         g_issued = c;
@@ -625,7 +650,7 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
         if (!ok) break;
         tc_fence_after();
         lr_mma<SF>(tmem + static_cast<uint32_t>((c & 1) * kLrChunk), own_tile, go, stage(c) + L.sw_off, gs, kLrChunk,
-                   false);
+                   false, so.lo_off, ss.lo_off);
         umma_commit(&mbS[c & 1]);
         s_issued = c;
         if constexpr (kGrad) {
@@ -835,7 +860,8 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
   const int row = quarter * 32 + lane;
   const int col0 = half * 16;
   const int i = i0 + row;
-  const TileGeo go = tile_geo(SF, kLrRows, K), gs = tile_geo(SF, kLrChunk, K);
+  const STile so = s_tile(SF, kLrRows, K), ss = s_tile(SF, kLrChunk, K);
+  const TileGeo go = so.g, gs = ss.g;
   const LrSmem L = lr_smem(P, kLrStats, K);
   const int R = L.nstage;
 
@@ -878,7 +904,7 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
         uint8_t* st = stage(b);
         uint64_t* bar = &mbT[b % R];
         mbar_arrive_expect_tx(bar, L.tx_bytes);
-        for (int part = 0; part < fmt_parts(SF); ++part) {
+        for (int part = 0; part < so.parts; ++part) {  // so.parts == ss.parts
           for (int kb = 0; kb < go.kblocks; ++kb)
             tma_load_3d(st + part * go.bytes_part() + kb * kLrRows * 128, &maps.own[part], bar, kb * (128 / esS), i0,
                         b);
@@ -909,7 +935,7 @@ __global__ void __launch_bounds__(kLrThreadsFused, 2)
         if (!ok) break;
         tc_fence_after();
         lr_mma<SF>(tmem + static_cast<uint32_t>((b & 1) * kLrChunk), stage(b), go, stage(b) + L.sw_off, gs,
-                   kLrChunk, false);
+                   kLrChunk, false, so.lo_off, ss.lo_off);
         umma_commit(&mbS[b & 1]);
         s_issued = b;
       }
@@ -1004,13 +1030,26 @@ struct LrOp {
   Operand part[2];
   int parts = 0;
   pc_precision_t ety = PC_PREC_TF32;
+  long long packed_lo = 0;  // packed (lr_packed): the lo values start this many elements into a row
 };
-LrOp carve_op(Carver& c, int F, long long groups, long long rows, long long cols) {
+// pack: an S operand (K = cols), which may take the packed layout
+LrOp carve_op(Carver& c, int F, long long groups, long long rows, long long cols, bool pack = false) {
   LrOp o;
-  o.parts = fmt_parts(F);
   o.ety = fmt_bytes(F) == 2 ? PC_PREC_AUTO : PC_PREC_TF32;
+  if (pack && lr_packed(F, static_cast<int>(cols))) {  // one array of rows [hi | lo]
+    o.parts = 1;
+    o.packed_lo = cols;
+    o.part[0] = c.operand(o.ety, groups, rows, 2 * cols);
+    return o;
+  }
+  o.parts = fmt_parts(F);
   for (int p = 0; p < o.parts; ++p) o.part[p] = c.operand(o.ety, groups, rows, cols);
   return o;
+}
+void* op_lo(const LrOp& o) {
+  if (o.packed_lo)
+    return static_cast<uint8_t*>(o.part[0].ptr) + o.packed_lo * (o.ety == PC_PREC_AUTO ? 2 : 4);
+  return o.parts > 1 ? o.part[1].ptr : nullptr;
 }
 
 struct LrWs {
@@ -1030,8 +1069,8 @@ size_t carve_lr(void* base, pc_precision_t prec, int M, int N, int K, int B, boo
   w->m = static_cast<float*>(c.take(size_t(B) * 4));
   w->u = c.operand(PC_PREC_TF32, 1, B, N);
   w->theta = c.operand(PC_PREC_TF32, 1, M, N);
-  w->Aop = carve_op(c, s_fmt(P), B, M, K);
-  w->BTop = carve_op(c, s_fmt(P), B, N, K);
+  w->Aop = carve_op(c, s_fmt(P), B, M, K, true);
+  w->BTop = carve_op(c, s_fmt(P), B, N, K, true);
   if (bwd) {
     w->thetaT = c.operand(PC_PREC_TF32, 1, N, M);
     w->rf_lz = c.operand(PC_PREC_TF32, 1, B, M);
@@ -1068,7 +1107,7 @@ pc_status_t to_op(const float* src, long long sg, long long sr, long long sc, in
   if (sr == 1 && sc != 1 && G <= 65535) {  // a transpose: tiled through shared memory
     const dim3 grid(cdiv(R, 32), cdiv(C, 32), G);
     k_lr_to_op_t<F><<<grid, dim3(32, 8), 0, s>>>(src, sg, sc, G, R, C, o.part[0].ptr,
-                                                 o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
+                                                 op_lo(o), o.part[0].ld);
     PC_LAUNCH_CHECK();
     return PC_OK;
   }
@@ -1076,13 +1115,13 @@ pc_status_t to_op(const float* src, long long sg, long long sr, long long sc, in
   if (sc == 1 && C % 4 == 0 && sr % 4 == 0 && sg % 4 == 0 && aligned16(src) && o.part[0].ld % 4 == 0) {
     const int blocks = static_cast<int>(std::min<long long>(cdiv(rows * (C / 4), 256), 65535));
     k_lr_to_op4<F><<<blocks, 256, 0, s>>>(src, sg, sr, R, C / 4, rows, o.part[0].ptr,
-                                          o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
+                                          op_lo(o), o.part[0].ld);
     PC_LAUNCH_CHECK();
     return PC_OK;
   }
   const int blocks = static_cast<int>(std::min<long long>(cdiv(rows, 8), 8192));
   k_lr_to_op<F><<<blocks, dim3(32, 8), 0, s>>>(src, sg, sr, sc, G, R, C, o.part[0].ptr,
-                                               o.parts > 1 ? o.part[1].ptr : nullptr, o.part[0].ld);
+                                               op_lo(o), o.part[0].ld);
   PC_LAUNCH_CHECK();
   return PC_OK;
 }

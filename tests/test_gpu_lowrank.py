@@ -71,7 +71,8 @@ def test_ragged_tiles(mode):
 # Ranks 1 .. 64 at a 1-nat spread. (At 4 nats and rank 64 the entries of S reach ~20 nats,
 # and the accumulator's truncation over 8 TF32 k-steps moves exp(S) by ~1e-5 relative in
 # fp32 mode: the spread-4 case is covered at the workload's rank 16 below.)
-@pytest.mark.parametrize("K", [1, 16, 17, 40, 64])
+# (16 and 32 in bf16, 8 and 16 in TF32 take the operand layout with hi and lo in one row)
+@pytest.mark.parametrize("K", [1, 8, 16, 17, 32, 40, 64])
 def test_ranks(K):
     d = lowrank_inputs(130, 100, K, 2, 1.0, seed=301 + K, f_kind="uniform")
     r = _oracle(d)
