@@ -226,7 +226,11 @@ __global__ void __launch_bounds__(256) k_hclt_product(
 // reduction, and a lane's loads of one child row are independent, so they are all in
 // flight together. Warp w of the launch takes node s0 + w / B, sample w % B.
 constexpr int kWarpRuns = 8;  // runs of four latents per lane: H <= 4 * 32 * 8
-template <int P, bool kVec>
+// kLeaf: nodes without children below the root (height 0), where n' = E_v[., x_v] itself:
+// its maximum is taken on the values and u = n' * (1 / max n'), the same bits as the
+// exponent-tracked path gives while u is a normal float (a power-of-two scale of a
+// product rounds the same way), with a third of its work per latent.
+template <int P, bool kVec, bool kLeaf = false>
 __global__ void __launch_bounds__(256) k_hclt_product_warp(
     int s0, int G, int root_slot, int nvars, int H, int B, const int* __restrict__ data,
     const int* __restrict__ var_of_slot, const int* __restrict__ child_ptr, const int* __restrict__ child_slots,
@@ -244,6 +248,51 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
   const bool xin = x >= 0 && x < C;
   const int c0 = child_ptr[s], c1 = child_ptr[s + 1];
   const float* er = Et + (static_cast<long long>(v) * C + (xin ? x : 0)) * H;
+  const long long row = static_cast<long long>(s) * B + b;
+  if constexpr (kLeaf) {
+    float ev[kWarpRuns][4];
+    float mx = 0.f;
+#pragma unroll
+    for (int r = 0; r < kWarpRuns; ++r) {
+      const int q = lane + 32 * r;
+      const float4 x4 = (xin && 4 * q < H) ? load_run4<kVec>(er, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ev[r][0] = x4.x;
+      ev[r][1] = x4.y;
+      ev[r][2] = x4.z;
+      ev[r][3] = x4.w;
+      mx = fmaxf(mx, fmaxf(fmaxf(x4.x, x4.y), fmaxf(x4.z, x4.w)));
+    }
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const bool live = mx > 0.f;
+    int emax = 0;
+    const float mmax = live ? renorm(mx, emax) : 1.f;
+    const float rinv = live ? 1.f / mx : 0.f;
+    float* u32 = U32 ? U32 + row * H - u32_off : nullptr;
+#pragma unroll
+    for (int r = 0; r < kWarpRuns; ++r) {
+      const int q = lane + 32 * r;
+      const int z = 4 * q;
+      if (z >= H) continue;
+      float uu[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) uu[k] = ev[r][k] > 0.f ? ev[r][k] * rinv : 0.f;
+      const float4 u = make_float4(uu[0], uu[1], uu[2], uu[3]);
+      if constexpr (kVec) {
+        if (u32) reinterpret_cast<float4*>(u32)[q] = u;
+        store_child4<P>(uop, static_cast<size_t>(row * uop_ld + z), uop_lo, u);
+      } else {
+        for (int k = 0; k < 4 && z + k < H; ++k) {
+          if (u32) u32[z + k] = uu[k];
+          store_child<P>(uop, static_cast<size_t>(row * uop_ld + z + k), uop_lo, uu[k]);
+        }
+      }
+    }
+    if (lane == 0) {
+      Ex[row] = live ? emax : 0;
+      Lm[row] = live ? logf(mmax) : -INFINITY;
+    }
+    return;
+  }
   float m[kWarpRuns][4];
   int e[kWarpRuns][4];
 #pragma unroll
@@ -288,7 +337,6 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
   const int emax = live ? static_cast<int>((best - static_cast<long long>(mbits)) / 4294967296LL) : 0;
   const float mmax = live ? __uint_as_float(mbits) : 1.f;
   const float rinv = 1.f / mmax;
-  const long long row = static_cast<long long>(s) * B + b;
   float* u32 = U32 ? U32 + row * H - u32_off : nullptr;  // NULL: the bf16 operand parts carry u
   float dot = 0.f;
 #pragma unroll
@@ -982,7 +1030,10 @@ pc_status_t hclt_run(int n, int H, int C, int B, const int32_t* parent, const in
                         (edges ? G * BH * eb2 : H * 4ll + B * 4ll));
     if (H <= 4 * 32 * kWarpRuns) {
       const unsigned blocks = static_cast<unsigned>(cdiv(static_cast<long long>(G) * B, 8));
-      (prod_vec ? k_hclt_product_warp<P, true> : k_hclt_product_warp<P, false>)<<<blocks, 256, 0, s>>>(
+      // height 0 below the root: nodes without children (the leaf kernel)
+      const bool leaf = L == 0 && edges;
+      (leaf ? (prod_vec ? k_hclt_product_warp<P, true, true> : k_hclt_product_warp<P, false, true>)
+            : (prod_vec ? k_hclt_product_warp<P, true> : k_hclt_product_warp<P, false>))<<<blocks, 256, 0, s>>>(
           sA, G, root, n, H, B, data, d_var, d_cptr, d_cslots, w.Et, w.D, C, u32_out, w.u32_off, edges ? w.Uop.ptr : nullptr,
           w.Uop.ld, w.Uop.lo_elems, w.Ex, w.Lm, pi, w.rdot);
     } else {
