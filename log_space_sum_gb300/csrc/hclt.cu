@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
   }
   float m[kWarpRuns][4];
   int e[kWarpRuns][4];
+  float4 d[kWarpRuns];
 #pragma unroll
   for (int r = 0; r < kWarpRuns; ++r) {
     const int q = lane + 32 * r;
@@ -303,20 +304,27 @@ __global__ void __launch_bounds__(256) k_hclt_product_warp(
     m[r][1] = ev.y;
     m[r][2] = ev.z;
     m[r][3] = ev.w;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      e[r][k] = 0;
-      m[r][k] = renorm(m[r][k], e[r][k]);
-    }
   }
-  for (int c = c0; c < c1; ++c) {
+  auto load_child = [&](int c) {
     const float* drow = D + (static_cast<long long>(child_slots[c]) * B + b) * H;
-    float4 d[kWarpRuns];
 #pragma unroll
     for (int r = 0; r < kWarpRuns; ++r) {
       const int q = lane + 32 * r;
       d[r] = 4 * q < H ? load_run4<kVec>(drow, q, H) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  };
+  // the first child's row goes out together with the emission row: one memory round
+  // trip fewer per (node, sample)
+  if (c0 < c1) load_child(c0);
+#pragma unroll
+  for (int r = 0; r < kWarpRuns; ++r)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      e[r][k] = 0;
+      m[r][k] = renorm(m[r][k], e[r][k]);
+    }
+  for (int c = c0; c < c1; ++c) {
+    if (c > c0) load_child(c);
 #pragma unroll
     for (int r = 0; r < kWarpRuns; ++r) {
       m[r][0] = renorm(m[r][0] * d[r].x, e[r][0]);
